@@ -1,0 +1,178 @@
+"""Float64 CPU oracle for sparse MLA attention over the 656-byte FP8 cache.
+
+TEST INFRASTRUCTURE ONLY: the test-suite, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` are the only callers.  The product path
+(``sparse_mla_attention_fp8_gb300``) never imports this package, and this
+package never imports the product.  They share no code; they meet only
+through the seeded input generators in ``smla_inputs``.
+
+The arithmetic lives in ``smla_oracle.c`` (plain C, double precision, OpenMP
+over tokens); this module builds it with gcc and marshals numpy arrays.
+Every function cites the passage of the pages it follows in the C source:
+vLLM ``flashmla_sparse.py`` (module docstring on the "FP8 with scale" layout,
+``triton_convert_req_index_to_global_index`` and its docstring formula,
+``FlashMLASparseImpl.forward``) and the OCP 8-bit floating point
+specification for E4M3.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "smla_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "libsmla_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+ROW_BYTES = 656
+D_QK = 576
+D_V = 512
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle shared library in place (gcc, -O2, OpenMP)."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-ffp-contract=off", "-fno-fast-math",
+           "-fPIC", "-shared", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB_PATH)
+            P = ctypes.c_void_p
+            i32, i64, f64 = ctypes.c_int, ctypes.c_int64, ctypes.c_double
+            lib.oracle_e4m3_to_double.argtypes = [ctypes.c_uint8]
+            lib.oracle_e4m3_to_double.restype = f64
+            lib.oracle_e4m3_from_float.argtypes = [ctypes.c_float]
+            lib.oracle_e4m3_from_float.restype = ctypes.c_uint8
+            lib.oracle_dequant_row.argtypes = [P, P]
+            lib.oracle_dequant_row.restype = None
+            lib.oracle_translate.argtypes = [P, P, P, i32, i32, i32, i32, i64, P]
+            lib.oracle_translate.restype = None
+            lib.oracle_quantize_store.argtypes = [P, P, P, i32, i64]
+            lib.oracle_quantize_store.restype = None
+            lib.oracle_sparse_mla_decode.argtypes = [P, P, P, P, P, f64, i32, i32, i32, i32, i32, i64, P, i32,
+                                                     P, P, i32, P, P]
+            lib.oracle_sparse_mla_decode.restype = None
+            lib.oracle_sparse_mla_prefill.argtypes = [P, P, P, f64, i32, i32, i64, i32, P, i32, P, P, i32, P, P]
+            lib.oracle_sparse_mla_prefill.restype = None
+            _lib = lib
+    return _lib
+
+
+def _p(a: np.ndarray | None):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def default_threads() -> int:
+    return max(1, os.cpu_count() or 1)
+
+
+# ---------------------------------------------------------------- formats
+
+def e4m3_to_double(code: int) -> float:
+    return _load().oracle_e4m3_to_double(int(code) & 0xFF)
+
+
+def e4m3_from_float(y: float) -> int:
+    return int(_load().oracle_e4m3_from_float(float(y)))
+
+
+def dequant_row(row: np.ndarray) -> np.ndarray:
+    """One 656-byte cache row -> float64[576] (NoPE dequantized, RoPE exact)."""
+    row = _c(row, np.uint8).reshape(-1)
+    assert row.size == ROW_BYTES
+    out = np.empty(D_QK, np.float64)
+    _load().oracle_dequant_row(_p(row), _p(out))
+    return out
+
+
+# ---------------------------------------------------------------- steps
+
+def translate(indices, block_table, req_id_per_token, num_blocks: int) -> np.ndarray:
+    """Logical top-k index -> physical cache slot (int32, -1 = invalid)."""
+    idx = _c(indices, np.int32)
+    bt = _c(block_table, np.int32)
+    req = _c(req_id_per_token, np.int32)
+    T, K = idx.shape
+    R, MB = bt.shape
+    out = np.empty((T, K), np.int32)
+    _load().oracle_translate(_p(idx), _p(bt), _p(req), T, K, R, MB, int(num_blocks), _p(out))
+    return out
+
+
+def quantize_store(kv_new_bits, slot_mapping, cache: np.ndarray) -> None:
+    """Quantize bf16 rows (uint16 bits [T, 576]) into ``cache`` (uint8
+    [NB, 64, 656], modified in place) at ``slot_mapping`` (int64 [T])."""
+    kv = _c(kv_new_bits, np.uint16)
+    sm = _c(slot_mapping, np.int64)
+    assert cache.dtype == np.uint8 and cache.flags.c_contiguous and cache.shape[-1] == ROW_BYTES
+    NB = cache.shape[0]
+    T = kv.shape[0]
+    assert kv.shape == (T, D_QK) and sm.shape == (T,)
+    _load().oracle_quantize_store(_p(kv), _p(sm), _p(cache), T, NB)
+
+
+def sparse_mla_decode(q_bits, cache, indices, block_table, req_id_per_token, sm_scale: float,
+                      tokens=None, nthreads: int | None = None):
+    """FP8 sparse decode; returns (out float64 [n, H, 512], lse float64 [n, H])
+    for the listed tokens (all tokens when ``tokens`` is None)."""
+    q = _c(q_bits, np.uint16)
+    T, H, D = q.shape
+    assert D == D_QK
+    assert cache.dtype == np.uint8 and cache.flags.c_contiguous
+    NB = cache.shape[0]
+    idx = _c(indices, np.int32)
+    K = idx.shape[1]
+    bt = _c(block_table, np.int32)
+    R, MB = bt.shape
+    req = _c(req_id_per_token, np.int32)
+    tok = None if tokens is None else _c(tokens, np.int32)
+    n = T if tok is None else tok.size
+    nth = nthreads or default_threads()
+    ws_rows = np.empty((nth, max(K, 1), D_QK), np.float64)
+    ws_s = np.empty((nth, max(K, 1)), np.float64)
+    out = np.empty((n, H, D_V), np.float64)
+    lse = np.empty((n, H), np.float64)
+    _load().oracle_sparse_mla_decode(_p(q), _p(cache), _p(idx), _p(bt), _p(req), float(sm_scale), T, H, K, R, MB,
+                                     NB, _p(tok), n, _p(ws_rows), _p(ws_s), nth, _p(out), _p(lse))
+    return out, lse
+
+
+def sparse_mla_prefill(q_bits, kv_bits, indices, sm_scale: float, tokens=None, nthreads: int | None = None):
+    """BF16 sparse prefill over a dense latent buffer (uint16 bits [N, 576])."""
+    q = _c(q_bits, np.uint16)
+    T, H, D = q.shape
+    assert D == D_QK
+    kv = _c(kv_bits, np.uint16)
+    N = kv.shape[0]
+    idx = _c(indices, np.int32)
+    K = idx.shape[1]
+    tok = None if tokens is None else _c(tokens, np.int32)
+    n = T if tok is None else tok.size
+    nth = nthreads or default_threads()
+    ws_rows = np.empty((nth, max(K, 1), D_QK), np.float64)
+    ws_s = np.empty((nth, max(K, 1)), np.float64)
+    out = np.empty((n, H, D_V), np.float64)
+    lse = np.empty((n, H), np.float64)
+    _load().oracle_sparse_mla_prefill(_p(q), _p(kv), _p(idx), float(sm_scale), T, H, N, K, _p(tok), n,
+                                      _p(ws_rows), _p(ws_s), nth, _p(out), _p(lse))
+    return out, lse

@@ -1,0 +1,275 @@
+/*
+ * smla_oracle.c -- plain, slow, float64 CPU reference for sparse MLA attention
+ * over the 656-byte "FP8 with scale" paged cache.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or call
+ * this file: only the test-suite, the smoke check and the benchmark's CPU
+ * baseline leg use it.  It shares no code, header, table or constant with the
+ * CUDA library; the two meet only through the seeded synthetic inputs.
+ *
+ * Sources (the pages this follows):
+ *  [P2] vLLM, "vllm/v1/attention/backends/mla/flashmla_sparse.py":
+ *       - module docstring, "FP8 with scale" format (656 bytes per token:
+ *         512 float8_e4m3 NoPE values, 4 float32 scales one per 128 values,
+ *         64 bfloat16 RoPE values, not quantized);
+ *       - triton_convert_req_index_to_global_index, its docstring formula
+ *         out = block_table[req, idx // BLOCK_SIZE] * BLOCK_SIZE + idx % BLOCK_SIZE,
+ *         -1 for idx == -1 or an out-of-range block id;
+ *       - FlashMLASparseImpl.forward: MQA 576/512 (head_dim_v = 512),
+ *         softmax_scale, the write of k_c_normed (512) and k_pe (64) into the
+ *         cache through slot_mapping (concat_and_cache_mla).
+ *  [OCP] OCP 8-bit floating point specification, E4M3: 1 sign, 4 exponent
+ *        (bias 7), 3 mantissa bits; subnormals; no infinities; S.1111.111 NaN.
+ *
+ * Readings where the pages are silent (each one is also listed in the design doc):
+ *  R1 translate also rejects a physical block id outside [0, NB) and a request
+ *     id outside [0, R) (the page would emit a slot from garbage);
+ *  R2 the quantizer scale is amax/448 in float32, codes are the float32
+ *     quotient x/scale rounded to nearest-even e4m3, saturating to +-448; a
+ *     group whose scale is 0 stores code 0 everywhere and scale 0.0f;
+ *  R3 V is the NoPE part, columns 0..511 of the 576-wide latent row;
+ *  R4 LSE is the natural log of the sum of exp of the scaled logits; a token
+ *     with no valid index has output 0 and LSE -infinity;
+ *  R5 slot_mapping < 0 (or >= NB*64) skips the token.
+ *
+ * Every floating-point step of attention is in double.  The quantizer decides
+ * integer codes, so it runs in float32, the precision the CUDA kernel uses.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ROW_BYTES 656
+#define D_QK 576
+#define D_V 512
+#define D_NOPE 512
+#define GROUP 128
+#define BLOCK 64
+
+/* ---------------------------------------------------------------- formats */
+
+/* [OCP] E4M3 decode: value = (-1)^s * 2^(e-7) * (1 + m/8) for e > 0,
+ * (-1)^s * 2^-6 * (m/8) for e == 0; e == 15 && m == 7 is NaN. */
+double oracle_e4m3_to_double(uint8_t code) {
+  int s = (code >> 7) & 1;
+  int e = (code >> 3) & 15;
+  int m = code & 7;
+  double v;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0)
+    v = ldexp((double)m / 8.0, -6);
+  else
+    v = ldexp(1.0 + (double)m / 8.0, e - 7);
+  return s ? -v : v;
+}
+
+/* [OCP] encode a float to E4M3 with round-to-nearest, ties to even, and
+ * saturation to the largest finite magnitude (448).  Written from the format:
+ * find the exponent bucket, scale the magnitude to an integer grid of 8 steps
+ * per binade (or per 2^-9 in the subnormal range) and round on that grid. */
+uint8_t oracle_e4m3_from_float(float y) {
+  if (isnan(y)) return 0x7F;
+  uint8_t sign = signbit(y) ? 0x80 : 0x00;
+  double a = fabs((double)y);
+  if (a >= 448.0) return sign | 0x7E;
+  if (a < ldexp(1.0, -6)) {
+    /* subnormal grid: multiples of 2^-9, mantissa 0..8 (8 == smallest normal) */
+    double q = nearbyint(a * 512.0); /* default rounding mode: ties to even */
+    int m = (int)q;
+    if (m >= 8) return sign | 0x08;
+    return sign | (uint8_t)m;
+  }
+  int ex;
+  double fr = frexp(a, &ex); /* a = fr * 2^ex, fr in [0.5, 1) */
+  int e = ex - 1;            /* a = (2*fr) * 2^e, 2*fr in [1, 2) */
+  double q = nearbyint(fr * 2.0 * 8.0); /* 8..16 */
+  int m8 = (int)q;
+  if (m8 == 16) {
+    m8 = 8;
+    e += 1;
+  }
+  int biased = e + 7;
+  if (biased > 15 || (biased == 15 && m8 - 8 == 7)) return sign | 0x7E; /* saturate */
+  return sign | (uint8_t)((biased << 3) | (m8 - 8));
+}
+
+double oracle_bf16_to_double(uint16_t bits) {
+  uint32_t u = (uint32_t)bits << 16;
+  float f;
+  memcpy(&f, &u, 4);
+  return (double)f;
+}
+
+static float bf16_to_float(uint16_t bits) {
+  uint32_t u = (uint32_t)bits << 16;
+  float f;
+  memcpy(&f, &u, 4);
+  return f;
+}
+
+/* [P2 docstring] Dequantize one 656-byte row as stored:
+ * K[c] = e4m3(byte c) * scale[c / 128] for c < 512 (scales are little-endian
+ * float32 at bytes 512 + 4g); K[512 + r] = bf16 at bytes 528 + 2r. */
+void oracle_dequant_row(const uint8_t* row, double* out) {
+  for (int c = 0; c < D_NOPE; ++c) {
+    float sc;
+    memcpy(&sc, row + D_NOPE + 4 * (c / GROUP), 4);
+    out[c] = oracle_e4m3_to_double(row[c]) * (double)sc;
+  }
+  for (int r = 0; r < D_QK - D_NOPE; ++r) {
+    uint16_t b;
+    memcpy(&b, row + D_NOPE + 16 + 2 * r, 2);
+    out[D_NOPE + r] = oracle_bf16_to_double(b);
+  }
+}
+
+/* ---------------------------------------------------------------- translate */
+
+/* [P2 triton_convert_req_index_to_global_index] plus reading R1. */
+int32_t oracle_translate_one(int32_t idx, int32_t req, const int32_t* block_table, int R, int MB, int64_t NB) {
+  if (idx < 0) return -1;
+  if (req < 0 || req >= R) return -1;
+  int32_t b = idx / BLOCK;
+  int32_t o = idx % BLOCK;
+  if (b >= MB) return -1;
+  int32_t p = block_table[(int64_t)req * MB + b];
+  if (p < 0 || (int64_t)p >= NB) return -1;
+  return p * BLOCK + o;
+}
+
+void oracle_translate(const int32_t* indices, const int32_t* block_table, const int32_t* req_id, int T, int K, int R,
+                      int MB, int64_t NB, int32_t* slots) {
+  for (int t = 0; t < T; ++t)
+    for (int k = 0; k < K; ++k)
+      slots[(int64_t)t * K + k] =
+          oracle_translate_one(indices[(int64_t)t * K + k], req_id[t], block_table, R, MB, NB);
+}
+
+/* ---------------------------------------------------------------- quantize */
+
+/* [P2 forward / concat_and_cache_mla] + reading R2: write each new token's
+ * latent (512 NoPE, quantized per 128-group) and RoPE (64 bf16, copied) into
+ * its cache row at slot_mapping[t]. */
+void oracle_quantize_store(const uint16_t* kv_new, const int64_t* slot_mapping, uint8_t* cache, int T, int64_t NB) {
+  for (int t = 0; t < T; ++t) {
+    int64_t slot = slot_mapping[t];
+    if (slot < 0 || slot >= NB * BLOCK) continue;
+    const uint16_t* x = kv_new + (int64_t)t * D_QK;
+    uint8_t* row = cache + slot * ROW_BYTES;
+    for (int g = 0; g < D_NOPE / GROUP; ++g) {
+      float amax = 0.0f;
+      for (int c = g * GROUP; c < (g + 1) * GROUP; ++c) {
+        float v = fabsf(bf16_to_float(x[c]));
+        if (v > amax) amax = v;
+      }
+      float scale = amax / 448.0f;
+      for (int c = g * GROUP; c < (g + 1) * GROUP; ++c) {
+        if (scale == 0.0f) {
+          row[c] = 0;
+        } else {
+          float y = bf16_to_float(x[c]) / scale;
+          row[c] = oracle_e4m3_from_float(y);
+        }
+      }
+      memcpy(row + D_NOPE + 4 * g, &scale, 4);
+    }
+    memcpy(row + D_NOPE + 16, x + D_NOPE, 2 * (D_QK - D_NOPE));
+  }
+}
+
+/* ---------------------------------------------------------------- attention */
+
+/* Attention of one query head over n dequantized rows (n x 576), [P2]
+ * MQA 576/512 with softmax_scale, and readings R3, R4. */
+static void attend_head(const double* qh, const double* rows, int n, double sm_scale, double* s_buf, double* out,
+                        double* lse) {
+  if (n == 0) {
+    for (int c = 0; c < D_V; ++c) out[c] = 0.0;
+    *lse = -INFINITY;
+    return;
+  }
+  double m = -INFINITY;
+  for (int j = 0; j < n; ++j) {
+    double acc = 0.0;
+    for (int c = 0; c < D_QK; ++c) acc += qh[c] * rows[(int64_t)j * D_QK + c];
+    s_buf[j] = sm_scale * acc;
+    if (s_buf[j] > m) m = s_buf[j];
+  }
+  double l = 0.0;
+  for (int c = 0; c < D_V; ++c) out[c] = 0.0;
+  for (int j = 0; j < n; ++j) {
+    double w = exp(s_buf[j] - m);
+    l += w;
+    for (int c = 0; c < D_V; ++c) out[c] += w * rows[(int64_t)j * D_QK + c];
+  }
+  for (int c = 0; c < D_V; ++c) out[c] /= l;
+  *lse = m + log(l);
+}
+
+/* FP8 sparse decode.  For each requested token (tokens[i], or i when tokens is
+ * NULL): translate its K logical indices, dequantize every valid row as
+ * stored, and attend with each of its H heads.
+ * q: bf16 bits [T, H, 576]; cache: [NB, 64, 656] bytes; out: [n, H, 512];
+ * lse: [n, H].  Workspace is allocated by the caller: rows [K * 576] and
+ * s [K] doubles per thread (nthreads copies). */
+void oracle_sparse_mla_decode(const uint16_t* q, const uint8_t* cache, const int32_t* indices,
+                              const int32_t* block_table, const int32_t* req_id, double sm_scale, int T, int H, int K,
+                              int R, int MB, int64_t NB, const int32_t* tokens, int n_tokens, double* ws_rows,
+                              double* ws_s, int nthreads, double* out, double* lse) {
+  (void)T;
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
+  for (int i = 0; i < n_tokens; ++i) {
+    int tid = 0;
+#ifdef _OPENMP
+    tid = omp_get_thread_num();
+#endif
+    double* rows = ws_rows + (int64_t)tid * K * D_QK;
+    double* s_buf = ws_s + (int64_t)tid * K;
+    double qh[D_QK];
+    int t = tokens ? tokens[i] : i;
+    int n = 0;
+    for (int k = 0; k < K; ++k) {
+      int32_t slot = oracle_translate_one(indices[(int64_t)t * K + k], req_id[t], block_table, R, MB, NB);
+      if (slot < 0) continue;
+      oracle_dequant_row(cache + (int64_t)slot * ROW_BYTES, rows + (int64_t)n * D_QK);
+      ++n;
+    }
+    for (int h = 0; h < H; ++h) {
+      for (int c = 0; c < D_QK; ++c) qh[c] = oracle_bf16_to_double(q[((int64_t)t * H + h) * D_QK + c]);
+      attend_head(qh, rows, n, sm_scale, s_buf, out + ((int64_t)i * H + h) * D_V, lse + (int64_t)i * H + h);
+    }
+  }
+}
+
+/* BF16 sparse prefill over a dense latent buffer kv [N, 576]: index i is a row
+ * of kv; i < 0 or i >= N is invalid (the prefill analogue of R1). */
+void oracle_sparse_mla_prefill(const uint16_t* q, const uint16_t* kv, const int32_t* indices, double sm_scale, int T,
+                               int H, int64_t N, int K, const int32_t* tokens, int n_tokens, double* ws_rows,
+                               double* ws_s, int nthreads, double* out, double* lse) {
+  (void)T;
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
+  for (int i = 0; i < n_tokens; ++i) {
+    int tid = 0;
+#ifdef _OPENMP
+    tid = omp_get_thread_num();
+#endif
+    double* rows = ws_rows + (int64_t)tid * K * D_QK;
+    double* s_buf = ws_s + (int64_t)tid * K;
+    double qh[D_QK];
+    int t = tokens ? tokens[i] : i;
+    int n = 0;
+    for (int k = 0; k < K; ++k) {
+      int32_t idx = indices[(int64_t)t * K + k];
+      if (idx < 0 || (int64_t)idx >= N) continue;
+      for (int c = 0; c < D_QK; ++c) rows[(int64_t)n * D_QK + c] = oracle_bf16_to_double(kv[(int64_t)idx * D_QK + c]);
+      ++n;
+    }
+    for (int h = 0; h < H; ++h) {
+      for (int c = 0; c < D_QK; ++c) qh[c] = oracle_bf16_to_double(q[((int64_t)t * H + h) * D_QK + c]);
+      attend_head(qh, rows, n, sm_scale, s_buf, out + ((int64_t)i * H + h) * D_V, lse + (int64_t)i * H + h);
+    }
+  }
+}
