@@ -1,0 +1,470 @@
+#!/usr/bin/env python
+"""Benchmark: sparse MLA decode throughput over the 656-byte FP8 cache.
+
+Default workload (one step = the whole decode hot path over one batch):
+  64 requests x 1 query token, H = 16 heads, top-k = 2048, per-request
+  context uniform in [8192, 32768], block size 64, shuffled block table,
+  latent N(0,1) with 1% of the channels x8, quantized into the FP8 cache.
+  A step is: quantize-and-store of the 64 new tokens' rows, then the sparse
+  decode (index translation, row gather + dequantization, QK^T, online
+  softmax, P.V, split combine).  Eight independent top-k index sets rotate
+  from step to step, so each step gathers ~86 MB of rows that were not just
+  read (8 x 86 MB >> 129 MB of L2).
+
+Prints one JSON line (rank 0).  --impl reference times the float64 CPU
+oracle on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import smla_inputs as inp  # noqa: E402
+
+METRIC = "sparse MLA decode query-tokens/s + HBM GB/s (H=16, topk=2048) vs roofline"
+UNIT = "query-tokens/s"
+
+
+# ---------------------------------------------------------------- helpers
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="smla_clocks_", suffix=".csv")
+            os.close(fd)
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
+            if self.gpu_id:
+                cmd += ["-i", self.gpu_id]
+            self.proc = subprocess.Popen(cmd, stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 8:
+                    continue
+                try:
+                    rows.append((float(parts[0]), float(parts[1]), float(parts[2]), parts[4:8]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[3]) if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "power_w_max": max(r[2] for r in rows), "reasons": reasons, "samples": len(rows)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier(world, device=None):
+    if world > 1:
+        import torch.distributed as dist
+        if device is not None and device.type == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def decode_algorithmic_bytes(case: inp.RotatingDecode, index_set: np.ndarray) -> int:
+    """Bytes one decode launch must move at minimum: every valid gathered row
+    once per query token (656 B), q, out, lse, the index row, the request id
+    and the used part of the request's block-table row."""
+    T, H = case.q.shape[0], case.H
+    rows = int((index_set >= 0).sum())
+    used_blocks = int(((case.ctx_lens + 63) // 64).sum())  # block-table entries read (one request per token)
+    return (rows * 656 + T * H * 576 * 2 + T * H * 512 * 2 + T * H * 4 + index_set.size * 4 + T * 4
+            + used_blocks * 4)
+
+
+def decode_flops(case, index_set) -> int:
+    return 2 * case.H * int((index_set >= 0).sum()) * (576 + 512)
+
+
+# ---------------------------------------------------------------- CPU oracle sample
+
+def host_sample_cache(case: inp.RotatingDecode, index_set: np.ndarray, tokens: np.ndarray, seed: int):
+    """Host cache holding every row the sampled tokens reference, quantized by
+    the oracle from host-drawn latent rows of the same distribution."""
+    import oracle
+    slots = oracle.translate(index_set[tokens], case.block_table, case.req_id_per_token[tokens], case.num_blocks)
+    need = np.unique(slots[slots >= 0]).astype(np.int64)
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal((len(need), 576), dtype=np.float32)
+    if len(case.outlier_channels):
+        x[:, case.outlier_channels] *= 8.0
+    cache = np.zeros((case.num_blocks, 64, 656), np.uint8)
+    oracle.quantize_store(inp.bf16_bits(x), need, cache)
+    return cache
+
+
+def time_oracle(case, index_set, tokens, cache, nthreads):
+    import oracle
+    t0 = time.perf_counter()
+    oracle.sparse_mla_decode(case.q, cache, index_set, case.block_table, case.req_id_per_token, case.sm_scale,
+                             tokens=tokens, nthreads=nthreads)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(case, budget_s: float = 12.0):
+    """Oracle throughput on the host cores: whole passes over the 64 tokens of
+    index set 0 until about budget_s of CPU work (at least one pass)."""
+    import oracle
+    nth = oracle.default_threads()
+    tokens = np.arange(case.q.shape[0], dtype=np.int32)
+    cache = host_sample_cache(case, case.index_sets[0], tokens, seed=12345)
+    n_tok, elapsed, passes = 0, 0.0, 0
+    while passes == 0 or elapsed < budget_s:
+        elapsed += time_oracle(case, case.index_sets[0], tokens, cache, nth)
+        n_tok += len(tokens)
+        passes += 1
+    return {"value": n_tok / elapsed, "unit": UNIT, "cores": nth, "kind": "oracle",
+            "sample": f"{passes} pass(es) over all {len(tokens)} query tokens of one index set "
+                      f"(float64 C oracle, OpenMP over tokens, {nth} threads), {elapsed:.1f} s"}
+
+
+# ---------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    rank, world, local = dist_setup()
+    if rank != 0:
+        barrier(world)
+        return
+    import oracle
+    oracle.build()
+    case = inp.rotating_decode(seed=1)
+    nth = oracle.default_threads()
+    S = max(1, min(case.q.shape[0], nth))  # tokens per step: one per host thread
+    rng = np.random.default_rng(99)
+    toks = [np.sort(rng.choice(case.q.shape[0], S, replace=False)).astype(np.int32)
+            for _ in range(args.warmup + args.steps)]
+    all_tok = np.unique(np.concatenate(toks)).astype(np.int32)
+    cache = host_sample_cache(case, case.index_sets[0], all_tok, seed=12345)
+    for i in range(args.warmup):
+        time_oracle(case, case.index_sets[0], toks[i], cache, nth)
+    t = 0.0
+    for i in range(args.steps):
+        t += time_oracle(case, case.index_sets[0], toks[args.warmup + i], cache, nth)
+    value = args.steps * S / t
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{case.name}: memory-bound FP8 sparse decode, 64 requests x 1 token, H=16, "
+                                   f"top-k 2048, context U[8192,32768], 656-byte FP8 cache",
+                       "step": f"float64 CPU oracle on {S} of the 64 query tokens (one per host thread)"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": nth, "kind": "oracle",
+                             "sample": f"{S} query tokens per step, {args.steps} steps"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    barrier(world)
+
+
+# ---------------------------------------------------------------- our arm
+
+def run_ours(args):
+    import torch
+    import sparse_mla_attention_fp8_gb300 as smla
+
+    rank, world, local = dist_setup()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU for the library path (use --impl reference for the oracle)")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    smla.build()
+    peaks = load_peaks()
+
+    case = inp.rotating_decode(seed=1 + rank)
+    T, H, K = case.q.shape[0], case.H, case.K
+    NB = case.num_blocks
+    stream = torch.cuda.Stream(device)
+
+    def bf16(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device).view(torch.bfloat16)
+
+    with torch.cuda.stream(stream):
+        cache = torch.zeros((NB, 64, 656), dtype=torch.uint8, device=device)
+        lat = inp.device_latent(len(case.ctx_slots), case.latent_seed, case.outlier_channels, device)
+        smla.mla_cache_store_fp8(lat, torch.from_numpy(case.ctx_slots).to(device), cache, stream=stream)
+        new_rows = inp.device_latent(T, case.latent_seed + 1, case.outlier_channels, device)
+        new_slots = torch.from_numpy(case.new_slots).to(device)
+        q = bf16(case.q)
+        idx_sets = [torch.from_numpy(s).to(device) for s in case.index_sets]
+        bt = torch.from_numpy(case.block_table).to(device)
+        req = torch.from_numpy(case.req_id_per_token).to(device)
+        ws = torch.zeros(smla.decode_workspace_bytes(T, H, K, 0), dtype=torch.uint8, device=device)
+        out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=device)
+        lse = torch.empty((T, H), dtype=torch.float32, device=device)
+    stream.synchronize()
+    del lat
+
+    def store():
+        smla.mla_cache_store_fp8(new_rows, new_slots, cache, stream=stream)
+
+    def decode(i):
+        smla.sparse_mla_decode_fp8(q, cache, idx_sets[i % len(idx_sets)], bt, req, case.sm_scale, 0, out, lse, ws,
+                                   stream=stream)
+
+    # eager warm-up (sets kernel attributes), then one graph per rotation slot
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            store()
+            decode(i)
+    stream.synchronize()
+    if smla.read_device_status(ws, stream) != 0:
+        raise SystemExit("device status reports a kernel wait timeout")
+    n_rot = len(idx_sets)
+    step_graphs, decode_graphs = [], []
+    for i in range(n_rot):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            store()
+            decode(i)
+        step_graphs.append(g)
+        g2 = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g2, stream=stream):
+            decode(i)
+        decode_graphs.append(g2)
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step_graphs[i % n_rot].replay()
+    stream.synchronize()
+
+    launches_per_step = 1 + (2 if smla_plan_needs_combine(smla, T, H, K) else 1)
+
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
+    except Exception:
+        pass
+    clocks = ClockSampler(uuid)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+
+    # ---- timed region: exactly K steps
+    clocks.start()
+    barrier(world, device)
+    torch.cuda.synchronize(device)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(args.steps):
+            step_graphs[i % n_rot].replay()
+        e1.record(stream)
+    torch.cuda.synchronize(device)
+    barrier(world, device)
+    step_ms = e0.elapsed_time(e1) / args.steps
+    # ---- the decode launches alone, same rotation (roofline of the dominant kernel)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(args.steps):
+            decode_graphs[i % n_rot].replay()
+        e1.record(stream)
+    torch.cuda.synchronize(device)
+    clk = clocks.stop()
+    decode_ms = e0.elapsed_time(e1) / args.steps
+    if smla.read_device_status(ws, stream) != 0:
+        raise SystemExit("device status reports a kernel wait timeout")
+
+    step_ms_max = max_over_ranks(step_ms, world, device)
+    value = world * T / (step_ms_max * 1e-3)
+    alg_bytes = statistics.mean(decode_algorithmic_bytes(case, s) for s in case.index_sets)
+    flops = statistics.mean(decode_flops(case, s) for s in case.index_sets)
+    achieved_gbs = alg_bytes / (decode_ms * 1e-3) / 1e9
+
+    # ---- end to end through the public API with pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, smla, case, device, stream, cache, ws)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(case)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": step_ms_max, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {
+                "workload": f"{case.name}: memory-bound FP8 sparse decode, {T} requests x 1 token, H={H}, "
+                            f"top-k {K}, context U[8192,32768], block 64, 656-byte FP8 cache ({NB} blocks, "
+                            f"{NB * 64 * 656 / 1e9:.2f} GB)",
+                "step": "quantize-and-store of the 64 new rows + sparse decode (translate, gather/dequant, "
+                        "QK^T, softmax, P.V, combine)",
+                "l2": f"{n_rot} rotating top-k index sets ({n_rot} x {alg_bytes / 1e6:.0f} MB gathered) > 129 MB L2",
+                "parallelism": f"weak: {world} independent replica(s), one per GPU",
+                "launch": "CUDA graph per step",
+            },
+            "gb_per_s": achieved_gbs,
+            "tflops": flops / (decode_ms * 1e-3) / 1e12,
+            "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": None,
+                         "peak_source": peaks["source"],
+                         "kernel": "sparse decode launch (attention kernel + split combine)",
+                         "algorithmic_bytes_per_launch": int(alg_bytes), "avg_launch_us": decode_ms * 1e3},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def smla_plan_needs_combine(smla, T, H, K) -> bool:
+    import torch
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    hg = 32 if H % 32 == 0 else 16
+    units = T * (H // hg)
+    nt = max(1, (K + 63) // 64)
+    total = units * nt
+    G = max(1, min(total, sms))
+    return not (total % G == 0 and (total // G) % nt == 0)
+
+
+def run_e2e(args, smla, case, device, stream, cache, ws):
+    """Same step through the public API from pinned host buffers: each step
+    copies its inputs host->device, runs store + decode, and copies out + lse
+    back."""
+    import torch
+    T, H = case.q.shape[0], case.H
+    n_rot = len(case.index_sets)
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
+    h_q = pin(case.q.view(np.int16))
+    h_idx = [pin(s) for s in case.index_sets]
+    h_bt = pin(case.block_table)
+    h_req = pin(case.req_id_per_token)
+    rows = inp.device_latent(T, case.latent_seed + 1, case.outlier_channels, device)
+    h_rows = rows.view(torch.int16).cpu().pin_memory()
+    h_slots = pin(case.new_slots)
+    h_out = torch.empty((T, H, 512), dtype=torch.bfloat16).pin_memory()
+    h_lse = torch.empty((T, H), dtype=torch.float32).pin_memory()
+    d_q = torch.empty((T, H, 576), dtype=torch.int16, device=device)
+    d_idx = torch.empty_like(h_idx[0], device=device)
+    d_bt = torch.empty_like(h_bt, device=device)
+    d_req = torch.empty_like(h_req, device=device)
+    d_rows = torch.empty((T, 576), dtype=torch.int16, device=device)
+    d_slots = torch.empty_like(h_slots, device=device)
+    d_out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=device)
+    d_lse = torch.empty((T, H), dtype=torch.float32, device=device)
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_idx[0], h_bt, h_req, h_rows, h_slots))
+    d2h = h_out.numel() * 2 + h_lse.numel() * 4
+
+    def step(i):
+        d_q.copy_(h_q, non_blocking=True)
+        d_idx.copy_(h_idx[i % n_rot], non_blocking=True)
+        d_bt.copy_(h_bt, non_blocking=True)
+        d_req.copy_(h_req, non_blocking=True)
+        d_rows.copy_(h_rows, non_blocking=True)
+        d_slots.copy_(h_slots, non_blocking=True)
+        smla.mla_cache_store_fp8(d_rows.view(torch.bfloat16), d_slots, cache, stream=stream)
+        smla.sparse_mla_decode_fp8(d_q.view(torch.bfloat16), cache, d_idx, d_bt, d_req, case.sm_scale, 0, d_out,
+                                   d_lse, ws, stream=stream)
+        h_out.copy_(d_out, non_blocking=True)
+        h_lse.copy_(d_lse, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            step(i)
+    stream.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(args.steps):
+            step(i)
+        e1.record(stream)
+    stream.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    return {"value": T / (ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "ms_per_step": ms, "path": "public Python API (ctypes -> C ABI), eager launches, pinned host buffers"}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

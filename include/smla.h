@@ -1,0 +1,120 @@
+/*
+ * smla.h -- C ABI of the sparse MLA attention library for GB300 (sm_103a).
+ *
+ * The operations follow vLLM "vllm/v1/attention/backends/mla/flashmla_sparse.py"
+ * (cited below as [flashmla_sparse.py]):
+ *   - the "FP8 with scale" cache row (module docstring): 656 bytes per token =
+ *     512 float8_e4m3 NoPE values, 4 float32 scales (one per 128 values),
+ *     64 bfloat16 RoPE values;
+ *   - the paged cache [num_blocks, 64, 656] (FlashMLASparseBackend.get_kv_cache_shape);
+ *   - triton_convert_req_index_to_global_index (logical top-k index -> slot);
+ *   - FlashMLASparseImpl.forward: the cache write through slot_mapping
+ *     (concat_and_cache_mla), MQA 576/512 sparse attention with softmax_scale
+ *     through flash_mla_with_kvcache (FP8 decode) and flash_mla_sparse_prefill
+ *     (BF16 prefill).
+ *
+ * Conventions for every entry point:
+ *   - all tensor arguments are DEVICE pointers owned by the caller, contiguous,
+ *     row-major, on the current CUDA device; the library keeps no reference
+ *     after the call returns (the work itself is asynchronous on `stream`);
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream);
+ *   - calls enqueue work and return without synchronizing the host; they do not
+ *     allocate when the caller supplies the workspace;
+ *   - bf16 tensors are passed as void* holding IEEE bfloat16 values;
+ *   - return value: SMLA_OK, or a negative status; smla_last_error() returns a
+ *     thread-local description of the last failure on the calling thread.
+ *   - invalid DEVICE data (index -1, a block id out of range, a negative slot)
+ *     is never an error: it is masked (attention) or skipped (store).
+ */
+#ifndef SMLA_H_
+#define SMLA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SMLA_OK 0
+#define SMLA_ERR_INVALID_ARG -1   /* null pointer, bad size, misaligned pointer */
+#define SMLA_ERR_UNSUPPORTED -2   /* e.g. H not a multiple of 16, or H > 128 */
+#define SMLA_ERR_CUDA -3          /* a CUDA call or kernel launch failed */
+#define SMLA_ERR_WORKSPACE -4     /* caller workspace smaller than required */
+
+/* Sparse MLA decode over the FP8 paged cache (FP8 path of
+ * FlashMLASparseImpl.forward in [flashmla_sparse.py]; indices are translated
+ * inside, as triton_convert_req_index_to_global_index does).
+ *   q                bf16  [T, H, 576]   query (512 absorbed NoPE + 64 RoPE), 16-byte aligned
+ *   kv_cache         uint8 [NB, 64, 656] "FP8 with scale" rows, 16-byte aligned
+ *   indices          int32 [T, K]        logical positions within the token's request; <0 = none
+ *   block_table      int32 [R, MB]       physical block of each logical block of a request
+ *   req_id_per_token int32 [T]           request of each query token
+ *   sm_scale         softmax scale applied to q.k
+ *   num_splits       0 = automatic work split over all SMs; s > 0 = about s CTAs per (token, head group)
+ *   out              bf16  [T, H, 512]   attention output (written)
+ *   lse              fp32  [T, H]        natural-log sum of exp of the scaled logits (written);
+ *                                        a token with no valid index gets out = 0 and lse = -inf
+ *   T, H, K, R, MB, NB  sizes; H must be a multiple of 16 and at most 128
+ *   workspace        device scratch of at least sparse_mla_decode_workspace_bytes(T, H, K, num_splits)
+ *                    bytes, 256-byte aligned; NULL = a buffer cached by the library per device
+ *                    (allocated on first use, so that call is not graph-capturable)
+ * A slot is invalid (masked) when the index is negative, its block id is >= MB, the request id is
+ * outside [0, R) or the physical block is outside [0, NB). */
+int sparse_mla_decode_fp8(const void* q, const uint8_t* kv_cache, const int32_t* indices,
+                          const int32_t* block_table, const int32_t* req_id_per_token, float sm_scale,
+                          int num_splits, void* out, float* lse, int T, int H, int K, int R, int MB, int NB,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace bytes sparse_mla_decode_fp8 needs on the current device. */
+size_t sparse_mla_decode_workspace_bytes(int T, int H, int K, int num_splits);
+
+/* Sparse MLA prefill over a dense bf16 latent buffer (flash_mla_sparse_prefill
+ * as called by FlashMLASparseImpl._bf16_flash_mla_kernel in
+ * [flashmla_sparse.py]; heads need no padding here).
+ *   q        bf16 [T, H, 576]; kv bf16 [N, 576] (row i = latent row i); indices int32 [T, K] rows of
+ *   kv, an index < 0 or >= N is masked; out bf16 [T, H, 512]; lse fp32 [T, H].
+ *   num_splits / workspace as for decode (sparse_mla_prefill_workspace_bytes). */
+int sparse_mla_prefill_bf16(const void* q, const void* kv, const int32_t* indices, float sm_scale,
+                            int num_splits, void* out, float* lse, int T, int H, int N, int K, void* workspace,
+                            size_t workspace_bytes, void* stream);
+
+size_t sparse_mla_prefill_workspace_bytes(int T, int H, int K, int num_splits);
+
+/* Quantize-and-store of new tokens into the FP8 cache (cache write of
+ * FlashMLASparseImpl.forward, concat_and_cache_mla with "fp8_ds_mla", in
+ * [flashmla_sparse.py]).
+ *   kv_new       bf16 [T, 576]: 512 latent (NoPE) values followed by 64 RoPE values, 16-byte aligned
+ *   slot_mapping int64 [T]: destination row (block * 64 + offset); < 0 or >= NB*64 skips the token
+ *   kv_cache     uint8 [NB, 64, 656], 16-byte aligned
+ * Per group of 128 NoPE values: scale = amax / 448 in IEEE float32, code = the float32 quotient
+ * value / scale rounded to nearest-even e4m3 with saturation (a group with scale 0 stores zeros);
+ * the 4 scales and the RoPE values are stored verbatim.  Two tokens with the same slot race. */
+int mla_cache_store_fp8(const void* kv_new, const int64_t* slot_mapping, uint8_t* kv_cache, int T, int NB,
+                        void* stream);
+
+/* Logical -> physical slot translation on its own (the step the decode
+ * kernel fuses), as triton_convert_req_index_to_global_index in
+ * [flashmla_sparse.py]: slots_out[t, k] = block_table[req[t], idx // 64] * 64 + idx % 64, or -1
+ * under the invalid conditions listed for sparse_mla_decode_fp8.  slots_out int32 [T, K]. */
+int sparse_mla_translate_indices(const int32_t* indices, const int32_t* block_table,
+                                 const int32_t* req_id_per_token, int32_t* slots_out, int T, int K, int R,
+                                 int MB, int NB, void* stream);
+
+/* Reads (and clears) the device status word of a workspace after
+ * synchronizing `stream`: 0 = no fault; 1 = a kernel wait ran past its time
+ * limit and the kernel unwound (its outputs are not valid).  workspace NULL =
+ * the library-cached workspace of the current device. */
+int smla_read_device_status(void* workspace, int* status_out, void* stream);
+
+/* Thread-local description of the last failing call on this thread. */
+const char* smla_last_error(void);
+
+/* Library ABI version (major * 100 + minor). */
+int smla_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SMLA_H_ */

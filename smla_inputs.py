@@ -24,11 +24,14 @@ D_V = 512
 
 
 def bf16_bits(x: np.ndarray) -> np.ndarray:
-    """float32 array -> bfloat16 bit patterns (uint16), round to nearest even."""
-    f = np.ascontiguousarray(x, dtype=np.float32)
-    u = f.view(np.uint32).astype(np.uint64)
-    rounded = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
-    return rounded.astype(np.uint16)
+    """float32 array -> bfloat16 bit patterns (uint16), round to nearest even
+    (finite inputs)."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    r = (u >> 16) & 1
+    r += 0x7FFF
+    r += u
+    r >>= 16
+    return r.astype(np.uint16)
 
 
 def bits_to_float(b: np.ndarray) -> np.ndarray:
@@ -249,3 +252,63 @@ def make_cache(case: DecodeCase, quantize_store) -> np.ndarray:
     if len(case.cache_slots):
         quantize_store(case.cache_rows, case.cache_slots, cache)
     return cache
+
+
+# ---------------------------------------------------------------- benchmark inputs
+
+@dataclass
+class RotatingDecode:
+    """A decode workload with several independent top-k index sets over one
+    cache, so successive steps gather different rows.  Latent rows are drawn
+    on the device (``device_latent``) because the cache holds every context
+    row of every request: ``ctx_slots`` are positions 0..ctx-2 of each
+    request, ``new_slots`` the step's new token (position ctx-1), one per
+    decode token."""
+    name: str
+    H: int
+    K: int
+    sm_scale: float
+    q: np.ndarray
+    index_sets: list
+    block_table: np.ndarray
+    req_id_per_token: np.ndarray
+    num_blocks: int
+    ctx_lens: np.ndarray
+    ctx_slots: np.ndarray
+    new_slots: np.ndarray
+    outlier_channels: np.ndarray
+    latent_seed: int
+
+
+def rotating_decode(seed: int = 1, R: int = 64, ctx_lo: int = 8192, ctx_hi: int = 32768, K: int = 2048, H: int = 16,
+                    n_sets: int = 8, outliers: bool = True) -> RotatingDecode:
+    """Benchmark form of the memory-bound decode workload: R requests x 1
+    token, context uniform in [ctx_lo, ctx_hi], latent N(0,1) with 1% of the
+    channels x8, unique unsorted top-k indices, ``n_sets`` independent index
+    sets."""
+    rng = np.random.default_rng(seed)
+    ctx = rng.integers(ctx_lo, ctx_hi + 1, size=R).astype(np.int64)
+    bt, NB = _paged_layout(rng, ctx)
+    outlier_ch = (np.sort(rng.choice(D_QK, size=int(np.ceil(0.01 * D_QK)), replace=False)) if outliers
+                  else np.zeros(0, np.int64))
+    q = bf16_bits(rng.standard_normal((R, H, D_QK), dtype=np.float32))
+    sets = [np.stack([_causal_topk(rng, int(c), K) for c in ctx]).astype(np.int32) for _ in range(n_sets)]
+    ctx_slots = np.concatenate([_slot_of(bt, r, np.arange(ctx[r] - 1)) for r in range(R)])
+    new_slots = np.array([_slot_of(bt, r, np.array([ctx[r] - 1]))[0] for r in range(R)], np.int64)
+    return RotatingDecode(name=f"decode_h{H}_k{K}_r{R}", H=H, K=K, sm_scale=D_QK ** -0.5, q=q, index_sets=sets,
+                          block_table=bt, req_id_per_token=np.arange(R, dtype=np.int32), num_blocks=NB,
+                          ctx_lens=ctx, ctx_slots=ctx_slots.astype(np.int64), new_slots=new_slots,
+                          outlier_channels=outlier_ch, latent_seed=seed + 7919)
+
+
+def device_latent(n: int, seed: int, outlier_channels, device="cuda"):
+    """n latent rows N(0,1) (1% outlier channels x8) as a bf16 torch tensor
+    [n, 576] drawn on ``device`` with a seeded torch generator (deterministic
+    for a given torch build and device type)."""
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    x = torch.randn((n, D_QK), generator=g, device=device, dtype=torch.float32)
+    if outlier_channels is not None and len(outlier_channels):
+        x[:, torch.as_tensor(np.asarray(outlier_channels), device=device)] *= 8.0
+    return x.to(torch.bfloat16)

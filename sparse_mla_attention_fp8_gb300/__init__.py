@@ -1,0 +1,256 @@
+"""Sparse MLA attention over the 656-byte FP8 cache, for GB300 (sm_103a).
+
+Thin Python binding of the C-ABI library ``libsmla.so`` (declared in
+``include/smla.h``).  Every function here only marshals torch tensors into
+pointers and sizes and calls the same-named C entry point; all the work runs
+in the library's CUDA kernels.  There is no CPU fallback: if the library has
+not been built, or a tensor is not on a CUDA device, the call raises.
+
+Entry points (see include/smla.h for layouts and semantics):
+  sparse_mla_decode_fp8, sparse_mla_prefill_bf16, mla_cache_store_fp8,
+  sparse_mla_translate_indices, plus workspace-size and status helpers.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from concurrent.futures import ThreadPoolExecutor
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_ROOT = os.path.dirname(_PKG)
+_CSRC = os.path.join(_PKG, "csrc")
+_BUILD = os.path.join(_PKG, "_build")
+LIB_PATH = os.path.join(_PKG, "libsmla.so")
+HEADER = os.path.join(_ROOT, "include", "smla.h")
+
+SOURCES = ["smla_attn.cu", "smla_store.cu", "smla_api.cu"]
+NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-std=c++17", "-lineinfo",
+              "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall"]
+
+SMLA_OK = 0
+_lock = threading.Lock()
+_lib = None
+
+
+class SmlaError(RuntimeError):
+    pass
+
+
+def _nvcc() -> str:
+    cand = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "bin", "nvcc")
+    return cand if os.path.exists(cand) else "nvcc"
+
+
+def _stale(obj: str, src: str) -> bool:
+    if not os.path.exists(obj):
+        return True
+    deps = [src] + [os.path.join(_CSRC, f) for f in os.listdir(_CSRC) if f.endswith((".cuh", ".h"))] + [HEADER]
+    t = os.path.getmtime(obj)
+    return any(os.path.getmtime(d) > t for d in deps)
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile the CUDA sources for sm_103a (in parallel) and link libsmla.so
+    in place.  Works without a GPU (nvcc cross-compiles)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    nvcc = _nvcc()
+    jobs = []
+    for s in SOURCES:
+        src = os.path.join(_CSRC, s)
+        obj = os.path.join(_BUILD, s.replace(".cu", ".o"))
+        if force or _stale(obj, src):
+            jobs.append([nvcc, *NVCC_FLAGS, "-c", src, "-o", obj])
+
+    def run(cmd):
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise SmlaError(f"nvcc failed: {' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
+        if verbose:
+            print(r.stdout + r.stderr)
+
+    if jobs:
+        with ThreadPoolExecutor(max_workers=len(jobs)) as ex:
+            list(ex.map(run, jobs))
+    objs = [os.path.join(_BUILD, s.replace(".cu", ".o")) for s in SOURCES]
+    if force or jobs or not os.path.exists(LIB_PATH):
+        tmp = LIB_PATH + f".tmp{os.getpid()}"
+        run([nvcc, "-shared", "-gencode", "arch=compute_103a,code=sm_103a", *objs, "-o", tmp])
+        os.replace(tmp, LIB_PATH)
+    return LIB_PATH
+
+
+def lib():
+    """The loaded C library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise SmlaError(f"{LIB_PATH} is missing: run sparse_mla_attention_fp8_gb300.build() first")
+            L = ctypes.CDLL(LIB_PATH)
+            P, i32, sz, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_float
+            L.sparse_mla_decode_fp8.argtypes = [P, P, P, P, P, f32, i32, P, P, i32, i32, i32, i32, i32, i32, P, sz, P]
+            L.sparse_mla_decode_fp8.restype = i32
+            L.sparse_mla_decode_workspace_bytes.argtypes = [i32, i32, i32, i32]
+            L.sparse_mla_decode_workspace_bytes.restype = sz
+            L.sparse_mla_prefill_bf16.argtypes = [P, P, P, f32, i32, P, P, i32, i32, i32, i32, P, sz, P]
+            L.sparse_mla_prefill_bf16.restype = i32
+            L.sparse_mla_prefill_workspace_bytes.argtypes = [i32, i32, i32, i32]
+            L.sparse_mla_prefill_workspace_bytes.restype = sz
+            L.mla_cache_store_fp8.argtypes = [P, P, P, i32, i32, P]
+            L.mla_cache_store_fp8.restype = i32
+            L.sparse_mla_translate_indices.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, P]
+            L.sparse_mla_translate_indices.restype = i32
+            L.smla_read_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_int), P]
+            L.smla_read_device_status.restype = i32
+            L.smla_last_error.argtypes = []
+            L.smla_last_error.restype = ctypes.c_char_p
+            L.smla_version.argtypes = []
+            L.smla_version.restype = i32
+            _lib = L
+    return _lib
+
+
+def _check(rc: int, what: str):
+    if rc != SMLA_OK:
+        msg = lib().smla_last_error().decode(errors="replace")
+        raise SmlaError(f"{what} failed with status {rc}: {msg}")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_ptr(stream, device):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dev(*tensors):
+    dev = None
+    for t in tensors:
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise SmlaError("all tensors must be CUDA tensors (there is no CPU path)")
+        if not t.is_contiguous():
+            raise SmlaError("all tensors must be contiguous")
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise SmlaError("all tensors must be on the same device")
+    return dev
+
+
+def _expect(t, dtype, shape, name):
+    if t.dtype != dtype:
+        raise SmlaError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise SmlaError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def decode_workspace_bytes(T: int, H: int, K: int, num_splits: int = 0) -> int:
+    return int(lib().sparse_mla_decode_workspace_bytes(T, H, K, num_splits))
+
+
+def prefill_workspace_bytes(T: int, H: int, K: int, num_splits: int = 0) -> int:
+    return int(lib().sparse_mla_prefill_workspace_bytes(T, H, K, num_splits))
+
+
+def sparse_mla_decode_fp8(q, kv_cache, indices, block_table, req_id_per_token, sm_scale: float,
+                          num_splits: int = 0, out=None, lse=None, workspace=None, stream=None):
+    """FP8 sparse decode.  q bf16 [T,H,576]; kv_cache uint8 [NB,64,656];
+    indices int32 [T,K] (logical, <0 = none); block_table int32 [R,MB];
+    req_id_per_token int32 [T].  Returns (out bf16 [T,H,512], lse fp32 [T,H])."""
+    import torch
+    dev = _dev(q, kv_cache, indices, block_table, req_id_per_token, out, lse, workspace)
+    T, H, D = q.shape
+    NB = kv_cache.shape[0]
+    K = indices.shape[1]
+    R, MB = block_table.shape
+    _expect(q, torch.bfloat16, (T, H, 576), "q")
+    _expect(kv_cache, torch.uint8, (NB, 64, 656), "kv_cache")
+    _expect(indices, torch.int32, (T, K), "indices")
+    _expect(req_id_per_token, torch.int32, (T,), "req_id_per_token")
+    if block_table.dtype != torch.int32:
+        raise SmlaError("block_table must be int32")
+    if out is None:
+        out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+    _expect(out, torch.bfloat16, (T, H, 512), "out")
+    _expect(lse, torch.float32, (T, H), "lse")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib().sparse_mla_decode_fp8(_ptr(q), _ptr(kv_cache), _ptr(indices), _ptr(block_table),
+                                     _ptr(req_id_per_token), float(sm_scale), int(num_splits), _ptr(out), _ptr(lse),
+                                     T, H, K, R, MB, NB, _ptr(workspace), ws_bytes, _stream_ptr(stream, dev))
+    _check(rc, "sparse_mla_decode_fp8")
+    return out, lse
+
+
+def sparse_mla_prefill_bf16(q, kv, indices, sm_scale: float, num_splits: int = 0, out=None, lse=None,
+                            workspace=None, stream=None):
+    """BF16 sparse prefill.  q bf16 [T,H,576]; kv bf16 [N,576]; indices int32
+    [T,K] rows of kv (<0 or >=N = none).  Returns (out, lse)."""
+    import torch
+    dev = _dev(q, kv, indices, out, lse, workspace)
+    T, H, D = q.shape
+    N = kv.shape[0]
+    K = indices.shape[1]
+    _expect(q, torch.bfloat16, (T, H, 576), "q")
+    _expect(kv, torch.bfloat16, (N, 576), "kv")
+    _expect(indices, torch.int32, (T, K), "indices")
+    if out is None:
+        out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+    _expect(out, torch.bfloat16, (T, H, 512), "out")
+    _expect(lse, torch.float32, (T, H), "lse")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib().sparse_mla_prefill_bf16(_ptr(q), _ptr(kv), _ptr(indices), float(sm_scale), int(num_splits),
+                                       _ptr(out), _ptr(lse), T, H, N, K, _ptr(workspace), ws_bytes,
+                                       _stream_ptr(stream, dev))
+    _check(rc, "sparse_mla_prefill_bf16")
+    return out, lse
+
+
+def mla_cache_store_fp8(kv_new, slot_mapping, kv_cache, stream=None):
+    """Quantize bf16 [T,576] rows into kv_cache uint8 [NB,64,656] at
+    slot_mapping int64 [T] (<0 skips).  Modifies kv_cache in place."""
+    import torch
+    dev = _dev(kv_new, slot_mapping, kv_cache)
+    T = kv_new.shape[0]
+    NB = kv_cache.shape[0]
+    _expect(kv_new, torch.bfloat16, (T, 576), "kv_new")
+    _expect(slot_mapping, torch.int64, (T,), "slot_mapping")
+    _expect(kv_cache, torch.uint8, (NB, 64, 656), "kv_cache")
+    rc = lib().mla_cache_store_fp8(_ptr(kv_new), _ptr(slot_mapping), _ptr(kv_cache), T, NB, _stream_ptr(stream, dev))
+    _check(rc, "mla_cache_store_fp8")
+    return kv_cache
+
+
+def sparse_mla_translate_indices(indices, block_table, req_id_per_token, num_blocks: int, out=None, stream=None):
+    """Logical top-k indices -> physical cache slots (int32 [T,K], -1 = none)."""
+    import torch
+    dev = _dev(indices, block_table, req_id_per_token, out)
+    T, K = indices.shape
+    R, MB = block_table.shape
+    if out is None:
+        out = torch.empty((T, K), dtype=torch.int32, device=dev)
+    rc = lib().sparse_mla_translate_indices(_ptr(indices), _ptr(block_table), _ptr(req_id_per_token), _ptr(out),
+                                            T, K, R, MB, int(num_blocks), _stream_ptr(stream, dev))
+    _check(rc, "sparse_mla_translate_indices")
+    return out
+
+
+def read_device_status(workspace=None, stream=None) -> int:
+    """Synchronize and read/clear the kernels' device status word (0 = ok)."""
+    import torch
+    st = ctypes.c_int(0)
+    dev = workspace.device if workspace is not None else torch.device("cuda", torch.cuda.current_device())
+    rc = lib().smla_read_device_status(_ptr(workspace), ctypes.byref(st), _stream_ptr(stream, dev))
+    _check(rc, "smla_read_device_status")
+    return int(st.value)

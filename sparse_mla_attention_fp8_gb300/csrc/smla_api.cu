@@ -1,0 +1,260 @@
+// C-ABI entry points: argument validation, work planning, workspace handling
+// and kernel dispatch.  Every function returns a status code; nothing throws
+// and nothing synchronizes the host on the launch path.
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include <cuda_runtime.h>
+
+#include "../../include/smla.h"
+#include "smla_kernels.h"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(SMLA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  int num_sms = 0;
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+};
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+
+int current_device(int* dev) {
+  cudaError_t e = cudaGetDevice(dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (*dev < 0 || *dev >= kMaxDevices) return fail(SMLA_ERR_UNSUPPORTED, "device ordinal %d out of range", *dev);
+  return SMLA_OK;
+}
+
+int num_sms(int* out) {
+  int dev;
+  int rc = current_device(&dev);
+  if (rc != SMLA_OK) return rc;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (g_dev[dev].num_sms == 0) {
+    int n = 0;
+    cudaError_t e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    g_dev[dev].num_sms = n;
+  }
+  *out = g_dev[dev].num_sms;
+  return SMLA_OK;
+}
+
+// Library-cached workspace of the current device, grown on demand.  Growing
+// frees the old buffer after a device synchronize, so callers must not have
+// other work using it in flight on other streams.
+int cached_workspace(size_t need, void** out) {
+  int dev;
+  int rc = current_device(&dev);
+  if (rc != SMLA_OK) return rc;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState& d = g_dev[dev];
+  if (d.ws_bytes < need) {
+    if (d.ws) {
+      cudaDeviceSynchronize();
+      cudaFree(d.ws);
+      d.ws = nullptr;
+      d.ws_bytes = 0;
+    }
+    size_t sz = need < (size_t(1) << 20) ? (size_t(1) << 20) : need;
+    cudaError_t e = cudaMalloc(&d.ws, sz);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(workspace)");
+    e = cudaMemset(d.ws, 0, sz);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(workspace)");
+    d.ws_bytes = sz;
+  }
+  *out = d.ws;
+  return SMLA_OK;
+}
+
+int check_heads(int H) {
+  if (H <= 0 || H % 16 != 0 || H > 128)
+    return fail(SMLA_ERR_UNSUPPORTED, "H=%d unsupported: must be a positive multiple of 16, at most 128", H);
+  return SMLA_OK;
+}
+
+int run_attention(bool fp8, smla::AttnArgs& a, int num_splits, void* workspace, size_t workspace_bytes,
+                  void* stream) {
+  int sms = 0;
+  int rc = num_sms(&sms);
+  if (rc != SMLA_OK) return rc;
+  const smla::AttnPlan plan = smla::plan_attention(a.T, a.H, a.K, num_splits, sms);
+  if (workspace) {
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+      return fail(SMLA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    if (workspace_bytes < plan.ws_bytes)
+      return fail(SMLA_ERR_WORKSPACE, "workspace has %zu bytes, %zu needed", workspace_bytes, plan.ws_bytes);
+  } else {
+    rc = cached_workspace(plan.ws_bytes, &workspace);
+    if (rc != SMLA_OK) return rc;
+  }
+  a.workspace = workspace;
+  cudaError_t e = smla::launch_attention(fp8, a, plan, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, fp8 ? "sparse_mla_decode_fp8 launch" : "sparse_mla_prefill_bf16 launch");
+  return SMLA_OK;
+}
+
+size_t workspace_bytes_for(int T, int H, int K, int num_splits) {
+  if (T <= 0 || check_heads(H) != SMLA_OK || K < 0) return 0;
+  int sms = 0;
+  if (num_sms(&sms) != SMLA_OK) return 0;
+  return smla::plan_attention(T, H, K, num_splits, sms).ws_bytes;
+}
+
+}  // namespace
+
+extern "C" {
+
+int sparse_mla_decode_fp8(const void* q, const uint8_t* kv_cache, const int32_t* indices,
+                          const int32_t* block_table, const int32_t* req_id_per_token, float sm_scale,
+                          int num_splits, void* out, float* lse, int T, int H, int K, int R, int MB, int NB,
+                          void* workspace, size_t workspace_bytes, void* stream) {
+  if (T < 0 || K < 0 || R <= 0 || MB <= 0 || NB <= 0 || num_splits < 0)
+    return fail(SMLA_ERR_INVALID_ARG, "bad sizes T=%d K=%d R=%d MB=%d NB=%d num_splits=%d", T, K, R, MB, NB,
+                num_splits);
+  int rc = check_heads(H);
+  if (rc != SMLA_OK) return rc;
+  if (T == 0) return SMLA_OK;
+  if (!q || !kv_cache || (!indices && K > 0) || !block_table || !req_id_per_token || !out || !lse)
+    return fail(SMLA_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned16(q) || !aligned16(kv_cache) || !aligned16(out))
+    return fail(SMLA_ERR_INVALID_ARG, "q, kv_cache and out must be 16-byte aligned");
+  if ((int64_t)NB * 64 > INT32_MAX) return fail(SMLA_ERR_UNSUPPORTED, "NB*64 must fit in int32");
+  smla::AttnArgs a{};
+  a.q = q;
+  a.cache = kv_cache;
+  a.kv = nullptr;
+  a.indices = indices;
+  a.block_table = block_table;
+  a.req_id = req_id_per_token;
+  a.out = out;
+  a.lse = lse;
+  a.sm_scale = sm_scale;
+  a.T = T;
+  a.H = H;
+  a.K = K;
+  a.R = R;
+  a.MB = MB;
+  a.NB = NB;
+  return run_attention(true, a, num_splits, workspace, workspace_bytes, stream);
+}
+
+size_t sparse_mla_decode_workspace_bytes(int T, int H, int K, int num_splits) {
+  return workspace_bytes_for(T, H, K, num_splits);
+}
+
+int sparse_mla_prefill_bf16(const void* q, const void* kv, const int32_t* indices, float sm_scale,
+                            int num_splits, void* out, float* lse, int T, int H, int N, int K, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+  if (T < 0 || K < 0 || N <= 0 || num_splits < 0)
+    return fail(SMLA_ERR_INVALID_ARG, "bad sizes T=%d N=%d K=%d num_splits=%d", T, N, K, num_splits);
+  int rc = check_heads(H);
+  if (rc != SMLA_OK) return rc;
+  if (T == 0) return SMLA_OK;
+  if (!q || !kv || (!indices && K > 0) || !out || !lse) return fail(SMLA_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned16(q) || !aligned16(kv) || !aligned16(out))
+    return fail(SMLA_ERR_INVALID_ARG, "q, kv and out must be 16-byte aligned");
+  smla::AttnArgs a{};
+  a.q = q;
+  a.cache = nullptr;
+  a.kv = kv;
+  a.indices = indices;
+  a.block_table = nullptr;
+  a.req_id = nullptr;
+  a.out = out;
+  a.lse = lse;
+  a.sm_scale = sm_scale;
+  a.T = T;
+  a.H = H;
+  a.K = K;
+  a.R = 1;
+  a.MB = 1;
+  a.NB = N;
+  return run_attention(false, a, num_splits, workspace, workspace_bytes, stream);
+}
+
+size_t sparse_mla_prefill_workspace_bytes(int T, int H, int K, int num_splits) {
+  return workspace_bytes_for(T, H, K, num_splits);
+}
+
+int mla_cache_store_fp8(const void* kv_new, const int64_t* slot_mapping, uint8_t* kv_cache, int T, int NB,
+                        void* stream) {
+  if (T < 0 || NB <= 0) return fail(SMLA_ERR_INVALID_ARG, "bad sizes T=%d NB=%d", T, NB);
+  if (T == 0) return SMLA_OK;
+  if (!kv_new || !slot_mapping || !kv_cache) return fail(SMLA_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned16(kv_new) || !aligned16(kv_cache))
+    return fail(SMLA_ERR_INVALID_ARG, "kv_new and kv_cache must be 16-byte aligned");
+  cudaError_t e = smla::launch_quantize_store(kv_new, slot_mapping, kv_cache, T, NB, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "mla_cache_store_fp8 launch");
+  return SMLA_OK;
+}
+
+int sparse_mla_translate_indices(const int32_t* indices, const int32_t* block_table,
+                                 const int32_t* req_id_per_token, int32_t* slots_out, int T, int K, int R,
+                                 int MB, int NB, void* stream) {
+  if (T < 0 || K < 0 || R <= 0 || MB <= 0 || NB <= 0)
+    return fail(SMLA_ERR_INVALID_ARG, "bad sizes T=%d K=%d R=%d MB=%d NB=%d", T, K, R, MB, NB);
+  if (T == 0 || K == 0) return SMLA_OK;
+  if (!indices || !block_table || !req_id_per_token || !slots_out)
+    return fail(SMLA_ERR_INVALID_ARG, "null pointer argument");
+  if ((int64_t)NB * 64 > INT32_MAX) return fail(SMLA_ERR_UNSUPPORTED, "NB*64 must fit in int32");
+  cudaError_t e = smla::launch_translate(indices, block_table, req_id_per_token, slots_out, T, K, R, MB, NB,
+                                         static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "sparse_mla_translate_indices launch");
+  return SMLA_OK;
+}
+
+int smla_read_device_status(void* workspace, int* status_out, void* stream) {
+  if (!status_out) return fail(SMLA_ERR_INVALID_ARG, "null status_out");
+  if (!workspace) {
+    int dev;
+    int rc = current_device(&dev);
+    if (rc != SMLA_OK) return rc;
+    std::lock_guard<std::mutex> lk(g_mu);
+    workspace = g_dev[dev].ws;
+  }
+  if (!workspace) {
+    *status_out = 0;
+    return SMLA_OK;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  int v = 0;
+  e = cudaMemcpy(&v, workspace, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(status)");
+  if (v != 0) {
+    e = cudaMemset(workspace, 0, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(status)");
+  }
+  *status_out = v;
+  return SMLA_OK;
+}
+
+const char* smla_last_error(void) { return g_err; }
+
+int smla_version(void) { return 100; }
+
+}  // extern "C"

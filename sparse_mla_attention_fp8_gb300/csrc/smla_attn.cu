@@ -1,0 +1,784 @@
+// Sparse MLA attention on sm_103a: FP8 decode over the paged 656-byte cache
+// and BF16 prefill over a dense [N, 576] latent buffer.
+//
+// What is computed (vLLM flashmla_sparse.py, FlashMLASparseImpl.forward and
+// its FlashMLA kernel calls): every query token t attends with each of its H
+// heads to its own K top-k latent rows (MQA 576/512: all heads share the
+// rows; V is the 512-wide NoPE part of each row).  Per head h:
+//   s_j   = softmax_scale * <q[t,h,:], row_j>        (576-wide)
+//   out   = sum_j softmax(s)_j * row_j[0:512]         (bf16 [T, H, 512])
+//   lse   = log(sum_j exp(s_j))                       (fp32 [T, H])
+// Invalid indices (-1 after translation) are masked; a token with no valid
+// row gets out = 0 and lse = -inf.
+//
+// Design (one persistent CTA per SM, warp-specialised, tcgen05 tensor cores):
+//  * Work units are (token, head group of HG heads); each unit is K/64 tiles
+//    of 64 top-k rows.  The CTAs split the unit-major tile sequence into equal
+//    contiguous ranges, so a unit may be split across CTAs ("segments"); a
+//    unit finished inside one CTA is written directly, the others go through
+//    an LSE-weighted combine kernel.
+//  * Index warp: translates tile row indices to cache slots into a 4-deep
+//    shared ring and (re)loads the unit's Q block into shared memory.
+//  * Converter warps: stream rows straight from HBM with 16-byte coalesced
+//    loads (a warp reads one 656-byte row per step, 6 rows in flight) and
+//    write the K-major, 128-byte-swizzled bf16 operand tile (two tiles are
+//    double-buffered).  The e4m3 codes are widened exactly (every e4m3 value
+//    is a bf16 value); the row's four float32 scales go to a side array.
+//  * MMA warp (one thread): S_g^T = E_g Q_g^T per 128-column scale group g
+//    (four accumulators) plus the RoPE part, with tcgen05.mma (M = 64 rows,
+//    N = HG heads); O^T += V^T P_q^T per 128-column value chunk q (M = 128,
+//    N = HG, K = 64 rows), reading V straight from the same tile as an
+//    MN-major operand.  Accumulators live in tensor memory.
+//  * Softmax warpgroup (4 warps): s = sum_g scale_g * S_g + S_rope in fp32
+//    (so quantization scales never pass through bf16 on the logit path),
+//    online softmax with lazy rescaling of O (only when a running max grows
+//    by more than 2^8), P_q = p * scale_q written to shared memory as the B
+//    operand of chunk q (value chunk q is exactly scale group q), epilogue.
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "sm103_ptx.cuh"
+#include "smla_common.cuh"
+#include "smla_kernels.h"
+
+namespace smla {
+
+namespace {
+
+constexpr uint32_t kFull = 0xffffffffu;
+
+template <int HG, bool kFp8>
+struct Cfg {
+  static constexpr int kRows = 64;                       // top-k rows per tile
+  static constexpr int kPanel = kRows * 128;             // one 64-column panel of the row tile
+  static constexpr int kKvTile = 9 * kPanel;             // 576 columns
+  static constexpr int kQPanel = HG * 128;
+  static constexpr int kQBytes = 9 * kQPanel;
+  static constexpr int kPBytes = kRows * HG * 2;
+  static constexpr int kMmaWarp = 4;
+  static constexpr int kIndexWarp = 5;
+  static constexpr int kConvWarp0 = 6;
+  static constexpr int kConvWarps = 10;
+  static constexpr int kThreads = 32 * (kConvWarp0 + kConvWarps);
+  static constexpr int kDepth = kFp8 ? 6 : 4;            // rows in flight per converter warp
+  static constexpr int kNS = kFp8 ? 5 : 1;              // S^T accumulators per tile: 4 scale groups + RoPE
+  static constexpr int kNP = kFp8 ? 4 : 1;              // P^T operands per tile (one per value chunk)
+  static constexpr int kSCol = 0;                        // S^T buffers: columns [0, 2 * kNS * HG)
+  static constexpr int kOCol = 2 * kNS * HG;             // O^T: 4 chunks of HG columns
+  static constexpr int kColsUsed = kOCol + 4 * HG;
+  static constexpr int kTmemCols = kColsUsed <= 128 ? 128 : (kColsUsed <= 256 ? 256 : 512);
+  // shared memory layout, offsets from a 1024-byte aligned base
+  static constexpr int kOffKv = 0;
+  static constexpr int kOffQ = kOffKv + 2 * kKvTile;
+  static constexpr int kOffP = kOffQ + kQBytes;
+  static constexpr int kOffScale = kOffP + 2 * kNP * kPBytes;  // float [2][64][4] row scales
+  static constexpr int kOffSlots = kOffScale + 2 * kRows * 16;  // int32 [4][64]
+  static constexpr int kOffValid = kOffSlots + 4 * kRows * 4;  // uint8 [2][64]
+  static constexpr int kOffRedMax = kOffValid + 2 * kRows;     // float [2][4][HG]
+  static constexpr int kOffRedSum = kOffRedMax + 2 * 4 * HG * 4;  // float [4][HG]
+  static constexpr int kOffBar = kOffRedSum + 4 * HG * 4;
+  // barriers
+  static constexpr int kBarKvFull = 0, kBarKvEmpty = 2, kBarSFull = 4, kBarPFull = 6, kBarPvDone = 8,
+                       kBarIdxFull = 10, kBarIdxEmpty = 14, kBarQFull = 18, kBarQEmpty = 19, kBarOFree = 20;
+  static constexpr int kNumBars = 21;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort flag
+  static constexpr int kSmemBytes = kOffMisc + 16;
+  static constexpr int kSmemAlloc = kSmemBytes + 1024;
+  static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0, "operand tiles must be 1024-byte aligned");
+  static_assert(kOffBar % 8 == 0, "mbarrier alignment");
+  static_assert(kSmemAlloc <= 232448, "shared memory budget");
+  static_assert(kColsUsed <= 512, "tensor memory budget");
+};
+
+struct Params {
+  const __nv_bfloat16* q;
+  const uint8_t* cache;
+  const __nv_bfloat16* kv;
+  const int32_t* indices;
+  const int32_t* block_table;
+  const int32_t* req_id;
+  __nv_bfloat16* out;
+  float* lse;
+  float* part_o;
+  float* part_lse;
+  int* status;
+  float scale_log2;
+  int T, H, K, R, MB;
+  int64_t NB;
+  int n_hg, nt;
+  int64_t total;
+  int G;
+};
+
+__device__ __forceinline__ int64_t tile_begin(int64_t c, int64_t total, int G) { return (c * total) / G; }
+
+struct TileInfo {
+  int u, kt, t, hg;
+  bool seg_start, seg_end;
+};
+
+__device__ __forceinline__ TileInfo tile_info(const Params& p, int64_t x, int64_t xbeg, int64_t xend) {
+  TileInfo ti;
+  ti.u = (int)(x / p.nt);
+  ti.kt = (int)(x - (int64_t)ti.u * p.nt);
+  ti.t = ti.u / p.n_hg;
+  ti.hg = ti.u - ti.t * p.n_hg;
+  ti.seg_start = (x == xbeg) || (ti.kt == 0);
+  ti.seg_end = (x == xend - 1) || (ti.kt == p.nt - 1);
+  return ti;
+}
+
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+__device__ __forceinline__ void named_bar_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// 4 e4m3 codes (one 32-bit word, lowest byte first) -> 2 words of bf16x2
+// (lowest column in the low half).  Exact: every e4m3 value is a bf16 value.
+__device__ __forceinline__ void widen4(uint32_t w, uint32_t& o0, uint32_t& o1) {
+  uint32_t h01, h23;
+  const uint16_t lo = (uint16_t)(w & 0xFFFFu), hi = (uint16_t)(w >> 16);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h01) : "h"(lo));
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h23) : "h"(hi));
+  const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
+  const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
+  o0 = pack_bf16x2(f01.x, f01.y);
+  o1 = pack_bf16x2(f23.x, f23.y);
+}
+
+// Reduce 16 values per lane across the 32 lanes of a warp.  On return every
+// lane holds the full reduction of value index (lane >> 1).
+template <bool kMax>
+__device__ __forceinline__ float warp_reduce16(float (&v)[16], int lane) {
+  auto op = [](float a, float b) { return kMax ? fmaxf(a, b) : a + b; };
+  {
+    const bool up = lane & 16;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float send = up ? v[j] : v[j + 8];
+      const float keep = up ? v[j + 8] : v[j];
+      v[j] = op(keep, __shfl_xor_sync(kFull, send, 16));
+    }
+  }
+  {
+    const bool up = lane & 8;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float send = up ? v[j] : v[j + 4];
+      const float keep = up ? v[j + 4] : v[j];
+      v[j] = op(keep, __shfl_xor_sync(kFull, send, 8));
+    }
+  }
+  {
+    const bool up = lane & 4;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const float send = up ? v[j] : v[j + 2];
+      const float keep = up ? v[j + 2] : v[j];
+      v[j] = op(keep, __shfl_xor_sync(kFull, send, 4));
+    }
+  }
+  {
+    const bool up = lane & 2;
+    const float send = up ? v[0] : v[1];
+    const float keep = up ? v[1] : v[0];
+    v[0] = op(keep, __shfl_xor_sync(kFull, send, 2));
+  }
+  v[0] = op(v[0], __shfl_xor_sync(kFull, v[0], 1));
+  return v[0];
+}
+
+template <int HG, bool kFp8>
+__global__ void __launch_bounds__(Cfg<HG, kFp8>::kThreads, 1) sparse_mla_attn_kernel(const __grid_constant__ Params p) {
+  using C = Cfg<HG, kFp8>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
+  int32_t* slots_ring = reinterpret_cast<int32_t*>(smem + C::kOffSlots);
+  uint8_t* valid = smem + C::kOffValid;
+  float* red_max = reinterpret_cast<float*>(smem + C::kOffRedMax);
+  float* red_sum = reinterpret_cast<float*>(smem + C::kOffRedSum);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+  const int64_t xbeg = tile_begin(blockIdx.x, p.total, p.G);
+  const int64_t xend = tile_begin(blockIdx.x + 1, p.total, p.G);
+  const int n_local = (int)(xend - xbeg);
+
+  if (tid == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars[C::kBarKvFull + i], C::kConvWarps);
+      mbar_init(&bars[C::kBarKvEmpty + i], 1);
+      mbar_init(&bars[C::kBarSFull + i], 1);
+      mbar_init(&bars[C::kBarPFull + i], 4);
+      mbar_init(&bars[C::kBarPvDone + i], 1);
+    }
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(&bars[C::kBarIdxFull + i], 32);
+      mbar_init(&bars[C::kBarIdxEmpty + i], C::kConvWarps);
+    }
+    mbar_init(&bars[C::kBarQFull], 32);
+    mbar_init(&bars[C::kBarQEmpty], 1);
+    mbar_init(&bars[C::kBarOFree], 4);
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == C::kMmaWarp) {
+    tmem_alloc(tmem_slot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+#define SMLA_WAIT(bar_idx, parity) mbar_wait(&bars[(bar_idx)], (parity), abort_flag, p.status, kDevWaitTimeout)
+
+  if (warp == C::kIndexWarp) {
+    // ------------------------------------------------------------ index warp
+    int seg = 0;
+    for (int tl = 0; tl < n_local; ++tl) {
+      const TileInfo ti = tile_info(p, xbeg + tl, xbeg, xend);
+      const int b4 = tl & 3;
+      if (tl >= 4 && !SMLA_WAIT(C::kBarIdxEmpty + b4, ((tl >> 2) + 1) & 1)) break;
+      int32_t* slots = slots_ring + b4 * C::kRows;
+      for (int r = lane; r < C::kRows; r += 32) {
+        const int k = ti.kt * C::kRows + r;
+        int32_t s = -1;
+        if (k < p.K) {
+          const int32_t idx = __ldg(p.indices + (int64_t)ti.t * p.K + k);
+          if constexpr (kFp8) {
+            s = translate_slot(idx, __ldg(p.req_id + ti.t), p.block_table, p.R, p.MB, p.NB);
+          } else {
+            s = (idx >= 0 && (int64_t)idx < p.NB) ? idx : -1;
+          }
+        }
+        slots[r] = s;
+      }
+      mbar_arrive(&bars[C::kBarIdxFull + b4]);
+      if (ti.seg_start) {
+        if (seg > 0 && !SMLA_WAIT(C::kBarQEmpty, (seg - 1) & 1)) break;
+        const __nv_bfloat16* qsrc = p.q + ((int64_t)ti.t * p.H + (int64_t)ti.hg * HG) * kDqk;
+        const uint32_t qbase = smem_u32(smem + C::kOffQ);
+        for (int i = lane; i < HG * 72; i += 32) {
+          const int h = i / 72, ch = i - h * 72;
+          const uint4 v = __ldg(reinterpret_cast<const uint4*>(qsrc + (int64_t)h * kDqk) + ch);
+          sts128(qbase + sw128_chunk(HG, h, ch), v);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(&bars[C::kBarQFull]);
+        ++seg;
+      }
+    }
+  } else if (warp >= C::kConvWarp0) {
+    // ------------------------------------------------------------ converters
+    const int cw = warp - C::kConvWarp0;
+    const int RW = (C::kRows - cw + C::kConvWarps - 1) / C::kConvWarps;  // rows of each tile handled here
+    const int n_items = n_local * RW;
+    struct Raw {
+      uint4 a, b, c;  // FP8: a = NoPE bytes, b = scales/RoPE (lanes 0..8); BF16: three 16-byte chunks
+      int32_t slot;
+    };
+    Raw buf[C::kDepth];
+    bool ok = true;
+
+    auto issue = [&](int m, Raw& rb) {
+      const int tl = m / RW, k = m - tl * RW;
+      const int r = cw + k * C::kConvWarps;
+      const int b4 = tl & 3;
+      if (k == 0) ok = ok && SMLA_WAIT(C::kBarIdxFull + b4, (tl >> 2) & 1);
+      if (!ok) return;
+      const int32_t slot = slots_ring[b4 * C::kRows + r];
+      if (k == RW - 1) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[C::kBarIdxEmpty + b4]);
+      }
+      rb.slot = slot;
+      if (slot >= 0) {
+        if constexpr (kFp8) {
+          const uint8_t* row = p.cache + (int64_t)slot * kRowBytes;
+          rb.a = ld_stream(row + 16 * lane);
+          if (lane < 9) rb.b = ld_stream(row + kNope + 16 * lane);
+        } else {
+          const uint8_t* row = reinterpret_cast<const uint8_t*>(p.kv + (int64_t)slot * kDqk);
+          rb.a = ld_stream(row + 16 * lane);
+          rb.b = ld_stream(row + 16 * (lane + 32));
+          if (lane < 8) rb.c = ld_stream(row + 16 * (lane + 64));
+        }
+      }
+    };
+
+    auto convert = [&](int m, Raw& rb) {
+      const int tl = m / RW, k = m - tl * RW;
+      const int r = cw + k * C::kConvWarps;
+      const int b = tl & 1;
+      if (k == 0 && tl >= 2) ok = ok && SMLA_WAIT(C::kBarKvEmpty + b, ((tl >> 1) + 1) & 1);
+      if (!ok) return;
+      const uint32_t tile = smem_u32(smem + C::kOffKv + b * C::kKvTile);
+      const bool v = rb.slot >= 0;
+      if constexpr (kFp8) {
+        uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
+        if (v) {
+          widen4(rb.a.x, lo.x, lo.y);
+          widen4(rb.a.y, lo.z, lo.w);
+          widen4(rb.a.z, hi.x, hi.y);
+          widen4(rb.a.w, hi.z, hi.w);
+        }
+        // NoPE columns 16*lane .. 16*lane+15 = chunks 2*lane, 2*lane+1.  Lanes
+        // 4..7 of every 8 store their odd chunk first so the 8 lanes of each
+        // store phase hit 8 distinct bank groups.
+        const uint32_t a0 = tile + sw128_chunk(C::kRows, r, 2 * lane);
+        const uint32_t a1 = tile + sw128_chunk(C::kRows, r, 2 * lane + 1);
+        if ((lane >> 2) & 1) {
+          sts128(a1, hi);
+          sts128(a0, lo);
+        } else {
+          sts128(a0, lo);
+          sts128(a1, hi);
+        }
+        const uint4 tail = v ? rb.b : make_uint4(0, 0, 0, 0);
+        if (lane >= 1 && lane <= 8) sts128(tile + sw128_chunk(C::kRows, r, 64 + lane - 1), tail);
+        if (lane == 0) sts128(smem_u32(smem + C::kOffScale + (b * C::kRows + r) * 16), tail);  // 4 scales
+      } else {
+        const uint4 z = make_uint4(0, 0, 0, 0);
+        sts128(tile + sw128_chunk(C::kRows, r, lane), v ? rb.a : z);
+        sts128(tile + sw128_chunk(C::kRows, r, lane + 32), v ? rb.b : z);
+        if (lane < 8) sts128(tile + sw128_chunk(C::kRows, r, lane + 64), v ? rb.c : z);
+      }
+      if (lane == 0) valid[b * C::kRows + r] = v ? 1 : 0;
+      if (k == RW - 1) {
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[C::kBarKvFull + b]);
+      }
+    };
+
+#pragma unroll
+    for (int j = 0; j < C::kDepth; ++j)
+      if (j < n_items) issue(j, buf[j]);
+    for (int base = 0; base < n_items && ok; base += C::kDepth) {
+#pragma unroll
+      for (int j = 0; j < C::kDepth; ++j) {
+        const int m = base + j;
+        if (m < n_items) {
+          convert(m, buf[j]);
+          if (m + C::kDepth < n_items) issue(m + C::kDepth, buf[j]);
+        }
+      }
+    }
+  } else if (warp == C::kMmaWarp) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0 && n_local > 0) {
+      int seg_q = 0, seg_o = 0;
+      constexpr uint32_t idesc_qk = make_idesc_bf16(64, HG, 0, 0);
+      constexpr uint32_t idesc_pv = make_idesc_bf16(128, HG, 1, 1);
+      constexpr uint32_t pkb = HG * 16;  // bytes per 8-row block of P^T
+      const uint32_t kv_base = smem_u32(smem + C::kOffKv);
+      const uint32_t q_base = smem_u32(smem + C::kOffQ);
+      const uint32_t p_base = smem_u32(smem + C::kOffP);
+
+      auto issue_qk = [&](int tl) -> bool {
+        const TileInfo ti = tile_info(p, xbeg + tl, xbeg, xend);
+        const int b = tl & 1;
+        if (ti.seg_start) {
+          if (!SMLA_WAIT(C::kBarQFull, seg_q & 1)) return false;
+          ++seg_q;
+        }
+        if (!SMLA_WAIT(C::kBarKvFull + b, (tl >> 1) & 1)) return false;
+        tc_fence_after();
+        const uint32_t kv = kv_base + b * C::kKvTile;
+        const uint32_t sbuf = tmem + C::kSCol + b * C::kNS * HG;
+#pragma unroll
+        for (int s = 0; s < 36; ++s) {
+          const uint32_t off = (s & 3) * 32;
+          const uint64_t da = make_sdesc(kv + (s >> 2) * C::kPanel + off, 16, 1024, kLayoutSw128);
+          const uint64_t db = make_sdesc(q_base + (s >> 2) * C::kQPanel + off, 16, 1024, kLayoutSw128);
+          // FP8: NoPE scale group g = s / 8 (columns 128g..128g+127) and the RoPE
+          // columns each get their own accumulator; BF16: one accumulator.
+          const int g = kFp8 ? (s < 32 ? (s >> 3) : 4) : 0;
+          const bool first = kFp8 ? (s < 32 ? (s & 7) == 0 : s == 32) : s == 0;
+          mma_ss(sbuf + g * HG, da, db, idesc_qk, first ? 0u : 1u);
+        }
+        mma_commit(&bars[C::kBarSFull + b]);
+        if (ti.seg_end) mma_commit(&bars[C::kBarQEmpty]);
+        return true;
+      };
+      auto issue_pv = [&](int tl) -> bool {
+        const TileInfo ti = tile_info(p, xbeg + tl, xbeg, xend);
+        const int b = tl & 1;
+        if (!SMLA_WAIT(C::kBarPFull + b, (tl >> 1) & 1)) return false;
+        if (ti.seg_start) {
+          if (seg_o > 0 && !SMLA_WAIT(C::kBarOFree, (seg_o - 1) & 1)) return false;
+          ++seg_o;
+        }
+        tc_fence_after();
+        const uint32_t kv = kv_base + b * C::kKvTile;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t pb = p_base + (b * C::kNP + (kFp8 ? q : 0)) * C::kPBytes;
+#pragma unroll
+          for (int s = 0; s < 4; ++s) {
+            const uint64_t da = make_sdesc(kv + 2 * q * C::kPanel + s * 2048, C::kPanel, 1024, kLayoutSw128);
+            const uint64_t db = make_sdesc(pb + 2 * s * pkb, pkb, 128, kLayoutNone);
+            mma_ss(tmem + C::kOCol + q * HG, da, db, idesc_pv, (ti.seg_start && s == 0) ? 0u : 1u);
+          }
+        }
+        mma_commit(&bars[C::kBarKvEmpty + b]);
+        mma_commit(&bars[C::kBarPvDone + b]);
+        return true;
+      };
+      bool ok = issue_qk(0);
+      for (int tl = 1; ok && tl < n_local; ++tl) ok = issue_pv(tl - 1) && issue_qk(tl);
+      if (ok) issue_pv(n_local - 1);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax warpgroup (warps 0..3)
+    const int w = warp;
+    const int r = 16 * w + lane;  // tile row held in this thread's TMEM lane (lanes 0..15 only)
+    const uint32_t lane_base = (uint32_t)(32 * w) << 16;
+    const uint32_t p_base = smem_u32(smem + C::kOffP);
+    constexpr int NB16 = HG / 16;
+    float m_used[HG], l_part[HG];
+    int seg_first_kt = 0, n_seg_tiles = 0;
+    bool dead = false;
+    for (int tl = 0; tl < n_local; ++tl) {
+      const TileInfo ti = tile_info(p, xbeg + tl, xbeg, xend);
+      const int b = tl & 1;
+      if (ti.seg_start) {
+#pragma unroll
+        for (int h = 0; h < HG; ++h) {
+          m_used[h] = -INFINITY;
+          l_part[h] = 0.f;
+        }
+        seg_first_kt = ti.kt;
+        n_seg_tiles = 0;
+      }
+      if (!dead) dead = !SMLA_WAIT(C::kBarSFull + b, (tl >> 1) & 1);
+      if (!dead) dead = !SMLA_WAIT(C::kBarKvFull + b, (tl >> 1) & 1);  // orders the row-valid flags
+      tc_fence_after();
+      const bool row_ok = !dead && lane < 16 && valid[b * C::kRows + r] != 0;
+      const uint32_t s_addr = tmem + lane_base + C::kSCol + b * C::kNS * HG;
+      float scs[4] = {0.f, 0.f, 0.f, 0.f};
+      if constexpr (kFp8) {
+        if (row_ok) {
+          const float4 v4 = *reinterpret_cast<const float4*>(smem + C::kOffScale + (b * C::kRows + r) * 16);
+          scs[0] = v4.x;
+          scs[1] = v4.y;
+          scs[2] = v4.z;
+          scs[3] = v4.w;
+        }
+      }
+      // scaled logits (log2 units) of head block hb: sum_g scale_g * S_g + S_rope
+      auto logits = [&](int hb, float (&sv)[16]) {
+        uint32_t raw[16];
+        if constexpr (kFp8) {
+          tmem_ld16_sync(s_addr + 4 * HG + hb * 16, raw);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) sv[j] = __uint_as_float(raw[j]);
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            tmem_ld16_sync(s_addr + g * HG + hb * 16, raw);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) sv[j] = fmaf(scs[g], __uint_as_float(raw[j]), sv[j]);
+          }
+        } else {
+          tmem_ld16_sync(s_addr + hb * 16, raw);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) sv[j] = __uint_as_float(raw[j]);
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) sv[j] = row_ok ? sv[j] * p.scale_log2 : -INFINITY;
+      };
+      // pass 1: per-head maximum of this tile
+      float* redm = red_max + (tl & 1) * 4 * HG;
+#pragma unroll
+      for (int hb = 0; hb < NB16; ++hb) {
+        float v[16];
+        if (!dead) {
+          logits(hb, v);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] = -INFINITY;
+        }
+        const float mx = warp_reduce16<true>(v, lane);
+        if ((lane & 1) == 0) redm[w * HG + hb * 16 + (lane >> 1)] = mx;
+      }
+      named_bar_sync(1, 128);
+      bool any_rescale = false;
+      float alpha[HG];
+#pragma unroll
+      for (int h = 0; h < HG; ++h) {
+        const float tmax = fmaxf(fmaxf(redm[h], redm[HG + h]), fmaxf(redm[2 * HG + h], redm[3 * HG + h]));
+        const float nm = fmaxf(m_used[h], tmax);
+        alpha[h] = 1.f;
+        if (nm > m_used[h] + 8.0f) {
+          alpha[h] = exp2f(m_used[h] - nm);
+          m_used[h] = nm;
+          any_rescale = true;
+        }
+        l_part[h] *= alpha[h];
+      }
+      if (any_rescale && n_seg_tiles > 0 && !dead) {
+        // O^T holds the P.V of this segment's earlier tiles: wait for the latest, rescale in place.
+        dead = !SMLA_WAIT(C::kBarPvDone + ((tl - 1) & 1), ((tl - 1) >> 1) & 1);
+        if (!dead) {
+          tc_fence_after();
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+#pragma unroll
+            for (int hb = 0; hb < NB16; ++hb) {
+              uint32_t o[16];
+              const uint32_t addr = tmem + lane_base + C::kOCol + q * HG + hb * 16;
+              tmem_ld16_sync(addr, o);
+#pragma unroll
+              for (int j = 0; j < 16; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * alpha[hb * 16 + j]);
+              tmem_st16(addr, o);
+            }
+          }
+          tmem_st_wait();
+        }
+      }
+      // pass 2: probabilities, running sums, P_q^T rows (p times the value
+      // chunk's scale for FP8; p itself for BF16)
+      if (tl >= 2 && !dead) dead = !SMLA_WAIT(C::kBarPvDone + b, ((tl >> 1) + 1) & 1);  // P buffers free
+#pragma unroll
+      for (int hb = 0; hb < NB16; ++hb) {
+        float pr[16];
+        if (!dead) {
+          logits(hb, pr);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) pr[j] = -INFINITY;
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          pr[j] = row_ok ? exp2f(pr[j] - m_used[hb * 16 + j]) : 0.f;
+          l_part[hb * 16 + j] += pr[j];
+        }
+        if (!dead && lane < 16) {
+#pragma unroll
+          for (int q = 0; q < C::kNP; ++q) {
+            const float sq = kFp8 ? scs[q] : 1.f;
+            const uint32_t pbuf = p_base + (b * C::kNP + q) * C::kPBytes;
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const uint4 v = make_uint4(pack_bf16x2(pr[8 * e + 0] * sq, pr[8 * e + 1] * sq),
+                                         pack_bf16x2(pr[8 * e + 2] * sq, pr[8 * e + 3] * sq),
+                                         pack_bf16x2(pr[8 * e + 4] * sq, pr[8 * e + 5] * sq),
+                                         pack_bf16x2(pr[8 * e + 6] * sq, pr[8 * e + 7] * sq));
+              sts128(pbuf + pt_offset<HG>(r, hb * 16 + 8 * e), v);
+            }
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0 && !dead) mbar_arrive(&bars[C::kBarPFull + b]);
+      ++n_seg_tiles;
+
+      if (ti.seg_end) {
+        // final sums across the 64 rows
+#pragma unroll
+        for (int hb = 0; hb < NB16; ++hb) {
+          float v[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) v[j] = l_part[hb * 16 + j];
+          const float sm = warp_reduce16<false>(v, lane);
+          if ((lane & 1) == 0) red_sum[w * HG + hb * 16 + (lane >> 1)] = sm;
+        }
+        named_bar_sync(1, 128);
+        if (!dead) dead = !SMLA_WAIT(C::kBarPvDone + b, (tl >> 1) & 1);  // all P.V of the segment done
+        tc_fence_after();
+        const bool full = (seg_first_kt == 0) && (ti.kt == p.nt - 1);
+        const int64_t slot = (int64_t)blockIdx.x + ti.u;  // partial-result slot of this segment
+        float inv[HG];
+#pragma unroll
+        for (int h = 0; h < HG; ++h) {
+          const float lt = red_sum[h] + red_sum[HG + h] + red_sum[2 * HG + h] + red_sum[3 * HG + h];
+          inv[h] = lt > 0.f ? 1.f / lt : 0.f;
+          if (tid == h) {
+            const float lse2 = lt > 0.f ? (m_used[h] + log2f(lt)) : -INFINITY;
+            const float lse_v = lse2 * 0.69314718055994530942f;
+            if (full) {
+              p.lse[(int64_t)ti.t * p.H + ti.hg * HG + h] = lse_v;
+            } else {
+              p.part_lse[slot * HG + h] = lse_v;
+            }
+          }
+        }
+        if (!dead) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int c = 128 * q + 32 * w + lane;
+#pragma unroll
+            for (int hb = 0; hb < NB16; ++hb) {
+              uint32_t o[16];
+              tmem_ld16_sync(tmem + lane_base + C::kOCol + q * HG + hb * 16, o);
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const int h = hb * 16 + j;
+                const float val = __uint_as_float(o[j]) * inv[h];
+                if (full) {
+                  p.out[((int64_t)ti.t * p.H + ti.hg * HG + h) * kDv + c] = __float2bfloat16_rn(val);
+                } else {
+                  p.part_o[(slot * HG + h) * kDv + c] = val;
+                }
+              }
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0 && !dead) mbar_arrive(&bars[C::kBarOFree]);
+      }
+    }
+  }
+#undef SMLA_WAIT
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == C::kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+// LSE-weighted merge of the partial results of units split across CTAs.
+template <int HG>
+__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ part_o,
+                                                      const float* __restrict__ part_lse,
+                                                      __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
+                                                      int H, int n_hg, int nt, int64_t total, int G) {
+  const int64_t u = blockIdx.x;
+  auto owner = [&](int64_t x) -> int64_t {
+    int64_t c = ((x + 1) * G - 1) / total;
+    if (c >= G) c = G - 1;
+    while (c + 1 < G && tile_begin(c + 1, total, G) <= x) ++c;
+    while (c > 0 && tile_begin(c, total, G) > x) --c;
+    return c;
+  };
+  const int64_t c_lo = owner(u * nt), c_hi = owner(u * nt + nt - 1);
+  if (c_lo == c_hi) return;  // finished inside one CTA, already written
+  const int t = (int)(u / n_hg), hg = (int)(u % n_hg);
+  __shared__ float s_m[HG], s_w_sum[HG];
+  if (threadIdx.x < HG) {
+    const int h = threadIdx.x;
+    float m = -INFINITY;
+    for (int64_t c = c_lo; c <= c_hi; ++c) m = fmaxf(m, part_lse[(c + u) * HG + h]);
+    float wsum = 0.f;
+    if (m != -INFINITY)
+      for (int64_t c = c_lo; c <= c_hi; ++c) wsum += expf(part_lse[(c + u) * HG + h] - m);
+    s_m[h] = m;
+    s_w_sum[h] = wsum;
+    lse[(int64_t)t * H + hg * HG + h] = (m == -INFINITY) ? -INFINITY : m + logf(wsum);
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < HG * (kDv / 4); i += blockDim.x) {
+    const int h = i / (kDv / 4), c4 = i - h * (kDv / 4);
+    const float m = s_m[h];
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (m != -INFINITY) {
+      const float inv = 1.f / s_w_sum[h];
+      for (int64_t c = c_lo; c <= c_hi; ++c) {
+        const float wgt = expf(part_lse[(c + u) * HG + h] - m) * inv;
+        const float4 v = reinterpret_cast<const float4*>(part_o + ((c + u) * HG + h) * kDv)[c4];
+        acc.x += wgt * v.x;
+        acc.y += wgt * v.y;
+        acc.z += wgt * v.z;
+        acc.w += wgt * v.w;
+      }
+    }
+    __nv_bfloat16* o = out + ((int64_t)t * H + hg * HG + h) * kDv + 4 * c4;
+    reinterpret_cast<__nv_bfloat162*>(o)[0] = __floats2bfloat162_rn(acc.x, acc.y);
+    reinterpret_cast<__nv_bfloat162*>(o)[1] = __floats2bfloat162_rn(acc.z, acc.w);
+  }
+}
+
+template <int HG, bool kFp8>
+cudaError_t launch_impl(const AttnArgs& a, const AttnPlan& plan, cudaStream_t stream) {
+  using C = Cfg<HG, kFp8>;
+  static bool attr_set = false;  // per instantiation; set once per process
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(sparse_mla_attn_kernel<HG, kFp8>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemAlloc);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  uint8_t* ws = static_cast<uint8_t*>(a.workspace);
+  const int64_t n_slots = (int64_t)plan.G + plan.units - 1;
+  Params p;
+  p.q = static_cast<const __nv_bfloat16*>(a.q);
+  p.cache = a.cache;
+  p.kv = static_cast<const __nv_bfloat16*>(a.kv);
+  p.indices = a.indices;
+  p.block_table = a.block_table;
+  p.req_id = a.req_id;
+  p.out = static_cast<__nv_bfloat16*>(a.out);
+  p.lse = a.lse;
+  p.status = reinterpret_cast<int*>(ws);
+  p.part_lse = reinterpret_cast<float*>(ws + kWsStatusBytes);
+  p.part_o = reinterpret_cast<float*>(ws + kWsStatusBytes + ((n_slots * HG * 4 + 255) / 256) * 256);
+  p.scale_log2 = a.sm_scale * 1.4426950408889634f;
+  p.T = a.T;
+  p.H = a.H;
+  p.K = a.K;
+  p.R = a.R;
+  p.MB = a.MB;
+  p.NB = a.NB;
+  p.n_hg = plan.n_hg;
+  p.nt = plan.nt;
+  p.total = plan.total;
+  p.G = plan.G;
+  sparse_mla_attn_kernel<HG, kFp8><<<plan.G, C::kThreads, C::kSmemAlloc, stream>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || !plan.need_combine) return e;
+  combine_kernel<HG><<<(unsigned)plan.units, 256, 0, stream>>>(p.part_o, p.part_lse, p.out, p.lse, p.H, p.n_hg, p.nt,
+                                                               p.total, p.G);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+AttnPlan plan_attention(int T, int H, int K, int num_splits, int num_sms) {
+  AttnPlan pl;
+  pl.HG = (H % 32 == 0) ? 32 : 16;
+  pl.n_hg = H / pl.HG;
+  pl.nt = K > 0 ? (K + 63) / 64 : 1;
+  pl.units = (int64_t)T * pl.n_hg;
+  pl.total = pl.units * pl.nt;
+  int64_t G = num_splits > 0 ? pl.units * (int64_t)num_splits : (int64_t)num_sms;
+  if (G > pl.total) G = pl.total;
+  if (G < 1) G = 1;
+  pl.G = (int)G;
+  pl.need_combine = !(pl.total % pl.G == 0 && (pl.total / pl.G) % pl.nt == 0);
+  const int64_t n_slots = (int64_t)pl.G + pl.units - 1;
+  const size_t lse_bytes = (size_t)(((n_slots * pl.HG * 4) + 255) / 256) * 256;
+  pl.ws_bytes = kWsStatusBytes + lse_bytes + (size_t)n_slots * pl.HG * kDv * 4;
+  return pl;
+}
+
+cudaError_t launch_attention(bool fp8, const AttnArgs& a, const AttnPlan& plan, cudaStream_t stream) {
+  if (plan.HG == 16) return fp8 ? launch_impl<16, true>(a, plan, stream) : launch_impl<16, false>(a, plan, stream);
+  return fp8 ? launch_impl<32, true>(a, plan, stream) : launch_impl<32, false>(a, plan, stream);
+}
+
+}  // namespace smla

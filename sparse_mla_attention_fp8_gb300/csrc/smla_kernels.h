@@ -1,0 +1,51 @@
+// Internal launch interface between the C-ABI layer and the CUDA kernels.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace smla {
+
+cudaError_t launch_quantize_store(const void* kv_new, const int64_t* slot_mapping, uint8_t* cache, int T, int64_t NB,
+                                  cudaStream_t stream);
+
+cudaError_t launch_translate(const int32_t* indices, const int32_t* block_table, const int32_t* req_id,
+                             int32_t* slots, int T, int K, int R, int MB, int64_t NB, cudaStream_t stream);
+
+// Work decomposition of one sparse-attention call: units are (token, head
+// group) pairs, each split into nt tiles of 64 top-k rows; G persistent CTAs
+// take contiguous, balanced ranges of the unit-major tile sequence.
+struct AttnPlan {
+  int HG;             // heads per CTA (16 or 32)
+  int n_hg;           // head groups per token
+  int nt;             // tiles per unit
+  int64_t units;      // T * n_hg
+  int64_t total;      // units * nt
+  int G;              // CTAs
+  bool need_combine;  // some unit spans more than one CTA
+  size_t ws_bytes;    // workspace bytes (status word + partial results)
+};
+
+AttnPlan plan_attention(int T, int H, int K, int num_splits, int num_sms);
+
+struct AttnArgs {
+  const void* q;
+  const uint8_t* cache;      // FP8 decode: [NB, 64, 656]
+  const void* kv;            // BF16 prefill: [N, 576]
+  const int32_t* indices;    // [T, K]
+  const int32_t* block_table;
+  const int32_t* req_id;
+  void* out;                 // bf16 [T, H, 512]
+  float* lse;                // [T, H]
+  void* workspace;
+  float sm_scale;
+  int T, H, K, R, MB;
+  int64_t NB;                // physical blocks (FP8) or kv rows (BF16)
+};
+
+cudaError_t launch_attention(bool fp8, const AttnArgs& a, const AttnPlan& plan, cudaStream_t stream);
+
+// Offsets inside the workspace.
+constexpr size_t kWsStatusBytes = 256;
+
+}  // namespace smla

@@ -1,0 +1,124 @@
+"""GPU parity: FP8 sparse decode against the float64 oracle on the same
+stored bytes (atol 1e-2 + rtol 2e-2 on the output, 1e-3 on the LSE)."""
+import numpy as np
+import pytest
+
+import oracle
+import smla_inputs as inp
+from helpers import (assert_lse_close, assert_out_close, bf16_dev, check_decode, dev, oracle_cache,
+                     run_gpu_decode)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def smla():
+    import sparse_mla_attention_fp8_gb300 as m
+    m.build()
+    return m
+
+
+def test_tiny_decode_h16_k64():
+    check_decode(inp.tiny_decode(0))
+
+
+@pytest.mark.parametrize("num_splits", [0, 1, 2, 3, 5])
+def test_ragged_topk_several_tiles(num_splits):
+    # K = 200: three full tiles of 64 rows and a ragged tail of 8
+    case = inp.memory_bound_decode(seed=5, R=9, ctx_lo=300, ctx_hi=2500, K=200)
+    check_decode(case, num_splits=num_splits)
+
+
+@pytest.mark.parametrize("H", [32, 48, 64, 128])
+def test_head_counts(H):
+    case = inp.memory_bound_decode(seed=6, R=5, ctx_lo=200, ctx_hi=900, K=150, H=H)
+    check_decode(case)
+    check_decode(case, num_splits=1)
+
+
+@pytest.mark.parametrize("K", [1, 37, 64, 65, 2048])
+def test_topk_widths(K):
+    case = inp.memory_bound_decode(seed=7, R=6, ctx_lo=2100, ctx_hi=4000, K=K)
+    check_decode(case)
+
+
+def test_all_indices_invalid_gives_zero_and_minus_inf():
+    case = inp.memory_bound_decode(seed=8, R=4, ctx_lo=200, ctx_hi=400, K=130)
+    case.indices[:] = -1
+    out, lse = run_gpu_decode(case, oracle_cache(case))
+    assert np.all(out == 0) and np.all(np.isneginf(lse))
+    case.indices[1, 77] = 5  # one token with a single valid row
+    check_decode(case)
+    check_decode(case, num_splits=2)
+
+
+def test_single_valid_index_returns_its_row():
+    case = inp.memory_bound_decode(seed=9, R=6, ctx_lo=300, ctx_hi=500, K=96)
+    rng = np.random.default_rng(0)
+    keep = rng.integers(0, 96, size=6)
+    for t in range(6):
+        v = case.indices[t, keep[t]]
+        case.indices[t, :] = -1
+        case.indices[t, keep[t]] = v
+    check_decode(case)
+
+
+def test_duplicated_and_out_of_range_indices():
+    case = inp.memory_bound_decode(seed=10, R=5, ctx_lo=700, ctx_hi=900, K=180)
+    case.indices[:, 100:140] = case.indices[:, 0:40]          # duplicates count once per occurrence
+    case.indices[0, 5] = case.block_table.shape[1] * 64 + 3    # block id >= MB
+    case.indices[1, 7] = -77
+    case.block_table[2, 3] = case.num_blocks + 9               # physical block >= NB
+    case.block_table[3, 1] = -4                                # negative physical block
+    check_decode(case)
+
+
+def test_speculative_two_token_requests():
+    case = inp.mixed_batch(11, n_decode=6, n_prefill=0, ctx_lo=500, ctx_hi=3000, K=256)
+    check_decode(case)
+
+
+def test_mixed_batch_store_then_decode():
+    import torch
+    import sparse_mla_attention_fp8_gb300 as smla
+    case = inp.mixed_batch(12, n_decode=5, n_prefill=2, prefill_tokens=200, ctx_lo=400, ctx_hi=1500, K=128)
+    ref_cache = oracle_cache(case, with_new=True)
+    cache = torch.from_numpy(oracle_cache(case, with_new=False)).cuda()
+    smla.mla_cache_store_fp8(bf16_dev(case.new_rows), dev(case.new_slots), cache)
+    assert np.array_equal(cache.cpu().numpy(), ref_cache)
+    out, lse = smla.sparse_mla_decode_fp8(bf16_dev(case.q), cache, dev(case.indices), dev(case.block_table),
+                                          dev(case.req_id_per_token), case.sm_scale)
+    ref_out, ref_lse = oracle.sparse_mla_decode(case.q, ref_cache, case.indices, case.block_table,
+                                                case.req_id_per_token, case.sm_scale)
+    assert_out_close(out.float().cpu().numpy(), ref_out, case.name)
+    assert_lse_close(lse.cpu().numpy(), ref_lse, case.name)
+
+
+def test_explicit_workspace_and_too_small_workspace():
+    import torch
+    import sparse_mla_attention_fp8_gb300 as smla
+    case = inp.memory_bound_decode(seed=13, R=4, ctx_lo=300, ctx_hi=600, K=128)
+    cache = oracle_cache(case)
+    need = smla.decode_workspace_bytes(case.T, case.H, case.K, 0)
+    assert need > 0
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    out, lse = run_gpu_decode(case, cache, workspace=ws)
+    ref_out, ref_lse = oracle.sparse_mla_decode(case.q, cache, case.indices, case.block_table,
+                                                case.req_id_per_token, case.sm_scale)
+    assert_out_close(out, ref_out)
+    assert_lse_close(lse, ref_lse)
+    small = torch.zeros(need - 256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(smla.SmlaError, match="status -4"):
+        smla.sparse_mla_decode_fp8(bf16_dev(case.q), dev(cache), dev(case.indices), dev(case.block_table),
+                                   dev(case.req_id_per_token), case.sm_scale, workspace=small)
+
+
+def test_repeated_calls_are_deterministic():
+    import sparse_mla_attention_fp8_gb300 as smla
+    case = inp.memory_bound_decode(seed=14, R=8, ctx_lo=1000, ctx_hi=3000, K=512)
+    cache = dev(oracle_cache(case))
+    args = (bf16_dev(case.q), cache, dev(case.indices), dev(case.block_table), dev(case.req_id_per_token),
+            case.sm_scale)
+    o1, l1 = smla.sparse_mla_decode_fp8(*args)
+    o2, l2 = smla.sparse_mla_decode_fp8(*args)
+    assert (o1 == o2).all() and (l1 == l2).all()

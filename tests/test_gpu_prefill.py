@@ -1,0 +1,53 @@
+"""GPU parity: BF16 sparse prefill against the float64 oracle."""
+import numpy as np
+import pytest
+
+import oracle
+import smla_inputs as inp
+from helpers import assert_lse_close, assert_out_close, bf16_dev, dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def smla():
+    import sparse_mla_attention_fp8_gb300 as m
+    m.build()
+    return m
+
+
+def run_prefill(case, num_splits=0, tokens=None):
+    import torch
+    import sparse_mla_attention_fp8_gb300 as smla
+    out, lse = smla.sparse_mla_prefill_bf16(bf16_dev(case.q), bf16_dev(case.kv), dev(case.indices), case.sm_scale,
+                                            num_splits=num_splits)
+    torch.cuda.synchronize()
+    assert smla.read_device_status() == 0
+    ref_out, ref_lse = oracle.sparse_mla_prefill(case.q, case.kv, case.indices, case.sm_scale, tokens=tokens)
+    sel = slice(None) if tokens is None else tokens
+    assert_out_close(out.float().cpu().numpy()[sel], ref_out, case.name)
+    assert_lse_close(lse.cpu().numpy()[sel], ref_lse, case.name)
+
+
+@pytest.mark.parametrize("H", [16, 64, 128])
+def test_prefill_causal_padding(H):
+    # 40 cached + 30 new tokens per request, K = 100: early tokens see fewer than
+    # K positions, so their index rows end in -1 padding
+    case = inp.prefill(seed=3, R=3, cached=40, new=30, K=100, H=H)
+    assert (case.indices < 0).any()
+    run_prefill(case)
+
+
+@pytest.mark.parametrize("num_splits", [0, 1, 2])
+def test_prefill_splits(num_splits):
+    case = inp.prefill(seed=4, R=2, cached=300, new=20, K=256, H=32)
+    run_prefill(case, num_splits=num_splits)
+
+
+def test_prefill_out_of_range_rows_are_masked():
+    case = inp.prefill(seed=5, R=2, cached=100, new=10, K=64, H=16)
+    N = case.kv.shape[0]
+    case.indices[0, 3] = N
+    case.indices[1, 9] = N + 1000
+    case.indices[2, :] = -1
+    run_prefill(case)
