@@ -49,6 +49,28 @@ namespace {
 
 constexpr uint32_t kFull = 0xffffffffu;
 
+// Optional per-tile timeline for performance work: with SMLA_TRACE defined,
+// each role records %globaltimer at its hand-off points into g_smla_trace
+// (set by the host through smla_trace_set).  Compiled out otherwise.
+#ifdef SMLA_TRACE
+__device__ unsigned long long* g_smla_trace = nullptr;
+constexpr int kTraceTiles = 64, kTraceEvents = 8;
+enum { kEvIdx = 0, kEvConvStart = 1, kEvConvDone = 2, kEvQk = 3, kEvSoftStart = 4, kEvSoftDone = 5, kEvPv = 6,
+       kEvQLoaded = 7 };
+#define SMLA_TRACE_EV(tl, ev, op)                                                                       \
+  do {                                                                                                  \
+    if (g_smla_trace && (tl) < kTraceTiles) {                                                          \
+      unsigned long long* _p = g_smla_trace + ((size_t)blockIdx.x * kTraceTiles + (tl)) * kTraceEvents + (ev); \
+      op(_p, (unsigned long long)globaltimer_ns());                                                    \
+    }                                                                                                   \
+  } while (0)
+#define SMLA_TRACE_SET(tl, ev) SMLA_TRACE_EV(tl, ev, [](unsigned long long* a, unsigned long long v) { *a = v; })
+#define SMLA_TRACE_MAX(tl, ev) SMLA_TRACE_EV(tl, ev, atomicMax)
+#else
+#define SMLA_TRACE_SET(tl, ev) ((void)0)
+#define SMLA_TRACE_MAX(tl, ev) ((void)0)
+#endif
+
 template <int HG, bool kFp8>
 struct Cfg {
   static constexpr int kRows = 64;                       // top-k rows per tile
@@ -56,6 +78,7 @@ struct Cfg {
   static constexpr int kKvTile = 9 * kPanel;             // 576 columns
   static constexpr int kQPanel = HG * 128;
   static constexpr int kQBytes = 9 * kQPanel;
+  static constexpr int kQBufs = HG == 16 ? 2 : 1;       // Q blocks in flight (next unit prefetched)
   static constexpr int kPBytes = kRows * HG * 2;
   static constexpr int kMmaWarp = 4;
   static constexpr int kIndexWarp = 5;
@@ -72,7 +95,7 @@ struct Cfg {
   // shared memory layout, offsets from a 1024-byte aligned base
   static constexpr int kOffKv = 0;
   static constexpr int kOffQ = kOffKv + 2 * kKvTile;
-  static constexpr int kOffP = kOffQ + kQBytes;
+  static constexpr int kOffP = kOffQ + kQBufs * kQBytes;
   static constexpr int kOffScale = kOffP + 2 * kNP * kPBytes;  // float [2][64][4] row scales
   static constexpr int kOffSlots = kOffScale + 2 * kRows * 16;  // int32 [4][64]
   static constexpr int kOffValid = kOffSlots + 4 * kRows * 4;  // uint8 [2][64]
@@ -81,8 +104,8 @@ struct Cfg {
   static constexpr int kOffBar = kOffRedSum + 4 * HG * 4;
   // barriers
   static constexpr int kBarKvFull = 0, kBarKvEmpty = 2, kBarSFull = 4, kBarPFull = 6, kBarPvDone = 8,
-                       kBarIdxFull = 10, kBarIdxEmpty = 14, kBarQFull = 18, kBarQEmpty = 19, kBarOFree = 20;
-  static constexpr int kNumBars = 21;
+                       kBarIdxFull = 10, kBarIdxEmpty = 14, kBarQFull = 18, kBarQEmpty = 20, kBarOFree = 22;
+  static constexpr int kNumBars = 23;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort flag
   static constexpr int kSmemBytes = kOffMisc + 16;
   static constexpr int kSmemAlloc = kSmemBytes + 1024;
@@ -234,8 +257,10 @@ __global__ void __launch_bounds__(Cfg<HG, kFp8>::kThreads, 1) sparse_mla_attn_ke
       mbar_init(&bars[C::kBarIdxFull + i], 32);
       mbar_init(&bars[C::kBarIdxEmpty + i], C::kConvWarps);
     }
-    mbar_init(&bars[C::kBarQFull], 32);
-    mbar_init(&bars[C::kBarQEmpty], 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars[C::kBarQFull + i], 32);
+      mbar_init(&bars[C::kBarQEmpty + i], 1);
+    }
     mbar_init(&bars[C::kBarOFree], 4);
     *abort_flag = 0;
     mbar_fence_init();
@@ -273,17 +298,21 @@ __global__ void __launch_bounds__(Cfg<HG, kFp8>::kThreads, 1) sparse_mla_attn_ke
         slots[r] = s;
       }
       mbar_arrive(&bars[C::kBarIdxFull + b4]);
+      if (lane == 0) SMLA_TRACE_SET(tl, kEvIdx);
       if (ti.seg_start) {
-        if (seg > 0 && !SMLA_WAIT(C::kBarQEmpty, (seg - 1) & 1)) break;
+        const int qb = seg % C::kQBufs;
+        if (seg >= C::kQBufs && !SMLA_WAIT(C::kBarQEmpty + qb, ((seg / C::kQBufs) - 1) & 1)) break;
         const __nv_bfloat16* qsrc = p.q + ((int64_t)ti.t * p.H + (int64_t)ti.hg * HG) * kDqk;
-        const uint32_t qbase = smem_u32(smem + C::kOffQ);
+        const uint32_t qbase = smem_u32(smem + C::kOffQ + qb * C::kQBytes);
+        // all 16-byte chunks in flight at once (asynchronous copies), then one wait
         for (int i = lane; i < HG * 72; i += 32) {
           const int h = i / 72, ch = i - h * 72;
-          const uint4 v = __ldg(reinterpret_cast<const uint4*>(qsrc + (int64_t)h * kDqk) + ch);
-          sts128(qbase + sw128_chunk(HG, h, ch), v);
+          cp_async16(qbase + sw128_chunk(HG, h, ch), qsrc + (int64_t)h * kDqk + ch * 8);
         }
+        cp_async_wait_all();
         fence_proxy_async_smem();
-        mbar_arrive(&bars[C::kBarQFull]);
+        mbar_arrive(&bars[C::kBarQFull + qb]);
+        if (lane == 0) SMLA_TRACE_SET(tl, kEvQLoaded);
         ++seg;
       }
     }
@@ -330,6 +359,7 @@ __global__ void __launch_bounds__(Cfg<HG, kFp8>::kThreads, 1) sparse_mla_attn_ke
       const int r = cw + k * C::kConvWarps;
       const int b = tl & 1;
       if (k == 0 && tl >= 2) ok = ok && SMLA_WAIT(C::kBarKvEmpty + b, ((tl >> 1) + 1) & 1);
+      if (k == 0 && lane == 0 && cw == 0) SMLA_TRACE_SET(tl, kEvConvStart);
       if (!ok) return;
       const uint32_t tile = smem_u32(smem + C::kOffKv + b * C::kKvTile);
       const bool v = rb.slot >= 0;
@@ -367,6 +397,7 @@ __global__ void __launch_bounds__(Cfg<HG, kFp8>::kThreads, 1) sparse_mla_attn_ke
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[C::kBarKvFull + b]);
+        if (lane == 0) SMLA_TRACE_MAX(tl, kEvConvDone);
       }
     };
 
@@ -385,68 +416,97 @@ __global__ void __launch_bounds__(Cfg<HG, kFp8>::kThreads, 1) sparse_mla_attn_ke
     }
   } else if (warp == C::kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
+    // One thread issues every tensor-core op.  It polls (never blocks on) the
+    // two inputs it can consume: the next converted tile for QK^T (which may
+    // run up to two tiles ahead of P.V, one per S buffer) and the next P
+    // operand for P.V, and issues whichever is ready first.
     if (lane == 0 && n_local > 0) {
-      int seg_q = 0, seg_o = 0;
+      int seg_q = 0, seg_o = 0;  // segments whose first QK^T / first P.V was issued
       constexpr uint32_t idesc_qk = make_idesc_bf16(64, HG, 0, 0);
       constexpr uint32_t idesc_pv = make_idesc_bf16(128, HG, 1, 1);
       constexpr uint32_t pkb = HG * 16;  // bytes per 8-row block of P^T
       const uint32_t kv_base = smem_u32(smem + C::kOffKv);
       const uint32_t q_base = smem_u32(smem + C::kOffQ);
       const uint32_t p_base = smem_u32(smem + C::kOffP);
-
-      auto issue_qk = [&](int tl) -> bool {
-        const TileInfo ti = tile_info(p, xbeg + tl, xbeg, xend);
-        const int b = tl & 1;
-        if (ti.seg_start) {
-          if (!SMLA_WAIT(C::kBarQFull, seg_q & 1)) return false;
-          ++seg_q;
-        }
-        if (!SMLA_WAIT(C::kBarKvFull + b, (tl >> 1) & 1)) return false;
-        tc_fence_after();
-        const uint32_t kv = kv_base + b * C::kKvTile;
-        const uint32_t sbuf = tmem + C::kSCol + b * C::kNS * HG;
+      int next_qk = 0, next_pv = 0;
+      uint64_t t_idle = 0;
+      while (next_pv < n_local) {
+        bool progressed = false;
+        // ---- QK^T of tile next_qk: needs its tile, its Q block and a free S buffer
+        if (next_qk < n_local && next_qk < next_pv + 2) {
+          const int tl = next_qk;
+          const TileInfo ti = tile_info(p, xbeg + tl, xbeg, xend);
+          const int b = tl & 1;
+          const int seg = ti.seg_start ? seg_q : seg_q - 1;
+          const int qb = seg % C::kQBufs;
+          const bool q_ok = !ti.seg_start || mbar_test_wait(&bars[C::kBarQFull + qb], (seg / C::kQBufs) & 1);
+          if (q_ok && mbar_test_wait(&bars[C::kBarKvFull + b], (tl >> 1) & 1)) {
+            if (ti.seg_start) ++seg_q;
+            tc_fence_after();
+            const uint32_t kv = kv_base + b * C::kKvTile;
+            const uint32_t qs = q_base + qb * C::kQBytes;
+            const uint32_t sbuf = tmem + C::kSCol + b * C::kNS * HG;
 #pragma unroll
-        for (int s = 0; s < 36; ++s) {
-          const uint32_t off = (s & 3) * 32;
-          const uint64_t da = make_sdesc(kv + (s >> 2) * C::kPanel + off, 16, 1024, kLayoutSw128);
-          const uint64_t db = make_sdesc(q_base + (s >> 2) * C::kQPanel + off, 16, 1024, kLayoutSw128);
-          // FP8: NoPE scale group g = s / 8 (columns 128g..128g+127) and the RoPE
-          // columns each get their own accumulator; BF16: one accumulator.
-          const int g = kFp8 ? (s < 32 ? (s >> 3) : 4) : 0;
-          const bool first = kFp8 ? (s < 32 ? (s & 7) == 0 : s == 32) : s == 0;
-          mma_ss(sbuf + g * HG, da, db, idesc_qk, first ? 0u : 1u);
-        }
-        mma_commit(&bars[C::kBarSFull + b]);
-        if (ti.seg_end) mma_commit(&bars[C::kBarQEmpty]);
-        return true;
-      };
-      auto issue_pv = [&](int tl) -> bool {
-        const TileInfo ti = tile_info(p, xbeg + tl, xbeg, xend);
-        const int b = tl & 1;
-        if (!SMLA_WAIT(C::kBarPFull + b, (tl >> 1) & 1)) return false;
-        if (ti.seg_start) {
-          if (seg_o > 0 && !SMLA_WAIT(C::kBarOFree, (seg_o - 1) & 1)) return false;
-          ++seg_o;
-        }
-        tc_fence_after();
-        const uint32_t kv = kv_base + b * C::kKvTile;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint32_t pb = p_base + (b * C::kNP + (kFp8 ? q : 0)) * C::kPBytes;
-#pragma unroll
-          for (int s = 0; s < 4; ++s) {
-            const uint64_t da = make_sdesc(kv + 2 * q * C::kPanel + s * 2048, C::kPanel, 1024, kLayoutSw128);
-            const uint64_t db = make_sdesc(pb + 2 * s * pkb, pkb, 128, kLayoutNone);
-            mma_ss(tmem + C::kOCol + q * HG, da, db, idesc_pv, (ti.seg_start && s == 0) ? 0u : 1u);
+            for (int s = 0; s < 36; ++s) {
+              const uint32_t off = (s & 3) * 32;
+              const uint64_t da = make_sdesc(kv + (s >> 2) * C::kPanel + off, 16, 1024, kLayoutSw128);
+              const uint64_t db = make_sdesc(qs + (s >> 2) * C::kQPanel + off, 16, 1024, kLayoutSw128);
+              // FP8: NoPE scale group g = s / 8 (columns 128g..128g+127) and the
+              // RoPE columns each get their own accumulator; BF16: one accumulator.
+              const int g = kFp8 ? (s < 32 ? (s >> 3) : 4) : 0;
+              const bool first = kFp8 ? (s < 32 ? (s & 7) == 0 : s == 32) : s == 0;
+              mma_ss(sbuf + g * HG, da, db, idesc_qk, first ? 0u : 1u);
+            }
+            mma_commit(&bars[C::kBarSFull + b]);
+            SMLA_TRACE_SET(tl, kEvQk);
+            if (ti.seg_end) mma_commit(&bars[C::kBarQEmpty + qb]);
+            ++next_qk;
+            progressed = true;
           }
         }
-        mma_commit(&bars[C::kBarKvEmpty + b]);
-        mma_commit(&bars[C::kBarPvDone + b]);
-        return true;
-      };
-      bool ok = issue_qk(0);
-      for (int tl = 1; ok && tl < n_local; ++tl) ok = issue_pv(tl - 1) && issue_qk(tl);
-      if (ok) issue_pv(n_local - 1);
+        // ---- P.V of tile next_pv: needs its P operands (and, for a segment's
+        // first tile, the previous segment's epilogue to have read O)
+        if (next_pv < next_qk) {
+          const int tl = next_pv;
+          const TileInfo ti = tile_info(p, xbeg + tl, xbeg, xend);
+          const int b = tl & 1;
+          const bool o_ok = !ti.seg_start || seg_o == 0 || mbar_test_wait(&bars[C::kBarOFree], (seg_o - 1) & 1);
+          if (o_ok && mbar_test_wait(&bars[C::kBarPFull + b], (tl >> 1) & 1)) {
+            if (ti.seg_start) ++seg_o;
+            tc_fence_after();
+            const uint32_t kv = kv_base + b * C::kKvTile;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const uint32_t pb = p_base + (b * C::kNP + (kFp8 ? q : 0)) * C::kPBytes;
+#pragma unroll
+              for (int s = 0; s < 4; ++s) {
+                const uint64_t da = make_sdesc(kv + 2 * q * C::kPanel + s * 2048, C::kPanel, 1024, kLayoutSw128);
+                const uint64_t db = make_sdesc(pb + 2 * s * pkb, pkb, 128, kLayoutNone);
+                mma_ss(tmem + C::kOCol + q * HG, da, db, idesc_pv, (ti.seg_start && s == 0) ? 0u : 1u);
+              }
+            }
+            mma_commit(&bars[C::kBarKvEmpty + b]);
+            mma_commit(&bars[C::kBarPvDone + b]);
+            SMLA_TRACE_SET(tl, kEvPv);
+            ++next_pv;
+            progressed = true;
+          }
+        }
+        if (progressed) {
+          t_idle = 0;
+        } else {
+          // bounded idle: give up (and unwind the CTA) if nothing became ready
+          if (*abort_flag) break;
+          const uint64_t now = globaltimer_ns();
+          if (t_idle == 0) {
+            t_idle = now;
+          } else if (now - t_idle > kWaitLimitNs) {
+            *abort_flag = 1;
+            atomicCAS(p.status, 0, kDevWaitTimeout);
+            break;
+          }
+        }
+      }
     }
     __syncwarp();
   } else {
@@ -472,6 +532,7 @@ __global__ void __launch_bounds__(Cfg<HG, kFp8>::kThreads, 1) sparse_mla_attn_ke
         n_seg_tiles = 0;
       }
       if (!dead) dead = !SMLA_WAIT(C::kBarSFull + b, (tl >> 1) & 1);
+      if (tid == 0) SMLA_TRACE_SET(tl, kEvSoftStart);
       if (!dead) dead = !SMLA_WAIT(C::kBarKvFull + b, (tl >> 1) & 1);  // orders the row-valid flags
       tc_fence_after();
       const bool row_ok = !dead && lane < 16 && valid[b * C::kRows + r] != 0;
@@ -486,38 +547,54 @@ __global__ void __launch_bounds__(Cfg<HG, kFp8>::kThreads, 1) sparse_mla_attn_ke
           scs[3] = v4.w;
         }
       }
-      // scaled logits (log2 units) of head block hb: sum_g scale_g * S_g + S_rope
+      // scaled logits (log2 units) of head block hb: sum_g scale_g * S_g + S_rope.
+      // All accumulator loads of a block are issued before one wait; the empty
+      // asm statements after the wait keep every use of the loaded registers
+      // behind it.
       auto logits = [&](int hb, float (&sv)[16]) {
-        uint32_t raw[16];
         if constexpr (kFp8) {
-          tmem_ld16_sync(s_addr + 4 * HG + hb * 16, raw);
+          uint32_t a0[16], a1[16], a2[16], a3[16], a4[16];
+          tmem_ld16(s_addr + 0 * HG + hb * 16, a0);
+          tmem_ld16(s_addr + 1 * HG + hb * 16, a1);
+          tmem_ld16(s_addr + 2 * HG + hb * 16, a2);
+          tmem_ld16(s_addr + 3 * HG + hb * 16, a3);
+          tmem_ld16(s_addr + 4 * HG + hb * 16, a4);
+          tmem_ld_wait();
+          reg_fence16(a0);
+          reg_fence16(a1);
+          reg_fence16(a2);
+          reg_fence16(a3);
+          reg_fence16(a4);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) sv[j] = __uint_as_float(raw[j]);
-#pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            tmem_ld16_sync(s_addr + g * HG + hb * 16, raw);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) sv[j] = fmaf(scs[g], __uint_as_float(raw[j]), sv[j]);
+          for (int j = 0; j < 16; ++j) {
+            float acc = __uint_as_float(a4[j]);
+            acc = fmaf(scs[0], __uint_as_float(a0[j]), acc);
+            acc = fmaf(scs[1], __uint_as_float(a1[j]), acc);
+            acc = fmaf(scs[2], __uint_as_float(a2[j]), acc);
+            acc = fmaf(scs[3], __uint_as_float(a3[j]), acc);
+            sv[j] = row_ok ? acc * p.scale_log2 : -INFINITY;
           }
         } else {
-          tmem_ld16_sync(s_addr + hb * 16, raw);
+          uint32_t a0[16];
+          tmem_ld16_sync(s_addr + hb * 16, a0);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) sv[j] = __uint_as_float(raw[j]);
+          for (int j = 0; j < 16; ++j) sv[j] = row_ok ? __uint_as_float(a0[j]) * p.scale_log2 : -INFINITY;
         }
-#pragma unroll
-        for (int j = 0; j < 16; ++j) sv[j] = row_ok ? sv[j] * p.scale_log2 : -INFINITY;
       };
-      // pass 1: per-head maximum of this tile
+      // pass 1: logits (kept for pass 2) and the per-head maximum of this tile
       float* redm = red_max + (tl & 1) * 4 * HG;
+      float sl[NB16][16];
 #pragma unroll
       for (int hb = 0; hb < NB16; ++hb) {
-        float v[16];
         if (!dead) {
-          logits(hb, v);
+          logits(hb, sl[hb]);
         } else {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) v[j] = -INFINITY;
+          for (int j = 0; j < 16; ++j) sl[hb][j] = -INFINITY;
         }
+        float v[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = sl[hb][j];
         const float mx = warp_reduce16<true>(v, lane);
         if ((lane & 1) == 0) redm[w * HG + hb * 16 + (lane >> 1)] = mx;
       }
@@ -562,15 +639,9 @@ __global__ void __launch_bounds__(Cfg<HG, kFp8>::kThreads, 1) sparse_mla_attn_ke
 #pragma unroll
       for (int hb = 0; hb < NB16; ++hb) {
         float pr[16];
-        if (!dead) {
-          logits(hb, pr);
-        } else {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) pr[j] = -INFINITY;
-        }
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-          pr[j] = row_ok ? exp2f(pr[j] - m_used[hb * 16 + j]) : 0.f;
+          pr[j] = row_ok ? exp2f(sl[hb][j] - m_used[hb * 16 + j]) : 0.f;
           l_part[hb * 16 + j] += pr[j];
         }
         if (!dead && lane < 16) {
@@ -593,6 +664,7 @@ __global__ void __launch_bounds__(Cfg<HG, kFp8>::kThreads, 1) sparse_mla_attn_ke
       tc_fence_before();
       __syncwarp();
       if (lane == 0 && !dead) mbar_arrive(&bars[C::kBarPFull + b]);
+      if (tid == 0) SMLA_TRACE_SET(tl, kEvSoftDone);
       ++n_seg_tiles;
 
       if (ti.seg_end) {
@@ -662,7 +734,10 @@ __global__ void __launch_bounds__(Cfg<HG, kFp8>::kThreads, 1) sparse_mla_attn_ke
   }
 }
 
-// LSE-weighted merge of the partial results of units split across CTAs.
+// LSE-weighted merge of the partial results of units split across CTAs:
+//   M = max_s lse_s,  w_s = exp(lse_s - M) / sum_s' exp(lse_s' - M),
+//   out = sum_s w_s * O_s,  lse = M + log(sum_s exp(lse_s - M)).
+// One block per unit; thread (h, c4) owns head h and float4 column chunks.
 template <int HG>
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ part_o,
                                                       const float* __restrict__ part_lse,
@@ -679,37 +754,41 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
   const int64_t c_lo = owner(u * nt), c_hi = owner(u * nt + nt - 1);
   if (c_lo == c_hi) return;  // finished inside one CTA, already written
   const int t = (int)(u / n_hg), hg = (int)(u % n_hg);
-  __shared__ float s_m[HG], s_w_sum[HG];
-  if (threadIdx.x < HG) {
-    const int h = threadIdx.x;
-    float m = -INFINITY;
-    for (int64_t c = c_lo; c <= c_hi; ++c) m = fmaxf(m, part_lse[(c + u) * HG + h]);
-    float wsum = 0.f;
-    if (m != -INFINITY)
-      for (int64_t c = c_lo; c <= c_hi; ++c) wsum += expf(part_lse[(c + u) * HG + h] - m);
-    s_m[h] = m;
-    s_w_sum[h] = wsum;
-    lse[(int64_t)t * H + hg * HG + h] = (m == -INFINITY) ? -INFINITY : m + logf(wsum);
-  }
-  __syncthreads();
-  for (int i = threadIdx.x; i < HG * (kDv / 4); i += blockDim.x) {
-    const int h = i / (kDv / 4), c4 = i - h * (kDv / 4);
-    const float m = s_m[h];
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (m != -INFINITY) {
-      const float inv = 1.f / s_w_sum[h];
-      for (int64_t c = c_lo; c <= c_hi; ++c) {
-        const float wgt = expf(part_lse[(c + u) * HG + h] - m) * inv;
-        const float4 v = reinterpret_cast<const float4*>(part_o + ((c + u) * HG + h) * kDv)[c4];
-        acc.x += wgt * v.x;
-        acc.y += wgt * v.y;
-        acc.z += wgt * v.z;
-        acc.w += wgt * v.w;
+  constexpr int kThreadsPerHead = 256 / HG;      // 16 (HG=16) or 8 (HG=32)
+  const int h = threadIdx.x / kThreadsPerHead;
+  const int sub = threadIdx.x % kThreadsPerHead;
+  float m = -INFINITY;
+  for (int64_t c = c_lo; c <= c_hi; ++c) m = fmaxf(m, __ldg(part_lse + (c + u) * HG + h));
+  float wsum = 0.f;
+  if (m != -INFINITY)
+    for (int64_t c = c_lo; c <= c_hi; ++c) wsum += expf(__ldg(part_lse + (c + u) * HG + h) - m);
+  if (sub == 0) lse[(int64_t)t * H + hg * HG + h] = (m == -INFINITY) ? -INFINITY : m + logf(wsum);
+  const float inv = m == -INFINITY ? 0.f : 1.f / wsum;
+  constexpr int kChunks = kDv / 4;                // 128 float4 per head row
+  float4 acc[kChunks / kThreadsPerHead];
+#pragma unroll
+  for (int k = 0; k < kChunks / kThreadsPerHead; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (m != -INFINITY) {
+    for (int64_t c = c_lo; c <= c_hi; ++c) {
+      const float wgt = expf(__ldg(part_lse + (c + u) * HG + h) - m) * inv;
+      const float4* src = reinterpret_cast<const float4*>(part_o + ((c + u) * HG + h) * kDv);
+#pragma unroll
+      for (int k = 0; k < kChunks / kThreadsPerHead; ++k) {
+        const float4 v = __ldg(src + sub + k * kThreadsPerHead);
+        acc[k].x += wgt * v.x;
+        acc[k].y += wgt * v.y;
+        acc[k].z += wgt * v.z;
+        acc[k].w += wgt * v.w;
       }
     }
-    __nv_bfloat16* o = out + ((int64_t)t * H + hg * HG + h) * kDv + 4 * c4;
-    reinterpret_cast<__nv_bfloat162*>(o)[0] = __floats2bfloat162_rn(acc.x, acc.y);
-    reinterpret_cast<__nv_bfloat162*>(o)[1] = __floats2bfloat162_rn(acc.z, acc.w);
+  }
+  __nv_bfloat16* o = out + ((int64_t)t * H + hg * HG + h) * kDv;
+#pragma unroll
+  for (int k = 0; k < kChunks / kThreadsPerHead; ++k) {
+    const int c4 = sub + k * kThreadsPerHead;
+    __nv_bfloat162* d = reinterpret_cast<__nv_bfloat162*>(o + 4 * c4);
+    d[0] = __floats2bfloat162_rn(acc[k].x, acc[k].y);
+    d[1] = __floats2bfloat162_rn(acc[k].z, acc[k].w);
   }
 }
 
@@ -757,6 +836,12 @@ cudaError_t launch_impl(const AttnArgs& a, const AttnPlan& plan, cudaStream_t st
 }
 
 }  // namespace
+
+#ifdef SMLA_TRACE
+extern "C" int smla_trace_set(unsigned long long* buf) {
+  return (int)cudaMemcpyToSymbol(g_smla_trace, &buf, sizeof(buf));
+}
+#endif
 
 AttnPlan plan_attention(int T, int H, int K, int num_splits, int num_sms) {
   AttnPlan pl;
