@@ -100,7 +100,7 @@ int run_attention(bool fp8, smla::AttnArgs& a, int num_splits, void* workspace, 
   int sms = 0;
   int rc = num_sms(&sms);
   if (rc != SMLA_OK) return rc;
-  const smla::AttnPlan plan = smla::plan_attention(a.T, a.H, a.K, num_splits, sms);
+  const smla::AttnPlan plan = smla::plan_attention(fp8, a.T, a.H, a.K, num_splits, sms);
   if (workspace) {
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
       return fail(SMLA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
@@ -116,11 +116,11 @@ int run_attention(bool fp8, smla::AttnArgs& a, int num_splits, void* workspace, 
   return SMLA_OK;
 }
 
-size_t workspace_bytes_for(int T, int H, int K, int num_splits) {
+size_t workspace_bytes_for(bool fp8, int T, int H, int K, int num_splits) {
   if (T <= 0 || check_heads(H) != SMLA_OK || K < 0) return 0;
   int sms = 0;
   if (num_sms(&sms) != SMLA_OK) return 0;
-  return smla::plan_attention(T, H, K, num_splits, sms).ws_bytes;
+  return smla::plan_attention(fp8, T, H, K, num_splits, sms).ws_bytes;
 }
 
 }  // namespace
@@ -162,7 +162,7 @@ int sparse_mla_decode_fp8(const void* q, const uint8_t* kv_cache, const int32_t*
 }
 
 size_t sparse_mla_decode_workspace_bytes(int T, int H, int K, int num_splits) {
-  return workspace_bytes_for(T, H, K, num_splits);
+  return workspace_bytes_for(true, T, H, K, num_splits);
 }
 
 int sparse_mla_prefill_bf16(const void* q, const void* kv, const int32_t* indices, float sm_scale,
@@ -196,7 +196,7 @@ int sparse_mla_prefill_bf16(const void* q, const void* kv, const int32_t* indice
 }
 
 size_t sparse_mla_prefill_workspace_bytes(int T, int H, int K, int num_splits) {
-  return workspace_bytes_for(T, H, K, num_splits);
+  return workspace_bytes_for(false, T, H, K, num_splits);
 }
 
 int mla_cache_store_fp8(const void* kv_new, const int64_t* slot_mapping, uint8_t* kv_cache, int T, int NB,

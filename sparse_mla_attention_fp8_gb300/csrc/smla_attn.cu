@@ -41,6 +41,7 @@
 
 #include "sm103_ptx.cuh"
 #include "smla_common.cuh"
+#include "smla_combine.cuh"
 #include "smla_kernels.h"
 
 namespace smla {
@@ -135,7 +136,6 @@ struct Params {
   int G;
 };
 
-__device__ __forceinline__ int64_t tile_begin(int64_t c, int64_t total, int G) { return (c * total) / G; }
 
 struct TileInfo {
   int u, kt, t, hg;
@@ -734,64 +734,6 @@ __global__ void __launch_bounds__(Cfg<HG, kFp8>::kThreads, 1) sparse_mla_attn_ke
   }
 }
 
-// LSE-weighted merge of the partial results of units split across CTAs:
-//   M = max_s lse_s,  w_s = exp(lse_s - M) / sum_s' exp(lse_s' - M),
-//   out = sum_s w_s * O_s,  lse = M + log(sum_s exp(lse_s - M)).
-// One block per unit; thread (h, c4) owns head h and float4 column chunks.
-template <int HG>
-__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ part_o,
-                                                      const float* __restrict__ part_lse,
-                                                      __nv_bfloat16* __restrict__ out, float* __restrict__ lse,
-                                                      int H, int n_hg, int nt, int64_t total, int G) {
-  const int64_t u = blockIdx.x;
-  auto owner = [&](int64_t x) -> int64_t {
-    int64_t c = ((x + 1) * G - 1) / total;
-    if (c >= G) c = G - 1;
-    while (c + 1 < G && tile_begin(c + 1, total, G) <= x) ++c;
-    while (c > 0 && tile_begin(c, total, G) > x) --c;
-    return c;
-  };
-  const int64_t c_lo = owner(u * nt), c_hi = owner(u * nt + nt - 1);
-  if (c_lo == c_hi) return;  // finished inside one CTA, already written
-  const int t = (int)(u / n_hg), hg = (int)(u % n_hg);
-  constexpr int kThreadsPerHead = 256 / HG;      // 16 (HG=16) or 8 (HG=32)
-  const int h = threadIdx.x / kThreadsPerHead;
-  const int sub = threadIdx.x % kThreadsPerHead;
-  float m = -INFINITY;
-  for (int64_t c = c_lo; c <= c_hi; ++c) m = fmaxf(m, __ldg(part_lse + (c + u) * HG + h));
-  float wsum = 0.f;
-  if (m != -INFINITY)
-    for (int64_t c = c_lo; c <= c_hi; ++c) wsum += expf(__ldg(part_lse + (c + u) * HG + h) - m);
-  if (sub == 0) lse[(int64_t)t * H + hg * HG + h] = (m == -INFINITY) ? -INFINITY : m + logf(wsum);
-  const float inv = m == -INFINITY ? 0.f : 1.f / wsum;
-  constexpr int kChunks = kDv / 4;                // 128 float4 per head row
-  float4 acc[kChunks / kThreadsPerHead];
-#pragma unroll
-  for (int k = 0; k < kChunks / kThreadsPerHead; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (m != -INFINITY) {
-    for (int64_t c = c_lo; c <= c_hi; ++c) {
-      const float wgt = expf(__ldg(part_lse + (c + u) * HG + h) - m) * inv;
-      const float4* src = reinterpret_cast<const float4*>(part_o + ((c + u) * HG + h) * kDv);
-#pragma unroll
-      for (int k = 0; k < kChunks / kThreadsPerHead; ++k) {
-        const float4 v = __ldg(src + sub + k * kThreadsPerHead);
-        acc[k].x += wgt * v.x;
-        acc[k].y += wgt * v.y;
-        acc[k].z += wgt * v.z;
-        acc[k].w += wgt * v.w;
-      }
-    }
-  }
-  __nv_bfloat16* o = out + ((int64_t)t * H + hg * HG + h) * kDv;
-#pragma unroll
-  for (int k = 0; k < kChunks / kThreadsPerHead; ++k) {
-    const int c4 = sub + k * kThreadsPerHead;
-    __nv_bfloat162* d = reinterpret_cast<__nv_bfloat162*>(o + 4 * c4);
-    d[0] = __floats2bfloat162_rn(acc[k].x, acc[k].y);
-    d[1] = __floats2bfloat162_rn(acc[k].z, acc[k].w);
-  }
-}
-
 template <int HG, bool kFp8>
 cudaError_t launch_impl(const AttnArgs& a, const AttnPlan& plan, cudaStream_t stream) {
   using C = Cfg<HG, kFp8>;
@@ -843,7 +785,7 @@ extern "C" int smla_trace_set(unsigned long long* buf) {
 }
 #endif
 
-AttnPlan plan_attention(int T, int H, int K, int num_splits, int num_sms) {
+AttnPlan plan_prefill_bf16(int T, int H, int K, int num_splits, int num_sms) {
   AttnPlan pl;
   pl.HG = (H % 32 == 0) ? 32 : 16;
   pl.n_hg = H / pl.HG;
@@ -861,9 +803,16 @@ AttnPlan plan_attention(int T, int H, int K, int num_splits, int num_sms) {
   return pl;
 }
 
+cudaError_t launch_prefill_bf16(const AttnArgs& a, const AttnPlan& plan, cudaStream_t stream) {
+  return plan.HG == 16 ? launch_impl<16, false>(a, plan, stream) : launch_impl<32, false>(a, plan, stream);
+}
+
+AttnPlan plan_attention(bool fp8, int T, int H, int K, int num_splits, int num_sms) {
+  return fp8 ? plan_decode_fp8(T, H, K, num_splits, num_sms) : plan_prefill_bf16(T, H, K, num_splits, num_sms);
+}
+
 cudaError_t launch_attention(bool fp8, const AttnArgs& a, const AttnPlan& plan, cudaStream_t stream) {
-  if (plan.HG == 16) return fp8 ? launch_impl<16, true>(a, plan, stream) : launch_impl<16, false>(a, plan, stream);
-  return fp8 ? launch_impl<32, true>(a, plan, stream) : launch_impl<32, false>(a, plan, stream);
+  return fp8 ? launch_decode_fp8(a, plan, stream) : launch_prefill_bf16(a, plan, stream);
 }
 
 }  // namespace smla

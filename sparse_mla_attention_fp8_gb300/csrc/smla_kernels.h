@@ -16,7 +16,7 @@ cudaError_t launch_translate(const int32_t* indices, const int32_t* block_table,
 // group) pairs, each split into nt tiles of 64 top-k rows; G persistent CTAs
 // take contiguous, balanced ranges of the unit-major tile sequence.
 struct AttnPlan {
-  int HG;             // heads per CTA (16 or 32)
+  int HG;             // heads per work unit
   int n_hg;           // head groups per token
   int nt;             // tiles per unit
   int64_t units;      // T * n_hg
@@ -26,7 +26,9 @@ struct AttnPlan {
   size_t ws_bytes;    // workspace bytes (status word + partial results)
 };
 
-AttnPlan plan_attention(int T, int H, int K, int num_splits, int num_sms);
+AttnPlan plan_attention(bool fp8, int T, int H, int K, int num_splits, int num_sms);
+AttnPlan plan_decode_fp8(int T, int H, int K, int num_splits, int num_sms);
+AttnPlan plan_prefill_bf16(int T, int H, int K, int num_splits, int num_sms);
 
 struct AttnArgs {
   const void* q;
@@ -44,6 +46,8 @@ struct AttnArgs {
 };
 
 cudaError_t launch_attention(bool fp8, const AttnArgs& a, const AttnPlan& plan, cudaStream_t stream);
+cudaError_t launch_decode_fp8(const AttnArgs& a, const AttnPlan& plan, cudaStream_t stream);
+cudaError_t launch_prefill_bf16(const AttnArgs& a, const AttnPlan& plan, cudaStream_t stream);
 
 // Offsets inside the workspace.
 constexpr size_t kWsStatusBytes = 256;
