@@ -83,6 +83,17 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   return false;
 }
 
+// Wait used on the way out of a kernel for the kernel's own asynchronous work
+// (copies, tensor-core operations) still in flight: ignores the abort flag,
+// gives up after the same time limit.  Returns true once the phase completed.
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 0;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255u) == 255u && globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
 // ---------------------------------------------------------------- bulk copy
 // 1-D TMA copy global -> shared, completion counted in bytes on an mbarrier.
 // dst, src 16-byte aligned; bytes a multiple of 16.
@@ -96,6 +107,11 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 // 16-byte asynchronous copy global -> shared (L2 only), and its completion.
 __device__ __forceinline__ void cp_async16(uint32_t dst_smem, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst_smem), "l"(src) : "memory");
+}
+// Same with a byte count of 0 or 16: 0 fills the 16 destination bytes with
+// zeros without reading the source.
+__device__ __forceinline__ void cp_async16_zfill(uint32_t dst_smem, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst_smem), "l"(src), "r"(src_bytes) : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
@@ -182,6 +198,19 @@ __device__ __forceinline__ void tmem_ld16_sync(uint32_t taddr, uint32_t (&r)[16]
 __device__ __forceinline__ void reg_fence16(uint32_t (&r)[16]) {
 #pragma unroll
   for (int i = 0; i < 16; ++i) asm volatile("" : "+r"(r[i]));
+}
+// 16 TMEM lanes x 256 bits, twice: columns col .. col + 15 of lanes base .. base + 15
+// (base = the warp's lane quarter).  Thread t receives lane t/4 in registers
+// 0, 1, 4, 5 and lane t/4 + 8 in registers 2, 3, 6, 7, at columns 2(t%4),
+// 2(t%4) + 1 (registers 0..3) and the same + 8 (registers 4..7).
+__device__ __forceinline__ void tmem_ld_16x256b_x2(uint32_t taddr, uint32_t (&r)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+}
+__device__ __forceinline__ void reg_fence8(uint32_t (&r)[8]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) asm volatile("" : "+r"(r[i]));
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 

@@ -9,17 +9,23 @@
 // over the token's top-k rows (translated through the paged block table);
 // invalid rows are masked, a token without valid rows gets out = 0, lse = -inf.
 //
-// Design: the tensor cores read the cache bytes as stored, with no
+// Design: the tensor cores read the cache codes as stored, with no
 // dequantization pass.
-//  * Tiles of 128 top-k rows are gathered by TMA (tile::gather4, 128-byte
-//    swizzle) straight into shared memory: the 512 e4m3 codes as four
-//    K-major operand panels, the 64 bf16 RoPE values as a fifth panel and the
-//    four float32 scales beside them.  Two tiles are double-buffered.
+//  * Transport: one producer warp issues one 656-byte bulk copy (TMA, 1-D)
+//    per valid row into a ring of raw row stages (4 x 32 rows in flight).
+//    Bulk copies keep many rows in flight per instruction; 16-byte
+//    asynchronous copies or register loads are limited to a few rows in
+//    flight per warp.
+//  * Layout: two rearrange warps move each row's 16-byte chunks from the raw
+//    stage to their 128-byte-swizzled operand positions in a 64-row tile (the
+//    512 e4m3 codes as four K-major panels, the 64 bf16 RoPE values as a
+//    fifth panel, the four float32 scales beside them); invalid rows are
+//    zero-filled.  Two operand tiles are double-buffered.
 //  * Q is split once per (token, 16-head group) into two e4m3 terms,
 //    q * 2^s_h = hi + lo (s_h a per-head power of two putting max |q| near
 //    448), exact for all but negligibly small components; hi and lo are the
 //    two halves of an N = 32 operand.  QK^T for each 128-column scale group g
-//    is one kind::f8f6f4 product E_g [Q_hi Q_lo]^T (M = 128 rows, N = 32,
+//    is one kind::f8f6f4 product E_g [Q_hi Q_lo]^T (M = 64 rows, N = 32,
 //    K = 128 codes), the RoPE part a bf16 product; the softmax combines
 //    s = 2^-s_h sum_g scale_g (S_g,hi + S_g,lo) + S_rope in fp32.
 //  * P.V for value chunk q (= scale group q) is one kind::f8f6f4 product
@@ -30,10 +36,9 @@
 //    which keeps P' <= 256: the top of the e4m3 range, where hi + lo carries
 //    8 significant bits down to ~2^-10 of the largest weight.  O is rescaled
 //    in tensor memory when R_q or the running max changes.
-//  * Warp roles: index translation (1 warp), TMA producer (1), tensor-core
-//    issuer (1 thread), Q preparation (4 warps), softmax / epilogue (4 warps,
-//    one thread per tile row / output column).
-#include <cuda.h>
+//  * Warp roles: softmax / epilogue (4 warps), tensor-core issuer (1 thread),
+//    index translation (1 warp), bulk-copy producer (1 warp), rearrange
+//    (2 warps), Q preparation (2 warps).
 #include <cstdint>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -49,41 +54,85 @@ namespace smla {
 namespace {
 
 constexpr uint32_t kFullMask = 0xffffffffu;
-constexpr int HG = 16;       // heads per CTA work unit
+
+// Optional per-tile timeline for performance work: with SMLA_TRACE defined,
+// roles record %globaltimer at their hand-off points into g_smla_trace_fp8
+// (set by the host through smla_trace_set_fp8).  Compiled out otherwise.
+#ifdef SMLA_TRACE
+__device__ unsigned long long* g_smla_trace_fp8 = nullptr;
+constexpr int kTraceTiles = 64, kTraceEvents = 14;
+enum { kEvIdx = 0, kEvRawLanded = 1, kEvOpFull = 2, kEvQk = 3, kEvSoftStart = 4, kEvSoftDone = 5, kEvPv = 6,
+       kEvQReady = 7, kEvRawFull = 8, kEvOpEmpty = 9, kEvIssue = 10, kEvSoftLogits = 11, kEvSoftBar = 12,
+       kEvSoftPWait = 13 };
+#define SMLA_TRACE_SET(tl, ev)                                                                                  \
+  do {                                                                                                          \
+    if (g_smla_trace_fp8 && (tl) < kTraceTiles)                                                                  \
+      g_smla_trace_fp8[((size_t)blockIdx.x * kTraceTiles + (tl)) * kTraceEvents + (ev)] = globaltimer_ns();    \
+  } while (0)
+// Cycle counters of the softmax sections (thread 0), stored after the per-tile events.
+#define SMLA_CLK_DECL unsigned clk_acc[8] = {0, 0, 0, 0, 0, 0, 0, 0}, clk_prev = (unsigned)clock()
+#define SMLA_CLK_START() (clk_prev = (unsigned)clock())
+#define SMLA_CLK_MARK(i)                   \
+  do {                                     \
+    const unsigned now_ = (unsigned)clock(); \
+    clk_acc[(i)] += now_ - clk_prev;       \
+    clk_prev = now_;                       \
+  } while (0)
+#define SMLA_CLK_STORE()                                                                                        \
+  do {                                                                                                          \
+    if (g_smla_trace_fp8 && tid == 0)                                                                           \
+      for (int i_ = 0; i_ < 8; ++i_)                                                                            \
+        g_smla_trace_fp8[(size_t)gridDim.x * kTraceTiles * kTraceEvents + blockIdx.x * 8 + i_] = clk_acc[i_]; \
+  } while (0)
+#else
+#define SMLA_TRACE_SET(tl, ev) ((void)0)
+#define SMLA_CLK_DECL
+#define SMLA_CLK_START() ((void)0)
+#define SMLA_CLK_MARK(i) ((void)0)
+#define SMLA_CLK_STORE() ((void)0)
+#endif
+
+constexpr int HG = 16;                 // heads per CTA work unit
+constexpr int kRows = 64;              // top-k rows per tile
+constexpr int kRawRows = 32;           // rows per raw stage (two stages per tile)
+constexpr int kRawStages = 4;          // raw ring depth (128 rows in flight)
 constexpr float kMaxSlack = 1.0f;      // log2 growth of a head's max tolerated before rescaling O (p <= 2)
 constexpr float kPScale = 128.0f;      // P' = kPScale * p * scale / R  <=  256
 constexpr float kPScaleInv = 1.0f / 128.0f;
-constexpr int kRows = 128;   // top-k rows per tile
 
 // ---- shared memory layout (offsets from a 1024-byte aligned base)
-constexpr int kPanel = kRows * 128;                   // 16 KB: 128 rows x 128 bytes
-constexpr int kKvRope = 4 * kPanel;                   // RoPE panel after the 4 code panels
-// Scale rows: each TMA destination must be 128-byte aligned, so the 4 rows of
-// one gather (64 bytes) get a 128-byte slot: row r at (r / 4) * 128 + (r % 4) * 16.
-constexpr int kKvScale = 5 * kPanel;
-constexpr int kKvBuf = 5 * kPanel + (kRows / 4) * 128;  // 86016
+constexpr int kPanel = kRows * 128;                   // 8 KB: 64 rows x 128 bytes
+constexpr int kOpRope = 4 * kPanel;                   // RoPE panel after the 4 code panels
+constexpr int kOpScale = 5 * kPanel;                  // 64 x 16-byte scale rows
+constexpr int kOpBuf = 5 * kPanel + kRows * 16;       // 41984
+constexpr int kRawStage = kRawRows * kRowBytes;       // 20992
 constexpr int kQPanel = 32 * 128;                     // 32 operand rows (hi, lo) x 128 codes
 constexpr int kQRope = 4 * kQPanel;                   // 16 rows x 64 bf16
 constexpr int kQBuf = 4 * kQPanel + HG * 128;         // 18432
-constexpr int kPGroup = kRows * 32;                   // P'_q: 128 rows x 32 codes
-constexpr int kOffKv = 0;
-constexpr int kOffQ = kOffKv + 2 * kKvBuf;
+constexpr int kPGroup = kRows * 32;                   // P'_q: 64 rows x 32 codes
+constexpr int kOffOp = 0;
+constexpr int kOffQ = kOffOp + 2 * kOpBuf;
 constexpr int kOffP = kOffQ + 2 * kQBuf;
-constexpr int kOffSlots = kOffP + 4 * kPGroup;        // int32 [4][128]
-constexpr int kOffValid = kOffSlots + 4 * kRows * 4;  // uint8 [2][128]
+constexpr int kOffRaw = kOffP + 4 * kPGroup;
+constexpr int kOffRawMeta = kOffRaw + kRawStages * kRawStage;  // int32 [stages][32] slots
+constexpr int kOffSlots = kOffRawMeta + kRawStages * kRawRows * 4;  // int32 [4][64]
+constexpr int kOffValid = kOffSlots + 4 * kRows * 4;  // uint8 [2][64]
 constexpr int kOffPre = kOffValid + 2 * kRows;        // float [4][16] inverse Q prescales
 constexpr int kOffRedMax = kOffPre + 4 * HG * 4;      // float [2][4 warps][16]
 constexpr int kOffRedSc = kOffRedMax + 2 * 4 * HG * 4;  // float [2][4 warps][4]
 constexpr int kOffRedSum = kOffRedSc + 2 * 4 * 4 * 4;   // float [4 warps][16]
-constexpr int kOffBar = kOffRedSum + 4 * HG * 4;
+constexpr int kOffDummy = kOffRedSum + 4 * HG * 4;   // 16 bytes per rearrange lane: sink for idle lanes
+constexpr int kOffBar = kOffDummy + 2 * 32 * 16;
 enum {
-  kBarKvFull = 0, kBarKvEmpty = 2, kBarSFull = 4, kBarPFull = 6, kBarPvDone = 7, kBarIdxFull = 8,
-  kBarIdxEmpty = 12, kBarQFull = 16, kBarQEmpty = 18, kBarOFree = 20, kNumBars = 21
+  kBarOpFull = 0, kBarOpEmpty = 2, kBarSFull = 4, kBarPFull = 6, kBarPvDone = 7, kBarIdxFull = 8,
+  kBarIdxEmpty = 12, kBarQFull = 16, kBarQEmpty = 18, kBarOFree = 20, kBarRawFull = 21,
+  kBarRawEmpty = kBarRawFull + kRawStages, kBarDrain = kBarRawEmpty + kRawStages, kNumBars = kBarDrain + 1
 };
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 16;
 constexpr int kSmemAlloc = kSmemBytes + 1024;
-static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0 && kKvBuf % 1024 == 0, "operand alignment");
+static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0 && kOpBuf % 1024 == 0, "operand alignment");
+static_assert(kOffRaw % 16 == 0 && kRawStage % 16 == 0 && kOffBar % 8 == 0, "copy / barrier alignment");
 static_assert(kSmemAlloc <= 232448, "shared memory budget");
 
 // ---- tensor memory columns
@@ -92,9 +141,15 @@ constexpr int kOCol = 2 * kSCols;     // O^T: 4 chunks x (hi, lo) x 16 heads
 constexpr int kTmemCols = 512;
 static_assert(kOCol + 4 * 32 <= kTmemCols, "tensor memory budget");
 
-// ---- warp roles
-constexpr int kMmaWarp = 4, kIndexWarp = 5, kTmaWarp = 6, kQWarp0 = 7;
-constexpr int kThreads = 32 * 11;
+// ---- warp roles (11 warps; with at most 3 warps per SM sub-partition each
+// thread may hold up to 168 registers).  Warp w runs on sub-partition w % 4:
+// each sub-partition carries one softmax warp; the rearrange and Q warps sit
+// on sub-partitions 0 and 1, the issuer and index warps on 2, the producer on 3.
+constexpr int kRearrWarp0 = 4, kRearrWarps = 2, kMmaWarp = 6, kProdWarp = 7, kQWarp0 = 8, kQWarps = 2,
+              kIndexWarp = 10;
+constexpr int kNumWarps = 11;
+constexpr int kThreads = 32 * kNumWarps;
+static_assert(kQWarp0 + kQWarps <= kIndexWarp && kIndexWarp < kNumWarps, "warp roles");
 
 __host__ __device__ constexpr uint32_t idesc_e4m3(uint32_t M, uint32_t N, uint32_t a_mn, uint32_t b_mn) {
   return (1u << 4) | (a_mn << 15) | (b_mn << 16) | ((N >> 3) << 17) | ((M >> 4) << 24);
@@ -102,6 +157,7 @@ __host__ __device__ constexpr uint32_t idesc_e4m3(uint32_t M, uint32_t N, uint32
 
 struct Params {
   const __nv_bfloat16* q;
+  const uint8_t* cache;
   const int32_t* indices;
   const int32_t* block_table;
   const int32_t* req_id;
@@ -141,17 +197,14 @@ __device__ __forceinline__ void mma_f8(uint32_t d, uint64_t a, uint64_t b, uint3
       : "memory");
 }
 
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int x, int r0, int r1, int r2, int r3,
-                                            uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
-      "%4, %5, %6}], [%7];" ::"r"(dst),
-      "l"(map), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar))
-      : "memory");
-}
-
 __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
   asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
 }
 
 __device__ __forceinline__ void named_bar_sync(int id, int n) {
@@ -195,21 +248,63 @@ __device__ __forceinline__ float warp_reduce16(float (&v)[16], int lane) {
   return v[0];
 }
 
-__device__ __forceinline__ float pow2_ceil(float x) {  // smallest power of two >= x (x > 0, normal)
+__device__ __forceinline__ float pow2_ceil(float x) {  // smallest power of two >= x (x > 0)
   const uint32_t u = __float_as_uint(x);
   const uint32_t e = u & 0x7F800000u;
   return __uint_as_float((u & 0x007FFFFFu) ? e + 0x00800000u : e);
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
-    sparse_mla_decode_fp8_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap map_row,
-                                 const __grid_constant__ CUtensorMap map_scale) {
+// 1 / x for a power of two x in the normal range (exact).
+__device__ __forceinline__ float rcp_pow2(float x) { return __uint_as_float(0x7F000000u - __float_as_uint(x)); }
+
+__device__ __forceinline__ float ex2_approx(float x) {  // 2^x; 2^-inf = 0
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Four floats -> e4m3 hi and lo words (byte i from value i), x_i ~ hi_i + lo_i.
+// The split runs in f16x2: the values are first rounded to f16 (11 significant
+// bits, more than the 8 that hi + lo keep), hi is the e4m3 rounding, lo the
+// e4m3 rounding of the exact f16 difference.
+__device__ __forceinline__ void split4(float x0, float x1, float x2, float x3, uint32_t& hi, uint32_t& lo) {
+  uint32_t a, b, ha, hb, da, db, ra, rb;
+  uint16_t t;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(a) : "f"(x1), "f"(x0));
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(b) : "f"(x3), "f"(x2));
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(t) : "r"(a));
+  ha = t;
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(t) : "r"(b));
+  hb = t;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(da) : "h"((uint16_t)ha));
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(db) : "h"((uint16_t)hb));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(da));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(rb) : "r"(b), "r"(db));
+  uint32_t la, lb;
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(t) : "r"(ra));
+  la = t;
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(t) : "r"(rb));
+  lb = t;
+  hi = ha | (hb << 16);
+  lo = la | (lb << 16);
+}
+
+__device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// QK^T column n (of 16) holds head pi(n) with pi(2c + e + 8d) = 4c + e + 2d,
+// so that the 16x256b read of S gives thread c (lane % 4) heads 4c .. 4c + 3.
+__device__ __forceinline__ int q_row_of_head(int h) { return 2 * (h >> 2) + (h & 1) + 8 * ((h >> 1) & 1); }
+
+__global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
   int32_t* slots_ring = reinterpret_cast<int32_t*>(smem + kOffSlots);
+  int32_t* raw_meta = reinterpret_cast<int32_t*>(smem + kOffRawMeta);
   uint8_t* valid = smem + kOffValid;
   float* pre_ring = reinterpret_cast<float*>(smem + kOffPre);
 
@@ -220,10 +315,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars[kBarKvFull + i], 1);
-      mbar_init(&bars[kBarKvEmpty + i], 1);
+      mbar_init(&bars[kBarOpFull + i], kRearrWarps);
+      mbar_init(&bars[kBarOpEmpty + i], 1);
       mbar_init(&bars[kBarSFull + i], 1);
-      mbar_init(&bars[kBarQFull + i], 4);
+      mbar_init(&bars[kBarQFull + i], kQWarps);
       mbar_init(&bars[kBarQEmpty + i], 1);
     }
     mbar_init(&bars[kBarPFull], 4);
@@ -232,7 +327,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars[kBarIdxFull + i], 32);
       mbar_init(&bars[kBarIdxEmpty + i], 1);
     }
+    for (int i = 0; i < kRawStages; ++i) {
+      mbar_init(&bars[kBarRawFull + i], 1);
+      mbar_init(&bars[kBarRawEmpty + i], 1);
+    }
     mbar_init(&bars[kBarOFree], 4);
+    mbar_init(&bars[kBarDrain], 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -251,12 +351,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ index translation
     // The next tile's indices are loaded before this tile's block-table reads,
     // so each tile costs about one memory round trip.
-    int32_t cur[4], nxt[4], req_cur = 0, req_nxt = 0;
-    auto load_idx = [&](int tl, int32_t (&v)[4], int32_t& rq) {
+    int32_t cur[2], nxt[2], req_cur = 0, req_nxt = 0;
+    auto load_idx = [&](int tl, int32_t (&v)[2], int32_t& rq) {
       const TileInfo ti = tile_info(p, xbeg + tl, xbeg, xend);
       rq = __ldg(p.req_id + ti.t);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
+      for (int i = 0; i < 2; ++i) {
         const int k = ti.kt * kRows + lane + 32 * i;
         v[i] = k < p.K ? __ldg(p.indices + (int64_t)ti.t * p.K + k) : -1;
       }
@@ -267,48 +367,116 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int b4 = tl & 3;
       if (tl >= 4 && !SMLA_WAIT(kBarIdxEmpty + b4, ((tl >> 2) + 1) & 1)) break;
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
+      for (int i = 0; i < 2; ++i)
         slots_ring[b4 * kRows + lane + 32 * i] = translate_slot(cur[i], req_cur, p.block_table, p.R, p.MB, p.NB);
       mbar_arrive(&bars[kBarIdxFull + b4]);
+      if (lane == 0) SMLA_TRACE_SET(tl, kEvIdx);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) cur[i] = nxt[i];
+      for (int i = 0; i < 2; ++i) cur[i] = nxt[i];
       req_cur = req_nxt;
     }
-  } else if (warp == kTmaWarp) {
-    // ------------------------------------------------------------ TMA producer
-    // Lane l gathers rows 4l..4l+3 of each tile: the four 128-code panels, the
-    // RoPE values and the scales.  Invalid rows use row coordinate -1, which
-    // the tensor map fills with zeros.
-    const uint32_t kv0 = smem_u32(smem + kOffKv);
-    const int r = 4 * lane;
-    const uint32_t roff = (uint32_t)((r >> 3) * 1024 + (r & 7) * 128);
-    for (int tl = 0; tl < n_local; ++tl) {
-      const int b = tl & 1, b4 = tl & 3;
-      if (!SMLA_WAIT(kBarIdxFull + b4, (tl >> 2) & 1)) break;
-      if (tl >= 2 && !SMLA_WAIT(kBarKvEmpty + b, ((tl >> 1) + 1) & 1)) break;
-      const int4 s = *reinterpret_cast<const int4*>(slots_ring + b4 * kRows + r);
-      *reinterpret_cast<uint32_t*>(valid + b * kRows + r) =
-          (s.x >= 0 ? 1u : 0u) | (s.y >= 0 ? 1u << 8 : 0u) | (s.z >= 0 ? 1u << 16 : 0u) | (s.w >= 0 ? 1u << 24 : 0u);
+  } else if (warp == kProdWarp) {
+    // ------------------------------------------------------------ bulk-copy producer
+    // Raw stage s holds rows 32 (s % 2) .. +31 of tile s / 2.  Lane l issues
+    // the 656-byte copy of the stage's row l when its slot is valid.
+    int issued = 0;
+    for (int s = 0; s < 2 * n_local; ++s) {
+      const int tl = s >> 1, b4 = tl & 3, rs = s % kRawStages;
+      if ((s & 1) == 0 && !SMLA_WAIT(kBarIdxFull + b4, (tl >> 2) & 1)) break;
+      if (s >= kRawStages && !SMLA_WAIT(kBarRawEmpty + rs, ((s / kRawStages) + 1) & 1)) break;
+      const int32_t slot = slots_ring[b4 * kRows + kRawRows * (s & 1) + lane];
+      raw_meta[rs * kRawRows + lane] = slot;
+      const uint32_t nvalid = __popc(__ballot_sync(kFullMask, slot >= 0));
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive_expect_tx(&bars[kBarKvFull + b], kRows * (512 + 128 + 16));
-        mbar_arrive(&bars[kBarIdxEmpty + b4]);  // slots copied to registers
+        mbar_arrive_expect_tx(&bars[kBarRawFull + rs], nvalid * kRowBytes);
+        if (s & 1) mbar_arrive(&bars[kBarIdxEmpty + b4]);  // both halves' slots read
       }
       __syncwarp();
-      const uint32_t kv = kv0 + b * kKvBuf;
-#pragma unroll
-      for (int pn = 0; pn < 4; ++pn)
-        tma_gather4(kv + pn * kPanel + roff, &map_row, 128 * pn, s.x, s.y, s.z, s.w, &bars[kBarKvFull + b]);
-      tma_gather4(kv + kKvRope + roff, &map_row, kRopeOff, s.x, s.y, s.z, s.w, &bars[kBarKvFull + b]);
-      tma_gather4(kv + kKvScale + lane * 128, &map_scale, kScaleOff, s.x, s.y, s.z, s.w, &bars[kBarKvFull + b]);
+      if (slot >= 0)
+        bulk_g2s(smem + kOffRaw + rs * kRawStage + lane * kRowBytes, p.cache + (int64_t)slot * kRowBytes, kRowBytes,
+                 &bars[kBarRawFull + rs]);
+      issued = s + 1;
+      if (lane == 0 && (s & 1) == 0) SMLA_TRACE_SET(tl, kEvIssue);
     }
-  } else if (warp >= kQWarp0) {
+    // No copy may still be landing in shared memory when the CTA exits (only
+    // possible after an abort; the consumers have waited for every stage otherwise).
+    for (int s = issued > kRawStages ? issued - kRawStages : 0; s < issued; ++s)
+      mbar_wait_drain(&bars[kBarRawFull + s % kRawStages], (s / kRawStages) & 1);
+  } else if (warp >= kRearrWarp0 && warp < kRearrWarp0 + kRearrWarps) {
+    // ------------------------------------------------------------ rearrange raw rows -> operand tile
+    // Warp rw handles the raw stage of tile rows 32 rw .. 32 rw + 31, in
+    // batches of 8 rows.  Lane l moves code chunk l (bytes 16l..16l+15) of
+    // each row to panel l/8 at its swizzled position.  The 9-chunk tails
+    // (4 scales, then 8 RoPE chunks) of the batch's 8 rows are 72 moves spread
+    // over three rounds of the 32 lanes; idle lanes store to a private sink.
+    // Everything is branch-free so that a batch's loads are all in flight
+    // before its stores; invalid rows are zero-filled by selects.
+    const int rw = warp - kRearrWarp0;
+    const int chunk = lane & 7, panel = lane >> 3;
+    int tail_j[3], tail_k[3];
+    bool tail_on[3];
+#pragma unroll
+    for (int q = 0; q < 3; ++q) {
+      const int sidx = 32 * q + lane;
+      tail_on[q] = sidx < 72;
+      tail_j[q] = tail_on[q] ? sidx / 9 : 0;
+      tail_k[q] = tail_on[q] ? sidx % 9 : 0;
+    }
+    const uint32_t sink = smem_u32(smem + kOffDummy + (rw * 32 + lane) * 16);
+    for (int tl = 0; tl < n_local; ++tl) {
+      const int b = tl & 1;
+      const int s = 2 * tl + rw, rs = s % kRawStages;
+      if (!SMLA_WAIT(kBarRawFull + rs, (s / kRawStages) & 1)) break;
+      if (lane == 0 && rw == 0) SMLA_TRACE_SET(tl, kEvRawFull);
+      if (tl >= 2 && !SMLA_WAIT(kBarOpEmpty + b, ((tl >> 1) + 1) & 1)) break;
+      if (lane == 0 && rw == 0) SMLA_TRACE_SET(tl, kEvOpEmpty);
+      const uint32_t op = smem_u32(smem + kOffOp + b * kOpBuf);
+      const uint32_t raw = smem_u32(smem + kOffRaw + rs * kRawStage);
+      const uint32_t vmask = __ballot_sync(kFullMask, raw_meta[rs * kRawRows + lane] >= 0);
+#pragma unroll 1
+      for (int i0 = 0; i0 < kRawRows; i0 += 8) {
+        uint4 c[8], t[3];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) c[j] = lds128(raw + (i0 + j) * kRowBytes + 16 * lane);
+#pragma unroll
+        for (int q = 0; q < 3; ++q) t[q] = lds128(raw + (i0 + tail_j[q]) * kRowBytes + kScaleOff + 16 * tail_k[q]);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int r = kRawRows * rw + i0 + j;
+          const bool v = (vmask >> (i0 + j)) & 1u;
+          const uint4 x = v ? c[j] : make_uint4(0u, 0u, 0u, 0u);
+          sts128(op + panel * kPanel + (uint32_t)((r >> 3) * 1024 + (r & 7) * 128) + ((chunk ^ (r & 7)) << 4), x);
+        }
+#pragma unroll
+        for (int q = 0; q < 3; ++q) {
+          const int r = kRawRows * rw + i0 + tail_j[q];
+          const bool v = (vmask >> (i0 + tail_j[q])) & 1u;
+          const uint4 x = v ? t[q] : make_uint4(0u, 0u, 0u, 0u);
+          const uint32_t rope_dst =
+              op + kOpRope + (uint32_t)((r >> 3) * 1024 + (r & 7) * 128) + ((((tail_k[q] + 7) & 7) ^ (r & 7)) << 4);
+          const uint32_t dst = !tail_on[q] ? sink : (tail_k[q] == 0 ? op + kOpScale + 16 * r : rope_dst);
+          sts128(dst, x);
+        }
+      }
+      valid[b * kRows + kRawRows * rw + lane] = (uint8_t)((vmask >> lane) & 1u);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&bars[kBarRawEmpty + rs]);
+        mbar_arrive(&bars[kBarOpFull + b]);
+        if (rw == 0) SMLA_TRACE_SET(tl, kEvRawLanded);
+      }
+    }
+  } else if (warp >= kQWarp0 && warp < kQWarp0 + kQWarps) {
     // ------------------------------------------------------------ Q preparation
-    // 8 threads per head: thread part owns NoPE columns [64 part, 64 part + 64)
-    // and RoPE chunk `part`.  q * 2^s_h = hi + lo in e4m3 with s_h chosen so
-    // that max |q * 2^s_h| <= 448.
-    const int qt = tid - 32 * kQWarp0;  // 0..127
-    const int h = qt >> 3, part = qt & 7;
+    // 4 threads per head: thread part owns NoPE columns [128 part, 128 part +
+    // 128) (code panel `part`) and RoPE chunks 2 part, 2 part + 1.  Head h is
+    // stored in operand row q_row_of_head(h) (hi) and 16 + that row (lo).
+    // q * 2^s_h = hi + lo in e4m3 with s_h chosen so that max |q * 2^s_h| <= 448.
+    const int qt = tid - 32 * kQWarp0;  // 0..63
+    const int h = qt >> 2, part = qt & 3;
+    const int qrow = q_row_of_head(h);
     int seg = 0;
     for (int tl = 0; tl < n_local; ++tl) {
       const TileInfo ti = tile_info(p, xbeg + tl, xbeg, xend);
@@ -316,13 +484,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int qb = seg & 1;
       if (seg >= 2 && !SMLA_WAIT(kBarQEmpty + qb, ((seg >> 1) + 1) & 1)) break;
       const uint4* src = reinterpret_cast<const uint4*>(p.q + ((int64_t)ti.t * p.H + ti.hg * HG + h) * kDqk);
-      uint4 v[8];
+      uint4 v[16];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] = __ldg(src + 8 * part + i);
-      const uint4 rope = __ldg(src + 64 + part);
+      for (int i = 0; i < 16; ++i) v[i] = __ldg(src + 16 * part + i);
+      const uint4 rope0 = __ldg(src + 64 + 2 * part), rope1 = __ldg(src + 64 + 2 * part + 1);
       float amax = 0.f;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
+      for (int i = 0; i < 16; ++i) {
         const uint32_t w4[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
 #pragma unroll
         for (int k = 0; k < 4; ++k)
@@ -330,7 +498,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 1));
       amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 2));
-      amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 4));
       int sh = 0;
       if (amax > 0.f) {
         int e;
@@ -338,13 +505,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         sh = e - 1;
       }
       const float pre = ldexpf(1.f, sh);
-      const uint32_t qs = smem_u32(smem + kOffQ + qb * kQBuf);
-      // codes for columns 64 part .. 64 part + 63: panel part / 2, chunks 4 (part % 2) .. +3
-      const int pn = part >> 1;
+      const uint32_t qpanel = smem_u32(smem + kOffQ + qb * kQBuf + part * kQPanel);
 #pragma unroll
-      for (int i = 0; i < 8; i += 2) {  // 16 columns per chunk = two uint4 of bf16
+      for (int ch = 0; ch < 8; ++ch) {  // 16 codes per chunk = two uint4 of bf16
         uint32_t hi[4], lo[4];
-        const uint32_t w8[8] = {v[i].x, v[i].y, v[i].z, v[i].w, v[i + 1].x, v[i + 1].y, v[i + 1].z, v[i + 1].w};
+        const uint32_t w8[8] = {v[2 * ch].x,     v[2 * ch].y,     v[2 * ch].z,     v[2 * ch].w,
+                                v[2 * ch + 1].x, v[2 * ch + 1].y, v[2 * ch + 1].z, v[2 * ch + 1].w};
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           uint32_t h0, l0, h1, l1;
@@ -353,85 +519,96 @@ __global__ void __launch_bounds__(kThreads, 1)
           hi[k] = h0 | (h1 << 16);
           lo[k] = l0 | (l1 << 16);
         }
-        const int ch = 4 * (part & 1) + (i >> 1);
-        sts128(qs + pn * kQPanel + sw128_chunk(32, h, ch) - (ch >> 3) * 32 * 128,
-               make_uint4(hi[0], hi[1], hi[2], hi[3]));
-        sts128(qs + pn * kQPanel + sw128_chunk(32, 16 + h, ch) - (ch >> 3) * 32 * 128,
-               make_uint4(lo[0], lo[1], lo[2], lo[3]));
+        sts128(qpanel + sw128_chunk(32, qrow, ch), make_uint4(hi[0], hi[1], hi[2], hi[3]));
+        sts128(qpanel + sw128_chunk(32, 16 + qrow, ch), make_uint4(lo[0], lo[1], lo[2], lo[3]));
       }
-      sts128(qs + kQRope + sw128_chunk(HG, h, part), rope);
+      const uint32_t qrope = smem_u32(smem + kOffQ + qb * kQBuf + kQRope);
+      sts128(qrope + sw128_chunk(HG, qrow, 2 * part), rope0);
+      sts128(qrope + sw128_chunk(HG, qrow, 2 * part + 1), rope1);
       if (part == 0) pre_ring[(seg & 3) * HG + h] = ldexpf(1.f, -sh);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[kBarQFull + qb]);
+      if (qt == 0) SMLA_TRACE_SET(tl, kEvQReady);
       ++seg;
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ tensor-core issuer
+    // Polls (never blocks on) the next operand tile + Q block for QK^T (up to
+    // two tiles ahead of P.V, one per S buffer) and the next P' for P.V.
     if (lane == 0 && n_local > 0) {
-      constexpr uint32_t id_qk8 = idesc_e4m3(128, 32, 0, 0);
-      constexpr uint32_t id_qkr = make_idesc_bf16(128, HG, 0, 0);
+      constexpr uint32_t id_qk8 = idesc_e4m3(64, 32, 0, 0);
+      constexpr uint32_t id_qkr = make_idesc_bf16(64, HG, 0, 0);
       constexpr uint32_t id_pv = idesc_e4m3(128, 32, 1, 1);
-      const uint32_t kv0 = smem_u32(smem + kOffKv), q0 = smem_u32(smem + kOffQ), p0 = smem_u32(smem + kOffP);
+      const uint32_t op0 = smem_u32(smem + kOffOp), q0 = smem_u32(smem + kOffQ), p0 = smem_u32(smem + kOffP);
       int seg_q = 0, seg_o = 0, next_qk = 0, next_pv = 0;
+      // top-k tile index within its unit of the next QK^T / P.V tile (advanced
+      // incrementally: no divisions in the polling loop)
+      const int kt0 = (int)(xbeg % p.nt);
+      int kt_qk = kt0, kt_pv = kt0;
       uint64_t t_idle = 0;
       while (next_pv < n_local) {
         bool progressed = false;
         if (next_qk < n_local && next_qk < next_pv + 2) {
           const int tl = next_qk;
-          const TileInfo ti = tile_info(p, xbeg + tl, xbeg, xend);
+          const bool seg_start = tl == 0 || kt_qk == 0;
+          const bool seg_end = tl == n_local - 1 || kt_qk == p.nt - 1;
           const int b = tl & 1;
-          const int seg = ti.seg_start ? seg_q : seg_q - 1;
+          const int seg = seg_start ? seg_q : seg_q - 1;
           const int qb = seg & 1;
-          const bool q_ok = !ti.seg_start || mbar_test_wait(&bars[kBarQFull + qb], (seg >> 1) & 1);
-          if (q_ok && mbar_test_wait(&bars[kBarKvFull + b], (tl >> 1) & 1)) {
-            if (ti.seg_start) ++seg_q;
+          const bool q_ok = !seg_start || mbar_test_wait(&bars[kBarQFull + qb], (seg >> 1) & 1);
+          if (q_ok && mbar_test_wait(&bars[kBarOpFull + b], (tl >> 1) & 1)) {
+            if (seg_start) ++seg_q;
             tc_fence_after();
-            const uint32_t kv = kv0 + b * kKvBuf, qs = q0 + qb * kQBuf;
+            const uint32_t op = op0 + b * kOpBuf, qs = q0 + qb * kQBuf;
             const uint32_t sb = tmem + b * kSCols;
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
 #pragma unroll
               for (int k = 0; k < 4; ++k) {
-                const uint64_t da = make_sdesc(kv + g * kPanel + 32 * k, 16, 1024, kLayoutSw128);
+                const uint64_t da = make_sdesc(op + g * kPanel + 32 * k, 16, 1024, kLayoutSw128);
                 const uint64_t db = make_sdesc(qs + g * kQPanel + 32 * k, 16, 1024, kLayoutSw128);
                 mma_f8(sb + 32 * g, da, db, id_qk8, k > 0 ? 1u : 0u);
               }
             }
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-              const uint64_t da = make_sdesc(kv + kKvRope + 32 * k, 16, 1024, kLayoutSw128);
+              const uint64_t da = make_sdesc(op + kOpRope + 32 * k, 16, 1024, kLayoutSw128);
               const uint64_t db = make_sdesc(qs + kQRope + 32 * k, 16, 1024, kLayoutSw128);
               mma_ss(sb + 128, da, db, id_qkr, k > 0 ? 1u : 0u);
             }
             mma_commit(&bars[kBarSFull + b]);
-            if (ti.seg_end) mma_commit(&bars[kBarQEmpty + qb]);
+            if (seg_end) mma_commit(&bars[kBarQEmpty + qb]);
+            SMLA_TRACE_SET(tl, kEvQk);
             ++next_qk;
+            kt_qk = kt_qk + 1 == p.nt ? 0 : kt_qk + 1;
             progressed = true;
           }
         }
         if (next_pv < next_qk) {
           const int tl = next_pv;
-          const TileInfo ti = tile_info(p, xbeg + tl, xbeg, xend);
+          const bool seg_start = tl == 0 || kt_pv == 0;
           const int b = tl & 1;
-          const bool o_ok = !ti.seg_start || seg_o == 0 || mbar_test_wait(&bars[kBarOFree], (seg_o - 1) & 1);
+          const bool o_ok = !seg_start || seg_o == 0 || mbar_test_wait(&bars[kBarOFree], (seg_o - 1) & 1);
           if (o_ok && mbar_test_wait(&bars[kBarPFull], tl & 1)) {
-            if (ti.seg_start) ++seg_o;
+            if (seg_start) ++seg_o;
             tc_fence_after();
-            const uint32_t kv = kv0 + b * kKvBuf;
+            const uint32_t op = op0 + b * kOpBuf;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
 #pragma unroll
-              for (int k = 0; k < 4; ++k) {
+              for (int k = 0; k < 2; ++k) {
                 // A = codes^T (value column c x row j), MN-major; B = P'_q (row j x 32), MN-major
-                const uint64_t da = make_sdesc(kv + q * kPanel + 4096 * k, kPanel, 1024, kLayoutSw128);
+                const uint64_t da = make_sdesc(op + q * kPanel + 4096 * k, kPanel, 1024, kLayoutSw128);
                 const uint64_t db = make_sdesc(p0 + q * kPGroup + 1024 * k, 256, 128, kLayoutNone);
-                mma_f8(tmem + kOCol + 32 * q, da, db, id_pv, (ti.seg_start && k == 0) ? 0u : 1u);
+                mma_f8(tmem + kOCol + 32 * q, da, db, id_pv, (seg_start && k == 0) ? 0u : 1u);
               }
             }
-            mma_commit(&bars[kBarKvEmpty + b]);
+            mma_commit(&bars[kBarOpEmpty + b]);
             mma_commit(&bars[kBarPvDone]);
+            SMLA_TRACE_SET(tl, kEvPv);
             ++next_pv;
+            kt_pv = kt_pv + 1 == p.nt ? 0 : kt_pv + 1;
             progressed = true;
           }
         }
@@ -439,6 +616,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           t_idle = 0;
         } else {
           if (*abort_flag) break;
+          __nanosleep(32);
           const uint64_t now = globaltimer_ns();
           if (t_idle == 0) {
             t_idle = now;
@@ -449,202 +627,282 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      // every issued tensor-core operation completes before tensor memory is released
+      if (next_qk > 0) {
+        mma_commit(&bars[kBarDrain]);
+        mbar_wait_drain(&bars[kBarDrain], 0);
+      }
     }
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax / epilogue (warps 0..3)
+    // QK^T with M = 64 leaves tile row r in TMEM lane 32 (r / 16) + r % 16.
+    // Read with the 16x256b shape (and the Q row order of q_row_of_head),
+    // thread (w, lane) holds rows r0 = 16 w + lane / 4 and r1 = r0 + 8 for
+    // heads 4c .. 4c + 3 (c = lane % 4): item k (0..7) is row rho = (k >> 1) & 1
+    // of head 4c + i, i = (k & 1) + 2 (k >> 2).  Each thread keeps the running
+    // state of its 4 heads; the 16 heads are gathered by shuffles only where
+    // the P.V accumulator is rescaled.  For the P.V output (M = 128) thread tid
+    // owns value column tid of each chunk.
     const int w = warp;
-    const int j = tid;  // tile row of this thread's TMEM lane; also the value column within a chunk
+    const int c4 = lane & 3;
+    const int r0 = 16 * w + (lane >> 2), r1 = r0 + 8;
     const uint32_t lane_base = (uint32_t)(32 * w) << 16;
     const uint32_t p0 = smem_u32(smem + kOffP);
     float* red_max = reinterpret_cast<float*>(smem + kOffRedMax);
     float* red_sc = reinterpret_cast<float*>(smem + kOffRedSc);
     float* red_sum = reinterpret_cast<float*>(smem + kOffRedSum);
-    float m_used[HG], l_part[HG], ip[HG], Rq[4];
+    float m4[4], l4[4], ip4[4], Rq[4];
+    SMLA_CLK_DECL;
     int seg = -1, seg_first_kt = 0, n_seg_tiles = 0;
     bool dead = false;
+    // waits of this role keep `dead` warp-uniform: the tensor-memory accesses
+    // and shuffles it guards are warp-collective
+    auto wait_s = [&](int bar_idx, uint32_t parity) {
+      if (!dead) dead = !SMLA_WAIT(bar_idx, parity);
+      dead = __any_sync(kFullMask, dead);
+    };
     for (int tl = 0; tl < n_local; ++tl) {
       const TileInfo ti = tile_info(p, xbeg + tl, xbeg, xend);
       const int b = tl & 1;
       if (ti.seg_start) {
         ++seg;
 #pragma unroll
-        for (int h = 0; h < HG; ++h) {
-          m_used[h] = -INFINITY;
-          l_part[h] = 0.f;
+        for (int i = 0; i < 4; ++i) {
+          m4[i] = -INFINITY;
+          l4[i] = 0.f;
+          Rq[i] = 0.f;
         }
-#pragma unroll
-        for (int g = 0; g < 4; ++g) Rq[g] = 0.f;
         seg_first_kt = ti.kt;
         n_seg_tiles = 0;
       }
-      if (!dead) dead = !SMLA_WAIT(kBarSFull + b, (tl >> 1) & 1);
-      if (!dead) dead = !SMLA_WAIT(kBarKvFull + b, (tl >> 1) & 1);  // row flags and scales
+      wait_s(kBarOpFull + b, (tl >> 1) & 1);  // row flags and scales
+      if (tid == 0) SMLA_TRACE_SET(tl, kEvOpFull);
+      wait_s(kBarSFull + b, (tl >> 1) & 1);
+      if (tid == 0) SMLA_TRACE_SET(tl, kEvSoftStart);
+      SMLA_CLK_START();
       tc_fence_after();
       if (ti.seg_start) {
-#pragma unroll
-        for (int h = 0; h < HG; ++h) ip[h] = pre_ring[(seg & 3) * HG + h];
+        const float4 v = *reinterpret_cast<const float4*>(pre_ring + (seg & 3) * HG + 4 * c4);
+        ip4[0] = v.x;
+        ip4[1] = v.y;
+        ip4[2] = v.z;
+        ip4[3] = v.w;
       }
-      const bool row_ok = !dead && valid[b * kRows + j] != 0;
-      float sc[4];
-      {
-        const float4 v4 =
-            *reinterpret_cast<const float4*>(smem + kOffKv + b * kKvBuf + kKvScale + (j >> 2) * 128 + (j & 3) * 16);
-        sc[0] = row_ok ? v4.x : 0.f;
-        sc[1] = row_ok ? v4.y : 0.f;
-        sc[2] = row_ok ? v4.z : 0.f;
-        sc[3] = row_ok ? v4.w : 0.f;
-      }
+      const bool ok0 = !dead && valid[b * kRows + r0] != 0;
+      const bool ok1 = !dead && valid[b * kRows + r1] != 0;
+      const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
+      const float4 s0 = ok0 ? *reinterpret_cast<const float4*>(smem + kOffOp + b * kOpBuf + kOpScale + 16 * r0) : zero4;
+      const float4 s1 = ok1 ? *reinterpret_cast<const float4*>(smem + kOffOp + b * kOpBuf + kOpScale + 16 * r1) : zero4;
+      const float sc0[4] = {s0.x, s0.y, s0.z, s0.w};
+      const float sc1[4] = {s1.x, s1.y, s1.z, s1.w};
       // logits (log2 units): 2^-s_h sum_g scale_g (S_g,hi + S_g,lo) + S_rope
-      float sl[HG];
+      float sl[8];
       {
         const uint32_t sa = tmem + lane_base + b * kSCols;
-        float acc[HG];
+        float acc[8];
 #pragma unroll
-        for (int h = 0; h < HG; ++h) acc[h] = 0.f;
+        for (int k = 0; k < 8; ++k) acc[k] = 0.f;
         if (!dead) {
+          uint32_t hi[4][8], lo[4][8], rp[8];
 #pragma unroll
           for (int g = 0; g < 4; ++g) {
-            uint32_t hi[16], lo[16];
-            tmem_ld16(sa + 32 * g, hi);
-            tmem_ld16(sa + 32 * g + 16, lo);
-            tmem_ld_wait();
-            reg_fence16(hi);
-            reg_fence16(lo);
-#pragma unroll
-            for (int h = 0; h < HG; ++h) acc[h] = fmaf(sc[g], __uint_as_float(hi[h]) + __uint_as_float(lo[h]), acc[h]);
+            tmem_ld_16x256b_x2(sa + 32 * g, hi[g]);
+            tmem_ld_16x256b_x2(sa + 32 * g + 16, lo[g]);
           }
-          uint32_t rp[16];
-          tmem_ld16_sync(sa + 128, rp);
+          tmem_ld_16x256b_x2(sa + 128, rp);
+          tmem_ld_wait();
 #pragma unroll
-          for (int h = 0; h < HG; ++h) acc[h] = fmaf(acc[h], ip[h], __uint_as_float(rp[h]));
+          for (int g = 0; g < 4; ++g) {
+            reg_fence8(hi[g]);
+            reg_fence8(lo[g]);
+          }
+          reg_fence8(rp);
+#pragma unroll
+          for (int g = 0; g < 4; ++g)
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              acc[k] = fmaf(((k >> 1) & 1) ? sc1[g] : sc0[g], __uint_as_float(hi[g][k]) + __uint_as_float(lo[g][k]),
+                            acc[k]);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) acc[k] = fmaf(acc[k], ip4[(k & 1) + 2 * (k >> 2)], __uint_as_float(rp[k]));
         }
 #pragma unroll
-        for (int h = 0; h < HG; ++h) sl[h] = row_ok ? acc[h] * p.scale_log2 : -INFINITY;
+        for (int k = 0; k < 8; ++k) sl[k] = (((k >> 1) & 1) ? ok1 : ok0) ? acc[k] * p.scale_log2 : -INFINITY;
       }
-      // tile maxima: per head (logits) and per scale group (scales), across the 128 rows
+      if (tid == 0) SMLA_TRACE_SET(tl, kEvSoftLogits);
+      SMLA_CLK_MARK(0);
+      // tile maxima: per head (logits) and per scale group (scales), across the 64 rows
       float* redm = red_max + (tl & 1) * 4 * HG;
       float* reds = red_sc + (tl & 1) * 4 * 4;
       {
-        float v[16];
+        float t4[4];
 #pragma unroll
-        for (int h = 0; h < HG; ++h) v[h] = sl[h];
-        const float mx = warp_reduce16<true>(v, lane);
-        if ((lane & 1) == 0) redm[w * HG + (lane >> 1)] = mx;
-        float s4[4] = {sc[0], sc[1], sc[2], sc[3]};
+        for (int i = 0; i < 4; ++i) {
+          const int k = (i & 1) + 4 * (i >> 1);  // row r0 item of head slot i; row r1 item is k + 2
+          t4[i] = fmaxf(sl[k], sl[k + 2]);
+        }
+        float s4[4];
 #pragma unroll
-        for (int off = 16; off >= 1; off >>= 1)
+        for (int g = 0; g < 4; ++g) s4[g] = fmaxf(sc0[g], sc1[g]);
 #pragma unroll
-          for (int g = 0; g < 4; ++g) s4[g] = fmaxf(s4[g], __shfl_xor_sync(kFullMask, s4[g], off));
-        if (lane == 0)
+        for (int off = 4; off <= 16; off <<= 1)
 #pragma unroll
-          for (int g = 0; g < 4; ++g) reds[w * 4 + g] = s4[g];
+          for (int i = 0; i < 4; ++i) {
+            t4[i] = fmaxf(t4[i], __shfl_xor_sync(kFullMask, t4[i], off));
+            s4[i] = fmaxf(s4[i], __shfl_xor_sync(kFullMask, s4[i], off));
+          }
+        if (lane < 4) *reinterpret_cast<float4*>(redm + w * HG + 4 * c4) = make_float4(t4[0], t4[1], t4[2], t4[3]);
+        if (lane == 0) *reinterpret_cast<float4*>(reds + w * 4) = make_float4(s4[0], s4[1], s4[2], s4[3]);
       }
       named_bar_sync(1, 128);
-      bool rescale = false;
-      float alpha[HG], beta[4];
+      if (tid == 0) SMLA_TRACE_SET(tl, kEvSoftBar);
+      SMLA_CLK_MARK(1);
+      // running maxima of the own heads (lazy: refreshed only when the tile
+      // maximum exceeds them by more than kMaxSlack) and power-of-two bounds
+      // of the scale groups
+      float alpha4[4], beta[4];
+      bool up_any = false, rq_changed = false;
+      {
+        float4 a[4], c[4];
 #pragma unroll
-      for (int h = 0; h < HG; ++h) {
-        const float tmax = fmaxf(fmaxf(redm[h], redm[HG + h]), fmaxf(redm[2 * HG + h], redm[3 * HG + h]));
-        const float nm = fmaxf(m_used[h], tmax);
-        alpha[h] = 1.f;
-        if (nm > m_used[h] + kMaxSlack) {
-          alpha[h] = exp2f(m_used[h] - nm);
-          m_used[h] = nm;
-          rescale = true;
+        for (int v = 0; v < 4; ++v) {
+          a[v] = *reinterpret_cast<const float4*>(redm + v * HG + 4 * c4);
+          c[v] = *reinterpret_cast<const float4*>(reds + 4 * v);
         }
-        l_part[h] *= alpha[h];
-      }
+        const float tmax[4] = {fmaxf(fmaxf(a[0].x, a[1].x), fmaxf(a[2].x, a[3].x)),
+                               fmaxf(fmaxf(a[0].y, a[1].y), fmaxf(a[2].y, a[3].y)),
+                               fmaxf(fmaxf(a[0].z, a[1].z), fmaxf(a[2].z, a[3].z)),
+                               fmaxf(fmaxf(a[0].w, a[1].w), fmaxf(a[2].w, a[3].w))};
+        const float smax[4] = {fmaxf(fmaxf(c[0].x, c[1].x), fmaxf(c[2].x, c[3].x)),
+                               fmaxf(fmaxf(c[0].y, c[1].y), fmaxf(c[2].y, c[3].y)),
+                               fmaxf(fmaxf(c[0].z, c[1].z), fmaxf(c[2].z, c[3].z)),
+                               fmaxf(fmaxf(c[0].w, c[1].w), fmaxf(c[2].w, c[3].w))};
 #pragma unroll
-      for (int g = 0; g < 4; ++g) {
-        const float smax = fmaxf(fmaxf(reds[g], reds[4 + g]), fmaxf(reds[8 + g], reds[12 + g]));
-        beta[g] = 1.f;
-        if (smax > Rq[g]) {
-          const float rn = pow2_ceil(smax);
-          if (Rq[g] > 0.f) {
-            beta[g] = Rq[g] / rn;
-            rescale = true;
-          }
+        for (int i = 0; i < 4; ++i) {
+          const float nm = fmaxf(m4[i], tmax[i]);
+          const bool up = nm > m4[i] + kMaxSlack;
+          alpha4[i] = up ? ex2_approx(m4[i] - nm) : 1.f;
+          m4[i] = up ? nm : m4[i];
+          l4[i] *= alpha4[i];
+          up_any |= up;
+        }
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const bool grow = smax[g] > Rq[g];
+          const float rn = grow ? pow2_ceil(smax[g]) : Rq[g];
+          beta[g] = (grow && Rq[g] > 0.f) ? Rq[g] * rcp_pow2(rn) : 1.f;
+          rq_changed |= grow && Rq[g] > 0.f;
           Rq[g] = rn;
         }
       }
-      if (rescale && n_seg_tiles > 0 && !dead) {
+      // every warp sees all 16 heads (lanes 0..3) and the same shared maxima: the decision is CTA-uniform
+      const bool rescale = __any_sync(kFullMask, up_any) || rq_changed;
+      SMLA_CLK_MARK(2);
+      if (rescale && n_seg_tiles > 0) {
         // O^T holds this segment's earlier P.V: wait for the latest and rescale in place
-        dead = !SMLA_WAIT(kBarPvDone, (tl - 1) & 1);
+        float alpha[HG];
+#pragma unroll
+        for (int h = 0; h < HG; ++h) alpha[h] = __shfl_sync(kFullMask, alpha4[h & 3], h >> 2);
+        wait_s(kBarPvDone, (tl - 1) & 1);
         if (!dead) {
           tc_fence_after();
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
+            uint32_t oh[16], ol[16];
+            const uint32_t addr = tmem + lane_base + kOCol + 32 * q;
+            tmem_ld16(addr, oh);
+            tmem_ld16(addr + 16, ol);
+            tmem_ld_wait();
+            reg_fence16(oh);
+            reg_fence16(ol);
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-              uint32_t o[16];
-              const uint32_t addr = tmem + lane_base + kOCol + 32 * q + 16 * half;
-              tmem_ld16_sync(addr, o);
-#pragma unroll
-              for (int h = 0; h < HG; ++h) o[h] = __float_as_uint(__uint_as_float(o[h]) * alpha[h] * beta[q]);
-              tmem_st16(addr, o);
+            for (int h = 0; h < HG; ++h) {
+              const float f = alpha[h] * beta[q];
+              oh[h] = __float_as_uint(__uint_as_float(oh[h]) * f);
+              ol[h] = __float_as_uint(__uint_as_float(ol[h]) * f);
             }
+            tmem_st16(addr, oh);
+            tmem_st16(addr + 16, ol);
           }
           tmem_st_wait();
         }
       }
-      // probabilities, running sums, P'_q = p * scale_q / R_q as e4m3 hi + lo
-      float pr[HG];
+      SMLA_CLK_MARK(3);
+      // probabilities and running sums
+      float pr[8];
 #pragma unroll
-      for (int h = 0; h < HG; ++h) {
-        pr[h] = row_ok ? exp2f(sl[h] - m_used[h]) : 0.f;
-        l_part[h] += pr[h];
+      for (int k = 0; k < 8; ++k) {
+        const int i = (k & 1) + 2 * (k >> 2);
+        pr[k] = (((k >> 1) & 1) ? ok1 : ok0) ? ex2_approx(sl[k] - m4[i]) : 0.f;
+        l4[i] += pr[k];
       }
-      if (tl >= 1 && !dead) dead = !SMLA_WAIT(kBarPvDone, (tl - 1) & 1);  // P buffer free
+      SMLA_CLK_MARK(4);
+      if (tl >= 1) wait_s(kBarPvDone, (tl - 1) & 1);  // P buffer free
+      if (tid == 0) SMLA_TRACE_SET(tl, kEvSoftPWait);
+      SMLA_CLK_MARK(5);
+      // P'_q = kPScale * p * scale_q / R_q as e4m3 hi + lo: MN-major core
+      // matrices of 8 rows x 16 codes (heads), hi and lo blocks 128 B apart,
+      // row blocks 256 B apart
       if (!dead) {
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
-          const float f = Rq[g] > 0.f ? kPScale * sc[g] / Rq[g] : 0.f;
-          uint32_t hi[4], lo[4];
+          const float inv_r = Rq[g] > 0.f ? kPScale * rcp_pow2(Rq[g]) : 0.f;
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            uint32_t h0, l0, h1, l1;
-            split2(pr[4 * k] * f, pr[4 * k + 1] * f, h0, l0);
-            split2(pr[4 * k + 2] * f, pr[4 * k + 3] * f, h1, l1);
-            hi[k] = h0 | (h1 << 16);
-            lo[k] = l0 | (l1 << 16);
+          for (int rho = 0; rho < 2; ++rho) {
+            const int r = rho ? r1 : r0;
+            const float f = (rho ? sc1[g] : sc0[g]) * inv_r;
+            uint32_t hw, lw;
+            split4(pr[2 * rho] * f, pr[2 * rho + 1] * f, pr[4 + 2 * rho] * f, pr[5 + 2 * rho] * f, hw, lw);
+            const uint32_t base = p0 + g * kPGroup + (r >> 3) * 256 + (r & 7) * 16 + 4 * c4;
+            sts32(base, hw);
+            sts32(base + 128, lw);
           }
-          // MN-major core matrices: 8 rows x 16 codes; code blocks 128 B apart, row blocks 256 B apart
-          const uint32_t base = p0 + g * kPGroup + (j >> 3) * 256 + (j & 7) * 16;
-          sts128(base, make_uint4(hi[0], hi[1], hi[2], hi[3]));
-          sts128(base + 128, make_uint4(lo[0], lo[1], lo[2], lo[3]));
         }
       }
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0 && !dead) mbar_arrive(&bars[kBarPFull]);
+      if (tid == 0) SMLA_TRACE_SET(tl, kEvSoftDone);
+      SMLA_CLK_MARK(6);
       ++n_seg_tiles;
 
       if (ti.seg_end) {
         {
-          float v[16];
+          float v4[4] = {l4[0], l4[1], l4[2], l4[3]};
 #pragma unroll
-          for (int h = 0; h < HG; ++h) v[h] = l_part[h];
-          const float sm = warp_reduce16<false>(v, lane);
-          if ((lane & 1) == 0) red_sum[w * HG + (lane >> 1)] = sm;
+          for (int off = 4; off <= 16; off <<= 1)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) v4[i] += __shfl_xor_sync(kFullMask, v4[i], off);
+          if (lane < 4) *reinterpret_cast<float4*>(red_sum + w * HG + 4 * c4) = make_float4(v4[0], v4[1], v4[2], v4[3]);
         }
         named_bar_sync(1, 128);
-        if (!dead) dead = !SMLA_WAIT(kBarPvDone, tl & 1);  // last P.V of the segment
+        wait_s(kBarPvDone, tl & 1);  // last P.V of the segment
         tc_fence_after();
         const bool full = (seg_first_kt == 0) && (ti.kt == p.nt - 1);
         const int64_t slot = (int64_t)blockIdx.x + ti.u;
         float inv[HG];
 #pragma unroll
-        for (int h = 0; h < HG; ++h) {
-          const float lt = red_sum[h] + red_sum[HG + h] + red_sum[2 * HG + h] + red_sum[3 * HG + h];
-          inv[h] = lt > 0.f ? 1.f / lt : 0.f;
-          if (tid == h) {
-            const float lse_v = lt > 0.f ? (m_used[h] + log2f(lt)) * 0.69314718055994530942f : -INFINITY;
-            if (full)
-              p.lse[(int64_t)ti.t * p.H + ti.hg * HG + h] = lse_v;
-            else
-              p.part_lse[slot * HG + h] = lse_v;
+        for (int j = 0; j < 4; ++j) {
+          const float4 a0 = *reinterpret_cast<const float4*>(red_sum + 4 * j);
+          const float4 a1 = *reinterpret_cast<const float4*>(red_sum + HG + 4 * j);
+          const float4 a2 = *reinterpret_cast<const float4*>(red_sum + 2 * HG + 4 * j);
+          const float4 a3 = *reinterpret_cast<const float4*>(red_sum + 3 * HG + 4 * j);
+          const float lt[4] = {(a0.x + a1.x) + (a2.x + a3.x), (a0.y + a1.y) + (a2.y + a3.y),
+                               (a0.z + a1.z) + (a2.z + a3.z), (a0.w + a1.w) + (a2.w + a3.w)};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            inv[4 * j + e] = lt[e] > 0.f ? __frcp_rn(lt[e]) : 0.f;
+            // lse of head 4j + e from the thread that holds its running maximum
+            if (w == 0 && lane == j) {
+              const float lse_v = lt[e] > 0.f ? (m4[e] + log2f(lt[e])) * 0.69314718055994530942f : -INFINITY;
+              const int h = 4 * j + e;
+              if (full)
+                p.lse[(int64_t)ti.t * p.H + ti.hg * HG + h] = lse_v;
+              else
+                p.part_lse[slot * HG + h] = lse_v;
+            }
           }
         }
         if (!dead) {
@@ -656,10 +914,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld_wait();
             reg_fence16(ohi);
             reg_fence16(olo);
-            const int c = 128 * q + j;
+            const int c = 128 * q + tid;
+            const float rs = Rq[q] * kPScaleInv;
 #pragma unroll
             for (int h = 0; h < HG; ++h) {
-              const float val = (__uint_as_float(ohi[h]) + __uint_as_float(olo[h])) * (Rq[q] * kPScaleInv) * inv[h];
+              const float val = (__uint_as_float(ohi[h]) + __uint_as_float(olo[h])) * rs * inv[h];
               if (full)
                 p.out[((int64_t)ti.t * p.H + ti.hg * HG + h) * kDv + c] = __float2bfloat16_rn(val);
               else
@@ -670,8 +929,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0 && !dead) mbar_arrive(&bars[kBarOFree]);
+        SMLA_CLK_MARK(7);
       }
     }
+    SMLA_CLK_STORE();
   }
 #undef SMLA_WAIT
 
@@ -683,44 +944,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// ---------------------------------------------------------------- host side
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (!fn) {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
-  }
-  return fn;
-}
-
 }  // namespace
 
-// Tensor maps of the cache viewed as a 2-D byte array [NB*64 rows, 656 bytes]:
-// 128-byte boxes with the 128-byte swizzle (codes, RoPE) and 16-byte boxes
-// without swizzle (scales).
-cudaError_t make_cache_maps(const uint8_t* cache, int64_t NB, CUtensorMap* row_map, CUtensorMap* scale_map) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return cudaErrorNotSupported;
-  const cuuint64_t gdim[2] = {(cuuint64_t)kRowBytes, (cuuint64_t)(NB * kBlock)};
-  const cuuint64_t gstride[1] = {(cuuint64_t)kRowBytes};
-  const cuuint32_t box_row[2] = {128, 1}, box_scale[2] = {16, 1}, es[2] = {1, 1};
-  CUresult r = enc(row_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(cache), gdim, gstride, box_row, es,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-  r = enc(scale_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(cache), gdim, gstride, box_scale, es,
-          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+#ifdef SMLA_TRACE
+extern "C" int smla_trace_set_fp8(unsigned long long* buf) {
+  return (int)cudaMemcpyToSymbol(g_smla_trace_fp8, &buf, sizeof(buf));
 }
+#endif
 
 AttnPlan plan_decode_fp8(int T, int H, int K, int num_splits, int num_sms) {
   AttnPlan pl;
@@ -748,13 +978,11 @@ cudaError_t launch_decode_fp8(const AttnArgs& a, const AttnPlan& plan, cudaStrea
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  CUtensorMap row_map, scale_map;
-  cudaError_t e = make_cache_maps(a.cache, a.NB, &row_map, &scale_map);
-  if (e != cudaSuccess) return e;
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
   const int64_t n_slots = (int64_t)plan.G + plan.units - 1;
   Params p;
   p.q = static_cast<const __nv_bfloat16*>(a.q);
+  p.cache = a.cache;
   p.indices = a.indices;
   p.block_table = a.block_table;
   p.req_id = a.req_id;
@@ -774,8 +1002,8 @@ cudaError_t launch_decode_fp8(const AttnArgs& a, const AttnPlan& plan, cudaStrea
   p.nt = plan.nt;
   p.total = plan.total;
   p.G = plan.G;
-  sparse_mla_decode_fp8_kernel<<<plan.G, kThreads, kSmemAlloc, stream>>>(p, row_map, scale_map);
-  e = cudaGetLastError();
+  sparse_mla_decode_fp8_kernel<<<plan.G, kThreads, kSmemAlloc, stream>>>(p);
+  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || !plan.need_combine) return e;
   combine_kernel<HG><<<(unsigned)plan.units, 256, 0, stream>>>(p.part_o, p.part_lse, p.out, p.lse, p.H, p.n_hg, p.nt,
                                                                p.total, p.G);
