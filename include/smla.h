@@ -69,6 +69,37 @@ int sparse_mla_decode_fp8(const void* q, const uint8_t* kv_cache, const int32_t*
 /* Workspace bytes sparse_mla_decode_fp8 needs on the current device. */
 size_t sparse_mla_decode_workspace_bytes(int T, int H, int K, int num_splits);
 
+/* sparse_mla_decode_fp8 without any allocation: the same computation and
+ * arguments, minus the workspace, whose role a fixed scratch array compiled
+ * into the library (SMLA_NOALLOC_SCRATCH_BYTES, 32 MiB of device memory per
+ * device the library is loaded on) takes.  The pages have no counterpart of
+ * this call: it exists for callers that cannot allocate device memory at
+ * call time, e.g. code being captured into a CUDA graph (cudaMalloc is not
+ * allowed during stream capture), serving loops that must never block in an
+ * allocator (cudaMalloc/cudaFree can synchronize the device), or processes
+ * whose memory is already fully handed to a caching allocator.
+ *   - No cudaMalloc, cudaFree or other allocating routine is called.
+ *   - The first call on a device looks up the scratch array's address
+ *     (cudaGetSymbolAddress, which may load the library's device module);
+ *     make that first call outside any stream capture.
+ *   - A call whose work split needs more than SMLA_NOALLOC_SCRATCH_BYTES of
+ *     scratch (sparse_mla_decode_workspace_bytes(T, H, K, num_splits)) is
+ *     rejected with SMLA_ERR_WORKSPACE; num_splits = 1, or fewer tokens per
+ *     call, needs less.
+ *   - Every call shares the one scratch array per device and leaves its
+ *     contents behind; the call clears the status word it needs at zero (an
+ *     asynchronous memset on `stream`) and overwrites everything else it
+ *     reads.  Calls whose execution overlaps on the GPU (other streams, other
+ *     host threads) race on the scratch and give wrong results: serialize
+ *     them, or use sparse_mla_decode_fp8 with one workspace per stream.
+ *   - The device status word of these calls is not exposed; a kernel wait
+ *     that runs past its time limit still ends the kernel. */
+#define SMLA_NOALLOC_SCRATCH_BYTES (32u << 20)
+int sparse_mla_decode_fp8_noalloc(const void* q, const uint8_t* kv_cache, const int32_t* indices,
+                                  const int32_t* block_table, const int32_t* req_id_per_token, float sm_scale,
+                                  int num_splits, void* out, float* lse, int T, int H, int K, int R, int MB,
+                                  int NB, void* stream);
+
 /* Sparse MLA prefill over a dense bf16 latent buffer (flash_mla_sparse_prefill
  * as called by FlashMLASparseImpl._bf16_flash_mla_kernel in
  * [flashmla_sparse.py]; heads need no padding here).

@@ -92,6 +92,8 @@ def lib():
             P, i32, sz, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_float
             L.sparse_mla_decode_fp8.argtypes = [P, P, P, P, P, f32, i32, P, P, i32, i32, i32, i32, i32, i32, P, sz, P]
             L.sparse_mla_decode_fp8.restype = i32
+            L.sparse_mla_decode_fp8_noalloc.argtypes = [P, P, P, P, P, f32, i32, P, P, i32, i32, i32, i32, i32, i32, P]
+            L.sparse_mla_decode_fp8_noalloc.restype = i32
             L.sparse_mla_decode_workspace_bytes.argtypes = [i32, i32, i32, i32]
             L.sparse_mla_decode_workspace_bytes.restype = sz
             L.sparse_mla_prefill_bf16.argtypes = [P, P, P, f32, i32, P, P, i32, i32, i32, i32, P, sz, P]
@@ -188,6 +190,40 @@ def sparse_mla_decode_fp8(q, kv_cache, indices, block_table, req_id_per_token, s
                                      _ptr(req_id_per_token), float(sm_scale), int(num_splits), _ptr(out), _ptr(lse),
                                      T, H, K, R, MB, NB, _ptr(workspace), ws_bytes, _stream_ptr(stream, dev))
     _check(rc, "sparse_mla_decode_fp8")
+    return out, lse
+
+
+def sparse_mla_decode_fp8_noalloc(q, kv_cache, indices, block_table, req_id_per_token, sm_scale: float,
+                                  num_splits: int = 0, out=None, lse=None, stream=None):
+    """sparse_mla_decode_fp8 for callers that cannot allocate device memory
+    at call time (code under CUDA graph capture, allocation-free serving
+    loops): the library's fixed 32 MiB per-device scratch replaces the
+    workspace.  Pass preallocated `out` and `lse` to keep the call free of
+    allocations on the Python side too.  The first call on a device should
+    come before any stream capture; calls that overlap on the GPU race on the
+    shared scratch.  Raises SmlaError if the work split needs more scratch."""
+    import torch
+    dev = _dev(q, kv_cache, indices, block_table, req_id_per_token, out, lse)
+    T, H, D = q.shape
+    NB = kv_cache.shape[0]
+    K = indices.shape[1]
+    R, MB = block_table.shape
+    _expect(q, torch.bfloat16, (T, H, 576), "q")
+    _expect(kv_cache, torch.uint8, (NB, 64, 656), "kv_cache")
+    _expect(indices, torch.int32, (T, K), "indices")
+    _expect(req_id_per_token, torch.int32, (T,), "req_id_per_token")
+    if block_table.dtype != torch.int32:
+        raise SmlaError("block_table must be int32")
+    if out is None:
+        out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+    _expect(out, torch.bfloat16, (T, H, 512), "out")
+    _expect(lse, torch.float32, (T, H), "lse")
+    rc = lib().sparse_mla_decode_fp8_noalloc(_ptr(q), _ptr(kv_cache), _ptr(indices), _ptr(block_table),
+                                             _ptr(req_id_per_token), float(sm_scale), int(num_splits), _ptr(out),
+                                             _ptr(lse), T, H, K, R, MB, NB, _stream_ptr(stream, dev))
+    _check(rc, "sparse_mla_decode_fp8_noalloc")
     return out, lse
 
 

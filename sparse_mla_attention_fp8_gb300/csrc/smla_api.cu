@@ -123,6 +123,27 @@ size_t workspace_bytes_for(bool fp8, int T, int H, int K, int num_splits) {
   return smla::plan_attention(fp8, T, H, K, num_splits, sms).ws_bytes;
 }
 
+// ---- fixed scratch for sparse_mla_decode_fp8_noalloc: part of the module
+// image, so no call ever allocates.  Its device address is looked up once per
+// device, with that device current.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[SMLA_NOALLOC_SCRATCH_BYTES];
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+int noalloc_scratch(void** out) {
+  int dev;
+  int rc = current_device(&dev);
+  if (rc != SMLA_OK) return rc;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* ptr = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(no-alloc scratch)");
+    g_noalloc_ptr[dev] = ptr;
+  }
+  *out = g_noalloc_ptr[dev];
+  return SMLA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -159,6 +180,59 @@ int sparse_mla_decode_fp8(const void* q, const uint8_t* kv_cache, const int32_t*
   a.MB = MB;
   a.NB = NB;
   return run_attention(true, a, num_splits, workspace, workspace_bytes, stream);
+}
+
+int sparse_mla_decode_fp8_noalloc(const void* q, const uint8_t* kv_cache, const int32_t* indices,
+                                  const int32_t* block_table, const int32_t* req_id_per_token, float sm_scale,
+                                  int num_splits, void* out, float* lse, int T, int H, int K, int R, int MB,
+                                  int NB, void* stream) {
+  if (T < 0 || K < 0 || R <= 0 || MB <= 0 || NB <= 0 || num_splits < 0)
+    return fail(SMLA_ERR_INVALID_ARG, "bad sizes T=%d K=%d R=%d MB=%d NB=%d num_splits=%d", T, K, R, MB, NB,
+                num_splits);
+  int rc = check_heads(H);
+  if (rc != SMLA_OK) return rc;
+  if (T == 0) return SMLA_OK;
+  if (!q || !kv_cache || (!indices && K > 0) || !block_table || !req_id_per_token || !out || !lse)
+    return fail(SMLA_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned16(q) || !aligned16(kv_cache) || !aligned16(out))
+    return fail(SMLA_ERR_INVALID_ARG, "q, kv_cache and out must be 16-byte aligned");
+  if ((int64_t)NB * 64 > INT32_MAX) return fail(SMLA_ERR_UNSUPPORTED, "NB*64 must fit in int32");
+  int sms = 0;
+  rc = num_sms(&sms);
+  if (rc != SMLA_OK) return rc;
+  const smla::AttnPlan plan = smla::plan_decode_fp8(T, H, K, num_splits, sms);
+  if (plan.ws_bytes > SMLA_NOALLOC_SCRATCH_BYTES)
+    return fail(SMLA_ERR_WORKSPACE,
+                "this call needs %zu bytes of scratch; the fixed scratch holds %zu (use num_splits=1, fewer "
+                "tokens per call, or sparse_mla_decode_fp8 with a workspace)",
+                plan.ws_bytes, (size_t)SMLA_NOALLOC_SCRATCH_BYTES);
+  void* scratch = nullptr;
+  rc = noalloc_scratch(&scratch);
+  if (rc != SMLA_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // the status word must start at zero; partial results are written before they are read
+  cudaError_t e = cudaMemsetAsync(scratch, 0, smla::kWsStatusBytes, s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(no-alloc status)");
+  smla::AttnArgs a{};
+  a.q = q;
+  a.cache = kv_cache;
+  a.kv = nullptr;
+  a.indices = indices;
+  a.block_table = block_table;
+  a.req_id = req_id_per_token;
+  a.out = out;
+  a.lse = lse;
+  a.sm_scale = sm_scale;
+  a.T = T;
+  a.H = H;
+  a.K = K;
+  a.R = R;
+  a.MB = MB;
+  a.NB = NB;
+  a.workspace = scratch;
+  e = smla::launch_decode_fp8(a, plan, s);
+  if (e != cudaSuccess) return cuda_fail(e, "sparse_mla_decode_fp8_noalloc launch");
+  return SMLA_OK;
 }
 
 size_t sparse_mla_decode_workspace_bytes(int T, int H, int K, int num_splits) {
