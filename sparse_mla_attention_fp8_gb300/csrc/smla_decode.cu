@@ -31,11 +31,13 @@
 //  * P.V for value chunk q (= scale group q) is one kind::f8f6f4 product
 //    O_q^T += E_q^T P'_q with the same code panel read MN-major and
 //    P'_q = 2^7 p * scale_q / R_q split into e4m3 hi + lo (R_q a running
-//    power-of-two bound of the group's scales).  The running max is refreshed
-//    whenever a tile's maximum exceeds it by more than a factor 2 (so p <= 2),
-//    which keeps P' <= 256: the top of the e4m3 range, where hi + lo carries
-//    8 significant bits down to ~2^-10 of the largest weight.  O is rescaled
-//    in tensor memory when R_q or the running max changes.
+//    power-of-two bound of the group's scales).  The running max of a head is
+//    refreshed (to 2^0.75 above the tile's maximum) only when a tile's maximum
+//    exceeds it by more than 2^1.75, so p <= 2^1.75 and P' < 430 stays at the
+//    top of the e4m3 range (max 448), where hi + lo carries 8 significant
+//    bits.  O is rescaled in tensor memory when R_q or a running max changes;
+//    the slack and overshoot keep that to a few tiles per unit.  P' is
+//    double-buffered.
 //  * Warp roles: softmax / epilogue (4 warps), tensor-core issuer (1 thread),
 //    index translation (1 warp), bulk-copy producer (1 warp), rearrange
 //    (2 warps), Q preparation (2 warps).
@@ -60,17 +62,17 @@ constexpr uint32_t kFullMask = 0xffffffffu;
 // (set by the host through smla_trace_set_fp8).  Compiled out otherwise.
 #ifdef SMLA_TRACE
 __device__ unsigned long long* g_smla_trace_fp8 = nullptr;
-constexpr int kTraceTiles = 64, kTraceEvents = 14;
+constexpr int kTraceTiles = 64, kTraceEvents = 16;
 enum { kEvIdx = 0, kEvRawLanded = 1, kEvOpFull = 2, kEvQk = 3, kEvSoftStart = 4, kEvSoftDone = 5, kEvPv = 6,
        kEvQReady = 7, kEvRawFull = 8, kEvOpEmpty = 9, kEvIssue = 10, kEvSoftLogits = 11, kEvSoftBar = 12,
-       kEvSoftPWait = 13 };
+       kEvSoftPWait = 13, kEvQkSeen = 14, kEvPvSeen = 15 };
 #define SMLA_TRACE_SET(tl, ev)                                                                                  \
   do {                                                                                                          \
     if (g_smla_trace_fp8 && (tl) < kTraceTiles)                                                                  \
       g_smla_trace_fp8[((size_t)blockIdx.x * kTraceTiles + (tl)) * kTraceEvents + (ev)] = globaltimer_ns();    \
   } while (0)
 // Cycle counters of the softmax sections (thread 0), stored after the per-tile events.
-#define SMLA_CLK_DECL unsigned clk_acc[8] = {0, 0, 0, 0, 0, 0, 0, 0}, clk_prev = (unsigned)clock()
+#define SMLA_CLK_DECL unsigned clk_acc[12] = {0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0}, clk_prev = (unsigned)clock()
 #define SMLA_CLK_START() (clk_prev = (unsigned)clock())
 #define SMLA_CLK_MARK(i)                   \
   do {                                     \
@@ -81,8 +83,8 @@ enum { kEvIdx = 0, kEvRawLanded = 1, kEvOpFull = 2, kEvQk = 3, kEvSoftStart = 4,
 #define SMLA_CLK_STORE()                                                                                        \
   do {                                                                                                          \
     if (g_smla_trace_fp8 && tid == 0)                                                                           \
-      for (int i_ = 0; i_ < 8; ++i_)                                                                            \
-        g_smla_trace_fp8[(size_t)gridDim.x * kTraceTiles * kTraceEvents + blockIdx.x * 8 + i_] = clk_acc[i_]; \
+      for (int i_ = 0; i_ < 12; ++i_)                                                                           \
+        g_smla_trace_fp8[(size_t)gridDim.x * kTraceTiles * kTraceEvents + blockIdx.x * 12 + i_] = clk_acc[i_]; \
   } while (0)
 #else
 #define SMLA_TRACE_SET(tl, ev) ((void)0)
@@ -96,8 +98,9 @@ constexpr int HG = 16;                 // heads per CTA work unit
 constexpr int kRows = 64;              // top-k rows per tile
 constexpr int kRawRows = 32;           // rows per raw stage (two stages per tile)
 constexpr int kRawStages = 4;          // raw ring depth (128 rows in flight)
-constexpr float kMaxSlack = 1.0f;      // log2 growth of a head's max tolerated before rescaling O (p <= 2)
-constexpr float kPScale = 128.0f;      // P' = kPScale * p * scale / R  <=  256
+constexpr float kMaxSlack = 1.75f;     // log2 growth of a head's max tolerated before rescaling O (p <= 2^1.75)
+constexpr float kMaxOvershoot = 0.75f; // a refreshed running max is set this far above the tile max
+constexpr float kPScale = 128.0f;      // P' = kPScale * p * scale / R  <=  128 * 2^1.75 < 430 (e4m3 max 448)
 constexpr float kPScaleInv = 1.0f / 128.0f;
 
 // ---- shared memory layout (offsets from a 1024-byte aligned base)
@@ -113,7 +116,7 @@ constexpr int kPGroup = kRows * 32;                   // P'_q: 64 rows x 32 code
 constexpr int kOffOp = 0;
 constexpr int kOffQ = kOffOp + 2 * kOpBuf;
 constexpr int kOffP = kOffQ + 2 * kQBuf;
-constexpr int kOffRaw = kOffP + 4 * kPGroup;
+constexpr int kOffRaw = kOffP + 2 * 4 * kPGroup;     // P' double-buffered
 constexpr int kOffRawMeta = kOffRaw + kRawStages * kRawStage;  // int32 [stages][32] slots
 constexpr int kOffSlots = kOffRawMeta + kRawStages * kRawRows * 4;  // int32 [4][64]
 constexpr int kOffValid = kOffSlots + 4 * kRows * 4;  // uint8 [2][64]
@@ -124,8 +127,8 @@ constexpr int kOffRedSum = kOffRedSc + 2 * 4 * 4 * 4;   // float [4 warps][16]
 constexpr int kOffDummy = kOffRedSum + 4 * HG * 4;   // 16 bytes per rearrange lane: sink for idle lanes
 constexpr int kOffBar = kOffDummy + 2 * 32 * 16;
 enum {
-  kBarOpFull = 0, kBarOpEmpty = 2, kBarSFull = 4, kBarPFull = 6, kBarPvDone = 7, kBarIdxFull = 8,
-  kBarIdxEmpty = 12, kBarQFull = 16, kBarQEmpty = 18, kBarOFree = 20, kBarRawFull = 21,
+  kBarOpFull = 0, kBarOpEmpty = 2, kBarSFull = 4, kBarPFull = 6, kBarPvDone = 8, kBarIdxFull = 10,
+  kBarIdxEmpty = 14, kBarQFull = 18, kBarQEmpty = 20, kBarOFree = 22, kBarRawFull = 23,
   kBarRawEmpty = kBarRawFull + kRawStages, kBarDrain = kBarRawEmpty + kRawStages, kNumBars = kBarDrain + 1
 };
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
@@ -321,8 +324,10 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(cons
       mbar_init(&bars[kBarQFull + i], kQWarps);
       mbar_init(&bars[kBarQEmpty + i], 1);
     }
-    mbar_init(&bars[kBarPFull], 4);
-    mbar_init(&bars[kBarPvDone], 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars[kBarPFull + i], 4);
+      mbar_init(&bars[kBarPvDone + i], 1);
+    }
     for (int i = 0; i < 4; ++i) {
       mbar_init(&bars[kBarIdxFull + i], 32);
       mbar_init(&bars[kBarIdxEmpty + i], 1);
@@ -541,12 +546,21 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(cons
       constexpr uint32_t id_qkr = make_idesc_bf16(64, HG, 0, 0);
       constexpr uint32_t id_pv = idesc_e4m3(128, 32, 1, 1);
       const uint32_t op0 = smem_u32(smem + kOffOp), q0 = smem_u32(smem + kOffQ), p0 = smem_u32(smem + kOffP);
+      // Shared-memory descriptors are built once per buffer; an operand at a
+      // byte offset o from a buffer's base is that descriptor + o / 16 (the
+      // start-address field holds bits 4..17 of the address, and no offset here
+      // carries out of it).
+      const uint64_t dK0 = make_sdesc(op0, 16, 1024, kLayoutSw128), dK1 = dK0 + (kOpBuf >> 4);
+      const uint64_t dQ0 = make_sdesc(q0, 16, 1024, kLayoutSw128), dQ1 = dQ0 + (kQBuf >> 4);
+      const uint64_t dV0 = make_sdesc(op0, kPanel, 1024, kLayoutSw128), dV1 = dV0 + (kOpBuf >> 4);
+      const uint64_t dP0 = make_sdesc(p0, 256, 128, kLayoutNone), dP1 = dP0 + ((4 * kPGroup) >> 4);
       int seg_q = 0, seg_o = 0, next_qk = 0, next_pv = 0;
       // top-k tile index within its unit of the next QK^T / P.V tile (advanced
       // incrementally: no divisions in the polling loop)
       const int kt0 = (int)(xbeg % p.nt);
       int kt_qk = kt0, kt_pv = kt0;
       uint64_t t_idle = 0;
+      uint32_t idle_polls = 0;
       while (next_pv < n_local) {
         bool progressed = false;
         if (next_qk < n_local && next_qk < next_pv + 2) {
@@ -558,25 +572,21 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(cons
           const int qb = seg & 1;
           const bool q_ok = !seg_start || mbar_test_wait(&bars[kBarQFull + qb], (seg >> 1) & 1);
           if (q_ok && mbar_test_wait(&bars[kBarOpFull + b], (tl >> 1) & 1)) {
+            SMLA_TRACE_SET(tl, kEvQkSeen);
             if (seg_start) ++seg_q;
             tc_fence_after();
-            const uint32_t op = op0 + b * kOpBuf, qs = q0 + qb * kQBuf;
+            const uint64_t dk = b ? dK1 : dK0, dq = qb ? dQ1 : dQ0;
             const uint32_t sb = tmem + b * kSCols;
 #pragma unroll
             for (int g = 0; g < 4; ++g) {
 #pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                const uint64_t da = make_sdesc(op + g * kPanel + 32 * k, 16, 1024, kLayoutSw128);
-                const uint64_t db = make_sdesc(qs + g * kQPanel + 32 * k, 16, 1024, kLayoutSw128);
-                mma_f8(sb + 32 * g, da, db, id_qk8, k > 0 ? 1u : 0u);
-              }
+              for (int k = 0; k < 4; ++k)
+                mma_f8(sb + 32 * g, dk + ((g * kPanel + 32 * k) >> 4), dq + ((g * kQPanel + 32 * k) >> 4), id_qk8,
+                       k > 0 ? 1u : 0u);
             }
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const uint64_t da = make_sdesc(op + kOpRope + 32 * k, 16, 1024, kLayoutSw128);
-              const uint64_t db = make_sdesc(qs + kQRope + 32 * k, 16, 1024, kLayoutSw128);
-              mma_ss(sb + 128, da, db, id_qkr, k > 0 ? 1u : 0u);
-            }
+            for (int k = 0; k < 4; ++k)
+              mma_ss(sb + 128, dk + ((kOpRope + 32 * k) >> 4), dq + ((kQRope + 32 * k) >> 4), id_qkr, k > 0 ? 1u : 0u);
             mma_commit(&bars[kBarSFull + b]);
             if (seg_end) mma_commit(&bars[kBarQEmpty + qb]);
             SMLA_TRACE_SET(tl, kEvQk);
@@ -590,22 +600,21 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(cons
           const bool seg_start = tl == 0 || kt_pv == 0;
           const int b = tl & 1;
           const bool o_ok = !seg_start || seg_o == 0 || mbar_test_wait(&bars[kBarOFree], (seg_o - 1) & 1);
-          if (o_ok && mbar_test_wait(&bars[kBarPFull], tl & 1)) {
+          if (o_ok && mbar_test_wait(&bars[kBarPFull + b], (tl >> 1) & 1)) {
+            SMLA_TRACE_SET(tl, kEvPvSeen);
             if (seg_start) ++seg_o;
             tc_fence_after();
-            const uint32_t op = op0 + b * kOpBuf;
+            const uint64_t dv = b ? dV1 : dV0, dp = b ? dP1 : dP0;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
 #pragma unroll
-              for (int k = 0; k < 2; ++k) {
+              for (int k = 0; k < 2; ++k)
                 // A = codes^T (value column c x row j), MN-major; B = P'_q (row j x 32), MN-major
-                const uint64_t da = make_sdesc(op + q * kPanel + 4096 * k, kPanel, 1024, kLayoutSw128);
-                const uint64_t db = make_sdesc(p0 + q * kPGroup + 1024 * k, 256, 128, kLayoutNone);
-                mma_f8(tmem + kOCol + 32 * q, da, db, id_pv, (seg_start && k == 0) ? 0u : 1u);
-              }
+                mma_f8(tmem + kOCol + 32 * q, dv + ((q * kPanel + 4096 * k) >> 4), dp + ((q * kPGroup + 1024 * k) >> 4),
+                       id_pv, (seg_start && k == 0) ? 0u : 1u);
             }
             mma_commit(&bars[kBarOpEmpty + b]);
-            mma_commit(&bars[kBarPvDone]);
+            mma_commit(&bars[kBarPvDone + b]);
             SMLA_TRACE_SET(tl, kEvPv);
             ++next_pv;
             kt_pv = kt_pv + 1 == p.nt ? 0 : kt_pv + 1;
@@ -614,9 +623,11 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(cons
         }
         if (progressed) {
           t_idle = 0;
-        } else {
+          idle_polls = 0;
+        } else if ((++idle_polls & 255u) == 0u) {
+          // the abort flag and the clock are looked at every 256 idle polls only:
+          // reading %globaltimer on every poll slows the reaction to ready work
           if (*abort_flag) break;
-          __nanosleep(32);
           const uint64_t now = globaltimer_ns();
           if (t_idle == 0) {
             t_idle = now;
@@ -782,8 +793,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(cons
         for (int i = 0; i < 4; ++i) {
           const float nm = fmaxf(m4[i], tmax[i]);
           const bool up = nm > m4[i] + kMaxSlack;
-          alpha4[i] = up ? ex2_approx(m4[i] - nm) : 1.f;
-          m4[i] = up ? nm : m4[i];
+          const float mnew = nm + kMaxOvershoot;
+          alpha4[i] = up ? ex2_approx(m4[i] - mnew) : 1.f;
+          m4[i] = up ? mnew : m4[i];
           l4[i] *= alpha4[i];
           up_any |= up;
         }
@@ -798,13 +810,20 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(cons
       }
       // every warp sees all 16 heads (lanes 0..3) and the same shared maxima: the decision is CTA-uniform
       const bool rescale = __any_sync(kFullMask, up_any) || rq_changed;
+#ifdef SMLA_TRACE
+      if (n_seg_tiles > 0) {
+        clk_acc[8] += __any_sync(kFullMask, up_any) ? 1u : 0u;
+        clk_acc[9] += rq_changed ? 1u : 0u;
+        clk_acc[10] += 1u;
+      }
+#endif
       SMLA_CLK_MARK(2);
       if (rescale && n_seg_tiles > 0) {
         // O^T holds this segment's earlier P.V: wait for the latest and rescale in place
         float alpha[HG];
 #pragma unroll
         for (int h = 0; h < HG; ++h) alpha[h] = __shfl_sync(kFullMask, alpha4[h & 3], h >> 2);
-        wait_s(kBarPvDone, (tl - 1) & 1);
+        wait_s(kBarPvDone + ((tl - 1) & 1), ((tl - 1) >> 1) & 1);  // P.V(tl - 1) and all before
         if (!dead) {
           tc_fence_after();
 #pragma unroll
@@ -838,7 +857,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(cons
         l4[i] += pr[k];
       }
       SMLA_CLK_MARK(4);
-      if (tl >= 1) wait_s(kBarPvDone, (tl - 1) & 1);  // P buffer free
+      if (tl >= 2) wait_s(kBarPvDone + (tl & 1), ((tl - 2) >> 1) & 1);  // P buffer free: P.V(tl - 2) done
       if (tid == 0) SMLA_TRACE_SET(tl, kEvSoftPWait);
       SMLA_CLK_MARK(5);
       // P'_q = kPScale * p * scale_q / R_q as e4m3 hi + lo: MN-major core
@@ -854,7 +873,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(cons
             const float f = (rho ? sc1[g] : sc0[g]) * inv_r;
             uint32_t hw, lw;
             split4(pr[2 * rho] * f, pr[2 * rho + 1] * f, pr[4 + 2 * rho] * f, pr[5 + 2 * rho] * f, hw, lw);
-            const uint32_t base = p0 + g * kPGroup + (r >> 3) * 256 + (r & 7) * 16 + 4 * c4;
+            const uint32_t base = p0 + ((tl & 1) * 4 + g) * kPGroup + (r >> 3) * 256 + (r & 7) * 16 + 4 * c4;
             sts32(base, hw);
             sts32(base + 128, lw);
           }
@@ -863,7 +882,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(cons
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0 && !dead) mbar_arrive(&bars[kBarPFull]);
+      if (lane == 0 && !dead) mbar_arrive(&bars[kBarPFull + (tl & 1)]);
       if (tid == 0) SMLA_TRACE_SET(tl, kEvSoftDone);
       SMLA_CLK_MARK(6);
       ++n_seg_tiles;
@@ -878,7 +897,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(cons
           if (lane < 4) *reinterpret_cast<float4*>(red_sum + w * HG + 4 * c4) = make_float4(v4[0], v4[1], v4[2], v4[3]);
         }
         named_bar_sync(1, 128);
-        wait_s(kBarPvDone, tl & 1);  // last P.V of the segment
+        wait_s(kBarPvDone + (tl & 1), (tl >> 1) & 1);  // last P.V of the segment
         tc_fence_after();
         const bool full = (seg_first_kt == 0) && (ti.kt == p.nt - 1);
         const int64_t slot = (int64_t)blockIdx.x + ti.u;
