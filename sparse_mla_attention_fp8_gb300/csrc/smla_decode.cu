@@ -1024,7 +1024,7 @@ cudaError_t launch_decode_fp8(const AttnArgs& a, const AttnPlan& plan, cudaStrea
   sparse_mla_decode_fp8_kernel<<<plan.G, kThreads, kSmemAlloc, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || !plan.need_combine) return e;
-  combine_kernel<HG><<<(unsigned)plan.units, 256, 0, stream>>>(p.part_o, p.part_lse, p.out, p.lse, p.H, p.n_hg, p.nt,
+  combine_kernel<HG><<<(unsigned)(plan.units * kCombineSplit), kCombineThreads, 0, stream>>>(p.part_o, p.part_lse, p.out, p.lse, p.H, p.n_hg, p.nt,
                                                                p.total, p.G);
   return cudaGetLastError();
 }
