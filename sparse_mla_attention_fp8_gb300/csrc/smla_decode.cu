@@ -11,16 +11,17 @@
 //
 // Design: the tensor cores read the cache codes as stored, with no
 // dequantization pass.
-//  * Transport: one producer warp issues one 656-byte bulk copy (TMA, 1-D)
-//    per valid row into a ring of raw row stages (4 x 32 rows in flight).
-//    Bulk copies keep many rows in flight per instruction; 16-byte
-//    asynchronous copies or register loads are limited to a few rows in
-//    flight per warp.
-//  * Layout: two rearrange warps move each row's 16-byte chunks from the raw
-//    stage to their 128-byte-swizzled operand positions in a 64-row tile (the
-//    512 e4m3 codes as four K-major panels, the 64 bf16 RoPE values as a
+//  * Transport: TMA tile::gather4 copies of whole rows (the cache viewed as a
+//    2-D array of 164 4-byte words per row, box 164 x 1), four rows per
+//    instruction, into 3 raw stages of 32 rows.  Issuing copies costs the
+//    issuing warp about as many cycles as bytes / 16, so three warps issue, each
+//    for its own raw stage, with 8 lanes issuing one gather4 each.
+//  * Layout: the same three warps move each landed row's 16-byte chunks to
+//    their 128-byte-swizzled operand positions in a 64-row tile
+//    (the 512 e4m3 codes as four K-major panels, the 64 bf16 RoPE values as a
 //    fifth panel, the four float32 scales beside them); invalid rows are
-//    zero-filled.  Two operand tiles are double-buffered.
+//    zero-filled.  Three operand tiles, so that the rearrange of a tile never
+//    waits for the P.V of the tile before.
 //  * Q is split once per (token, 16-head group) into two e4m3 terms,
 //    q * 2^s_h = hi + lo (s_h a per-head power of two putting max |q| near
 //    448), exact for all but negligibly small components; hi and lo are the
@@ -38,12 +39,17 @@
 //    bits.  O is rescaled in tensor memory when R_q or a running max changes;
 //    the slack and overshoot keep that to a few tiles per unit.  P' is
 //    double-buffered.
-//  * Warp roles: softmax / epilogue (4 warps), tensor-core issuer (1 thread),
-//    index translation (1 warp), bulk-copy producer (1 warp), rearrange
-//    (2 warps), Q preparation (2 warps).
+//  * Heads live in "S column" order throughout: column n of S, of P' and of O
+//    holds head pi(n) = 4 ((n & 7) >> 1) + (n & 1) + 2 (n >> 3); only the
+//    output stores translate.
+//  * Warp roles: softmax / epilogue (8 warps: two per TMEM lane quarter, one
+//    per half of the 16 head columns), tensor-core issuer (1 thread), index
+//    translation (1 warp), bulk-copy producer (1 warp), rearrange (3 warps),
+//    Q preparation (2 warps).
 #include <cstdint>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "sm103_ptx.cuh"
@@ -62,10 +68,11 @@ constexpr uint32_t kFullMask = 0xffffffffu;
 // (set by the host through smla_trace_set_fp8).  Compiled out otherwise.
 #ifdef SMLA_TRACE
 __device__ unsigned long long* g_smla_trace_fp8 = nullptr;
-constexpr int kTraceTiles = 64, kTraceEvents = 16;
+constexpr int kTraceTiles = 64, kTraceEvents = 19;
 enum { kEvIdx = 0, kEvRawLanded = 1, kEvOpFull = 2, kEvQk = 3, kEvSoftStart = 4, kEvSoftDone = 5, kEvPv = 6,
        kEvQReady = 7, kEvRawFull = 8, kEvOpEmpty = 9, kEvIssue = 10, kEvSoftLogits = 11, kEvSoftBar = 12,
-       kEvSoftPWait = 13, kEvQkSeen = 14, kEvPvSeen = 15 };
+       kEvSoftPWait = 13, kEvQkSeen = 14, kEvPvSeen = 15, kEvRawFullH1 = 16,
+       kEvRawLandedH1 = 17, kEvIssueH1 = 18 };
 #define SMLA_TRACE_SET(tl, ev)                                                                                  \
   do {                                                                                                          \
     if (g_smla_trace_fp8 && (tl) < kTraceTiles)                                                                  \
@@ -97,7 +104,8 @@ enum { kEvIdx = 0, kEvRawLanded = 1, kEvOpFull = 2, kEvQk = 3, kEvSoftStart = 4,
 constexpr int HG = 16;                 // heads per CTA work unit
 constexpr int kRows = 64;              // top-k rows per tile
 constexpr int kRawRows = 32;           // rows per raw stage (two stages per tile)
-constexpr int kRawStages = 4;          // raw ring depth (128 rows in flight)
+constexpr int kRawStages = 3;          // raw ring depth (96 rows in flight); stage s is rearranged by warp s % 3
+constexpr int kOpBufs = 3;             // operand tiles
 constexpr float kMaxSlack = 1.75f;     // log2 growth of a head's max tolerated before rescaling O (p <= 2^1.75)
 constexpr float kMaxOvershoot = 0.75f; // a refreshed running max is set this far above the tile max
 constexpr float kPScale = 128.0f;      // P' = kPScale * p * scale / R  <=  128 * 2^1.75 < 430 (e4m3 max 448)
@@ -108,34 +116,38 @@ constexpr int kPanel = kRows * 128;                   // 8 KB: 64 rows x 128 byt
 constexpr int kOpRope = 4 * kPanel;                   // RoPE panel after the 4 code panels
 constexpr int kOpScale = 5 * kPanel;                  // 64 x 16-byte scale rows
 constexpr int kOpBuf = 5 * kPanel + kRows * 16;       // 41984
-constexpr int kRawStage = kRawRows * kRowBytes;       // 20992
+constexpr int kGroupBytes = 2688;                     // 4 gathered rows (2624 bytes) padded to 128-byte alignment
+constexpr int kRawStage = (kRawRows / 4) * kGroupBytes;  // 21504
 constexpr int kQPanel = 32 * 128;                     // 32 operand rows (hi, lo) x 128 codes
 constexpr int kQRope = 4 * kQPanel;                   // 16 rows x 64 bf16
 constexpr int kQBuf = 4 * kQPanel + HG * 128;         // 18432
 constexpr int kPGroup = kRows * 32;                   // P'_q: 64 rows x 32 codes
+constexpr int kPBuf = 4 * kPGroup;                    // 8192
 constexpr int kOffOp = 0;
-constexpr int kOffQ = kOffOp + 2 * kOpBuf;
-constexpr int kOffP = kOffQ + 2 * kQBuf;
-constexpr int kOffRaw = kOffP + 2 * 4 * kPGroup;     // P' double-buffered
-constexpr int kOffRawMeta = kOffRaw + kRawStages * kRawStage;  // int32 [stages][32] slots
-constexpr int kOffSlots = kOffRawMeta + kRawStages * kRawRows * 4;  // int32 [4][64]
-constexpr int kOffValid = kOffSlots + 4 * kRows * 4;  // uint8 [2][64]
-constexpr int kOffPre = kOffValid + 2 * kRows;        // float [4][16] inverse Q prescales
-constexpr int kOffRedMax = kOffPre + 4 * HG * 4;      // float [2][4 warps][16]
-constexpr int kOffRedSc = kOffRedMax + 2 * 4 * HG * 4;  // float [2][4 warps][4]
-constexpr int kOffRedSum = kOffRedSc + 2 * 4 * 4 * 4;   // float [4 warps][16]
-constexpr int kOffDummy = kOffRedSum + 4 * HG * 4;   // 16 bytes per rearrange lane: sink for idle lanes
-constexpr int kOffBar = kOffDummy + 2 * 32 * 16;
+constexpr int kOffQ = kOffOp + kOpBufs * kOpBuf;
+constexpr int kOffP = kOffQ + kQBuf;
+constexpr int kOffRaw = kOffP + 2 * kPBuf;            // P' double-buffered
+constexpr int kOffSlots = kOffRaw + kRawStages * kRawStage;         // int32 [4][64]
+constexpr int kOffValid = kOffSlots + 4 * kRows * 4;                // uint8 [3][64]
+constexpr int kOffPre = kOffValid + kOpBufs * kRows;                // float [4][16 columns] inverse Q prescales
+constexpr int kOffRedMax = kOffPre + 4 * HG * 4;                    // float [2][4 quarters][16 columns]
+constexpr int kOffRedSc = kOffRedMax + 2 * 4 * HG * 4;              // float [2][2 halves][4 quarters][4]
+constexpr int kOffRedSum = kOffRedSc + 2 * 2 * 4 * 4 * 4;           // float [4 quarters][16 columns]
+constexpr int kOffDummy = kOffRedSum + 4 * HG * 4;  // 16 bytes per rearrange lane: sink for idle lanes
+constexpr int kOffBar = kOffDummy + kRawStages * 32 * 16;
 enum {
-  kBarOpFull = 0, kBarOpEmpty = 2, kBarSFull = 4, kBarPFull = 6, kBarPvDone = 8, kBarIdxFull = 10,
-  kBarIdxEmpty = 14, kBarQFull = 18, kBarQEmpty = 20, kBarOFree = 22, kBarRawFull = 23,
-  kBarRawEmpty = kBarRawFull + kRawStages, kBarDrain = kBarRawEmpty + kRawStages, kNumBars = kBarDrain + 1
+  kBarOpFull = 0, kBarOpEmpty = kBarOpFull + kOpBufs, kBarSFull = kBarOpEmpty + kOpBufs, kBarPFull = kBarSFull + 2,
+  kBarPvDone = kBarPFull + 2, kBarIdxFull = kBarPvDone + 2, kBarIdxEmpty = kBarIdxFull + 4,
+  kBarQFull = kBarIdxEmpty + 4, kBarQEmpty = kBarQFull + 1, kBarOFree = kBarQEmpty + 1, kBarRawFull = kBarOFree + 1,
+  kBarDrain = kBarRawFull + kRawStages, kNumBars = kBarDrain + 1
 };
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 16;
 constexpr int kSmemAlloc = kSmemBytes + 1024;
 static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0 && kOpBuf % 1024 == 0, "operand alignment");
-static_assert(kOffRaw % 16 == 0 && kRawStage % 16 == 0 && kOffBar % 8 == 0, "copy / barrier alignment");
+static_assert(kOffRaw % 128 == 0 && kRawStage % 128 == 0 && kGroupBytes % 128 == 0 && kOffBar % 8 == 0,
+              "TMA destinations 128-byte aligned; barriers 8-byte aligned");
+static_assert(kOffPre % 16 == 0 && kOffRedMax % 16 == 0 && kOffRedSc % 16 == 0 && kOffRedSum % 16 == 0, "float4");
 static_assert(kSmemAlloc <= 232448, "shared memory budget");
 
 // ---- tensor memory columns
@@ -144,15 +156,14 @@ constexpr int kOCol = 2 * kSCols;     // O^T: 4 chunks x (hi, lo) x 16 heads
 constexpr int kTmemCols = 512;
 static_assert(kOCol + 4 * 32 <= kTmemCols, "tensor memory budget");
 
-// ---- warp roles (11 warps; with at most 3 warps per SM sub-partition each
-// thread may hold up to 168 registers).  Warp w runs on sub-partition w % 4:
-// each sub-partition carries one softmax warp; the rearrange and Q warps sit
-// on sub-partitions 0 and 1, the issuer and index warps on 2, the producer on 3.
-constexpr int kRearrWarp0 = 4, kRearrWarps = 2, kMmaWarp = 6, kProdWarp = 7, kQWarp0 = 8, kQWarps = 2,
-              kIndexWarp = 10;
-constexpr int kNumWarps = 11;
+// ---- warp roles (15 warps; 128 registers per thread).  Warp w runs on
+// sub-partition w % 4: each sub-partition carries two softmax warps (one per
+// head half) and one or two of the other roles.
+constexpr int kSoftWarps = 8, kRearrWarp0 = 8, kRearrWarps = kRawStages, kMmaWarp = 11, kIndexWarp = 12,
+              kQWarp0 = 13, kQWarps = 2;
+constexpr int kNumWarps = 15;
 constexpr int kThreads = 32 * kNumWarps;
-static_assert(kQWarp0 + kQWarps <= kIndexWarp && kIndexWarp < kNumWarps, "warp roles");
+static_assert(kRearrWarp0 + kRearrWarps == kMmaWarp && kQWarp0 + kQWarps == kNumWarps, "warp roles");
 
 __host__ __device__ constexpr uint32_t idesc_e4m3(uint32_t M, uint32_t N, uint32_t a_mn, uint32_t b_mn) {
   return (1u << 4) | (a_mn << 15) | (b_mn << 16) | ((N >> 3) << 17) | ((M >> 4) << 24);
@@ -233,24 +244,6 @@ __device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_
   lo = e4m3x2(x0 - d.x, x1 - d.y);
 }
 
-// 16 values per lane reduced across the warp; lane l ends with value index l >> 1.
-template <bool kMax>
-__device__ __forceinline__ float warp_reduce16(float (&v)[16], int lane) {
-  auto op = [](float a, float b) { return kMax ? fmaxf(a, b) : a + b; };
-#pragma unroll
-  for (int w = 16, n = 8; n >= 1; w >>= 1, n >>= 1) {
-    const bool up = lane & w;
-#pragma unroll
-    for (int j = 0; j < n; ++j) {
-      const float send = up ? v[j] : v[j + n];
-      const float keep = up ? v[j + n] : v[j];
-      v[j] = op(keep, __shfl_xor_sync(kFullMask, send, w));
-    }
-  }
-  v[0] = op(v[0], __shfl_xor_sync(kFullMask, v[0], 1));
-  return v[0];
-}
-
 __device__ __forceinline__ float pow2_ceil(float x) {  // smallest power of two >= x (x > 0)
   const uint32_t u = __float_as_uint(x);
   const uint32_t e = u & 0x7F800000u;
@@ -266,48 +259,54 @@ __device__ __forceinline__ float ex2_approx(float x) {  // 2^x; 2^-inf = 0
   return y;
 }
 
-// Four floats -> e4m3 hi and lo words (byte i from value i), x_i ~ hi_i + lo_i.
-// The split runs in f16x2: the values are first rounded to f16 (11 significant
-// bits, more than the 8 that hi + lo keep), hi is the e4m3 rounding, lo the
-// e4m3 rounding of the exact f16 difference.
-__device__ __forceinline__ void split4(float x0, float x1, float x2, float x3, uint32_t& hi, uint32_t& lo) {
-  uint32_t a, b, ha, hb, da, db, ra, rb;
-  uint16_t t;
-  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(a) : "f"(x1), "f"(x0));
-  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(b) : "f"(x3), "f"(x2));
-  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(t) : "r"(a));
-  ha = t;
-  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(t) : "r"(b));
-  hb = t;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(da) : "h"((uint16_t)ha));
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(db) : "h"((uint16_t)hb));
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(ra) : "r"(a), "r"(da));
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(rb) : "r"(b), "r"(db));
-  uint32_t la, lb;
-  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(t) : "r"(ra));
-  la = t;
-  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(t) : "r"(rb));
-  lb = t;
-  hi = ha | (hb << 16);
-  lo = la | (lb << 16);
-}
-
-__device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
-  asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-
-// QK^T column n (of 16) holds head pi(n) with pi(2c + e + 8d) = 4c + e + 2d,
-// so that the 16x256b read of S gives thread c (lane % 4) heads 4c .. 4c + 3.
+// Q operand row (and so S column) of head h: column n holds head pi(n) with
+// pi(2c + e + 8d) = 4c + e + 2d, so that the 16x256b.x1 read of column half d
+// gives thread c (lane % 4) the two adjacent columns 8d + 2c, 8d + 2c + 1.
 __device__ __forceinline__ int q_row_of_head(int h) { return 2 * (h >> 2) + (h & 1) + 8 * ((h >> 1) & 1); }
 
-__global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(const __grid_constant__ Params p) {
+// Head held by column n of S, P' and O (the inverse of q_row_of_head).
+__device__ __forceinline__ int head_of_col(int n) { return 4 * ((n & 7) >> 1) + (n & 1) + 2 * (n >> 3); }
+
+// Two floats -> e4m3 hi and lo pairs (low byte from x0), x ~ hi + lo; the
+// split runs in f16x2 (11 significant bits, more than the 8 that hi + lo keep).
+__device__ __forceinline__ void split2_f16(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  uint32_t a, d, r;
+  uint16_t t;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(a) : "f"(x1), "f"(x0));
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(t) : "r"(a));
+  hi = t;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(d) : "h"(t));
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(d));
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(t) : "r"(r));
+  lo = t;
+}
+
+__device__ __forceinline__ void sts16(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"((uint16_t)v) : "memory");
+}
+
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int x, int r0, int r1, int r2, int r3,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
+      "%4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(map), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Shared address of row i of a raw stage (4-row gather groups, 128-byte aligned).
+__device__ __forceinline__ uint32_t raw_row(uint32_t raw, int i) {
+  return raw + (uint32_t)((i >> 2) * kGroupBytes + (i & 3) * kRowBytes);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    sparse_mla_decode_fp8_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap row_map) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
   int32_t* slots_ring = reinterpret_cast<int32_t*>(smem + kOffSlots);
-  int32_t* raw_meta = reinterpret_cast<int32_t*>(smem + kOffRawMeta);
   uint8_t* valid = smem + kOffValid;
   float* pre_ring = reinterpret_cast<float*>(smem + kOffPre);
 
@@ -317,26 +316,23 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(cons
   const int n_local = (int)(xend - xbeg);
 
   if (tid == 0) {
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars[kBarOpFull + i], kRearrWarps);
+    for (int i = 0; i < kOpBufs; ++i) {
+      mbar_init(&bars[kBarOpFull + i], 2);  // one arrival per 32-row half
       mbar_init(&bars[kBarOpEmpty + i], 1);
-      mbar_init(&bars[kBarSFull + i], 1);
-      mbar_init(&bars[kBarQFull + i], kQWarps);
-      mbar_init(&bars[kBarQEmpty + i], 1);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars[kBarPFull + i], 4);
+      mbar_init(&bars[kBarSFull + i], 1);
+      mbar_init(&bars[kBarPFull + i], kSoftWarps);
       mbar_init(&bars[kBarPvDone + i], 1);
     }
     for (int i = 0; i < 4; ++i) {
       mbar_init(&bars[kBarIdxFull + i], 32);
-      mbar_init(&bars[kBarIdxEmpty + i], 1);
+      mbar_init(&bars[kBarIdxEmpty + i], 2);  // one arrival per 32-row half
     }
-    for (int i = 0; i < kRawStages; ++i) {
-      mbar_init(&bars[kBarRawFull + i], 1);
-      mbar_init(&bars[kBarRawEmpty + i], 1);
-    }
-    mbar_init(&bars[kBarOFree], 4);
+    for (int i = 0; i < kRawStages; ++i) mbar_init(&bars[kBarRawFull + i], 1);
+    mbar_init(&bars[kBarQFull], kQWarps);
+    mbar_init(&bars[kBarQEmpty], 1);
+    mbar_init(&bars[kBarOFree], kSoftWarps);
     mbar_init(&bars[kBarDrain], 1);
     *abort_flag = 0;
     mbar_fence_init();
@@ -380,82 +376,72 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(cons
       for (int i = 0; i < 2; ++i) cur[i] = nxt[i];
       req_cur = req_nxt;
     }
-  } else if (warp == kProdWarp) {
-    // ------------------------------------------------------------ bulk-copy producer
-    // Raw stage s holds rows 32 (s % 2) .. +31 of tile s / 2.  Lane l issues
-    // the 656-byte copy of the stage's row l when its slot is valid.
-    int issued = 0;
-    for (int s = 0; s < 2 * n_local; ++s) {
-      const int tl = s >> 1, b4 = tl & 3, rs = s % kRawStages;
-      if ((s & 1) == 0 && !SMLA_WAIT(kBarIdxFull + b4, (tl >> 2) & 1)) break;
-      if (s >= kRawStages && !SMLA_WAIT(kBarRawEmpty + rs, ((s / kRawStages) + 1) & 1)) break;
-      const int32_t slot = slots_ring[b4 * kRows + kRawRows * (s & 1) + lane];
-      raw_meta[rs * kRawRows + lane] = slot;
-      const uint32_t nvalid = __popc(__ballot_sync(kFullMask, slot >= 0));
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&bars[kBarRawFull + rs], nvalid * kRowBytes);
-        if (s & 1) mbar_arrive(&bars[kBarIdxEmpty + b4]);  // both halves' slots read
-      }
-      __syncwarp();
-      if (slot >= 0)
-        bulk_g2s(smem + kOffRaw + rs * kRawStage + lane * kRowBytes, p.cache + (int64_t)slot * kRowBytes, kRowBytes,
-                 &bars[kBarRawFull + rs]);
-      issued = s + 1;
-      if (lane == 0 && (s & 1) == 0) SMLA_TRACE_SET(tl, kEvIssue);
-    }
-    // No copy may still be landing in shared memory when the CTA exits (only
-    // possible after an abort; the consumers have waited for every stage otherwise).
-    for (int s = issued > kRawStages ? issued - kRawStages : 0; s < issued; ++s)
-      mbar_wait_drain(&bars[kBarRawFull + s % kRawStages], (s / kRawStages) & 1);
   } else if (warp >= kRearrWarp0 && warp < kRearrWarp0 + kRearrWarps) {
-    // ------------------------------------------------------------ rearrange raw rows -> operand tile
-    // Warp rw handles the raw stage of tile rows 32 rw .. 32 rw + 31, in
-    // batches of 8 rows.  Lane l moves code chunk l (bytes 16l..16l+15) of
-    // each row to panel l/8 at its swizzled position.  The 9-chunk tails
-    // (4 scales, then 8 RoPE chunks) of the batch's 8 rows are 72 moves spread
-    // over three rounds of the 32 lanes; idle lanes store to a private sink.
-    // Everything is branch-free so that a batch's loads are all in flight
-    // before its stores; invalid rows are zero-filled by selects.
+    // ------------------------------------------------------------ load + rearrange
+    // Warp rw handles the 32-row stages s = rw, rw + 3, ... (rows 32 (s % 2)
+    // .. +31 of tile s / 2) in its own raw stage rw.  Lanes 0..7 each issue one
+    // gather4 of 4 whole rows (invalid rows at row -1: the TMA zero-fills
+    // them); once they have landed, lane l moves code chunk l (bytes
+    // 16l..16l+15) of each row to panel l/8 at its swizzled position, in
+    // batches of 8 rows.  The 9-chunk tails (4 scales, then 8 RoPE chunks) of
+    // the batch's 8 rows are 72 moves spread over three rounds of the 32
+    // lanes; idle lanes store to a private sink.  Everything is branch-free so
+    // that a batch's loads are all in flight before its stores; invalid rows
+    // are zero-filled by selects.
     const int rw = warp - kRearrWarp0;
     const int chunk = lane & 7, panel = lane >> 3;
-    int tail_j[3], tail_k[3];
-    bool tail_on[3];
-#pragma unroll
-    for (int q = 0; q < 3; ++q) {
-      const int sidx = 32 * q + lane;
-      tail_on[q] = sidx < 72;
-      tail_j[q] = tail_on[q] ? sidx / 9 : 0;
-      tail_k[q] = tail_on[q] ? sidx % 9 : 0;
-    }
     const uint32_t sink = smem_u32(smem + kOffDummy + (rw * 32 + lane) * 16);
-    for (int tl = 0; tl < n_local; ++tl) {
-      const int b = tl & 1;
-      const int s = 2 * tl + rw, rs = s % kRawStages;
+    const int rs = rw;
+    const uint32_t raw = smem_u32(smem + kOffRaw + rs * kRawStage);
+    int issued = 0;
+    for (int s = rw; s < 2 * n_local; s += kRawStages) {
+      const int tl = s >> 1, half = s & 1, b4 = tl & 3;
+      const int ob = tl % kOpBufs, use = tl / kOpBufs;
+      if (!SMLA_WAIT(kBarIdxFull + b4, (tl >> 2) & 1)) break;
+      const int32_t slot = slots_ring[b4 * kRows + kRawRows * half + lane];
+      const uint32_t vmask = __ballot_sync(kFullMask, slot >= 0);
+      const int row = slot >= 0 ? slot : -1;
+      const int g0 = __shfl_sync(kFullMask, row, (4 * lane) & 31), g1 = __shfl_sync(kFullMask, row, (4 * lane + 1) & 31);
+      const int g2 = __shfl_sync(kFullMask, row, (4 * lane + 2) & 31), g3 = __shfl_sync(kFullMask, row, (4 * lane + 3) & 31);
+      if (lane == 0) {
+        mbar_arrive(&bars[kBarIdxEmpty + b4]);  // this half's slots read
+        mbar_arrive_expect_tx(&bars[kBarRawFull + rs], kRawRows * kRowBytes);
+      }
+      __syncwarp();
+      if (lane < 8) tma_gather4(raw + lane * kGroupBytes, &row_map, 0, g0, g1, g2, g3, &bars[kBarRawFull + rs]);
+      if (lane == 0) SMLA_TRACE_SET(tl, half ? kEvIssueH1 : kEvIssue);
+      ++issued;
       if (!SMLA_WAIT(kBarRawFull + rs, (s / kRawStages) & 1)) break;
-      if (lane == 0 && rw == 0) SMLA_TRACE_SET(tl, kEvRawFull);
-      if (tl >= 2 && !SMLA_WAIT(kBarOpEmpty + b, ((tl >> 1) + 1) & 1)) break;
-      if (lane == 0 && rw == 0) SMLA_TRACE_SET(tl, kEvOpEmpty);
-      const uint32_t op = smem_u32(smem + kOffOp + b * kOpBuf);
-      const uint32_t raw = smem_u32(smem + kOffRaw + rs * kRawStage);
-      const uint32_t vmask = __ballot_sync(kFullMask, raw_meta[rs * kRawRows + lane] >= 0);
+      if (lane == 0) SMLA_TRACE_SET(tl, half ? kEvRawFullH1 : kEvRawFull);
+      if (use >= 1 && !SMLA_WAIT(kBarOpEmpty + ob, (use + 1) & 1)) break;
+      if (lane == 0 && half == 0) SMLA_TRACE_SET(tl, kEvOpEmpty);
+      const uint32_t op = smem_u32(smem + kOffOp + ob * kOpBuf);
 #pragma unroll 1
       for (int i0 = 0; i0 < kRawRows; i0 += 8) {
+        int tail_j[3], tail_k[3];
+        bool tail_on[3];
+#pragma unroll
+        for (int q = 0; q < 3; ++q) {
+          const int sidx = 32 * q + lane;
+          tail_on[q] = sidx < 72;
+          tail_j[q] = tail_on[q] ? sidx / 9 : 0;
+          tail_k[q] = tail_on[q] ? sidx % 9 : 0;
+        }
         uint4 c[8], t[3];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) c[j] = lds128(raw + (i0 + j) * kRowBytes + 16 * lane);
+        for (int j = 0; j < 8; ++j) c[j] = lds128(raw_row(raw, i0 + j) + 16 * lane);
 #pragma unroll
-        for (int q = 0; q < 3; ++q) t[q] = lds128(raw + (i0 + tail_j[q]) * kRowBytes + kScaleOff + 16 * tail_k[q]);
+        for (int q = 0; q < 3; ++q) t[q] = lds128(raw_row(raw, i0 + tail_j[q]) + kScaleOff + 16 * tail_k[q]);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          const int r = kRawRows * rw + i0 + j;
+          const int r = kRawRows * half + i0 + j;
           const bool v = (vmask >> (i0 + j)) & 1u;
           const uint4 x = v ? c[j] : make_uint4(0u, 0u, 0u, 0u);
           sts128(op + panel * kPanel + (uint32_t)((r >> 3) * 1024 + (r & 7) * 128) + ((chunk ^ (r & 7)) << 4), x);
         }
 #pragma unroll
         for (int q = 0; q < 3; ++q) {
-          const int r = kRawRows * rw + i0 + tail_j[q];
+          const int r = kRawRows * half + i0 + tail_j[q];
           const bool v = (vmask >> (i0 + tail_j[q])) & 1u;
           const uint4 x = v ? t[q] : make_uint4(0u, 0u, 0u, 0u);
           const uint32_t rope_dst =
@@ -464,35 +450,44 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(cons
           sts128(dst, x);
         }
       }
-      valid[b * kRows + kRawRows * rw + lane] = (uint8_t)((vmask >> lane) & 1u);
+      valid[ob * kRows + kRawRows * half + lane] = (uint8_t)((vmask >> lane) & 1u);
+      // orders this stage's reads of the raw stage and writes of the operand
+      // tile before the tensor-memory-side accesses that follow (the next
+      // gather into the raw stage, the MMAs on the tile)
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(&bars[kBarRawEmpty + rs]);
-        mbar_arrive(&bars[kBarOpFull + b]);
-        if (rw == 0) SMLA_TRACE_SET(tl, kEvRawLanded);
+        mbar_arrive(&bars[kBarOpFull + ob]);
+        SMLA_TRACE_SET(tl, half ? kEvRawLandedH1 : kEvRawLanded);
       }
     }
+    // No copy may still be landing in shared memory when the CTA exits (only
+    // possible after an abort; the stage's wait has run otherwise).
+    if (issued > 0) mbar_wait_drain(&bars[kBarRawFull + rs], ((issued - 1) & 1));
   } else if (warp >= kQWarp0 && warp < kQWarp0 + kQWarps) {
     // ------------------------------------------------------------ Q preparation
     // 4 threads per head: thread part owns NoPE columns [128 part, 128 part +
     // 128) (code panel `part`) and RoPE chunks 2 part, 2 part + 1.  Head h is
-    // stored in operand row q_row_of_head(h) (hi) and 16 + that row (lo).
+    // stored in operand row n = q_row_of_head(h) (hi) and 16 + n (lo).
     // q * 2^s_h = hi + lo in e4m3 with s_h chosen so that max |q * 2^s_h| <= 448.
+    // One Q buffer: the next segment's q is loaded into registers while the
+    // current one is in use, and converted once the buffer is released.
     const int qt = tid - 32 * kQWarp0;  // 0..63
     const int h = qt >> 2, part = qt & 3;
     const int qrow = q_row_of_head(h);
-    int seg = 0;
-    for (int tl = 0; tl < n_local; ++tl) {
+    uint4 v[16], rope0, rope1;
+    auto load_q = [&](int tl) {
       const TileInfo ti = tile_info(p, xbeg + tl, xbeg, xend);
-      if (!ti.seg_start) continue;
-      const int qb = seg & 1;
-      if (seg >= 2 && !SMLA_WAIT(kBarQEmpty + qb, ((seg >> 1) + 1) & 1)) break;
       const uint4* src = reinterpret_cast<const uint4*>(p.q + ((int64_t)ti.t * p.H + ti.hg * HG + h) * kDqk);
-      uint4 v[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) v[i] = __ldg(src + 16 * part + i);
-      const uint4 rope0 = __ldg(src + 64 + 2 * part), rope1 = __ldg(src + 64 + 2 * part + 1);
+      rope0 = __ldg(src + 64 + 2 * part);
+      rope1 = __ldg(src + 64 + 2 * part + 1);
+    };
+    int tl = 0, seg = 0;
+    if (n_local > 0) load_q(0);
+    while (tl < n_local) {
+      if (seg >= 1 && !SMLA_WAIT(kBarQEmpty, (seg - 1) & 1)) break;
       float amax = 0.f;
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
@@ -510,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(cons
         sh = e - 1;
       }
       const float pre = ldexpf(1.f, sh);
-      const uint32_t qpanel = smem_u32(smem + kOffQ + qb * kQBuf + part * kQPanel);
+      const uint32_t qpanel = smem_u32(smem + kOffQ + part * kQPanel);
 #pragma unroll
       for (int ch = 0; ch < 8; ++ch) {  // 16 codes per chunk = two uint4 of bf16
         uint32_t hi[4], lo[4];
@@ -527,84 +522,58 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(cons
         sts128(qpanel + sw128_chunk(32, qrow, ch), make_uint4(hi[0], hi[1], hi[2], hi[3]));
         sts128(qpanel + sw128_chunk(32, 16 + qrow, ch), make_uint4(lo[0], lo[1], lo[2], lo[3]));
       }
-      const uint32_t qrope = smem_u32(smem + kOffQ + qb * kQBuf + kQRope);
+      const uint32_t qrope = smem_u32(smem + kOffQ + kQRope);
       sts128(qrope + sw128_chunk(HG, qrow, 2 * part), rope0);
       sts128(qrope + sw128_chunk(HG, qrow, 2 * part + 1), rope1);
-      if (part == 0) pre_ring[(seg & 3) * HG + h] = ldexpf(1.f, -sh);
+      if (part == 0) pre_ring[(seg & 3) * HG + qrow] = ldexpf(1.f, -sh);
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kBarQFull + qb]);
+      if (lane == 0) mbar_arrive(&bars[kBarQFull]);
       if (qt == 0) SMLA_TRACE_SET(tl, kEvQReady);
+      // the next segment starts at the next tile with top-k tile index 0
+      do {
+        ++tl;
+      } while (tl < n_local && tile_info(p, xbeg + tl, xbeg, xend).kt != 0);
+      if (tl < n_local) load_q(tl);
       ++seg;
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ tensor-core issuer
-    // Polls (never blocks on) the next operand tile + Q block for QK^T (up to
-    // two tiles ahead of P.V, one per S buffer) and the next P' for P.V.
+    // Polls (never blocks on) the next P' for P.V, then the next operand tile
+    // + Q for QK^T (at most one tile ahead of the oldest P.V not yet issued,
+    // one per S buffer).  P.V goes first: its completion frees the operand
+    // tile and the P buffer that the other roles wait for.
     if (lane == 0 && n_local > 0) {
       constexpr uint32_t id_qk8 = idesc_e4m3(64, 32, 0, 0);
       constexpr uint32_t id_qkr = make_idesc_bf16(64, HG, 0, 0);
       constexpr uint32_t id_pv = idesc_e4m3(128, 32, 1, 1);
       const uint32_t op0 = smem_u32(smem + kOffOp), q0 = smem_u32(smem + kOffQ), p0 = smem_u32(smem + kOffP);
-      // Shared-memory descriptors are built once per buffer; an operand at a
-      // byte offset o from a buffer's base is that descriptor + o / 16 (the
-      // start-address field holds bits 4..17 of the address, and no offset here
-      // carries out of it).
-      const uint64_t dK0 = make_sdesc(op0, 16, 1024, kLayoutSw128), dK1 = dK0 + (kOpBuf >> 4);
-      const uint64_t dQ0 = make_sdesc(q0, 16, 1024, kLayoutSw128), dQ1 = dQ0 + (kQBuf >> 4);
-      const uint64_t dV0 = make_sdesc(op0, kPanel, 1024, kLayoutSw128), dV1 = dV0 + (kOpBuf >> 4);
-      const uint64_t dP0 = make_sdesc(p0, 256, 128, kLayoutNone), dP1 = dP0 + ((4 * kPGroup) >> 4);
+      // Shared-memory descriptors are built once; an operand at a byte offset
+      // o from a base is that descriptor + o / 16 (the start-address field holds
+      // bits 4..17 of the address, and no offset here carries out of it).
+      const uint64_t dK0 = make_sdesc(op0, 16, 1024, kLayoutSw128);
+      const uint64_t dQ = make_sdesc(q0, 16, 1024, kLayoutSw128);
+      const uint64_t dV0 = make_sdesc(op0, kPanel, 1024, kLayoutSw128);
+      const uint64_t dP0 = make_sdesc(p0, 256, 128, kLayoutNone);
       int seg_q = 0, seg_o = 0, next_qk = 0, next_pv = 0;
       // top-k tile index within its unit of the next QK^T / P.V tile (advanced
       // incrementally: no divisions in the polling loop)
       const int kt0 = (int)(xbeg % p.nt);
-      int kt_qk = kt0, kt_pv = kt0;
+      int kt_qk = kt0, kt_pv = kt0, ob_qk = 0, ob_pv = 0;
       uint64_t t_idle = 0;
       uint32_t idle_polls = 0;
       while (next_pv < n_local) {
         bool progressed = false;
-        if (next_qk < n_local && next_qk < next_pv + 2) {
-          const int tl = next_qk;
-          const bool seg_start = tl == 0 || kt_qk == 0;
-          const bool seg_end = tl == n_local - 1 || kt_qk == p.nt - 1;
-          const int b = tl & 1;
-          const int seg = seg_start ? seg_q : seg_q - 1;
-          const int qb = seg & 1;
-          const bool q_ok = !seg_start || mbar_test_wait(&bars[kBarQFull + qb], (seg >> 1) & 1);
-          if (q_ok && mbar_test_wait(&bars[kBarOpFull + b], (tl >> 1) & 1)) {
-            SMLA_TRACE_SET(tl, kEvQkSeen);
-            if (seg_start) ++seg_q;
-            tc_fence_after();
-            const uint64_t dk = b ? dK1 : dK0, dq = qb ? dQ1 : dQ0;
-            const uint32_t sb = tmem + b * kSCols;
-#pragma unroll
-            for (int g = 0; g < 4; ++g) {
-#pragma unroll
-              for (int k = 0; k < 4; ++k)
-                mma_f8(sb + 32 * g, dk + ((g * kPanel + 32 * k) >> 4), dq + ((g * kQPanel + 32 * k) >> 4), id_qk8,
-                       k > 0 ? 1u : 0u);
-            }
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              mma_ss(sb + 128, dk + ((kOpRope + 32 * k) >> 4), dq + ((kQRope + 32 * k) >> 4), id_qkr, k > 0 ? 1u : 0u);
-            mma_commit(&bars[kBarSFull + b]);
-            if (seg_end) mma_commit(&bars[kBarQEmpty + qb]);
-            SMLA_TRACE_SET(tl, kEvQk);
-            ++next_qk;
-            kt_qk = kt_qk + 1 == p.nt ? 0 : kt_qk + 1;
-            progressed = true;
-          }
-        }
         if (next_pv < next_qk) {
           const int tl = next_pv;
           const bool seg_start = tl == 0 || kt_pv == 0;
-          const int b = tl & 1;
+          const int pb = tl & 1;
           const bool o_ok = !seg_start || seg_o == 0 || mbar_test_wait(&bars[kBarOFree], (seg_o - 1) & 1);
-          if (o_ok && mbar_test_wait(&bars[kBarPFull + b], (tl >> 1) & 1)) {
+          if (o_ok && mbar_test_wait(&bars[kBarPFull + pb], (tl >> 1) & 1)) {
             SMLA_TRACE_SET(tl, kEvPvSeen);
             if (seg_start) ++seg_o;
             tc_fence_after();
-            const uint64_t dv = b ? dV1 : dV0, dp = b ? dP1 : dP0;
+            const uint64_t dv = dV0 + (uint64_t)((ob_pv * kOpBuf) >> 4), dp = dP0 + (uint64_t)((pb * kPBuf) >> 4);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
 #pragma unroll
@@ -613,11 +582,44 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(cons
                 mma_f8(tmem + kOCol + 32 * q, dv + ((q * kPanel + 4096 * k) >> 4), dp + ((q * kPGroup + 1024 * k) >> 4),
                        id_pv, (seg_start && k == 0) ? 0u : 1u);
             }
-            mma_commit(&bars[kBarOpEmpty + b]);
-            mma_commit(&bars[kBarPvDone + b]);
+            mma_commit(&bars[kBarOpEmpty + ob_pv]);
+            mma_commit(&bars[kBarPvDone + pb]);
             SMLA_TRACE_SET(tl, kEvPv);
             ++next_pv;
             kt_pv = kt_pv + 1 == p.nt ? 0 : kt_pv + 1;
+            ob_pv = ob_pv + 1 == kOpBufs ? 0 : ob_pv + 1;
+            progressed = true;
+          }
+        }
+        if (next_qk < n_local && next_qk < next_pv + 2) {
+          const int tl = next_qk;
+          const bool seg_start = tl == 0 || kt_qk == 0;
+          const bool seg_end = tl == n_local - 1 || kt_qk == p.nt - 1;
+          const int sbuf = tl & 1;
+          const int seg = seg_start ? seg_q : seg_q - 1;
+          const bool q_ok = !seg_start || mbar_test_wait(&bars[kBarQFull], seg & 1);
+          if (q_ok && mbar_test_wait(&bars[kBarOpFull + ob_qk], (tl / kOpBufs) & 1)) {
+            SMLA_TRACE_SET(tl, kEvQkSeen);
+            if (seg_start) ++seg_q;
+            tc_fence_after();
+            const uint64_t dk = dK0 + (uint64_t)((ob_qk * kOpBuf) >> 4);
+            const uint32_t sb = tmem + sbuf * kSCols;
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                mma_f8(sb + 32 * g, dk + ((g * kPanel + 32 * k) >> 4), dQ + ((g * kQPanel + 32 * k) >> 4), id_qk8,
+                       k > 0 ? 1u : 0u);
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              mma_ss(sb + 128, dk + ((kOpRope + 32 * k) >> 4), dQ + ((kQRope + 32 * k) >> 4), id_qkr, k > 0 ? 1u : 0u);
+            mma_commit(&bars[kBarSFull + sbuf]);
+            if (seg_end) mma_commit(&bars[kBarQEmpty]);
+            SMLA_TRACE_SET(tl, kEvQk);
+            ++next_qk;
+            kt_qk = kt_qk + 1 == p.nt ? 0 : kt_qk + 1;
+            ob_qk = ob_qk + 1 == kOpBufs ? 0 : ob_qk + 1;
             progressed = true;
           }
         }
@@ -646,24 +648,28 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(cons
     }
     __syncwarp();
   } else {
-    // ------------------------------------------------------------ softmax / epilogue (warps 0..3)
+    // ------------------------------------------------------------ softmax / epilogue (warps 0..7)
     // QK^T with M = 64 leaves tile row r in TMEM lane 32 (r / 16) + r % 16.
-    // Read with the 16x256b shape (and the Q row order of q_row_of_head),
-    // thread (w, lane) holds rows r0 = 16 w + lane / 4 and r1 = r0 + 8 for
-    // heads 4c .. 4c + 3 (c = lane % 4): item k (0..7) is row rho = (k >> 1) & 1
-    // of head 4c + i, i = (k & 1) + 2 (k >> 2).  Each thread keeps the running
-    // state of its 4 heads; the 16 heads are gathered by shuffles only where
-    // the P.V accumulator is rescaled.  For the P.V output (M = 128) thread tid
-    // owns value column tid of each chunk.
-    const int w = warp;
+    // Warp w reads lane quarter qd = w % 4 and the head columns of half
+    // hh = w / 4 with the 16x256b shape: thread (w, lane) holds rows
+    // r0 = 16 qd + lane / 4 and r1 = r0 + 8 of columns nA = 8 hh + 2 (lane % 4)
+    // and nA + 1; item k (0..3) is row k >> 1 of column nA + (k & 1).  Each
+    // thread keeps the running state of its 2 columns.  The two halves share
+    // nothing but the barriers on S, P' and O: each decides its own rescales
+    // and rescales its own columns of O.  For the P.V output (M = 128) thread
+    // lane of warp w owns value column 32 qd + lane of each chunk, for the
+    // columns of its half.
+    const int w = warp, qd = w & 3, hh = w >> 2;
     const int c4 = lane & 3;
-    const int r0 = 16 * w + (lane >> 2), r1 = r0 + 8;
-    const uint32_t lane_base = (uint32_t)(32 * w) << 16;
+    const int r0 = 16 * qd + (lane >> 2), r1 = r0 + 8;
+    const int nA = 8 * hh + 2 * c4;
+    const uint32_t lane_base = (uint32_t)(32 * qd) << 16;
     const uint32_t p0 = smem_u32(smem + kOffP);
+    const int bar_id = 1 + hh;  // named barrier of the half (4 warps)
     float* red_max = reinterpret_cast<float*>(smem + kOffRedMax);
     float* red_sc = reinterpret_cast<float*>(smem + kOffRedSc);
     float* red_sum = reinterpret_cast<float*>(smem + kOffRedSum);
-    float m4[4], l4[4], ip4[4], Rq[4];
+    float m2[2], l2[2], ip2[2], Rq[4];
     SMLA_CLK_DECL;
     int seg = -1, seg_first_kt = 0, n_seg_tiles = 0;
     bool dead = false;
@@ -675,128 +681,116 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(cons
     };
     for (int tl = 0; tl < n_local; ++tl) {
       const TileInfo ti = tile_info(p, xbeg + tl, xbeg, xend);
-      const int b = tl & 1;
+      const int ob = tl % kOpBufs, sbuf = tl & 1;
       if (ti.seg_start) {
         ++seg;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          m4[i] = -INFINITY;
-          l4[i] = 0.f;
-          Rq[i] = 0.f;
+        for (int e = 0; e < 2; ++e) {
+          m2[e] = -INFINITY;
+          l2[e] = 0.f;
         }
+#pragma unroll
+        for (int g = 0; g < 4; ++g) Rq[g] = 0.f;
         seg_first_kt = ti.kt;
         n_seg_tiles = 0;
       }
-      wait_s(kBarOpFull + b, (tl >> 1) & 1);  // row flags and scales
+      wait_s(kBarOpFull + ob, (tl / kOpBufs) & 1);  // row flags and scales
       if (tid == 0) SMLA_TRACE_SET(tl, kEvOpFull);
-      wait_s(kBarSFull + b, (tl >> 1) & 1);
+      wait_s(kBarSFull + sbuf, (tl >> 1) & 1);
       if (tid == 0) SMLA_TRACE_SET(tl, kEvSoftStart);
       SMLA_CLK_START();
       tc_fence_after();
       if (ti.seg_start) {
-        const float4 v = *reinterpret_cast<const float4*>(pre_ring + (seg & 3) * HG + 4 * c4);
-        ip4[0] = v.x;
-        ip4[1] = v.y;
-        ip4[2] = v.z;
-        ip4[3] = v.w;
+        const float2 v = *reinterpret_cast<const float2*>(pre_ring + (seg & 3) * HG + nA);
+        ip2[0] = v.x;
+        ip2[1] = v.y;
       }
-      const bool ok0 = !dead && valid[b * kRows + r0] != 0;
-      const bool ok1 = !dead && valid[b * kRows + r1] != 0;
+      const bool ok0 = !dead && valid[ob * kRows + r0] != 0;
+      const bool ok1 = !dead && valid[ob * kRows + r1] != 0;
       const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
-      const float4 s0 = ok0 ? *reinterpret_cast<const float4*>(smem + kOffOp + b * kOpBuf + kOpScale + 16 * r0) : zero4;
-      const float4 s1 = ok1 ? *reinterpret_cast<const float4*>(smem + kOffOp + b * kOpBuf + kOpScale + 16 * r1) : zero4;
+      const float4 s0 = ok0 ? *reinterpret_cast<const float4*>(smem + kOffOp + ob * kOpBuf + kOpScale + 16 * r0) : zero4;
+      const float4 s1 = ok1 ? *reinterpret_cast<const float4*>(smem + kOffOp + ob * kOpBuf + kOpScale + 16 * r1) : zero4;
       const float sc0[4] = {s0.x, s0.y, s0.z, s0.w};
       const float sc1[4] = {s1.x, s1.y, s1.z, s1.w};
       // logits (log2 units): 2^-s_h sum_g scale_g (S_g,hi + S_g,lo) + S_rope
-      float sl[8];
+      float sl[4];
       {
-        const uint32_t sa = tmem + lane_base + b * kSCols;
-        float acc[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) acc[k] = 0.f;
+        const uint32_t sa = tmem + lane_base + sbuf * kSCols + 8 * hh;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
         if (!dead) {
-          uint32_t hi[4][8], lo[4][8], rp[8];
+          uint32_t hi[4][4], lo[4][4], rp[4];
 #pragma unroll
           for (int g = 0; g < 4; ++g) {
-            tmem_ld_16x256b_x2(sa + 32 * g, hi[g]);
-            tmem_ld_16x256b_x2(sa + 32 * g + 16, lo[g]);
+            tmem_ld_16x256b_x1(sa + 32 * g, hi[g]);
+            tmem_ld_16x256b_x1(sa + 32 * g + 16, lo[g]);
           }
-          tmem_ld_16x256b_x2(sa + 128, rp);
+          tmem_ld_16x256b_x1(sa + 128, rp);
           tmem_ld_wait();
 #pragma unroll
           for (int g = 0; g < 4; ++g) {
-            reg_fence8(hi[g]);
-            reg_fence8(lo[g]);
+            reg_fence4(hi[g]);
+            reg_fence4(lo[g]);
           }
-          reg_fence8(rp);
+          reg_fence4(rp);
 #pragma unroll
           for (int g = 0; g < 4; ++g)
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-              acc[k] = fmaf(((k >> 1) & 1) ? sc1[g] : sc0[g], __uint_as_float(hi[g][k]) + __uint_as_float(lo[g][k]),
-                            acc[k]);
+            for (int k = 0; k < 4; ++k)
+              acc[k] = fmaf((k >> 1) ? sc1[g] : sc0[g], __uint_as_float(hi[g][k]) + __uint_as_float(lo[g][k]), acc[k]);
 #pragma unroll
-          for (int k = 0; k < 8; ++k) acc[k] = fmaf(acc[k], ip4[(k & 1) + 2 * (k >> 2)], __uint_as_float(rp[k]));
+          for (int k = 0; k < 4; ++k) acc[k] = fmaf(acc[k], ip2[k & 1], __uint_as_float(rp[k]));
         }
 #pragma unroll
-        for (int k = 0; k < 8; ++k) sl[k] = (((k >> 1) & 1) ? ok1 : ok0) ? acc[k] * p.scale_log2 : -INFINITY;
+        for (int k = 0; k < 4; ++k) sl[k] = ((k >> 1) ? ok1 : ok0) ? acc[k] * p.scale_log2 : -INFINITY;
       }
       if (tid == 0) SMLA_TRACE_SET(tl, kEvSoftLogits);
       SMLA_CLK_MARK(0);
-      // tile maxima: per head (logits) and per scale group (scales), across the 64 rows
+      // tile maxima: per column (logits) and per scale group (scales), across the 64 rows
       float* redm = red_max + (tl & 1) * 4 * HG;
-      float* reds = red_sc + (tl & 1) * 4 * 4;
+      float* reds = red_sc + ((tl & 1) * 2 + hh) * 4 * 4;
       {
-        float t4[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int k = (i & 1) + 4 * (i >> 1);  // row r0 item of head slot i; row r1 item is k + 2
-          t4[i] = fmaxf(sl[k], sl[k + 2]);
-        }
+        float t2[2] = {fmaxf(sl[0], sl[2]), fmaxf(sl[1], sl[3])};
         float s4[4];
 #pragma unroll
         for (int g = 0; g < 4; ++g) s4[g] = fmaxf(sc0[g], sc1[g]);
 #pragma unroll
-        for (int off = 4; off <= 16; off <<= 1)
+        for (int off = 4; off <= 16; off <<= 1) {
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            t4[i] = fmaxf(t4[i], __shfl_xor_sync(kFullMask, t4[i], off));
-            s4[i] = fmaxf(s4[i], __shfl_xor_sync(kFullMask, s4[i], off));
-          }
-        if (lane < 4) *reinterpret_cast<float4*>(redm + w * HG + 4 * c4) = make_float4(t4[0], t4[1], t4[2], t4[3]);
-        if (lane == 0) *reinterpret_cast<float4*>(reds + w * 4) = make_float4(s4[0], s4[1], s4[2], s4[3]);
+          for (int e = 0; e < 2; ++e) t2[e] = fmaxf(t2[e], __shfl_xor_sync(kFullMask, t2[e], off));
+#pragma unroll
+          for (int g = 0; g < 4; ++g) s4[g] = fmaxf(s4[g], __shfl_xor_sync(kFullMask, s4[g], off));
+        }
+        if (lane < 4) *reinterpret_cast<float2*>(redm + qd * HG + nA) = make_float2(t2[0], t2[1]);
+        if (lane == 0) *reinterpret_cast<float4*>(reds + qd * 4) = make_float4(s4[0], s4[1], s4[2], s4[3]);
       }
-      named_bar_sync(1, 128);
+      named_bar_sync(bar_id, 128);
       if (tid == 0) SMLA_TRACE_SET(tl, kEvSoftBar);
       SMLA_CLK_MARK(1);
-      // running maxima of the own heads (lazy: refreshed only when the tile
+      // running maxima of the own columns (lazy: refreshed only when the tile
       // maximum exceeds them by more than kMaxSlack) and power-of-two bounds
       // of the scale groups
-      float alpha4[4], beta[4];
+      float alpha2[2], beta[4];
       bool up_any = false, rq_changed = false;
       {
-        float4 a[4], c[4];
+        float2 a[4];
+        float4 c[4];
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
-          a[v] = *reinterpret_cast<const float4*>(redm + v * HG + 4 * c4);
+          a[v] = *reinterpret_cast<const float2*>(redm + v * HG + nA);
           c[v] = *reinterpret_cast<const float4*>(reds + 4 * v);
         }
-        const float tmax[4] = {fmaxf(fmaxf(a[0].x, a[1].x), fmaxf(a[2].x, a[3].x)),
-                               fmaxf(fmaxf(a[0].y, a[1].y), fmaxf(a[2].y, a[3].y)),
-                               fmaxf(fmaxf(a[0].z, a[1].z), fmaxf(a[2].z, a[3].z)),
-                               fmaxf(fmaxf(a[0].w, a[1].w), fmaxf(a[2].w, a[3].w))};
-        const float smax[4] = {fmaxf(fmaxf(c[0].x, c[1].x), fmaxf(c[2].x, c[3].x)),
-                               fmaxf(fmaxf(c[0].y, c[1].y), fmaxf(c[2].y, c[3].y)),
-                               fmaxf(fmaxf(c[0].z, c[1].z), fmaxf(c[2].z, c[3].z)),
-                               fmaxf(fmaxf(c[0].w, c[1].w), fmaxf(c[2].w, c[3].w))};
+        const float tmax[2] = {fmaxf(fmaxf(a[0].x, a[1].x), fmaxf(a[2].x, a[3].x)),
+                               fmaxf(fmaxf(a[0].y, a[1].y), fmaxf(a[2].y, a[3].y))};
+        const float smax[4] = {fmaxf(fmaxf(c[0].x, c[1].x), fmaxf(c[2].x, c[3].x)), fmaxf(fmaxf(c[0].y, c[1].y), fmaxf(c[2].y, c[3].y)),
+                               fmaxf(fmaxf(c[0].z, c[1].z), fmaxf(c[2].z, c[3].z)), fmaxf(fmaxf(c[0].w, c[1].w), fmaxf(c[2].w, c[3].w))};
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float nm = fmaxf(m4[i], tmax[i]);
-          const bool up = nm > m4[i] + kMaxSlack;
+        for (int e = 0; e < 2; ++e) {
+          const float nm = fmaxf(m2[e], tmax[e]);
+          const bool up = nm > m2[e] + kMaxSlack;
           const float mnew = nm + kMaxOvershoot;
-          alpha4[i] = up ? ex2_approx(m4[i] - mnew) : 1.f;
-          m4[i] = up ? mnew : m4[i];
-          l4[i] *= alpha4[i];
+          alpha2[e] = up ? ex2_approx(m2[e] - mnew) : 1.f;
+          m2[e] = up ? mnew : m2[e];
+          l2[e] *= alpha2[e];
           up_any |= up;
         }
 #pragma unroll
@@ -808,7 +802,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(cons
           Rq[g] = rn;
         }
       }
-      // every warp sees all 16 heads (lanes 0..3) and the same shared maxima: the decision is CTA-uniform
+      // every warp of a half sees all 8 of its columns (lanes 0..3) and the same
+      // shared maxima: the decision is uniform over the half
       const bool rescale = __any_sync(kFullMask, up_any) || rq_changed;
 #ifdef SMLA_TRACE
       if (n_seg_tiles > 0) {
@@ -819,49 +814,49 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(cons
 #endif
       SMLA_CLK_MARK(2);
       if (rescale && n_seg_tiles > 0) {
-        // O^T holds this segment's earlier P.V: wait for the latest and rescale in place
-        float alpha[HG];
+        // O^T holds this segment's earlier P.V: wait for the latest and rescale
+        // this half's columns in place (column 8 hh + j: alpha of lane j / 2)
+        float alpha[8];
 #pragma unroll
-        for (int h = 0; h < HG; ++h) alpha[h] = __shfl_sync(kFullMask, alpha4[h & 3], h >> 2);
+        for (int j = 0; j < 8; ++j) alpha[j] = __shfl_sync(kFullMask, alpha2[j & 1], j >> 1);
         wait_s(kBarPvDone + ((tl - 1) & 1), ((tl - 1) >> 1) & 1);  // P.V(tl - 1) and all before
         if (!dead) {
           tc_fence_after();
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            uint32_t oh[16], ol[16];
-            const uint32_t addr = tmem + lane_base + kOCol + 32 * q;
-            tmem_ld16(addr, oh);
-            tmem_ld16(addr + 16, ol);
+            uint32_t oh[8], ol[8];
+            const uint32_t addr = tmem + lane_base + kOCol + 32 * q + 8 * hh;
+            tmem_ld8(addr, oh);
+            tmem_ld8(addr + 16, ol);
             tmem_ld_wait();
-            reg_fence16(oh);
-            reg_fence16(ol);
+            reg_fence8(oh);
+            reg_fence8(ol);
 #pragma unroll
-            for (int h = 0; h < HG; ++h) {
-              const float f = alpha[h] * beta[q];
-              oh[h] = __float_as_uint(__uint_as_float(oh[h]) * f);
-              ol[h] = __float_as_uint(__uint_as_float(ol[h]) * f);
+            for (int j = 0; j < 8; ++j) {
+              const float f = alpha[j] * beta[q];
+              oh[j] = __float_as_uint(__uint_as_float(oh[j]) * f);
+              ol[j] = __float_as_uint(__uint_as_float(ol[j]) * f);
             }
-            tmem_st16(addr, oh);
-            tmem_st16(addr + 16, ol);
+            tmem_st8(addr, oh);
+            tmem_st8(addr + 16, ol);
           }
           tmem_st_wait();
         }
       }
       SMLA_CLK_MARK(3);
       // probabilities and running sums
-      float pr[8];
+      float pr[4];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int i = (k & 1) + 2 * (k >> 2);
-        pr[k] = (((k >> 1) & 1) ? ok1 : ok0) ? ex2_approx(sl[k] - m4[i]) : 0.f;
-        l4[i] += pr[k];
+      for (int k = 0; k < 4; ++k) {
+        pr[k] = ((k >> 1) ? ok1 : ok0) ? ex2_approx(sl[k] - m2[k & 1]) : 0.f;
+        l2[k & 1] += pr[k];
       }
       SMLA_CLK_MARK(4);
-      if (tl >= 2) wait_s(kBarPvDone + (tl & 1), ((tl - 2) >> 1) & 1);  // P buffer free: P.V(tl - 2) done
+      if (tl >= 2) wait_s(kBarPvDone + sbuf, ((tl - 2) >> 1) & 1);  // P buffer free: P.V(tl - 2) done
       if (tid == 0) SMLA_TRACE_SET(tl, kEvSoftPWait);
       SMLA_CLK_MARK(5);
       // P'_q = kPScale * p * scale_q / R_q as e4m3 hi + lo: MN-major core
-      // matrices of 8 rows x 16 codes (heads), hi and lo blocks 128 B apart,
+      // matrices of 8 rows x 16 codes (columns), hi and lo blocks 128 B apart,
       // row blocks 256 B apart
       if (!dead) {
 #pragma unroll
@@ -872,53 +867,56 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(cons
             const int r = rho ? r1 : r0;
             const float f = (rho ? sc1[g] : sc0[g]) * inv_r;
             uint32_t hw, lw;
-            split4(pr[2 * rho] * f, pr[2 * rho + 1] * f, pr[4 + 2 * rho] * f, pr[5 + 2 * rho] * f, hw, lw);
-            const uint32_t base = p0 + ((tl & 1) * 4 + g) * kPGroup + (r >> 3) * 256 + (r & 7) * 16 + 4 * c4;
-            sts32(base, hw);
-            sts32(base + 128, lw);
+            split2_f16(pr[2 * rho] * f, pr[2 * rho + 1] * f, hw, lw);
+            const uint32_t base = p0 + sbuf * kPBuf + g * kPGroup + (r >> 3) * 256 + (r & 7) * 16 + nA;
+            sts16(base, hw);
+            sts16(base + 128, lw);
           }
         }
       }
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0 && !dead) mbar_arrive(&bars[kBarPFull + (tl & 1)]);
+      if (lane == 0 && !dead) mbar_arrive(&bars[kBarPFull + sbuf]);
       if (tid == 0) SMLA_TRACE_SET(tl, kEvSoftDone);
       SMLA_CLK_MARK(6);
       ++n_seg_tiles;
 
       if (ti.seg_end) {
         {
-          float v4[4] = {l4[0], l4[1], l4[2], l4[3]};
+          float v2[2] = {l2[0], l2[1]};
 #pragma unroll
           for (int off = 4; off <= 16; off <<= 1)
 #pragma unroll
-            for (int i = 0; i < 4; ++i) v4[i] += __shfl_xor_sync(kFullMask, v4[i], off);
-          if (lane < 4) *reinterpret_cast<float4*>(red_sum + w * HG + 4 * c4) = make_float4(v4[0], v4[1], v4[2], v4[3]);
+            for (int e = 0; e < 2; ++e) v2[e] += __shfl_xor_sync(kFullMask, v2[e], off);
+          if (lane < 4) *reinterpret_cast<float2*>(red_sum + qd * HG + nA) = make_float2(v2[0], v2[1]);
         }
-        named_bar_sync(1, 128);
-        wait_s(kBarPvDone + (tl & 1), (tl >> 1) & 1);  // last P.V of the segment
+        named_bar_sync(bar_id, 128);
+        wait_s(kBarPvDone + sbuf, (tl >> 1) & 1);  // last P.V of the segment
         tc_fence_after();
         const bool full = (seg_first_kt == 0) && (ti.kt == p.nt - 1);
         const int64_t slot = (int64_t)blockIdx.x + ti.u;
-        float inv[HG];
+        const int64_t row0 = (int64_t)ti.t * p.H + ti.hg * HG;
+        float inv[8];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float4 a0 = *reinterpret_cast<const float4*>(red_sum + 4 * j);
-          const float4 a1 = *reinterpret_cast<const float4*>(red_sum + HG + 4 * j);
-          const float4 a2 = *reinterpret_cast<const float4*>(red_sum + 2 * HG + 4 * j);
-          const float4 a3 = *reinterpret_cast<const float4*>(red_sum + 3 * HG + 4 * j);
+        for (int j4 = 0; j4 < 2; ++j4) {
+          const int n0 = 8 * hh + 4 * j4;
+          const float4 a0 = *reinterpret_cast<const float4*>(red_sum + n0);
+          const float4 a1 = *reinterpret_cast<const float4*>(red_sum + HG + n0);
+          const float4 a2 = *reinterpret_cast<const float4*>(red_sum + 2 * HG + n0);
+          const float4 a3 = *reinterpret_cast<const float4*>(red_sum + 3 * HG + n0);
           const float lt[4] = {(a0.x + a1.x) + (a2.x + a3.x), (a0.y + a1.y) + (a2.y + a3.y),
                                (a0.z + a1.z) + (a2.z + a3.z), (a0.w + a1.w) + (a2.w + a3.w)};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            inv[4 * j + e] = lt[e] > 0.f ? __frcp_rn(lt[e]) : 0.f;
-            // lse of head 4j + e from the thread that holds its running maximum
-            if (w == 0 && lane == j) {
-              const float lse_v = lt[e] > 0.f ? (m4[e] + log2f(lt[e])) * 0.69314718055994530942f : -INFINITY;
-              const int h = 4 * j + e;
+            inv[4 * j4 + e] = lt[e] > 0.f ? __frcp_rn(lt[e]) : 0.f;
+            // lse of column n0 + e from the thread that holds its running maximum
+            const int n = n0 + e;
+            if (qd == 0 && lane == ((n & 7) >> 1)) {
+              const float lse_v = lt[e] > 0.f ? (m2[n & 1] + log2f(lt[e])) * 0.69314718055994530942f : -INFINITY;
+              const int h = head_of_col(n);
               if (full)
-                p.lse[(int64_t)ti.t * p.H + ti.hg * HG + h] = lse_v;
+                p.lse[row0 + h] = lse_v;
               else
                 p.part_lse[slot * HG + h] = lse_v;
             }
@@ -927,19 +925,20 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(cons
         if (!dead) {
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            uint32_t ohi[16], olo[16];
-            tmem_ld16(tmem + lane_base + kOCol + 32 * q, ohi);
-            tmem_ld16(tmem + lane_base + kOCol + 32 * q + 16, olo);
+            uint32_t ohi[8], olo[8];
+            tmem_ld8(tmem + lane_base + kOCol + 32 * q + 8 * hh, ohi);
+            tmem_ld8(tmem + lane_base + kOCol + 32 * q + 16 + 8 * hh, olo);
             tmem_ld_wait();
-            reg_fence16(ohi);
-            reg_fence16(olo);
-            const int c = 128 * q + tid;
+            reg_fence8(ohi);
+            reg_fence8(olo);
+            const int c = 128 * q + 32 * qd + lane;
             const float rs = Rq[q] * kPScaleInv;
 #pragma unroll
-            for (int h = 0; h < HG; ++h) {
-              const float val = (__uint_as_float(ohi[h]) + __uint_as_float(olo[h])) * rs * inv[h];
+            for (int j = 0; j < 8; ++j) {
+              const int h = head_of_col(8 * hh + j);
+              const float val = (__uint_as_float(ohi[j]) + __uint_as_float(olo[j])) * rs * inv[j];
               if (full)
-                p.out[((int64_t)ti.t * p.H + ti.hg * HG + h) * kDv + c] = __float2bfloat16_rn(val);
+                p.out[(row0 + h) * kDv + c] = __float2bfloat16_rn(val);
               else
                 p.part_o[(slot * HG + h) * kDv + c] = val;
             }
@@ -961,6 +960,40 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(cons
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+}
+
+// ---------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// The driver's tensor-map encoder, looked up once through the runtime.
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+// The cache as a 2-D array [NB * 64 rows][164 four-byte words] (row stride
+// 656 bytes), box 164 x 1, no swizzle: one tile::gather4 copies 4 whole rows;
+// rows outside [0, NB * 64) read as zeros.
+cudaError_t make_row_map(const uint8_t* cache, int64_t NB, CUtensorMap* map) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t gdim[2] = {(cuuint64_t)(kRowBytes / 4), (cuuint64_t)(NB * kBlock)};
+  const cuuint64_t gstride[1] = {(cuuint64_t)kRowBytes};
+  const cuuint32_t box[2] = {(cuuint32_t)(kRowBytes / 4), 1}, es[2] = {1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint8_t*>(cache), gdim, gstride, box, es,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 }  // namespace
@@ -1021,7 +1054,10 @@ cudaError_t launch_decode_fp8(const AttnArgs& a, const AttnPlan& plan, cudaStrea
   p.nt = plan.nt;
   p.total = plan.total;
   p.G = plan.G;
-  sparse_mla_decode_fp8_kernel<<<plan.G, kThreads, kSmemAlloc, stream>>>(p);
+  CUtensorMap row_map;
+  cudaError_t em = make_row_map(a.cache, a.NB, &row_map);
+  if (em != cudaSuccess) return em;
+  sparse_mla_decode_fp8_kernel<<<plan.G, kThreads, kSmemAlloc, stream>>>(p, row_map);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || !plan.need_combine) return e;
   combine_kernel<HG><<<(unsigned)(plan.units * kCombineSplit), kCombineThreads, 0, stream>>>(p.part_o, p.part_lse, p.out, p.lse, p.H, p.n_hg, p.nt,
