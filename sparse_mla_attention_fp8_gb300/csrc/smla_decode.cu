@@ -11,17 +11,15 @@
 //
 // Design: the tensor cores read the cache codes as stored, with no
 // dequantization pass.
-//  * Transport: TMA tile::gather4 copies of whole rows (the cache viewed as a
-//    2-D array of 164 4-byte words per row, box 164 x 1), four rows per
-//    instruction, into 3 raw stages of 32 rows.  Issuing copies costs the
-//    issuing warp about as many cycles as bytes / 16, so three warps issue, each
-//    for its own raw stage, with 8 lanes issuing one gather4 each.
-//  * Layout: the same three warps move each landed row's 16-byte chunks to
-//    their 128-byte-swizzled operand positions in a 64-row tile
-//    (the 512 e4m3 codes as four K-major panels, the 64 bf16 RoPE values as a
-//    fifth panel, the four float32 scales beside them); invalid rows are
-//    zero-filled.  Three operand tiles, so that the rearrange of a tile never
-//    waits for the P.V of the tile before.
+//  * Transport: TMA tile::gather4 copies straight into the operand tiles,
+//    four rows per instruction: the 512 e4m3 codes as four K-major panels with
+//    the 128-byte swizzle (64 rows x 128 bytes each), the 64 bf16 RoPE values
+//    as a fifth panel, the four float32 scales beside them.  Invalid rows are
+//    gathered at row -1, which the TMA zero-fills.  Four loader warps, one per
+//    16-row quarter of every tile, each lane issuing one copy: the cost of
+//    issuing copies falls on the issuing warp, so it is spread.  Four operand
+//    tiles, so that the loads of the next tiles are in flight while one is
+//    in use.
 //  * Q is split once per (token, 16-head group) into two e4m3 terms,
 //    q * 2^s_h = hi + lo (s_h a per-head power of two putting max |q| near
 //    448), exact for all but negligibly small components; hi and lo are the
@@ -44,8 +42,7 @@
 //    output stores translate.
 //  * Warp roles: softmax / epilogue (8 warps: two per TMEM lane quarter, one
 //    per half of the 16 head columns), tensor-core issuer (1 thread), index
-//    translation (1 warp), bulk-copy producer (1 warp), rearrange (3 warps),
-//    Q preparation (2 warps).
+//    translation (1 warp), loaders (4 warps), Q preparation (2 warps).
 #include <cstdint>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -79,8 +76,8 @@ enum { kEvIdx = 0, kEvRawLanded = 1, kEvOpFull = 2, kEvQk = 3, kEvSoftStart = 4,
       g_smla_trace_fp8[((size_t)blockIdx.x * kTraceTiles + (tl)) * kTraceEvents + (ev)] = globaltimer_ns();    \
   } while (0)
 // Cycle counters of the softmax sections (thread 0), stored after the per-tile events.
-#define SMLA_CLK_DECL unsigned clk_acc[12] = {0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0}, clk_prev = (unsigned)clock()
-#define SMLA_CLK_START() (clk_prev = (unsigned)clock())
+#define SMLA_CLK_DECL unsigned clk_acc[16] = {0}, clk_prev = (unsigned)clock()
+#define SMLA_CLK_START() SMLA_CLK_MARK(13)
 #define SMLA_CLK_MARK(i)                   \
   do {                                     \
     const unsigned now_ = (unsigned)clock(); \
@@ -90,8 +87,8 @@ enum { kEvIdx = 0, kEvRawLanded = 1, kEvOpFull = 2, kEvQk = 3, kEvSoftStart = 4,
 #define SMLA_CLK_STORE()                                                                                        \
   do {                                                                                                          \
     if (g_smla_trace_fp8 && tid == 0)                                                                           \
-      for (int i_ = 0; i_ < 12; ++i_)                                                                           \
-        g_smla_trace_fp8[(size_t)gridDim.x * kTraceTiles * kTraceEvents + blockIdx.x * 12 + i_] = clk_acc[i_]; \
+      for (int i_ = 0; i_ < 16; ++i_)                                                                           \
+        g_smla_trace_fp8[(size_t)gridDim.x * kTraceTiles * kTraceEvents + blockIdx.x * 16 + i_] = clk_acc[i_]; \
   } while (0)
 #else
 #define SMLA_TRACE_SET(tl, ev) ((void)0)
@@ -103,9 +100,8 @@ enum { kEvIdx = 0, kEvRawLanded = 1, kEvOpFull = 2, kEvQk = 3, kEvSoftStart = 4,
 
 constexpr int HG = 16;                 // heads per CTA work unit
 constexpr int kRows = 64;              // top-k rows per tile
-constexpr int kRawRows = 32;           // rows per raw stage (two stages per tile)
-constexpr int kRawStages = 3;          // raw ring depth (96 rows in flight); stage s is rearranged by warp s % 3
-constexpr int kOpBufs = 3;             // operand tiles
+constexpr int kLoaders = 4;            // loader warps: loader lw gathers rows 16 lw .. 16 lw + 15 of every tile
+constexpr int kOpBufs = 4;             // operand tiles
 constexpr float kMaxSlack = 1.75f;     // log2 growth of a head's max tolerated before rescaling O (p <= 2^1.75)
 constexpr float kMaxOvershoot = 0.75f; // a refreshed running max is set this far above the tile max
 constexpr float kPScale = 128.0f;      // P' = kPScale * p * scale / R  <=  128 * 2^1.75 < 430 (e4m3 max 448)
@@ -114,10 +110,8 @@ constexpr float kPScaleInv = 1.0f / 128.0f;
 // ---- shared memory layout (offsets from a 1024-byte aligned base)
 constexpr int kPanel = kRows * 128;                   // 8 KB: 64 rows x 128 bytes
 constexpr int kOpRope = 4 * kPanel;                   // RoPE panel after the 4 code panels
-constexpr int kOpScale = 5 * kPanel;                  // 64 x 16-byte scale rows
-constexpr int kOpBuf = 5 * kPanel + kRows * 16;       // 41984
-constexpr int kGroupBytes = 2688;                     // 4 gathered rows (2624 bytes) padded to 128-byte alignment
-constexpr int kRawStage = (kRawRows / 4) * kGroupBytes;  // 21504
+constexpr int kOpScale = 5 * kPanel;                  // scales: 16 groups of 4 rows x 16 bytes, 128 bytes apart
+constexpr int kOpBuf = 5 * kPanel + (kRows / 4) * 128;  // 43008
 constexpr int kQPanel = 32 * 128;                     // 32 operand rows (hi, lo) x 128 codes
 constexpr int kQRope = 4 * kQPanel;                   // 16 rows x 64 bf16
 constexpr int kQBuf = 4 * kQPanel + HG * 128;         // 18432
@@ -126,27 +120,24 @@ constexpr int kPBuf = 4 * kPGroup;                    // 8192
 constexpr int kOffOp = 0;
 constexpr int kOffQ = kOffOp + kOpBufs * kOpBuf;
 constexpr int kOffP = kOffQ + kQBuf;
-constexpr int kOffRaw = kOffP + 2 * kPBuf;            // P' double-buffered
-constexpr int kOffSlots = kOffRaw + kRawStages * kRawStage;         // int32 [4][64]
-constexpr int kOffValid = kOffSlots + 4 * kRows * 4;                // uint8 [3][64]
+constexpr int kOffSlots = kOffP + 2 * kPBuf;                       // P' double-buffered; int32 [4][64]
+constexpr int kOffValid = kOffSlots + 4 * kRows * 4;                // uint8 [4][64]
 constexpr int kOffPre = kOffValid + kOpBufs * kRows;                // float [4][16 columns] inverse Q prescales
 constexpr int kOffRedMax = kOffPre + 4 * HG * 4;                    // float [2][4 quarters][16 columns]
 constexpr int kOffRedSc = kOffRedMax + 2 * 4 * HG * 4;              // float [2][2 halves][4 quarters][4]
 constexpr int kOffRedSum = kOffRedSc + 2 * 2 * 4 * 4 * 4;           // float [4 quarters][16 columns]
-constexpr int kOffDummy = kOffRedSum + 4 * HG * 4;  // 16 bytes per rearrange lane: sink for idle lanes
-constexpr int kOffBar = kOffDummy + kRawStages * 32 * 16;
+constexpr int kOffBar = kOffRedSum + 4 * HG * 4;
 enum {
   kBarOpFull = 0, kBarOpEmpty = kBarOpFull + kOpBufs, kBarSFull = kBarOpEmpty + kOpBufs, kBarPFull = kBarSFull + 2,
   kBarPvDone = kBarPFull + 2, kBarIdxFull = kBarPvDone + 2, kBarIdxEmpty = kBarIdxFull + 4,
-  kBarQFull = kBarIdxEmpty + 4, kBarQEmpty = kBarQFull + 1, kBarOFree = kBarQEmpty + 1, kBarRawFull = kBarOFree + 1,
-  kBarDrain = kBarRawFull + kRawStages, kNumBars = kBarDrain + 1
+  kBarQFull = kBarIdxEmpty + 4, kBarQEmpty = kBarQFull + 1, kBarOFree = kBarQEmpty + 1, kBarDrain = kBarOFree + 1,
+  kNumBars = kBarDrain + 1
 };
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 16;
 constexpr int kSmemAlloc = kSmemBytes + 1024;
 static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0 && kOpBuf % 1024 == 0, "operand alignment");
-static_assert(kOffRaw % 128 == 0 && kRawStage % 128 == 0 && kGroupBytes % 128 == 0 && kOffBar % 8 == 0,
-              "TMA destinations 128-byte aligned; barriers 8-byte aligned");
+static_assert(kOffBar % 8 == 0, "barriers 8-byte aligned");
 static_assert(kOffPre % 16 == 0 && kOffRedMax % 16 == 0 && kOffRedSc % 16 == 0 && kOffRedSum % 16 == 0, "float4");
 static_assert(kSmemAlloc <= 232448, "shared memory budget");
 
@@ -156,14 +147,13 @@ constexpr int kOCol = 2 * kSCols;     // O^T: 4 chunks x (hi, lo) x 16 heads
 constexpr int kTmemCols = 512;
 static_assert(kOCol + 4 * 32 <= kTmemCols, "tensor memory budget");
 
-// ---- warp roles (15 warps; 128 registers per thread).  Warp w runs on
+// ---- warp roles (16 warps; 128 registers per thread).  Warp w runs on
 // sub-partition w % 4: each sub-partition carries two softmax warps (one per
-// head half) and one or two of the other roles.
-constexpr int kSoftWarps = 8, kRearrWarp0 = 8, kRearrWarps = kRawStages, kMmaWarp = 11, kIndexWarp = 12,
-              kQWarp0 = 13, kQWarps = 2;
-constexpr int kNumWarps = 15;
+// head half), a loader and one more role.
+constexpr int kSoftWarps = 8, kLoadWarp0 = 8, kMmaWarp = 12, kIndexWarp = 13, kQWarp0 = 14, kQWarps = 2;
+constexpr int kNumWarps = 16;
 constexpr int kThreads = 32 * kNumWarps;
-static_assert(kRearrWarp0 + kRearrWarps == kMmaWarp && kQWarp0 + kQWarps == kNumWarps, "warp roles");
+static_assert(kLoadWarp0 + kLoaders == kMmaWarp && kQWarp0 + kQWarps == kNumWarps, "warp roles");
 
 __host__ __device__ constexpr uint32_t idesc_e4m3(uint32_t M, uint32_t N, uint32_t a_mn, uint32_t b_mn) {
   return (1u << 4) | (a_mn << 15) | (b_mn << 16) | ((N >> 3) << 17) | ((M >> 4) << 24);
@@ -215,11 +205,6 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
   asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
 }
 
-__device__ __forceinline__ uint4 lds128(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
-  return v;
-}
 
 __device__ __forceinline__ void named_bar_sync(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
@@ -294,13 +279,9 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-// Shared address of row i of a raw stage (4-row gather groups, 128-byte aligned).
-__device__ __forceinline__ uint32_t raw_row(uint32_t raw, int i) {
-  return raw + (uint32_t)((i >> 2) * kGroupBytes + (i & 3) * kRowBytes);
-}
-
 __global__ void __launch_bounds__(kThreads, 1)
-    sparse_mla_decode_fp8_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap row_map) {
+    sparse_mla_decode_fp8_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap panel_map,
+                                 const __grid_constant__ CUtensorMap scale_map) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
@@ -317,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     for (int i = 0; i < kOpBufs; ++i) {
-      mbar_init(&bars[kBarOpFull + i], 2);  // one arrival per 32-row half
+      mbar_init(&bars[kBarOpFull + i], kLoaders);  // one arrival (with its bytes) per loader
       mbar_init(&bars[kBarOpEmpty + i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -327,9 +308,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 4; ++i) {
       mbar_init(&bars[kBarIdxFull + i], 32);
-      mbar_init(&bars[kBarIdxEmpty + i], 2);  // one arrival per 32-row half
+      mbar_init(&bars[kBarIdxEmpty + i], kLoaders);
     }
-    for (int i = 0; i < kRawStages; ++i) mbar_init(&bars[kBarRawFull + i], 1);
     mbar_init(&bars[kBarQFull], kQWarps);
     mbar_init(&bars[kBarQEmpty], 1);
     mbar_init(&bars[kBarOFree], kSoftWarps);
@@ -376,94 +356,48 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < 2; ++i) cur[i] = nxt[i];
       req_cur = req_nxt;
     }
-  } else if (warp >= kRearrWarp0 && warp < kRearrWarp0 + kRearrWarps) {
-    // ------------------------------------------------------------ load + rearrange
-    // Warp rw handles the 32-row stages s = rw, rw + 3, ... (rows 32 (s % 2)
-    // .. +31 of tile s / 2) in its own raw stage rw.  Lanes 0..7 each issue one
-    // gather4 of 4 whole rows (invalid rows at row -1: the TMA zero-fills
-    // them); once they have landed, lane l moves code chunk l (bytes
-    // 16l..16l+15) of each row to panel l/8 at its swizzled position, in
-    // batches of 8 rows.  The 9-chunk tails (4 scales, then 8 RoPE chunks) of
-    // the batch's 8 rows are 72 moves spread over three rounds of the 32
-    // lanes; idle lanes store to a private sink.  Everything is branch-free so
-    // that a batch's loads are all in flight before its stores; invalid rows
-    // are zero-filled by selects.
-    const int rw = warp - kRearrWarp0;
-    const int chunk = lane & 7, panel = lane >> 3;
-    const uint32_t sink = smem_u32(smem + kOffDummy + (rw * 32 + lane) * 16);
-    const int rs = rw;
-    const uint32_t raw = smem_u32(smem + kOffRaw + rs * kRawStage);
-    int issued = 0;
-    for (int s = rw; s < 2 * n_local; s += kRawStages) {
-      const int tl = s >> 1, half = s & 1, b4 = tl & 3;
-      const int ob = tl % kOpBufs, use = tl / kOpBufs;
+  } else if (warp >= kLoadWarp0 && warp < kLoadWarp0 + kLoaders) {
+    // ------------------------------------------------------------ loaders
+    // Loader lw gathers rows 16 lw .. 16 lw + 15 of every tile: 4 groups of 4
+    // rows x 6 copies (code panels 0..3, RoPE panel, scales), lane 6 g + b
+    // issuing copy b of group g.  Its one arrival on the tile's full barrier
+    // carries the bytes of its 16 rows and follows its writes of the rows'
+    // valid flags.
+    const int lw = warp - kLoadWarp0;
+    const int grp = lane / 6, box = lane % 6;  // lanes 0..23 issue
+    const int r_g = 16 * lw + 4 * grp;         // tile row of the lane's group
+    int last_ob = -1, last_use = 0;
+    for (int tl = 0; tl < n_local; ++tl) {
+      const int b4 = tl & 3, ob = tl % kOpBufs, use = tl / kOpBufs;
       if (!SMLA_WAIT(kBarIdxFull + b4, (tl >> 2) & 1)) break;
-      const int32_t slot = slots_ring[b4 * kRows + kRawRows * half + lane];
+      const int32_t slot = lane < 16 ? slots_ring[b4 * kRows + 16 * lw + lane] : -1;
       const uint32_t vmask = __ballot_sync(kFullMask, slot >= 0);
       const int row = slot >= 0 ? slot : -1;
-      const int g0 = __shfl_sync(kFullMask, row, (4 * lane) & 31), g1 = __shfl_sync(kFullMask, row, (4 * lane + 1) & 31);
-      const int g2 = __shfl_sync(kFullMask, row, (4 * lane + 2) & 31), g3 = __shfl_sync(kFullMask, row, (4 * lane + 3) & 31);
-      if (lane == 0) {
-        mbar_arrive(&bars[kBarIdxEmpty + b4]);  // this half's slots read
-        mbar_arrive_expect_tx(&bars[kBarRawFull + rs], kRawRows * kRowBytes);
-      }
-      __syncwarp();
-      if (lane < 8) tma_gather4(raw + lane * kGroupBytes, &row_map, 0, g0, g1, g2, g3, &bars[kBarRawFull + rs]);
-      if (lane == 0) SMLA_TRACE_SET(tl, half ? kEvIssueH1 : kEvIssue);
-      ++issued;
-      if (!SMLA_WAIT(kBarRawFull + rs, (s / kRawStages) & 1)) break;
-      if (lane == 0) SMLA_TRACE_SET(tl, half ? kEvRawFullH1 : kEvRawFull);
+      const int g0 = __shfl_sync(kFullMask, row, (4 * grp) & 31), g1 = __shfl_sync(kFullMask, row, (4 * grp + 1) & 31);
+      const int g2 = __shfl_sync(kFullMask, row, (4 * grp + 2) & 31), g3 = __shfl_sync(kFullMask, row, (4 * grp + 3) & 31);
+      if (lane == 0) mbar_arrive(&bars[kBarIdxEmpty + b4]);  // this quarter's slots read
       if (use >= 1 && !SMLA_WAIT(kBarOpEmpty + ob, (use + 1) & 1)) break;
-      if (lane == 0 && half == 0) SMLA_TRACE_SET(tl, kEvOpEmpty);
-      const uint32_t op = smem_u32(smem + kOffOp + ob * kOpBuf);
-#pragma unroll 1
-      for (int i0 = 0; i0 < kRawRows; i0 += 8) {
-        int tail_j[3], tail_k[3];
-        bool tail_on[3];
-#pragma unroll
-        for (int q = 0; q < 3; ++q) {
-          const int sidx = 32 * q + lane;
-          tail_on[q] = sidx < 72;
-          tail_j[q] = tail_on[q] ? sidx / 9 : 0;
-          tail_k[q] = tail_on[q] ? sidx % 9 : 0;
-        }
-        uint4 c[8], t[3];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) c[j] = lds128(raw_row(raw, i0 + j) + 16 * lane);
-#pragma unroll
-        for (int q = 0; q < 3; ++q) t[q] = lds128(raw_row(raw, i0 + tail_j[q]) + kScaleOff + 16 * tail_k[q]);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const int r = kRawRows * half + i0 + j;
-          const bool v = (vmask >> (i0 + j)) & 1u;
-          const uint4 x = v ? c[j] : make_uint4(0u, 0u, 0u, 0u);
-          sts128(op + panel * kPanel + (uint32_t)((r >> 3) * 1024 + (r & 7) * 128) + ((chunk ^ (r & 7)) << 4), x);
-        }
-#pragma unroll
-        for (int q = 0; q < 3; ++q) {
-          const int r = kRawRows * half + i0 + tail_j[q];
-          const bool v = (vmask >> (i0 + tail_j[q])) & 1u;
-          const uint4 x = v ? t[q] : make_uint4(0u, 0u, 0u, 0u);
-          const uint32_t rope_dst =
-              op + kOpRope + (uint32_t)((r >> 3) * 1024 + (r & 7) * 128) + ((((tail_k[q] + 7) & 7) ^ (r & 7)) << 4);
-          const uint32_t dst = !tail_on[q] ? sink : (tail_k[q] == 0 ? op + kOpScale + 16 * r : rope_dst);
-          sts128(dst, x);
-        }
-      }
-      valid[ob * kRows + kRawRows * half + lane] = (uint8_t)((vmask >> lane) & 1u);
-      // orders this stage's reads of the raw stage and writes of the operand
-      // tile before the tensor-memory-side accesses that follow (the next
-      // gather into the raw stage, the MMAs on the tile)
-      fence_proxy_async_smem();
+      if (lane == 0 && lw == 0) SMLA_TRACE_SET(tl, kEvOpEmpty);
+      if (lane < 16) valid[ob * kRows + 16 * lw + lane] = (uint8_t)((vmask >> lane) & 1u);
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&bars[kBarOpFull + ob]);
-        SMLA_TRACE_SET(tl, half ? kEvRawLandedH1 : kEvRawLanded);
+      if (lane == 0) mbar_arrive_expect_tx(&bars[kBarOpFull + ob], 16 * kRowBytes);
+      __syncwarp();
+      if (lane < 24) {
+        const uint32_t op = smem_u32(smem + kOffOp + ob * kOpBuf);
+        const uint32_t in_panel = (uint32_t)((r_g >> 3) * 1024 + (r_g & 7) * 128);
+        const uint32_t dst = box < 4    ? op + box * kPanel + in_panel
+                             : box == 4 ? op + kOpRope + in_panel
+                                        : op + kOpScale + (r_g >> 2) * 128;
+        const int x = box < 4 ? 128 * box : box == 4 ? kRopeOff : kScaleOff;
+        tma_gather4(dst, box < 5 ? &panel_map : &scale_map, x, g0, g1, g2, g3, &bars[kBarOpFull + ob]);
       }
+      if (lane == 0 && lw == 0) SMLA_TRACE_SET(tl, kEvIssue);
+      last_ob = ob;
+      last_use = use;
     }
     // No copy may still be landing in shared memory when the CTA exits (only
-    // possible after an abort; the stage's wait has run otherwise).
-    if (issued > 0) mbar_wait_drain(&bars[kBarRawFull + rs], ((issued - 1) & 1));
+    // possible after an abort; the consumers have waited for every tile otherwise).
+    if (last_ob >= 0) mbar_wait_drain(&bars[kBarOpFull + last_ob], last_use & 1);
   } else if (warp >= kQWarp0 && warp < kQWarp0 + kQWarps) {
     // ------------------------------------------------------------ Q preparation
     // 4 threads per head: thread part owns NoPE columns [128 part, 128 part +
@@ -694,8 +628,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         seg_first_kt = ti.kt;
         n_seg_tiles = 0;
       }
+      SMLA_CLK_MARK(11);
       wait_s(kBarOpFull + ob, (tl / kOpBufs) & 1);  // row flags and scales
       if (tid == 0) SMLA_TRACE_SET(tl, kEvOpFull);
+      SMLA_CLK_MARK(12);
       wait_s(kBarSFull + sbuf, (tl >> 1) & 1);
       if (tid == 0) SMLA_TRACE_SET(tl, kEvSoftStart);
       SMLA_CLK_START();
@@ -708,8 +644,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool ok0 = !dead && valid[ob * kRows + r0] != 0;
       const bool ok1 = !dead && valid[ob * kRows + r1] != 0;
       const float4 zero4 = make_float4(0.f, 0.f, 0.f, 0.f);
-      const float4 s0 = ok0 ? *reinterpret_cast<const float4*>(smem + kOffOp + ob * kOpBuf + kOpScale + 16 * r0) : zero4;
-      const float4 s1 = ok1 ? *reinterpret_cast<const float4*>(smem + kOffOp + ob * kOpBuf + kOpScale + 16 * r1) : zero4;
+      const uint8_t* scl = smem + kOffOp + ob * kOpBuf + kOpScale;
+      const float4 s0 = ok0 ? *reinterpret_cast<const float4*>(scl + (r0 >> 2) * 128 + (r0 & 3) * 16) : zero4;
+      const float4 s1 = ok1 ? *reinterpret_cast<const float4*>(scl + (r1 >> 2) * 128 + (r1 & 3) * 16) : zero4;
       const float sc0[4] = {s0.x, s0.y, s0.z, s0.w};
       const float sc1[4] = {s1.x, s1.y, s1.z, s1.w};
       // logits (log2 units): 2^-s_h sum_g scale_g (S_g,hi + S_g,lo) + S_rope
@@ -981,18 +918,23 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// The cache as a 2-D array [NB * 64 rows][164 four-byte words] (row stride
-// 656 bytes), box 164 x 1, no swizzle: one tile::gather4 copies 4 whole rows;
-// rows outside [0, NB * 64) read as zeros.
-cudaError_t make_row_map(const uint8_t* cache, int64_t NB, CUtensorMap* map) {
+// Tensor maps of the cache viewed as a 2-D byte array [NB * 64 rows, 656
+// bytes]: 128-byte boxes with the 128-byte swizzle (code and RoPE panels)
+// and 16-byte boxes without swizzle (scales).  Rows outside [0, NB * 64)
+// read as zeros.
+cudaError_t make_cache_maps(const uint8_t* cache, int64_t NB, CUtensorMap* panel_map, CUtensorMap* scale_map) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
-  const cuuint64_t gdim[2] = {(cuuint64_t)(kRowBytes / 4), (cuuint64_t)(NB * kBlock)};
+  const cuuint64_t gdim[2] = {(cuuint64_t)kRowBytes, (cuuint64_t)(NB * kBlock)};
   const cuuint64_t gstride[1] = {(cuuint64_t)kRowBytes};
-  const cuuint32_t box[2] = {(cuuint32_t)(kRowBytes / 4), 1}, es[2] = {1, 1};
-  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint8_t*>(cache), gdim, gstride, box, es,
-                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  const cuuint32_t box_panel[2] = {128, 1}, box_scale[2] = {16, 1}, es[2] = {1, 1};
+  CUresult r = enc(panel_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(cache), gdim, gstride, box_panel, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  r = enc(scale_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(cache), gdim, gstride, box_scale, es,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
@@ -1054,10 +996,10 @@ cudaError_t launch_decode_fp8(const AttnArgs& a, const AttnPlan& plan, cudaStrea
   p.nt = plan.nt;
   p.total = plan.total;
   p.G = plan.G;
-  CUtensorMap row_map;
-  cudaError_t em = make_row_map(a.cache, a.NB, &row_map);
+  CUtensorMap panel_map, scale_map;
+  cudaError_t em = make_cache_maps(a.cache, a.NB, &panel_map, &scale_map);
   if (em != cudaSuccess) return em;
-  sparse_mla_decode_fp8_kernel<<<plan.G, kThreads, kSmemAlloc, stream>>>(p, row_map);
+  sparse_mla_decode_fp8_kernel<<<plan.G, kThreads, kSmemAlloc, stream>>>(p, panel_map, scale_map);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || !plan.need_combine) return e;
   combine_kernel<HG><<<(unsigned)(plan.units * kCombineSplit), kCombineThreads, 0, stream>>>(p.part_o, p.part_lse, p.out, p.lse, p.H, p.n_hg, p.nt,
