@@ -772,7 +772,7 @@ cudaError_t launch_impl(const AttnArgs& a, const AttnPlan& plan, cudaStream_t st
   sparse_mla_attn_kernel<HG, kFp8><<<plan.G, C::kThreads, C::kSmemAlloc, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || !plan.need_combine) return e;
-  combine_kernel<HG><<<(unsigned)(plan.units * kCombineSplit), kCombineThreads, 0, stream>>>(p.part_o, p.part_lse, p.out, p.lse, p.H, p.n_hg, p.nt,
+  combine_kernel<HG><<<(unsigned)(plan.units * kCombineSplit), combine_threads<HG>(), 0, stream>>>(p.part_o, p.part_lse, p.out, p.lse, p.H, p.n_hg, p.nt,
                                                                p.total, p.G);
   return cudaGetLastError();
 }

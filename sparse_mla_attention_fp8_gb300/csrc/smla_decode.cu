@@ -120,7 +120,8 @@ constexpr int kPBuf = 4 * kPGroup;                    // 8192
 constexpr int kOffOp = 0;
 constexpr int kOffQ = kOffOp + kOpBufs * kOpBuf;
 constexpr int kOffP = kOffQ + kQBuf;
-constexpr int kOffSlots = kOffP + 2 * kPBuf;                       // P' double-buffered; int32 [4][64]
+constexpr int kPBufs = 3;                                           // P' buffers
+constexpr int kOffSlots = kOffP + kPBufs * kPBuf;                   // int32 [4][64]
 constexpr int kOffValid = kOffSlots + 4 * kRows * 4;                // uint8 [4][64]
 constexpr int kOffPre = kOffValid + kOpBufs * kRows;                // float [4][16 columns] inverse Q prescales
 constexpr int kOffRedMax = kOffPre + 4 * HG * 4;                    // float [2][4 quarters][16 columns]
@@ -128,8 +129,9 @@ constexpr int kOffRedSc = kOffRedMax + 2 * 4 * HG * 4;              // float [2]
 constexpr int kOffRedSum = kOffRedSc + 2 * 2 * 4 * 4 * 4;           // float [4 quarters][16 columns]
 constexpr int kOffBar = kOffRedSum + 4 * HG * 4;
 enum {
-  kBarOpFull = 0, kBarOpEmpty = kBarOpFull + kOpBufs, kBarSFull = kBarOpEmpty + kOpBufs, kBarPFull = kBarSFull + 2,
-  kBarPvDone = kBarPFull + 2, kBarIdxFull = kBarPvDone + 2, kBarIdxEmpty = kBarIdxFull + 4,
+  kBarOpFull = 0, kBarOpEmpty = kBarOpFull + kOpBufs, kBarSFull = kBarOpEmpty + kOpBufs, kBarSFree = kBarSFull + 2,
+  kBarPFull = kBarSFree + 2,
+  kBarPvDone = kBarPFull + kPBufs, kBarIdxFull = kBarPvDone + kPBufs, kBarIdxEmpty = kBarIdxFull + 4,
   kBarQFull = kBarIdxEmpty + 4, kBarQEmpty = kBarQFull + 1, kBarOFree = kBarQEmpty + 1, kBarDrain = kBarOFree + 1,
   kNumBars = kBarDrain + 1
 };
@@ -303,6 +305,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars[kBarSFull + i], 1);
+      mbar_init(&bars[kBarSFree + i], kSoftWarps);
+    }
+    for (int i = 0; i < kPBufs; ++i) {
       mbar_init(&bars[kBarPFull + i], kSoftWarps);
       mbar_init(&bars[kBarPvDone + i], 1);
     }
@@ -474,9 +479,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ tensor-core issuer
     // Polls (never blocks on) the next P' for P.V, then the next operand tile
-    // + Q for QK^T (at most one tile ahead of the oldest P.V not yet issued,
-    // one per S buffer).  P.V goes first: its completion frees the operand
-    // tile and the P buffer that the other roles wait for.
+    // + Q + free S buffer for QK^T (an S buffer is free once the softmax has
+    // read the tile two before out of it).  P.V goes first: its completion
+    // frees the operand tile and the P buffer that the other roles wait for.
     if (lane == 0 && n_local > 0) {
       constexpr uint32_t id_qk8 = idesc_e4m3(64, 32, 0, 0);
       constexpr uint32_t id_qkr = make_idesc_bf16(64, HG, 0, 0);
@@ -493,7 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // top-k tile index within its unit of the next QK^T / P.V tile (advanced
       // incrementally: no divisions in the polling loop)
       const int kt0 = (int)(xbeg % p.nt);
-      int kt_qk = kt0, kt_pv = kt0, ob_qk = 0, ob_pv = 0;
+      int kt_qk = kt0, kt_pv = kt0, ob_qk = 0, ob_pv = 0, pb_pv = 0, pb_use = 0;
       uint64_t t_idle = 0;
       uint32_t idle_polls = 0;
       while (next_pv < n_local) {
@@ -501,9 +506,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (next_pv < next_qk) {
           const int tl = next_pv;
           const bool seg_start = tl == 0 || kt_pv == 0;
-          const int pb = tl & 1;
+          const int pb = pb_pv;
           const bool o_ok = !seg_start || seg_o == 0 || mbar_test_wait(&bars[kBarOFree], (seg_o - 1) & 1);
-          if (o_ok && mbar_test_wait(&bars[kBarPFull + pb], (tl >> 1) & 1)) {
+          if (o_ok && mbar_test_wait(&bars[kBarPFull + pb], pb_use & 1)) {
             SMLA_TRACE_SET(tl, kEvPvSeen);
             if (seg_start) ++seg_o;
             tc_fence_after();
@@ -522,10 +527,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++next_pv;
             kt_pv = kt_pv + 1 == p.nt ? 0 : kt_pv + 1;
             ob_pv = ob_pv + 1 == kOpBufs ? 0 : ob_pv + 1;
+            if (++pb_pv == kPBufs) {
+              pb_pv = 0;
+              ++pb_use;
+            }
             progressed = true;
           }
         }
-        if (next_qk < n_local && next_qk < next_pv + 2) {
+        if (next_qk < n_local &&
+            (next_qk < 2 || mbar_test_wait(&bars[kBarSFree + (next_qk & 1)], ((next_qk - 2) >> 1) & 1))) {
           const int tl = next_qk;
           const bool seg_start = tl == 0 || kt_qk == 0;
           const bool seg_end = tl == n_local - 1 || kt_qk == p.nt - 1;
@@ -613,9 +623,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!dead) dead = !SMLA_WAIT(bar_idx, parity);
       dead = __any_sync(kFullMask, dead);
     };
+    TileInfo ti = tile_info(p, xbeg, xbeg, xend);
     for (int tl = 0; tl < n_local; ++tl) {
-      const TileInfo ti = tile_info(p, xbeg + tl, xbeg, xend);
-      const int ob = tl % kOpBufs, sbuf = tl & 1;
+      if (tl > 0) {  // advance the tile position without divisions
+        ti.seg_start = ++ti.kt == p.nt;
+        if (ti.seg_start) {
+          ti.kt = 0;
+          ++ti.u;
+          if (++ti.hg == p.n_hg) {
+            ti.hg = 0;
+            ++ti.t;
+          }
+        }
+        ti.seg_end = tl == n_local - 1 || ti.kt == p.nt - 1;
+      }
+      const int ob = tl % kOpBufs, sbuf = tl & 1, pb = tl % kPBufs, puse = tl / kPBufs;
       if (ti.seg_start) {
         ++seg;
 #pragma unroll
@@ -663,6 +685,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tmem_ld_16x256b_x1(sa + 128, rp);
           tmem_ld_wait();
+          // S of this tile is in registers: its buffer may take QK^T of tile tl + 2
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars[kBarSFree + sbuf]);
 #pragma unroll
           for (int g = 0; g < 4; ++g) {
             reg_fence4(hi[g]);
@@ -676,6 +702,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               acc[k] = fmaf((k >> 1) ? sc1[g] : sc0[g], __uint_as_float(hi[g][k]) + __uint_as_float(lo[g][k]), acc[k]);
 #pragma unroll
           for (int k = 0; k < 4; ++k) acc[k] = fmaf(acc[k], ip2[k & 1], __uint_as_float(rp[k]));
+        } else if (lane == 0) {
+          mbar_arrive(&bars[kBarSFree + sbuf]);
         }
 #pragma unroll
         for (int k = 0; k < 4; ++k) sl[k] = ((k >> 1) ? ok1 : ok0) ? acc[k] * p.scale_log2 : -INFINITY;
@@ -756,7 +784,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float alpha[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) alpha[j] = __shfl_sync(kFullMask, alpha2[j & 1], j >> 1);
-        wait_s(kBarPvDone + ((tl - 1) & 1), ((tl - 1) >> 1) & 1);  // P.V(tl - 1) and all before
+        wait_s(kBarPvDone + (tl - 1) % kPBufs, ((tl - 1) / kPBufs) & 1);  // P.V(tl - 1) and all before
         if (!dead) {
           tc_fence_after();
 #pragma unroll
@@ -789,7 +817,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         l2[k & 1] += pr[k];
       }
       SMLA_CLK_MARK(4);
-      if (tl >= 2) wait_s(kBarPvDone + sbuf, ((tl - 2) >> 1) & 1);  // P buffer free: P.V(tl - 2) done
+      if (tl >= kPBufs) wait_s(kBarPvDone + pb, (puse + 1) & 1);  // P buffer free: P.V(tl - 3) done
       if (tid == 0) SMLA_TRACE_SET(tl, kEvSoftPWait);
       SMLA_CLK_MARK(5);
       // P'_q = kPScale * p * scale_q / R_q as e4m3 hi + lo: MN-major core
@@ -805,7 +833,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float f = (rho ? sc1[g] : sc0[g]) * inv_r;
             uint32_t hw, lw;
             split2_f16(pr[2 * rho] * f, pr[2 * rho + 1] * f, hw, lw);
-            const uint32_t base = p0 + sbuf * kPBuf + g * kPGroup + (r >> 3) * 256 + (r & 7) * 16 + nA;
+            const uint32_t base = p0 + pb * kPBuf + g * kPGroup + (r >> 3) * 256 + (r & 7) * 16 + nA;
             sts16(base, hw);
             sts16(base + 128, lw);
           }
@@ -814,7 +842,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0 && !dead) mbar_arrive(&bars[kBarPFull + sbuf]);
+      if (lane == 0 && !dead) mbar_arrive(&bars[kBarPFull + pb]);
       if (tid == 0) SMLA_TRACE_SET(tl, kEvSoftDone);
       SMLA_CLK_MARK(6);
       ++n_seg_tiles;
@@ -829,7 +857,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane < 4) *reinterpret_cast<float2*>(red_sum + qd * HG + nA) = make_float2(v2[0], v2[1]);
         }
         named_bar_sync(bar_id, 128);
-        wait_s(kBarPvDone + sbuf, (tl >> 1) & 1);  // last P.V of the segment
+        wait_s(kBarPvDone + pb, puse & 1);  // last P.V of the segment
         tc_fence_after();
         const bool full = (seg_first_kt == 0) && (ti.kt == p.nt - 1);
         const int64_t slot = (int64_t)blockIdx.x + ti.u;
@@ -1002,7 +1030,7 @@ cudaError_t launch_decode_fp8(const AttnArgs& a, const AttnPlan& plan, cudaStrea
   sparse_mla_decode_fp8_kernel<<<plan.G, kThreads, kSmemAlloc, stream>>>(p, panel_map, scale_map);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || !plan.need_combine) return e;
-  combine_kernel<HG><<<(unsigned)(plan.units * kCombineSplit), kCombineThreads, 0, stream>>>(p.part_o, p.part_lse, p.out, p.lse, p.H, p.n_hg, p.nt,
+  combine_kernel<HG><<<(unsigned)(plan.units * kCombineSplit), combine_threads<HG>(), 0, stream>>>(p.part_o, p.part_lse, p.out, p.lse, p.H, p.n_hg, p.nt,
                                                                p.total, p.G);
   return cudaGetLastError();
 }
