@@ -37,6 +37,30 @@ METRIC = "sparse MLA decode query-tokens/s + HBM GB/s (H=16, topk=2048) vs roofl
 UNIT = "query-tokens/s"
 
 
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one decode
+# launch, from an ncu capture of the kernels built from the sources whose
+# hash is the key (profiles/sparse_mla_decode_fp8_kernel_decode_h16_k2048.md):
+# the attention kernel plus the combine of split units.  Once the kernel
+# sources change, the figure no longer applies and the roofline reports null.
+TRAFFIC_SOURCES = ("smla_decode.cu", "smla_combine.cuh", "smla_common.cuh", "sm103_ptx.cuh")
+TRAFFIC_BY_SOURCE = {
+    "d535234b0453ebf4": 100_883_456 + 2_937_344 + 6_845_184 + 0,
+}
+
+
+def captured_traffic():
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "sparse_mla_attention_fp8_gb300", "csrc")
+    try:
+        for f in TRAFFIC_SOURCES:
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(fh.read())
+    except OSError:
+        return None
+    return TRAFFIC_BY_SOURCE.get(h.hexdigest()[:16])
+
+
 # ---------------------------------------------------------------- helpers
 
 def load_peaks():
@@ -365,7 +389,7 @@ def run_ours(args):
             "gb_per_s": achieved_gbs,
             "tflops": flops / (decode_ms * 1e-3) / 1e12,
             "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                         "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": None,
+                         "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": captured_traffic(),
                          "peak_source": peaks["source"],
                          "kernel": "sparse decode launch (attention kernel + split combine)",
                          "algorithmic_bytes_per_launch": int(alg_bytes), "avg_launch_us": decode_ms * 1e3},
