@@ -404,15 +404,173 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def smla_plan_needs_combine(smla, T, H, K) -> bool:
+def smla_plan_needs_combine(smla, T, H, K, hg=16) -> bool:
+    """Whether the work split leaves units spanning CTAs (then a combine
+    launch follows the attention kernel).  The FP8 decode works on 16-head
+    units; the bf16 prefill on 32-head units when H allows."""
     import torch
     sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
-    hg = 32 if H % 32 == 0 else 16
     units = T * (H // hg)
     nt = max(1, (K + 63) // 64)
     total = units * nt
     G = max(1, min(total, sms))
     return not (total % G == 0 and (total // G) % nt == 0)
+
+
+# ---------------------------------------------------------------- tensor-bound workloads (not the default line)
+
+def tensor_peak_tflops(peaks, fp8: bool) -> float:
+    """Dense tensor peak for the path's MMA type: the measured bf16 burst
+    figure, times the nominal fp8 / bf16 ratio (4.5 / 2.25) for FP8 MMAs."""
+    return peaks["bf16_tflops"] * (2.0 if fp8 else 1.0)
+
+
+def time_graphs(graphs, steps, stream):
+    import torch
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(steps):
+            graphs[i % len(graphs)].replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def run_tensor_workload(args):
+    """The tensor-bound configurations of the hot path, for the record (the
+    default line is the memory-bound decode):
+      decode_h128_k2048: FP8 decode, 128 requests x 1 token, H = 128, top-k
+        2048, context 65536 (5.5 GB cache), 8 rotating index sets;
+      prefill_h128_k2048: bf16 prefill, 4 requests x 1024 new tokens over
+        3072 cached, H = 128, top-k 2048, dense latent buffer of 16384 rows.
+    Prints one JSON line: query-tokens/s, TFLOP/s against the dense tensor
+    peak of the path's MMA type, and the oracle on a bounded token sample."""
+    import torch
+    import oracle
+    import sparse_mla_attention_fp8_gb300 as smla
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU for the library path")
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    smla.build()
+    oracle.build()
+    peaks = load_peaks()
+    stream = torch.cuda.Stream(device)
+    nth = oracle.default_threads()
+
+    def bf16(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device).view(torch.bfloat16)
+
+    if args.workload == "decode_h128_k2048":
+        case = inp.rotating_decode(seed=2, R=128, ctx_lo=65536, ctx_hi=65536, K=2048, H=128, outliers=False)
+        T, H, K, NB = case.q.shape[0], case.H, case.K, case.num_blocks
+        with torch.cuda.stream(stream):
+            cache = torch.zeros((NB, 64, 656), dtype=torch.uint8, device=device)
+            lat = inp.device_latent(len(case.ctx_slots), case.latent_seed, case.outlier_channels, device)
+            smla.mla_cache_store_fp8(lat, torch.from_numpy(case.ctx_slots).to(device), cache, stream=stream)
+            q = bf16(case.q)
+            idx_sets = [torch.from_numpy(x).to(device) for x in case.index_sets]
+            bt = torch.from_numpy(case.block_table).to(device)
+            req = torch.from_numpy(case.req_id_per_token).to(device)
+            ws = torch.zeros(smla.decode_workspace_bytes(T, H, K, 0), dtype=torch.uint8, device=device)
+            out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=device)
+            lse = torch.empty((T, H), dtype=torch.float32, device=device)
+        stream.synchronize()
+        del lat
+
+        def launch(i):
+            smla.sparse_mla_decode_fp8(q, cache, idx_sets[i % len(idx_sets)], bt, req, case.sm_scale, 0, out, lse,
+                                       ws, stream=stream)
+        n_graphs = len(idx_sets)
+        flops = statistics.mean(decode_flops(case, x) for x in case.index_sets)
+        fp8 = True
+        launches = 1 + (1 if smla_plan_needs_combine(smla, T, H, K, hg=16) else 0)
+        desc = (f"{case.name}: tensor-bound FP8 sparse decode, {T} requests x 1 token, H={H}, top-k {K}, "
+                f"context 65536, 656-byte FP8 cache ({NB} blocks, {NB * 64 * 656 / 1e9:.1f} GB), "
+                f"{n_graphs} rotating index sets")
+        # oracle sample: a few tokens on a host cache holding the rows they reference
+        tok = np.arange(min(nth, 8), dtype=np.int32)
+        hcache = host_sample_cache(case, case.index_sets[0], tok, seed=777)
+
+        def oracle_run():
+            oracle.sparse_mla_decode(case.q, hcache, case.index_sets[0], case.block_table, case.req_id_per_token,
+                                     case.sm_scale, tokens=tok, nthreads=nth)
+    else:
+        case = inp.prefill(seed=3)
+        T, H, K = case.T, case.H, case.K
+        N = case.kv.shape[0]
+        with torch.cuda.stream(stream):
+            q = bf16(case.q)
+            kv = bf16(case.kv)
+            idx = torch.from_numpy(case.indices).to(device)
+            ws = torch.zeros(smla.prefill_workspace_bytes(T, H, K, 0), dtype=torch.uint8, device=device)
+            out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=device)
+            lse = torch.empty((T, H), dtype=torch.float32, device=device)
+        stream.synchronize()
+
+        def launch(i):
+            smla.sparse_mla_prefill_bf16(q, kv, idx, case.sm_scale, 0, out, lse, ws, stream=stream)
+        n_graphs = 1
+        flops = 2 * H * int((case.indices >= 0).sum()) * (576 + 512)
+        fp8 = False
+        launches = 1 + (1 if smla_plan_needs_combine(smla, T, H, K, hg=32) else 0)
+        desc = (f"{case.name}: bf16 sparse prefill, 4 requests x 1024 new tokens over 3072 cached, H={H}, "
+                f"top-k {K}, dense latent buffer [{N}, 576] (L2-resident)")
+        tok = np.linspace(0, T - 1, min(nth, 8)).astype(np.int32)
+
+        def oracle_run():
+            oracle.sparse_mla_prefill(case.q, case.kv, case.indices, case.sm_scale, tokens=tok, nthreads=nth)
+
+    with torch.cuda.stream(stream):
+        for i in range(max(args.warmup, 3)):
+            launch(i)
+    stream.synchronize()
+    graphs = []
+    for i in range(n_graphs):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            launch(i)
+        graphs.append(g)
+    time_graphs(graphs, max(args.warmup, 3), stream)
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
+    except Exception:
+        pass
+    clocks = ClockSampler(uuid)
+    clocks.start()
+    ms = time_graphs(graphs, args.steps, stream)
+    clk = clocks.stop()
+    if smla.read_device_status(ws, stream) != 0:
+        raise SystemExit("device status reports a kernel wait timeout")
+    tflops = flops / (ms * 1e-3) / 1e12
+    peak = tensor_peak_tflops(peaks, fp8)
+    cpu = None
+    if not args.no_cpu_baseline:
+        t0 = time.perf_counter()
+        oracle_run()
+        el = time.perf_counter() - t0
+        cpu = {"value": len(tok) / el, "unit": UNIT, "cores": nth, "kind": "oracle",
+               "sample": f"{len(tok)} query tokens of the workload (float64 C oracle, {nth} threads), {el:.1f} s"}
+    line = {
+        "metric": f"{args.workload} query-tokens/s + TFLOP/s vs tensor roofline", "value": T / (ms * 1e-3),
+        "unit": UNIT, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp8" if fp8 else "bf16",
+        "data": "synthetic",
+        "config": {"workload": desc, "step": "one attention launch (plus the split combine)",
+                   "l2": "8 rotating index sets (decode); the prefill's 18.9 MB buffer is L2-resident by design",
+                   "parallelism": "single GPU", "launch": "CUDA graph per step"},
+        "tflops": tflops,
+        "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak,
+                     "traffic": None, "peak_source": peaks["source"] + (" bf16 x 2 (fp8/bf16 nominal)" if fp8 else ""),
+                     "kernel": "attention launch (attention kernel + split combine)", "flops_per_launch": flops,
+                     "avg_launch_us": ms * 1e3},
+        "cpu_baseline": cpu, "e2e": None, "gpu_launches": launches * args.steps, "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
 
 
 def run_e2e(args, smla, case, device, stream, cache, ws):
@@ -481,11 +639,17 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=["decode_h16_k2048", "decode_h128_k2048", "prefill_h128_k2048"],
+                    default="decode_h16_k2048",
+                    help="decode_h16_k2048 (default) is the headline; the other two are the tensor-bound "
+                         "configurations, reported on their own line")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload != "decode_h16_k2048":
+        run_tensor_workload(args)
     else:
         run_ours(args)
 
