@@ -25,7 +25,7 @@ _BUILD = os.path.join(_PKG, "_build")
 LIB_PATH = os.path.join(_PKG, "libsmla.so")
 HEADER = os.path.join(_ROOT, "include", "smla.h")
 
-SOURCES = ["smla_decode.cu", "smla_attn.cu", "smla_store.cu", "smla_api.cu"]
+SOURCES = ["smla_decode.cu", "smla_attn.cu", "smla_wide.cu", "smla_store.cu", "smla_api.cu"]
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-std=c++17", "-lineinfo",
               "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall"]
 

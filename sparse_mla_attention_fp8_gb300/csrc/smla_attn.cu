@@ -772,7 +772,7 @@ cudaError_t launch_impl(const AttnArgs& a, const AttnPlan& plan, cudaStream_t st
   sparse_mla_attn_kernel<HG, kFp8><<<plan.G, C::kThreads, C::kSmemAlloc, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || !plan.need_combine) return e;
-  combine_kernel<HG><<<(unsigned)(plan.units * kCombineSplit), combine_threads<HG>(), 0, stream>>>(p.part_o, p.part_lse, p.out, p.lse, p.H, p.n_hg, p.nt,
+  combine_kernel<HG><<<(unsigned)(plan.units * combine_split<HG>()), combine_threads<HG>(), 0, stream>>>(p.part_o, p.part_lse, p.out, p.lse, p.H, p.n_hg, p.nt,
                                                                p.total, p.G);
   return cudaGetLastError();
 }
@@ -786,6 +786,7 @@ extern "C" int smla_trace_set(unsigned long long* buf) {
 #endif
 
 AttnPlan plan_prefill_bf16(int T, int H, int K, int num_splits, int num_sms) {
+  if (wide_prefill_supported(H)) return plan_prefill_wide(T, K, num_splits, num_sms);
   AttnPlan pl;
   pl.HG = (H % 32 == 0) ? 32 : 16;
   pl.n_hg = H / pl.HG;
@@ -804,6 +805,7 @@ AttnPlan plan_prefill_bf16(int T, int H, int K, int num_splits, int num_sms) {
 }
 
 cudaError_t launch_prefill_bf16(const AttnArgs& a, const AttnPlan& plan, cudaStream_t stream) {
+  if (plan.HG == 128) return launch_prefill_wide(a, plan, stream);
   return plan.HG == 16 ? launch_impl<16, false>(a, plan, stream) : launch_impl<32, false>(a, plan, stream);
 }
 

@@ -20,21 +20,24 @@ __host__ __device__ __forceinline__ int64_t tile_owner(int64_t x, int64_t total,
   return c;
 }
 
-// Blocks per unit of combine_kernel: each merges 512 / kCombineSplit value
+// Blocks per unit of combine_kernel: each merges 512 / combine_split value
 // columns of every head of the unit, one (head, float4 column chunk) pair per
 // thread.
-constexpr int kCombineSplit = 8;
 template <int HG>
-constexpr int combine_threads() {
-  return HG * (128 / kCombineSplit);
+__host__ __device__ constexpr int combine_split() {
+  return HG <= 32 ? 8 : 32;
+}
+template <int HG>
+__host__ __device__ constexpr int combine_threads() {
+  return HG * (128 / combine_split<HG>());
 }
 constexpr int kCombineChunk = 8;  // parts per round: their loads are in flight together
 
 // LSE-weighted merge of the partial results of units split across CTAs:
 //   M = max_s lse_s,  w_s = exp(lse_s - M) / sum_s' exp(lse_s' - M),
 //   out = sum_s w_s * O_s,  lse = M + log(sum_s exp(lse_s - M)).
-// Grid: units x kCombineSplit blocks of combine_threads<HG>() = HG x
-// (128 / kCombineSplit) threads.  Each thread first issues the loads of its
+// Grid: units x combine_split<HG>() blocks of combine_threads<HG>() = HG x
+// (128 / combine_split<HG>()) threads.  Each thread first issues the loads of its
 // partial-O chunk for kCombineChunk parts, then reads the parts' LSEs (from
 // L2 or L1, shared by the block), so that one round trip covers both; parts
 // beyond the first round are merged with a running max and sum.
@@ -44,9 +47,10 @@ __global__ void __launch_bounds__(combine_threads<HG>()) combine_kernel(const fl
                                                                   __nv_bfloat16* __restrict__ out,
                                                                   float* __restrict__ lse, int H, int n_hg, int nt,
                                                                   int64_t total, int G) {
-  constexpr int kChunks = 128 / kCombineSplit;  // float4 column chunks per block and head
-  const int64_t u = blockIdx.x / kCombineSplit;
-  const int part = blockIdx.x % kCombineSplit;
+  constexpr int kSplit = combine_split<HG>();
+  constexpr int kChunks = 128 / kSplit;  // float4 column chunks per block and head
+  const int64_t u = blockIdx.x / kSplit;
+  const int part = blockIdx.x % kSplit;
   const int64_t c_lo = tile_owner(u * nt, total, G), c_hi = tile_owner(u * nt + nt - 1, total, G);
   if (c_lo == c_hi) return;  // finished inside one CTA, already written
   const int tid = threadIdx.x;

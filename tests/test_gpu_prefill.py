@@ -38,14 +38,17 @@ def test_prefill_causal_padding(H):
     run_prefill(case)
 
 
-@pytest.mark.parametrize("num_splits", [0, 1, 2])
-def test_prefill_splits(num_splits):
-    case = inp.prefill(seed=4, R=2, cached=300, new=20, K=256, H=32)
+@pytest.mark.parametrize("H", [32, 128])
+@pytest.mark.parametrize("num_splits", [0, 1, 2, 3])
+def test_prefill_splits(H, num_splits):
+    # K = 256 is 4 tiles of 64 rows: 3 splits leave ragged per-pair ranges
+    case = inp.prefill(seed=4, R=2, cached=300, new=20, K=256, H=H)
     run_prefill(case, num_splits=num_splits)
 
 
-def test_prefill_out_of_range_rows_are_masked():
-    case = inp.prefill(seed=5, R=2, cached=100, new=10, K=64, H=16)
+@pytest.mark.parametrize("H", [16, 128])
+def test_prefill_out_of_range_rows_are_masked(H):
+    case = inp.prefill(seed=5, R=2, cached=100, new=10, K=64, H=H)
     N = case.kv.shape[0]
     case.indices[0, 3] = N
     case.indices[1, 9] = N + 1000
