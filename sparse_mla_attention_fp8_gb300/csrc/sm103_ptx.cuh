@@ -94,6 +94,19 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) 
   }
 }
 
+// 2^x by the special-function unit (approximate, subnormal results flushed to
+// zero; 2^-inf = 0).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Named barrier over `n` threads (a multiple of 32) of the CTA.
+__device__ __forceinline__ void named_bar_sync(int id, int n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
 // ---------------------------------------------------------------- clusters
 // Rank of this CTA in its cluster.
 __device__ __forceinline__ uint32_t cluster_ctarank() {
@@ -111,6 +124,13 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t local, uint32_t rank) {
 // 16-byte store into another CTA's shared memory (cluster address).
 __device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
   asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+// Asynchronous 16-byte store into another CTA's shared memory that counts its
+// bytes on an mbarrier of that CTA (both cluster addresses).
+__device__ __forceinline__ void st_async_v4(uint32_t addr, float a, float b, float c, float d, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(addr),
+               "f"(a), "f"(b), "f"(c), "f"(d), "r"(bar)
                : "memory");
 }
 // Arrive on an mbarrier of another CTA (cluster address), releasing this

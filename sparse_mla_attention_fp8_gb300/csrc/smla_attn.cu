@@ -166,9 +166,6 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
                : "memory");
 }
 
-__device__ __forceinline__ void named_bar_sync(int id, int n) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
 
 // 4 e4m3 codes (one 32-bit word, lowest byte first) -> 2 words of bf16x2
 // (lowest column in the low half).  Exact: every e4m3 value is a bf16 value.

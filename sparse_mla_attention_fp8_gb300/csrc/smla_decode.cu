@@ -207,11 +207,6 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
   asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
 }
 
-
-__device__ __forceinline__ void named_bar_sync(int id, int n) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-
 // e4m3 pair (round to nearest even, saturating) of two floats: lo in the low byte.
 __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
   uint16_t r;
