@@ -138,6 +138,12 @@ __device__ __forceinline__ void st_async_v4(uint32_t addr, float a, float b, flo
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster_addr) : "memory");
 }
+// Arrive on an mbarrier of another CTA without ordering this thread's earlier
+// memory operations (for a consumer whose reads of the guarded data have
+// already delivered their values).
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t bar_cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster_addr) : "memory");
+}
 // try_wait with cluster-scope acquire: the writes other CTAs released before
 // arriving are visible after it returns true.
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
@@ -354,6 +360,22 @@ __device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr, uint32_t lbo_byte
   d |= (uint64_t)1u << 46;
   d |= (uint64_t)(layout & 7u) << 61;
   return d;
+}
+
+// The same descriptor split into its two 32-bit words.  The high word (stride
+// byte offset, version, layout) is a compile-time constant; the low word
+// (start address, leading byte offset) is the only one an operand offset
+// changes, and an offset inside shared memory never carries out of the 14-bit
+// start-address field, so one 32-bit add moves a descriptor to another operand.
+__host__ __device__ constexpr uint32_t sdesc_hi(uint32_t sbo_bytes, uint32_t layout) {
+  return ((sbo_bytes >> 4) & 0x3FFFu) | (1u << 14) | ((layout & 7u) << 29);
+}
+__device__ __forceinline__ uint32_t sdesc_lo(uint32_t saddr, uint32_t lbo_bytes) {
+  return ((saddr >> 4) & 0x3FFFu) | (((lbo_bytes >> 4) & 0x3FFFu) << 16);
+}
+template <uint32_t kHi>
+__device__ __forceinline__ uint64_t sdesc_join(uint32_t lo) {
+  return ((uint64_t)kHi << 32) | lo;
 }
 
 // Instruction descriptor for kind::f16 with bf16 A and B, fp32 accumulator.

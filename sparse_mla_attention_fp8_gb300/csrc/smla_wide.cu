@@ -74,11 +74,12 @@ constexpr int kOffK = kOffQ + kQBuf;
 constexpr int kOffX = kOffK + kKBufs * kKBuf;
 constexpr int kOffSlots = kOffX + 2 * kXSlot;      // int32 [4][64]
 constexpr int kOffValid = kOffSlots + 4 * kRows * 4;  // uint8 [2][64]
-constexpr int kOffRed = kOffValid + kKBufs * kRows;    // float [2 S buffers][2 halves][128]: maxima (log2 domain)
-constexpr int kOffBar = kOffRed + 2 * 2 * kHeads * 4;
+constexpr int kSBufs = 3;                              // S buffers in tensor memory
+constexpr int kOffRed = kOffValid + kKBufs * kRows;    // float [kSBufs][2 halves][128]: maxima (log2 domain)
+constexpr int kOffBar = kOffRed + kSBufs * 2 * kHeads * 4;
 enum {
-  kBarKFull = 0, kBarKEmpty = kBarKFull + kKBufs, kBarSFull = kBarKEmpty + kKBufs, kBarSReady = kBarSFull + 2,
-  kBarSFree = kBarSReady + 2, kBarPFull = kBarSFree + 2, kBarPDone = kBarPFull + 2, kBarXFull = kBarPDone + 2,
+  kBarKFull = 0, kBarKEmpty = kBarKFull + kKBufs, kBarSFull = kBarKEmpty + kKBufs, kBarSReady = kBarSFull + kSBufs,
+  kBarSFree = kBarSReady + kSBufs, kBarPFull = kBarSFree + kSBufs, kBarPDone = kBarPFull + 2, kBarXFull = kBarPDone + 2,
   kBarXFree = kBarXFull + 2, kBarIdxFull = kBarXFree + 2, kBarIdxEmpty = kBarIdxFull + 4, kBarQFull = kBarIdxEmpty + 4,
   kBarQEmpty = kBarQFull + 1, kBarOFree = kBarQEmpty + 1, kBarDrain = kBarOFree + 1, kNumBars = kBarDrain + 1
 };
@@ -92,8 +93,8 @@ static_assert(kSmemAlloc <= 232448, "shared memory budget");
 
 // tensor memory columns
 constexpr int kOCol = 0;    // O_c: 256 fp32 columns
-constexpr int kSCol = 256;  // S: 2 buffers x 64 columns
-constexpr int kPCol = 384;  // P: 2 buffers x 32 columns (bf16 pairs)
+constexpr int kSCol = 256;  // S: 3 buffers x 64 columns
+constexpr int kPCol = 448;  // P: 2 buffers x 32 columns (bf16 pairs)
 constexpr int kTmemCols = 512;
 
 constexpr int kSoftWarps = 4, kXchgWarp0 = 4, kXchgWarps = 8, kMmaWarp = 12, kIndexWarp = 13, kLoadWarp0 = 14;
@@ -173,10 +174,12 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
       mbar_init(&bars[kBarKFull + i], kLoaders);
       mbar_init(&bars[kBarKEmpty + i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kSBufs; ++i) {
       mbar_init(&bars[kBarSFull + i], 1);
       mbar_init(&bars[kBarSReady + i], 32 * kXchgWarps);
       mbar_init(&bars[kBarSFree + i], 32 * kSoftWarps);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&bars[kBarPFull + i], 32 * kSoftWarps);
       mbar_init(&bars[kBarPDone + i], 1);
     }
@@ -291,72 +294,73 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
     if (lane == 0 && n_local > 0) {
       constexpr uint32_t id_qk = make_idesc_bf16(128, kRows, 0, 0);
       constexpr uint32_t id_pv = make_idesc_bf16(128, 256, 0, 1);
-      const uint32_t q0 = smem_u32(smem + kOffQ), k0 = smem_u32(smem + kOffK);
+      const uint32_t q0 = smem_u32(smem + kOffQ), k0 = smem_u32(smem + kOffK);  // 1024-byte aligned
       int seg_q = 0, seg_o = 0, next_qk = 0, next_pv = 0;
       const int kt0 = (int)(xbeg % p.nt);
       int kt_qk = kt0, kt_pv = kt0;
       uint64_t t_idle = 0;
       uint32_t idle_polls = 0;
+      // shared-memory descriptors: constant high words, low words = base + offset / 16
+      constexpr uint32_t kHi128 = sdesc_hi(1024, kLayoutSw128), kHi64 = sdesc_hi(512, kLayoutSw64);
+      const uint32_t dq = sdesc_lo(q0, 16), dk0 = sdesc_lo(k0, 16), dv0 = sdesc_lo(k0, kPanel);
+      // P.V of tile next_pv once its P is written (and, first in a segment, O
+      // is free).  Tried before every QK^T panel too: its completion frees the
+      // row tile the loaders wait for, so it never waits out a whole QK^T.
+      auto try_pv = [&]() -> bool {
+        if (next_pv >= next_qk) return false;
+        const int tl = next_pv, kb = tl % kKBufs, pb = tl & 1;
+        const bool seg_start = tl == 0 || kt_pv == 0;
+        const bool o_ok = !seg_start || seg_o == 0 || mbar_test_wait(&bars[kBarOFree], (seg_o - 1) & 1);
+        if (!o_ok || !mbar_test_wait(&bars[kBarPFull + pb], (tl >> 1) & 1)) return false;
+        if (seg_start) ++seg_o;
+        tc_fence_after();
+        const uint32_t dv = dv0 + ((kb * kKBuf) >> 4);
+#pragma unroll
+        for (int s = 0; s < 4; ++s)
+          // B = V rows 16 s .. 16 s + 15 x 256 value columns, MN-major:
+          // 64-column panels kPanel apart, 8-row groups 1024 bytes apart
+          mma_ts(tmem + kOCol, tmem + kPCol + 32 * pb + 8 * s, sdesc_join<kHi128>(dv + ((2048 * s) >> 4)), id_pv,
+                 (seg_start && s == 0) ? 0u : 1u);
+        mma_commit(&bars[kBarKEmpty + kb]);
+        mma_commit(&bars[kBarPDone + pb]);
+        WIDE_TRACE(tl, kEvPv);
+        ++next_pv;
+        kt_pv = kt_pv + 1 == p.nt ? 0 : kt_pv + 1;
+        return true;
+      };
       while (next_pv < n_local) {
-        bool progressed = false;
+        bool progressed = try_pv();
         // QK^T of tile next_qk: its rows, the segment's Q and a free S buffer
-        if (next_qk < n_local && next_qk < next_pv + 2) {
-          const int tl = next_qk, kb = tl % kKBufs, sb = tl & 1;
+        if (next_qk < n_local) {
+          const int tl = next_qk, kb = tl % kKBufs, sb = tl % kSBufs;
           const bool seg_start = tl == 0 || kt_qk == 0;
           const bool seg_end = tl == n_local - 1 || kt_qk == p.nt - 1;
           const int seg = seg_start ? seg_q : seg_q - 1;
-          const bool s_ok = tl < 2 || mbar_test_wait(&bars[kBarSFree + sb], ((tl >> 1) + 1) & 1);
+          const bool s_ok = tl < kSBufs || mbar_test_wait(&bars[kBarSFree + sb], ((tl / kSBufs) + 1) & 1);
           const bool q_ok = !seg_start || mbar_test_wait(&bars[kBarQFull], seg & 1);
           if (s_ok && q_ok && mbar_test_wait(&bars[kBarKFull + kb], (tl / kKBufs) & 1)) {
             if (seg_start) ++seg_q;
             WIDE_TRACE(tl, kEvQkSeen);
             tc_fence_after();
-            const uint32_t kt = k0 + kb * kKBuf;
+            const uint32_t dk = dk0 + ((kb * kKBuf) >> 4);
             const uint32_t sacc = tmem + kSCol + 64 * sb;
 #pragma unroll
             for (int b = 0; b < 4; ++b) {
 #pragma unroll
-              for (int s = 0; s < 4; ++s) {
-                const uint64_t da = make_sdesc(q0 + b * kQPanel + 32 * s, 16, 1024, kLayoutSw128);
-                const uint64_t db = make_sdesc(kt + b * kPanel + 32 * s, 16, 1024, kLayoutSw128);
-                mma_ss(sacc, da, db, id_qk, (b | s) != 0 ? 1u : 0u);
-              }
+              for (int s = 0; s < 4; ++s)
+                mma_ss(sacc, sdesc_join<kHi128>(dq + ((b * kQPanel + 32 * s) >> 4)),
+                       sdesc_join<kHi128>(dk + ((b * kPanel + 32 * s) >> 4)), id_qk, (b | s) != 0 ? 1u : 0u);
+              try_pv();
             }
 #pragma unroll
-            for (int s = 0; s < 2; ++s) {  // RoPE half: 8-row atoms of 64 bytes
-              const uint64_t da = make_sdesc(q0 + 4 * kQPanel + 32 * s, 16, 512, kLayoutSw64);
-              const uint64_t db = make_sdesc(kt + 4 * kPanel + 32 * s, 16, 512, kLayoutSw64);
-              mma_ss(sacc, da, db, id_qk, 1u);
-            }
+            for (int s = 0; s < 2; ++s)  // RoPE half: 8-row atoms of 64 bytes
+              mma_ss(sacc, sdesc_join<kHi64>(dq + ((4 * kQPanel + 32 * s) >> 4)),
+                     sdesc_join<kHi64>(dk + ((4 * kPanel + 32 * s) >> 4)), id_qk, 1u);
             mma_commit(&bars[kBarSFull + sb]);
             if (seg_end) mma_commit(&bars[kBarQEmpty]);
             WIDE_TRACE(tl, kEvQk);
             ++next_qk;
             kt_qk = kt_qk + 1 == p.nt ? 0 : kt_qk + 1;
-            progressed = true;
-          }
-        }
-        // P.V of tile next_pv: its P (and, first in a segment, a free O)
-        if (next_pv < next_qk) {
-          const int tl = next_pv, kb = tl % kKBufs, sb = tl & 1;
-          const bool seg_start = tl == 0 || kt_pv == 0;
-          const bool o_ok = !seg_start || seg_o == 0 || mbar_test_wait(&bars[kBarOFree], (seg_o - 1) & 1);
-          if (o_ok && mbar_test_wait(&bars[kBarPFull + sb], (tl >> 1) & 1)) {
-            if (seg_start) ++seg_o;
-            tc_fence_after();
-            const uint32_t kt = k0 + kb * kKBuf;
-#pragma unroll
-            for (int s = 0; s < 4; ++s) {
-              // B = V rows 16 s .. 16 s + 15 x 256 value columns, MN-major:
-              // 64-column panels kPanel apart, 8-row groups 1024 bytes apart
-              const uint64_t db = make_sdesc(kt + 2048 * s, kPanel, 1024, kLayoutSw128);
-              mma_ts(tmem + kOCol, tmem + kPCol + 32 * sb + 8 * s, db, id_pv, (seg_start && s == 0) ? 0u : 1u);
-            }
-            mma_commit(&bars[kBarKEmpty + kb]);
-            mma_commit(&bars[kBarPDone + sb]);
-            WIDE_TRACE(tl, kEvPv);
-            ++next_pv;
-            kt_pv = kt_pv + 1 == p.nt ? 0 : kt_pv + 1;
             progressed = true;
           }
         }
@@ -406,7 +410,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
       const bool lead = lane == 0 && qd == 0;  // registers the slot's expected bytes
       bool dead = false;
       for (int tl = 0; tl < n_local; ++tl) {
-        const int sb = tl & 1, kb = tl % kKBufs;
+        const int sb = tl % kSBufs, kb = tl % kKBufs;
         // row validity (written by the loaders before the tile's full barrier)
         if (!dead) dead = !SMLA_WAIT(kBarKFull + kb, (tl / kKBufs) & 1);
         uint32_t vb = 0u;
@@ -426,7 +430,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
             }
           }
         }
-        if (!dead) dead = !SMLA_WAIT(kBarSFull + sb, (tl >> 1) & 1);
+        if (!dead) dead = !SMLA_WAIT(kBarSFull + sb, (tl / kSBufs) & 1);
         if (tid == 32 * kXchgWarp0) WIDE_TRACE(tl, kEvSFull);
         tc_fence_after();
         float mt = -INFINITY;
@@ -470,8 +474,9 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
               s[4 * i + 3] += v.w;
             }
           }
+          // the slot's values are in registers: the peer may overwrite it
           __syncwarp();
-          if (!dead && lane == 0) mbar_arrive_cluster(xfree_remote + 8 * e);
+          if (!dead && lane == 0) mbar_arrive_cluster_relaxed(xfree_remote + 8 * e);
           uint32_t r[2][16];
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
@@ -498,14 +503,14 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
       for (int tl = 0; tl < n_local; ++tl) {
         const bool seg_start = tl == 0 || kt == 0;
         const bool seg_end = tl == n_local - 1 || kt == p.nt - 1;
-        const int sb = tl & 1;
+        const int sb = tl % kSBufs, pb = tl & 1;
         if (seg_start) {
           m_used = -INFINITY;
           l_sum = 0.f;
           n_seg_tiles = 0;
         }
         // full, masked log2-domain logits of the tile and their maximum
-        if (!dead) dead = !SMLA_WAIT(kBarSReady + sb, (tl >> 1) & 1);
+        if (!dead) dead = !SMLA_WAIT(kBarSReady + sb, (tl / kSBufs) & 1);
         tc_fence_after();
         const float mt = fmaxf(red[(sb * 2) * kHeads + h], red[(sb * 2 + 1) * kHeads + h]);
         // A head whose max grew by more than kMaxSlack takes the new max; when
@@ -531,7 +536,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
         }
         // P (bf16 pairs) into TMEM, 32 rows at a time, once P.V(tl - 2) has
         // read the buffer
-        if (tl >= 2 && !dead) dead = !SMLA_WAIT(kBarPDone + sb, ((tl >> 1) + 1) & 1);
+        if (tl >= 2 && !dead) dead = !SMLA_WAIT(kBarPDone + pb, ((tl >> 1) + 1) & 1);
         tc_fence_after();
         const bool none = m_used == -INFINITY;
         float lt = 0.f;
@@ -557,19 +562,19 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
             pk[8 + j] = pack_bf16x2(p2, p3);
           }
           lt += l0 + l1;
-          tmem_st16(tmem + lane_base + kPCol + 32 * sb + 16 * e, pk);
+          tmem_st16(tmem + lane_base + kPCol + 32 * pb + 16 * e, pk);
         }
         tc_fence_before();
         mbar_arrive(&bars[kBarSFree + sb]);
         l_sum = l_sum * a + lt;
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&bars[kBarPFull + sb]);
+        mbar_arrive(&bars[kBarPFull + pb]);
         if (tid == 0) WIDE_TRACE(tl, kEvPFull);
         ++n_seg_tiles;
         // epilogue at the end of a segment
         if (seg_end) {
-          if (!dead) dead = !SMLA_WAIT(kBarPDone + sb, (tl >> 1) & 1);
+          if (!dead) dead = !SMLA_WAIT(kBarPDone + pb, (tl >> 1) & 1);
           tc_fence_after();
           const bool full_unit = n_seg_tiles == p.nt;  // the whole token ran in this pair
           const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
