@@ -321,7 +321,7 @@ def run_ours(args):
             step_graphs[i % n_rot].replay()
     stream.synchronize()
 
-    launches_per_step = 1 + (2 if smla_plan_needs_combine(smla, T, H, K) else 1)
+    launches_per_step = 1 + smla.attention_plan(True, T, H, K, 0)[0]  # store + the decode's launches
 
     uuid = None
     try:
@@ -404,19 +404,6 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def smla_plan_needs_combine(smla, T, H, K, hg=16) -> bool:
-    """Whether the work split leaves units spanning CTAs (then a combine
-    launch follows the attention kernel).  The FP8 decode works on 16-head
-    units; the bf16 prefill on 32-head units when H allows."""
-    import torch
-    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
-    units = T * (H // hg)
-    nt = max(1, (K + 63) // 64)
-    total = units * nt
-    G = max(1, min(total, sms))
-    return not (total % G == 0 and (total // G) % nt == 0)
-
-
 # ---------------------------------------------------------------- tensor-bound workloads (not the default line)
 
 def tensor_peak_tflops(peaks, fp8: bool) -> float:
@@ -487,7 +474,7 @@ def run_tensor_workload(args):
         n_graphs = len(idx_sets)
         flops = statistics.mean(decode_flops(case, x) for x in case.index_sets)
         fp8 = True
-        launches = 1 + (1 if smla_plan_needs_combine(smla, T, H, K, hg=16) else 0)
+        launches = smla.attention_plan(True, T, H, K, 0)[0]
         desc = (f"{case.name}: tensor-bound FP8 sparse decode, {T} requests x 1 token, H={H}, top-k {K}, "
                 f"context 65536, 656-byte FP8 cache ({NB} blocks, {NB * 64 * 656 / 1e9:.1f} GB), "
                 f"{n_graphs} rotating index sets")
@@ -516,7 +503,7 @@ def run_tensor_workload(args):
         n_graphs = 1
         flops = 2 * H * int((case.indices >= 0).sum()) * (576 + 512)
         fp8 = False
-        launches = 1 + (1 if smla_plan_needs_combine(smla, T, H, K, hg=32) else 0)
+        launches = smla.attention_plan(False, T, H, K, 0)[0]
         desc = (f"{case.name}: bf16 sparse prefill, 4 requests x 1024 new tokens over 3072 cached, H={H}, "
                 f"top-k {K}, dense latent buffer [{N}, 576] (L2-resident)")
         tok = np.linspace(0, T - 1, min(nth, 8)).astype(np.int32)

@@ -112,6 +112,17 @@ int sparse_mla_prefill_bf16(const void* q, const void* kv, const int32_t* indice
 
 size_t sparse_mla_prefill_workspace_bytes(int T, int H, int K, int num_splits);
 
+/* Work split of one attention call on the current device, for callers that
+ * count kernel launches or size grids (no work is done):
+ *   fp8      nonzero for sparse_mla_decode_fp8, zero for sparse_mla_prefill_bf16
+ *   T, H, K, num_splits as for those calls
+ *   launches out: kernels the call launches (the attention kernel, plus the
+ *            LSE combine when a unit is split across CTAs)
+ *   ctas     out: CTAs of the attention kernel's grid
+ * Returns SMLA_OK, or SMLA_ERR_INVALID_ARG / SMLA_ERR_UNSUPPORTED for sizes
+ * the call itself would reject, or SMLA_ERR_CUDA without a device. */
+int sparse_mla_attention_plan(int fp8, int T, int H, int K, int num_splits, int* launches, int* ctas);
+
 /* Quantize-and-store of new tokens into the FP8 cache (cache write of
  * FlashMLASparseImpl.forward, concat_and_cache_mla with "fp8_ds_mla", in
  * [flashmla_sparse.py]).

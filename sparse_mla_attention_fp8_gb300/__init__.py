@@ -100,6 +100,8 @@ def lib():
             L.sparse_mla_prefill_bf16.restype = i32
             L.sparse_mla_prefill_workspace_bytes.argtypes = [i32, i32, i32, i32]
             L.sparse_mla_prefill_workspace_bytes.restype = sz
+            L.sparse_mla_attention_plan.argtypes = [i32, i32, i32, i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32)]
+            L.sparse_mla_attention_plan.restype = i32
             L.mla_cache_store_fp8.argtypes = [P, P, P, i32, i32, P]
             L.mla_cache_store_fp8.restype = i32
             L.sparse_mla_translate_indices.argtypes = [P, P, P, P, i32, i32, i32, i32, i32, P]
@@ -160,6 +162,15 @@ def decode_workspace_bytes(T: int, H: int, K: int, num_splits: int = 0) -> int:
 
 def prefill_workspace_bytes(T: int, H: int, K: int, num_splits: int = 0) -> int:
     return int(lib().sparse_mla_prefill_workspace_bytes(T, H, K, num_splits))
+
+
+def attention_plan(fp8: bool, T: int, H: int, K: int, num_splits: int = 0) -> tuple:
+    """(kernel launches, attention-kernel CTAs) of one decode (fp8=True) or
+    prefill call with these sizes on the current device."""
+    launches, ctas = ctypes.c_int(0), ctypes.c_int(0)
+    _check(lib().sparse_mla_attention_plan(int(bool(fp8)), T, H, K, num_splits, ctypes.byref(launches),
+                                           ctypes.byref(ctas)), "sparse_mla_attention_plan")
+    return int(launches.value), int(ctas.value)
 
 
 def sparse_mla_decode_fp8(q, kv_cache, indices, block_table, req_id_per_token, sm_scale: float,

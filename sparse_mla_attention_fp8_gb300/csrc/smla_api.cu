@@ -273,6 +273,20 @@ size_t sparse_mla_prefill_workspace_bytes(int T, int H, int K, int num_splits) {
   return workspace_bytes_for(false, T, H, K, num_splits);
 }
 
+int sparse_mla_attention_plan(int fp8, int T, int H, int K, int num_splits, int* launches, int* ctas) {
+  if (!launches || !ctas) return fail(SMLA_ERR_INVALID_ARG, "null output pointer");
+  if (T <= 0 || K < 0 || num_splits < 0) return fail(SMLA_ERR_INVALID_ARG, "bad sizes T=%d K=%d num_splits=%d", T, K, num_splits);
+  int rc = check_heads(H);
+  if (rc != SMLA_OK) return rc;
+  int sms = 0;
+  rc = num_sms(&sms);
+  if (rc != SMLA_OK) return rc;
+  const smla::AttnPlan plan = smla::plan_attention(fp8 != 0, T, H, K, num_splits, sms);
+  *launches = plan.need_combine ? 2 : 1;
+  *ctas = plan.HG == 128 && fp8 == 0 ? 2 * plan.G : plan.G;  // the 128-head prefill runs CTA pairs
+  return SMLA_OK;
+}
+
 int mla_cache_store_fp8(const void* kv_new, const int64_t* slot_mapping, uint8_t* kv_cache, int T, int NB,
                         void* stream) {
   if (T < 0 || NB <= 0) return fail(SMLA_ERR_INVALID_ARG, "bad sizes T=%d NB=%d", T, NB);

@@ -54,3 +54,17 @@ def test_prefill_out_of_range_rows_are_masked(H):
     case.indices[1, 9] = N + 1000
     case.indices[2, :] = -1
     run_prefill(case)
+
+
+@pytest.mark.parametrize("fp8,H", [(False, 128), (False, 32), (True, 16), (True, 128)])
+def test_attention_plan_matches_the_launch_shape(fp8, H):
+    import torch
+    import sparse_mla_attention_fp8_gb300 as smla
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    launches, ctas = smla.attention_plan(fp8, 4096, H, 2048, 0)
+    assert launches in (1, 2) and 1 <= ctas <= sms
+    if not fp8 and H == 128:
+        assert ctas % 2 == 0  # CTA pairs
+    # one unit per CTA range never needs the combine
+    launches1, ctas1 = smla.attention_plan(fp8, 3, H, 2048, 1)
+    assert launches1 == 1 and ctas1 == (3 * (H // (128 if not fp8 and H == 128 else (32 if not fp8 and H % 32 == 0 else 16)))) * (2 if not fp8 and H == 128 else 1)
