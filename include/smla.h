@@ -117,7 +117,8 @@ size_t sparse_mla_prefill_workspace_bytes(int T, int H, int K, int num_splits);
  *   fp8      nonzero for sparse_mla_decode_fp8, zero for sparse_mla_prefill_bf16
  *   T, H, K, num_splits as for those calls
  *   launches out: kernels the call launches (the attention kernel, plus the
- *            LSE combine when a unit is split across CTAs)
+ *            LSE combine when a unit is split across CTAs, plus the Q
+ *            preparation of the 128-head FP8 decode)
  *   ctas     out: CTAs of the attention kernel's grid
  * Returns SMLA_OK, or SMLA_ERR_INVALID_ARG / SMLA_ERR_UNSUPPORTED for sizes
  * the call itself would reject, or SMLA_ERR_CUDA without a device. */

@@ -282,8 +282,9 @@ int sparse_mla_attention_plan(int fp8, int T, int H, int K, int num_splits, int*
   rc = num_sms(&sms);
   if (rc != SMLA_OK) return rc;
   const smla::AttnPlan plan = smla::plan_attention(fp8 != 0, T, H, K, num_splits, sms);
-  *launches = plan.need_combine ? 2 : 1;
-  *ctas = plan.HG == 128 && fp8 == 0 ? 2 * plan.G : plan.G;  // the 128-head prefill runs CTA pairs
+  // the 128-head FP8 path prepares Q in a launch of its own
+  *launches = (plan.need_combine ? 2 : 1) + (fp8 != 0 && plan.HG == 128 ? 1 : 0);
+  *ctas = plan.HG == 128 ? 2 * plan.G : plan.G;  // the 128-head kernels run CTA pairs
   return SMLA_OK;
 }
 

@@ -783,7 +783,7 @@ extern "C" int smla_trace_set(unsigned long long* buf) {
 #endif
 
 AttnPlan plan_prefill_bf16(int T, int H, int K, int num_splits, int num_sms) {
-  if (wide_prefill_supported(H)) return plan_prefill_wide(T, K, num_splits, num_sms);
+  if (wide_supported(H)) return plan_prefill_wide(T, K, num_splits, num_sms);
   AttnPlan pl;
   pl.HG = (H % 32 == 0) ? 32 : 16;
   pl.n_hg = H / pl.HG;

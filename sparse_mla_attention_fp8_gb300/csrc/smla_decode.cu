@@ -970,6 +970,7 @@ extern "C" int smla_trace_set_fp8(unsigned long long* buf) {
 #endif
 
 AttnPlan plan_decode_fp8(int T, int H, int K, int num_splits, int num_sms) {
+  if (wide_supported(H)) return plan_decode_wide(T, K, num_splits, num_sms);
   AttnPlan pl;
   pl.HG = HG;
   pl.n_hg = H / HG;
@@ -988,6 +989,7 @@ AttnPlan plan_decode_fp8(int T, int H, int K, int num_splits, int num_sms) {
 }
 
 cudaError_t launch_decode_fp8(const AttnArgs& a, const AttnPlan& plan, cudaStream_t stream) {
+  if (plan.HG == 128) return launch_decode_wide(a, plan, stream);
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(sparse_mla_decode_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

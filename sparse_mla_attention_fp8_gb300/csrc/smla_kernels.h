@@ -47,10 +47,13 @@ struct AttnArgs {
 
 cudaError_t launch_attention(bool fp8, const AttnArgs& a, const AttnPlan& plan, cudaStream_t stream);
 
-// BF16 prefill with all 128 heads of a token per CTA pair (smla_wide.cu).
-bool wide_prefill_supported(int H);
+// Attention with all 128 heads of a token per CTA pair (smla_wide.cu), over
+// the bf16 latent buffer (prefill) or the FP8 paged cache (decode).
+bool wide_supported(int H);
 AttnPlan plan_prefill_wide(int T, int K, int num_splits, int num_sms);
+AttnPlan plan_decode_wide(int T, int K, int num_splits, int num_sms);
 cudaError_t launch_prefill_wide(const AttnArgs& a, const AttnPlan& plan, cudaStream_t stream);
+cudaError_t launch_decode_wide(const AttnArgs& a, const AttnPlan& plan, cudaStream_t stream);
 cudaError_t launch_decode_fp8(const AttnArgs& a, const AttnPlan& plan, cudaStream_t stream);
 cudaError_t launch_prefill_bf16(const AttnArgs& a, const AttnPlan& plan, cudaStream_t stream);
 

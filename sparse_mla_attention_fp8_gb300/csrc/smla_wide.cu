@@ -42,6 +42,7 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include "sm103_ptx.cuh"
@@ -60,7 +61,6 @@ constexpr int kPanel = kRows * 128;         // 8 KB: 64 rows x 64 bf16
 constexpr int kQPanel = kHeads * 128;       // 16 KB: 128 heads x 64 bf16
 constexpr int kRopePanel = kRows * 64;      // 4 KB: 64 rows x 32 bf16 (this CTA's RoPE half)
 constexpr int kQRopePanel = kHeads * 64;    // 8 KB: 128 heads x 32 bf16
-constexpr int kKBufs = 3;                   // row tiles in flight
 constexpr int kKBuf = 4 * kPanel + kRopePanel;     // 36 KB
 constexpr int kQBuf = 4 * kQPanel + kQRopePanel;   // 72 KB
 constexpr int kXSlot = kHeads * 32 * 4;     // 16 KB: the peer's partial logits of one half tile (32 rows)
@@ -68,28 +68,45 @@ constexpr int kRowBytesBf16 = kDqk * 2;     // 1152
 constexpr int kLoaders = 4;                 // loader lw gathers rows 16 lw .. 16 lw + 15
 constexpr float kMaxSlack = 8.0f;           // log2 growth of a head's max tolerated before rescaling O
 
-// shared memory (offsets from a 1024-byte aligned base)
-constexpr int kOffQ = 0;
-constexpr int kOffK = kOffQ + kQBuf;
-constexpr int kOffX = kOffK + kKBufs * kKBuf;
-constexpr int kOffSlots = kOffX + 2 * kXSlot;      // int32 [4][64]
-constexpr int kOffValid = kOffSlots + 4 * kRows * 4;  // uint8 [2][64]
-constexpr int kSBufs = 3;                              // S buffers in tensor memory
-constexpr int kOffRed = kOffValid + kKBufs * kRows;    // float [kSBufs][2 halves][128]: maxima (log2 domain)
-constexpr int kOffBar = kOffRed + kSBufs * 2 * kHeads * 4;
-enum {
-  kBarKFull = 0, kBarKEmpty = kBarKFull + kKBufs, kBarSFull = kBarKEmpty + kKBufs, kBarSReady = kBarSFull + kSBufs,
-  kBarSFree = kBarSReady + kSBufs, kBarPFull = kBarSFree + kSBufs, kBarPDone = kBarPFull + 2, kBarXFull = kBarPDone + 2,
-  kBarXFree = kBarXFull + 2, kBarIdxFull = kBarXFree + 2, kBarIdxEmpty = kBarIdxFull + 4, kBarQFull = kBarIdxEmpty + 4,
-  kBarQEmpty = kBarQFull + 1, kBarOFree = kBarQEmpty + 1, kBarDrain = kBarOFree + 1, kNumBars = kBarDrain + 1
+// FP8 rows: per 4-row group the staging holds codes 0..127 and 128..255 of
+// the CTA's two scale groups (4 x 128 bytes each) and the rows' four scales
+// (4 x 16 bytes), padded to a multiple of 128 bytes (TMA destinations).
+constexpr int kRawGroup = 1152;
+constexpr int kRawBuf = (kRows / 4) * kRawGroup;  // 18 KB per tile
+constexpr int kRawRowBytes = 128 + 128 + 16;      // gathered into staging per row
+constexpr int kSBufs = 3;                         // S buffers in tensor memory
+
+// shared memory (offsets from a 1024-byte aligned base): Q, the bf16 operand
+// tiles, FP8 staging (FP8 rows only), exchange slots, index ring, row flags,
+// maxima, barriers
+template <bool kFp8>
+struct Lay {
+  static constexpr int kKBufs = kFp8 ? 2 : 3;    // operand tiles in flight
+  static constexpr int kRawBufs = kFp8 ? 2 : 0;  // FP8 staging slots
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kOffQ + kQBuf;
+  static constexpr int kOffRaw = kOffK + kKBufs * kKBuf;
+  static constexpr int kOffX = kOffRaw + kRawBufs * kRawBuf;
+  static constexpr int kOffSlots = kOffX + 2 * kXSlot;            // int32 [4][64]
+  static constexpr int kOffValid = kOffSlots + 4 * kRows * 4;      // uint8 [kKBufs][64]
+  static constexpr int kOffRed = kOffValid + kKBufs * kRows;       // float [kSBufs][2 halves][128]: maxima (log2)
+  static constexpr int kOffBar = kOffRed + kSBufs * 2 * kHeads * 4;
+  enum {
+    kBarKFull = 0, kBarKEmpty = kBarKFull + kKBufs, kBarSFull = kBarKEmpty + kKBufs, kBarSReady = kBarSFull + kSBufs,
+    kBarSFree = kBarSReady + kSBufs, kBarPFull = kBarSFree + kSBufs, kBarPDone = kBarPFull + 2,
+    kBarXFull = kBarPDone + 2, kBarXFree = kBarXFull + 2, kBarIdxFull = kBarXFree + 2,
+    kBarIdxEmpty = kBarIdxFull + 4, kBarQFull = kBarIdxEmpty + 4, kBarQEmpty = kBarQFull + 1,
+    kBarOFree = kBarQEmpty + 1, kBarDrain = kBarOFree + 1,
+    kBarRawFull = kBarDrain + 1,  // [loader][staging slot], FP8 rows only
+    kNumBars = kBarRawFull + 2 * kLoaders
+  };
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort flag
+  static constexpr int kSmemAlloc = kOffMisc + 16 + 1024;
+  static_assert(kOffK % 1024 == 0 && kOffRaw % 128 == 0 && kKBuf % 1024 == 0, "operand alignment");
+  static_assert(kOffBar % 8 == 0 && kOffRed % 16 == 0 && kOffX % 16 == 0, "alignment");
+  static_assert(kSmemAlloc <= 232448, "shared memory budget");
 };
-constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort flag
-constexpr int kSmemBytes = kOffMisc + 16;
-constexpr int kSmemAlloc = kSmemBytes + 1024;
-static_assert(kOffK % 1024 == 0 && kOffX % 1024 == 0 && kKBuf % 1024 == 0, "operand alignment");
 static_assert((4 * kPanel) % 512 == 0 && (4 * kQPanel) % 512 == 0, "64-byte-swizzle atoms are 512 bytes");
-static_assert(kOffBar % 8 == 0 && kOffRed % 16 == 0, "alignment");
-static_assert(kSmemAlloc <= 232448, "shared memory budget");
 
 // tensor memory columns
 constexpr int kOCol = 0;    // O_c: 256 fp32 columns
@@ -120,7 +137,11 @@ enum { kEvSFull = 0, kEvSLoaded, kEvXFree, kEvSent, kEvXFull, kEvPReady, kEvPFul
 
 struct Params {
   const __nv_bfloat16* q;  // [T, 128, 576]
-  const int32_t* indices;  // [T, K]
+  const int32_t* indices;  // [T, K]: kv rows (bf16) or logical token indices (FP8)
+  const int32_t* block_table;  // FP8 rows: [R, MB]
+  const int32_t* req_id;       // FP8 rows: [T]
+  const float* qinv;           // FP8 rows: [T, 128] 2^-s of each head's Q prescale
+  int R, MB;
   __nv_bfloat16* out;      // [T, 128, 512]
   float* lse;              // [T, 128]
   float* part_o;           // [slots, 128, 512]
@@ -128,7 +149,7 @@ struct Params {
   int* status;
   float scale_log2;        // softmax_scale * log2(e)
   int T, K;
-  int64_t N;               // kv rows
+  int64_t N;               // kv rows (bf16) or physical 64-row blocks (FP8)
   int nt;                  // tiles per token
   int64_t total;           // T * nt
   int G;                   // pairs
@@ -148,17 +169,23 @@ __device__ __forceinline__ TileInfo tile_info(const Params& p, int64_t x, int64_
   return ti;
 }
 
+// Row maps: bf16 rows: m0 = 128-byte value panels (128-byte swizzle), m1
+// unused, m2 = 64-byte RoPE halves (64-byte swizzle).  FP8 rows: m0 = 128
+// bytes of codes, m1 = the 16 scale bytes (both unswizzled, into staging), m2
+// = the 64-byte RoPE halves (64-byte swizzle, into the operand tile).
+template <bool kFp8>
 __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
-    sparse_mla_wide_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap kv_map,
-                           const __grid_constant__ CUtensorMap kv_rope_map, const __grid_constant__ CUtensorMap q_map,
-                           const __grid_constant__ CUtensorMap q_rope_map) {
+    sparse_mla_wide_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap m0,
+                           const __grid_constant__ CUtensorMap m1, const __grid_constant__ CUtensorMap m2,
+                           const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap q_rope_map) {
+  using L = Lay<kFp8>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
-  int32_t* slots_ring = reinterpret_cast<int32_t*>(smem + kOffSlots);
-  uint8_t* valid = smem + kOffValid;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kOffMisc + 4);
+  int32_t* slots_ring = reinterpret_cast<int32_t*>(smem + L::kOffSlots);
+  uint8_t* valid = smem + L::kOffValid;
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
@@ -170,31 +197,33 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
   const int n_local = (int)(xend - xbeg);
 
   if (tid == 0) {
-    for (int i = 0; i < kKBufs; ++i) {
-      mbar_init(&bars[kBarKFull + i], kLoaders);
-      mbar_init(&bars[kBarKEmpty + i], 1);
+    for (int i = 0; i < L::kKBufs; ++i) {
+      mbar_init(&bars[L::kBarKFull + i], kLoaders);
+      mbar_init(&bars[L::kBarKEmpty + i], 1);
     }
     for (int i = 0; i < kSBufs; ++i) {
-      mbar_init(&bars[kBarSFull + i], 1);
-      mbar_init(&bars[kBarSReady + i], 32 * kXchgWarps);
-      mbar_init(&bars[kBarSFree + i], 32 * kSoftWarps);
+      mbar_init(&bars[L::kBarSFull + i], 1);
+      mbar_init(&bars[L::kBarSReady + i], 32 * kXchgWarps);
+      mbar_init(&bars[L::kBarSFree + i], 32 * kSoftWarps);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&bars[kBarPFull + i], 32 * kSoftWarps);
-      mbar_init(&bars[kBarPDone + i], 1);
+      mbar_init(&bars[L::kBarPFull + i], 32 * kSoftWarps);
+      mbar_init(&bars[L::kBarPDone + i], 1);
     }
     for (int i = 0; i < 2; ++i) {               // exchange slot i carries half i of every tile
-      mbar_init(&bars[kBarXFull + i], 1);           // own expect_tx + the peer's st.async bytes
-      mbar_init(&bars[kBarXFree + i], kSoftWarps);  // one arrival per peer exchange warp
+      mbar_init(&bars[L::kBarXFull + i], 1);           // own expect_tx + the peer's st.async bytes
+      mbar_init(&bars[L::kBarXFree + i], kSoftWarps);  // one arrival per peer exchange warp
     }
     for (int i = 0; i < 4; ++i) {
-      mbar_init(&bars[kBarIdxFull + i], 32);
-      mbar_init(&bars[kBarIdxEmpty + i], kLoaders);
+      mbar_init(&bars[L::kBarIdxFull + i], 32);
+      mbar_init(&bars[L::kBarIdxEmpty + i], kLoaders);
     }
-    mbar_init(&bars[kBarQFull], 1);
-    mbar_init(&bars[kBarQEmpty], 1);
-    mbar_init(&bars[kBarOFree], 32 * kSoftWarps);
-    mbar_init(&bars[kBarDrain], 1);
+    if (kFp8)
+      for (int i = 0; i < 2 * kLoaders; ++i) mbar_init(&bars[L::kBarRawFull + i], 1);  // per loader and slot
+    mbar_init(&bars[L::kBarQFull], 1);
+    mbar_init(&bars[L::kBarQEmpty], 1);
+    mbar_init(&bars[L::kBarOFree], 32 * kSoftWarps);
+    mbar_init(&bars[L::kBarDrain], 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -218,7 +247,8 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
     for (int tl = 0; tl < n_local; ++tl) {
       const TileInfo ti = tile_info(p, xbeg + tl, xbeg, xend);
       const int b4 = tl & 3;
-      if (tl >= 4 && !SMLA_WAIT(kBarIdxEmpty + b4, ((tl >> 2) + 1) & 1)) break;
+      if (tl >= 4 && !SMLA_WAIT(L::kBarIdxEmpty + b4, ((tl >> 2) + 1) & 1)) break;
+      const int32_t req = kFp8 ? __ldg(p.req_id + ti.u) : 0;
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
         const int r = lane + 32 * i;
@@ -226,28 +256,124 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
         int32_t s = -1;
         if (k < p.K) {
           const int32_t idx = __ldg(p.indices + (int64_t)ti.u * p.K + k);
-          s = (idx >= 0 && (int64_t)idx < p.N) ? idx : -1;
+          if constexpr (kFp8)
+            s = translate_slot(idx, req, p.block_table, p.R, p.MB, p.N);
+          else
+            s = (idx >= 0 && (int64_t)idx < p.N) ? idx : -1;
         }
         slots_ring[b4 * kRows + r] = s;
       }
-      mbar_arrive(&bars[kBarIdxFull + b4]);
+      mbar_arrive(&bars[L::kBarIdxFull + b4]);
       if (ti.seg_start) {
         // the segment's Q block, once the previous segment's last QK^T is done
-        if (seg >= 1 && !SMLA_WAIT(kBarQEmpty, (seg - 1) & 1)) break;
+        if (seg >= 1 && !SMLA_WAIT(L::kBarQEmpty, (seg - 1) & 1)) break;
         if (lane == 0) {
-          mbar_arrive_expect_tx(&bars[kBarQFull], (uint32_t)kQBuf);
+          mbar_arrive_expect_tx(&bars[L::kBarQFull], (uint32_t)kQBuf);
           for (int b = 0; b < 4; ++b)
-            tma_load_2d(smem_u32(smem + kOffQ + b * kQPanel), &q_map, 128 * (4 * c + b), ti.u * kHeads,
-                        &bars[kBarQFull]);
-          tma_load_2d(smem_u32(smem + kOffQ + 4 * kQPanel), &q_rope_map, 2 * kDv + 64 * c, ti.u * kHeads,
-                      &bars[kBarQFull]);
+            tma_load_2d(smem_u32(smem + L::kOffQ + b * kQPanel), &q_map, 128 * (4 * c + b), ti.u * kHeads,
+                        &bars[L::kBarQFull]);
+          tma_load_2d(smem_u32(smem + L::kOffQ + 4 * kQPanel), &q_rope_map, 2 * kDv + 64 * c, ti.u * kHeads,
+                      &bars[L::kBarQFull]);
         }
         __syncwarp();
         ++seg;
       }
     }
     // no Q copy may still be landing in shared memory when the CTA exits
-    if (seg > 0 && lane == 0) mbar_wait_drain(&bars[kBarQFull], (seg - 1) & 1);
+    if (seg > 0 && lane == 0) mbar_wait_drain(&bars[L::kBarQFull], (seg - 1) & 1);
+    __syncwarp();
+  } else if (kFp8 && warp >= kLoadWarp0) {
+    // ------------------------------------------------------------ FP8 row loaders + converters
+    // Loader lw owns tile rows 16 lw .. 16 lw + 15 (staging groups 4 lw ..
+    // 4 lw + 3).  Two tiles ahead it gathers their codes (the CTA's two scale
+    // groups) and scales into a staging slot, lane 3 g + b issuing copy b of
+    // group g; when an operand tile is free it gathers the RoPE half straight
+    // into it (bf16 in the row) and converts the staged codes to f16 (code x
+    // scale, exact e4m3 widening then one rounding to 11 bits), lane l
+    // handling codes 8 l .. 8 l + 7 of each row.
+    const int lw = warp - kLoadWarp0;
+    uint8_t* raw_base = smem + L::kOffRaw;
+    const int rgrp = lane / 3, rbox = lane - 3 * rgrp;
+    int raw_issued = 0;
+    auto issue_raw = [&](int t2) -> bool {
+      const int b4 = t2 & 3, sl = t2 & 1;
+      if (!SMLA_WAIT(L::kBarIdxFull + b4, (t2 >> 2) & 1)) return false;
+      const int32_t s = lane < 16 ? slots_ring[b4 * kRows + 16 * lw + lane] : -1;
+      const int r0 = __shfl_sync(kFullMask, s, (4 * rgrp) & 31), r1 = __shfl_sync(kFullMask, s, (4 * rgrp + 1) & 31);
+      const int r2 = __shfl_sync(kFullMask, s, (4 * rgrp + 2) & 31), r3 = __shfl_sync(kFullMask, s, (4 * rgrp + 3) & 31);
+      uint64_t* bar = &bars[L::kBarRawFull + 2 * lw + sl];
+      if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(16 * kRawRowBytes));
+      __syncwarp();
+      if (lane < 12) {
+        const uint32_t dst = smem_u32(raw_base + sl * kRawBuf + (4 * lw + rgrp) * kRawGroup + 512 * rbox);
+        if (rbox < 2)
+          tma_gather4_2d(dst, &m0, 256 * c + 128 * rbox, r0, r1, r2, r3, bar);
+        else
+          tma_gather4_2d(dst, &m1, kScaleOff, r0, r1, r2, r3, bar);
+      }
+      ++raw_issued;
+      return true;
+    };
+    bool ok = true;
+    if (n_local > 0) ok = issue_raw(0);
+    if (ok && n_local > 1) ok = issue_raw(1);
+    int last_b = -1, last_use = 0, converted = 0;
+    for (int tl = 0; ok && tl < n_local; ++tl) {
+      const int b4 = tl & 3, kb = tl % L::kKBufs, use = tl / L::kKBufs, sl = tl & 1;
+      if (!SMLA_WAIT(L::kBarIdxFull + b4, (tl >> 2) & 1)) break;
+      const int32_t slot = lane < 16 ? slots_ring[b4 * kRows + 16 * lw + lane] : -1;
+      const uint32_t vmask = __ballot_sync(kFullMask, slot >= 0);
+      const int g0 = __shfl_sync(kFullMask, slot, (4 * lane) & 31), g1 = __shfl_sync(kFullMask, slot, (4 * lane + 1) & 31);
+      const int g2 = __shfl_sync(kFullMask, slot, (4 * lane + 2) & 31), g3 = __shfl_sync(kFullMask, slot, (4 * lane + 3) & 31);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[L::kBarIdxEmpty + b4]);
+      if (!SMLA_WAIT(L::kBarRawFull + 2 * lw + sl, (tl >> 1) & 1)) break;
+      if (use >= 1 && !SMLA_WAIT(L::kBarKEmpty + kb, (use + 1) & 1)) break;
+      if (lane == 0 && lw == 0) WIDE_TRACE(tl, kEvKEmpty);
+      if (lane < 16) valid[kb * kRows + 16 * lw + lane] = (uint8_t)((vmask >> lane) & 1u);
+      const uint32_t tile = smem_u32(smem + L::kOffK + kb * kKBuf);
+      // the tile's full barrier: this warp's RoPE bytes (registered before the
+      // copies), then its arrival once its rows are converted
+      if (lane == 0) mbar_expect_tx(&bars[L::kBarKFull + kb], (uint32_t)(16 * 64));
+      __syncwarp();
+      if (lane < 4) {
+        const int r_g = 16 * lw + 4 * lane;
+        tma_gather4_2d(tile + 4 * kPanel + (uint32_t)((r_g >> 3) * 512 + (r_g & 7) * 64), &m2, kRopeOff + 64 * c, g0,
+                       g1, g2, g3, &bars[L::kBarKFull + kb]);
+      }
+      const uint8_t* raw = raw_base + sl * kRawBuf;
+      const int half = lane >> 4, pnl = lane >> 3, ch = lane & 7;
+#pragma unroll 4
+      for (int rr = 0; rr < 16; ++rr) {
+        const int r = 16 * lw + rr;
+        const uint8_t* grp = raw + (r >> 2) * kRawGroup;
+        const uint2 cw = *reinterpret_cast<const uint2*>(grp + 512 * half + (r & 3) * 128 + 8 * (lane & 15));
+        const float sc = *reinterpret_cast<const float*>(grp + 1024 + (r & 3) * 16 + 4 * (2 * c + half));
+        uint32_t o[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint16_t pr = (uint16_t)(((k < 2 ? cw.x : cw.y) >> (16 * (k & 1))) & 0xFFFFu);
+          uint32_t h2;
+          asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(pr));
+          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+          o[k] = pack_f16x2(f.x * sc, f.y * sc);
+        }
+        st_shared_v4(tile + pnl * kPanel + (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((ch ^ (r & 7)) << 4)), o[0],
+                     o[1], o[2], o[3]);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[L::kBarKFull + kb]);
+      if (lane == 0 && lw == 0) WIDE_TRACE(tl, kEvIssue);
+      last_b = kb;
+      last_use = use;
+      converted = tl + 1;
+      if (tl + 2 < n_local) ok = issue_raw(tl + 2);
+    }
+    // no copy may still be landing in shared memory when the CTA exits
+    if (last_b >= 0) mbar_wait_drain(&bars[L::kBarKFull + last_b], last_use & 1);
+    for (int t2 = converted; t2 < raw_issued; ++t2)
+      if (lane == 0) mbar_wait_drain(&bars[L::kBarRawFull + 2 * lw + (t2 & 1)], (t2 >> 1) & 1);
     __syncwarp();
   } else if (warp >= kLoadWarp0) {
     // ------------------------------------------------------------ row loaders
@@ -260,41 +386,43 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
     const int r_g = 16 * lw + 4 * grp;  // tile row of the lane's group
     int last_b = -1, last_use = 0;
     for (int tl = 0; tl < n_local; ++tl) {
-      const int b4 = tl & 3, kb = tl % kKBufs, use = tl / kKBufs;
-      if (!SMLA_WAIT(kBarIdxFull + b4, (tl >> 2) & 1)) break;
+      const int b4 = tl & 3, kb = tl % L::kKBufs, use = tl / L::kKBufs;
+      if (!SMLA_WAIT(L::kBarIdxFull + b4, (tl >> 2) & 1)) break;
       const int32_t slot = lane < 16 ? slots_ring[b4 * kRows + 16 * lw + lane] : -1;
       const uint32_t vmask = __ballot_sync(kFullMask, slot >= 0);
       const int g0 = __shfl_sync(kFullMask, slot, (4 * grp) & 31), g1 = __shfl_sync(kFullMask, slot, (4 * grp + 1) & 31);
       const int g2 = __shfl_sync(kFullMask, slot, (4 * grp + 2) & 31), g3 = __shfl_sync(kFullMask, slot, (4 * grp + 3) & 31);
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[kBarIdxEmpty + b4]);
-      if (use >= 1 && !SMLA_WAIT(kBarKEmpty + kb, (use + 1) & 1)) break;
+      if (lane == 0) mbar_arrive(&bars[L::kBarIdxEmpty + b4]);
+      if (use >= 1 && !SMLA_WAIT(L::kBarKEmpty + kb, (use + 1) & 1)) break;
       if (lane == 0 && lw == 0) WIDE_TRACE(tl, kEvKEmpty);
       if (lane < 16) valid[kb * kRows + 16 * lw + lane] = (uint8_t)((vmask >> lane) & 1u);
       __syncwarp();
-      if (lane == 0) mbar_arrive_expect_tx(&bars[kBarKFull + kb], (uint32_t)(16 * (kKBuf / kRows)));
+      if (lane == 0) mbar_arrive_expect_tx(&bars[L::kBarKFull + kb], (uint32_t)(16 * (kKBuf / kRows)));
       __syncwarp();
       if (lane < 20) {
-        const uint32_t tile = smem_u32(smem + kOffK + kb * kKBuf);
+        const uint32_t tile = smem_u32(smem + L::kOffK + kb * kKBuf);
         if (box < 4)
-          tma_gather4_2d(tile + box * kPanel + (uint32_t)((r_g >> 3) * 1024 + (r_g & 7) * 128), &kv_map,
-                         128 * (4 * c + box), g0, g1, g2, g3, &bars[kBarKFull + kb]);
+          tma_gather4_2d(tile + box * kPanel + (uint32_t)((r_g >> 3) * 1024 + (r_g & 7) * 128), &m0,
+                         128 * (4 * c + box), g0, g1, g2, g3, &bars[L::kBarKFull + kb]);
         else
-          tma_gather4_2d(tile + 4 * kPanel + (uint32_t)((r_g >> 3) * 512 + (r_g & 7) * 64), &kv_rope_map,
-                         2 * kDv + 64 * c, g0, g1, g2, g3, &bars[kBarKFull + kb]);
+          tma_gather4_2d(tile + 4 * kPanel + (uint32_t)((r_g >> 3) * 512 + (r_g & 7) * 64), &m2,
+                         2 * kDv + 64 * c, g0, g1, g2, g3, &bars[L::kBarKFull + kb]);
       }
       if (lane == 0 && lw == 0) WIDE_TRACE(tl, kEvIssue);
       last_b = kb;
       last_use = use;
     }
     // no copy may still be landing in shared memory when the CTA exits
-    if (last_b >= 0) mbar_wait_drain(&bars[kBarKFull + last_b], last_use & 1);
+    if (last_b >= 0) mbar_wait_drain(&bars[L::kBarKFull + last_b], last_use & 1);
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------ tensor-core issuer
     if (lane == 0 && n_local > 0) {
-      constexpr uint32_t id_qk = make_idesc_bf16(128, kRows, 0, 0);
-      constexpr uint32_t id_pv = make_idesc_bf16(128, 256, 0, 1);
-      const uint32_t q0 = smem_u32(smem + kOffQ), k0 = smem_u32(smem + kOffK);  // 1024-byte aligned
+      // FP8 rows: value panels, Q's value part and P in f16; RoPE parts in bf16
+      constexpr uint32_t id_qk = kFp8 ? make_idesc_f16(128, kRows, 0, 0) : make_idesc_bf16(128, kRows, 0, 0);
+      constexpr uint32_t id_qkr = make_idesc_bf16(128, kRows, 0, 0);
+      constexpr uint32_t id_pv = kFp8 ? make_idesc_f16(128, 256, 0, 1) : make_idesc_bf16(128, 256, 0, 1);
+      const uint32_t q0 = smem_u32(smem + L::kOffQ), k0 = smem_u32(smem + L::kOffK);  // 1024-byte aligned
       int seg_q = 0, seg_o = 0, next_qk = 0, next_pv = 0;
       const int kt0 = (int)(xbeg % p.nt);
       int kt_qk = kt0, kt_pv = kt0;
@@ -308,10 +436,10 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
       // row tile the loaders wait for, so it never waits out a whole QK^T.
       auto try_pv = [&]() -> bool {
         if (next_pv >= next_qk) return false;
-        const int tl = next_pv, kb = tl % kKBufs, pb = tl & 1;
+        const int tl = next_pv, kb = tl % L::kKBufs, pb = tl & 1;
         const bool seg_start = tl == 0 || kt_pv == 0;
-        const bool o_ok = !seg_start || seg_o == 0 || mbar_test_wait(&bars[kBarOFree], (seg_o - 1) & 1);
-        if (!o_ok || !mbar_test_wait(&bars[kBarPFull + pb], (tl >> 1) & 1)) return false;
+        const bool o_ok = !seg_start || seg_o == 0 || mbar_test_wait(&bars[L::kBarOFree], (seg_o - 1) & 1);
+        if (!o_ok || !mbar_test_wait(&bars[L::kBarPFull + pb], (tl >> 1) & 1)) return false;
         if (seg_start) ++seg_o;
         tc_fence_after();
         const uint32_t dv = dv0 + ((kb * kKBuf) >> 4);
@@ -321,8 +449,8 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
           // 64-column panels kPanel apart, 8-row groups 1024 bytes apart
           mma_ts(tmem + kOCol, tmem + kPCol + 32 * pb + 8 * s, sdesc_join<kHi128>(dv + ((2048 * s) >> 4)), id_pv,
                  (seg_start && s == 0) ? 0u : 1u);
-        mma_commit(&bars[kBarKEmpty + kb]);
-        mma_commit(&bars[kBarPDone + pb]);
+        mma_commit(&bars[L::kBarKEmpty + kb]);
+        mma_commit(&bars[L::kBarPDone + pb]);
         WIDE_TRACE(tl, kEvPv);
         ++next_pv;
         kt_pv = kt_pv + 1 == p.nt ? 0 : kt_pv + 1;
@@ -332,13 +460,13 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
         bool progressed = try_pv();
         // QK^T of tile next_qk: its rows, the segment's Q and a free S buffer
         if (next_qk < n_local) {
-          const int tl = next_qk, kb = tl % kKBufs, sb = tl % kSBufs;
+          const int tl = next_qk, kb = tl % L::kKBufs, sb = tl % kSBufs;
           const bool seg_start = tl == 0 || kt_qk == 0;
           const bool seg_end = tl == n_local - 1 || kt_qk == p.nt - 1;
           const int seg = seg_start ? seg_q : seg_q - 1;
-          const bool s_ok = tl < kSBufs || mbar_test_wait(&bars[kBarSFree + sb], ((tl / kSBufs) + 1) & 1);
-          const bool q_ok = !seg_start || mbar_test_wait(&bars[kBarQFull], seg & 1);
-          if (s_ok && q_ok && mbar_test_wait(&bars[kBarKFull + kb], (tl / kKBufs) & 1)) {
+          const bool s_ok = tl < kSBufs || mbar_test_wait(&bars[L::kBarSFree + sb], ((tl / kSBufs) + 1) & 1);
+          const bool q_ok = !seg_start || mbar_test_wait(&bars[L::kBarQFull], seg & 1);
+          if (s_ok && q_ok && mbar_test_wait(&bars[L::kBarKFull + kb], (tl / L::kKBufs) & 1)) {
             if (seg_start) ++seg_q;
             WIDE_TRACE(tl, kEvQkSeen);
             tc_fence_after();
@@ -355,9 +483,9 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
 #pragma unroll
             for (int s = 0; s < 2; ++s)  // RoPE half: 8-row atoms of 64 bytes
               mma_ss(sacc, sdesc_join<kHi64>(dq + ((4 * kQPanel + 32 * s) >> 4)),
-                     sdesc_join<kHi64>(dk + ((4 * kPanel + 32 * s) >> 4)), id_qk, 1u);
-            mma_commit(&bars[kBarSFull + sb]);
-            if (seg_end) mma_commit(&bars[kBarQEmpty]);
+                     sdesc_join<kHi64>(dk + ((4 * kPanel + 32 * s) >> 4)), id_qkr, 1u);
+            mma_commit(&bars[L::kBarSFull + sb]);
+            if (seg_end) mma_commit(&bars[L::kBarQEmpty]);
             WIDE_TRACE(tl, kEvQk);
             ++next_qk;
             kt_qk = kt_qk + 1 == p.nt ? 0 : kt_qk + 1;
@@ -381,8 +509,8 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
       }
       // every issued tensor-core operation completes before tensor memory is released
       if (next_qk > 0) {
-        mma_commit(&bars[kBarDrain]);
-        mbar_wait_drain(&bars[kBarDrain], 0);
+        mma_commit(&bars[L::kBarDrain]);
+        mbar_wait_drain(&bars[L::kBarDrain], 0);
       }
     }
     __syncwarp();
@@ -390,7 +518,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
     const int qd = warp & 3;
     const int h = 32 * qd + lane;  // head = TMEM lane of S, P and O
     const uint32_t lane_base = (uint32_t)(32 * qd) << 16;
-    float* red = reinterpret_cast<float*>(smem + kOffRed);
+    float* red = reinterpret_cast<float*>(smem + L::kOffRed);
     if (warp >= kXchgWarp0) {
       // ---------------------------------------------------------- exchange (warps 4..11)
       // Warp group e handles half e of every tile (rows 32 e .. 32 e + 31,
@@ -402,17 +530,24 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
       // the log2 domain, and the result is written back over the S buffer.  A
       // half is sent once the peer has read the same half of the previous tile.
       const uint32_t peer = (uint32_t)(c ^ 1);
-      const uint32_t x_local = smem_u32(smem + kOffX) + (uint32_t)(h * 128);
+      const uint32_t x_local = smem_u32(smem + L::kOffX) + (uint32_t)(h * 128);
       const uint32_t x_remote = mapa_shared(x_local, peer);
-      const uint32_t xfull_remote = mapa_shared(smem_u32(&bars[kBarXFull]), peer);
-      const uint32_t xfree_remote = mapa_shared(smem_u32(&bars[kBarXFree]), peer);
+      const uint32_t xfull_remote = mapa_shared(smem_u32(&bars[L::kBarXFull]), peer);
+      const uint32_t xfree_remote = mapa_shared(smem_u32(&bars[L::kBarXFree]), peer);
       const int e = (warp - kXchgWarp0) >> 2;
       const bool lead = lane == 0 && qd == 0;  // registers the slot's expected bytes
       bool dead = false;
+      int u = (int)(xbeg / p.nt), kt = (int)(xbeg - (int64_t)u * p.nt);
       for (int tl = 0; tl < n_local; ++tl) {
-        const int sb = tl % kSBufs, kb = tl % kKBufs;
+        // FP8 rows: Q was scaled by 2^s per head; the logits take 2^-s back
+        const float sl2 = kFp8 ? p.scale_log2 * __ldg(p.qinv + (int64_t)u * kHeads + h) : p.scale_log2;
+        if (++kt == p.nt) {
+          kt = 0;
+          ++u;
+        }
+        const int sb = tl % kSBufs, kb = tl % L::kKBufs;
         // row validity (written by the loaders before the tile's full barrier)
-        if (!dead) dead = !SMLA_WAIT(kBarKFull + kb, (tl / kKBufs) & 1);
+        if (!dead) dead = !SMLA_WAIT(L::kBarKFull + kb, (tl / L::kKBufs) & 1);
         uint32_t vb = 0u;
         {
           const uint4* vf = reinterpret_cast<const uint4*>(valid + kb * kRows + 32 * e);
@@ -430,13 +565,13 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
             }
           }
         }
-        if (!dead) dead = !SMLA_WAIT(kBarSFull + sb, (tl / kSBufs) & 1);
+        if (!dead) dead = !SMLA_WAIT(L::kBarSFull + sb, (tl / kSBufs) & 1);
         if (tid == 32 * kXchgWarp0) WIDE_TRACE(tl, kEvSFull);
         tc_fence_after();
         float mt = -INFINITY;
         {
           const uint32_t scol = tmem + lane_base + kSCol + 64 * sb + 32 * e;
-          if (lead) mbar_arrive_expect_tx(&bars[kBarXFull + e], (uint32_t)kXSlot);
+          if (lead) mbar_arrive_expect_tx(&bars[L::kBarXFull + e], (uint32_t)kXSlot);
           float s[32];
           {
             uint32_t r0[16], r1[16];
@@ -452,7 +587,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
             }
           }
           if (tid == 32 * kXchgWarp0 && e == 0) WIDE_TRACE(tl, kEvSLoaded);
-          if (tl >= 1 && !dead) dead = !SMLA_WAIT_X(kBarXFree + e, (tl - 1) & 1);
+          if (tl >= 1 && !dead) dead = !SMLA_WAIT_X(L::kBarXFree + e, (tl - 1) & 1);
           if (tid == 32 * kXchgWarp0 && e == 0) WIDE_TRACE(tl, kEvXFree);
           if (!dead) {
 #pragma unroll
@@ -461,10 +596,10 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
                           s[4 * i + 3], xfull_remote + 8 * e);
           }
           if (tid == 32 * kXchgWarp0 && e == 0) WIDE_TRACE(tl, kEvSent);
-          if (!dead) dead = !SMLA_WAIT_X(kBarXFull + e, tl & 1);
+          if (!dead) dead = !SMLA_WAIT_X(L::kBarXFull + e, tl & 1);
           if (tid == 32 * kXchgWarp0 && e == 0) WIDE_TRACE(tl, kEvXFull);
           if (!dead) {
-            const uint8_t* src = smem + kOffX + e * kXSlot + h * 128;
+            const uint8_t* src = smem + L::kOffX + e * kXSlot + h * 128;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
               const float4 v = *reinterpret_cast<const float4*>(src + 16 * ((i + h) & 7));
@@ -480,7 +615,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
           uint32_t r[2][16];
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            const float x = (vb >> j) & 1u ? s[j] * p.scale_log2 : -INFINITY;
+            const float x = (vb >> j) & 1u ? s[j] * sl2 : -INFINITY;
             mt = fmaxf(mt, x);
             r[j >> 4][j & 15] = __float_as_uint(x);
           }
@@ -491,7 +626,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
         tmem_st_wait();
         red[(sb * 2 + e) * kHeads + h] = mt;
         tc_fence_before();
-        mbar_arrive(&bars[kBarSReady + sb]);
+        mbar_arrive(&bars[L::kBarSReady + sb]);
         if (tid == 32 * kXchgWarp0) WIDE_TRACE(tl, kEvPReady);
       }
     } else {
@@ -510,7 +645,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
           n_seg_tiles = 0;
         }
         // full, masked log2-domain logits of the tile and their maximum
-        if (!dead) dead = !SMLA_WAIT(kBarSReady + sb, (tl / kSBufs) & 1);
+        if (!dead) dead = !SMLA_WAIT(L::kBarSReady + sb, (tl / kSBufs) & 1);
         tc_fence_after();
         const float mt = fmaxf(red[(sb * 2) * kHeads + h], red[(sb * 2 + 1) * kHeads + h]);
         // A head whose max grew by more than kMaxSlack takes the new max; when
@@ -523,7 +658,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
         // TMEM access is warp-wide: a warp with any head to rescale runs the
         // pass (factor 1 for its other heads), once P.V(tl - 1) has landed in O
         if (__any_sync(kFullMask, scale_o)) {
-          if (!dead) dead = !SMLA_WAIT(kBarPDone + ((tl - 1) & 1), ((tl - 1) >> 1) & 1);
+          if (!dead) dead = !SMLA_WAIT(L::kBarPDone + ((tl - 1) & 1), ((tl - 1) >> 1) & 1);
           tc_fence_after();
 #pragma unroll 1
           for (int q = 0; q < 256 / 16; ++q) {
@@ -536,7 +671,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
         }
         // P (bf16 pairs) into TMEM, 32 rows at a time, once P.V(tl - 2) has
         // read the buffer
-        if (tl >= 2 && !dead) dead = !SMLA_WAIT(kBarPDone + pb, ((tl >> 1) + 1) & 1);
+        if (tl >= 2 && !dead) dead = !SMLA_WAIT(L::kBarPDone + pb, ((tl >> 1) + 1) & 1);
         tc_fence_after();
         const bool none = m_used == -INFINITY;
         float lt = 0.f;
@@ -558,23 +693,23 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
             const float p3 = none ? 0.f : ex2_approx(__uint_as_float(r1[2 * j + 1]) - m_used);
             l0 += p0 + p2;
             l1 += p1 + p3;
-            pk[j] = pack_bf16x2(p0, p1);
-            pk[8 + j] = pack_bf16x2(p2, p3);
+            pk[j] = kFp8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
+            pk[8 + j] = kFp8 ? pack_f16x2(p2, p3) : pack_bf16x2(p2, p3);
           }
           lt += l0 + l1;
           tmem_st16(tmem + lane_base + kPCol + 32 * pb + 16 * e, pk);
         }
         tc_fence_before();
-        mbar_arrive(&bars[kBarSFree + sb]);
+        mbar_arrive(&bars[L::kBarSFree + sb]);
         l_sum = l_sum * a + lt;
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&bars[kBarPFull + pb]);
+        mbar_arrive(&bars[L::kBarPFull + pb]);
         if (tid == 0) WIDE_TRACE(tl, kEvPFull);
         ++n_seg_tiles;
         // epilogue at the end of a segment
         if (seg_end) {
-          if (!dead) dead = !SMLA_WAIT(kBarPDone + pb, (tl >> 1) & 1);
+          if (!dead) dead = !SMLA_WAIT(L::kBarPDone + pb, (tl >> 1) & 1);
           tc_fence_after();
           const bool full_unit = n_seg_tiles == p.nt;  // the whole token ran in this pair
           const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
@@ -607,7 +742,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
               p.part_lse[slot * kHeads + h] = lse_v;
           }
           tc_fence_before();
-          mbar_arrive(&bars[kBarOFree]);
+          mbar_arrive(&bars[L::kBarOFree]);
         }
         if (++kt == p.nt) {
           kt = 0;
@@ -628,6 +763,59 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
   cluster_sync_all();
 }
 
+// Q of the FP8 path: each (token, head) row of 576 bf16 values is scaled by
+// 2^s, s chosen so that its largest magnitude lands in [2^14, 2^15), and
+// stored as f16 (value part, exact for the bf16 values in range) and bf16
+// (RoPE part, exact power-of-two scaling); qinv = 2^-s.  One warp per row.
+__global__ void __launch_bounds__(256) wide_q_prep_kernel(const __nv_bfloat16* __restrict__ q, uint16_t* __restrict__ q16,
+                                                         float* __restrict__ qinv, int64_t rows) {
+  const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const uint4* src = reinterpret_cast<const uint4*>(q + row * kDqk);  // 72 chunks of 8 values
+  uint4 v[3];
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 3; ++i) {
+    const int ch = lane + 32 * i;
+    v[i] = ch < 72 ? __ldg(src + ch) : make_uint4(0, 0, 0, 0);
+    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[k] << 16)), fabsf(__uint_as_float(w[k] & 0xFFFF0000u))));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, o));
+  int sh = 0;
+  if (amax > 0.f) {
+    int ex;
+    frexpf(32768.f / amax, &ex);  // 32768 / amax = m * 2^ex, m in [0.5, 1)
+    sh = ex - 1;
+  }
+  const float pre = ldexpf(1.f, sh);
+  uint4* dst = reinterpret_cast<uint4*>(q16 + row * kDqk);
+#pragma unroll
+  for (int i = 0; i < 3; ++i) {
+    const int ch = lane + 32 * i;
+    if (ch >= 72) continue;
+    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+    uint32_t o[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float lo = __uint_as_float(w[k] << 16) * pre, hi = __uint_as_float(w[k] & 0xFFFF0000u) * pre;
+      o[k] = ch < 64 ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi);
+    }
+    dst[ch] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+  if (lane == 0) qinv[row] = ldexpf(1.f, -sh);
+}
+
+// Workspace of the FP8 path beyond the partial results: the prepared Q and
+// the heads' inverse prescales.
+size_t q_prep_bytes(int T) {
+  return (((size_t)T * kHeads * kDqk * 2 + 255) / 256) * 256 + (size_t)T * kHeads * 4;
+}
+
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -644,32 +832,38 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// kv [N, 576] bf16 and q [T * 128, 576] bf16, both as bytes.  The kv maps
-// gather single rows: one 128-byte value panel (128-byte swizzle) or one
-// 64-byte RoPE half (64-byte swizzle); the q maps load the same slices of
-// 128 consecutive head rows.
-cudaError_t make_maps(const void* kv, int64_t N, const void* q, int T, CUtensorMap* kv_map, CUtensorMap* kv_rope_map,
-                      CUtensorMap* q_map, CUtensorMap* q_rope_map) {
+// Tensor maps, all over bytes.  bf16 rows (kv [N, 576]): m0 gathers one
+// 128-byte value panel of single rows (128-byte swizzle), m2 one 64-byte RoPE
+// half (64-byte swizzle).  FP8 rows (the [NB * 64, 656] cache): m0 gathers
+// 128 bytes of codes, m1 the 16 scale bytes (unswizzled, into staging), m2
+// the 64-byte RoPE half (64-byte swizzle).  q [T * 128, 576] bf16: the same
+// slices of 128 consecutive head rows.
+template <bool kFp8>
+cudaError_t make_maps(const void* rows, int64_t n_rows, const void* q, int T, CUtensorMap* m0, CUtensorMap* m1,
+                      CUtensorMap* m2, CUtensorMap* q_map, CUtensorMap* q_rope_map) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
-  const cuuint64_t gstride[1] = {(cuuint64_t)kRowBytesBf16};
+  const cuuint64_t row_bytes = kFp8 ? (cuuint64_t)kRowBytes : (cuuint64_t)kRowBytesBf16;
+  const cuuint64_t rstride[1] = {row_bytes}, qstride[1] = {(cuuint64_t)kRowBytesBf16};
   const cuuint32_t es[2] = {1, 1};
-  const cuuint64_t kv_dim[2] = {(cuuint64_t)kRowBytesBf16, (cuuint64_t)N};
+  const cuuint64_t r_dim[2] = {row_bytes, (cuuint64_t)n_rows};
   const cuuint64_t q_dim[2] = {(cuuint64_t)kRowBytesBf16, (cuuint64_t)T * kHeads};
   struct Spec {
     CUtensorMap* map;
     const void* base;
     const cuuint64_t* dim;
+    const cuuint64_t* stride;
     cuuint32_t box0, box1;
     CUtensorMapSwizzle sw;
-  } specs[4] = {{kv_map, kv, kv_dim, 128, 1, CU_TENSOR_MAP_SWIZZLE_128B},
-                {kv_rope_map, kv, kv_dim, 64, 1, CU_TENSOR_MAP_SWIZZLE_64B},
-                {q_map, q, q_dim, 128, kHeads, CU_TENSOR_MAP_SWIZZLE_128B},
-                {q_rope_map, q, q_dim, 64, kHeads, CU_TENSOR_MAP_SWIZZLE_64B}};
+  } specs[5] = {{m0, rows, r_dim, rstride, 128, 1, kFp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B},
+                {m1, rows, r_dim, rstride, kFp8 ? 16u : 128u, 1, kFp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B},
+                {m2, rows, r_dim, rstride, 64, 1, CU_TENSOR_MAP_SWIZZLE_64B},
+                {q_map, q, q_dim, qstride, 128, kHeads, CU_TENSOR_MAP_SWIZZLE_128B},
+                {q_rope_map, q, q_dim, qstride, 64, kHeads, CU_TENSOR_MAP_SWIZZLE_64B}};
   for (const Spec& sp : specs) {
     const cuuint32_t box[2] = {sp.box0, sp.box1};
-    const CUresult r = enc(sp.map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(sp.base), sp.dim, gstride, box,
-                           es, CU_TENSOR_MAP_INTERLEAVE_NONE, sp.sw, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+    const CUresult r = enc(sp.map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(sp.base), sp.dim, sp.stride,
+                           box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sp.sw, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   }
@@ -677,19 +871,20 @@ cudaError_t make_maps(const void* kv, int64_t N, const void* q, int T, CUtensorM
 }
 
 // Pairs that can be resident at once (one CTA per SM), looked up once per device.
+template <bool kFp8>
 int resident_pairs(int num_sms) {
   static int cached[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return num_sms / 2;
   if (cached[dev] > 0) return cached[dev];
   int n = 0;
-  if (cudaFuncSetAttribute(sparse_mla_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc) ==
-      cudaSuccess) {
+  if (cudaFuncSetAttribute(sparse_mla_wide_kernel<kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Lay<kFp8>::kSmemAlloc) == cudaSuccess) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * (unsigned)(num_sms / 2), 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = kSmemAlloc;
-    if (cudaOccupancyMaxActiveClusters(&n, (void*)sparse_mla_wide_kernel, &cfg) != cudaSuccess) n = 0;
+    cfg.dynamicSmemBytes = Lay<kFp8>::kSmemAlloc;
+    if (cudaOccupancyMaxActiveClusters(&n, (void*)sparse_mla_wide_kernel<kFp8>, &cfg) != cudaSuccess) n = 0;
   }
   (void)cudaGetLastError();
   if (n <= 0) n = num_sms / 2;
@@ -697,24 +892,15 @@ int resident_pairs(int num_sms) {
   return n;
 }
 
-}  // namespace
-
-#ifdef SMLA_TRACE
-extern "C" int smla_trace_set_wide(long long* buf) {
-  return (int)cudaMemcpyToSymbol(g_smla_trace_wide, &buf, sizeof(buf));
-}
-#endif
-
-bool wide_prefill_supported(int H) { return H == kHeads; }
-
-AttnPlan plan_prefill_wide(int T, int K, int num_splits, int num_sms) {
+AttnPlan plan_wide(bool fp8, int T, int K, int num_splits, int num_sms) {
   AttnPlan pl;
   pl.HG = kHeads;
   pl.n_hg = 1;
   pl.nt = K > 0 ? (K + kRows - 1) / kRows : 1;
   pl.units = T;
   pl.total = pl.units * pl.nt;
-  int64_t G = num_splits > 0 ? pl.units * (int64_t)num_splits : (int64_t)resident_pairs(num_sms);
+  const int pairs = fp8 ? resident_pairs<true>(num_sms) : resident_pairs<false>(num_sms);
+  int64_t G = num_splits > 0 ? pl.units * (int64_t)num_splits : (int64_t)pairs;
   if (G > pl.total) G = pl.total;
   if (G < 1) G = 1;
   pl.G = (int)G;
@@ -722,13 +908,19 @@ AttnPlan plan_prefill_wide(int T, int K, int num_splits, int num_sms) {
   const int64_t n_slots = (int64_t)pl.G + pl.units - 1;
   const size_t lse_bytes = (size_t)(((n_slots * kHeads * 4) + 255) / 256) * 256;
   pl.ws_bytes = kWsStatusBytes + lse_bytes + (size_t)n_slots * kHeads * kDv * 4;
+  if (fp8) pl.ws_bytes += q_prep_bytes(T);
   return pl;
 }
 
-cudaError_t launch_prefill_wide(const AttnArgs& a, const AttnPlan& plan, cudaStream_t stream) {
+template <bool kFp8>
+cudaError_t launch_wide(const AttnArgs& a, const AttnPlan& plan, cudaStream_t stream) {
   Params p{};
   p.q = static_cast<const __nv_bfloat16*>(a.q);
   p.indices = a.indices;
+  p.block_table = a.block_table;
+  p.req_id = a.req_id;
+  p.R = a.R;
+  p.MB = a.MB;
   p.out = static_cast<__nv_bfloat16*>(a.out);
   p.lse = a.lse;
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
@@ -744,17 +936,58 @@ cudaError_t launch_prefill_wide(const AttnArgs& a, const AttnPlan& plan, cudaStr
   p.nt = plan.nt;
   p.total = plan.total;
   p.G = plan.G;
-  CUtensorMap kv_map, kv_rope_map, q_map, q_rope_map;
-  cudaError_t e = make_maps(a.kv, a.NB, a.q, a.T, &kv_map, &kv_rope_map, &q_map, &q_rope_map);
+  const void* qsrc = a.q;
+  if (kFp8) {
+    // prepared Q after the partial results (256-byte aligned)
+    uint8_t* qp = ws + kWsStatusBytes + lse_bytes + (size_t)n_slots * kHeads * kDv * 4;
+    uint16_t* q16 = reinterpret_cast<uint16_t*>(qp);
+    float* qinv = reinterpret_cast<float*>(qp + (((size_t)a.T * kHeads * kDqk * 2 + 255) / 256) * 256);
+    const int64_t rows = (int64_t)a.T * kHeads;
+    wide_q_prep_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(a.q), q16,
+                                                                     qinv, rows);
+    cudaError_t e0 = cudaGetLastError();
+    if (e0 != cudaSuccess) return e0;
+    p.qinv = qinv;
+    qsrc = q16;
+  }
+  CUtensorMap m0, m1, m2, q_map, q_rope_map;
+  const void* rows = kFp8 ? static_cast<const void*>(a.cache) : a.kv;
+  const int64_t n_rows = kFp8 ? a.NB * kBlock : a.NB;
+  cudaError_t e = make_maps<kFp8>(rows, n_rows, qsrc, a.T, &m0, &m1, &m2, &q_map, &q_rope_map);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(sparse_mla_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+  e = cudaFuncSetAttribute(sparse_mla_wide_kernel<kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Lay<kFp8>::kSmemAlloc);
   if (e != cudaSuccess) return e;
-  sparse_mla_wide_kernel<<<2 * plan.G, kThreads, kSmemAlloc, stream>>>(p, kv_map, kv_rope_map, q_map, q_rope_map);
+  sparse_mla_wide_kernel<kFp8><<<2 * plan.G, kThreads, Lay<kFp8>::kSmemAlloc, stream>>>(p, m0, m1, m2, q_map,
+                                                                                         q_rope_map);
   e = cudaGetLastError();
   if (e != cudaSuccess || !plan.need_combine) return e;
   combine_kernel<kHeads><<<(unsigned)(plan.units * combine_split<kHeads>()), combine_threads<kHeads>(), 0, stream>>>(
       p.part_o, p.part_lse, p.out, p.lse, kHeads, 1, p.nt, p.total, p.G);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+#ifdef SMLA_TRACE
+extern "C" int smla_trace_set_wide(long long* buf) {
+  return (int)cudaMemcpyToSymbol(g_smla_trace_wide, &buf, sizeof(buf));
+}
+#endif
+
+bool wide_supported(int H) { return H == kHeads; }
+
+AttnPlan plan_prefill_wide(int T, int K, int num_splits, int num_sms) {
+  return plan_wide(false, T, K, num_splits, num_sms);
+}
+AttnPlan plan_decode_wide(int T, int K, int num_splits, int num_sms) {
+  return plan_wide(true, T, K, num_splits, num_sms);
+}
+cudaError_t launch_prefill_wide(const AttnArgs& a, const AttnPlan& plan, cudaStream_t stream) {
+  return launch_wide<false>(a, plan, stream);
+}
+cudaError_t launch_decode_wide(const AttnArgs& a, const AttnPlan& plan, cudaStream_t stream) {
+  return launch_wide<true>(a, plan, stream);
 }
 
 }  // namespace smla

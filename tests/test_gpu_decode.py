@@ -22,10 +22,11 @@ def test_tiny_decode_h16_k64():
     check_decode(inp.tiny_decode(0))
 
 
+@pytest.mark.parametrize("H", [16, 128])
 @pytest.mark.parametrize("num_splits", [0, 1, 2, 3, 5])
-def test_ragged_topk_several_tiles(num_splits):
-    # K = 200: three full tiles of 64 rows and a ragged tail of 8
-    case = inp.memory_bound_decode(seed=5, R=9, ctx_lo=300, ctx_hi=2500, K=200)
+def test_ragged_topk_several_tiles(num_splits, H):
+    # K = 200: three full tiles of 64 rows and a ragged tail of 8 (H = 128 runs the CTA-pair kernel)
+    case = inp.memory_bound_decode(seed=5, R=9, ctx_lo=300, ctx_hi=2500, K=200, H=H)
     check_decode(case, num_splits=num_splits)
 
 
@@ -36,14 +37,16 @@ def test_head_counts(H):
     check_decode(case, num_splits=1)
 
 
+@pytest.mark.parametrize("H", [16, 128])
 @pytest.mark.parametrize("K", [1, 37, 64, 65, 2048])
-def test_topk_widths(K):
-    case = inp.memory_bound_decode(seed=7, R=6, ctx_lo=2100, ctx_hi=4000, K=K)
+def test_topk_widths(K, H):
+    case = inp.memory_bound_decode(seed=7, R=6, ctx_lo=2100, ctx_hi=4000, K=K, H=H)
     check_decode(case)
 
 
-def test_all_indices_invalid_gives_zero_and_minus_inf():
-    case = inp.memory_bound_decode(seed=8, R=4, ctx_lo=200, ctx_hi=400, K=130)
+@pytest.mark.parametrize("H", [16, 128])
+def test_all_indices_invalid_gives_zero_and_minus_inf(H):
+    case = inp.memory_bound_decode(seed=8, R=4, ctx_lo=200, ctx_hi=400, K=130, H=H)
     case.indices[:] = -1
     out, lse = run_gpu_decode(case, oracle_cache(case))
     assert np.all(out == 0) and np.all(np.isneginf(lse))
@@ -52,8 +55,9 @@ def test_all_indices_invalid_gives_zero_and_minus_inf():
     check_decode(case, num_splits=2)
 
 
-def test_single_valid_index_returns_its_row():
-    case = inp.memory_bound_decode(seed=9, R=6, ctx_lo=300, ctx_hi=500, K=96)
+@pytest.mark.parametrize("H", [16, 128])
+def test_single_valid_index_returns_its_row(H):
+    case = inp.memory_bound_decode(seed=9, R=6, ctx_lo=300, ctx_hi=500, K=96, H=H)
     rng = np.random.default_rng(0)
     keep = rng.integers(0, 96, size=6)
     for t in range(6):
@@ -63,8 +67,9 @@ def test_single_valid_index_returns_its_row():
     check_decode(case)
 
 
-def test_duplicated_and_out_of_range_indices():
-    case = inp.memory_bound_decode(seed=10, R=5, ctx_lo=700, ctx_hi=900, K=180)
+@pytest.mark.parametrize("H", [16, 128])
+def test_duplicated_and_out_of_range_indices(H):
+    case = inp.memory_bound_decode(seed=10, R=5, ctx_lo=700, ctx_hi=900, K=180, H=H)
     case.indices[:, 100:140] = case.indices[:, 0:40]          # duplicates count once per occurrence
     case.indices[0, 5] = case.block_table.shape[1] * 64 + 3    # block id >= MB
     case.indices[1, 7] = -77
