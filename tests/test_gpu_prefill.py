@@ -63,8 +63,12 @@ def test_attention_plan_matches_the_launch_shape(fp8, H):
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     launches, ctas = smla.attention_plan(fp8, 4096, H, 2048, 0)
     assert launches in (1, 2, 3) and 1 <= ctas <= sms
-    if not fp8 and H == 128:
-        assert ctas % 2 == 0  # CTA pairs
-    # one unit per CTA range never needs the combine
+    if H == 128:
+        assert ctas % 2 == 0  # 128 heads run CTA pairs
+    # num_splits = 1: one CTA (pair) per unit, so no combine; units are tokens
+    # at 128 heads, (token, 16- or 32-head group) pairs otherwise
     launches1, ctas1 = smla.attention_plan(fp8, 3, H, 2048, 1)
-    assert launches1 == (2 if fp8 and H == 128 else 1) and ctas1 == (3 * (H // (128 if not fp8 and H == 128 else (32 if not fp8 and H % 32 == 0 else 16)))) * (2 if not fp8 and H == 128 else 1)
+    heads_per_unit = 128 if H == 128 else (32 if not fp8 and H % 32 == 0 else 16)
+    units = 3 * (H // heads_per_unit)
+    assert ctas1 == units * (2 if H == 128 else 1)
+    assert launches1 == (2 if fp8 and H == 128 else 1)  # + the Q preparation of the 128-head FP8 path
