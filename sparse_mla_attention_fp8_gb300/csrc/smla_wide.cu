@@ -123,7 +123,7 @@ constexpr int kThreads = 32 * kNumWarps;
 // (set by the host through smla_trace_set_wide).  Compiled out otherwise.
 #ifdef SMLA_TRACE
 __device__ long long* g_smla_trace_wide = nullptr;
-constexpr int kTraceTiles = 64, kTraceEvents = 12;
+constexpr int kTraceTiles = 64, kTraceEvents = 14;
 #define WIDE_TRACE(tl, ev)                                                                                   \
   do {                                                                                                       \
     if (g_smla_trace_wide && (tl) < kTraceTiles)                                                           \
@@ -133,7 +133,7 @@ constexpr int kTraceTiles = 64, kTraceEvents = 12;
 #define WIDE_TRACE(tl, ev) ((void)0)
 #endif
 enum { kEvSFull = 0, kEvSLoaded, kEvXFree, kEvSent, kEvXFull, kEvPReady, kEvPFull, kEvQk, kEvPv, kEvIssue, kEvQkSeen,
-       kEvKEmpty };
+       kEvKEmpty, kEvConverted, kEvRawFull };
 
 struct Params {
   const __nv_bfloat16* q;  // [T, 128, 576]
@@ -288,9 +288,10 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
     // 4 lw + 3).  Two tiles ahead it gathers their codes (the CTA's two scale
     // groups) and scales into a staging slot, lane 3 g + b issuing copy b of
     // group g; when an operand tile is free it gathers the RoPE half straight
-    // into it (bf16 in the row) and converts the staged codes to f16 (code x
-    // scale, exact e4m3 widening then one rounding to 11 bits), lane l
-    // handling codes 8 l .. 8 l + 7 of each row.
+    // into it (bf16 in the row) and converts the staged codes to f16: the
+    // exact e4m3 widening times the scale rounded to f16, one f16 product
+    // (relative error below 2^-11), lane l handling codes 8 l .. 8 l + 7 of
+    // each row.
     const int lw = warp - kLoadWarp0;
     uint8_t* raw_base = smem + L::kOffRaw;
     const int rgrp = lane / 3, rbox = lane - 3 * rgrp;
@@ -328,12 +329,48 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[L::kBarIdxEmpty + b4]);
       if (!SMLA_WAIT(L::kBarRawFull + 2 * lw + sl, (tl >> 1) & 1)) break;
+      if (lane == 0 && lw == 0) WIDE_TRACE(tl, kEvRawFull);
       if (use >= 1 && !SMLA_WAIT(L::kBarKEmpty + kb, (use + 1) & 1)) break;
       if (lane == 0 && lw == 0) WIDE_TRACE(tl, kEvKEmpty);
       if (lane < 16) valid[kb * kRows + 16 * lw + lane] = (uint8_t)((vmask >> lane) & 1u);
       const uint32_t tile = smem_u32(smem + L::kOffK + kb * kKBuf);
+      const uint8_t* raw = raw_base + sl * kRawBuf;
+      const int half = lane >> 4, pnl = lane >> 3, ch = lane & 7;
+      // 4 rows at a time: all their loads first, so that one load latency
+      // covers 4 rows (the stores are ordered after them)
+#pragma unroll 1
+      for (int rb = 0; rb < 16; rb += 4) {
+        uint2 cw[4];
+        float sc[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int r = 16 * lw + rb + i;
+          const uint8_t* grp = raw + (r >> 2) * kRawGroup;
+          cw[i] = *reinterpret_cast<const uint2*>(grp + 512 * half + (r & 3) * 128 + 8 * (lane & 15));
+          sc[i] = *reinterpret_cast<const float*>(grp + 1024 + (r & 3) * 16 + 4 * (2 * c + half));
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int r = 16 * lw + rb + i;
+          const uint32_t sc2 = pack_f16x2(sc[i], sc[i]);
+          uint32_t o[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const uint16_t pr = (uint16_t)(((k < 2 ? cw[i].x : cw[i].y) >> (16 * (k & 1))) & 0xFFFFu);
+            uint32_t h2;
+            asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(pr));  // exact
+            asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(o[k]) : "r"(h2), "r"(sc2));
+          }
+          st_shared_v4(tile + pnl * kPanel + (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((ch ^ (r & 7)) << 4)), o[0],
+                       o[1], o[2], o[3]);
+        }
+      }
+      if (lane == 0 && lw == 0) WIDE_TRACE(tl, kEvConverted);
+      fence_proxy_async_smem();
+      __syncwarp();
       // the tile's full barrier: this warp's RoPE bytes (registered before the
-      // copies), then its arrival once its rows are converted
+      // copies, which go after the conversion so that a busy TMA unit does not
+      // hold it up), then its arrival for the converted rows
       if (lane == 0) mbar_expect_tx(&bars[L::kBarKFull + kb], (uint32_t)(16 * 64));
       __syncwarp();
       if (lane < 4) {
@@ -341,27 +378,6 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
         tma_gather4_2d(tile + 4 * kPanel + (uint32_t)((r_g >> 3) * 512 + (r_g & 7) * 64), &m2, kRopeOff + 64 * c, g0,
                        g1, g2, g3, &bars[L::kBarKFull + kb]);
       }
-      const uint8_t* raw = raw_base + sl * kRawBuf;
-      const int half = lane >> 4, pnl = lane >> 3, ch = lane & 7;
-#pragma unroll 4
-      for (int rr = 0; rr < 16; ++rr) {
-        const int r = 16 * lw + rr;
-        const uint8_t* grp = raw + (r >> 2) * kRawGroup;
-        const uint2 cw = *reinterpret_cast<const uint2*>(grp + 512 * half + (r & 3) * 128 + 8 * (lane & 15));
-        const float sc = *reinterpret_cast<const float*>(grp + 1024 + (r & 3) * 16 + 4 * (2 * c + half));
-        uint32_t o[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint16_t pr = (uint16_t)(((k < 2 ? cw.x : cw.y) >> (16 * (k & 1))) & 0xFFFFu);
-          uint32_t h2;
-          asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(pr));
-          const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
-          o[k] = pack_f16x2(f.x * sc, f.y * sc);
-        }
-        st_shared_v4(tile + pnl * kPanel + (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((ch ^ (r & 7)) << 4)), o[0],
-                     o[1], o[2], o[3]);
-      }
-      fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[L::kBarKFull + kb]);
       if (lane == 0 && lw == 0) WIDE_TRACE(tl, kEvIssue);
