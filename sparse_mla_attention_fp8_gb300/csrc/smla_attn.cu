@@ -769,8 +769,11 @@ cudaError_t launch_impl(const AttnArgs& a, const AttnPlan& plan, cudaStream_t st
   sparse_mla_attn_kernel<HG, kFp8><<<plan.G, C::kThreads, C::kSmemAlloc, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || !plan.need_combine) return e;
-  combine_kernel<HG><<<(unsigned)(plan.units * combine_split<HG>()), combine_threads<HG>(), 0, stream>>>(p.part_o, p.part_lse, p.out, p.lse, p.H, p.n_hg, p.nt,
-                                                               p.total, p.G);
+  unsigned cblocks;
+  int by_boundary;
+  combine_grid<HG>(plan.units, plan.G, &cblocks, &by_boundary);
+  combine_kernel<HG><<<cblocks, combine_threads<HG>(), 0, stream>>>(p.part_o, p.part_lse, p.out, p.lse, p.H, p.n_hg,
+                                                                  p.nt, p.total, p.G, by_boundary);
   return cudaGetLastError();
 }
 

@@ -36,8 +36,11 @@ constexpr int kCombineChunk = 8;  // parts per round: their loads are in flight 
 // LSE-weighted merge of the partial results of units split across CTAs:
 //   M = max_s lse_s,  w_s = exp(lse_s - M) / sum_s' exp(lse_s' - M),
 //   out = sum_s w_s * O_s,  lse = M + log(sum_s exp(lse_s - M)).
-// Grid: units x combine_split<HG>() blocks of combine_threads<HG>() = HG x
-// (128 / combine_split<HG>()) threads.  Each thread first issues the loads of its
+// Grid: combine_split<HG>() blocks of combine_threads<HG>() = HG x
+// (128 / combine_split<HG>()) threads per unit (by_boundary = 0), or per
+// boundary between consecutive CTA ranges (by_boundary = 1: the unit the
+// boundary cuts, merged by the first boundary inside it; for many units over
+// few CTAs).  combine_grid() picks the smaller.  Each thread first issues the loads of its
 // partial-O chunk for kCombineChunk parts, then reads the parts' LSEs (from
 // L2 or L1, shared by the block), so that one round trip covers both; parts
 // beyond the first round are merged with a running max and sum.
@@ -46,10 +49,19 @@ __global__ void __launch_bounds__(combine_threads<HG>()) combine_kernel(const fl
                                                                   const float* __restrict__ part_lse,
                                                                   __nv_bfloat16* __restrict__ out,
                                                                   float* __restrict__ lse, int H, int n_hg, int nt,
-                                                                  int64_t total, int G) {
+                                                                  int64_t total, int G, int by_boundary) {
   constexpr int kSplit = combine_split<HG>();
   constexpr int kChunks = 128 / kSplit;  // float4 column chunks per block and head
-  const int64_t u = blockIdx.x / kSplit;
+  int64_t u;
+  if (by_boundary) {
+    const int64_t c = blockIdx.x / kSplit + 1;  // boundary between CTA ranges c - 1 and c
+    const int64_t b = tile_begin(c, total, G);
+    if (b % nt == 0) return;                                   // no unit is cut here
+    u = b / nt;
+    if (tile_begin(c - 1, total, G) > u * nt) return;          // an earlier boundary cuts this unit
+  } else {
+    u = blockIdx.x / kSplit;
+  }
   const int part = blockIdx.x % kSplit;
   const int64_t c_lo = tile_owner(u * nt, total, G), c_hi = tile_owner(u * nt + nt - 1, total, G);
   if (c_lo == c_hi) return;  // finished inside one CTA, already written
@@ -96,6 +108,15 @@ __global__ void __launch_bounds__(combine_threads<HG>()) combine_kernel(const fl
   d[0] = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
   d[1] = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
   if (part == 0 && j == 0) lse[(int64_t)t * H + hg * HG + h] = ssum > 0.f ? m + logf(ssum) : -INFINITY;
+}
+
+// Blocks and mode of combine_kernel for a split of `units` units over G CTA
+// ranges.
+template <int HG>
+inline void combine_grid(int64_t units, int G, unsigned* blocks, int* by_boundary) {
+  const int64_t boundaries = G > 1 ? G - 1 : 1;
+  *by_boundary = boundaries < units ? 1 : 0;
+  *blocks = (unsigned)((*by_boundary ? boundaries : units) * combine_split<HG>());
 }
 
 }  // namespace smla

@@ -1027,8 +1027,11 @@ cudaError_t launch_decode_fp8(const AttnArgs& a, const AttnPlan& plan, cudaStrea
   sparse_mla_decode_fp8_kernel<<<plan.G, kThreads, kSmemAlloc, stream>>>(p, panel_map, scale_map);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || !plan.need_combine) return e;
-  combine_kernel<HG><<<(unsigned)(plan.units * combine_split<HG>()), combine_threads<HG>(), 0, stream>>>(p.part_o, p.part_lse, p.out, p.lse, p.H, p.n_hg, p.nt,
-                                                               p.total, p.G);
+  unsigned cblocks;
+  int by_boundary;
+  combine_grid<HG>(plan.units, plan.G, &cblocks, &by_boundary);
+  combine_kernel<HG><<<cblocks, combine_threads<HG>(), 0, stream>>>(p.part_o, p.part_lse, p.out, p.lse, p.H, p.n_hg,
+                                                                  p.nt, p.total, p.G, by_boundary);
   return cudaGetLastError();
 }
 

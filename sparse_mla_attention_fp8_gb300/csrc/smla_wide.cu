@@ -978,8 +978,11 @@ cudaError_t launch_wide(const AttnArgs& a, const AttnPlan& plan, cudaStream_t st
                                                                                          q_rope_map);
   e = cudaGetLastError();
   if (e != cudaSuccess || !plan.need_combine) return e;
-  combine_kernel<kHeads><<<(unsigned)(plan.units * combine_split<kHeads>()), combine_threads<kHeads>(), 0, stream>>>(
-      p.part_o, p.part_lse, p.out, p.lse, kHeads, 1, p.nt, p.total, p.G);
+  unsigned cblocks;
+  int by_boundary;
+  combine_grid<kHeads>(plan.units, plan.G, &cblocks, &by_boundary);
+  combine_kernel<kHeads><<<cblocks, combine_threads<kHeads>(), 0, stream>>>(p.part_o, p.part_lse, p.out, p.lse, kHeads,
+                                                                           1, p.nt, p.total, p.G, by_boundary);
   return cudaGetLastError();
 }
 
