@@ -226,6 +226,7 @@ template <int HG, bool kFp8>
 __global__ void __launch_bounds__(Cfg<HG, kFp8>::kThreads, 1) sparse_mla_attn_kernel(const __grid_constant__ Params p) {
   using C = Cfg<HG, kFp8>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
+  grid_launch_dependents();  // the combine may be launched behind this grid right away
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
@@ -769,11 +770,8 @@ cudaError_t launch_impl(const AttnArgs& a, const AttnPlan& plan, cudaStream_t st
   sparse_mla_attn_kernel<HG, kFp8><<<plan.G, C::kThreads, C::kSmemAlloc, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || !plan.need_combine) return e;
-  unsigned cblocks;
-  int by_boundary;
-  combine_grid<HG>(plan.units, plan.G, &cblocks, &by_boundary);
-  combine_kernel<HG><<<cblocks, combine_threads<HG>(), 0, stream>>>(p.part_o, p.part_lse, p.out, p.lse, p.H, p.n_hg,
-                                                                  p.nt, p.total, p.G, by_boundary);
+  e = launch_combine<HG>(p.part_o, p.part_lse, p.out, p.lse, p.H, p.n_hg, p.nt, p.total, p.G, plan.units, stream);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -4,6 +4,7 @@
 #include <cstdint>
 #include <cuda_bf16.h>
 
+#include "sm103_ptx.cuh"
 #include "smla_common.cuh"
 
 namespace smla {
@@ -52,6 +53,7 @@ __global__ void __launch_bounds__(combine_threads<HG>()) combine_kernel(const fl
                                                                   int64_t total, int G, int by_boundary) {
   constexpr int kSplit = combine_split<HG>();
   constexpr int kChunks = 128 / kSplit;  // float4 column chunks per block and head
+  grid_dependency_wait();  // the attention kernel's partials (launched as its programmatic dependent)
   int64_t u;
   if (by_boundary) {
     const int64_t c = blockIdx.x / kSplit + 1;  // boundary between CTA ranges c - 1 and c
@@ -110,6 +112,13 @@ __global__ void __launch_bounds__(combine_threads<HG>()) combine_kernel(const fl
   if (part == 0 && j == 0) lse[(int64_t)t * H + hg * HG + h] = ssum > 0.f ? m + logf(ssum) : -INFINITY;
 }
 
+// Launches combine_kernel behind the attention kernel just issued on `stream`
+// as its programmatic dependent: its launch overlaps the attention kernel's
+// tail, and its first instruction waits for the partial results.
+template <int HG>
+inline cudaError_t launch_combine(const float* part_o, const float* part_lse, __nv_bfloat16* out, float* lse, int H,
+                                  int n_hg, int nt, int64_t total, int G, int64_t units, cudaStream_t stream);
+
 // Blocks and mode of combine_kernel for a split of `units` units over G CTA
 // ranges.
 template <int HG>
@@ -117,6 +126,25 @@ inline void combine_grid(int64_t units, int G, unsigned* blocks, int* by_boundar
   const int64_t boundaries = G > 1 ? G - 1 : 1;
   *by_boundary = boundaries < units ? 1 : 0;
   *blocks = (unsigned)((*by_boundary ? boundaries : units) * combine_split<HG>());
+}
+
+template <int HG>
+inline cudaError_t launch_combine(const float* part_o, const float* part_lse, __nv_bfloat16* out, float* lse, int H,
+                                  int n_hg, int nt, int64_t total, int G, int64_t units, cudaStream_t stream) {
+  unsigned blocks;
+  int by_boundary;
+  combine_grid<HG>(units, G, &blocks, &by_boundary);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(blocks, 1, 1);
+  cfg.blockDim = dim3(combine_threads<HG>(), 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, combine_kernel<HG>, part_o, part_lse, out, lse, H, n_hg, nt, total, G, by_boundary);
 }
 
 }  // namespace smla

@@ -280,6 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     sparse_mla_decode_fp8_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap panel_map,
                                  const __grid_constant__ CUtensorMap scale_map) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
+  grid_launch_dependents();  // the combine may be launched behind this grid right away
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
@@ -1027,11 +1028,8 @@ cudaError_t launch_decode_fp8(const AttnArgs& a, const AttnPlan& plan, cudaStrea
   sparse_mla_decode_fp8_kernel<<<plan.G, kThreads, kSmemAlloc, stream>>>(p, panel_map, scale_map);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || !plan.need_combine) return e;
-  unsigned cblocks;
-  int by_boundary;
-  combine_grid<HG>(plan.units, plan.G, &cblocks, &by_boundary);
-  combine_kernel<HG><<<cblocks, combine_threads<HG>(), 0, stream>>>(p.part_o, p.part_lse, p.out, p.lse, p.H, p.n_hg,
-                                                                  p.nt, p.total, p.G, by_boundary);
+  e = launch_combine<HG>(p.part_o, p.part_lse, p.out, p.lse, p.H, p.n_hg, p.nt, p.total, p.G, plan.units, stream);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

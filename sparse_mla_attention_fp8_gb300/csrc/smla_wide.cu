@@ -180,6 +180,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
                            const __grid_constant__ CUtensorMap q_map, const __grid_constant__ CUtensorMap q_rope_map) {
   using L = Lay<kFp8>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
+  grid_launch_dependents();  // the combine may be launched behind this grid right away
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kOffBar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kOffMisc);
@@ -978,11 +979,8 @@ cudaError_t launch_wide(const AttnArgs& a, const AttnPlan& plan, cudaStream_t st
                                                                                          q_rope_map);
   e = cudaGetLastError();
   if (e != cudaSuccess || !plan.need_combine) return e;
-  unsigned cblocks;
-  int by_boundary;
-  combine_grid<kHeads>(plan.units, plan.G, &cblocks, &by_boundary);
-  combine_kernel<kHeads><<<cblocks, combine_threads<kHeads>(), 0, stream>>>(p.part_o, p.part_lse, p.out, p.lse, kHeads,
-                                                                           1, p.nt, p.total, p.G, by_boundary);
+  e = launch_combine<kHeads>(p.part_o, p.part_lse, p.out, p.lse, kHeads, 1, p.nt, p.total, p.G, plan.units, stream);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
