@@ -31,11 +31,12 @@
 //     value panels of the same row tile (MN-major), N = 256.
 // Warp roles: 0..3 softmax, 4..7 and 8..11 exchange of tile rows 0..31 and
 // 32..63 (partial logits -> full, masked, log2-domain logits back in TMEM +
-// the maximum), 12 tensor-core issuer, 13 index translation + Q, 14..17 row
-// loaders (TMA tile::gather4 straight into swizzled K-major operand tiles).
+// the maximum), 12 QK^T issuer, 13 index translation + Q, 14..17 row loaders
+// (TMA tile::gather4 straight into swizzled K-major operand tiles), 18 P.V
+// issuer.
 // Warp w of the first three groups handles heads 32 (w % 4) .. + 31 (its
 // TMEM lane quarter), one per thread; the two halves' exchanges run side by
-// side and overlap the softmax of the previous tile.  18 warps: at most 5 per
+// side and overlap the softmax of the previous tile.  19 warps: at most 5 per
 // sub-partition, so 96 registers per thread.  Work: pairs take contiguous balanced ranges of the
 // token-major tile sequence; a token split over pairs goes through the
 // LSE-weighted combine.
@@ -96,8 +97,8 @@ struct Lay {
     kBarSFree = kBarSReady + kSBufs, kBarPFull = kBarSFree + kSBufs, kBarPDone = kBarPFull + 2,
     kBarXFull = kBarPDone + 2, kBarXFree = kBarXFull + 2, kBarIdxFull = kBarXFree + 2,
     kBarIdxEmpty = kBarIdxFull + 4, kBarQFull = kBarIdxEmpty + 4, kBarQEmpty = kBarQFull + 1,
-    kBarOFree = kBarQEmpty + 1, kBarDrain = kBarOFree + 1,
-    kBarRawFull = kBarDrain + 1,  // [loader][staging slot], FP8 rows only
+    kBarOFree = kBarQEmpty + 1, kBarDrain = kBarOFree + 1, kBarDrainPv = kBarDrain + 1,
+    kBarRawFull = kBarDrainPv + 1,  // [loader][staging slot], FP8 rows only
     kNumBars = kBarRawFull + 2 * kLoaders
   };
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort flag
@@ -115,7 +116,8 @@ constexpr int kPCol = 448;  // P: 2 buffers x 32 columns (bf16 pairs)
 constexpr int kTmemCols = 512;
 
 constexpr int kSoftWarps = 4, kXchgWarp0 = 4, kXchgWarps = 8, kMmaWarp = 12, kIndexWarp = 13, kLoadWarp0 = 14;
-constexpr int kNumWarps = kLoadWarp0 + kLoaders;
+constexpr int kPvWarp = kLoadWarp0 + kLoaders;  // issues P.V (kMmaWarp issues QK^T)
+constexpr int kNumWarps = kPvWarp + 1;
 constexpr int kThreads = 32 * kNumWarps;
 
 // Optional per-tile timeline for performance work: with SMLA_TRACE defined,
@@ -225,6 +227,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
     mbar_init(&bars[L::kBarQEmpty], 1);
     mbar_init(&bars[L::kBarOFree], 32 * kSoftWarps);
     mbar_init(&bars[L::kBarDrain], 1);
+    mbar_init(&bars[L::kBarDrainPv], 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -283,7 +286,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
     // no Q copy may still be landing in shared memory when the CTA exits
     if (seg > 0 && lane == 0) mbar_wait_drain(&bars[L::kBarQFull], (seg - 1) & 1);
     __syncwarp();
-  } else if (kFp8 && warp >= kLoadWarp0) {
+  } else if (kFp8 && warp >= kLoadWarp0 && warp < kPvWarp) {
     // ------------------------------------------------------------ FP8 row loaders + converters
     // Loader lw owns tile rows 16 lw .. 16 lw + 15 (staging groups 4 lw ..
     // 4 lw + 3).  Two tiles ahead it gathers their codes (the CTA's two scale
@@ -392,7 +395,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
     for (int t2 = converted; t2 < raw_issued; ++t2)
       if (lane == 0) mbar_wait_drain(&bars[L::kBarRawFull + 2 * lw + (t2 & 1)], (t2 >> 1) & 1);
     __syncwarp();
-  } else if (warp >= kLoadWarp0) {
+  } else if (warp >= kLoadWarp0 && warp < kPvWarp) {
     // ------------------------------------------------------------ row loaders
     // Loader lw gathers rows 16 lw .. 16 lw + 15 of every tile: 4 groups of 4
     // rows x 5 boxes (4 value panels, the RoPE half), lane 5 g + b issuing box
@@ -433,30 +436,71 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
     // no copy may still be landing in shared memory when the CTA exits
     if (last_b >= 0) mbar_wait_drain(&bars[L::kBarKFull + last_b], last_use & 1);
   } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------ tensor-core issuer
+    // ------------------------------------------------------------ QK^T issuer
+    // One thread: QK^T of each tile once its rows, the segment's Q and a free
+    // S buffer are there (P.V has its own issuer warp, so it never waits
+    // behind a QK^T).
     if (lane == 0 && n_local > 0) {
-      // FP8 rows: value panels, Q's value part and P in f16; RoPE parts in bf16
+      // FP8 rows: value panels and Q's value part in f16; RoPE parts in bf16
       constexpr uint32_t id_qk = kFp8 ? make_idesc_f16(128, kRows, 0, 0) : make_idesc_bf16(128, kRows, 0, 0);
       constexpr uint32_t id_qkr = make_idesc_bf16(128, kRows, 0, 0);
-      constexpr uint32_t id_pv = kFp8 ? make_idesc_f16(128, 256, 0, 1) : make_idesc_bf16(128, 256, 0, 1);
-      const uint32_t q0 = smem_u32(smem + L::kOffQ), k0 = smem_u32(smem + L::kOffK);  // 1024-byte aligned
-      int seg_q = 0, seg_o = 0, next_qk = 0, next_pv = 0;
-      const int kt0 = (int)(xbeg % p.nt);
-      int kt_qk = kt0, kt_pv = kt0;
-      uint64_t t_idle = 0;
-      uint32_t idle_polls = 0;
       // shared-memory descriptors: constant high words, low words = base + offset / 16
       constexpr uint32_t kHi128 = sdesc_hi(1024, kLayoutSw128), kHi64 = sdesc_hi(512, kLayoutSw64);
-      const uint32_t dq = sdesc_lo(q0, 16), dk0 = sdesc_lo(k0, 16), dv0 = sdesc_lo(k0, kPanel);
-      // P.V of tile next_pv once its P is written (and, first in a segment, O
-      // is free).  Tried before every QK^T panel too: its completion frees the
-      // row tile the loaders wait for, so it never waits out a whole QK^T.
-      auto try_pv = [&]() -> bool {
-        if (next_pv >= next_qk) return false;
-        const int tl = next_pv, kb = tl % L::kKBufs, pb = tl & 1;
-        const bool seg_start = tl == 0 || kt_pv == 0;
-        const bool o_ok = !seg_start || seg_o == 0 || mbar_test_wait(&bars[L::kBarOFree], (seg_o - 1) & 1);
-        if (!o_ok || !mbar_test_wait(&bars[L::kBarPFull + pb], (tl >> 1) & 1)) return false;
+      const uint32_t dq = sdesc_lo(smem_u32(smem + L::kOffQ), 16), dk0 = sdesc_lo(smem_u32(smem + L::kOffK), 16);
+      int seg = 0, kt = (int)(xbeg % p.nt), issued = 0;
+      for (int tl = 0; tl < n_local; ++tl) {
+        const int kb = tl % L::kKBufs, sb = tl % kSBufs;
+        const bool seg_start = tl == 0 || kt == 0;
+        const bool seg_end = tl == n_local - 1 || kt == p.nt - 1;
+        if (tl >= kSBufs && !SMLA_WAIT(L::kBarSFree + sb, ((tl / kSBufs) + 1) & 1)) break;
+        if (seg_start && !SMLA_WAIT(L::kBarQFull, seg & 1)) break;
+        if (!SMLA_WAIT(L::kBarKFull + kb, (tl / L::kKBufs) & 1)) break;
+        WIDE_TRACE(tl, kEvQkSeen);
+        tc_fence_after();
+        const uint32_t dk = dk0 + ((kb * kKBuf) >> 4);
+        const uint32_t sacc = tmem + kSCol + 64 * sb;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+#pragma unroll
+          for (int s = 0; s < 4; ++s)
+            mma_ss(sacc, sdesc_join<kHi128>(dq + ((b * kQPanel + 32 * s) >> 4)),
+                   sdesc_join<kHi128>(dk + ((b * kPanel + 32 * s) >> 4)), id_qk, (b | s) != 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int s = 0; s < 2; ++s)  // RoPE half: 8-row atoms of 64 bytes
+          mma_ss(sacc, sdesc_join<kHi64>(dq + ((4 * kQPanel + 32 * s) >> 4)),
+                 sdesc_join<kHi64>(dk + ((4 * kPanel + 32 * s) >> 4)), id_qkr, 1u);
+        mma_commit(&bars[L::kBarSFull + sb]);
+        if (seg_end) {
+          mma_commit(&bars[L::kBarQEmpty]);
+          ++seg;
+        }
+        WIDE_TRACE(tl, kEvQk);
+        ++issued;
+        kt = kt + 1 == p.nt ? 0 : kt + 1;
+      }
+      // every issued tensor-core operation completes before tensor memory is released
+      if (issued > 0) {
+        mma_commit(&bars[L::kBarDrain]);
+        mbar_wait_drain(&bars[L::kBarDrain], 0);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kPvWarp) {
+    // ------------------------------------------------------------ P.V issuer
+    // One thread: O_c += P V of each tile once its P is written (and, first in
+    // a segment, the previous segment's epilogue has read O).  Its completion
+    // frees the row tile and the P buffer.
+    if (lane == 0 && n_local > 0) {
+      constexpr uint32_t id_pv = kFp8 ? make_idesc_f16(128, 256, 0, 1) : make_idesc_bf16(128, 256, 0, 1);
+      constexpr uint32_t kHi128 = sdesc_hi(1024, kLayoutSw128);
+      const uint32_t dv0 = sdesc_lo(smem_u32(smem + L::kOffK), kPanel);
+      int seg_o = 0, kt = (int)(xbeg % p.nt), issued = 0;
+      for (int tl = 0; tl < n_local; ++tl) {
+        const int kb = tl % L::kKBufs, pb = tl & 1;
+        const bool seg_start = tl == 0 || kt == 0;
+        if (seg_start && seg_o > 0 && !SMLA_WAIT(L::kBarOFree, (seg_o - 1) & 1)) break;
+        if (!SMLA_WAIT(L::kBarPFull + pb, (tl >> 1) & 1)) break;
         if (seg_start) ++seg_o;
         tc_fence_after();
         const uint32_t dv = dv0 + ((kb * kKBuf) >> 4);
@@ -469,65 +513,12 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
         mma_commit(&bars[L::kBarKEmpty + kb]);
         mma_commit(&bars[L::kBarPDone + pb]);
         WIDE_TRACE(tl, kEvPv);
-        ++next_pv;
-        kt_pv = kt_pv + 1 == p.nt ? 0 : kt_pv + 1;
-        return true;
-      };
-      while (next_pv < n_local) {
-        bool progressed = try_pv();
-        // QK^T of tile next_qk: its rows, the segment's Q and a free S buffer
-        if (next_qk < n_local) {
-          const int tl = next_qk, kb = tl % L::kKBufs, sb = tl % kSBufs;
-          const bool seg_start = tl == 0 || kt_qk == 0;
-          const bool seg_end = tl == n_local - 1 || kt_qk == p.nt - 1;
-          const int seg = seg_start ? seg_q : seg_q - 1;
-          const bool s_ok = tl < kSBufs || mbar_test_wait(&bars[L::kBarSFree + sb], ((tl / kSBufs) + 1) & 1);
-          const bool q_ok = !seg_start || mbar_test_wait(&bars[L::kBarQFull], seg & 1);
-          if (s_ok && q_ok && mbar_test_wait(&bars[L::kBarKFull + kb], (tl / L::kKBufs) & 1)) {
-            if (seg_start) ++seg_q;
-            WIDE_TRACE(tl, kEvQkSeen);
-            tc_fence_after();
-            const uint32_t dk = dk0 + ((kb * kKBuf) >> 4);
-            const uint32_t sacc = tmem + kSCol + 64 * sb;
-#pragma unroll
-            for (int b = 0; b < 4; ++b) {
-#pragma unroll
-              for (int s = 0; s < 4; ++s)
-                mma_ss(sacc, sdesc_join<kHi128>(dq + ((b * kQPanel + 32 * s) >> 4)),
-                       sdesc_join<kHi128>(dk + ((b * kPanel + 32 * s) >> 4)), id_qk, (b | s) != 0 ? 1u : 0u);
-              try_pv();
-            }
-#pragma unroll
-            for (int s = 0; s < 2; ++s)  // RoPE half: 8-row atoms of 64 bytes
-              mma_ss(sacc, sdesc_join<kHi64>(dq + ((4 * kQPanel + 32 * s) >> 4)),
-                     sdesc_join<kHi64>(dk + ((4 * kPanel + 32 * s) >> 4)), id_qkr, 1u);
-            mma_commit(&bars[L::kBarSFull + sb]);
-            if (seg_end) mma_commit(&bars[L::kBarQEmpty]);
-            WIDE_TRACE(tl, kEvQk);
-            ++next_qk;
-            kt_qk = kt_qk + 1 == p.nt ? 0 : kt_qk + 1;
-            progressed = true;
-          }
-        }
-        if (progressed) {
-          t_idle = 0;
-          idle_polls = 0;
-        } else if ((++idle_polls & 255u) == 0u) {
-          if (*abort_flag) break;
-          const uint64_t now = globaltimer_ns();
-          if (t_idle == 0) {
-            t_idle = now;
-          } else if (now - t_idle > kWaitLimitNs) {
-            *abort_flag = 1;
-            atomicCAS(p.status, 0, kDevWaitTimeout);
-            break;
-          }
-        }
+        ++issued;
+        kt = kt + 1 == p.nt ? 0 : kt + 1;
       }
-      // every issued tensor-core operation completes before tensor memory is released
-      if (next_qk > 0) {
-        mma_commit(&bars[L::kBarDrain]);
-        mbar_wait_drain(&bars[L::kBarDrain], 0);
+      if (issued > 0) {
+        mma_commit(&bars[L::kBarDrainPv]);
+        mbar_wait_drain(&bars[L::kBarDrainPv], 0);
       }
     }
     __syncwarp();
