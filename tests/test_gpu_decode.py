@@ -127,3 +127,17 @@ def test_repeated_calls_are_deterministic():
     o1, l1 = smla.sparse_mla_decode_fp8(*args)
     o2, l2 = smla.sparse_mla_decode_fp8(*args)
     assert (o1 == o2).all() and (l1 == l2).all()
+
+
+@pytest.mark.parametrize("H", [16, 128])
+def test_zero_topk_gives_zero_and_minus_inf(H):
+    import torch
+    import sparse_mla_attention_fp8_gb300 as smla
+    case = inp.memory_bound_decode(seed=14, R=3, ctx_lo=200, ctx_hi=300, K=64, H=H)
+    cache = dev(oracle_cache(case))
+    idx0 = torch.zeros((case.T, 0), dtype=torch.int32, device="cuda")
+    out, lse = smla.sparse_mla_decode_fp8(bf16_dev(case.q), cache, idx0, dev(case.block_table),
+                                          dev(case.req_id_per_token), case.sm_scale)
+    torch.cuda.synchronize()
+    assert smla.read_device_status() == 0
+    assert torch.all(out == 0) and torch.all(torch.isneginf(lse))

@@ -72,3 +72,15 @@ def test_attention_plan_matches_the_launch_shape(fp8, H):
     units = 3 * (H // heads_per_unit)
     assert ctas1 == units * (2 if H == 128 else 1)
     assert launches1 == (2 if fp8 and H == 128 else 1)  # + the Q preparation of the 128-head FP8 path
+
+
+@pytest.mark.parametrize("H", [32, 128])
+def test_prefill_zero_topk_gives_zero_and_minus_inf(H):
+    import torch
+    import sparse_mla_attention_fp8_gb300 as smla
+    case = inp.prefill(seed=6, R=1, cached=50, new=5, K=64, H=H)
+    idx0 = torch.zeros((case.T, 0), dtype=torch.int32, device="cuda")
+    out, lse = smla.sparse_mla_prefill_bf16(bf16_dev(case.q), bf16_dev(case.kv), idx0, case.sm_scale)
+    torch.cuda.synchronize()
+    assert smla.read_device_status() == 0
+    assert torch.all(out == 0) and torch.all(torch.isneginf(lse))

@@ -47,11 +47,13 @@ def _workspace_call(smla, case, cache, num_splits):
     return out.float().cpu().numpy(), lse.cpu().numpy()
 
 
+@pytest.mark.parametrize("H", [16, 128])
 @pytest.mark.parametrize("num_splits", [0, 3])
-def test_noalloc_matches_workspace_entry_point_twice(smla, num_splits):
+def test_noalloc_matches_workspace_entry_point_twice(smla, num_splits, H):
     import torch
-    # two different batches (ragged top-k of 200 = 3 full tiles + a tail of 8), same shapes
-    cases = [inp.memory_bound_decode(seed=s, R=9, ctx_lo=300, ctx_hi=2500, K=200) for s in (5, 15)]
+    # two different batches (ragged top-k of 200 = 3 full tiles + a tail of 8), same shapes; H = 128 runs
+    # the CTA-pair kernel, whose prepared Q also lives in the fixed scratch
+    cases = [inp.memory_bound_decode(seed=s, R=9, ctx_lo=300, ctx_hi=2500, K=200, H=H) for s in (5, 15)]
     T, H, _ = cases[0].q.shape
     out = torch.empty((T, H, 512), dtype=torch.bfloat16, device="cuda")
     lse = torch.empty((T, H), dtype=torch.float32, device="cuda")
