@@ -64,7 +64,10 @@ constexpr int kRopePanel = kRows * 64;      // 4 KB: 64 rows x 32 bf16 (this CTA
 constexpr int kQRopePanel = kHeads * 64;    // 8 KB: 128 heads x 32 bf16
 constexpr int kKBuf = 4 * kPanel + kRopePanel;     // 36 KB
 constexpr int kQBuf = 4 * kQPanel + kQRopePanel;   // 72 KB
-constexpr int kXSlot = kHeads * 32 * 4;     // 16 KB: the peer's partial logits of one half tile (32 rows)
+// The peer's partial logits of one half tile (32 rows) as 16-bit fixed point:
+// 64 bytes per head, then one fp32 step per head.
+constexpr int kXData = kHeads * 64;         // 8 KB
+constexpr int kXSlot = kXData + kHeads * 4;  // 8.5 KB
 constexpr int kRowBytesBf16 = kDqk * 2;     // 1152
 constexpr int kLoaders = 4;                 // loader lw gathers rows 16 lw .. 16 lw + 15
 constexpr float kMaxSlack = 8.0f;           // log2 growth of a head's max tolerated before rescaling O
@@ -125,17 +128,17 @@ constexpr int kThreads = 32 * kNumWarps;
 // (set by the host through smla_trace_set_wide).  Compiled out otherwise.
 #ifdef SMLA_TRACE
 __device__ long long* g_smla_trace_wide = nullptr;
-constexpr int kTraceTiles = 64, kTraceEvents = 14;
+constexpr int kTraceTiles = 64, kTraceEvents = 16;
 #define WIDE_TRACE(tl, ev)                                                                                   \
   do {                                                                                                       \
-    if (g_smla_trace_wide && (tl) < kTraceTiles)                                                           \
-      g_smla_trace_wide[((size_t)blockIdx.x * kTraceTiles + (tl)) * kTraceEvents + (ev)] = clock64();     \
+    if (trace_buf && (tl) < kTraceTiles)                                                                   \
+      trace_buf[((size_t)blockIdx.x * kTraceTiles + (tl)) * kTraceEvents + (ev)] = clock64();             \
   } while (0)
 #else
 #define WIDE_TRACE(tl, ev) ((void)0)
 #endif
 enum { kEvSFull = 0, kEvSLoaded, kEvXFree, kEvSent, kEvXFull, kEvPReady, kEvPFull, kEvQk, kEvPv, kEvIssue, kEvQkSeen,
-       kEvKEmpty, kEvConverted, kEvRawFull };
+       kEvKEmpty, kEvConverted, kEvRawFull, kEvXTop, kEvXKFull };
 
 struct Params {
   const __nv_bfloat16* q;  // [T, 128, 576]
@@ -161,6 +164,20 @@ struct TileInfo {
   int u, kt;
   bool seg_start, seg_end;
 };
+
+// st.async of raw 32-bit words into a peer CTA's shared memory, completing
+// `bar` (cluster addresses) by the bytes written.
+__device__ __forceinline__ void st_async_v4_b32(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                                uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(addr),
+               "r"(a), "r"(b), "r"(c), "r"(d), "r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void st_async_b32(uint32_t addr, uint32_t a, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(addr), "r"(a),
+               "r"(bar)
+               : "memory");
+}
 
 __device__ __forceinline__ TileInfo tile_info(const Params& p, int64_t x, int64_t xbeg, int64_t xend) {
   TileInfo ti;
@@ -192,6 +209,10 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
+#ifdef SMLA_TRACE
+  // read once: a store through the global pointer would force a reload at every event
+  long long* __restrict__ const trace_buf = g_smla_trace_wide;
+#endif
   const int lane = tid & 31;
   const int c = (int)cluster_ctarank();  // value half owned by this CTA
   const int pair = blockIdx.x >> 1;
@@ -530,16 +551,26 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
     if (warp >= kXchgWarp0) {
       // ---------------------------------------------------------- exchange (warps 4..11)
       // Warp group e handles half e of every tile (rows 32 e .. 32 e + 31,
-      // exchange slot e): the
-      // partial logits go to the peer (st.async into its slot, the bytes
-      // completing its barrier; chunk i of head h at 16-byte slot (i + h) % 8 so
-      // a warp's stores spread over the banks, the reader using the same
-      // placement), the peer's partial is added, rows are masked and scaled to
-      // the log2 domain, and the result is written back over the S buffer.  A
-      // half is sent once the peer has read the same half of the previous tile.
+      // exchange slot e): the partial logits go to the peer (st.async into
+      // its slot, the bytes completing its barrier), the peer's partial is
+      // added, rows are masked and scaled to the log2 domain, and the result
+      // is written back over the S buffer.  A half is sent once the peer has
+      // read the same half of the previous tile.
+      //
+      // The SM-to-SM network moves about 12 bytes per cycle, so the partials
+      // travel as 16-bit fixed point: each head's 32 values as integers
+      // q = round(x * 32767 / a) with a the largest magnitude among them, plus
+      // the step a / 32767.  The error of a received value is at most a / 65534
+      // (plus fp32 rounding), i.e. 2^-16 of the half row's largest partial.
+      // The codes are q + 32768 (offset binary); both conversions stay on the
+      // full-rate pipes: fma(x, 32767 / a, 1.5 * 2^23 + 32768) rounds to the
+      // nearest integer and leaves the code in its low 16 bits, and a code u
+      // placed under the exponent of 2^23 reads as 2^23 + u.
+      // The 16-byte chunk i of head h sits at position (i + h / 2) % 4 of the
+      // head's 64 bytes, so that eight consecutive heads cover all banks.
       const uint32_t peer = (uint32_t)(c ^ 1);
-      const uint32_t x_local = smem_u32(smem + L::kOffX) + (uint32_t)(h * 128);
-      const uint32_t x_remote = mapa_shared(x_local, peer);
+      const uint32_t x_chunk = (uint32_t)(h * 64);
+      const uint32_t x_remote = mapa_shared(smem_u32(smem + L::kOffX), peer);
       const uint32_t xfull_remote = mapa_shared(smem_u32(&bars[L::kBarXFull]), peer);
       const uint32_t xfree_remote = mapa_shared(smem_u32(&bars[L::kBarXFree]), peer);
       const int e = (warp - kXchgWarp0) >> 2;
@@ -554,8 +585,10 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
           ++u;
         }
         const int sb = tl % kSBufs, kb = tl % L::kKBufs;
+        if (tid == 32 * kXchgWarp0) WIDE_TRACE(tl, kEvXTop);
         // row validity (written by the loaders before the tile's full barrier)
         if (!dead) dead = !SMLA_WAIT(L::kBarKFull + kb, (tl / L::kKBufs) & 1);
+        if (tid == 32 * kXchgWarp0) WIDE_TRACE(tl, kEvXKFull);
         uint32_t vb = 0u;
         {
           const uint4* vf = reinterpret_cast<const uint4*>(valid + kb * kRows + 32 * e);
@@ -594,27 +627,45 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
               s[16 + j] = __uint_as_float(r1[j]);
             }
           }
+          // 16-bit fixed point relative to the largest magnitude
+          float amax = 0.f;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(s[j]));
+          // (a magnitude below 2^-100 sends zeros)
+          const float inv = amax > 0x1p-100f ? __fdividef(32767.f, amax) : 0.f;
+          uint32_t pk[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            pk[j] = __byte_perm(__float_as_uint(fmaf(s[2 * j], inv, 12615680.f)),
+                                __float_as_uint(fmaf(s[2 * j + 1], inv, 12615680.f)), 0x5410);
           if (tid == 32 * kXchgWarp0 && e == 0) WIDE_TRACE(tl, kEvSLoaded);
           if (tl >= 1 && !dead) dead = !SMLA_WAIT_X(L::kBarXFree + e, (tl - 1) & 1);
           if (tid == 32 * kXchgWarp0 && e == 0) WIDE_TRACE(tl, kEvXFree);
           if (!dead) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              st_async_v4(x_remote + e * kXSlot + 16 * ((i + h) & 7), s[4 * i], s[4 * i + 1], s[4 * i + 2],
-                          s[4 * i + 3], xfull_remote + 8 * e);
+            for (int i = 0; i < 4; ++i)
+              st_async_v4_b32(x_remote + e * kXSlot + x_chunk + 16 * ((i + (h >> 1)) & 3), pk[4 * i],
+                              pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3], xfull_remote + 8 * e);
+            st_async_b32(x_remote + e * kXSlot + kXData + 4 * h, __float_as_uint(amax * (1.f / 32767.f)),
+                         xfull_remote + 8 * e);
           }
           if (tid == 32 * kXchgWarp0 && e == 0) WIDE_TRACE(tl, kEvSent);
           if (!dead) dead = !SMLA_WAIT_X(L::kBarXFull + e, tl & 1);
           if (tid == 32 * kXchgWarp0 && e == 0) WIDE_TRACE(tl, kEvXFull);
           if (!dead) {
-            const uint8_t* src = smem + L::kOffX + e * kXSlot + h * 128;
+            const uint8_t* src = smem + L::kOffX + e * kXSlot;
+            const float step = *reinterpret_cast<const float*>(src + kXData + 4 * h);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const float4 v = *reinterpret_cast<const float4*>(src + 16 * ((i + h) & 7));
-              s[4 * i] += v.x;
-              s[4 * i + 1] += v.y;
-              s[4 * i + 2] += v.z;
-              s[4 * i + 3] += v.w;
+            for (int i = 0; i < 4; ++i) {
+              const uint4 v = *reinterpret_cast<const uint4*>(src + x_chunk + 16 * ((i + (h >> 1)) & 3));
+              const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                const float lo = __uint_as_float(__byte_perm(w[k], 0x4B00u, 0x5410)) - 8421376.f;  // 2^23 + 32768
+                const float hi = __uint_as_float(__byte_perm(w[k], 0x4B00u, 0x5432)) - 8421376.f;
+                s[8 * i + 2 * k] = fmaf(lo, step, s[8 * i + 2 * k]);
+                s[8 * i + 2 * k + 1] = fmaf(hi, step, s[8 * i + 2 * k + 1]);
+              }
             }
           }
           // the slot's values are in registers: the peer may overwrite it
