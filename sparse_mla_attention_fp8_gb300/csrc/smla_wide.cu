@@ -73,11 +73,13 @@ constexpr int kLoaders = 4;                 // loader lw gathers rows 16 lw .. 1
 constexpr float kMaxSlack = 8.0f;           // log2 growth of a head's max tolerated before rescaling O
 
 // FP8 rows: per 4-row group the staging holds codes 0..127 and 128..255 of
-// the CTA's two scale groups (4 x 128 bytes each) and the rows' four scales
-// (4 x 16 bytes), padded to a multiple of 128 bytes (TMA destinations).
-constexpr int kRawGroup = 1152;
-constexpr int kRawBuf = (kRows / 4) * kRawGroup;  // 18 KB per tile
-constexpr int kRawRowBytes = 128 + 128 + 16;      // gathered into staging per row
+// the CTA's two scale groups (4 x 128 bytes each), the rows' four scales
+// (4 x 16 bytes, padded to 128) and the CTA's RoPE halves (4 x 64 bytes);
+// every part starts on a 128-byte boundary (TMA destinations).
+constexpr int kRawRope = 1152;                      // offset of the RoPE halves in a group
+constexpr int kRawGroup = kRawRope + 4 * 64;        // 1408
+constexpr int kRawBuf = (kRows / 4) * kRawGroup;    // 22 KB per tile
+constexpr int kRawRowBytes = 128 + 128 + 16 + 64;   // gathered into staging per row
 constexpr int kSBufs = 3;                         // S buffers in tensor memory
 
 // shared memory (offsets from a 1024-byte aligned base): Q, the bf16 operand
@@ -190,8 +192,8 @@ __device__ __forceinline__ TileInfo tile_info(const Params& p, int64_t x, int64_
 
 // Row maps: bf16 rows: m0 = 128-byte value panels (128-byte swizzle), m1
 // unused, m2 = 64-byte RoPE halves (64-byte swizzle).  FP8 rows: m0 = 128
-// bytes of codes, m1 = the 16 scale bytes (both unswizzled, into staging), m2
-// = the 64-byte RoPE halves (64-byte swizzle, into the operand tile).
+// bytes of codes, m1 = the 16 scale bytes, m2 = the 64-byte RoPE halves (all
+// unswizzled, into staging).
 template <bool kFp8>
 __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
     sparse_mla_wide_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap m0,
@@ -311,15 +313,16 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
     // ------------------------------------------------------------ FP8 row loaders + converters
     // Loader lw owns tile rows 16 lw .. 16 lw + 15 (staging groups 4 lw ..
     // 4 lw + 3).  Two tiles ahead it gathers their codes (the CTA's two scale
-    // groups) and scales into a staging slot, lane 3 g + b issuing copy b of
-    // group g; when an operand tile is free it gathers the RoPE half straight
-    // into it (bf16 in the row) and converts the staged codes to f16: the
-    // exact e4m3 widening times the scale rounded to f16, one f16 product
-    // (relative error below 2^-11), lane l handling codes 8 l .. 8 l + 7 of
-    // each row.
+    // groups), scales and RoPE halves into a staging slot, lane 4 g + b
+    // issuing copy b of group g; when an operand tile is free it converts the
+    // staged codes to f16 (the exact e4m3 widening times the scale rounded to
+    // f16, one f16 product: relative error below 2^-11), lane l handling
+    // codes 8 l .. 8 l + 7 of each row, and copies the RoPE halves (bf16) into
+    // the tile's 64-byte-swizzled panel.  Nothing on the way from a free tile
+    // to a full one waits for a copy from global memory.
     const int lw = warp - kLoadWarp0;
     uint8_t* raw_base = smem + L::kOffRaw;
-    const int rgrp = lane / 3, rbox = lane - 3 * rgrp;
+    const int rgrp = lane >> 2, rbox = lane & 3;
     int raw_issued = 0;
     auto issue_raw = [&](int t2) -> bool {
       const int b4 = t2 & 3, sl = t2 & 1;
@@ -330,12 +333,15 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
       uint64_t* bar = &bars[L::kBarRawFull + 2 * lw + sl];
       if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)(16 * kRawRowBytes));
       __syncwarp();
-      if (lane < 12) {
-        const uint32_t dst = smem_u32(raw_base + sl * kRawBuf + (4 * lw + rgrp) * kRawGroup + 512 * rbox);
+      if (lane < 16) {
+        const uint32_t dst =
+            smem_u32(raw_base + sl * kRawBuf + (4 * lw + rgrp) * kRawGroup + (rbox < 3 ? 512 * rbox : kRawRope));
         if (rbox < 2)
           tma_gather4_2d(dst, &m0, 256 * c + 128 * rbox, r0, r1, r2, r3, bar);
-        else
+        else if (rbox == 2)
           tma_gather4_2d(dst, &m1, kScaleOff, r0, r1, r2, r3, bar);
+        else
+          tma_gather4_2d(dst, &m2, kRopeOff + 64 * c, r0, r1, r2, r3, bar);
       }
       ++raw_issued;
       return true;
@@ -343,14 +349,12 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
     bool ok = true;
     if (n_local > 0) ok = issue_raw(0);
     if (ok && n_local > 1) ok = issue_raw(1);
-    int last_b = -1, last_use = 0, converted = 0;
+    int converted = 0;
     for (int tl = 0; ok && tl < n_local; ++tl) {
       const int b4 = tl & 3, kb = tl % L::kKBufs, use = tl / L::kKBufs, sl = tl & 1;
       if (!SMLA_WAIT(L::kBarIdxFull + b4, (tl >> 2) & 1)) break;
       const int32_t slot = lane < 16 ? slots_ring[b4 * kRows + 16 * lw + lane] : -1;
       const uint32_t vmask = __ballot_sync(kFullMask, slot >= 0);
-      const int g0 = __shfl_sync(kFullMask, slot, (4 * lane) & 31), g1 = __shfl_sync(kFullMask, slot, (4 * lane + 1) & 31);
-      const int g2 = __shfl_sync(kFullMask, slot, (4 * lane + 2) & 31), g3 = __shfl_sync(kFullMask, slot, (4 * lane + 3) & 31);
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[L::kBarIdxEmpty + b4]);
       if (!SMLA_WAIT(L::kBarRawFull + 2 * lw + sl, (tl >> 1) & 1)) break;
@@ -361,6 +365,15 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
       const uint32_t tile = smem_u32(smem + L::kOffK + kb * kKBuf);
       const uint8_t* raw = raw_base + sl * kRawBuf;
       const int half = lane >> 4, pnl = lane >> 3, ch = lane & 7;
+      // RoPE halves: 16 rows x 4 chunks of 16 bytes, two per lane, into the
+      // 64-byte swizzle (chunk j of row r at j ^ ((r >> 1) & 3) in its 64 bytes)
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int k = lane + 32 * i, r = 16 * lw + (k >> 2), j = k & 3;
+        const uint4 v = *reinterpret_cast<const uint4*>(raw + (r >> 2) * kRawGroup + kRawRope + (r & 3) * 64 + 16 * j);
+        st_shared_v4(tile + 4 * kPanel + (uint32_t)((r >> 3) * 512 + (r & 7) * 64 + ((j ^ ((r >> 1) & 3)) << 4)), v.x,
+                     v.y, v.z, v.w);
+      }
       // 4 rows at a time: all their loads first, so that one load latency
       // covers 4 rows (the stores are ordered after them)
 #pragma unroll 1
@@ -391,28 +404,15 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
         }
       }
       if (lane == 0 && lw == 0) WIDE_TRACE(tl, kEvConverted);
+      // the tile's full barrier: this warp's arrival for its converted rows
       fence_proxy_async_smem();
-      __syncwarp();
-      // the tile's full barrier: this warp's RoPE bytes (registered before the
-      // copies, which go after the conversion so that a busy TMA unit does not
-      // hold it up), then its arrival for the converted rows
-      if (lane == 0) mbar_expect_tx(&bars[L::kBarKFull + kb], (uint32_t)(16 * 64));
-      __syncwarp();
-      if (lane < 4) {
-        const int r_g = 16 * lw + 4 * lane;
-        tma_gather4_2d(tile + 4 * kPanel + (uint32_t)((r_g >> 3) * 512 + (r_g & 7) * 64), &m2, kRopeOff + 64 * c, g0,
-                       g1, g2, g3, &bars[L::kBarKFull + kb]);
-      }
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[L::kBarKFull + kb]);
       if (lane == 0 && lw == 0) WIDE_TRACE(tl, kEvIssue);
-      last_b = kb;
-      last_use = use;
       converted = tl + 1;
       if (tl + 2 < n_local) ok = issue_raw(tl + 2);
     }
     // no copy may still be landing in shared memory when the CTA exits
-    if (last_b >= 0) mbar_wait_drain(&bars[L::kBarKFull + last_b], last_use & 1);
     for (int t2 = converted; t2 < raw_issued; ++t2)
       if (lane == 0) mbar_wait_drain(&bars[L::kBarRawFull + 2 * lw + (t2 & 1)], (t2 >> 1) & 1);
     __syncwarp();
@@ -916,7 +916,7 @@ cudaError_t make_maps(const void* rows, int64_t n_rows, const void* q, int T, CU
     CUtensorMapSwizzle sw;
   } specs[5] = {{m0, rows, r_dim, rstride, 128, 1, kFp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B},
                 {m1, rows, r_dim, rstride, kFp8 ? 16u : 128u, 1, kFp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B},
-                {m2, rows, r_dim, rstride, 64, 1, CU_TENSOR_MAP_SWIZZLE_64B},
+                {m2, rows, r_dim, rstride, 64, 1, kFp8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_64B},
                 {q_map, q, q_dim, qstride, 128, kHeads, CU_TENSOR_MAP_SWIZZLE_128B},
                 {q_rope_map, q, q_dim, qstride, 64, kHeads, CU_TENSOR_MAP_SWIZZLE_64B}};
   for (const Spec& sp : specs) {
