@@ -46,19 +46,37 @@ TRAFFIC_SOURCES = ("smla_decode.cu", "smla_combine.cuh", "smla_common.cuh", "sm1
 TRAFFIC_BY_SOURCE = {
     "44405ffa0802da05": 100_888_576 + 2_535_168 + 7_378_432 + 0,
 }
+# The same for the 128-head CTA-pair kernel, per workload
+# (profiles/sparse_mla_wide_kernel_*.md): the bf16 prefill's attention kernel
+# plus its combine; the FP8 decode's attention kernel alone (its capture left
+# out the Q preparation and the combine).
+WIDE_TRAFFIC_SOURCES = ("smla_wide.cu", "smla_combine.cuh", "smla_common.cuh", "sm103_ptx.cuh")
+WIDE_TRAFFIC_BY_SOURCE = {
+    ("19629da18520f8de", "prefill_h128_k2048"): (671_053_056 + 524_675_840 + 38_473_472 + 210_944,
+                                                 "attention kernel + combine"),
+    ("19629da18520f8de", "decode_h128_k2048"): (231_825_408 + 23_199_232, "attention kernel only"),
+}
 
 
-def captured_traffic():
+def _source_key(files):
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "sparse_mla_attention_fp8_gb300", "csrc")
     try:
-        for f in TRAFFIC_SOURCES:
+        for f in files:
             with open(os.path.join(csrc, f), "rb") as fh:
                 h.update(fh.read())
     except OSError:
         return None
-    return TRAFFIC_BY_SOURCE.get(h.hexdigest()[:16])
+    return h.hexdigest()[:16]
+
+
+def captured_traffic():
+    return TRAFFIC_BY_SOURCE.get(_source_key(TRAFFIC_SOURCES))
+
+
+def captured_wide_traffic(workload):
+    return WIDE_TRAFFIC_BY_SOURCE.get((_source_key(WIDE_TRAFFIC_SOURCES), workload), (None, None))
 
 
 # ---------------------------------------------------------------- helpers
@@ -538,6 +556,7 @@ def run_tensor_workload(args):
         raise SystemExit("device status reports a kernel wait timeout")
     tflops = flops / (ms * 1e-3) / 1e12
     peak = tensor_peak_tflops(peaks, fp8)
+    wide_traffic, wide_traffic_kernels = captured_wide_traffic(args.workload)
     cpu = None
     if not args.no_cpu_baseline:
         t0 = time.perf_counter()
@@ -555,7 +574,7 @@ def run_tensor_workload(args):
                    "parallelism": "single GPU", "launch": "CUDA graph per step"},
         "tflops": tflops,
         "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak, "unit": "TFLOP/s", "frac": tflops / peak,
-                     "traffic": None, "peak_source": peaks["source"] + (" bf16 x 2 (fp8/bf16 nominal)" if fp8 else ""),
+                     "traffic": wide_traffic, "traffic_kernels": wide_traffic_kernels, "peak_source": peaks["source"] + (" bf16 x 2 (fp8/bf16 nominal)" if fp8 else ""),
                      "kernel": "attention launch (attention kernel + split combine)", "flops_per_launch": flops,
                      "avg_launch_us": ms * 1e3},
         "cpu_baseline": cpu, "e2e": None, "gpu_launches": launches * args.steps, "clocks": clk,
