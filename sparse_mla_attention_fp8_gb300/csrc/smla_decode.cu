@@ -326,6 +326,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Launched as a programmatic dependent (of the cache store, typically): the
+  // index translation and the Q split read only this call's inputs and write
+  // only shared memory, so they start at once; every other role reads the
+  // cache or writes global memory, and first waits for the preceding grid.
+  if (warp != kIndexWarp && (warp < kQWarp0 || warp >= kQWarp0 + kQWarps)) grid_dependency_wait();
 
 #define SMLA_WAIT(bar_idx, parity) mbar_wait(&bars[(bar_idx)], (parity), abort_flag, p.status, kDevWaitTimeout)
 
@@ -1025,8 +1030,19 @@ cudaError_t launch_decode_fp8(const AttnArgs& a, const AttnPlan& plan, cudaStrea
   CUtensorMap panel_map, scale_map;
   cudaError_t em = make_cache_maps(a.cache, a.NB, &panel_map, &scale_map);
   if (em != cudaSuccess) return em;
-  sparse_mla_decode_fp8_kernel<<<plan.G, kThreads, kSmemAlloc, stream>>>(p, panel_map, scale_map);
-  cudaError_t e = cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)plan.G, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemAlloc;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, sparse_mla_decode_fp8_kernel, p, panel_map, scale_map);
+  if (e != cudaSuccess) return e;
+  e = cudaGetLastError();
   if (e != cudaSuccess || !plan.need_combine) return e;
   e = launch_combine<HG>(p.part_o, p.part_lse, p.out, p.lse, p.H, p.n_hg, p.nt, p.total, p.G, plan.units, stream);
   if (e != cudaSuccess) return e;

@@ -11,6 +11,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "sm103_ptx.cuh"
 #include "smla_common.cuh"
 #include "smla_kernels.h"
 
@@ -35,6 +36,9 @@ __device__ __forceinline__ void bf16x2_to_f32(uint32_t w, float& lo, float& hi) 
 __global__ void __launch_bounds__(256) quantize_store_kernel(const uint4* __restrict__ kv_new,
                                                              const int64_t* __restrict__ slot_mapping,
                                                              uint8_t* __restrict__ cache, int T, int64_t NB) {
+  // a decode launched behind this grid as its programmatic dependent may start
+  // its prologue now; it waits for this grid before it reads the cache
+  grid_launch_dependents();
   const int token = (int)((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (token >= T) return;
