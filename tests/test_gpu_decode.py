@@ -141,3 +141,86 @@ def test_zero_topk_gives_zero_and_minus_inf(H):
     torch.cuda.synchronize()
     assert smla.read_device_status() == 0
     assert torch.all(out == 0) and torch.all(torch.isneginf(lse))
+
+
+def _mixed_case_on_device(seed):
+    import torch
+    case = inp.mixed_batch(seed, n_decode=5, n_prefill=2, prefill_tokens=200, ctx_lo=400, ctx_hi=1500, K=128)
+    old = torch.from_numpy(oracle_cache(case, with_new=False)).cuda()
+    ref_cache = oracle_cache(case, with_new=True)
+    ref_out, ref_lse = oracle.sparse_mla_decode(case.q, ref_cache, case.indices, case.block_table,
+                                                case.req_id_per_token, case.sm_scale)
+    args = dict(new_rows=bf16_dev(case.new_rows), new_slots=dev(case.new_slots), q=bf16_dev(case.q),
+                idx=dev(case.indices), bt=dev(case.block_table), req=dev(case.req_id_per_token))
+    return case, old, ref_out, ref_lse, args
+
+
+def test_store_then_decode_without_host_sync():
+    # The decode is launched as a programmatic dependent of the store: its
+    # prologue may overlap the store, its reads of the cache may not.
+    import torch
+    import sparse_mla_attention_fp8_gb300 as smla
+    case, old, ref_out, ref_lse, a = _mixed_case_on_device(21)
+    cache = old.clone()
+    torch.cuda.synchronize()
+    smla.mla_cache_store_fp8(a["new_rows"], a["new_slots"], cache)
+    out, lse = smla.sparse_mla_decode_fp8(a["q"], cache, a["idx"], a["bt"], a["req"], case.sm_scale)
+    torch.cuda.synchronize()
+    assert_out_close(out.float().cpu().numpy(), ref_out, case.name + " store->decode")
+    assert_lse_close(lse.cpu().numpy(), ref_lse, case.name + " store->decode")
+
+
+def test_store_then_decode_in_a_cuda_graph():
+    import torch
+    import sparse_mla_attention_fp8_gb300 as smla
+    case, old, ref_out, ref_lse, a = _mixed_case_on_device(22)
+    T, H = case.q.shape[0], case.q.shape[1]
+    cache = old.clone()
+    out = torch.empty((T, H, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((T, H), dtype=torch.float32, device="cuda")
+    ws = torch.zeros(smla.decode_workspace_bytes(T, H, case.K, 0), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):  # eager once: kernel attributes are set outside the capture
+        smla.mla_cache_store_fp8(a["new_rows"], a["new_slots"], cache, stream=stream)
+        smla.sparse_mla_decode_fp8(a["q"], cache, a["idx"], a["bt"], a["req"], case.sm_scale, 0, out, lse, ws,
+                                   stream=stream)
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        smla.mla_cache_store_fp8(a["new_rows"], a["new_slots"], cache, stream=stream)
+        smla.sparse_mla_decode_fp8(a["q"], cache, a["idx"], a["bt"], a["req"], case.sm_scale, 0, out, lse, ws,
+                                   stream=stream)
+    for _ in range(3):
+        cache.copy_(old)  # the rows the store writes are absent again before every replay
+        out.fill_(float("nan"))
+        lse.fill_(float("nan"))
+        torch.cuda.synchronize()
+        g.replay()
+        torch.cuda.synchronize()
+        assert_out_close(out.float().cpu().numpy(), ref_out, case.name + " graph")
+        assert_lse_close(lse.cpu().numpy(), ref_lse, case.name + " graph")
+    assert smla.read_device_status(ws) == 0
+
+
+@pytest.mark.parametrize("H", [16, 128])
+def test_back_to_back_decodes_into_the_same_buffers(H):
+    # The second call's result must replace the first's, whatever the calls'
+    # launches overlap.
+    import torch
+    import sparse_mla_attention_fp8_gb300 as smla
+    c1 = inp.memory_bound_decode(seed=31, R=6, ctx_lo=500, ctx_hi=2000, K=256, H=H)
+    c2 = inp.memory_bound_decode(seed=32, R=6, ctx_lo=500, ctx_hi=2000, K=256, H=H)
+    assert c1.q.shape == c2.q.shape and c1.num_blocks == c2.num_blocks
+    T = c1.q.shape[0]
+    caches = [dev(oracle_cache(c)) for c in (c1, c2)]
+    out = torch.empty((T, H, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((T, H), dtype=torch.float32, device="cuda")
+    torch.cuda.synchronize()
+    for c, cache in zip((c1, c2), caches):
+        smla.sparse_mla_decode_fp8(bf16_dev(c.q), cache, dev(c.indices), dev(c.block_table),
+                                   dev(c.req_id_per_token), c.sm_scale, 0, out, lse)
+    torch.cuda.synchronize()
+    ref_out, ref_lse = oracle.sparse_mla_decode(c2.q, oracle_cache(c2), c2.indices, c2.block_table,
+                                                c2.req_id_per_token, c2.sm_scale)
+    assert_out_close(out.float().cpu().numpy(), ref_out, c2.name + " second call")
+    assert_lse_close(lse.cpu().numpy(), ref_lse, c2.name + " second call")
