@@ -44,7 +44,7 @@ UNIT = "query-tokens/s"
 # sources change, the figure no longer applies and the roofline reports null.
 TRAFFIC_SOURCES = ("smla_decode.cu", "smla_combine.cuh", "smla_common.cuh", "sm103_ptx.cuh")
 TRAFFIC_BY_SOURCE = {
-    "cf0c8cc879b568b5": 100_884_224 + 2_507_008 + 7_378_688 + 0,
+    "4bf1514cc60d41f8": 100_889_344 + 2_852_352 + 7_377_408 + 0,
 }
 # The same for the 128-head CTA-pair kernel, per workload
 # (profiles/sparse_mla_wide_kernel_*.md): the bf16 prefill's attention kernel

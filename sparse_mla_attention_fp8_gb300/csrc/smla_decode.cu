@@ -14,8 +14,10 @@
 //  * Transport: TMA tile::gather4 copies straight into the operand tiles,
 //    four rows per instruction: the 512 e4m3 codes as four K-major panels with
 //    the 128-byte swizzle (64 rows x 128 bytes each), the 64 bf16 RoPE values
-//    as a fifth panel, the four float32 scales beside them.  Invalid rows are
-//    gathered at row -1, which the TMA zero-fills.  Four loader warps, one per
+//    as a fifth panel; the four float32 scales of a row go beside them as one
+//    16-byte cp.async, which keeps these small copies out of the TMA queue.
+//    Invalid rows are gathered at row -1, which the TMA zero-fills (the scale
+//    copy writes zeros).  Four loader warps, one per
 //    16-row quarter of every tile, each lane issuing one copy: the cost of
 //    issuing copies falls on the issuing warp, so it is spread.  Four operand
 //    tiles, so that the loads of the next tiles are in flight while one is
@@ -161,6 +163,16 @@ __host__ __device__ constexpr uint32_t idesc_e4m3(uint32_t M, uint32_t N, uint32
   return (1u << 4) | (a_mn << 15) | (b_mn << 16) | ((N >> 3) << 17) | ((M >> 4) << 24);
 }
 
+// 16-byte cp.async global -> shared (src_bytes = 0 writes zeros), and an
+// arrival on an mbarrier once every earlier cp.async of this thread has
+// landed (the barrier's count includes it).
+__device__ __forceinline__ void cp_async_16_zfill(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 struct Params {
   const __nv_bfloat16* q;
   const uint8_t* cache;
@@ -277,8 +289,7 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    sparse_mla_decode_fp8_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap panel_map,
-                                 const __grid_constant__ CUtensorMap scale_map) {
+    sparse_mla_decode_fp8_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap panel_map) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   grid_launch_dependents();  // the combine may be launched behind this grid right away
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -296,7 +307,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     for (int i = 0; i < kOpBufs; ++i) {
-      mbar_init(&bars[kBarOpFull + i], kLoaders);  // one arrival (with its bytes) per loader
+      // per loader: one arrival with its TMA bytes, and one per row when the row's scale copy lands
+      mbar_init(&bars[kBarOpFull + i], kLoaders + kRows);
       mbar_init(&bars[kBarOpEmpty + i], 1);
     }
     for (int i = 0; i < 2; ++i) {
@@ -365,12 +377,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp >= kLoadWarp0 && warp < kLoadWarp0 + kLoaders) {
     // ------------------------------------------------------------ loaders
     // Loader lw gathers rows 16 lw .. 16 lw + 15 of every tile: 4 groups of 4
-    // rows x 6 copies (code panels 0..3, RoPE panel, scales), lane 6 g + b
-    // issuing copy b of group g.  Its one arrival on the tile's full barrier
-    // carries the bytes of its 16 rows and follows its writes of the rows'
-    // valid flags.
+    // rows x 5 TMA copies (code panels 0..3, RoPE panel), lane 5 g + b
+    // issuing copy b of group g, and each row's 16 bytes of scales as one
+    // cp.async by lane r (zero-filled for an invalid row), which keeps these
+    // small copies out of the SM's TMA queue.  Its arrival on the tile's full
+    // barrier carries the TMA bytes of its 16 rows and follows its writes of
+    // the rows' valid flags; each scale copy arrives there when it lands.
     const int lw = warp - kLoadWarp0;
-    const int grp = lane / 6, box = lane % 6;  // lanes 0..23 issue
+    const int grp = lane / 5, box = lane % 5;  // lanes 0..19 issue TMA copies
     const int r_g = 16 * lw + 4 * grp;         // tile row of the lane's group
     int last_ob = -1, last_use = 0;
     for (int tl = 0; tl < n_local; ++tl) {
@@ -386,16 +400,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0 && lw == 0) SMLA_TRACE_SET(tl, kEvOpEmpty);
       if (lane < 16) valid[ob * kRows + 16 * lw + lane] = (uint8_t)((vmask >> lane) & 1u);
       __syncwarp();
-      if (lane == 0) mbar_arrive_expect_tx(&bars[kBarOpFull + ob], 16 * kRowBytes);
+      if (lane == 0) mbar_arrive_expect_tx(&bars[kBarOpFull + ob], 16 * (4 * 128 + 128));
       __syncwarp();
-      if (lane < 24) {
-        const uint32_t op = smem_u32(smem + kOffOp + ob * kOpBuf);
+      const uint32_t op = smem_u32(smem + kOffOp + ob * kOpBuf);
+      if (lane < 20) {
         const uint32_t in_panel = (uint32_t)((r_g >> 3) * 1024 + (r_g & 7) * 128);
-        const uint32_t dst = box < 4    ? op + box * kPanel + in_panel
-                             : box == 4 ? op + kOpRope + in_panel
-                                        : op + kOpScale + (r_g >> 2) * 128;
-        const int x = box < 4 ? 128 * box : box == 4 ? kRopeOff : kScaleOff;
-        tma_gather4(dst, box < 5 ? &panel_map : &scale_map, x, g0, g1, g2, g3, &bars[kBarOpFull + ob]);
+        const uint32_t dst = box < 4 ? op + box * kPanel + in_panel : op + kOpRope + in_panel;
+        tma_gather4(dst, &panel_map, box < 4 ? 128 * box : kRopeOff, g0, g1, g2, g3, &bars[kBarOpFull + ob]);
+      }
+      if (lane < 16) {
+        const int r = 16 * lw + lane;
+        const uint8_t* src = slot >= 0 ? p.cache + (int64_t)slot * kRowBytes + kScaleOff : p.cache;
+        cp_async_16_zfill(op + kOpScale + (uint32_t)((r >> 2) * 128 + (r & 3) * 16), src, slot >= 0 ? 16u : 0u);
+        cp_async_mbar_arrive_noinc(&bars[kBarOpFull + ob]);
       }
       if (lane == 0 && lw == 0) SMLA_TRACE_SET(tl, kEvIssue);
       last_ob = ob;
@@ -947,23 +964,18 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// Tensor maps of the cache viewed as a 2-D byte array [NB * 64 rows, 656
-// bytes]: 128-byte boxes with the 128-byte swizzle (code and RoPE panels)
-// and 16-byte boxes without swizzle (scales).  Rows outside [0, NB * 64)
-// read as zeros.
-cudaError_t make_cache_maps(const uint8_t* cache, int64_t NB, CUtensorMap* panel_map, CUtensorMap* scale_map) {
+// Tensor map of the cache viewed as a 2-D byte array [NB * 64 rows, 656
+// bytes]: 128-byte boxes with the 128-byte swizzle (code and RoPE panels).
+// Rows outside [0, NB * 64) read as zeros.
+cudaError_t make_cache_map(const uint8_t* cache, int64_t NB, CUtensorMap* panel_map) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return cudaErrorNotSupported;
   const cuuint64_t gdim[2] = {(cuuint64_t)kRowBytes, (cuuint64_t)(NB * kBlock)};
   const cuuint64_t gstride[1] = {(cuuint64_t)kRowBytes};
-  const cuuint32_t box_panel[2] = {128, 1}, box_scale[2] = {16, 1}, es[2] = {1, 1};
-  CUresult r = enc(panel_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(cache), gdim, gstride, box_panel, es,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
-  r = enc(scale_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(cache), gdim, gstride, box_scale, es,
-          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  const cuuint32_t box_panel[2] = {128, 1}, es[2] = {1, 1};
+  const CUresult r = enc(panel_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(cache), gdim, gstride,
+                         box_panel, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
@@ -1027,8 +1039,8 @@ cudaError_t launch_decode_fp8(const AttnArgs& a, const AttnPlan& plan, cudaStrea
   p.nt = plan.nt;
   p.total = plan.total;
   p.G = plan.G;
-  CUtensorMap panel_map, scale_map;
-  cudaError_t em = make_cache_maps(a.cache, a.NB, &panel_map, &scale_map);
+  CUtensorMap panel_map;
+  cudaError_t em = make_cache_map(a.cache, a.NB, &panel_map);
   if (em != cudaSuccess) return em;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)plan.G, 1, 1);
@@ -1040,7 +1052,7 @@ cudaError_t launch_decode_fp8(const AttnArgs& a, const AttnPlan& plan, cudaStrea
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, sparse_mla_decode_fp8_kernel, p, panel_map, scale_map);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, sparse_mla_decode_fp8_kernel, p, panel_map);
   if (e != cudaSuccess) return e;
   e = cudaGetLastError();
   if (e != cudaSuccess || !plan.need_combine) return e;
