@@ -52,9 +52,9 @@ TRAFFIC_BY_SOURCE = {
 # out the Q preparation and the combine).
 WIDE_TRAFFIC_SOURCES = ("smla_wide.cu", "smla_combine.cuh", "smla_common.cuh", "sm103_ptx.cuh")
 WIDE_TRAFFIC_BY_SOURCE = {
-    ("19629da18520f8de", "prefill_h128_k2048"): (671_053_056 + 524_675_840 + 38_473_472 + 210_944,
+    ("71d5b8755a8edd55", "prefill_h128_k2048"): (671_053_056 + 524_675_840 + 38_473_472 + 210_944,
                                                  "attention kernel + combine"),
-    ("19629da18520f8de", "decode_h128_k2048"): (231_825_408 + 23_199_232, "attention kernel only"),
+    ("71d5b8755a8edd55", "decode_h128_k2048"): (231_825_408 + 23_199_232, "attention kernel only"),
 }
 
 

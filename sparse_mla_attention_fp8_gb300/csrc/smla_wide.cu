@@ -20,10 +20,11 @@
 // swizzle), so both CTAs do the same QK^T work.  Per 64-row tile:
 //   * QK^T partial: S_c = Q[:, F_c] kv[rows, F_c]^T, M = 128 heads, N = 64
 //     rows, K = the CTA's panels (tcgen05.mma kind::f16, fp32 in TMEM);
-//   * the two fp32 partials are exchanged through distributed shared memory
-//     (each softmax thread sends its head's 64 partial logits to the peer with
-//     st.async, whose bytes complete the peer's barrier), so both CTAs hold
-//     the same S = S_0 + S_1 and take identical softmax decisions;
+//   * the two partials are exchanged through distributed shared memory (each
+//     exchange thread sends its head's 32 partial logits of a half tile to the
+//     peer as 16-bit fixed point with st.async, whose bytes complete the
+//     peer's barrier), and each CTA adds the peer's to its own: S = S_0 + S_1
+//     up to 2^-16 of the largest partial of the head's half tile;
 //   * softmax, one thread per head (the head's TMEM lane): online max and sum
 //     in the log2 domain with lazy rescaling of O, P in bf16 written back to
 //     TMEM;
