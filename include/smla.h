@@ -60,7 +60,13 @@ extern "C" {
  *                    bytes, 256-byte aligned; NULL = a buffer cached by the library per device
  *                    (allocated on first use, so that call is not graph-capturable)
  * A slot is invalid (masked) when the index is negative, its block id is >= MB, the request id is
- * outside [0, R) or the physical block is outside [0, NB). */
+ * outside [0, R) or the physical block is outside [0, NB).
+ * Launch order: for H < 128 the decode kernel is a programmatic dependent of the preceding kernel on
+ * `stream`.  If that kernel signals its dependents early (this library's mla_cache_store_fp8 and
+ * attention kernels do; ordinary kernels do not), the decode's index translation and Q split may read
+ * q, indices, block_table and req_id_per_token before it has finished.  Everything that reads kv_cache
+ * or writes out, lse or the workspace waits for it.  So write those four inputs with other kernels,
+ * not with a kernel of this library launched directly before the call. */
 int sparse_mla_decode_fp8(const void* q, const uint8_t* kv_cache, const int32_t* indices,
                           const int32_t* block_table, const int32_t* req_id_per_token, float sm_scale,
                           int num_splits, void* out, float* lse, int T, int H, int K, int R, int MB, int NB,
