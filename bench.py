@@ -470,7 +470,7 @@ def run_tensor_workload(args):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device).view(torch.bfloat16)
 
     if args.workload == "decode_h128_k2048":
-        case = inp.rotating_decode(seed=2, R=128, ctx_lo=65536, ctx_hi=65536, K=2048, H=128, outliers=False)
+        case = inp.rotating_decode(seed=2, R=128, ctx_lo=65536, ctx_hi=65536, K=2048, H=128, outliers=True)
         T, H, K, NB = case.q.shape[0], case.H, case.K, case.num_blocks
         with torch.cuda.stream(stream):
             cache = torch.zeros((NB, 64, 656), dtype=torch.uint8, device=device)

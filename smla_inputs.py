@@ -204,8 +204,11 @@ def memory_bound_decode(seed: int = 1, R: int = 64, ctx_lo: int = 8192, ctx_hi: 
 
 
 def tensor_bound_decode(seed: int = 2, R: int = 128, ctx: int = 65536, K: int = 2048, H: int = 128) -> DecodeCase:
-    """R requests x 1 token, H=128, top-k 2048, context 65536 each."""
-    return _decode_case(f"decode_h{H}_k{K}_r{R}", seed + 1000, np.full(R, ctx), np.ones(R, np.int64), H, K)
+    """R requests x 1 token, H=128, top-k 2048, context 65536 each, with the
+    memory-bound workload's cache distribution (latent N(0,1) with 1% of the
+    channels scaled x8)."""
+    return _decode_case(f"decode_h{H}_k{K}_r{R}", seed + 1000, np.full(R, ctx), np.ones(R, np.int64), H, K,
+                        outliers=True)
 
 
 def mixed_batch(seed: int = 4, n_decode: int = 32, decode_qlen: int = 2, n_prefill: int = 2,

@@ -23,12 +23,13 @@
 //    tiles, so that the loads of the next tiles are in flight while one is
 //    in use.
 //  * Q is split once per (token, 16-head group) into two e4m3 terms,
-//    q * 2^s_h = hi + lo (s_h a per-head power of two putting max |q| near
-//    448), exact for all but negligibly small components; hi and lo are the
-//    two halves of an N = 32 operand.  QK^T for each 128-column scale group g
-//    is one kind::f8f6f4 product E_g [Q_hi Q_lo]^T (M = 64 rows, N = 32,
-//    K = 128 codes), the RoPE part a bf16 product; the softmax combines
-//    s = 2^-s_h sum_g scale_g (S_g,hi + S_g,lo) + S_rope in fp32.
+//    q * 2^s_hg = hi + lo (s_hg a power of two per head and 128-column scale
+//    group g putting the group's max |q| near 448), exact for all but
+//    components far below their group's largest; hi and lo are the two halves
+//    of an N = 32 operand.  QK^T for each scale group g is one kind::f8f6f4
+//    product E_g [Q_hi Q_lo]^T (M = 64 rows, N = 32, K = 128 codes), the RoPE
+//    part a bf16 product; the softmax combines
+//    s = sum_g scale_g 2^-s_hg (S_g,hi + S_g,lo) + S_rope in fp32.
 //  * P.V for value chunk q (= scale group q) is one kind::f8f6f4 product
 //    O_q^T += E_q^T P'_q with the same code panel read MN-major and
 //    P'_q = 2^7 p * scale_q / R_q split into e4m3 hi + lo (R_q a running
@@ -125,8 +126,8 @@ constexpr int kOffP = kOffQ + kQBuf;
 constexpr int kPBufs = 3;                                           // P' buffers
 constexpr int kOffSlots = kOffP + kPBufs * kPBuf;                   // int32 [4][64]
 constexpr int kOffValid = kOffSlots + 4 * kRows * 4;                // uint8 [4][64]
-constexpr int kOffPre = kOffValid + kOpBufs * kRows;                // float [4][16 columns] inverse Q prescales
-constexpr int kOffRedMax = kOffPre + 4 * HG * 4;                    // float [2][4 quarters][16 columns]
+constexpr int kOffPre = kOffValid + kOpBufs * kRows;                // float [4][4 groups][16 columns] inverse Q prescales
+constexpr int kOffRedMax = kOffPre + 4 * 4 * HG * 4;                    // float [2][4 quarters][16 columns]
 constexpr int kOffRedSc = kOffRedMax + 2 * 4 * HG * 4;              // float [2][2 halves][4 quarters][4]
 constexpr int kOffRedSum = kOffRedSc + 2 * 2 * 4 * 4 * 4;           // float [4 quarters][16 columns]
 constexpr int kOffBar = kOffRedSum + 4 * HG * 4;
@@ -426,7 +427,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // 4 threads per head: thread part owns NoPE columns [128 part, 128 part +
     // 128) (code panel `part`) and RoPE chunks 2 part, 2 part + 1.  Head h is
     // stored in operand row n = q_row_of_head(h) (hi) and 16 + n (lo).
-    // q * 2^s_h = hi + lo in e4m3 with s_h chosen so that max |q * 2^s_h| <= 448.
+    // q * 2^s_hg = hi + lo in e4m3 with s_hg chosen so that the largest
+    // |q * 2^s_hg| over the thread's 128 columns (scale group g = part) is at
+    // most 448.
     // One Q buffer: the next segment's q is loaded into registers while the
     // current one is in use, and converted once the buffer is released.
     const int qt = tid - 32 * kQWarp0;  // 0..63
@@ -453,8 +456,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int k = 0; k < 4; ++k)
           amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w4[k] << 16)), fabsf(__uint_as_float(w4[k] & 0xFFFF0000u))));
       }
-      amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 1));
-      amax = fmaxf(amax, __shfl_xor_sync(kFullMask, amax, 2));
+      // one prescale per (head, scale group): the group's own largest |q| sets it
       int sh = 0;
       if (amax > 0.f) {
         int e;
@@ -482,7 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t qrope = smem_u32(smem + kOffQ + kQRope);
       sts128(qrope + sw128_chunk(HG, qrow, 2 * part), rope0);
       sts128(qrope + sw128_chunk(HG, qrow, 2 * part + 1), rope1);
-      if (part == 0) pre_ring[(seg & 3) * HG + qrow] = ldexpf(1.f, -sh);
+      pre_ring[((seg & 3) * 4 + part) * HG + qrow] = ldexpf(1.f, -sh);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[kBarQFull]);
@@ -631,7 +633,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* red_max = reinterpret_cast<float*>(smem + kOffRedMax);
     float* red_sc = reinterpret_cast<float*>(smem + kOffRedSc);
     float* red_sum = reinterpret_cast<float*>(smem + kOffRedSum);
-    float m2[2], l2[2], ip2[2], Rq[4];
+    float m2[2], l2[2], ip2[4][2], Rq[4];
     SMLA_CLK_DECL;
     int seg = -1, seg_first_kt = 0, n_seg_tiles = 0;
     bool dead = false;
@@ -677,9 +679,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       SMLA_CLK_START();
       tc_fence_after();
       if (ti.seg_start) {
-        const float2 v = *reinterpret_cast<const float2*>(pre_ring + (seg & 3) * HG + nA);
-        ip2[0] = v.x;
-        ip2[1] = v.y;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const float2 v = *reinterpret_cast<const float2*>(pre_ring + ((seg & 3) * 4 + g) * HG + nA);
+          ip2[g][0] = v.x;
+          ip2[g][1] = v.y;
+        }
       }
       const bool ok0 = !dead && valid[ob * kRows + r0] != 0;
       const bool ok1 = !dead && valid[ob * kRows + r1] != 0;
@@ -689,7 +694,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float4 s1 = ok1 ? *reinterpret_cast<const float4*>(scl + (r1 >> 2) * 128 + (r1 & 3) * 16) : zero4;
       const float sc0[4] = {s0.x, s0.y, s0.z, s0.w};
       const float sc1[4] = {s1.x, s1.y, s1.z, s1.w};
-      // logits (log2 units): 2^-s_h sum_g scale_g (S_g,hi + S_g,lo) + S_rope
+      // logits (log2 units): sum_g scale_g 2^-s_hg (S_g,hi + S_g,lo) + S_rope
       float sl[4];
       {
         const uint32_t sa = tmem + lane_base + sbuf * kSCols + 8 * hh;
@@ -717,9 +722,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int g = 0; g < 4; ++g)
 #pragma unroll
             for (int k = 0; k < 4; ++k)
-              acc[k] = fmaf((k >> 1) ? sc1[g] : sc0[g], __uint_as_float(hi[g][k]) + __uint_as_float(lo[g][k]), acc[k]);
+              acc[k] = fmaf(((k >> 1) ? sc1[g] : sc0[g]) * ip2[g][k & 1],
+                            __uint_as_float(hi[g][k]) + __uint_as_float(lo[g][k]), acc[k]);
 #pragma unroll
-          for (int k = 0; k < 4; ++k) acc[k] = fmaf(acc[k], ip2[k & 1], __uint_as_float(rp[k]));
+          for (int k = 0; k < 4; ++k) acc[k] += __uint_as_float(rp[k]);
         } else if (lane == 0) {
           mbar_arrive(&bars[kBarSFree + sbuf]);
         }

@@ -97,7 +97,9 @@ struct Lay {
   static constexpr int kOffSlots = kOffX + 2 * kXSlot;            // int32 [4][64]
   static constexpr int kOffValid = kOffSlots + 4 * kRows * 4;      // uint8 [kKBufs][64]
   static constexpr int kOffRed = kOffValid + kKBufs * kRows;       // float [kSBufs][2 halves][128]: maxima (log2)
-  static constexpr int kOffBar = kOffRed + kSBufs * 2 * kHeads * 4;
+  static constexpr int kOffExp = kOffRed + kSBufs * 2 * kHeads * 4;  // int [kKBufs][4 quarters] (FP8 rows)
+  static constexpr int kOffFac = kOffExp + kKBufs * 4 * 4;          // uint4 [loader][32] conversion factors (FP8 rows)
+  static constexpr int kOffBar = kOffFac + (kFp8 ? kLoaders * 32 * 16 : 0);
   enum {
     kBarKFull = 0, kBarKEmpty = kBarKFull + kKBufs, kBarSFull = kBarKEmpty + kKBufs, kBarSReady = kBarSFull + kSBufs,
     kBarSFree = kBarSReady + kSBufs, kBarPFull = kBarSFree + kSBufs, kBarPDone = kBarPFull + 2,
@@ -180,6 +182,30 @@ __device__ __forceinline__ void st_async_b32(uint32_t addr, uint32_t a, uint32_t
   asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(addr), "r"(a),
                "r"(bar)
                : "memory");
+}
+
+// 2^e for an integer e in [-127, 127] (-127 gives 0).
+__device__ __forceinline__ float exp2i(int e) { return __uint_as_float((uint32_t)(e + 127) << 23); }
+
+// FP8 rows: exponent E of a 16-row quarter of a tile.  Its codes become f16
+// values code * scale * 2^-E, and its RoPE values bf16 values RoPE * 2^-E;
+// the logits and P take 2^E back in fp32.  E = floor(log2(largest scale of
+// the quarter's four groups)) - 6 puts that scale in [64, 128), so every
+// product stays below 448 * 128 < 65504 (the f16 maximum) and the quarter's
+// large values are normal f16 numbers.  E is raised where needed so that the
+// RoPE values times 2^-E stay below 2^101, and clamped to [-120, 120].
+// smax = largest scale, rbits = largest |RoPE| as bf16 bits (0 = none).
+__device__ __forceinline__ int quarter_exponent(float smax, uint32_t rbits) {
+  int e = smax > 0.f ? (int)((__float_as_uint(smax) >> 23) & 0xFFu) - 127 - 6 : -1000;
+  if (rbits != 0u) e = max(e, (int)((rbits >> 7) & 0xFFu) - 127 - 100);
+  if (e == -1000) e = 0;  // nothing but zeros
+  return min(max(e, -120), 120);
+}
+
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
 }
 
 __device__ __forceinline__ TileInfo tile_info(const Params& p, int64_t x, int64_t xbeg, int64_t xend) {
@@ -316,11 +342,13 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
     // 4 lw + 3).  Two tiles ahead it gathers their codes (the CTA's two scale
     // groups), scales and RoPE halves into a staging slot, lane 4 g + b
     // issuing copy b of group g; when an operand tile is free it converts the
-    // staged codes to f16 (the exact e4m3 widening times the scale rounded to
-    // f16, one f16 product: relative error below 2^-11), lane l handling
-    // codes 8 l .. 8 l + 7 of each row, and copies the RoPE halves (bf16) into
-    // the tile's 64-byte-swizzled panel.  Nothing on the way from a free tile
-    // to a full one waits for a copy from global memory.
+    // staged codes to f16 values code * scale * 2^-E with one rounding
+    // (relative error at most 2^-11 plus a few units of 2^-22; E is the
+    // quarter's exponent, which keeps every value inside f16's range whatever
+    // the scales), lane l handling codes 8 l .. 8 l + 7 of each row, and copies
+    // the RoPE halves (bf16, times 2^-E) into the tile's 64-byte-swizzled
+    // panel.  Nothing on the way from a free tile to a full one waits for a
+    // copy from global memory.
     const int lw = warp - kLoadWarp0;
     uint8_t* raw_base = smem + L::kOffRaw;
     const int rgrp = lane >> 2, rbox = lane & 3;
@@ -360,45 +388,110 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
       if (lane == 0) mbar_arrive(&bars[L::kBarIdxEmpty + b4]);
       if (!SMLA_WAIT(L::kBarRawFull + 2 * lw + sl, (tl >> 1) & 1)) break;
       if (lane == 0 && lw == 0) WIDE_TRACE(tl, kEvRawFull);
-      if (use >= 1 && !SMLA_WAIT(L::kBarKEmpty + kb, (use + 1) & 1)) break;
-      if (lane == 0 && lw == 0) WIDE_TRACE(tl, kEvKEmpty);
-      if (lane < 16) valid[kb * kRows + 16 * lw + lane] = (uint8_t)((vmask >> lane) & 1u);
-      const uint32_t tile = smem_u32(smem + L::kOffK + kb * kKBuf);
       const uint8_t* raw = raw_base + sl * kRawBuf;
-      const int half = lane >> 4, pnl = lane >> 3, ch = lane & 7;
-      // RoPE halves: 16 rows x 4 chunks of 16 bytes, two per lane, into the
-      // 64-byte swizzle (chunk j of row r at j ^ ((r >> 1) & 3) in its 64 bytes)
+      // the quarter's exponent E from its rows' four scales and RoPE values
+      // (staged; the same bytes in both CTAs of the pair, so both take the same E)
+      uint4 rv[2];
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
         const int k = lane + 32 * i, r = 16 * lw + (k >> 2), j = k & 3;
-        const uint4 v = *reinterpret_cast<const uint4*>(raw + (r >> 2) * kRawGroup + kRawRope + (r & 3) * 64 + 16 * j);
-        st_shared_v4(tile + 4 * kPanel + (uint32_t)((r >> 3) * 512 + (r & 7) * 64 + ((j ^ ((r >> 1) & 3)) << 4)), v.x,
-                     v.y, v.z, v.w);
+        rv[i] = *reinterpret_cast<const uint4*>(raw + (r >> 2) * kRawGroup + kRawRope + (r & 3) * 64 + 16 * j);
+      }
+      int q_exp;
+      {
+        float smax = 0.f;
+        if (lane < 16) {
+          const int r = 16 * lw + lane;
+          const float4 s4 = *reinterpret_cast<const float4*>(raw + (r >> 2) * kRawGroup + 1024 + (r & 3) * 16);
+          smax = fmaxf(fmaxf(s4.x, s4.y), fmaxf(s4.z, s4.w));
+        }
+        // |bf16| orders as its bits with the sign cleared
+        uint32_t rb = 0u;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const uint32_t w[4] = {rv[i].x, rv[i].y, rv[i].z, rv[i].w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) rb = max(rb, max(w[k] & 0x7FFFu, (w[k] >> 16) & 0x7FFFu));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          smax = fmaxf(smax, __shfl_xor_sync(kFullMask, smax, o));
+          rb = max(rb, __shfl_xor_sync(kFullMask, rb, o));
+        }
+        q_exp = quarter_exponent(smax, rb);
+      }
+      const float q_fac = exp2i(-q_exp);                                    // 2^-E (exact)
+      const uint32_t q_fac_bf2 = (uint32_t)(127 - q_exp) * 0x00800080u;     // 2^-E as a bf16 pair
+      // conversion factors of row 16 lw + (lane & 15), scale group 2 c + (lane >> 4):
+      // s = scale * 2^-E (exact) is brought to t = s * 2^m in [1, 2) when
+      // 0 < s < 1 (m <= 24) and split as t_hi = f16(t), t_lo = f16(t - t_hi)
+      uint4* fac = reinterpret_cast<uint4*>(smem + L::kOffFac) + 32 * lw;
+      bool all_m0;
+      {
+        const int r = 16 * lw + (lane & 15);
+        const float sq =
+            *reinterpret_cast<const float*>(raw + (r >> 2) * kRawGroup + 1024 + (r & 3) * 16 + 4 * (2 * c + (lane >> 4))) *
+            q_fac;
+        const int m = (sq < 1.f && sq > 0.f) ? min(127 - (int)((__float_as_uint(sq) >> 23) & 0xFFu), 24) : 0;
+        const float t = sq * exp2i(m);
+        const __half t_hi = __float2half_rn(t);
+        const __half t_lo = __float2half_rn(t - __half2float(t_hi));
+        // 2^-m as f16 (subnormal below 2^-14)
+        const uint32_t sh = m <= 14 ? (uint32_t)(15 - m) << 10 : 1u << (24 - m);
+        __syncwarp();  // the previous tile's factors have been read
+        fac[lane] = make_uint4((uint32_t)__half_as_ushort(t_hi) * 0x00010001u,
+                               (uint32_t)__half_as_ushort(t_lo) * 0x00010001u, sh * 0x00010001u, 0u);
+        all_m0 = __all_sync(kFullMask, m == 0);
+        __syncwarp();
+      }
+      if (use >= 1 && !SMLA_WAIT(L::kBarKEmpty + kb, (use + 1) & 1)) break;
+      if (lane == 0 && lw == 0) WIDE_TRACE(tl, kEvKEmpty);
+      if (lane < 16) valid[kb * kRows + 16 * lw + lane] = (uint8_t)((vmask >> lane) & 1u);
+      if (lane == 0) reinterpret_cast<int*>(smem + L::kOffExp)[kb * 4 + lw] = q_exp;
+      const uint32_t tile = smem_u32(smem + L::kOffK + kb * kKBuf);
+      const int half = lane >> 4, pnl = lane >> 3, ch = lane & 7;
+      // RoPE halves times 2^-E (exact): 16 rows x 4 chunks of 16 bytes, two per
+      // lane, into the 64-byte swizzle (chunk j of row r at j ^ ((r >> 1) & 3)
+      // in its 64 bytes)
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int k = lane + 32 * i, r = 16 * lw + (k >> 2), j = k & 3;
+        st_shared_v4(tile + 4 * kPanel + (uint32_t)((r >> 3) * 512 + (r & 7) * 64 + ((j ^ ((r >> 1) & 3)) << 4)),
+                     mul_bf16x2(rv[i].x, q_fac_bf2), mul_bf16x2(rv[i].y, q_fac_bf2), mul_bf16x2(rv[i].z, q_fac_bf2),
+                     mul_bf16x2(rv[i].w, q_fac_bf2));
       }
       // 4 rows at a time: all their loads first, so that one load latency
-      // covers 4 rows (the stores are ordered after them)
+      // covers 4 rows (the stores are ordered after them).  code * scale * 2^-E
+      // in f16x2 with one rounding where the result is a normal f16:
+      // fma(code, t_hi, code * t_lo) * 2^-m (the codes widen to f16 exactly;
+      // the last product is exact unless its result is subnormal, and is
+      // skipped when m = 0 for every row and group of the quarter).
 #pragma unroll 1
       for (int rb = 0; rb < 16; rb += 4) {
         uint2 cw[4];
-        float sc[4];
+        uint4 f4[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int r = 16 * lw + rb + i;
           const uint8_t* grp = raw + (r >> 2) * kRawGroup;
           cw[i] = *reinterpret_cast<const uint2*>(grp + 512 * half + (r & 3) * 128 + 8 * (lane & 15));
-          sc[i] = *reinterpret_cast<const float*>(grp + 1024 + (r & 3) * 16 + 4 * (2 * c + half));
+          f4[i] = fac[rb + i + 16 * half];
         }
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int r = 16 * lw + rb + i;
-          const uint32_t sc2 = pack_f16x2(sc[i], sc[i]);
           uint32_t o[4];
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const uint16_t pr = (uint16_t)(((k < 2 ? cw[i].x : cw[i].y) >> (16 * (k & 1))) & 0xFFFFu);
-            uint32_t h2;
+            uint32_t h2, t2;
             asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(pr));  // exact
-            asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(o[k]) : "r"(h2), "r"(sc2));
+            asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(t2) : "r"(h2), "r"(f4[i].y));
+            asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(o[k]) : "r"(h2), "r"(f4[i].x), "r"(t2));
+          }
+          if (!all_m0) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(o[k]) : "r"(o[k]), "r"(f4[i].z));
           }
           st_shared_v4(tile + pnl * kPanel + (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((ch ^ (r & 7)) << 4)), o[0],
                        o[1], o[2], o[3]);
@@ -607,6 +700,17 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
             }
           }
         }
+        // FP8 rows: the half's two quarters hold logits times 2^-E0 and
+        // 2^-E1; both are brought to 2^-max(E0, E1) (the same in both CTAs),
+        // and the scale to the log2 domain takes 2^max(E0, E1) back
+        float qf0 = 1.f, qf1 = 1.f, sl2t = sl2;
+        if constexpr (kFp8) {
+          const int* qe = reinterpret_cast<const int*>(smem + L::kOffExp) + kb * 4 + 2 * e;
+          const int e0 = qe[0], e1 = qe[1], eh = max(e0, e1);
+          qf0 = exp2i(max(e0 - eh, -127));
+          qf1 = exp2i(max(e1 - eh, -127));
+          sl2t = sl2 * exp2i(eh);
+        }
         if (!dead) dead = !SMLA_WAIT(L::kBarSFull + sb, (tl / kSBufs) & 1);
         if (tid == 32 * kXchgWarp0) WIDE_TRACE(tl, kEvSFull);
         tc_fence_after();
@@ -626,6 +730,13 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
             for (int j = 0; j < 16; ++j) {
               s[j] = __uint_as_float(r0[j]);
               s[16 + j] = __uint_as_float(r1[j]);
+            }
+            if (kFp8 && (qf0 != 1.f || qf1 != 1.f)) {  // uniform: the tile's exponents
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                s[j] *= qf0;
+                s[16 + j] *= qf1;
+              }
             }
           }
           // 16-bit fixed point relative to the largest magnitude
@@ -675,7 +786,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
           uint32_t r[2][16];
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            const float x = (vb >> j) & 1u ? s[j] * sl2 : -INFINITY;
+            const float x = (vb >> j) & 1u ? s[j] * sl2t : -INFINITY;
             mt = fmaxf(mt, x);
             r[j >> 4][j & 15] = __float_as_uint(x);
           }
@@ -693,6 +804,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
       // ---------------------------------------------------------- softmax + epilogue (warps 0..3)
       float m_used = -INFINITY, l_sum = 0.f;
       int n_seg_tiles = 0;
+      int e_run = 0;  // FP8 rows: O holds sum_j p_j V_j * 2^-e_run
       bool dead = false;
       int u = (int)(xbeg / p.nt), kt = (int)(xbeg - (int64_t)u * p.nt);
       for (int tl = 0; tl < n_local; ++tl) {
@@ -712,9 +824,39 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
         // O already holds earlier tiles of the segment its row is scaled by
         // a = 2^(m_used - m_new).
         const bool need = mt > m_used + kMaxSlack || (m_used == -INFINITY && mt > -INFINITY);
-        const bool scale_o = need && n_seg_tiles > 0 && m_used > -INFINITY;
-        const float a = scale_o ? ex2_approx(m_used - mt) : 1.f;
+        const bool scale_m = need && n_seg_tiles > 0 && m_used > -INFINITY;
+        const float dm = scale_m ? m_used - mt : 0.f;
         if (need) m_used = mt;
+        // FP8 rows: quarter q of the tile carries V * 2^-E_q.  O stays in units
+        // of 2^e_run, raised (O rescaled) when a tile's largest E_q exceeds it
+        // by more than 7, so that P' = p * 2^(E_q - e_run) <= 2^8 * 2^7 stays
+        // inside f16.  P' is formed as 2^(logit - mu_q) with
+        // mu_q = m_used - (E_q - e_run) (the shift floored at -64, where P'
+        // weighs less than 2^-40 of the largest value O can hold), and the row
+        // sum takes the shift back.
+        bool e_up = false;
+        float de = 0.f, mu_q[4] = {m_used, m_used, m_used, m_used}, w_q[4] = {1.f, 1.f, 1.f, 1.f};
+        if constexpr (kFp8) {
+          const int* qe = reinterpret_cast<const int*>(smem + L::kOffExp) + (tl % L::kKBufs) * 4;
+          const int eq[4] = {qe[0], qe[1], qe[2], qe[3]};
+          const int emax = max(max(eq[0], eq[1]), max(eq[2], eq[3]));
+          if (seg_start) {
+            e_run = emax;
+          } else if (emax > e_run + 7) {
+            de = (float)(e_run - emax);
+            e_run = emax;
+            e_up = true;
+          }
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int d = max(eq[q] - e_run, -64);
+            mu_q[q] = m_used - (float)d;
+            w_q[q] = exp2i(-d);
+          }
+        }
+        const bool scale_o = scale_m || e_up;
+        const float a_l = scale_m ? ex2_approx(dm) : 1.f;        // row sums
+        const float a = scale_o ? ex2_approx(dm + de) : 1.f;     // O
         // TMEM access is warp-wide: a warp with any head to rescale runs the
         // pass (factor 1 for its other heads), once P.V(tl - 1) has landed in O
         if (__any_sync(kFullMask, scale_o)) {
@@ -745,23 +887,24 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
           reg_fence16(r1);
           uint32_t pk[16];
           float l0 = 0.f, l1 = 0.f;
+          const float mu0 = mu_q[2 * e], mu1 = mu_q[2 * e + 1];  // r0: quarter 2e, r1: quarter 2e + 1
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            const float p0 = none ? 0.f : ex2_approx(__uint_as_float(r0[2 * j]) - m_used);
-            const float p1 = none ? 0.f : ex2_approx(__uint_as_float(r0[2 * j + 1]) - m_used);
-            const float p2 = none ? 0.f : ex2_approx(__uint_as_float(r1[2 * j]) - m_used);
-            const float p3 = none ? 0.f : ex2_approx(__uint_as_float(r1[2 * j + 1]) - m_used);
-            l0 += p0 + p2;
-            l1 += p1 + p3;
+            const float p0 = none ? 0.f : ex2_approx(__uint_as_float(r0[2 * j]) - mu0);
+            const float p1 = none ? 0.f : ex2_approx(__uint_as_float(r0[2 * j + 1]) - mu0);
+            const float p2 = none ? 0.f : ex2_approx(__uint_as_float(r1[2 * j]) - mu1);
+            const float p3 = none ? 0.f : ex2_approx(__uint_as_float(r1[2 * j + 1]) - mu1);
+            l0 += p0 + p1;
+            l1 += p2 + p3;
             pk[j] = kFp8 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
             pk[8 + j] = kFp8 ? pack_f16x2(p2, p3) : pack_bf16x2(p2, p3);
           }
-          lt += l0 + l1;
+          lt += l0 * w_q[2 * e] + l1 * w_q[2 * e + 1];
           tmem_st16(tmem + lane_base + kPCol + 32 * pb + 16 * e, pk);
         }
         tc_fence_before();
         mbar_arrive(&bars[L::kBarSFree + sb]);
-        l_sum = l_sum * a + lt;
+        l_sum = l_sum * a_l + lt;
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&bars[L::kBarPFull + pb]);
@@ -772,7 +915,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
           if (!dead) dead = !SMLA_WAIT(L::kBarPDone + pb, (tl >> 1) & 1);
           tc_fence_after();
           const bool full_unit = n_seg_tiles == p.nt;  // the whole token ran in this pair
-          const float inv = l_sum > 0.f ? 1.f / l_sum : 0.f;
+          const float inv = l_sum > 0.f ? (kFp8 ? exp2i(e_run) : 1.f) / l_sum : 0.f;
           const int64_t slot = (int64_t)pair + u;
           for (int q = 0; q < 256 / 16; ++q) {
             uint32_t r[16];
