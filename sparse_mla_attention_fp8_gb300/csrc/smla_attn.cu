@@ -1,15 +1,15 @@
-// Sparse MLA attention on sm_103a: FP8 decode over the paged 656-byte cache
-// and BF16 prefill over a dense [N, 576] latent buffer.
+// BF16 sparse MLA prefill on sm_103a for head counts other than 128 (heads in
+// groups of 16 or 32), over a dense [N, 576] bf16 latent buffer.
 //
-// What is computed (vLLM flashmla_sparse.py, FlashMLASparseImpl.forward and
-// its FlashMLA kernel calls): every query token t attends with each of its H
-// heads to its own K top-k latent rows (MQA 576/512: all heads share the
-// rows; V is the 512-wide NoPE part of each row).  Per head h:
+// What is computed (vLLM flashmla_sparse.py, FlashMLASparseImpl.forward on
+// the prefill path, flash_mla_sparse_prefill): every query token t attends
+// with each of its H heads to its own K top-k latent rows (MQA 576/512: all
+// heads share the rows; V is the 512-wide NoPE part of each row).  Per head h:
 //   s_j   = softmax_scale * <q[t,h,:], row_j>        (576-wide)
 //   out   = sum_j softmax(s)_j * row_j[0:512]         (bf16 [T, H, 512])
 //   lse   = log(sum_j exp(s_j))                       (fp32 [T, H])
-// Invalid indices (-1 after translation) are masked; a token with no valid
-// row gets out = 0 and lse = -inf.
+// Indices outside [0, N) are masked; a token with no valid row gets out = 0
+// and lse = -inf.
 //
 // Design (one persistent CTA per SM, warp-specialised, tcgen05 tensor cores):
 //  * Work units are (token, head group of HG heads); each unit is K/64 tiles
@@ -17,24 +17,21 @@
 //    contiguous ranges, so a unit may be split across CTAs ("segments"); a
 //    unit finished inside one CTA is written directly, the others go through
 //    an LSE-weighted combine kernel.
-//  * Index warp: translates tile row indices to cache slots into a 4-deep
-//    shared ring and (re)loads the unit's Q block into shared memory.
-//  * Converter warps: stream rows straight from HBM with 16-byte coalesced
-//    loads (a warp reads one 656-byte row per step, 6 rows in flight) and
-//    write the K-major, 128-byte-swizzled bf16 operand tile (two tiles are
-//    double-buffered).  The e4m3 codes are widened exactly (every e4m3 value
-//    is a bf16 value); the row's four float32 scales go to a side array.
-//  * MMA warp (one thread): S_g^T = E_g Q_g^T per 128-column scale group g
-//    (four accumulators) plus the RoPE part, with tcgen05.mma (M = 64 rows,
-//    N = HG heads); O^T += V^T P_q^T per 128-column value chunk q (M = 128,
+//  * Index warp: checks tile row indices into a 4-deep shared ring and
+//    (re)loads the unit's Q block into shared memory.
+//  * Converter warps: stream rows from memory with 16-byte coalesced loads (a
+//    warp reads one 1152-byte row per step, 4 rows in flight) and write the
+//    K-major, 128-byte-swizzled bf16 operand tile (two tiles are
+//    double-buffered).
+//  * MMA warp (one thread): S^T = K Q^T with tcgen05.mma (M = 64 rows, N = HG
+//    heads, K = 576); O^T += V^T P^T per 128-column value chunk (M = 128,
 //    N = HG, K = 64 rows), reading V straight from the same tile as an
 //    MN-major operand.  Accumulators live in tensor memory.
-//  * Softmax warpgroup (4 warps): s = sum_g scale_g * S_g + S_rope in fp32
-//    (so quantization scales never pass through bf16 on the logit path),
-//    online softmax with lazy rescaling of O (only when a running max grows
-//    by more than 2^8), P_q = p * scale_q written to shared memory as the B
-//    operand of chunk q (value chunk q is exactly scale group q), epilogue.
+//  * Softmax warpgroup (4 warps): online softmax with lazy rescaling of O
+//    (only when a running max grows by more than 2^8), P written to shared
+//    memory as the B operand of P.V, epilogue.
 #include <cstdint>
+#include <mutex>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -50,29 +47,7 @@ namespace {
 
 constexpr uint32_t kFull = 0xffffffffu;
 
-// Optional per-tile timeline for performance work: with SMLA_TRACE defined,
-// each role records %globaltimer at its hand-off points into g_smla_trace
-// (set by the host through smla_trace_set).  Compiled out otherwise.
-#ifdef SMLA_TRACE
-__device__ unsigned long long* g_smla_trace = nullptr;
-constexpr int kTraceTiles = 64, kTraceEvents = 8;
-enum { kEvIdx = 0, kEvConvStart = 1, kEvConvDone = 2, kEvQk = 3, kEvSoftStart = 4, kEvSoftDone = 5, kEvPv = 6,
-       kEvQLoaded = 7 };
-#define SMLA_TRACE_EV(tl, ev, op)                                                                       \
-  do {                                                                                                  \
-    if (g_smla_trace && (tl) < kTraceTiles) {                                                          \
-      unsigned long long* _p = g_smla_trace + ((size_t)blockIdx.x * kTraceTiles + (tl)) * kTraceEvents + (ev); \
-      op(_p, (unsigned long long)globaltimer_ns());                                                    \
-    }                                                                                                   \
-  } while (0)
-#define SMLA_TRACE_SET(tl, ev) SMLA_TRACE_EV(tl, ev, [](unsigned long long* a, unsigned long long v) { *a = v; })
-#define SMLA_TRACE_MAX(tl, ev) SMLA_TRACE_EV(tl, ev, atomicMax)
-#else
-#define SMLA_TRACE_SET(tl, ev) ((void)0)
-#define SMLA_TRACE_MAX(tl, ev) ((void)0)
-#endif
-
-template <int HG, bool kFp8>
+template <int HG>
 struct Cfg {
   static constexpr int kRows = 64;                       // top-k rows per tile
   static constexpr int kPanel = kRows * 128;             // one 64-column panel of the row tile
@@ -86,19 +61,16 @@ struct Cfg {
   static constexpr int kConvWarp0 = 6;
   static constexpr int kConvWarps = 10;
   static constexpr int kThreads = 32 * (kConvWarp0 + kConvWarps);
-  static constexpr int kDepth = kFp8 ? 6 : 4;            // rows in flight per converter warp
-  static constexpr int kNS = kFp8 ? 5 : 1;              // S^T accumulators per tile: 4 scale groups + RoPE
-  static constexpr int kNP = kFp8 ? 4 : 1;              // P^T operands per tile (one per value chunk)
-  static constexpr int kSCol = 0;                        // S^T buffers: columns [0, 2 * kNS * HG)
-  static constexpr int kOCol = 2 * kNS * HG;             // O^T: 4 chunks of HG columns
+  static constexpr int kDepth = 4;                       // rows in flight per converter warp
+  static constexpr int kSCol = 0;                        // S^T buffers: columns [0, 2 * HG)
+  static constexpr int kOCol = 2 * HG;                   // O^T: 4 chunks of HG columns
   static constexpr int kColsUsed = kOCol + 4 * HG;
   static constexpr int kTmemCols = kColsUsed <= 128 ? 128 : (kColsUsed <= 256 ? 256 : 512);
   // shared memory layout, offsets from a 1024-byte aligned base
   static constexpr int kOffKv = 0;
   static constexpr int kOffQ = kOffKv + 2 * kKvTile;
   static constexpr int kOffP = kOffQ + kQBufs * kQBytes;
-  static constexpr int kOffScale = kOffP + 2 * kNP * kPBytes;  // float [2][64][4] row scales
-  static constexpr int kOffSlots = kOffScale + 2 * kRows * 16;  // int32 [4][64]
+  static constexpr int kOffSlots = kOffP + 2 * kPBytes;  // int32 [4][64]
   static constexpr int kOffValid = kOffSlots + 4 * kRows * 4;  // uint8 [2][64]
   static constexpr int kOffRedMax = kOffValid + 2 * kRows;     // float [2][4][HG]
   static constexpr int kOffRedSum = kOffRedMax + 2 * 4 * HG * 4;  // float [4][HG]
@@ -118,19 +90,16 @@ struct Cfg {
 
 struct Params {
   const __nv_bfloat16* q;
-  const uint8_t* cache;
   const __nv_bfloat16* kv;
   const int32_t* indices;
-  const int32_t* block_table;
-  const int32_t* req_id;
   __nv_bfloat16* out;
   float* lse;
   float* part_o;
   float* part_lse;
   int* status;
   float scale_log2;
-  int T, H, K, R, MB;
-  int64_t NB;
+  int T, H, K;
+  int64_t N;
   int n_hg, nt;
   int64_t total;
   int G;
@@ -166,19 +135,6 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
                : "memory");
 }
 
-
-// 4 e4m3 codes (one 32-bit word, lowest byte first) -> 2 words of bf16x2
-// (lowest column in the low half).  Exact: every e4m3 value is a bf16 value.
-__device__ __forceinline__ void widen4(uint32_t w, uint32_t& o0, uint32_t& o1) {
-  uint32_t h01, h23;
-  const uint16_t lo = (uint16_t)(w & 0xFFFFu), hi = (uint16_t)(w >> 16);
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h01) : "h"(lo));
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h23) : "h"(hi));
-  const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
-  const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
-  o0 = pack_bf16x2(f01.x, f01.y);
-  o1 = pack_bf16x2(f23.x, f23.y);
-}
 
 // Reduce 16 values per lane across the 32 lanes of a warp.  On return every
 // lane holds the full reduction of value index (lane >> 1).
@@ -222,9 +178,9 @@ __device__ __forceinline__ float warp_reduce16(float (&v)[16], int lane) {
   return v[0];
 }
 
-template <int HG, bool kFp8>
-__global__ void __launch_bounds__(Cfg<HG, kFp8>::kThreads, 1) sparse_mla_attn_kernel(const __grid_constant__ Params p) {
-  using C = Cfg<HG, kFp8>;
+template <int HG>
+__global__ void __launch_bounds__(Cfg<HG>::kThreads, 1) sparse_mla_attn_kernel(const __grid_constant__ Params p) {
+  using C = Cfg<HG>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   grid_launch_dependents();  // the combine may be launched behind this grid right away
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -287,16 +243,11 @@ __global__ void __launch_bounds__(Cfg<HG, kFp8>::kThreads, 1) sparse_mla_attn_ke
         int32_t s = -1;
         if (k < p.K) {
           const int32_t idx = __ldg(p.indices + (int64_t)ti.t * p.K + k);
-          if constexpr (kFp8) {
-            s = translate_slot(idx, __ldg(p.req_id + ti.t), p.block_table, p.R, p.MB, p.NB);
-          } else {
-            s = (idx >= 0 && (int64_t)idx < p.NB) ? idx : -1;
-          }
+          s = (idx >= 0 && (int64_t)idx < p.N) ? idx : -1;
         }
         slots[r] = s;
       }
       mbar_arrive(&bars[C::kBarIdxFull + b4]);
-      if (lane == 0) SMLA_TRACE_SET(tl, kEvIdx);
       if (ti.seg_start) {
         const int qb = seg % C::kQBufs;
         if (seg >= C::kQBufs && !SMLA_WAIT(C::kBarQEmpty + qb, ((seg / C::kQBufs) - 1) & 1)) break;
@@ -310,7 +261,6 @@ __global__ void __launch_bounds__(Cfg<HG, kFp8>::kThreads, 1) sparse_mla_attn_ke
         cp_async_wait_all();
         fence_proxy_async_smem();
         mbar_arrive(&bars[C::kBarQFull + qb]);
-        if (lane == 0) SMLA_TRACE_SET(tl, kEvQLoaded);
         ++seg;
       }
     }
@@ -320,7 +270,7 @@ __global__ void __launch_bounds__(Cfg<HG, kFp8>::kThreads, 1) sparse_mla_attn_ke
     const int RW = (C::kRows - cw + C::kConvWarps - 1) / C::kConvWarps;  // rows of each tile handled here
     const int n_items = n_local * RW;
     struct Raw {
-      uint4 a, b, c;  // FP8: a = NoPE bytes, b = scales/RoPE (lanes 0..8); BF16: three 16-byte chunks
+      uint4 a, b, c;  // three 16-byte chunks of the row
       int32_t slot;
     };
     Raw buf[C::kDepth];
@@ -339,16 +289,10 @@ __global__ void __launch_bounds__(Cfg<HG, kFp8>::kThreads, 1) sparse_mla_attn_ke
       }
       rb.slot = slot;
       if (slot >= 0) {
-        if constexpr (kFp8) {
-          const uint8_t* row = p.cache + (int64_t)slot * kRowBytes;
-          rb.a = ld_stream(row + 16 * lane);
-          if (lane < 9) rb.b = ld_stream(row + kNope + 16 * lane);
-        } else {
-          const uint8_t* row = reinterpret_cast<const uint8_t*>(p.kv + (int64_t)slot * kDqk);
-          rb.a = ld_stream(row + 16 * lane);
-          rb.b = ld_stream(row + 16 * (lane + 32));
-          if (lane < 8) rb.c = ld_stream(row + 16 * (lane + 64));
-        }
+        const uint8_t* row = reinterpret_cast<const uint8_t*>(p.kv + (int64_t)slot * kDqk);
+        rb.a = ld_stream(row + 16 * lane);
+        rb.b = ld_stream(row + 16 * (lane + 32));
+        if (lane < 8) rb.c = ld_stream(row + 16 * (lane + 64));
       }
     };
 
@@ -357,45 +301,18 @@ __global__ void __launch_bounds__(Cfg<HG, kFp8>::kThreads, 1) sparse_mla_attn_ke
       const int r = cw + k * C::kConvWarps;
       const int b = tl & 1;
       if (k == 0 && tl >= 2) ok = ok && SMLA_WAIT(C::kBarKvEmpty + b, ((tl >> 1) + 1) & 1);
-      if (k == 0 && lane == 0 && cw == 0) SMLA_TRACE_SET(tl, kEvConvStart);
       if (!ok) return;
       const uint32_t tile = smem_u32(smem + C::kOffKv + b * C::kKvTile);
       const bool v = rb.slot >= 0;
-      if constexpr (kFp8) {
-        uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
-        if (v) {
-          widen4(rb.a.x, lo.x, lo.y);
-          widen4(rb.a.y, lo.z, lo.w);
-          widen4(rb.a.z, hi.x, hi.y);
-          widen4(rb.a.w, hi.z, hi.w);
-        }
-        // NoPE columns 16*lane .. 16*lane+15 = chunks 2*lane, 2*lane+1.  Lanes
-        // 4..7 of every 8 store their odd chunk first so the 8 lanes of each
-        // store phase hit 8 distinct bank groups.
-        const uint32_t a0 = tile + sw128_chunk(C::kRows, r, 2 * lane);
-        const uint32_t a1 = tile + sw128_chunk(C::kRows, r, 2 * lane + 1);
-        if ((lane >> 2) & 1) {
-          sts128(a1, hi);
-          sts128(a0, lo);
-        } else {
-          sts128(a0, lo);
-          sts128(a1, hi);
-        }
-        const uint4 tail = v ? rb.b : make_uint4(0, 0, 0, 0);
-        if (lane >= 1 && lane <= 8) sts128(tile + sw128_chunk(C::kRows, r, 64 + lane - 1), tail);
-        if (lane == 0) sts128(smem_u32(smem + C::kOffScale + (b * C::kRows + r) * 16), tail);  // 4 scales
-      } else {
-        const uint4 z = make_uint4(0, 0, 0, 0);
-        sts128(tile + sw128_chunk(C::kRows, r, lane), v ? rb.a : z);
-        sts128(tile + sw128_chunk(C::kRows, r, lane + 32), v ? rb.b : z);
-        if (lane < 8) sts128(tile + sw128_chunk(C::kRows, r, lane + 64), v ? rb.c : z);
-      }
+      const uint4 z = make_uint4(0, 0, 0, 0);
+      sts128(tile + sw128_chunk(C::kRows, r, lane), v ? rb.a : z);
+      sts128(tile + sw128_chunk(C::kRows, r, lane + 32), v ? rb.b : z);
+      if (lane < 8) sts128(tile + sw128_chunk(C::kRows, r, lane + 64), v ? rb.c : z);
       if (lane == 0) valid[b * C::kRows + r] = v ? 1 : 0;
       if (k == RW - 1) {
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[C::kBarKvFull + b]);
-        if (lane == 0) SMLA_TRACE_MAX(tl, kEvConvDone);
       }
     };
 
@@ -443,20 +360,15 @@ __global__ void __launch_bounds__(Cfg<HG, kFp8>::kThreads, 1) sparse_mla_attn_ke
             tc_fence_after();
             const uint32_t kv = kv_base + b * C::kKvTile;
             const uint32_t qs = q_base + qb * C::kQBytes;
-            const uint32_t sbuf = tmem + C::kSCol + b * C::kNS * HG;
+            const uint32_t sbuf = tmem + C::kSCol + b * HG;
 #pragma unroll
             for (int s = 0; s < 36; ++s) {
               const uint32_t off = (s & 3) * 32;
               const uint64_t da = make_sdesc(kv + (s >> 2) * C::kPanel + off, 16, 1024, kLayoutSw128);
               const uint64_t db = make_sdesc(qs + (s >> 2) * C::kQPanel + off, 16, 1024, kLayoutSw128);
-              // FP8: NoPE scale group g = s / 8 (columns 128g..128g+127) and the
-              // RoPE columns each get their own accumulator; BF16: one accumulator.
-              const int g = kFp8 ? (s < 32 ? (s >> 3) : 4) : 0;
-              const bool first = kFp8 ? (s < 32 ? (s & 7) == 0 : s == 32) : s == 0;
-              mma_ss(sbuf + g * HG, da, db, idesc_qk, first ? 0u : 1u);
+              mma_ss(sbuf, da, db, idesc_qk, s == 0 ? 0u : 1u);
             }
             mma_commit(&bars[C::kBarSFull + b]);
-            SMLA_TRACE_SET(tl, kEvQk);
             if (ti.seg_end) mma_commit(&bars[C::kBarQEmpty + qb]);
             ++next_qk;
             progressed = true;
@@ -475,7 +387,7 @@ __global__ void __launch_bounds__(Cfg<HG, kFp8>::kThreads, 1) sparse_mla_attn_ke
             const uint32_t kv = kv_base + b * C::kKvTile;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-              const uint32_t pb = p_base + (b * C::kNP + (kFp8 ? q : 0)) * C::kPBytes;
+              const uint32_t pb = p_base + b * C::kPBytes;
 #pragma unroll
               for (int s = 0; s < 4; ++s) {
                 const uint64_t da = make_sdesc(kv + 2 * q * C::kPanel + s * 2048, C::kPanel, 1024, kLayoutSw128);
@@ -485,7 +397,6 @@ __global__ void __launch_bounds__(Cfg<HG, kFp8>::kThreads, 1) sparse_mla_attn_ke
             }
             mma_commit(&bars[C::kBarKvEmpty + b]);
             mma_commit(&bars[C::kBarPvDone + b]);
-            SMLA_TRACE_SET(tl, kEvPv);
             ++next_pv;
             progressed = true;
           }
@@ -530,54 +441,16 @@ __global__ void __launch_bounds__(Cfg<HG, kFp8>::kThreads, 1) sparse_mla_attn_ke
         n_seg_tiles = 0;
       }
       if (!dead) dead = !SMLA_WAIT(C::kBarSFull + b, (tl >> 1) & 1);
-      if (tid == 0) SMLA_TRACE_SET(tl, kEvSoftStart);
       if (!dead) dead = !SMLA_WAIT(C::kBarKvFull + b, (tl >> 1) & 1);  // orders the row-valid flags
       tc_fence_after();
       const bool row_ok = !dead && lane < 16 && valid[b * C::kRows + r] != 0;
-      const uint32_t s_addr = tmem + lane_base + C::kSCol + b * C::kNS * HG;
-      float scs[4] = {0.f, 0.f, 0.f, 0.f};
-      if constexpr (kFp8) {
-        if (row_ok) {
-          const float4 v4 = *reinterpret_cast<const float4*>(smem + C::kOffScale + (b * C::kRows + r) * 16);
-          scs[0] = v4.x;
-          scs[1] = v4.y;
-          scs[2] = v4.z;
-          scs[3] = v4.w;
-        }
-      }
-      // scaled logits (log2 units) of head block hb: sum_g scale_g * S_g + S_rope.
-      // All accumulator loads of a block are issued before one wait; the empty
-      // asm statements after the wait keep every use of the loaded registers
-      // behind it.
+      const uint32_t s_addr = tmem + lane_base + C::kSCol + b * HG;
+      // scaled logits (log2 units) of head block hb
       auto logits = [&](int hb, float (&sv)[16]) {
-        if constexpr (kFp8) {
-          uint32_t a0[16], a1[16], a2[16], a3[16], a4[16];
-          tmem_ld16(s_addr + 0 * HG + hb * 16, a0);
-          tmem_ld16(s_addr + 1 * HG + hb * 16, a1);
-          tmem_ld16(s_addr + 2 * HG + hb * 16, a2);
-          tmem_ld16(s_addr + 3 * HG + hb * 16, a3);
-          tmem_ld16(s_addr + 4 * HG + hb * 16, a4);
-          tmem_ld_wait();
-          reg_fence16(a0);
-          reg_fence16(a1);
-          reg_fence16(a2);
-          reg_fence16(a3);
-          reg_fence16(a4);
+        uint32_t a0[16];
+        tmem_ld16_sync(s_addr + hb * 16, a0);
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            float acc = __uint_as_float(a4[j]);
-            acc = fmaf(scs[0], __uint_as_float(a0[j]), acc);
-            acc = fmaf(scs[1], __uint_as_float(a1[j]), acc);
-            acc = fmaf(scs[2], __uint_as_float(a2[j]), acc);
-            acc = fmaf(scs[3], __uint_as_float(a3[j]), acc);
-            sv[j] = row_ok ? acc * p.scale_log2 : -INFINITY;
-          }
-        } else {
-          uint32_t a0[16];
-          tmem_ld16_sync(s_addr + hb * 16, a0);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) sv[j] = row_ok ? __uint_as_float(a0[j]) * p.scale_log2 : -INFINITY;
-        }
+        for (int j = 0; j < 16; ++j) sv[j] = row_ok ? __uint_as_float(a0[j]) * p.scale_log2 : -INFINITY;
       };
       // pass 1: logits (kept for pass 2) and the per-head maximum of this tile
       float* redm = red_max + (tl & 1) * 4 * HG;
@@ -631,8 +504,7 @@ __global__ void __launch_bounds__(Cfg<HG, kFp8>::kThreads, 1) sparse_mla_attn_ke
           tmem_st_wait();
         }
       }
-      // pass 2: probabilities, running sums, P_q^T rows (p times the value
-      // chunk's scale for FP8; p itself for BF16)
+      // pass 2: probabilities, running sums, P^T rows
       if (tl >= 2 && !dead) dead = !SMLA_WAIT(C::kBarPvDone + b, ((tl >> 1) + 1) & 1);  // P buffers free
 #pragma unroll
       for (int hb = 0; hb < NB16; ++hb) {
@@ -643,18 +515,12 @@ __global__ void __launch_bounds__(Cfg<HG, kFp8>::kThreads, 1) sparse_mla_attn_ke
           l_part[hb * 16 + j] += pr[j];
         }
         if (!dead && lane < 16) {
+          const uint32_t pbuf = p_base + b * C::kPBytes;
 #pragma unroll
-          for (int q = 0; q < C::kNP; ++q) {
-            const float sq = kFp8 ? scs[q] : 1.f;
-            const uint32_t pbuf = p_base + (b * C::kNP + q) * C::kPBytes;
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const uint4 v = make_uint4(pack_bf16x2(pr[8 * e + 0] * sq, pr[8 * e + 1] * sq),
-                                         pack_bf16x2(pr[8 * e + 2] * sq, pr[8 * e + 3] * sq),
-                                         pack_bf16x2(pr[8 * e + 4] * sq, pr[8 * e + 5] * sq),
-                                         pack_bf16x2(pr[8 * e + 6] * sq, pr[8 * e + 7] * sq));
-              sts128(pbuf + pt_offset<HG>(r, hb * 16 + 8 * e), v);
-            }
+          for (int e = 0; e < 2; ++e) {
+            const uint4 v = make_uint4(pack_bf16x2(pr[8 * e + 0], pr[8 * e + 1]), pack_bf16x2(pr[8 * e + 2], pr[8 * e + 3]),
+                                       pack_bf16x2(pr[8 * e + 4], pr[8 * e + 5]), pack_bf16x2(pr[8 * e + 6], pr[8 * e + 7]));
+            sts128(pbuf + pt_offset<HG>(r, hb * 16 + 8 * e), v);
           }
         }
       }
@@ -662,7 +528,6 @@ __global__ void __launch_bounds__(Cfg<HG, kFp8>::kThreads, 1) sparse_mla_attn_ke
       tc_fence_before();
       __syncwarp();
       if (lane == 0 && !dead) mbar_arrive(&bars[C::kBarPFull + b]);
-      if (tid == 0) SMLA_TRACE_SET(tl, kEvSoftDone);
       ++n_seg_tiles;
 
       if (ti.seg_end) {
@@ -732,25 +597,30 @@ __global__ void __launch_bounds__(Cfg<HG, kFp8>::kThreads, 1) sparse_mla_attn_ke
   }
 }
 
-template <int HG, bool kFp8>
+// Per device and head-group size: the kernel's dynamic shared memory limit
+// has been raised (once, thread-safely).
+std::once_flag g_attr_once[2][64];
+cudaError_t g_attr_err[2][64];
+
+template <int HG>
 cudaError_t launch_impl(const AttnArgs& a, const AttnPlan& plan, cudaStream_t stream) {
-  using C = Cfg<HG, kFp8>;
-  static bool attr_set = false;  // per instantiation; set once per process
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(sparse_mla_attn_kernel<HG, kFp8>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemAlloc);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  using C = Cfg<HG>;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  const int hi = HG == 16 ? 0 : 1;
+  std::call_once(g_attr_once[hi][dev], [hi, dev] {
+    g_attr_err[hi][dev] = cudaFuncSetAttribute(sparse_mla_attn_kernel<HG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               C::kSmemAlloc);
+  });
+  if (g_attr_err[hi][dev] != cudaSuccess) return g_attr_err[hi][dev];
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
   const int64_t n_slots = (int64_t)plan.G + plan.units - 1;
   Params p;
   p.q = static_cast<const __nv_bfloat16*>(a.q);
-  p.cache = a.cache;
   p.kv = static_cast<const __nv_bfloat16*>(a.kv);
   p.indices = a.indices;
-  p.block_table = a.block_table;
-  p.req_id = a.req_id;
   p.out = static_cast<__nv_bfloat16*>(a.out);
   p.lse = a.lse;
   p.status = reinterpret_cast<int*>(ws);
@@ -760,15 +630,13 @@ cudaError_t launch_impl(const AttnArgs& a, const AttnPlan& plan, cudaStream_t st
   p.T = a.T;
   p.H = a.H;
   p.K = a.K;
-  p.R = a.R;
-  p.MB = a.MB;
-  p.NB = a.NB;
+  p.N = a.NB;
   p.n_hg = plan.n_hg;
   p.nt = plan.nt;
   p.total = plan.total;
   p.G = plan.G;
-  sparse_mla_attn_kernel<HG, kFp8><<<plan.G, C::kThreads, C::kSmemAlloc, stream>>>(p);
-  cudaError_t e = cudaGetLastError();
+  sparse_mla_attn_kernel<HG><<<plan.G, C::kThreads, C::kSmemAlloc, stream>>>(p);
+  e = cudaGetLastError();
   if (e != cudaSuccess || !plan.need_combine) return e;
   e = launch_combine<HG>(p.part_o, p.part_lse, p.out, p.lse, p.H, p.n_hg, p.nt, p.total, p.G, plan.units, stream);
   if (e != cudaSuccess) return e;
@@ -776,12 +644,6 @@ cudaError_t launch_impl(const AttnArgs& a, const AttnPlan& plan, cudaStream_t st
 }
 
 }  // namespace
-
-#ifdef SMLA_TRACE
-extern "C" int smla_trace_set(unsigned long long* buf) {
-  return (int)cudaMemcpyToSymbol(g_smla_trace, &buf, sizeof(buf));
-}
-#endif
 
 AttnPlan plan_prefill_bf16(int T, int H, int K, int num_splits, int num_sms) {
   if (wide_supported(H)) return plan_prefill_wide(T, K, num_splits, num_sms);
@@ -804,7 +666,7 @@ AttnPlan plan_prefill_bf16(int T, int H, int K, int num_splits, int num_sms) {
 
 cudaError_t launch_prefill_bf16(const AttnArgs& a, const AttnPlan& plan, cudaStream_t stream) {
   if (plan.HG == 128) return launch_prefill_wide(a, plan, stream);
-  return plan.HG == 16 ? launch_impl<16, false>(a, plan, stream) : launch_impl<32, false>(a, plan, stream);
+  return plan.HG == 16 ? launch_impl<16>(a, plan, stream) : launch_impl<32>(a, plan, stream);
 }
 
 AttnPlan plan_attention(bool fp8, int T, int H, int K, int num_splits, int num_sms) {

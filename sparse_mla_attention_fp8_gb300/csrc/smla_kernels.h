@@ -22,8 +22,10 @@ struct AttnPlan {
   int64_t units;      // T * n_hg
   int64_t total;      // units * nt
   int G;              // CTAs
-  bool need_combine;  // some unit spans more than one CTA
+  bool need_combine;  // some unit spans more than one CTA, merged by the combine kernel
   size_t ws_bytes;    // workspace bytes (status word + partial results)
+  int cluster = 1;    // > 1: every unit is split into `cluster` parts run by one thread-block
+                      // cluster, merged in distributed shared memory (no combine kernel)
 };
 
 AttnPlan plan_attention(bool fp8, int T, int H, int K, int num_splits, int num_sms);

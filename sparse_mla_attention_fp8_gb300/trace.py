@@ -1,0 +1,137 @@
+"""Per-tile timeline of the 16-head FP8 decode kernel, for performance work.
+
+Builds a separate traced copy of the library (all sources compiled with
+SMLA_TRACE, in ``_build_trace/``), runs the memory-bound decode workload
+(64 requests x 1 token, H = 16, top-k 2048) a few times, then once with the
+trace buffer attached, and prints per-tile timings taken from %globaltimer at
+the kernel roles' hand-off points (median over CTAs, microseconds from the
+CTA's first index translation):
+
+    python -m sparse_mla_attention_fp8_gb300.trace
+
+The normal library (``libsmla.so``) carries none of this: the hooks compile
+to nothing without SMLA_TRACE.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import sys
+
+import numpy as np
+
+from . import NVCC_FLAGS, SOURCES, _CSRC, _PKG, _nvcc
+
+EVENTS = ["idx", "buf_free", "issued", "landed", "op_full", "qk", "soft_start", "soft_bar", "p_written", "pv",
+          "epilogue", "q_ready", "epi_start", "merge_wait", "merge_go"]
+# per-tile links: (name, from event, to event, tile offset of the end event)
+LINKS = [("copy issue (loader 0)", "buf_free", "issued", 0), ("copy landing (loader 0)", "issued", "landed", 0),
+         ("other loaders after loader 0", "landed", "op_full", 0), ("QK^T issue", "op_full", "qk", 0),
+         ("S ready after issue", "qk", "soft_start", 0), ("softmax to tile-max barrier", "soft_start", "soft_bar", 0),
+         ("softmax barrier to P' (warp 0)", "soft_bar", "p_written", 0), ("P' (warp 0) to P.V issued", "p_written", "pv", 0),
+         ("P.V issued to buffer free (tile + 2)", "pv", "buf_free", 2), ("Q ready to tile full", "q_ready", "op_full", 0),
+         ("last P.V issued to epilogue start", "pv", "epi_start", 0),
+         ("epilogue start to merge wait", "epi_start", "merge_wait", 0),
+         ("merge wait (other CTA)", "merge_wait", "merge_go", 0), ("merge to epilogue end", "merge_go", "epilogue", 0)]
+TILES = 16
+
+
+def build_traced(csrc: str = _CSRC, out_dir: str | None = None) -> str:
+    """Compile the sources in ``csrc`` with SMLA_TRACE into ``out_dir``."""
+    out_dir = out_dir or os.path.join(_PKG, "_build_trace")
+    os.makedirs(out_dir, exist_ok=True)
+    objs = []
+    for s in SOURCES:
+        obj = os.path.join(out_dir, s.replace(".cu", ".o"))
+        subprocess.run([_nvcc(), *NVCC_FLAGS, "-DSMLA_TRACE", "-c", os.path.join(csrc, s), "-o", obj], check=True)
+        objs.append(obj)
+    lib = os.path.join(out_dir, "libsmla_trace.so")
+    subprocess.run([_nvcc(), "-shared", "-gencode", "arch=compute_103a,code=sm_103a", *objs, "-o", lib], check=True)
+    return lib
+
+
+def main(lib_path: str | None = None):
+    import torch
+
+    root = os.path.dirname(_PKG)
+    if root not in sys.path:
+        sys.path.insert(0, root)
+    import smla_inputs as inp
+
+    L = ctypes.CDLL(lib_path or build_traced())
+    P, i32, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    L.sparse_mla_decode_fp8.argtypes = [P, P, P, P, P, f32, i32, P, P, i32, i32, i32, i32, i32, i32, P, sz, P]
+    L.mla_cache_store_fp8.argtypes = [P, P, P, i32, i32, P]
+    L.sparse_mla_decode_workspace_bytes.argtypes = [i32, i32, i32, i32]
+    L.sparse_mla_decode_workspace_bytes.restype = sz
+    L.sparse_mla_attention_plan.argtypes = [i32, i32, i32, i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32)]
+    L.smla_trace_set_fp8.argtypes = [P]
+    ptr = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+
+    dev = torch.device("cuda", 0)
+    case = inp.rotating_decode(seed=1)
+    T, H, K, NB = case.q.shape[0], case.H, case.K, case.num_blocks
+    cache = torch.zeros((NB, 64, 656), dtype=torch.uint8, device=dev)
+    lat = inp.device_latent(len(case.ctx_slots), case.latent_seed, case.outlier_channels, dev)
+    slots = torch.from_numpy(case.ctx_slots).to(dev)
+    assert L.mla_cache_store_fp8(ptr(lat), ptr(slots), ptr(cache), lat.shape[0], NB, None) == 0
+    q = torch.from_numpy(case.q.view(np.int16)).to(dev)
+    idx = [torch.from_numpy(s).to(dev) for s in case.index_sets]
+    bt = torch.from_numpy(case.block_table).to(dev)
+    req = torch.from_numpy(case.req_id_per_token).to(dev)
+    ws_bytes = L.sparse_mla_decode_workspace_bytes(T, H, K, 0)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+    out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+    launches, ctas = ctypes.c_int(0), ctypes.c_int(0)
+    L.sparse_mla_attention_plan(1, T, H, K, 0, ctypes.byref(launches), ctypes.byref(ctas))
+    G = ctas.value
+    buf = torch.zeros((G, TILES, len(EVENTS)), dtype=torch.int64, device=dev)
+
+    def call(i):
+        rc = L.sparse_mla_decode_fp8(ptr(q), ptr(cache), ptr(idx[i % len(idx)]), ptr(bt), ptr(req),
+                                     f32(case.sm_scale), 0, ptr(out), ptr(lse), T, H, K, bt.shape[0], bt.shape[1],
+                                     NB, ptr(ws), ws_bytes, None)
+        assert rc == 0
+
+    for i in range(5):
+        call(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(40):
+        call(i)
+    e1.record()
+    torch.cuda.synchronize()
+    print(f"decode call (attention + combine), eager, rotating index sets: {e0.elapsed_time(e1) / 40 * 1e3:.1f} us")
+    assert L.smla_trace_set_fp8(ptr(buf)) == 0
+    call(5)
+    torch.cuda.synchronize()
+    assert L.smla_trace_set_fp8(None) == 0
+    ev = buf.cpu().numpy().astype(np.float64)
+    t0 = np.where(ev[:, 0, 0] > 0, ev[:, 0, 0], np.nan)
+    start = np.nanmin(t0)
+    rel = np.where(ev > 0, (ev - start) / 1e3, np.nan)  # microseconds from the first CTA's first translation
+    print(f"CTAs {G}; first index translation spread over CTAs: {np.nanmax(t0 - start) / 1e3:.2f} us")
+    print("median over CTAs, us from the earliest CTA start; columns = tiles")
+    print("event        " + " ".join(f"{t:6d}" for t in range(TILES)))
+    for e, name in enumerate(EVENTS):
+        med = np.nanmedian(rel[:, :, e], axis=0)
+        print(f"{name:12s} " + " ".join("   -  " if np.isnan(x) else f"{x:6.2f}" for x in med))
+    print("per-tile links, median over CTAs and tiles (us):")
+    for name, a, b, off in LINKS:
+        ea, eb = rel[:, :, EVENTS.index(a)], rel[:, :, EVENTS.index(b)]
+        d = eb[:, off:] - ea[:, :TILES - off]
+        if np.isfinite(d).any():
+            print(f"  {name:38s} {np.nanmedian(d):6.2f}  (p90 {np.nanpercentile(d, 90):5.2f}, n {np.isfinite(d).sum()})")
+    pv = rel[:, :, EVENTS.index("pv")]
+    last = np.nanmax(pv, axis=1)
+    print(f"last P.V issued: min {np.nanmin(last):.2f} median {np.nanmedian(last):.2f} max {np.nanmax(last):.2f} us")
+    d = np.diff(pv, axis=1)
+    print(f"P.V cadence: median {np.nanmedian(d):.2f} us (p10 {np.nanpercentile(d, 10):.2f}, "
+          f"p90 {np.nanpercentile(d, 90):.2f})")
+
+
+if __name__ == "__main__":
+    main()

@@ -102,12 +102,13 @@ def test_mixed_batch_store_then_decode():
 def test_explicit_workspace_and_too_small_workspace():
     import torch
     import sparse_mla_attention_fp8_gb300 as smla
-    case = inp.memory_bound_decode(seed=13, R=4, ctx_lo=300, ctx_hi=600, K=128)
+    # 5 parts per token (more than a cluster merges): partial results in the workspace
+    case = inp.memory_bound_decode(seed=13, R=4, ctx_lo=800, ctx_hi=1500, K=700)
     cache = oracle_cache(case)
-    need = smla.decode_workspace_bytes(case.T, case.H, case.K, 0)
-    assert need > 0
+    need = smla.decode_workspace_bytes(case.T, case.H, case.K, 5)
+    assert need > 256
     ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
-    out, lse = run_gpu_decode(case, cache, workspace=ws)
+    out, lse = run_gpu_decode(case, cache, num_splits=5, workspace=ws)
     ref_out, ref_lse = oracle.sparse_mla_decode(case.q, cache, case.indices, case.block_table,
                                                 case.req_id_per_token, case.sm_scale)
     assert_out_close(out, ref_out)
@@ -115,7 +116,7 @@ def test_explicit_workspace_and_too_small_workspace():
     small = torch.zeros(need - 256, dtype=torch.uint8, device="cuda")
     with pytest.raises(smla.SmlaError, match="status -4"):
         smla.sparse_mla_decode_fp8(bf16_dev(case.q), dev(cache), dev(case.indices), dev(case.block_table),
-                                   dev(case.req_id_per_token), case.sm_scale, workspace=small)
+                                   dev(case.req_id_per_token), case.sm_scale, num_splits=5, workspace=small)
 
 
 def test_repeated_calls_are_deterministic():
