@@ -39,17 +39,16 @@ UNIT = "query-tokens/s"
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) of one decode
 # launch, from an ncu capture of the kernels built from the sources whose
-# hash is the key (profiles/sparse_mla_decode_fp8_kernel_decode_h16_k2048.md):
-# the attention kernel plus the combine of split units.  Once the kernel
-# sources change, the figure no longer applies and the roofline reports null.
+# hash is the key: the attention kernel plus, where units are split across
+# CTAs outside a cluster, the combine.  Once the kernel sources change, the
+# figure no longer applies and the roofline reports null.
 TRAFFIC_SOURCES = ("smla_decode.cu", "smla_combine.cuh", "smla_common.cuh", "sm103_ptx.cuh")
 TRAFFIC_BY_SOURCE = {
     "4bf1514cc60d41f8": 100_889_344 + 2_852_352 + 7_377_408 + 0,
 }
-# The same for the 128-head CTA-pair kernel, per workload
-# (profiles/sparse_mla_wide_kernel_*.md): the bf16 prefill's attention kernel
-# plus its combine; the FP8 decode's attention kernel alone (its capture left
-# out the Q preparation and the combine).
+# The same for the 128-head CTA-pair kernel, per workload: the bf16 prefill's
+# attention kernel plus its combine; the FP8 decode's attention kernel alone
+# (its capture left out the Q preparation and the combine).
 WIDE_TRAFFIC_SOURCES = ("smla_wide.cu", "smla_combine.cuh", "smla_common.cuh", "sm103_ptx.cuh")
 WIDE_TRAFFIC_BY_SOURCE = {
     ("71d5b8755a8edd55", "prefill_h128_k2048"): (671_053_056 + 524_675_840 + 38_473_472 + 210_944,
@@ -98,7 +97,7 @@ class ClockSampler:
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-              "clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_power_cap,utilization.gpu")
 
     def __init__(self, gpu_id: str | None):
         self.gpu_id = gpu_id
@@ -130,19 +129,22 @@ class ClockSampler:
         with open(self.path) as f:
             for line in f:
                 parts = [x.strip() for x in line.split(",")]
-                if len(parts) < 8:
+                if len(parts) < 9:
                     continue
                 try:
-                    rows.append((float(parts[0]), float(parts[1]), float(parts[2]), parts[4:8]))
+                    rows.append((float(parts[0]), float(parts[1]), float(parts[2]), parts[4:8], float(parts[8])))
                 except ValueError:
                     continue
         os.unlink(self.path)
         if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "samples_under_load": 0}
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in rows for i, v in enumerate(r[3]) if v.lower().startswith("active")})
-        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
-                "power_w_max": max(r[2] for r in rows), "reasons": reasons, "samples": len(rows)}
+        busy = [r for r in rows if r[4] >= 50.0]  # samples while the GPU was busy
+        use = busy or rows
+        return {"sm_mhz": statistics.median(r[0] for r in use), "sm_max_mhz": max(r[1] for r in rows),
+                "power_w_max": max(r[2] for r in rows), "reasons": reasons, "samples": len(rows),
+                "samples_under_load": len(busy)}
 
 
 def dist_setup():
@@ -350,8 +352,16 @@ def run_ours(args):
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
 
-    # ---- timed region: exactly K steps
+    # ---- clocks: sampled from an untimed burst of >= 1.2 s of steps under load
+    # through the timed region
     clocks.start()
+    t_burst = time.perf_counter()
+    with torch.cuda.stream(stream):
+        while time.perf_counter() - t_burst < 1.2:
+            for i in range(n_rot * 16):
+                step_graphs[i % n_rot].replay()
+            stream.synchronize()
+    # ---- timed region: exactly K steps
     barrier(world, device)
     torch.cuda.synchronize(device)
     with torch.cuda.stream(stream):
@@ -389,6 +399,17 @@ def run_ours(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(case)
 
+    # ---- the tensor-bound configurations, each with its own roofline (rank 0, N = 1)
+    extra = {}
+    if rank == 0 and world == 1 and not args.no_extra:
+        del cache
+        torch.cuda.empty_cache()
+        for name, k in (("decode_h128_k2048", max(20, args.steps // 20)), ("prefill_h128_k2048", max(5, args.steps // 200))):
+            sub = argparse.Namespace(**vars(args))
+            sub.workload, sub.steps = name, k
+            sub.no_cpu_baseline = True
+            extra[name] = tensor_workload(sub, quiet=True)
+
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -416,6 +437,8 @@ def run_ours(args):
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clk,
         }
+        for name, r in extra.items():
+            line[name] = r
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
@@ -445,6 +468,10 @@ def time_graphs(graphs, steps, stream):
 
 
 def run_tensor_workload(args):
+    print(json.dumps(tensor_workload(args)), flush=True)
+
+
+def tensor_workload(args, quiet=False):
     """The tensor-bound configurations of the hot path, for the record (the
     default line is the memory-bound decode):
       decode_h128_k2048: FP8 decode, 128 requests x 1 token, H = 128, top-k
@@ -458,8 +485,7 @@ def run_tensor_workload(args):
     import sparse_mla_attention_fp8_gb300 as smla
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA GPU for the library path")
-    device = torch.device("cuda", 0)
-    torch.cuda.set_device(device)
+    device = torch.device("cuda", torch.cuda.current_device())
     smla.build()
     oracle.build()
     peaks = load_peaks()
@@ -550,6 +576,10 @@ def run_tensor_workload(args):
         pass
     clocks = ClockSampler(uuid)
     clocks.start()
+    if not quiet:  # an untimed burst of >= 1.2 s under load for the clock record
+        t_burst = time.perf_counter()
+        while time.perf_counter() - t_burst < 1.2:
+            time_graphs(graphs, max(3, args.steps // 4), stream)
     ms = time_graphs(graphs, args.steps, stream)
     clk = clocks.stop()
     if smla.read_device_status(ws, stream) != 0:
@@ -579,65 +609,102 @@ def run_tensor_workload(args):
                      "avg_launch_us": ms * 1e3},
         "cpu_baseline": cpu, "e2e": None, "gpu_launches": launches * args.steps, "clocks": clk,
     }
-    print(json.dumps(line), flush=True)
+    return line
 
 
 def run_e2e(args, smla, case, device, stream, cache, ws):
-    """Same step through the public API from pinned host buffers: each step
-    copies its inputs host->device, runs store + decode, and copies out + lse
-    back."""
+    """The same step end to end through the C ABI with host buffers: every
+    step copies its inputs (q, the step's top-k indices, block table, request
+    ids, the new rows and their slots) from one pinned host buffer to the
+    device in one copy, runs quantize-and-store + decode through the C entry
+    points, and copies out + lse back in one copy.  Inputs and outputs are
+    double-buffered on the device, and the copies run on their own streams,
+    so step i's copies overlap steps i - 1 and i + 1's kernels."""
+    import ctypes
+
     import torch
-    T, H = case.q.shape[0], case.H
+    T, H, K = case.q.shape[0], case.H, case.K
+    R, MB = case.block_table.shape
+    NB = case.num_blocks
     n_rot = len(case.index_sets)
-    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
-    h_q = pin(case.q.view(np.int16))
-    h_idx = [pin(s) for s in case.index_sets]
-    h_bt = pin(case.block_table)
-    h_req = pin(case.req_id_per_token)
-    rows = inp.device_latent(T, case.latent_seed + 1, case.outlier_channels, device)
-    h_rows = rows.view(torch.int16).cpu().pin_memory()
-    h_slots = pin(case.new_slots)
-    h_out = torch.empty((T, H, 512), dtype=torch.bfloat16).pin_memory()
-    h_lse = torch.empty((T, H), dtype=torch.float32).pin_memory()
-    d_q = torch.empty((T, H, 576), dtype=torch.int16, device=device)
-    d_idx = torch.empty_like(h_idx[0], device=device)
-    d_bt = torch.empty_like(h_bt, device=device)
-    d_req = torch.empty_like(h_req, device=device)
-    d_rows = torch.empty((T, 576), dtype=torch.int16, device=device)
-    d_slots = torch.empty_like(h_slots, device=device)
-    d_out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=device)
-    d_lse = torch.empty((T, H), dtype=torch.float32, device=device)
-    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_idx[0], h_bt, h_req, h_rows, h_slots))
-    d2h = h_out.numel() * 2 + h_lse.numel() * 4
+    L = smla.lib()
+
+    def seg(nbytes):
+        return (nbytes + 255) // 256 * 256
+    rows = inp.device_latent(T, case.latent_seed + 1, case.outlier_channels, device).view(torch.int16).cpu().numpy()
+    parts = [("q", case.q.view(np.uint8)), ("idx", None), ("bt", case.block_table.view(np.uint8)),
+             ("req", case.req_id_per_token.view(np.uint8)), ("rows", rows.view(np.uint8)),
+             ("slots", case.new_slots.view(np.uint8))]
+    sizes = {"q": case.q.nbytes, "idx": case.index_sets[0].nbytes, "bt": case.block_table.nbytes,
+             "req": case.req_id_per_token.nbytes, "rows": rows.nbytes, "slots": case.new_slots.nbytes}
+    offs, off = {}, 0
+    for name, _ in parts:
+        offs[name] = off
+        off += seg(sizes[name])
+    in_bytes = off
+    h_in = []
+    for j in range(n_rot):  # one packed host input buffer per rotating index set
+        buf = np.zeros(in_bytes, np.uint8)
+        for name, arr in parts:
+            src = case.index_sets[j].view(np.uint8) if name == "idx" else arr
+            buf[offs[name]:offs[name] + sizes[name]] = src.reshape(-1)
+        h_in.append(torch.from_numpy(buf).pin_memory())
+    out_bytes = T * H * 512 * 2
+    o_lse = seg(out_bytes)
+    res_bytes = o_lse + T * H * 4
+    d_in = [torch.empty(in_bytes, dtype=torch.uint8, device=device) for _ in range(2)]
+    d_res = [torch.empty(res_bytes, dtype=torch.uint8, device=device) for _ in range(2)]
+    h_res = [torch.empty(res_bytes, dtype=torch.uint8).pin_memory() for _ in range(2)]
+    s_h2d, s_d2h = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    ev_in = [torch.cuda.Event() for _ in range(2)]     # inputs of the slot copied
+    ev_done = [torch.cuda.Event() for _ in range(2)]   # kernels of the slot done (inputs free, results ready)
+    ev_out = [torch.cuda.Event() for _ in range(2)]    # results of the slot copied back
+    cstream = ctypes.c_void_p(stream.cuda_stream)
+    cache_p = ctypes.c_void_p(cache.data_ptr())
+    ws_p, ws_n = ctypes.c_void_p(ws.data_ptr()), ws.numel()
 
     def step(i):
-        d_q.copy_(h_q, non_blocking=True)
-        d_idx.copy_(h_idx[i % n_rot], non_blocking=True)
-        d_bt.copy_(h_bt, non_blocking=True)
-        d_req.copy_(h_req, non_blocking=True)
-        d_rows.copy_(h_rows, non_blocking=True)
-        d_slots.copy_(h_slots, non_blocking=True)
-        smla.mla_cache_store_fp8(d_rows.view(torch.bfloat16), d_slots, cache, stream=stream)
-        smla.sparse_mla_decode_fp8(d_q.view(torch.bfloat16), cache, d_idx, d_bt, d_req, case.sm_scale, 0, d_out,
-                                   d_lse, ws, stream=stream)
-        h_out.copy_(d_out, non_blocking=True)
-        h_lse.copy_(d_lse, non_blocking=True)
+        k = i % 2
+        base_in, base_res = d_in[k].data_ptr(), d_res[k].data_ptr()
+        with torch.cuda.stream(s_h2d):
+            if i >= 2:
+                s_h2d.wait_event(ev_done[k])
+            d_in[k].copy_(h_in[i % n_rot], non_blocking=True)
+            ev_in[k].record(s_h2d)
+        stream.wait_event(ev_in[k])
+        if i >= 2:
+            stream.wait_event(ev_out[k])
+        P = lambda name: ctypes.c_void_p(base_in + offs[name])  # noqa: E731
+        rc = L.mla_cache_store_fp8(P("rows"), P("slots"), cache_p, T, NB, cstream)
+        rc |= L.sparse_mla_decode_fp8(P("q"), cache_p, P("idx"), P("bt"), P("req"), ctypes.c_float(case.sm_scale), 0,
+                                      ctypes.c_void_p(base_res), ctypes.c_void_p(base_res + o_lse), T, H, K, R, MB,
+                                      NB, ws_p, ws_n, cstream)
+        if rc != 0:
+            raise SystemExit("e2e: C-ABI call failed: " + L.smla_last_error().decode())
+        ev_done[k].record(stream)
+        with torch.cuda.stream(s_d2h):
+            s_d2h.wait_event(ev_done[k])
+            h_res[k].copy_(d_res[k], non_blocking=True)
+            ev_out[k].record(s_d2h)
 
-    with torch.cuda.stream(stream):
-        for i in range(max(args.warmup, 3)):
-            step(i)
-    stream.synchronize()
+    for i in range(max(args.warmup, 3)):
+        step(i)
+    torch.cuda.synchronize(device)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for i in range(args.steps):
-            step(i)
-        e1.record(stream)
-    stream.synchronize()
+    e0.record(s_h2d)
+    for i in range(args.steps):
+        step(i)
+    e1.record(s_d2h)
+    torch.cuda.synchronize(device)
     ms = e0.elapsed_time(e1) / args.steps
-    return {"value": T / (ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-            "ms_per_step": ms, "path": "public Python API (ctypes -> C ABI), eager launches, pinned host buffers"}
+    # the last step's results as copied back agree with the device buffers
+    last = (args.steps - 1) % 2
+    assert torch.equal(h_res[last].to(device), d_res[last])
+    return {"value": T / (ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": int(in_bytes),
+            "d2h_bytes_per_step": int(res_bytes), "ms_per_step": ms,
+            "path": "C ABI (ctypes) with pinned host buffers: one host-to-device copy of the packed inputs and one "
+                    "device-to-host copy of out + lse per step, double-buffered on copy streams"}
 
 
 def main():
@@ -648,6 +715,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="leave the tensor-bound configurations out of the default line")
     ap.add_argument("--workload", choices=["decode_h16_k2048", "decode_h128_k2048", "prefill_h128_k2048"],
                     default="decode_h16_k2048",
                     help="decode_h16_k2048 (default) is the headline; the other two are the tensor-bound "
