@@ -70,6 +70,12 @@ def _load():
             lib.oracle_sparse_mla_decode.restype = None
             lib.oracle_sparse_mla_prefill.argtypes = [P, P, P, f64, i32, i32, i64, i32, P, i32, P, P, i32, P, P]
             lib.oracle_sparse_mla_prefill.restype = None
+            lib.oracle_upconvert_row.argtypes = [P, P]
+            lib.oracle_upconvert_row.restype = None
+            lib.oracle_gather_upconvert.argtypes = [P, i64, P, i32, i32, P, P, P, i64]
+            lib.oracle_gather_upconvert.restype = None
+            lib.oracle_translate_workspace.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i64, i32, P]
+            lib.oracle_translate_workspace.restype = None
             _lib = lib
     return _lib
 
@@ -176,3 +182,60 @@ def sparse_mla_prefill(q_bits, kv_bits, indices, sm_scale: float, tokens=None, n
     _load().oracle_sparse_mla_prefill(_p(q), _p(kv), _p(idx), float(sm_scale), T, H, N, K, _p(tok), n,
                                       _p(ws_rows), _p(ws_s), nth, _p(out), _p(lse))
     return out, lse
+
+
+# ---------------------------------------------------------------- separate-mode FP8 prefill
+
+def upconvert_row(row: np.ndarray) -> np.ndarray:
+    """One 656-byte cache row -> bf16 bits uint16[576]: NoPE code * scale in
+    float32 rounded to bf16 (ties to even), RoPE as stored."""
+    row = _c(row, np.uint8).reshape(-1)
+    assert row.size == ROW_BYTES
+    out = np.empty(D_QK, np.uint16)
+    _load().oracle_upconvert_row(_p(row), _p(out))
+    return out
+
+
+def gather_upconvert(cache, block_table, seq_lens, workspace_starts, n_rows: int) -> np.ndarray:
+    """Positions 0 .. seq_lens[r] - 1 of each request r up-converted into a
+    bf16 workspace (uint16 bits [n_rows, 576]) at rows workspace_starts[r] + p;
+    rows nothing is written to are zero."""
+    assert cache.dtype == np.uint8 and cache.flags.c_contiguous
+    NB = cache.shape[0]
+    bt = _c(block_table, np.int32)
+    R, MB = bt.shape
+    sl = _c(seq_lens, np.int32)
+    st = _c(workspace_starts, np.int32)
+    assert sl.shape == (R,) and st.shape == (R,)
+    ws = np.zeros((int(n_rows), D_QK), np.uint16)
+    _load().oracle_gather_upconvert(_p(cache), NB, _p(bt), R, MB, _p(sl), _p(st), _p(ws), int(n_rows))
+    return ws
+
+
+def translate_workspace(indices, block_table, req_id_per_token, prefill_request_id, workspace_starts,
+                        num_blocks: int) -> np.ndarray:
+    """Logical top-k index -> cache slot (decode tokens, prefill_request_id < 0)
+    or prefill-workspace row (prefill tokens); int32, -1 = invalid."""
+    idx = _c(indices, np.int32)
+    bt = _c(block_table, np.int32)
+    req = _c(req_id_per_token, np.int32)
+    pr = _c(prefill_request_id, np.int32)
+    st = _c(workspace_starts, np.int32)
+    T, K = idx.shape
+    R, MB = bt.shape
+    out = np.empty((T, K), np.int32)
+    _load().oracle_translate_workspace(_p(idx), _p(bt), _p(req), _p(pr), _p(st), T, K, R, MB, int(num_blocks),
+                                       st.size, _p(out))
+    return out
+
+
+def sparse_mla_prefill_fp8(q_bits, cache, indices, block_table, req_id_per_token, seq_lens, workspace_starts,
+                           n_rows: int, sm_scale: float, tokens=None, nthreads: int | None = None):
+    """Separate-mode FP8 prefill of one chunk of prefill requests, step by
+    step as the pages do it: the requests' rows up-converted into a bf16
+    workspace, the tokens' indices mapped to workspace rows, then the bf16
+    prefill over the workspace.  Returns (out, lse) as sparse_mla_prefill."""
+    ws = gather_upconvert(cache, block_table, seq_lens, workspace_starts, n_rows)
+    req = _c(req_id_per_token, np.int32)
+    rows = translate_workspace(indices, block_table, req, req, workspace_starts, cache.shape[0])
+    return sparse_mla_prefill(q_bits, ws, rows, sm_scale, tokens=tokens, nthreads=nthreads)

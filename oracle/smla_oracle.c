@@ -21,7 +21,7 @@
  *  [OCP] OCP 8-bit floating point specification, E4M3: 1 sign, 4 exponent
  *        (bias 7), 3 mantissa bits; subnormals; no infinities; S.1111.111 NaN.
  *
- * Readings where the pages are silent (each one is also listed in the design doc):
+ * Readings where the pages are silent:
  *  R1 translate also rejects a physical block id outside [0, NB) and a request
  *     id outside [0, R) (the page would emit a slot from garbage);
  *  R2 the quantizer scale is amax/448 in float32, codes are the float32
@@ -30,7 +30,10 @@
  *  R3 V is the NoPE part, columns 0..511 of the 576-wide latent row;
  *  R4 LSE is the natural log of the sum of exp of the scaled logits; a token
  *     with no valid index has output 0 and LSE -infinity;
- *  R5 slot_mapping < 0 (or >= NB*64) skips the token.
+ *  R5 slot_mapping < 0 (or >= NB*64) skips the token;
+ *  R9 separate-mode FP8 prefill: a row is up-converted to bf16 from the float32
+ *     product code * scale (ties to even), an invalid slot gives a zero row,
+ *     and a prefill request id outside [0, P) gives -1.
  *
  * Every floating-point step of attention is in double.  The quantizer decides
  * integer codes, so it runs in float32, the precision the CUDA kernel uses.
@@ -270,6 +273,79 @@ void oracle_sparse_mla_prefill(const uint16_t* q, const uint16_t* kv, const int3
     for (int h = 0; h < H; ++h) {
       for (int c = 0; c < D_QK; ++c) qh[c] = oracle_bf16_to_double(q[((int64_t)t * H + h) * D_QK + c]);
       attend_head(qh, rows, n, sm_scale, s_buf, out + ((int64_t)i * H + h) * D_V, lse + (int64_t)i * H + h);
+    }
+  }
+}
+
+/* ---------------------------------------------------------------- separate-mode FP8 prefill */
+
+/* float32 -> bfloat16 bits, round to nearest, ties to even (finite inputs;
+ * an infinity or NaN keeps its class). */
+static uint16_t float_to_bf16_rne(float f) {
+  uint32_t u;
+  memcpy(&u, &f, 4);
+  if ((u & 0x7F800000u) == 0x7F800000u) return (uint16_t)((u >> 16) | ((u & 0xFFFFu) ? 0x40u : 0u));
+  u += 0x7FFFu + ((u >> 16) & 1u);
+  return (uint16_t)(u >> 16);
+}
+
+/* [P2 _forward_fp8_kv_separate_prefill_decode: cp_gather_and_upconvert_fp8_kv_cache]
+ * + reading R9: one cache row up-converted for the bf16 prefill kernel.  NoPE
+ * value c is e4m3(byte c) * scale[c / 128] formed in float32 (the precision
+ * of the stored scales; the e4m3 value is exact in float32) and rounded to
+ * bf16, nearest with ties to even; the 64 RoPE values are copied as stored. */
+void oracle_upconvert_row(const uint8_t* row, uint16_t* out) {
+  for (int c = 0; c < D_NOPE; ++c) {
+    float sc;
+    memcpy(&sc, row + D_NOPE + 4 * (c / GROUP), 4);
+    const float v = (float)oracle_e4m3_to_double(row[c]);
+    const float prod = v * sc;
+    out[c] = float_to_bf16_rne(prod);
+  }
+  memcpy(out + D_NOPE, row + D_NOPE + 16, 2 * (D_QK - D_NOPE));
+}
+
+/* [P2 cp_gather_and_upconvert_fp8_kv_cache(cache, workspace, block_table,
+ * seq_lens, workspace_starts, num_reqs)]: positions 0 .. seq_lens[r] - 1 of
+ * request r, in order, become workspace rows starts[r] .. starts[r] +
+ * seq_lens[r] - 1.  A position whose slot is invalid under R1 gives a row of
+ * zeros (reading R9); a destination outside [0, N) is not written. */
+void oracle_gather_upconvert(const uint8_t* cache, int64_t NB, const int32_t* block_table, int R, int MB,
+                             const int32_t* seq_lens, const int32_t* starts, uint16_t* ws, int64_t N) {
+  for (int r = 0; r < R; ++r) {
+    for (int32_t pos = 0; pos < seq_lens[r]; ++pos) {
+      const int64_t dst = (int64_t)starts[r] + pos;
+      if (dst < 0 || dst >= N) continue;
+      const int32_t slot = oracle_translate_one(pos, r, block_table, R, MB, NB);
+      if (slot < 0)
+        memset(ws + dst * D_QK, 0, 2 * D_QK);
+      else
+        oracle_upconvert_row(cache + (int64_t)slot * ROW_BYTES, ws + dst * D_QK);
+    }
+  }
+}
+
+/* [P2 _convert_req_index_to_global_index_kernel with HAS_PREFILL and its
+ * docstring]: a decode token (prefill_req_id < 0) is translated as above; a
+ * prefill token's index becomes workspace_starts[prefill_req_id] + index,
+ * -1 when the index is negative or its block id is outside [0, MB) (the
+ * kernel's own guard), or (reading R9) when prefill_req_id >= P. */
+void oracle_translate_workspace(const int32_t* indices, const int32_t* block_table, const int32_t* req_id,
+                                const int32_t* prefill_req_id, const int32_t* starts, int T, int K, int R, int MB,
+                                int64_t NB, int P, int32_t* out) {
+  for (int t = 0; t < T; ++t) {
+    const int32_t pr = prefill_req_id[t];
+    for (int k = 0; k < K; ++k) {
+      const int32_t idx = indices[(int64_t)t * K + k];
+      int32_t v;
+      if (pr < 0) {
+        v = oracle_translate_one(idx, req_id[t], block_table, R, MB, NB);
+      } else if (idx < 0 || idx / BLOCK >= MB || pr >= P) {
+        v = -1;
+      } else {
+        v = starts[pr] + idx;
+      }
+      out[(int64_t)t * K + k] = v;
     }
   }
 }

@@ -387,3 +387,129 @@ def test_generators_are_deterministic_and_well_formed():
     # bf16 conversion used by the generators is torch's round-to-nearest-even
     x = np.random.default_rng(0).standard_normal(1000).astype(np.float32)
     assert np.array_equal(inp.bf16_bits(x), torch.from_numpy(x).to(torch.bfloat16).view(torch.uint16).numpy())
+
+
+# ---------------------------------------------------------------- separate-mode FP8 prefill
+
+def _bf16_value(bits):
+    return inp.bits_to_float(np.asarray(bits, np.uint16)).astype(np.float64)
+
+
+def _random_rows(rng, n, pow2_scales=False):
+    """n 656-byte rows: random codes (no NaN), random or power-of-two scales, random bf16 RoPE."""
+    rows = np.zeros((n, 656), np.uint8)
+    codes = rng.integers(0, 256, size=(n, 512)).astype(np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0x00
+    rows[:, :512] = codes
+    if pow2_scales:
+        sc = np.ldexp(1.0, rng.integers(-20, 10, size=(n, 4))).astype(np.float32)
+    else:
+        sc = (np.exp(rng.uniform(np.log(1e-6), np.log(1e4), size=(n, 4)))).astype(np.float32)
+    rows[:, 512:528] = sc.astype("<f4").view(np.uint8)
+    rows[:, 528:656] = inp.bf16_bits(rng.standard_normal((n, 64)).astype(np.float32)).view(np.uint8)
+    return rows
+
+
+def test_upconvert_row_exact_for_power_of_two_scales():
+    # e4m3 values have 4 significant bits, so code * 2^k is a bf16 value: the
+    # up-converted row equals the float64 dequantization exactly
+    rows = _random_rows(np.random.default_rng(11), 64, pow2_scales=True)
+    for row in rows:
+        assert np.array_equal(_bf16_value(oracle.upconvert_row(row)), oracle.dequant_row(row))
+
+
+def test_upconvert_row_matches_torch_float32_product_rounded_to_bf16():
+    rows = _random_rows(np.random.default_rng(12), 256)
+    codes = torch.from_numpy(rows[:, :512].copy()).view(torch.float8_e4m3fn).to(torch.float32)
+    scales = torch.from_numpy(rows[:, 512:528].copy().view(np.float32))
+    ref = (codes.view(-1, 4, 128) * scales[:, :, None]).view(-1, 512).to(torch.bfloat16)
+    ref_bits = ref.view(torch.int16).numpy().view(np.uint16)
+    got = np.stack([oracle.upconvert_row(r) for r in rows])
+    assert np.array_equal(got[:, :512], ref_bits)
+    assert np.array_equal(got[:, 512:], rows[:, 528:656].copy().view(np.uint16))  # RoPE as stored
+    # and within half a bf16 unit of the exact dequantization
+    deq = np.stack([oracle.dequant_row(r) for r in rows])[:, :512]
+    err = np.abs(_bf16_value(got[:, :512]) - deq)
+    assert np.all(err <= np.abs(deq) * 2.0 ** -8 * (1 + 2.0 ** -15) + 1e-45)
+
+
+def test_gather_upconvert_by_block_table_expansion():
+    rng = np.random.default_rng(13)
+    NB, R, MB = 12, 3, 4
+    cache = _random_rows(rng, NB * 64).reshape(NB, 64, 656)
+    perm = rng.permutation(NB).astype(np.int32)
+    bt = perm[:R * MB].reshape(R, MB).copy()
+    bt[2, 3] = NB + 5  # an invalid physical block: its positions give zero rows
+    seq_lens = np.array([70, 0, 250], np.int32)
+    starts = np.array([3, 73, 80], np.int32)
+    N = 340
+    ws = oracle.gather_upconvert(cache, bt, seq_lens, starts, N)
+    expect = np.zeros((N, 576), np.uint16)
+    for r in range(R):
+        for pos in range(seq_lens[r]):
+            p = int(bt[r, pos // 64])
+            if 0 <= p < NB:
+                expect[starts[r] + pos] = oracle.upconvert_row(cache[p, pos % 64])
+    assert np.array_equal(ws, expect)
+
+
+def test_translate_workspace_golden():
+    bt_rows, cases, nb, starts = {}, [], None, None
+    with open(os.path.join(GOLDEN, "translate_workspace_small.txt")) as f:
+        for line in f:
+            tok = line.split("#")[0].split()
+            if not tok:
+                continue
+            if tok[0] == "block_table":
+                bt_rows[int(tok[1])] = [int(v) for v in tok[2:]]
+            elif tok[0] == "num_blocks":
+                nb = int(tok[1])
+            elif tok[0] == "starts":
+                starts = np.array([int(v) for v in tok[1:]], np.int32)
+            elif tok[0] == "case":
+                cases.append(tuple(int(v) for v in tok[1:5]))
+    bt = np.array([bt_rows[r] for r in sorted(bt_rows)], np.int32)
+    req = np.array([c[0] for c in cases], np.int32)
+    pr = np.array([c[1] for c in cases], np.int32)
+    idx = np.array([[c[2]] for c in cases], np.int32)
+    got = oracle.translate_workspace(idx, bt, req, pr, starts, nb)[:, 0]
+    assert got.tolist() == [c[3] for c in cases]
+
+
+def test_translate_workspace_decode_tokens_as_translate_prefill_tokens_offset():
+    rng = np.random.default_rng(14)
+    R, MB, NB, T, K = 5, 6, 40, 30, 50
+    bt = rng.integers(-2, NB + 3, size=(R, MB)).astype(np.int32)
+    req = rng.integers(0, R, size=T).astype(np.int32)
+    pr = np.where(rng.random(T) < 0.5, rng.integers(0, 3, size=T), -1).astype(np.int32)
+    starts = np.array([0, 200, 450], np.int32)
+    idx = rng.integers(-3, MB * 64 + 40, size=(T, K)).astype(np.int32)
+    got = oracle.translate_workspace(idx, bt, req, pr, starts, NB)
+    dec = pr < 0
+    assert np.array_equal(got[dec], oracle.translate(idx[dec], bt, req[dec], NB))
+    expect = np.where((idx >= 0) & (idx // 64 < MB), starts[np.maximum(pr, 0)][:, None] + idx, -1)
+    assert np.array_equal(got[~dec], expect[~dec])
+
+
+def test_prefill_fp8_equals_decode_when_upconvert_is_exact():
+    # With power-of-two scales the up-converted rows are the dequantized rows,
+    # so the separate-mode prefill (workspace + bf16 prefill) must give the
+    # decode path's result for the same tokens and logical indices.
+    rng = np.random.default_rng(15)
+    R, ctx, H, K = 3, 300, 16, 96
+    nblk = (ctx + 63) // 64
+    NB = R * nblk
+    cache = _random_rows(rng, NB * 64, pow2_scales=True).reshape(NB, 64, 656)
+    cache[..., :512] = np.where((cache[..., :512] & 0x78) >= 0x58, 0x30, cache[..., :512])  # keep logits moderate
+    bt = rng.permutation(NB).astype(np.int32).reshape(R, nblk)
+    seq_lens = np.full(R, ctx, np.int32)
+    starts = np.array([0, ctx, 2 * ctx], np.int32)
+    T = 7
+    req = rng.integers(0, R, size=T).astype(np.int32)
+    idx = np.stack([rng.choice(ctx, size=K, replace=False) for _ in range(T)]).astype(np.int32)
+    idx[0, :10] = -1
+    q = inp.bf16_bits(rng.standard_normal((T, H, 576)).astype(np.float32) * 0.05)
+    sm = 576 ** -0.5
+    o1, l1 = oracle.sparse_mla_prefill_fp8(q, cache, idx, bt, req, seq_lens, starts, R * ctx, sm)
+    o2, l2 = oracle.sparse_mla_decode(q, cache, idx, bt, req, sm)
+    assert np.allclose(o1, o2, rtol=1e-12, atol=1e-12) and np.allclose(l1, l2, rtol=0, atol=1e-12)
