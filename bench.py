@@ -404,7 +404,8 @@ def run_ours(args):
     if rank == 0 and world == 1 and not args.no_extra:
         del cache
         torch.cuda.empty_cache()
-        for name, k in (("decode_h128_k2048", max(20, args.steps // 20)), ("prefill_h128_k2048", max(5, args.steps // 200))):
+        for name, k in (("decode_h128_k2048", max(20, args.steps // 20)), ("prefill_h128_k2048", max(5, args.steps // 200)),
+                        ("prefill_fp8_h128_k2048", max(5, args.steps // 200))):
             sub = argparse.Namespace(**vars(args))
             sub.workload, sub.steps = name, k
             sub.no_cpu_baseline = True
@@ -531,6 +532,55 @@ def tensor_workload(args, quiet=False):
         def oracle_run():
             oracle.sparse_mla_decode(case.q, hcache, case.index_sets[0], case.block_table, case.req_id_per_token,
                                      case.sm_scale, tokens=tok, nthreads=nth)
+    elif args.workload == "prefill_fp8_h128_k2048":
+        # the bf16 prefill workload's shape over the FP8 paged cache, separate mode: each call gathers and
+        # up-converts the chunk's 4 x 4096 rows into a bf16 workspace, maps the indices, runs the bf16 prefill
+        case = inp.fp8_prefill_chunk(seed=5)
+        T, H, K, NB = case.T, case.H, case.K, case.num_blocks
+        R = case.block_table.shape[0]
+        seq_lens = np.zeros(R, np.int32)
+        for t in range(T):
+            r = case.req_id_per_token[t]
+            seq_lens[r] = max(seq_lens[r], case.positions[t] + 1)
+        starts = np.concatenate([[0], np.cumsum(seq_lens)[:-1]]).astype(np.int32)
+        N = int(seq_lens.sum())
+        with torch.cuda.stream(stream):
+            cache = torch.zeros((NB, 64, 656), dtype=torch.uint8, device=device)
+            smla.mla_cache_store_fp8(bf16(case.cache_rows), torch.from_numpy(case.cache_slots).to(device), cache,
+                                     stream=stream)
+            smla.mla_cache_store_fp8(bf16(case.new_rows), torch.from_numpy(case.new_slots).to(device), cache,
+                                     stream=stream)
+            q = bf16(case.q)
+            idx = torch.from_numpy(case.indices).to(device)
+            bt = torch.from_numpy(case.block_table).to(device)
+            req = torch.from_numpy(case.req_id_per_token).to(device)
+            d_sl = torch.from_numpy(seq_lens).to(device)
+            d_st = torch.from_numpy(starts).to(device)
+            kvw = torch.empty((N, 576), dtype=torch.bfloat16, device=device)
+            ws = torch.zeros(smla.prefill_fp8_workspace_bytes(T, H, K, 0), dtype=torch.uint8, device=device)
+            out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=device)
+            lse = torch.empty((T, H), dtype=torch.float32, device=device)
+        stream.synchronize()
+
+        def launch(i):
+            smla.sparse_mla_prefill_fp8(q, cache, idx, bt, req, d_sl, d_st, kvw, case.sm_scale, 0, out, lse, ws,
+                                        stream=stream)
+        n_graphs = 1
+        flops = 2 * H * int((case.indices >= 0).sum()) * (576 + 512)
+        fp8 = False
+        mma_dtype = "bf16"
+        launches = 2 + smla.attention_plan(False, T, H, K, 0)[0]  # gather + translate + the prefill's launches
+        desc = (f"{case.name}: separate-mode FP8 prefill, 4 requests x 1024 new tokens over 3072 cached in the "
+                f"656-byte FP8 paged cache, H={H}, top-k {K}: gather + up-convert of {N} rows to bf16, index "
+                f"mapping, bf16 prefill")
+        tok = np.linspace(0, T - 1, min(nth, 8)).astype(np.int32)
+        host_cache = np.zeros((NB, 64, 656), np.uint8)
+        oracle.quantize_store(case.cache_rows, case.cache_slots, host_cache)
+        oracle.quantize_store(case.new_rows, case.new_slots, host_cache)
+
+        def oracle_run():
+            oracle.sparse_mla_prefill_fp8(case.q, host_cache, case.indices, case.block_table, case.req_id_per_token,
+                                          seq_lens, starts, N, case.sm_scale, tokens=tok, nthreads=nth)
     else:
         case = inp.prefill(seed=3)
         T, H, K = case.T, case.H, case.K
@@ -717,7 +767,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true",
                     help="leave the tensor-bound configurations out of the default line")
-    ap.add_argument("--workload", choices=["decode_h16_k2048", "decode_h128_k2048", "prefill_h128_k2048"],
+    ap.add_argument("--workload", choices=["decode_h16_k2048", "decode_h128_k2048", "prefill_h128_k2048",
+                                           "prefill_fp8_h128_k2048"],
                     default="decode_h16_k2048",
                     help="decode_h16_k2048 (default) is the headline; the other two are the tensor-bound "
                          "configurations, reported on their own line")

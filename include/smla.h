@@ -93,13 +93,13 @@ size_t sparse_mla_decode_workspace_bytes(int T, int H, int K, int num_splits);
  *     rejected with SMLA_ERR_WORKSPACE; num_splits = 1, or fewer tokens per
  *     call, needs less.
  *   - Every call shares the one scratch array per device and leaves its
- *     contents behind; the call clears the status word it needs at zero (an
- *     asynchronous memset on `stream`) and overwrites everything else it
- *     reads.  Calls whose execution overlaps on the GPU (other streams, other
+ *     contents behind; a call overwrites everything it reads before reading
+ *     it.  Calls whose execution overlaps on the GPU (other streams, other
  *     host threads) race on the scratch and give wrong results: serialize
  *     them, or use sparse_mla_decode_fp8 with one workspace per stream.
- *   - The device status word of these calls is not exposed; a kernel wait
- *     that runs past its time limit still ends the kernel. */
+ *   - The scratch's device status word records a kernel wait that ran past
+ *     its time limit (the kernel still ends); smla_read_noalloc_status reads
+ *     and clears it. */
 #define SMLA_NOALLOC_SCRATCH_BYTES (32u << 20)
 int sparse_mla_decode_fp8_noalloc(const void* q, const uint8_t* kv_cache, const int32_t* indices,
                                   const int32_t* block_table, const int32_t* req_id_per_token, float sm_scale,
@@ -117,6 +117,63 @@ int sparse_mla_prefill_bf16(const void* q, const void* kv, const int32_t* indice
                             size_t workspace_bytes, void* stream);
 
 size_t sparse_mla_prefill_workspace_bytes(int T, int H, int K, int num_splits);
+
+/* Separate-mode FP8 prefill of one chunk of prefill requests
+ * (FlashMLASparseImpl._forward_fp8_kv_separate_prefill_decode in
+ * [flashmla_sparse.py], the path taken for prefill tokens over the FP8 cache):
+ *   1. positions 0 .. seq_lens[r] - 1 of each request r of the chunk are
+ *      gathered from the cache and up-converted into kv_workspace rows
+ *      workspace_starts[r] + p (as sparse_mla_gather_upconvert_fp8);
+ *   2. each token's logical top-k indices become kv_workspace rows
+ *      workspace_starts[req_id_per_token[t]] + idx (as
+ *      sparse_mla_translate_indices_workspace with every token a prefill token);
+ *   3. the bf16 sparse prefill (sparse_mla_prefill_bf16) runs over kv_workspace.
+ *   q bf16 [T, H, 576]; kv_cache uint8 [NB, 64, 656]; indices int32 [T, K] logical positions within the
+ *   token's request (< 0 = none); block_table int32 [R, MB] of the chunk's requests; req_id_per_token int32 [T]
+ *   in [0, R); seq_lens, workspace_starts int32 [R] (chunk-local rows, e.g. from sparse_mla_prefill_chunks);
+ *   out bf16 [T, H, 512], lse fp32 [T, H] as for sparse_mla_prefill_bf16.
+ *   kv_workspace  bf16 [N, 576], caller-owned, 16-byte aligned; rows the chunk does not cover are not read
+ *                 unless an index points there (then they are read as they are).
+ *   workspace     at least sparse_mla_prefill_fp8_workspace_bytes(T, H, K, num_splits) bytes, 256-byte
+ *                 aligned (the prefill's status word and partial results, then the translated indices;
+ *                 smla_read_device_status reads it); NULL = library-cached.
+ * An index whose block id is outside [0, MB) is masked, as is a row outside [0, N). */
+int sparse_mla_prefill_fp8(const void* q, const uint8_t* kv_cache, const int32_t* indices, const int32_t* block_table,
+                           const int32_t* req_id_per_token, const int32_t* seq_lens, const int32_t* workspace_starts,
+                           float sm_scale, int num_splits, void* out, float* lse, int T, int H, int K, int R, int MB,
+                           int NB, void* kv_workspace, int N, void* workspace, size_t workspace_bytes, void* stream);
+
+size_t sparse_mla_prefill_fp8_workspace_bytes(int T, int H, int K, int num_splits);
+
+/* Gather and up-convert of the FP8 prefill (ops.cp_gather_and_upconvert_fp8_kv_cache as called by
+ * _forward_fp8_kv_separate_prefill_decode in [flashmla_sparse.py]): for each request r < R and position
+ * p < seq_lens[r], the cache row at block_table[r, p // 64] * 64 + p % 64 becomes bf16 row
+ * workspace_starts[r] + p of kv_workspace [N, 576]: value c < 512 is the float32 product
+ * e4m3(code c) * scale[c / 128] rounded to bf16 (nearest, ties to even), the 64 RoPE values are copied.
+ * A position whose physical block is outside [0, NB) gives a zero row; a destination row outside
+ * [0, N) is not written.  seq_lens, workspace_starts int32 [R] device arrays. */
+int sparse_mla_gather_upconvert_fp8(const uint8_t* kv_cache, const int32_t* block_table, const int32_t* seq_lens,
+                                    const int32_t* workspace_starts, int R, int MB, int NB, void* kv_workspace, int N,
+                                    void* stream);
+
+/* Index translation with a prefill workspace (triton_convert_req_index_to_global_index with
+ * HAS_PREFILL_WORKSPACE in [flashmla_sparse.py]): for a token with prefill_request_id[t] < 0 (a
+ * decode token) out = the cache slot of sparse_mla_translate_indices; for a prefill token
+ * out = workspace_starts[prefill_request_id[t]] + idx; -1 when idx < 0, idx // 64 >= MB, or
+ * prefill_request_id[t] >= P.  prefill_request_id int32 [T]; workspace_starts int32 [P]; out int32 [T, K]. */
+int sparse_mla_translate_indices_workspace(const int32_t* indices, const int32_t* block_table,
+                                           const int32_t* req_id_per_token, const int32_t* prefill_request_id,
+                                           const int32_t* workspace_starts, int P, int32_t* out, int T, int K, int R,
+                                           int MB, int NB, void* stream);
+
+/* Host-side chunking of prefill requests into workspaces of workspace_rows rows (split_prefill_chunks
+ * and the per-chunk workspace starts of FlashMLASparseMetadataBuilder in [flashmla_sparse.py]): requests
+ * are taken in order and a chunk is closed before the request that would overflow it.  HOST arrays:
+ * seq_lens [R] in; chunk_ends [R] out (exclusive end request of each chunk, *n_chunks of them);
+ * workspace_starts [R] out (chunk-local first row of each request).  SMLA_ERR_WORKSPACE if one
+ * request alone exceeds workspace_rows.  No device work. */
+int sparse_mla_prefill_chunks(const int32_t* seq_lens, int R, int64_t workspace_rows, int32_t* chunk_ends,
+                              int32_t* workspace_starts, int* n_chunks);
 
 /* Work split of one attention call on the current device, for callers that
  * count kernel launches or size grids (no work is done):
@@ -155,6 +212,13 @@ int sparse_mla_translate_indices(const int32_t* indices, const int32_t* block_ta
  * limit and the kernel unwound (its outputs are not valid).  workspace NULL =
  * the library-cached workspace of the current device. */
 int smla_read_device_status(void* workspace, int* status_out, void* stream);
+
+/* smla_read_device_status for the fixed scratch of
+ * sparse_mla_decode_fp8_noalloc on the current device: synchronizes
+ * `stream`, then reads and clears the status word (0 = no fault; 1 = a kernel
+ * wait ran past its time limit and the kernel unwound, so the outputs of the
+ * calls since the last read are not valid). */
+int smla_read_noalloc_status(int* status_out, void* stream);
 
 /* Thread-local description of the last failing call on this thread. */
 const char* smla_last_error(void);

@@ -225,6 +225,18 @@ def mixed_batch(seed: int = 4, n_decode: int = 32, decode_qlen: int = 2, n_prefi
                         prefill_reqs=tuple(range(n_decode, n_decode + n_prefill)))
 
 
+def fp8_prefill_chunk(seed: int = 5, R: int = 4, cached: int = 3072, new: int = 1024, K: int = 2048,
+                      H: int = 128) -> DecodeCase:
+    """One chunk of R prefill requests over the FP8 paged cache: request r
+    has ``cached`` positions already in the cache and ``new`` query tokens
+    (positions cached .. cached + new - 1, written by quantize-and-store);
+    token at position p attends to K unique positions in [0, p] (-1 padding
+    when fewer are visible); latent N(0,1); shuffled block table."""
+    ctx = np.full(R, cached + new, np.int64)
+    return _decode_case(f"fp8_prefill_h{H}_k{K}_t{R * new}", seed + 1000, ctx, np.full(R, new, np.int64), H, K,
+                        prefill_reqs=tuple(range(R)), all_context_rows=True)
+
+
 def prefill(seed: int = 3, R: int = 4, cached: int = 3072, new: int = 1024, K: int = 2048, H: int = 128) -> PrefillCase:
     """R requests x ``new`` tokens appended to ``cached`` tokens each, in a
     dense bf16 latent buffer of R*(cached+new) rows; token i of request r sits

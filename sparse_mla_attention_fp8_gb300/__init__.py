@@ -8,7 +8,10 @@ not been built, or a tensor is not on a CUDA device, the call raises.
 
 Entry points (see include/smla.h for layouts and semantics):
   sparse_mla_decode_fp8, sparse_mla_prefill_bf16, mla_cache_store_fp8,
-  sparse_mla_translate_indices, plus workspace-size and status helpers.
+  sparse_mla_translate_indices, the separate-mode FP8 prefill
+  (sparse_mla_prefill_fp8 with its steps sparse_mla_gather_upconvert_fp8 and
+  sparse_mla_translate_indices_workspace, and the host-side
+  sparse_mla_prefill_chunks), plus workspace-size and status helpers.
 """
 from __future__ import annotations
 
@@ -108,6 +111,19 @@ def lib():
             L.sparse_mla_translate_indices.restype = i32
             L.smla_read_device_status.argtypes = [P, ctypes.POINTER(ctypes.c_int), P]
             L.smla_read_device_status.restype = i32
+            L.sparse_mla_prefill_fp8.argtypes = [P, P, P, P, P, P, P, f32, i32, P, P, i32, i32, i32, i32, i32, i32,
+                                                 P, i32, P, sz, P]
+            L.sparse_mla_prefill_fp8.restype = i32
+            L.sparse_mla_prefill_fp8_workspace_bytes.argtypes = [i32, i32, i32, i32]
+            L.sparse_mla_prefill_fp8_workspace_bytes.restype = sz
+            L.sparse_mla_gather_upconvert_fp8.argtypes = [P, P, P, P, i32, i32, i32, P, i32, P]
+            L.sparse_mla_gather_upconvert_fp8.restype = i32
+            L.sparse_mla_translate_indices_workspace.argtypes = [P, P, P, P, P, i32, P, i32, i32, i32, i32, i32, P]
+            L.sparse_mla_translate_indices_workspace.restype = i32
+            L.sparse_mla_prefill_chunks.argtypes = [P, i32, ctypes.c_int64, P, P, ctypes.POINTER(i32)]
+            L.sparse_mla_prefill_chunks.restype = i32
+            L.smla_read_noalloc_status.argtypes = [ctypes.POINTER(ctypes.c_int), P]
+            L.smla_read_noalloc_status.restype = i32
             L.smla_last_error.argtypes = []
             L.smla_last_error.restype = ctypes.c_char_p
             L.smla_version.argtypes = []
@@ -264,6 +280,102 @@ def sparse_mla_prefill_bf16(q, kv, indices, sm_scale: float, num_splits: int = 0
     return out, lse
 
 
+def prefill_fp8_workspace_bytes(T: int, H: int, K: int, num_splits: int = 0) -> int:
+    return int(lib().sparse_mla_prefill_fp8_workspace_bytes(T, H, K, num_splits))
+
+
+def sparse_mla_prefill_fp8(q, kv_cache, indices, block_table, req_id_per_token, seq_lens, workspace_starts,
+                           kv_workspace, sm_scale: float, num_splits: int = 0, out=None, lse=None, workspace=None,
+                           stream=None):
+    """Separate-mode FP8 prefill of one chunk of prefill requests: the
+    requests' cache rows up-converted into kv_workspace (bf16 [N, 576]), the
+    logical indices mapped to its rows, then the bf16 prefill.  q bf16
+    [T,H,576]; kv_cache uint8 [NB,64,656]; indices int32 [T,K]; block_table
+    int32 [R,MB]; req_id_per_token int32 [T]; seq_lens, workspace_starts int32
+    [R].  Returns (out bf16 [T,H,512], lse fp32 [T,H])."""
+    import torch
+    dev = _dev(q, kv_cache, indices, block_table, req_id_per_token, seq_lens, workspace_starts, kv_workspace, out,
+               lse, workspace)
+    T, H, _ = q.shape
+    NB = kv_cache.shape[0]
+    K = indices.shape[1]
+    R, MB = block_table.shape
+    N = kv_workspace.shape[0]
+    _expect(q, torch.bfloat16, (T, H, 576), "q")
+    _expect(kv_cache, torch.uint8, (NB, 64, 656), "kv_cache")
+    _expect(indices, torch.int32, (T, K), "indices")
+    _expect(req_id_per_token, torch.int32, (T,), "req_id_per_token")
+    _expect(seq_lens, torch.int32, (R,), "seq_lens")
+    _expect(workspace_starts, torch.int32, (R,), "workspace_starts")
+    _expect(kv_workspace, torch.bfloat16, (N, 576), "kv_workspace")
+    if block_table.dtype != torch.int32:
+        raise SmlaError("block_table must be int32")
+    if out is None:
+        out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+    _expect(out, torch.bfloat16, (T, H, 512), "out")
+    _expect(lse, torch.float32, (T, H), "lse")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib().sparse_mla_prefill_fp8(_ptr(q), _ptr(kv_cache), _ptr(indices), _ptr(block_table),
+                                      _ptr(req_id_per_token), _ptr(seq_lens), _ptr(workspace_starts),
+                                      float(sm_scale), int(num_splits), _ptr(out), _ptr(lse), T, H, K, R, MB, NB,
+                                      _ptr(kv_workspace), N, _ptr(workspace), ws_bytes, _stream_ptr(stream, dev))
+    _check(rc, "sparse_mla_prefill_fp8")
+    return out, lse
+
+
+def sparse_mla_gather_upconvert_fp8(kv_cache, block_table, seq_lens, workspace_starts, kv_workspace, stream=None):
+    """Up-convert positions 0 .. seq_lens[r] - 1 of each request into
+    kv_workspace (bf16 [N, 576]) rows workspace_starts[r] + p."""
+    import torch
+    dev = _dev(kv_cache, block_table, seq_lens, workspace_starts, kv_workspace)
+    R, MB = block_table.shape
+    _expect(kv_workspace, torch.bfloat16, (kv_workspace.shape[0], 576), "kv_workspace")
+    rc = lib().sparse_mla_gather_upconvert_fp8(_ptr(kv_cache), _ptr(block_table), _ptr(seq_lens),
+                                               _ptr(workspace_starts), R, MB, kv_cache.shape[0], _ptr(kv_workspace),
+                                               kv_workspace.shape[0], _stream_ptr(stream, dev))
+    _check(rc, "sparse_mla_gather_upconvert_fp8")
+    return kv_workspace
+
+
+def sparse_mla_translate_indices_workspace(indices, block_table, req_id_per_token, prefill_request_id,
+                                           workspace_starts, num_blocks: int, out=None, stream=None):
+    """Logical top-k indices -> cache slots (decode tokens) or prefill
+    workspace rows (prefill tokens), int32 [T, K], -1 = none."""
+    import torch
+    dev = _dev(indices, block_table, req_id_per_token, prefill_request_id, workspace_starts, out)
+    T, K = indices.shape
+    R, MB = block_table.shape
+    if out is None:
+        out = torch.empty((T, K), dtype=torch.int32, device=dev)
+    rc = lib().sparse_mla_translate_indices_workspace(_ptr(indices), _ptr(block_table), _ptr(req_id_per_token),
+                                                      _ptr(prefill_request_id), _ptr(workspace_starts),
+                                                      workspace_starts.numel(), _ptr(out), T, K, R, MB,
+                                                      int(num_blocks), _stream_ptr(stream, dev))
+    _check(rc, "sparse_mla_translate_indices_workspace")
+    return out
+
+
+def sparse_mla_prefill_chunks(seq_lens, workspace_rows: int):
+    """Host-side chunking of prefill requests (a sequence of ints) into
+    workspaces of ``workspace_rows`` rows: returns (list of (start, end)
+    request ranges, list of chunk-local workspace starts)."""
+    R = len(seq_lens)
+    sl = (ctypes.c_int32 * max(R, 1))(*[int(v) for v in seq_lens])
+    ends = (ctypes.c_int32 * max(R, 1))()
+    starts = (ctypes.c_int32 * max(R, 1))()
+    n = ctypes.c_int32(0)
+    _check(lib().sparse_mla_prefill_chunks(ctypes.cast(sl, ctypes.c_void_p), R, int(workspace_rows),
+                                           ctypes.cast(ends, ctypes.c_void_p), ctypes.cast(starts, ctypes.c_void_p),
+                                           ctypes.byref(n)), "sparse_mla_prefill_chunks")
+    bounds, b = [], 0
+    for i in range(n.value):
+        bounds.append((b, int(ends[i])))
+        b = int(ends[i])
+    return bounds, [int(starts[i]) for i in range(R)]
+
+
 def mla_cache_store_fp8(kv_new, slot_mapping, kv_cache, stream=None):
     """Quantize bf16 [T,576] rows into kv_cache uint8 [NB,64,656] at
     slot_mapping int64 [T] (<0 skips).  Modifies kv_cache in place."""
@@ -291,6 +403,16 @@ def sparse_mla_translate_indices(indices, block_table, req_id_per_token, num_blo
                                             T, K, R, MB, int(num_blocks), _stream_ptr(stream, dev))
     _check(rc, "sparse_mla_translate_indices")
     return out
+
+
+def read_noalloc_status(stream=None) -> int:
+    """Synchronize and read/clear the status word of the allocation-free
+    decode's fixed scratch on the current device (0 = ok)."""
+    import torch
+    st = ctypes.c_int(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    _check(lib().smla_read_noalloc_status(ctypes.byref(st), _stream_ptr(stream, dev)), "smla_read_noalloc_status")
+    return int(st.value)
 
 
 def read_device_status(workspace=None, stream=None) -> int:

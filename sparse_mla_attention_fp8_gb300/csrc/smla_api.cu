@@ -144,6 +144,9 @@ int noalloc_scratch(void** out) {
   return SMLA_OK;
 }
 
+// Bytes of the translated index rows of sparse_mla_prefill_fp8 (256-byte aligned).
+size_t fp8_prefill_index_bytes(int T, int K) { return (((size_t)T * (size_t)K * 4 + 255) / 256) * 256; }
+
 }  // namespace
 
 extern "C" {
@@ -210,9 +213,10 @@ int sparse_mla_decode_fp8_noalloc(const void* q, const uint8_t* kv_cache, const 
   rc = noalloc_scratch(&scratch);
   if (rc != SMLA_OK) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // the status word must start at zero; partial results are written before they are read
-  cudaError_t e = cudaMemsetAsync(scratch, 0, smla::kWsStatusBytes, s);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(no-alloc status)");
+  // The status word starts at zero (the array is zero-initialised when the
+  // module loads) and only a kernel wait that runs out sets it, so nothing
+  // needs clearing per call: smla_read_noalloc_status reads and clears it.
+  // Partial results are written before they are read.
   smla::AttnArgs a{};
   a.q = q;
   a.cache = kv_cache;
@@ -230,7 +234,7 @@ int sparse_mla_decode_fp8_noalloc(const void* q, const uint8_t* kv_cache, const 
   a.MB = MB;
   a.NB = NB;
   a.workspace = scratch;
-  e = smla::launch_decode_fp8(a, plan, s);
+  cudaError_t e = smla::launch_decode_fp8(a, plan, s);
   if (e != cudaSuccess) return cuda_fail(e, "sparse_mla_decode_fp8_noalloc launch");
   return SMLA_OK;
 }
@@ -271,6 +275,141 @@ int sparse_mla_prefill_bf16(const void* q, const void* kv, const int32_t* indice
 
 size_t sparse_mla_prefill_workspace_bytes(int T, int H, int K, int num_splits) {
   return workspace_bytes_for(false, T, H, K, num_splits);
+}
+
+// ---- separate-mode FP8 prefill
+
+size_t sparse_mla_prefill_fp8_workspace_bytes(int T, int H, int K, int num_splits) {
+  const size_t attn = workspace_bytes_for(false, T, H, K, num_splits);
+  if (attn == 0) return 0;
+  return ((attn + 255) / 256) * 256 + fp8_prefill_index_bytes(T, K);
+}
+
+int sparse_mla_gather_upconvert_fp8(const uint8_t* kv_cache, const int32_t* block_table, const int32_t* seq_lens,
+                                    const int32_t* workspace_starts, int R, int MB, int NB, void* kv_workspace, int N,
+                                    void* stream) {
+  if (R < 0 || MB <= 0 || NB <= 0 || N < 0) return fail(SMLA_ERR_INVALID_ARG, "bad sizes R=%d MB=%d NB=%d N=%d", R, MB, NB, N);
+  if (R == 0 || N == 0) return SMLA_OK;
+  if (!kv_cache || !block_table || !seq_lens || !workspace_starts || !kv_workspace)
+    return fail(SMLA_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned16(kv_cache) || !aligned16(kv_workspace))
+    return fail(SMLA_ERR_INVALID_ARG, "kv_cache and kv_workspace must be 16-byte aligned");
+  if ((int64_t)NB * 64 > INT32_MAX) return fail(SMLA_ERR_UNSUPPORTED, "NB*64 must fit in int32");
+  int sms = 0;
+  int rc = num_sms(&sms);
+  if (rc != SMLA_OK) return rc;
+  cudaError_t e = smla::launch_gather_upconvert(kv_cache, NB, block_table, R, MB, seq_lens, workspace_starts,
+                                                kv_workspace, N, sms, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "sparse_mla_gather_upconvert_fp8 launch");
+  return SMLA_OK;
+}
+
+int sparse_mla_translate_indices_workspace(const int32_t* indices, const int32_t* block_table,
+                                           const int32_t* req_id_per_token, const int32_t* prefill_request_id,
+                                           const int32_t* workspace_starts, int P, int32_t* out, int T, int K, int R,
+                                           int MB, int NB, void* stream) {
+  if (T < 0 || K < 0 || R <= 0 || MB <= 0 || NB <= 0 || P < 0)
+    return fail(SMLA_ERR_INVALID_ARG, "bad sizes T=%d K=%d R=%d MB=%d NB=%d P=%d", T, K, R, MB, NB, P);
+  if (T == 0 || K == 0) return SMLA_OK;
+  if (!indices || !block_table || !req_id_per_token || !prefill_request_id || (!workspace_starts && P > 0) || !out)
+    return fail(SMLA_ERR_INVALID_ARG, "null pointer argument");
+  if ((int64_t)NB * 64 > INT32_MAX) return fail(SMLA_ERR_UNSUPPORTED, "NB*64 must fit in int32");
+  cudaError_t e = smla::launch_translate_ws(indices, block_table, req_id_per_token, prefill_request_id,
+                                            workspace_starts, P, out, T, K, R, MB, NB, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "sparse_mla_translate_indices_workspace launch");
+  return SMLA_OK;
+}
+
+int sparse_mla_prefill_fp8(const void* q, const uint8_t* kv_cache, const int32_t* indices, const int32_t* block_table,
+                           const int32_t* req_id_per_token, const int32_t* seq_lens, const int32_t* workspace_starts,
+                           float sm_scale, int num_splits, void* out, float* lse, int T, int H, int K, int R, int MB,
+                           int NB, void* kv_workspace, int N, void* workspace, size_t workspace_bytes, void* stream) {
+  if (T < 0 || K < 0 || R <= 0 || MB <= 0 || NB <= 0 || N <= 0 || num_splits < 0)
+    return fail(SMLA_ERR_INVALID_ARG, "bad sizes T=%d K=%d R=%d MB=%d NB=%d N=%d num_splits=%d", T, K, R, MB, NB, N,
+                num_splits);
+  int rc = check_heads(H);
+  if (rc != SMLA_OK) return rc;
+  if (T == 0) return SMLA_OK;
+  if (!q || !kv_cache || (!indices && K > 0) || !block_table || !req_id_per_token || !seq_lens || !workspace_starts ||
+      !out || !lse || !kv_workspace)
+    return fail(SMLA_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned16(q) || !aligned16(kv_cache) || !aligned16(out) || !aligned16(kv_workspace))
+    return fail(SMLA_ERR_INVALID_ARG, "q, kv_cache, out and kv_workspace must be 16-byte aligned");
+  if ((int64_t)NB * 64 > INT32_MAX) return fail(SMLA_ERR_UNSUPPORTED, "NB*64 must fit in int32");
+  int sms = 0;
+  rc = num_sms(&sms);
+  if (rc != SMLA_OK) return rc;
+  const smla::AttnPlan plan = smla::plan_attention(false, T, H, K, num_splits, sms);
+  const size_t need = ((plan.ws_bytes + 255) / 256) * 256 + fp8_prefill_index_bytes(T, K);
+  if (workspace) {
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+      return fail(SMLA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    if (workspace_bytes < need) return fail(SMLA_ERR_WORKSPACE, "workspace has %zu bytes, %zu needed", workspace_bytes, need);
+  } else {
+    rc = cached_workspace(need, &workspace);
+    if (rc != SMLA_OK) return rc;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // 1. the chunk's requests' rows, up-converted to bf16 into kv_workspace
+  cudaError_t e = smla::launch_gather_upconvert(kv_cache, NB, block_table, R, MB, seq_lens, workspace_starts,
+                                                kv_workspace, N, sms, s);
+  if (e != cudaSuccess) return cuda_fail(e, "sparse_mla_prefill_fp8 gather launch");
+  // 2. the tokens' logical indices -> rows of kv_workspace (every token is a prefill token of request req_id[t]);
+  // the workspace holds the prefill's own workspace first (its status word leads), then these rows
+  const size_t attn_bytes = ((plan.ws_bytes + 255) / 256) * 256;
+  int32_t* rows = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + attn_bytes);
+  if (K > 0) {
+    e = smla::launch_translate_ws(indices, block_table, req_id_per_token, req_id_per_token, workspace_starts, R, rows,
+                                  T, K, R, MB, NB, s);
+    if (e != cudaSuccess) return cuda_fail(e, "sparse_mla_prefill_fp8 translate launch");
+  }
+  // 3. the bf16 prefill over kv_workspace; its own workspace follows the rows
+  smla::AttnArgs a{};
+  a.q = q;
+  a.cache = nullptr;
+  a.kv = kv_workspace;
+  a.indices = rows;
+  a.block_table = nullptr;
+  a.req_id = nullptr;
+  a.out = out;
+  a.lse = lse;
+  a.sm_scale = sm_scale;
+  a.T = T;
+  a.H = H;
+  a.K = K;
+  a.R = 1;
+  a.MB = 1;
+  a.NB = N;
+  a.workspace = workspace;
+  e = smla::launch_attention(false, a, plan, s);
+  if (e != cudaSuccess) return cuda_fail(e, "sparse_mla_prefill_fp8 attention launch");
+  return SMLA_OK;
+}
+
+int sparse_mla_prefill_chunks(const int32_t* seq_lens, int R, int64_t workspace_rows, int32_t* chunk_ends,
+                              int32_t* workspace_starts, int* n_chunks) {
+  if (R < 0 || workspace_rows <= 0) return fail(SMLA_ERR_INVALID_ARG, "bad sizes R=%d workspace_rows=%lld", R,
+                                                (long long)workspace_rows);
+  if (!n_chunks || (R > 0 && (!seq_lens || !chunk_ends || !workspace_starts)))
+    return fail(SMLA_ERR_INVALID_ARG, "null pointer argument");
+  int n = 0;
+  int64_t used = 0;
+  for (int r = 0; r < R; ++r) {
+    const int64_t len = seq_lens[r];
+    if (len < 0) return fail(SMLA_ERR_INVALID_ARG, "seq_lens[%d] = %lld is negative", r, (long long)len);
+    if (len > workspace_rows)
+      return fail(SMLA_ERR_WORKSPACE, "request %d has %lld rows, the workspace holds %lld", r, (long long)len,
+                  (long long)workspace_rows);
+    if (r > 0 && used + len > workspace_rows) {  // close the chunk before this request
+      chunk_ends[n++] = r;
+      used = 0;
+    }
+    workspace_starts[r] = (int32_t)used;
+    used += len;
+  }
+  if (R > 0) chunk_ends[n++] = R;
+  *n_chunks = n;
+  return SMLA_OK;
 }
 
 int sparse_mla_attention_plan(int fp8, int T, int H, int K, int num_splits, int* launches, int* ctas) {
@@ -340,6 +479,14 @@ int smla_read_device_status(void* workspace, int* status_out, void* stream) {
   }
   *status_out = v;
   return SMLA_OK;
+}
+
+int smla_read_noalloc_status(int* status_out, void* stream) {
+  if (!status_out) return fail(SMLA_ERR_INVALID_ARG, "null status_out");
+  void* scratch = nullptr;
+  int rc = noalloc_scratch(&scratch);
+  if (rc != SMLA_OK) return rc;
+  return smla_read_device_status(scratch, status_out, stream);
 }
 
 const char* smla_last_error(void) { return g_err; }

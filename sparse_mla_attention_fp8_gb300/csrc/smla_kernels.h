@@ -12,6 +12,15 @@ cudaError_t launch_quantize_store(const void* kv_new, const int64_t* slot_mappin
 cudaError_t launch_translate(const int32_t* indices, const int32_t* block_table, const int32_t* req_id,
                              int32_t* slots, int T, int K, int R, int MB, int64_t NB, cudaStream_t stream);
 
+// Separate-mode FP8 prefill: index translation with a prefill workspace, and
+// the gather + up-convert of prefill requests' cache rows into a bf16 workspace.
+cudaError_t launch_translate_ws(const int32_t* indices, const int32_t* block_table, const int32_t* req_id,
+                                const int32_t* prefill_req_id, const int32_t* starts, int P, int32_t* out, int T,
+                                int K, int R, int MB, int64_t NB, cudaStream_t stream);
+cudaError_t launch_gather_upconvert(const uint8_t* cache, int64_t NB, const int32_t* block_table, int R, int MB,
+                                    const int32_t* seq_lens, const int32_t* starts, void* ws, int64_t N,
+                                    int num_sms, cudaStream_t stream);
+
 // Work decomposition of one sparse-attention call: units are (token, head
 // group) pairs, each split into nt tiles of 64 top-k rows; G persistent CTAs
 // take contiguous, balanced ranges of the unit-major tile sequence.

@@ -97,3 +97,33 @@ def test_python_binding_has_no_cpu_path():
     with pytest.raises(smla.SmlaError):
         smla.sparse_mla_prefill_bf16(q, torch.zeros((4, 576), dtype=torch.bfloat16),
                                      torch.zeros((1, 4), dtype=torch.int32), 0.1)
+
+
+def test_prefill_chunks_docstring_example(L):
+    # flashmla_sparse.py, FlashMLASparseMetadataBuilder: seq_lens [10, 15, 20, 5] in chunks [[0, 2], [2, 4]]
+    # have workspace starts [0, 10, 0, 20] after the per-chunk adjustment (any workspace of 25..44 rows)
+    for rows in (25, 30, 44):
+        bounds, starts = smla.sparse_mla_prefill_chunks([10, 15, 20, 5], rows)
+        assert bounds == [(0, 2), (2, 4)] and starts == [0, 10, 0, 20]
+    assert smla.sparse_mla_prefill_chunks([10, 15, 20, 5], 45) == ([(0, 3), (3, 4)], [0, 10, 25, 0])
+    assert smla.sparse_mla_prefill_chunks([10, 15, 20, 5], 50) == ([(0, 4)], [0, 10, 25, 45])
+    assert smla.sparse_mla_prefill_chunks([], 8) == ([], [])
+    with pytest.raises(smla.SmlaError, match="status -4"):
+        smla.sparse_mla_prefill_chunks([10, 60, 5], 50)
+
+
+def test_prefill_fp8_rejects_bad_arguments(L):
+    args = dict(q=FAKE, cache=FAKE, idx=FAKE, bt=FAKE, req=FAKE, sl=FAKE, st=FAKE, scale=0.1, ns=0, out=FAKE,
+                lse=FAKE, T=4, H=16, K=64, R=2, MB=4, NB=16, kvw=FAKE, N=128, ws=None, wsb=0, stream=None)
+
+    def call(**kw):
+        a = dict(args)
+        a.update(kw)
+        return L.sparse_mla_prefill_fp8(a["q"], a["cache"], a["idx"], a["bt"], a["req"], a["sl"], a["st"],
+                                        a["scale"], a["ns"], a["out"], a["lse"], a["T"], a["H"], a["K"], a["R"],
+                                        a["MB"], a["NB"], a["kvw"], a["N"], a["ws"], a["wsb"], a["stream"])
+    assert call(H=24) == -2
+    assert call(N=0) == -1
+    assert call(kvw=None) == -1
+    assert call(q=ctypes.c_void_p(0x10008)) == -1  # misaligned
+    assert call(T=0) == 0

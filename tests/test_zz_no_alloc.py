@@ -1,11 +1,13 @@
 """GPU: the allocation-free decode entry point (fixed library scratch instead
-of a workspace) against the workspace entry point on the same inputs, two
-calls in a row with different inputs, through the C ABI."""
+of a workspace) against the workspace entry point and against the float64
+oracle on the same inputs, two calls in a row with different inputs, through
+the C ABI."""
 import ctypes
 
 import numpy as np
 import pytest
 
+import oracle
 import smla_inputs as inp
 from helpers import assert_lse_close, assert_out_close, bf16_dev, dev, oracle_cache
 
@@ -58,15 +60,21 @@ def test_noalloc_matches_workspace_entry_point_twice(smla, num_splits, H):
     out = torch.empty((T, H, 512), dtype=torch.bfloat16, device="cuda")
     lse = torch.empty((T, H), dtype=torch.float32, device="cuda")
     for case in cases:
-        cache = dev(oracle_cache(case))
-        ref_out, ref_lse = _workspace_call(smla, case, cache, num_splits)
+        cache_np = oracle_cache(case)
+        cache = dev(cache_np)
+        ws_out, ws_lse = _workspace_call(smla, case, cache, num_splits)
         out.fill_(float("nan"))
         lse.fill_(float("nan"))
         _noalloc_call(smla, case, cache, out, lse, num_splits)
         got_out, got_lse = out.float().cpu().numpy(), lse.cpu().numpy()
         assert np.all(np.isfinite(got_out))
-        assert_out_close(got_out, ref_out, case.name + " noalloc")
-        assert_lse_close(got_lse, ref_lse, case.name + " noalloc")
+        assert_out_close(got_out, ws_out, case.name + " noalloc vs workspace entry point")
+        assert_lse_close(got_lse, ws_lse, case.name + " noalloc vs workspace entry point")
+        ref_out, ref_lse = oracle.sparse_mla_decode(case.q, cache_np, case.indices, case.block_table,
+                                                    case.req_id_per_token, case.sm_scale)
+        assert_out_close(got_out, ref_out, case.name + " noalloc vs oracle")
+        assert_lse_close(got_lse, ref_lse, case.name + " noalloc vs oracle")
+    assert smla.read_noalloc_status() == 0
 
 
 def test_noalloc_rejects_work_beyond_the_fixed_scratch(smla):
