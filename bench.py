@@ -44,7 +44,7 @@ UNIT = "query-tokens/s"
 # figure no longer applies and the roofline reports null.
 TRAFFIC_SOURCES = ("smla_decode.cu", "smla_combine.cuh", "smla_common.cuh", "sm103_ptx.cuh")
 TRAFFIC_BY_SOURCE = {
-    "4bf1514cc60d41f8": 100_889_344 + 2_852_352 + 7_377_408 + 0,
+    "bb863e2a8d4971a2": 100_922_112 + 2_977_280,  # 128-row tiles, cluster merge: no combine launch
 }
 # The same for the 128-head CTA-pair kernel, per workload: the bf16 prefill's
 # attention kernel plus its combine; the FP8 decode's attention kernel alone
@@ -431,7 +431,8 @@ def run_ours(args):
             "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": captured_traffic(),
                          "peak_source": peaks["source"],
-                         "kernel": "sparse decode launch (attention kernel + split combine)",
+                         "kernel": "sparse decode launch (attention kernel, plus the combine where units are split "
+                                   "outside a cluster)",
                          "algorithmic_bytes_per_launch": int(alg_bytes), "avg_launch_us": decode_ms * 1e3},
             "cpu_baseline": cpu,
             "e2e": e2e,
