@@ -8,7 +8,10 @@ through the seeded input generators in ``smla_inputs``.
 
 The arithmetic lives in ``smla_oracle.c`` (plain C, double precision, OpenMP
 over tokens); this module builds it with gcc and marshals numpy arrays.
-Every function cites the passage of the pages it follows in the C source:
+The MLA weight absorption steps around the attention (``absorb_q``,
+``v_up_proj``) are float64 numpy matrix products written in this module.
+Every function cites the passage of the pages it follows (for the C
+functions, in the C source):
 vLLM ``flashmla_sparse.py`` (module docstring on the "FP8 with scale" layout,
 ``triton_convert_req_index_to_global_index`` and its docstring formula,
 ``FlashMLASparseImpl.forward``) and the OCP 8-bit floating point
@@ -239,3 +242,35 @@ def sparse_mla_prefill_fp8(q_bits, cache, indices, block_table, req_id_per_token
     req = _c(req_id_per_token, np.int32)
     rows = translate_workspace(indices, block_table, req, req, workspace_starts, cache.shape[0])
     return sparse_mla_prefill(q_bits, ws, rows, sm_scale, tokens=tokens, nthreads=nthreads)
+
+
+# ---------------------------------------------------------------- MLA weight absorption
+
+def _bf16_to_f64(bits):
+    return (np.ascontiguousarray(bits, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def absorb_q(q_bits, w_uk_t_bits) -> np.ndarray:
+    """FlashMLASparseImpl.forward before the attention, in float64: q (bf16
+    bits [T, H, P + 64]) is split into q_nope [T, H, P] and q_pe [T, H, 64];
+    ql_nope[t, h, :] = q_nope[t, h, :] @ W_UK_T[h] (bf16 bits [H, P, 512]);
+    the attention input is ql_nope ++ q_pe, float64 [T, H, 576]."""
+    q = _bf16_to_f64(q_bits)
+    w = _bf16_to_f64(w_uk_t_bits)
+    T, H, D = q.shape
+    P = D - 64
+    assert w.shape == (H, P, D_V)
+    q_nope, q_pe = q[..., :P], q[..., P:]
+    ql_nope = np.matmul(q_nope.transpose(1, 0, 2), w).transpose(1, 0, 2)  # (H, T, P) x (H, P, L) -> (T, H, L)
+    return np.concatenate([ql_nope, q_pe], axis=-1)
+
+
+def v_up_proj(attn_out_bits, w_uv_bits) -> np.ndarray:
+    """FlashMLASparseImpl._v_up_proj in float64: out[t, h, :] =
+    attn_out[t, h, :] @ W_UV[h] for attn_out bf16 bits [T, H, 512] and W_UV
+    bf16 bits [H, 512, V]; float64 [T, H, V]."""
+    a = _bf16_to_f64(attn_out_bits)
+    w = _bf16_to_f64(w_uv_bits)
+    T, H, L = a.shape
+    assert L == D_V and w.shape[:2] == (H, D_V)
+    return np.matmul(a.transpose(1, 0, 2), w).transpose(1, 0, 2)

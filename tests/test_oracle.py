@@ -513,3 +513,66 @@ def test_prefill_fp8_equals_decode_when_upconvert_is_exact():
     o1, l1 = oracle.sparse_mla_prefill_fp8(q, cache, idx, bt, req, seq_lens, starts, R * ctx, sm)
     o2, l2 = oracle.sparse_mla_decode(q, cache, idx, bt, req, sm)
     assert np.allclose(o1, o2, rtol=1e-12, atol=1e-12) and np.allclose(l1, l2, rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------- MLA weight absorption
+
+def _bf16_rand(rng, shape, scale=1.0):
+    return inp.bf16_bits((rng.standard_normal(shape) * scale).astype(np.float32))
+
+
+def test_absorb_q_brute_force_small():
+    rng = np.random.default_rng(21)
+    T, H, P = 3, 2, 64
+    q = _bf16_rand(rng, (T, H, P + 64))
+    w = _bf16_rand(rng, (H, P, 512), 0.1)
+    got = oracle.absorb_q(q, w)
+    qf, wf = _bf16_value(q).reshape(T, H, P + 64), _bf16_value(w).reshape(H, P, 512)
+    for t in range(T):
+        for h in range(H):
+            for l in (0, 17, 300, 511):
+                acc = 0.0
+                for p in range(P):
+                    acc += float(qf[t, h, p]) * float(wf[h, p, l])
+                assert abs(got[t, h, l] - acc) <= 1e-12 * (1 + abs(acc))
+            assert np.array_equal(got[t, h, 512:], qf[t, h, P:])  # q_pe after the absorbed part
+
+
+def test_absorb_q_identity_weights_and_head_independence():
+    rng = np.random.default_rng(22)
+    T, H, P = 5, 3, 128
+    q = _bf16_rand(rng, (T, H, P + 64))
+    w = np.zeros((H, P, 512), np.float32)
+    for h in range(H):
+        w[h, :, 128 * h:128 * h + P] = np.eye(P)  # head h copies q_nope into columns 128 h ..
+    got = oracle.absorb_q(q, inp.bf16_bits(w))
+    qf = _bf16_value(q).reshape(T, H, P + 64)
+    for h in range(H):
+        expect = np.zeros((T, 512))
+        expect[:, 128 * h:128 * h + P] = qf[:, h, :P]
+        assert np.array_equal(got[:, h, :512], expect)
+    # permuting the heads of q and W permutes the result's heads
+    wr = _bf16_rand(rng, (H, P, 512), 0.1)
+    perm = np.array([2, 0, 1])
+    assert np.allclose(oracle.absorb_q(q[:, perm], wr[perm]), oracle.absorb_q(q, wr)[:, perm], rtol=0, atol=0)
+
+
+def test_v_up_proj_one_hot_and_brute_force():
+    rng = np.random.default_rng(23)
+    T, H, V = 4, 2, 128
+    a = _bf16_rand(rng, (T, H, 512))
+    w = np.zeros((H, 512, V), np.float32)
+    w[0, 7, 3] = 1.0
+    w[1, 511, 127] = 2.0  # a power of two: exact
+    got = oracle.v_up_proj(a, inp.bf16_bits(w))
+    af = _bf16_value(a).reshape(T, H, 512)
+    expect = np.zeros((T, H, V))
+    expect[:, 0, 3] = af[:, 0, 7]
+    expect[:, 1, 127] = 2.0 * af[:, 1, 511]
+    assert np.array_equal(got, expect)
+    wr = _bf16_rand(rng, (H, 512, V), 0.05)
+    got = oracle.v_up_proj(a, wr)
+    wf = _bf16_value(wr).reshape(H, 512, V)
+    t, h, v = 2, 1, 77
+    acc = sum(float(af[t, h, k]) * float(wf[h, k, v]) for k in range(512))
+    assert abs(got[t, h, v] - acc) <= 1e-12 * (1 + abs(acc))
