@@ -405,7 +405,7 @@ def run_ours(args):
         del cache
         torch.cuda.empty_cache()
         for name, k in (("decode_h128_k2048", max(20, args.steps // 20)), ("prefill_h128_k2048", max(5, args.steps // 200)),
-                        ("prefill_fp8_h128_k2048", max(5, args.steps // 200))):
+                        ("prefill_fp8_h128_k2048", max(5, args.steps // 200)), ("mla_absorb_h128", max(20, args.steps // 20))):
             sub = argparse.Namespace(**vars(args))
             sub.workload, sub.steps = name, k
             sub.no_cpu_baseline = True
@@ -479,9 +479,14 @@ def tensor_workload(args, quiet=False):
       decode_h128_k2048: FP8 decode, 128 requests x 1 token, H = 128, top-k
         2048, context 65536 (5.5 GB cache), 8 rotating index sets;
       prefill_h128_k2048: bf16 prefill, 4 requests x 1024 new tokens over
-        3072 cached, H = 128, top-k 2048, dense latent buffer of 16384 rows.
+        3072 cached, H = 128, top-k 2048, dense latent buffer of 16384 rows;
+      prefill_fp8_h128_k2048: the same prefill over the FP8 cache (gather +
+        up-convert, index mapping, bf16 prefill);
+      mla_absorb_h128: the two weight-absorption GEMMs around the attention
+        at 4096 tokens, H = 128 (HBM-bound: ~93 FLOP per byte).
     Prints one JSON line: query-tokens/s, TFLOP/s against the dense tensor
-    peak of the path's MMA type, and the oracle on a bounded token sample."""
+    peak of the path's MMA type (HBM GB/s against measured copy bandwidth for
+    the absorption), and the oracle on a bounded token sample."""
     import torch
     import oracle
     import sparse_mla_attention_fp8_gb300 as smla
@@ -497,6 +502,7 @@ def tensor_workload(args, quiet=False):
     def bf16(bits):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device).view(torch.bfloat16)
 
+    algo_bytes = None  # set for an HBM-bound workload: its roofline is then bytes over measured copy bandwidth
     if args.workload == "decode_h128_k2048":
         case = inp.rotating_decode(seed=2, R=128, ctx_lo=65536, ctx_hi=65536, K=2048, H=128, outliers=True)
         T, H, K, NB = case.q.shape[0], case.H, case.K, case.num_blocks
@@ -533,6 +539,43 @@ def tensor_workload(args, quiet=False):
         def oracle_run():
             oracle.sparse_mla_decode(case.q, hcache, case.index_sets[0], case.block_table, case.req_id_per_token,
                                      case.sm_scale, tokens=tok, nthreads=nth)
+    elif args.workload == "mla_absorb_h128":
+        # the weight absorption around the attention at the prefill workload's shape: 4096 tokens, H = 128,
+        # q_nope 128 -> 512 (with q_pe appended) and 512 -> V = 128, synthetic weights
+        T, H, P, V = 4096, 128, 128, 128
+        K = 0
+        rng = np.random.default_rng(8)
+        with torch.cuda.stream(stream):
+            q = bf16(inp.bf16_bits(rng.standard_normal((T, H, P + 64), dtype=np.float32)))
+            w_uk = bf16(inp.bf16_bits((rng.standard_normal((H, P, 512), dtype=np.float32) * 0.08)))
+            a_out = bf16(inp.bf16_bits(rng.standard_normal((T, H, 512), dtype=np.float32)))
+            w_uv = bf16(inp.bf16_bits((rng.standard_normal((H, 512, V), dtype=np.float32) * 0.05)))
+            q_out = torch.empty((T, H, 576), dtype=torch.bfloat16, device=device)
+            y = torch.empty((T, H, V), dtype=torch.bfloat16, device=device)
+            ws = torch.zeros(256, dtype=torch.uint8, device=device)
+        stream.synchronize()
+
+        def launch(i):
+            smla.mla_absorb_q(q, w_uk, q_out, ws, stream=stream)
+            smla.mla_v_up_proj(a_out, w_uv, y, ws, stream=stream)
+        n_graphs = 1
+        flops = 2 * T * H * P * 512 + 2 * T * H * 512 * V
+        # q_nope read (the RoPE part is copied), W_UK_T, q_out written; attn_out, W_UV, the projection written
+        algo_bytes = 2 * (T * H * (P + 64) + H * P * 512 + T * H * 576 + T * H * 512 + H * 512 * V + T * H * V)
+        fp8 = False
+        mma_dtype = "bf16"
+        launches = 2
+        desc = (f"mla_absorb_h128: per-head GEMMs around the attention, {T} tokens, H={H}: q_nope ({P}) x W_UK_T "
+                f"-> 512 with q_pe appended, and 512 x W_UV -> {V}; synthetic weights")
+        tok = np.arange(min(nth, 8), dtype=np.int32)
+        qh = inp.bf16_bits(rng.standard_normal((len(tok), H, P + 64), dtype=np.float32))
+        wh = inp.bf16_bits(rng.standard_normal((H, P, 512), dtype=np.float32) * 0.08)
+        ah = inp.bf16_bits(rng.standard_normal((len(tok), H, 512), dtype=np.float32))
+        vh = inp.bf16_bits(rng.standard_normal((H, 512, V), dtype=np.float32) * 0.05)
+
+        def oracle_run():
+            oracle.absorb_q(qh, wh)
+            oracle.v_up_proj(ah, vh)
     elif args.workload == "prefill_fp8_h128_k2048":
         # the bf16 prefill workload's shape over the FP8 paged cache, separate mode: each call gathers and
         # up-converts the chunk's 4 x 4096 rows into a bf16 workspace, maps the indices, runs the bf16 prefill
@@ -660,6 +703,15 @@ def tensor_workload(args, quiet=False):
                      "avg_launch_us": ms * 1e3},
         "cpu_baseline": cpu, "e2e": None, "gpu_launches": launches * args.steps, "clocks": clk,
     }
+    if algo_bytes is not None:
+        gbs = algo_bytes / (ms * 1e-3) / 1e9
+        line["metric"] = f"{args.workload} query-tokens/s + GB/s vs HBM roofline"
+        line["config"]["step"] = "the query-side and value-side GEMM launches"
+        line["config"]["l2"] = "inputs (1.5 GB per step) larger than L2"
+        line["roofline"] = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                            "frac": gbs / peaks["hbm_gbs"], "traffic": None, "peak_source": peaks["source"],
+                            "kernel": "head_gemm_kernel (two launches per step)", "bytes_per_step": algo_bytes,
+                            "avg_step_us": ms * 1e3}
     return line
 
 
@@ -769,7 +821,7 @@ def main():
     ap.add_argument("--no-extra", action="store_true",
                     help="leave the tensor-bound configurations out of the default line")
     ap.add_argument("--workload", choices=["decode_h16_k2048", "decode_h128_k2048", "prefill_h128_k2048",
-                                           "prefill_fp8_h128_k2048"],
+                                           "prefill_fp8_h128_k2048", "mla_absorb_h128"],
                     default="decode_h16_k2048",
                     help="decode_h16_k2048 (default) is the headline; the other two are the tensor-bound "
                          "configurations, reported on their own line")

@@ -207,6 +207,24 @@ int sparse_mla_translate_indices(const int32_t* indices, const int32_t* block_ta
                                  const int32_t* req_id_per_token, int32_t* slots_out, int T, int K, int R,
                                  int MB, int NB, void* stream);
 
+/* MLA weight absorption before the attention (FlashMLASparseImpl.forward in [flashmla_sparse.py]: q is
+ * split into q_nope and q_pe, ql_nope = bmm(q_nope, W_UK_T) per head, and the attention input is
+ * cat(ql_nope, q_pe)), as one tensor-core kernel whose epilogue writes the attention-ready query:
+ *   q       bf16 [T, H, P + 64]   P NoPE features (a positive multiple of 64) then 64 RoPE features
+ *   w_uk_t  bf16 [H, P, 512]      per head, row p = the 512 latent weights of NoPE feature p
+ *   q_out   bf16 [T, H, 576]      q_out[t, h, 0:512] = q[t, h, 0:P] x w_uk_t[h] (fp32 accumulation, rounded
+ *                                 to bf16), q_out[t, h, 512:576] = q[t, h, P:P+64]
+ *   workspace  >= 256 bytes, 256-byte aligned (the status word); NULL = library-cached. */
+int mla_absorb_q(const void* q, const void* w_uk_t, void* q_out, int T, int H, int P, void* workspace,
+                 size_t workspace_bytes, void* stream);
+
+/* MLA value up-projection after the attention (FlashMLASparseImpl._v_up_proj in [flashmla_sparse.py]):
+ *   attn_out bf16 [T, H, 512]; w_uv bf16 [H, 512, V] (V a positive multiple of 128);
+ *   out bf16 [T, H, V] = attn_out[t, h, :] x w_uv[h] per head (fp32 accumulation, rounded to bf16).
+ *   workspace as for mla_absorb_q. */
+int mla_v_up_proj(const void* attn_out, const void* w_uv, void* out, int T, int H, int V, void* workspace,
+                  size_t workspace_bytes, void* stream);
+
 /* Reads (and clears) the device status word of a workspace after
  * synchronizing `stream`: 0 = no fault; 1 = a kernel wait ran past its time
  * limit and the kernel unwound (its outputs are not valid).  workspace NULL =

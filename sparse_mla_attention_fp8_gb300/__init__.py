@@ -28,7 +28,7 @@ _BUILD = os.path.join(_PKG, "_build")
 LIB_PATH = os.path.join(_PKG, "libsmla.so")
 HEADER = os.path.join(_ROOT, "include", "smla.h")
 
-SOURCES = ["smla_decode.cu", "smla_attn.cu", "smla_wide.cu", "smla_store.cu", "smla_api.cu"]
+SOURCES = ["smla_decode.cu", "smla_attn.cu", "smla_wide.cu", "smla_store.cu", "smla_absorb.cu", "smla_api.cu"]
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-std=c++17", "-lineinfo",
               "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall"]
 
@@ -122,6 +122,10 @@ def lib():
             L.sparse_mla_translate_indices_workspace.restype = i32
             L.sparse_mla_prefill_chunks.argtypes = [P, i32, ctypes.c_int64, P, P, ctypes.POINTER(i32)]
             L.sparse_mla_prefill_chunks.restype = i32
+            L.mla_absorb_q.argtypes = [P, P, P, i32, i32, i32, P, sz, P]
+            L.mla_absorb_q.restype = i32
+            L.mla_v_up_proj.argtypes = [P, P, P, i32, i32, i32, P, sz, P]
+            L.mla_v_up_proj.restype = i32
             L.smla_read_noalloc_status.argtypes = [ctypes.POINTER(ctypes.c_int), P]
             L.smla_read_noalloc_status.restype = i32
             L.smla_last_error.argtypes = []
@@ -374,6 +378,43 @@ def sparse_mla_prefill_chunks(seq_lens, workspace_rows: int):
         bounds.append((b, int(ends[i])))
         b = int(ends[i])
     return bounds, [int(starts[i]) for i in range(R)]
+
+
+def mla_absorb_q(q, w_uk_t, out=None, workspace=None, stream=None):
+    """Attention-ready query from q bf16 [T,H,P+64] and W_UK_T bf16 [H,P,512]:
+    bf16 [T,H,576] = (q_nope x W_UK_T per head) ++ q_pe."""
+    import torch
+    dev = _dev(q, w_uk_t, out, workspace)
+    T, H, D = q.shape
+    P = D - 64
+    _expect(w_uk_t, torch.bfloat16, (H, P, 512), "w_uk_t")
+    if q.dtype != torch.bfloat16:
+        raise SmlaError("q must be bf16")
+    if out is None:
+        out = torch.empty((T, H, 576), dtype=torch.bfloat16, device=dev)
+    _expect(out, torch.bfloat16, (T, H, 576), "out")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().mla_absorb_q(_ptr(q), _ptr(w_uk_t), _ptr(out), T, H, P, _ptr(workspace), ws_bytes,
+                              _stream_ptr(stream, dev)), "mla_absorb_q")
+    return out
+
+
+def mla_v_up_proj(attn_out, w_uv, out=None, workspace=None, stream=None):
+    """Per-head value up-projection: attn_out bf16 [T,H,512] x W_UV bf16
+    [H,512,V] -> bf16 [T,H,V]."""
+    import torch
+    dev = _dev(attn_out, w_uv, out, workspace)
+    T, H, _ = attn_out.shape
+    V = w_uv.shape[2]
+    _expect(attn_out, torch.bfloat16, (T, H, 512), "attn_out")
+    _expect(w_uv, torch.bfloat16, (H, 512, V), "w_uv")
+    if out is None:
+        out = torch.empty((T, H, V), dtype=torch.bfloat16, device=dev)
+    _expect(out, torch.bfloat16, (T, H, V), "out")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().mla_v_up_proj(_ptr(attn_out), _ptr(w_uv), _ptr(out), T, H, V, _ptr(workspace), ws_bytes,
+                               _stream_ptr(stream, dev)), "mla_v_up_proj")
+    return out
 
 
 def mla_cache_store_fp8(kv_new, slot_mapping, kv_cache, stream=None):

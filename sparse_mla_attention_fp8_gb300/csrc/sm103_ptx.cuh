@@ -211,6 +211,18 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* map, int x
       "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
       : "memory");
 }
+// 2-D tiled TMA store of one box from this CTA's shared memory (layout and
+// swizzle from the tensor map) into global memory, in the thread's bulk group.
+// Box elements outside the tensor are not written.  The source may be reused
+// once bulk_wait_read_all() returns.
+__device__ __forceinline__ void tma_store_2d(const void* map, uint32_t src, int x, int y) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(map), "r"(src),
+               "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until every committed bulk store of this thread has finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 // 2-D gather of 4 rows (one box-width slice of each) into 4 consecutive box
 // rows of shared memory.
 __device__ __forceinline__ void tma_gather4_2d(uint32_t dst, const void* map, int x, int r0, int r1, int r2, int r3,

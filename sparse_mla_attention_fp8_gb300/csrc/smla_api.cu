@@ -481,6 +481,55 @@ int smla_read_device_status(void* workspace, int* status_out, void* stream) {
   return SMLA_OK;
 }
 
+// ---- MLA weight absorption
+
+namespace {
+// The status word of a call that takes only a status workspace: the caller's
+// (>= 256 bytes, 256-byte aligned) or the library-cached workspace.
+int status_workspace(void** workspace, size_t workspace_bytes) {
+  if (*workspace) {
+    if ((reinterpret_cast<uintptr_t>(*workspace) & 255u) != 0)
+      return fail(SMLA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    if (workspace_bytes < smla::kWsStatusBytes)
+      return fail(SMLA_ERR_WORKSPACE, "workspace has %zu bytes, %zu needed", workspace_bytes, smla::kWsStatusBytes);
+    return SMLA_OK;
+  }
+  return cached_workspace(smla::kWsStatusBytes, workspace);
+}
+}  // namespace
+
+int mla_absorb_q(const void* q, const void* w_uk_t, void* q_out, int T, int H, int P, void* workspace,
+                 size_t workspace_bytes, void* stream) {
+  if (T < 0 || H <= 0 || P <= 0 || P % 64 != 0)
+    return fail(SMLA_ERR_INVALID_ARG, "bad sizes T=%d H=%d P=%d (P must be a positive multiple of 64)", T, H, P);
+  if (T == 0) return SMLA_OK;
+  if (!q || !w_uk_t || !q_out) return fail(SMLA_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned16(q) || !aligned16(w_uk_t) || !aligned16(q_out))
+    return fail(SMLA_ERR_INVALID_ARG, "q, w_uk_t and q_out must be 16-byte aligned");
+  int rc = status_workspace(&workspace, workspace_bytes);
+  if (rc != SMLA_OK) return rc;
+  cudaError_t e = smla::launch_absorb_q(q, w_uk_t, q_out, T, H, P, static_cast<int*>(workspace),
+                                        static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "mla_absorb_q launch");
+  return SMLA_OK;
+}
+
+int mla_v_up_proj(const void* attn_out, const void* w_uv, void* out, int T, int H, int V, void* workspace,
+                  size_t workspace_bytes, void* stream) {
+  if (T < 0 || H <= 0 || V <= 0 || V % 128 != 0)
+    return fail(SMLA_ERR_INVALID_ARG, "bad sizes T=%d H=%d V=%d (V must be a positive multiple of 128)", T, H, V);
+  if (T == 0) return SMLA_OK;
+  if (!attn_out || !w_uv || !out) return fail(SMLA_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned16(attn_out) || !aligned16(w_uv) || !aligned16(out))
+    return fail(SMLA_ERR_INVALID_ARG, "attn_out, w_uv and out must be 16-byte aligned");
+  int rc = status_workspace(&workspace, workspace_bytes);
+  if (rc != SMLA_OK) return rc;
+  cudaError_t e = smla::launch_v_up_proj(attn_out, w_uv, out, T, H, V, static_cast<int*>(workspace),
+                                         static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "mla_v_up_proj launch");
+  return SMLA_OK;
+}
+
 int smla_read_noalloc_status(int* status_out, void* stream) {
   if (!status_out) return fail(SMLA_ERR_INVALID_ARG, "null status_out");
   void* scratch = nullptr;

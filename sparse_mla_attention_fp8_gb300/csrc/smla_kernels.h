@@ -21,6 +21,13 @@ cudaError_t launch_gather_upconvert(const uint8_t* cache, int64_t NB, const int3
                                     const int32_t* seq_lens, const int32_t* starts, void* ws, int64_t N,
                                     int num_sms, cudaStream_t stream);
 
+// MLA weight absorption around the attention (smla_absorb.cu): per-head GEMMs
+// on the tensor cores.  status: a device word that a timed-out wait sets.
+cudaError_t launch_absorb_q(const void* q, const void* w_uk_t, void* q_out, int T, int H, int P, int* status,
+                            cudaStream_t stream);
+cudaError_t launch_v_up_proj(const void* attn_out, const void* w_uv, void* out, int T, int H, int V, int* status,
+                             cudaStream_t stream);
+
 // Work decomposition of one sparse-attention call: units are (token, head
 // group) pairs, each split into nt tiles of 64 top-k rows; G persistent CTAs
 // take contiguous, balanced ranges of the unit-major tile sequence.
