@@ -191,6 +191,13 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// The same without ordering the threads' earlier memory operations at cluster
+// scope: for start-up after fence.mbarrier_init (barrier initialisation is
+// the only thing other CTAs rely on), and for exit once every cross-CTA
+// transfer has been waited for.
+__device__ __forceinline__ void cluster_sync_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;\nbarrier.cluster.wait.aligned;" ::: "memory");
+}
 
 // ---------------------------------------------------------------- bulk copy
 // 1-D TMA copy global -> shared, completion counted in bytes on an mbarrier.

@@ -66,7 +66,7 @@ constexpr uint32_t kFullMask = 0xffffffffu;
 // through smla_trace_set_fp8.  Compiled out otherwise.
 #ifdef SMLA_TRACE
 __device__ unsigned long long* g_smla_trace_fp8 = nullptr;
-constexpr int kTraceTiles = 16, kTraceEvents = 15;
+constexpr int kTraceTiles = 16, kTraceEvents = 22;
 #define SMLA_TRACE_SET(tl, ev)                                                                                  \
   do {                                                                                                          \
     if (trace_buf && (tl) < kTraceTiles)                                                                        \
@@ -80,9 +80,12 @@ constexpr int kTraceTiles = 16, kTraceEvents = 15;
 // QK^T issued, softmax start (S ready), softmax past the tile-max barrier, P'
 // written (warp 0), P.V issued, epilogue done, Q of a segment ready (at the
 // segment's first tile), epilogue past the last P.V, cluster merge: before
-// the wait for the other CTA, after it
+// the wait for the other CTA, after it; the CTA's first instruction and its
+// exit (tile 0's slots); cluster merge steps: sums and LSEs done, readiness
+// signalled, the others' readiness seen, values sent, output written
 enum { kEvIdx = 0, kEvBufFree, kEvIssued, kEvLanded, kEvOpFull, kEvQk, kEvSoftStart, kEvSoftBar, kEvPWritten, kEvPv,
-       kEvEpi, kEvQReady, kEvEpiStart, kEvMergeWait, kEvMergeGo };
+       kEvEpi, kEvQReady, kEvEpiStart, kEvMergeWait, kEvMergeGo, kEvEnter, kEvExit, kEvEpiLse, kEvEpiSignal,
+       kEvEpiReady, kEvEpiSent, kEvEpiWritten };
 
 constexpr int HG = 16;                 // heads per CTA work unit
 constexpr int kRows = 128;             // top-k rows per tile
@@ -120,19 +123,20 @@ enum {
   kBarPFull = kBarSFree + 2, kBarPvDone = kBarPFull + kPBufs, kBarIdxFull = kBarPvDone + kPBufs,
   kBarIdxEmpty = kBarIdxFull + 4, kBarQFull = kBarIdxEmpty + 4, kBarQEmpty = kBarQFull + kQBufs,
   kBarOFree = kBarQEmpty + kQBufs, kBarDrain = kBarOFree + 1, kBarDrainPv = kBarDrain + 1,
-  kBarReady = kBarDrainPv + 1,  // cluster merge: the first CTA's receive buffer is free (arrived remotely)
-  kBarRecv = kBarReady + 1,     // cluster merge: the other parts' results have arrived (first CTA)
+  kBarReady = kBarDrainPv + 1,  // cluster merge: every other CTA's receive buffer is free (arrived remotely)
+  kBarRecv = kBarReady + 1,     // cluster merge: the other parts' values of this CTA's chunks have arrived
   kNumBars = kBarRecv + 1
 };
 constexpr int kOffMisc = kOffBar + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 16;
 constexpr int kSmemAlloc = kSmemBytes + 1024;
-// cluster merge: the first CTA receives the other parts' normalized outputs
-// (16 heads x 512 fp32) and LSEs (16 fp32), each part one block of
-// kPartBytes, in its operand tiles (free by then)
+// cluster merge: CTA c of a cluster of S writes the value chunks q (128
+// columns each) with q % S == c; it receives every other CTA's normalized
+// values of those chunks (128 columns x 16 heads fp32 per chunk) and its 16
+// LSEs in its operand tiles (free by then)
 constexpr int kMaxCluster = 4;
-constexpr int kPartBytes = HG * kDv * 4 + HG * 4;
-static_assert((kMaxCluster - 1) * kPartBytes <= kOpBufs * kOpBuf && kPartBytes % 16 == 0, "cluster receive buffer");
+constexpr int kChunkBytes = kRows * HG * 4;  // 8 KB: one value chunk of one part, [column][head]
+static_assert((kMaxCluster - 1) * (2 * kChunkBytes + HG * 4) <= kOpBufs * kOpBuf, "cluster receive buffer");
 static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0 && kOpBuf % 1024 == 0, "operand alignment");
 static_assert(kOffBar % 8 == 0, "barriers 8-byte aligned");
 static_assert(kOffPre % 16 == 0 && kOffRedMax % 16 == 0 && kOffRedSc % 16 == 0 && kOffRedSum % 16 == 0, "float4");
@@ -211,11 +215,12 @@ __device__ __forceinline__ void bulk_s2cluster(uint32_t dst, uint32_t src, uint3
                : "memory");
 }
 
-__device__ __forceinline__ float lds_f32(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+__device__ __forceinline__ float4 lds_f32x4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr) : "memory");
   return v;
 }
+
 
 __device__ __forceinline__ void sts64(uint32_t addr, uint32_t a, uint32_t b) {
   asm volatile("st.shared.v2.u32 [%0], {%1,%2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
@@ -356,6 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(cons
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 #ifdef SMLA_TRACE
   unsigned long long* __restrict__ const trace_buf = g_smla_trace_fp8;
+  if (tid == 0) SMLA_TRACE_SET(0, kEvEnter);
 #endif
   const int64_t xbeg = tile_begin(blockIdx.x, p.total, p.G);
   const int64_t xend = tile_begin(blockIdx.x + 1, p.total, p.G);
@@ -385,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(cons
     mbar_init(&bars[kBarOFree], kSoftWarps);
     mbar_init(&bars[kBarDrain], 1);
     mbar_init(&bars[kBarDrainPv], 1);
-    mbar_init(&bars[kBarReady], 1);
+    mbar_init(&bars[kBarReady], p.cluster > 1 ? p.cluster - 1 : 1);
     mbar_init(&bars[kBarRecv], 1);
     *abort_flag = 0;
     mbar_fence_init();
@@ -396,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(cons
   }
   tc_fence_before();
   if (p.cluster > 1)
-    cluster_sync_all();  // every CTA's barriers are initialised before another CTA of the cluster uses them
+    cluster_sync_relaxed();  // every CTA's barriers (fenced above) are initialised before another CTA uses them
   else
     __syncthreads();
   tc_fence_after();
@@ -906,8 +912,10 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(cons
             lse_own[h] = lt[h] > 0.f ? (m[h] + log2f(lt[h])) * 0.69314718055994530942f : -INFINITY;
           }
         }
-        // this thread's normalized output values of chunk q: head 8 hh + h,
-        // value column 128 q + 32 qd + lane
+        // The epilogue runs once per CTA, so its code is fetched cold: it is
+        // kept compact (rolled loops over chunks and parts, no divisions).
+        // load_out: this thread's normalized output values of chunk q, head
+        // 8 hh + h, value column 128 q + 32 qd + lane.
         auto load_out = [&](int q, float (&val)[8]) {
           uint32_t ohi[8], olo[8];
           tmem_ld8(tmem + lane_base + kOCol + 32 * q + 8 * hh, ohi);
@@ -915,98 +923,138 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(cons
           tmem_ld_wait();
           reg_fence8(ohi);
           reg_fence8(olo);
-          const float rsc = Rq[q] * kPScaleInv;
+          const float rq = q == 0 ? Rq[0] : q == 1 ? Rq[1] : q == 2 ? Rq[2] : Rq[3];
+          const float rsc = rq * kPScaleInv;
 #pragma unroll
           for (int h = 0; h < 8; ++h) val[h] = (__uint_as_float(ohi[h]) + __uint_as_float(olo[h])) * rsc * inv[h];
         };
         const int c0 = 32 * qd + lane;
+        if (tid == 0) SMLA_TRACE_SET(tl, kEvEpiLse);
         if (p.cluster > 1) {
-          // The unit's parts are the cluster's CTAs (one segment each).  The
-          // first CTA, its operand tiles free, tells the others, receives
-          // their outputs and LSEs there by bulk copies, and writes the
-          // LSE-weighted merge: M = max_r lse_r, w_r = exp(lse_r - M),
-          // out = sum_r w_r out_r / sum_r w_r, lse = M + log sum_r w_r.
-          const uint32_t rank = cluster_ctarank();
+          // The unit's parts are the cluster's S CTAs (2 <= S <= 4, one
+          // segment each).  CTA `rank` writes the value chunks q with
+          // q % S == rank (rank and rank + S).  Every CTA, its last P.V done,
+          // tells the others that its operand tiles are free, sends its
+          // normalized values of each chunk it does not write (and its LSEs)
+          // to the chunk's CTA by 16-byte st.async counted on that CTA's
+          // receive barrier, and merges what it receives for its own chunks:
+          // M = max_r lse_r, w_r = exp(lse_r - M), out = sum_r w_r out_r /
+          // sum_r w_r, lse = M + log sum_r w_r (CTA 0).  Receive layout of a
+          // CTA owning n chunks: the part in peer slot ps (the other ranks in
+          // order) has chunk j at (ps * n + j) * kChunkBytes, column c and head
+          // h at (c * 16 + h) * 4; the LSEs follow all values, 64 bytes per slot.
+          const int rank = (int)cluster_ctarank();
           const int S = p.cluster;
+          const int n_own = rank < 4 - S ? 2 : 1;
           const uint32_t recv = smem_u32(smem + kOffOp);
-          if (rank != 0) {
-            // the part goes to this CTA's own (free) first operand tile in the
-            // receive layout, then to the first CTA in one bulk copy
-            float* stage = reinterpret_cast<float*>(smem + kOffOp);
-            if (!dead) {
+          const uint32_t recv_bar = smem_u32(&bars[kBarRecv]);
+          if (tid == 0 && !dead) {
+            mbar_arrive_expect_tx(&bars[kBarRecv], (uint32_t)((S - 1) * (n_own * kChunkBytes + HG * 4)));
 #pragma unroll 1
-              for (int q = 0; q < 4; ++q) {
-                float val[8];
-                load_out(q, val);
+            for (int r = 0; r < S; ++r)
+              if (r != rank) mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&bars[kBarReady]), (uint32_t)r));
+          }
+          if (tid == 0) SMLA_TRACE_SET(tl, kEvEpiSignal);
+          if (tid == 0) SMLA_TRACE_SET(tl, kEvMergeWait);
+          if (!dead) dead = !SMLA_WAIT(kBarReady, 0);
+          dead = __any_sync(kFullMask, dead);
+          if (tid == 0) SMLA_TRACE_SET(tl, kEvEpiReady);
+          float own0[8], own1[8];  // this thread's values of chunks rank and rank + S
 #pragma unroll
-                for (int h = 0; h < 8; ++h) stage[(8 * hh + h) * kDv + 128 * q + c0] = val[h];
-              }
-#pragma unroll
-              for (int h = 0; h < 8; ++h)
-                if (qd == 0 && lane == h) stage[HG * kDv + 8 * hh + h] = lse_own[h];
-            }
-            fence_proxy_async_smem();
-            named_bar_sync(3, 32 * kSoftWarps);
-            if (tid == 0 && !dead) {
-              SMLA_TRACE_SET(tl, kEvMergeWait);
-              if (SMLA_WAIT(kBarReady, 0)) SMLA_TRACE_SET(tl, kEvMergeGo);
-              if (!*abort_flag)
-                bulk_s2cluster(mapa_shared(recv + (rank - 1) * kPartBytes, 0), recv, kPartBytes,
-                               mapa_shared(smem_u32(&bars[kBarRecv]), 0));
-            }
-          } else {
-            if (tid == 0 && !dead) {
-              mbar_arrive_expect_tx(&bars[kBarRecv], (uint32_t)((S - 1) * kPartBytes));
-              for (int r = 1; r < S; ++r) mbar_arrive_cluster(mapa_shared(smem_u32(&bars[kBarReady]), (uint32_t)r));
-            }
-            if (tid == 0) SMLA_TRACE_SET(tl, kEvMergeWait);
-            if (!dead) dead = !mbar_wait_cluster(&bars[kBarRecv], 0, abort_flag, p.status, kDevWaitTimeout);
-            dead = __any_sync(kFullMask, dead);
-            if (tid == 0) SMLA_TRACE_SET(tl, kEvMergeGo);
-            if (!dead) {
-              // merge weights per head: w_r / sum_r w_r for the own part (r = 0)
-              // and up to kMaxCluster - 1 received parts (part r at (r - 1) * kPartBytes)
-              float w[kMaxCluster][8];
-#pragma unroll
-              for (int h = 0; h < 8; ++h) {
-                const int hd = 8 * hh + h;
-                float lr[kMaxCluster];
-                lr[0] = lse_own[h];
-#pragma unroll
-                for (int r = 1; r < kMaxCluster; ++r)
-                  lr[r] = r < S ? lds_f32(recv + (uint32_t)((r - 1) * kPartBytes + (HG * kDv + hd) * 4)) : -INFINITY;
-                float mx = lr[0];
-#pragma unroll
-                for (int r = 1; r < kMaxCluster; ++r) mx = fmaxf(mx, lr[r]);
-                float wsum = 0.f;
-#pragma unroll
-                for (int r = 0; r < kMaxCluster; ++r) {
-                  w[r][h] = mx == -INFINITY ? 0.f : __expf(lr[r] - mx);
-                  wsum += w[r][h];
-                }
-                const float iw = wsum > 0.f ? 1.f / wsum : 0.f;
-#pragma unroll
-                for (int r = 0; r < kMaxCluster; ++r) w[r][h] *= iw;
-                if (qd == 0 && lane == h) p.lse[row0 + h] = wsum > 0.f ? mx + logf(wsum) : -INFINITY;
-              }
+          for (int h = 0; h < 8; ++h) own0[h] = own1[h] = 0.f;
+          if (!dead) {
 #pragma unroll 1
-              for (int q = 0; q < 4; ++q) {
-                float val[8];
-                load_out(q, val);
+            for (int q = 0; q < 4; ++q) {
+              float val[8];
+              load_out(q, val);
+              const int o = q < S ? q : q - S, j = q < S ? 0 : 1;  // the chunk's CTA and its index there
+              if (o == rank) {
 #pragma unroll
                 for (int h = 0; h < 8; ++h) {
-                  float acc = w[0][h] * val[h];
-#pragma unroll
-                  for (int r = 1; r < kMaxCluster; ++r)
-                    if (r < S)
-                      acc = fmaf(w[r][h],
-                                 lds_f32(recv + (uint32_t)((r - 1) * kPartBytes + ((8 * hh + h) * kDv + 128 * q + c0) * 4)),
-                                 acc);
-                  p.out[(row0 + h) * kDv + 128 * q + c0] = __float2bfloat16_rn(acc);
+                  own0[h] = j == 0 ? val[h] : own0[h];
+                  own1[h] = j == 0 ? own1[h] : val[h];
                 }
+              } else {
+                const int n_o = o < 4 - S ? 2 : 1, ps = rank < o ? rank : rank - 1;
+                const uint32_t dst =
+                    mapa_shared(recv + (uint32_t)(((ps * n_o + j) * kRows + c0) * (HG * 4) + 32 * hh), (uint32_t)o);
+                const uint32_t bar = mapa_shared(recv_bar, (uint32_t)o);
+                st_async_v4(dst, val[0], val[1], val[2], val[3], bar);
+                st_async_v4(dst + 16, val[4], val[5], val[6], val[7], bar);
+              }
+            }
+            if (qd == 0 && lane == 0) {
+#pragma unroll 1
+              for (int o = 0; o < S; ++o) {
+                if (o == rank) continue;
+                const int n_o = o < 4 - S ? 2 : 1, ps = rank < o ? rank : rank - 1;
+                const uint32_t dst = mapa_shared(
+                    recv + (uint32_t)((S - 1) * n_o * kChunkBytes + ps * HG * 4 + 32 * hh), (uint32_t)o);
+                const uint32_t bar = mapa_shared(recv_bar, (uint32_t)o);
+                st_async_v4(dst, lse_own[0], lse_own[1], lse_own[2], lse_own[3], bar);
+                st_async_v4(dst + 16, lse_own[4], lse_own[5], lse_own[6], lse_own[7], bar);
               }
             }
           }
+          if (tid == 0) SMLA_TRACE_SET(tl, kEvEpiSent);
+          if (!dead) dead = !SMLA_WAIT(kBarRecv, 0);
+          dead = __any_sync(kFullMask, dead);
+          if (tid == 0) SMLA_TRACE_SET(tl, kEvMergeGo);
+          if (!dead) {
+            // merge weights per head: the maximum M, 1 / sum_r w_r and the own
+            // part's weight are kept; a received part's weight is recomputed
+            // from its LSE where it is used
+            const uint32_t lse_base = recv + (uint32_t)((S - 1) * n_own * kChunkBytes) + 32 * hh;
+            float mx[8], iw[8], w0[8];
+#pragma unroll
+            for (int h = 0; h < 8; ++h) {
+              mx[h] = lse_own[h];
+              iw[h] = 0.f;
+            }
+#pragma unroll 1
+            for (int ps = 0; ps < S - 1; ++ps) {
+              const float4 a = lds_f32x4(lse_base + ps * HG * 4), b = lds_f32x4(lse_base + ps * HG * 4 + 16);
+              const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+              for (int h = 0; h < 8; ++h) mx[h] = fmaxf(mx[h], v[h]);
+            }
+#pragma unroll 1
+            for (int ps = 0; ps < S - 1; ++ps) {
+              const float4 a = lds_f32x4(lse_base + ps * HG * 4), b = lds_f32x4(lse_base + ps * HG * 4 + 16);
+              const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+              for (int h = 0; h < 8; ++h) iw[h] += mx[h] == -INFINITY ? 0.f : __expf(v[h] - mx[h]);
+            }
+#pragma unroll
+            for (int h = 0; h < 8; ++h) {
+              w0[h] = mx[h] == -INFINITY ? 0.f : __expf(lse_own[h] - mx[h]);
+              const float wsum = iw[h] + w0[h];
+              iw[h] = wsum > 0.f ? 1.f / wsum : 0.f;
+              w0[h] *= iw[h];
+              if (rank == 0 && qd == 0 && lane == h) p.lse[row0 + h] = wsum > 0.f ? mx[h] + logf(wsum) : -INFINITY;
+            }
+#pragma unroll 1
+            for (int j = 0; j < n_own; ++j) {
+              float acc[8];
+#pragma unroll
+              for (int h = 0; h < 8; ++h) acc[h] = w0[h] * (j == 0 ? own0[h] : own1[h]);
+#pragma unroll 1
+              for (int ps = 0; ps < S - 1; ++ps) {
+                const float4 a = lds_f32x4(lse_base + ps * HG * 4), b = lds_f32x4(lse_base + ps * HG * 4 + 16);
+                const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+                const uint32_t src = recv + (uint32_t)(((ps * n_own + j) * kRows + c0) * (HG * 4) + 32 * hh);
+                const float4 x0 = lds_f32x4(src), x1 = lds_f32x4(src + 16);
+                const float x[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+                for (int h = 0; h < 8; ++h)
+                  acc[h] = fmaf(mx[h] == -INFINITY ? 0.f : __expf(v[h] - mx[h]) * iw[h], x[h], acc[h]);
+              }
+              const int q = rank + j * S;
+#pragma unroll
+              for (int h = 0; h < 8; ++h) p.out[(row0 + h) * kDv + 128 * q + c0] = __float2bfloat16_rn(acc[h]);
+            }
+          }
+          if (tid == 0) SMLA_TRACE_SET(tl, kEvEpiWritten);
         } else {
 #pragma unroll
           for (int h = 0; h < 8; ++h) {
@@ -1048,7 +1096,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(cons
     tmem_dealloc(tmem, kTmemCols);
   }
   // no CTA leaves while another CTA of its cluster may still write into its shared memory
-  if (p.cluster > 1) cluster_sync_all();
+  if (p.cluster > 1) cluster_sync_relaxed();
+  if (tid == 0) SMLA_TRACE_SET(0, kEvExit);
 }
 
 // Per-device flag: the kernel's dynamic shared memory limit has been raised.

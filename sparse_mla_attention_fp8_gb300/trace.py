@@ -24,7 +24,8 @@ import numpy as np
 from . import NVCC_FLAGS, SOURCES, _CSRC, _PKG, _nvcc
 
 EVENTS = ["idx", "buf_free", "issued", "landed", "op_full", "qk", "soft_start", "soft_bar", "p_written", "pv",
-          "epilogue", "q_ready", "epi_start", "merge_wait", "merge_go"]
+          "epilogue", "q_ready", "epi_start", "merge_wait", "merge_go", "enter", "exit", "epi_lse", "epi_signal",
+          "epi_ready", "epi_sent", "epi_written"]
 # per-tile links: (name, from event, to event, tile offset of the end event)
 LINKS = [("copy issue (loader 0)", "buf_free", "issued", 0), ("copy landing (loader 0)", "issued", "landed", 0),
          ("other loaders after loader 0", "landed", "op_full", 0), ("QK^T issue", "op_full", "qk", 0),
@@ -92,7 +93,7 @@ def main(lib_path: str | None = None):
     def call(i):
         rc = L.sparse_mla_decode_fp8(ptr(q), ptr(cache), ptr(idx[i % len(idx)]), ptr(bt), ptr(req),
                                      f32(case.sm_scale), 0, ptr(out), ptr(lse), T, H, K, bt.shape[0], bt.shape[1],
-                                     NB, ptr(ws), ws_bytes, None)
+                                     NB, ptr(ws), ws_bytes, ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
         assert rc == 0
 
     for i in range(5):
@@ -111,7 +112,7 @@ def main(lib_path: str | None = None):
     assert L.smla_trace_set_fp8(None) == 0
     ev = buf.cpu().numpy().astype(np.float64)
     t0 = np.where(ev[:, 0, 0] > 0, ev[:, 0, 0], np.nan)
-    start = np.nanmin(t0)
+    start = np.nanmin(t0[np.isfinite(t0)])
     rel = np.where(ev > 0, (ev - start) / 1e3, np.nan)  # microseconds from the first CTA's first translation
     print(f"CTAs {G}; first index translation spread over CTAs: {np.nanmax(t0 - start) / 1e3:.2f} us")
     print("median over CTAs, us from the earliest CTA start; columns = tiles")
@@ -131,6 +132,32 @@ def main(lib_path: str | None = None):
     d = np.diff(pv, axis=1)
     print(f"P.V cadence: median {np.nanmedian(d):.2f} us (p10 {np.nanpercentile(d, 10):.2f}, "
           f"p90 {np.nanpercentile(d, 90):.2f})")
+    enter, ex = rel[:, 0, EVENTS.index("enter")], rel[:, 0, EVENTS.index("exit")]
+    if G == 2 * T:  # clusters of two (ranks 0 and 1 alternate)
+        for name, sel in (("rank 0", slice(0, G, 2)), ("rank 1", slice(1, G, 2))):
+            lastpv = np.nanmax(pv[sel], axis=1)
+            cols = [("last P.V", lastpv)] + [(e, np.nanmax(rel[sel, :, EVENTS.index(e)], axis=1))
+                                            for e in ("epi_start", "epi_lse", "epi_signal", "epi_ready", "epi_sent",
+                                                      "merge_go", "merge_wait", "epi_written", "epilogue", "exit")]
+            print(f"{name:8s} " + "  ".join(f"{n} {np.nanmedian(v):6.2f}" for n, v in cols))
+    print(f"CTA entry: first {np.nanmin(enter):.2f} last {np.nanmax(enter):.2f} us; exit: first {np.nanmin(ex):.2f} "
+          f"median {np.nanmedian(ex):.2f} last {np.nanmax(ex):.2f} us; first entry to last exit "
+          f"{np.nanmax(ex) - np.nanmin(enter):.2f} us")
+    # the same call timed alone and in CUDA graphs of 1 and 8 calls (no trace buffer)
+    for n in (1, 8):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(n):
+                call(i)
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        e0.record()
+        for _ in range(40):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        print(f"decode call in CUDA graphs of {n}: {e0.elapsed_time(e1) / (40 * n) * 1e3:.1f} us per call")
 
 
 if __name__ == "__main__":
