@@ -42,6 +42,8 @@ struct AttnPlan {
   size_t ws_bytes;    // workspace bytes (status word + partial results)
   int cluster = 1;    // > 1: every unit is split into `cluster` parts run by one thread-block
                       // cluster, merged in distributed shared memory (no combine kernel)
+  bool fused = false; // 128-head FP8 decode: every split unit has two parts, merged in the
+                      // attention kernel by whichever part finishes second (no combine kernel)
 };
 
 AttnPlan plan_attention(bool fp8, int T, int H, int K, int num_splits, int num_sms);

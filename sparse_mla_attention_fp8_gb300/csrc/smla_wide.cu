@@ -156,6 +156,12 @@ struct Params {
   float* lse;              // [T, 128]
   float* part_o;           // [slots, 128, 512]
   float* part_lse;         // [slots, 128]
+  // FP8 rows, every split token cut once (fused): the token's two parts merge
+  // in the kernel.  Per (token, CTA of the pair, part: 0 = from the token's
+  // first tile, 1 = to its last): a published flag and the part's LSEs.
+  int* merge_flag;         // [T, 2, 2], zeroed by the Q preparation kernel
+  float* merge_lse;        // [T, 2, 2, 128]
+  int fused;
   int* status;
   float scale_log2;        // softmax_scale * log2(e)
   int T, K;
@@ -916,33 +922,115 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
           tc_fence_after();
           const bool full_unit = n_seg_tiles == p.nt;  // the whole token ran in this pair
           const float inv = l_sum > 0.f ? (kFp8 ? exp2i(e_run) : 1.f) / l_sum : 0.f;
+          const float lse_v = l_sum > 0.f ? (m_used + log2f(l_sum)) * 0.69314718055994531f : -INFINITY;
           const int64_t slot = (int64_t)pair + u;
-          for (int q = 0; q < 256 / 16; ++q) {
-            uint32_t r[16];
-            tmem_ld16_sync(tmem + lane_base + kOCol + 16 * q, r);
-            if (dead) continue;
-            if (full_unit) {
-              uint32_t ow[8];
-#pragma unroll
-              for (int j = 0; j < 8; ++j)
-                ow[j] = pack_bf16x2(__uint_as_float(r[2 * j]) * inv, __uint_as_float(r[2 * j + 1]) * inv);
-              uint4* dst = reinterpret_cast<uint4*>(p.out + ((int64_t)u * kHeads + h) * kDv + 256 * c + 16 * q);
-              dst[0] = make_uint4(ow[0], ow[1], ow[2], ow[3]);
-              dst[1] = make_uint4(ow[4], ow[5], ow[6], ow[7]);
-            } else {
-              float4* dst = reinterpret_cast<float4*>(p.part_o + (slot * kHeads + h) * kDv + 256 * c + 16 * q);
+          // this thread's normalized output values of columns 256 c + 16 q ..
+          auto write_part = [&](float* base) {
+#pragma unroll 1
+            for (int q = 0; q < 256 / 16; ++q) {
+              uint32_t r[16];
+              tmem_ld16_sync(tmem + lane_base + kOCol + 16 * q, r);
+              float4* dst = reinterpret_cast<float4*>(base + 16 * q);
 #pragma unroll
               for (int j = 0; j < 4; ++j)
                 dst[j] = make_float4(__uint_as_float(r[4 * j]) * inv, __uint_as_float(r[4 * j + 1]) * inv,
                                      __uint_as_float(r[4 * j + 2]) * inv, __uint_as_float(r[4 * j + 3]) * inv);
             }
-          }
-          if (!dead && c == 0) {
-            const float lse_v = l_sum > 0.f ? (m_used + log2f(l_sum)) * 0.69314718055994531f : -INFINITY;
-            if (full_unit)
-              p.lse[(int64_t)u * kHeads + h] = lse_v;
-            else
-              p.part_lse[slot * kHeads + h] = lse_v;
+          };
+          if (kFp8 && p.fused && !full_unit) {
+            // The token's two parts: part 0 from its first tile (the end of
+            // this pair's range), part 1 to its last (the start of the next
+            // pair's).  A part whose partner has published merges at once;
+            // otherwise it publishes its normalized output and LSEs, then
+            // checks the partner again (sequentially consistent fences on
+            // both sides: at least one of the two sees the other, and two
+            // merges write the same values).  Nothing waits on another CTA.
+            const int part = kt + 1 > n_seg_tiles ? 1 : 0;  // the segment's first tile is not the token's first
+            const int64_t fi = ((int64_t)u * 2 + c) * 2;
+            int* flag_own = p.merge_flag + fi + part;
+            const int* flag_oth = p.merge_flag + fi + (1 - part);
+            const int64_t slot_oth = part == 1 ? slot - 1 : slot + 1;  // the partner's pair is the previous / next one
+            volatile int* bc = reinterpret_cast<volatile int*>(smem + L::kOffMisc + 8);
+            int merge = 0;
+            if (!dead) {
+              if (tid == 0) *bc = ld_acquire_gpu(flag_oth);
+              named_bar_sync(1, 32 * kSoftWarps);
+              merge = *bc;
+              named_bar_sync(1, 32 * kSoftWarps);
+              if (!merge) {
+                write_part(p.part_o + (slot * kHeads + h) * kDv + 256 * c);
+                p.merge_lse[(fi + part) * kHeads + h] = lse_v;
+                __threadfence();
+                named_bar_sync(1, 32 * kSoftWarps);
+                if (tid == 0) {
+                  st_release_gpu(flag_own, 1);
+                  __threadfence();
+                  *bc = ld_acquire_gpu(flag_oth);
+                }
+                named_bar_sync(1, 32 * kSoftWarps);
+                merge = *bc;
+              }
+            }
+            if (merge) {
+              // out = (w0 O_0 + w1 O_1) / (w0 + w1), w_i = exp(lse_i - M), in the same order on either side
+              const float lse_o = __ldcg(p.merge_lse + (fi + 1 - part) * kHeads + h);
+              const float l0 = part == 0 ? lse_v : lse_o, l1 = part == 0 ? lse_o : lse_v;
+              const float M = fmaxf(l0, l1);
+              const float w0 = M == -INFINITY ? 0.f : __expf(l0 - M), w1 = M == -INFINITY ? 0.f : __expf(l1 - M);
+              const float ws = w0 + w1, iw = ws > 0.f ? 1.f / ws : 0.f;
+              const float4* oth = reinterpret_cast<const float4*>(p.part_o + (slot_oth * kHeads + h) * kDv + 256 * c);
+#pragma unroll 1
+              for (int q = 0; q < 256 / 16; ++q) {
+                uint32_t r[16];
+                tmem_ld16_sync(tmem + lane_base + kOCol + 16 * q, r);
+                uint32_t ow[8];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  const float4 o = __ldcg(oth + 4 * q + j);
+                  const float ov[4] = {o.x, o.y, o.z, o.w};
+                  float v[4];
+#pragma unroll
+                  for (int k = 0; k < 4; ++k) {
+                    const float mine = __uint_as_float(r[4 * j + k]) * inv;
+                    const float x0 = part == 0 ? mine : ov[k], x1 = part == 0 ? ov[k] : mine;
+                    v[k] = fmaf(w1, x1, w0 * x0) * iw;
+                  }
+                  ow[2 * j] = pack_bf16x2(v[0], v[1]);
+                  ow[2 * j + 1] = pack_bf16x2(v[2], v[3]);
+                }
+                uint4* dst = reinterpret_cast<uint4*>(p.out + ((int64_t)u * kHeads + h) * kDv + 256 * c + 16 * q);
+                dst[0] = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+                dst[1] = make_uint4(ow[4], ow[5], ow[6], ow[7]);
+              }
+              if (c == 0) p.lse[(int64_t)u * kHeads + h] = ws > 0.f ? M + logf(ws) : -INFINITY;
+            }
+          } else {
+            for (int q = 0; q < 256 / 16; ++q) {
+              uint32_t r[16];
+              tmem_ld16_sync(tmem + lane_base + kOCol + 16 * q, r);
+              if (dead) continue;
+              if (full_unit) {
+                uint32_t ow[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                  ow[j] = pack_bf16x2(__uint_as_float(r[2 * j]) * inv, __uint_as_float(r[2 * j + 1]) * inv);
+                uint4* dst = reinterpret_cast<uint4*>(p.out + ((int64_t)u * kHeads + h) * kDv + 256 * c + 16 * q);
+                dst[0] = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+                dst[1] = make_uint4(ow[4], ow[5], ow[6], ow[7]);
+              } else {
+                float4* dst = reinterpret_cast<float4*>(p.part_o + (slot * kHeads + h) * kDv + 256 * c + 16 * q);
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                  dst[j] = make_float4(__uint_as_float(r[4 * j]) * inv, __uint_as_float(r[4 * j + 1]) * inv,
+                                       __uint_as_float(r[4 * j + 2]) * inv, __uint_as_float(r[4 * j + 3]) * inv);
+              }
+            }
+            if (!dead && c == 0) {
+              if (full_unit)
+                p.lse[(int64_t)u * kHeads + h] = lse_v;
+              else
+                p.part_lse[slot * kHeads + h] = lse_v;
+            }
           }
           tc_fence_before();
           mbar_arrive(&bars[L::kBarOFree]);
@@ -971,9 +1059,14 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
 // stored as f16 (value part, exact for the bf16 values in range) and bf16
 // (RoPE part, exact power-of-two scaling); qinv = 2^-s.  One warp per row.
 __global__ void __launch_bounds__(256) wide_q_prep_kernel(const __nv_bfloat16* __restrict__ q, uint16_t* __restrict__ q16,
-                                                         float* __restrict__ qinv, int64_t rows) {
+                                                         float* __restrict__ qinv, int64_t rows, int* merge_flag,
+                                                         int64_t n_flags) {
   const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
+  {  // the attention kernel's merge flags start each call at zero
+    const int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x;
+    if (i < n_flags) merge_flag[i] = 0;
+  }
   if (row >= rows) return;
   const uint4* src = reinterpret_cast<const uint4*>(q + row * kDqk);  // 72 chunks of 8 values
   uint4 v[3];
@@ -1016,8 +1109,10 @@ __global__ void __launch_bounds__(256) wide_q_prep_kernel(const __nv_bfloat16* _
 // Workspace of the FP8 path beyond the partial results: the prepared Q and
 // the heads' inverse prescales.
 size_t q_prep_bytes(int T) {
-  return (((size_t)T * kHeads * kDqk * 2 + 255) / 256) * 256 + (size_t)T * kHeads * 4;
+  return (((size_t)T * kHeads * kDqk * 2 + 255) / 256) * 256 + (((size_t)T * kHeads * 4 + 255) / 256) * 256;
 }
+// the fused merge's flags and LSEs (after the prepared Q)
+size_t merge_bytes(int T) { return (((size_t)T * 4 * 4 + 255) / 256) * 256 + (size_t)T * 4 * kHeads * 4; }
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -1108,10 +1203,14 @@ AttnPlan plan_wide(bool fp8, int T, int K, int num_splits, int num_sms) {
   if (G < 1) G = 1;
   pl.G = (int)G;
   pl.need_combine = !(pl.total % pl.G == 0 && (pl.total / pl.G) % pl.nt == 0);
+  // FP8 rows: when every pair's range holds at least a whole token's tiles, a
+  // split token has two parts, merged in the kernel
+  pl.fused = fp8 && pl.need_combine && pl.total / pl.G >= pl.nt;
+  if (pl.fused) pl.need_combine = false;
   const int64_t n_slots = (int64_t)pl.G + pl.units - 1;
   const size_t lse_bytes = (size_t)(((n_slots * kHeads * 4) + 255) / 256) * 256;
   pl.ws_bytes = kWsStatusBytes + lse_bytes + (size_t)n_slots * kHeads * kDv * 4;
-  if (fp8) pl.ws_bytes += q_prep_bytes(T);
+  if (fp8) pl.ws_bytes += q_prep_bytes(T) + merge_bytes(T);
   return pl;
 }
 
@@ -1146,8 +1245,12 @@ cudaError_t launch_wide(const AttnArgs& a, const AttnPlan& plan, cudaStream_t st
     uint16_t* q16 = reinterpret_cast<uint16_t*>(qp);
     float* qinv = reinterpret_cast<float*>(qp + (((size_t)a.T * kHeads * kDqk * 2 + 255) / 256) * 256);
     const int64_t rows = (int64_t)a.T * kHeads;
+    uint8_t* mg = qp + q_prep_bytes(a.T);
+    p.merge_flag = reinterpret_cast<int*>(mg);
+    p.merge_lse = reinterpret_cast<float*>(mg + (((size_t)a.T * 4 * 4 + 255) / 256) * 256);
+    p.fused = plan.fused ? 1 : 0;
     wide_q_prep_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(static_cast<const __nv_bfloat16*>(a.q), q16,
-                                                                     qinv, rows);
+                                                                     qinv, rows, p.merge_flag, (int64_t)a.T * 4);
     cudaError_t e0 = cudaGetLastError();
     if (e0 != cudaSuccess) return e0;
     p.qinv = qinv;

@@ -225,3 +225,17 @@ def test_back_to_back_decodes_into_the_same_buffers(H):
                                                 c2.req_id_per_token, c2.sm_scale)
     assert_out_close(out.float().cpu().numpy(), ref_out, c2.name + " second call")
     assert_lse_close(lse.cpu().numpy(), ref_lse, c2.name + " second call")
+
+
+def test_h128_split_tokens_merged_in_the_attention_kernel():
+    # 100 tokens of 11 tiles over the resident CTA pairs (14 tiles each): every pair's range holds more
+    # than a token, so each split token has two parts, merged in the attention kernel (no combine launch).
+    import sparse_mla_attention_fp8_gb300 as smla
+    case = inp.memory_bound_decode(seed=41, R=100, ctx_lo=800, ctx_hi=3000, K=700, H=128)
+    launches, ctas = smla.attention_plan(True, 100, 128, 700, 0)
+    assert launches == 2 and ctas >= 2 * 50  # Q preparation + attention, pairs on most SMs
+    case.indices[7, 350:] = -1   # parts without valid rows
+    case.indices[8, :400] = -1
+    case.indices[9, :] = -1      # a token without any
+    check_decode(case)
+    check_decode(case)  # the merge flags start from zero on the next call too
