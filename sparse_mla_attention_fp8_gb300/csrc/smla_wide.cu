@@ -133,7 +133,7 @@ constexpr int kThreads = 32 * kNumWarps;
 // (set by the host through smla_trace_set_wide).  Compiled out otherwise.
 #ifdef SMLA_TRACE
 __device__ long long* g_smla_trace_wide = nullptr;
-constexpr int kTraceTiles = 64, kTraceEvents = 16;
+constexpr int kTraceTiles = 64, kTraceEvents = 20;
 #define WIDE_TRACE(tl, ev)                                                                                   \
   do {                                                                                                       \
     if (trace_buf && (tl) < kTraceTiles)                                                                   \
@@ -142,8 +142,10 @@ constexpr int kTraceTiles = 64, kTraceEvents = 16;
 #else
 #define WIDE_TRACE(tl, ev) ((void)0)
 #endif
+// (the CTA's first instruction and its exit in tile 0's slots; a segment's
+// epilogue start and end in its last tile's)
 enum { kEvSFull = 0, kEvSLoaded, kEvXFree, kEvSent, kEvXFull, kEvPReady, kEvPFull, kEvQk, kEvPv, kEvIssue, kEvQkSeen,
-       kEvKEmpty, kEvConverted, kEvRawFull, kEvXTop, kEvXKFull };
+       kEvKEmpty, kEvConverted, kEvRawFull, kEvXTop, kEvXKFull, kEvEnter, kEvEpiStart, kEvEpiEnd, kEvExit };
 
 struct Params {
   const __nv_bfloat16* q;  // [T, 128, 576]
@@ -153,6 +155,7 @@ struct Params {
   const float* qinv;           // FP8 rows: [T, 128] 2^-s of each head's Q prescale
   int R, MB;
   __nv_bfloat16* out;      // [T, 128, 512]
+  int out_v8;              // out is 32-byte aligned: a thread writes 16 output values in one store
   float* lse;              // [T, 128]
   float* part_o;           // [slots, 128, 512]
   float* part_lse;         // [slots, 128]
@@ -247,6 +250,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
 #ifdef SMLA_TRACE
   // read once: a store through the global pointer would force a reload at every event
   long long* __restrict__ const trace_buf = g_smla_trace_wide;
+  if (tid == 0) WIDE_TRACE(0, kEvEnter);
 #endif
   const int lane = tid & 31;
   const int c = (int)cluster_ctarank();  // value half owned by this CTA
@@ -920,21 +924,38 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
         if (seg_end) {
           if (!dead) dead = !SMLA_WAIT(L::kBarPDone + pb, (tl >> 1) & 1);
           tc_fence_after();
+          if (tid == 0) WIDE_TRACE(tl, kEvEpiStart);
           const bool full_unit = n_seg_tiles == p.nt;  // the whole token ran in this pair
           const float inv = l_sum > 0.f ? (kFp8 ? exp2i(e_run) : 1.f) / l_sum : 0.f;
           const float lse_v = l_sum > 0.f ? (m_used + log2f(l_sum)) * 0.69314718055994531f : -INFINITY;
           const int64_t slot = (int64_t)pair + u;
-          // this thread's normalized output values of columns 256 c + 16 q ..
-          auto write_part = [&](float* base) {
+          // A fused part's normalized output in the slot's block for CTA c,
+          // lane-major so that a warp's accesses are contiguous: columns
+          // 256 c + 16 q + 4 j .. + 3 of head h at float4 (4 q + j) * 128 + h.
+          auto fused_block = [&](int64_t sl) {
+            return reinterpret_cast<float4*>(p.part_o + (sl * kHeads + 64 * c) * kDv);
+          };
+          auto write_part = [&](float4* base) {
 #pragma unroll 1
             for (int q = 0; q < 256 / 16; ++q) {
               uint32_t r[16];
               tmem_ld16_sync(tmem + lane_base + kOCol + 16 * q, r);
-              float4* dst = reinterpret_cast<float4*>(base + 16 * q);
 #pragma unroll
               for (int j = 0; j < 4; ++j)
-                dst[j] = make_float4(__uint_as_float(r[4 * j]) * inv, __uint_as_float(r[4 * j + 1]) * inv,
-                                     __uint_as_float(r[4 * j + 2]) * inv, __uint_as_float(r[4 * j + 3]) * inv);
+                base[(4 * q + j) * kHeads + h] =
+                    make_float4(__uint_as_float(r[4 * j]) * inv, __uint_as_float(r[4 * j + 1]) * inv,
+                                __uint_as_float(r[4 * j + 2]) * inv, __uint_as_float(r[4 * j + 3]) * inv);
+            }
+          };
+          // 16 bf16 output values (8 packed words) of head h at column 256 c + 16 q
+          auto store_out16 = [&](int q, const uint32_t (&ow)[8]) {
+            __nv_bfloat16* d = p.out + ((int64_t)u * kHeads + h) * kDv + 256 * c + 16 * q;
+            if (p.out_v8) {
+              st_global_v8(d, ow);
+            } else {
+              uint4* dst = reinterpret_cast<uint4*>(d);
+              dst[0] = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+              dst[1] = make_uint4(ow[4], ow[5], ow[6], ow[7]);
             }
           };
           if (kFp8 && p.fused && !full_unit) {
@@ -958,7 +979,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
               merge = *bc;
               named_bar_sync(1, 32 * kSoftWarps);
               if (!merge) {
-                write_part(p.part_o + (slot * kHeads + h) * kDv + 256 * c);
+                write_part(fused_block(slot));
                 p.merge_lse[(fi + part) * kHeads + h] = lse_v;
                 __threadfence();
                 named_bar_sync(1, 32 * kSoftWarps);
@@ -978,29 +999,36 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
               const float M = fmaxf(l0, l1);
               const float w0 = M == -INFINITY ? 0.f : __expf(l0 - M), w1 = M == -INFINITY ? 0.f : __expf(l1 - M);
               const float ws = w0 + w1, iw = ws > 0.f ? 1.f / ws : 0.f;
-              const float4* oth = reinterpret_cast<const float4*>(p.part_o + (slot_oth * kHeads + h) * kDv + 256 * c);
+              const float4* oth = fused_block(slot_oth);
+              // two 16-column chunks per step, the partner's eight loads issued first
 #pragma unroll 1
-              for (int q = 0; q < 256 / 16; ++q) {
-                uint32_t r[16];
-                tmem_ld16_sync(tmem + lane_base + kOCol + 16 * q, r);
-                uint32_t ow[8];
+              for (int q = 0; q < 256 / 16; q += 2) {
+                float4 o[8];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                  const float4 o = __ldcg(oth + 4 * q + j);
-                  const float ov[4] = {o.x, o.y, o.z, o.w};
-                  float v[4];
+                for (int j = 0; j < 8; ++j) o[j] = __ldcg(oth + (4 * q + j) * kHeads + h);
+                uint32_t r[2][16];
+                tmem_ld16(tmem + lane_base + kOCol + 16 * q, r[0]);
+                tmem_ld16(tmem + lane_base + kOCol + 16 * q + 16, r[1]);
+                tmem_ld_wait();
 #pragma unroll
-                  for (int k = 0; k < 4; ++k) {
-                    const float mine = __uint_as_float(r[4 * j + k]) * inv;
-                    const float x0 = part == 0 ? mine : ov[k], x1 = part == 0 ? ov[k] : mine;
-                    v[k] = fmaf(w1, x1, w0 * x0) * iw;
+                for (int e = 0; e < 2; ++e) {
+                  reg_fence16(r[e]);
+                  uint32_t ow[8];
+#pragma unroll
+                  for (int j = 0; j < 4; ++j) {
+                    const float ov[4] = {o[4 * e + j].x, o[4 * e + j].y, o[4 * e + j].z, o[4 * e + j].w};
+                    float v[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                      const float mine = __uint_as_float(r[e][4 * j + k]) * inv;
+                      const float x0 = part == 0 ? mine : ov[k], x1 = part == 0 ? ov[k] : mine;
+                      v[k] = fmaf(w1, x1, w0 * x0) * iw;
+                    }
+                    ow[2 * j] = pack_bf16x2(v[0], v[1]);
+                    ow[2 * j + 1] = pack_bf16x2(v[2], v[3]);
                   }
-                  ow[2 * j] = pack_bf16x2(v[0], v[1]);
-                  ow[2 * j + 1] = pack_bf16x2(v[2], v[3]);
+                  store_out16(q + e, ow);
                 }
-                uint4* dst = reinterpret_cast<uint4*>(p.out + ((int64_t)u * kHeads + h) * kDv + 256 * c + 16 * q);
-                dst[0] = make_uint4(ow[0], ow[1], ow[2], ow[3]);
-                dst[1] = make_uint4(ow[4], ow[5], ow[6], ow[7]);
               }
               if (c == 0) p.lse[(int64_t)u * kHeads + h] = ws > 0.f ? M + logf(ws) : -INFINITY;
             }
@@ -1014,15 +1042,17 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
                   ow[j] = pack_bf16x2(__uint_as_float(r[2 * j]) * inv, __uint_as_float(r[2 * j + 1]) * inv);
-                uint4* dst = reinterpret_cast<uint4*>(p.out + ((int64_t)u * kHeads + h) * kDv + 256 * c + 16 * q);
-                dst[0] = make_uint4(ow[0], ow[1], ow[2], ow[3]);
-                dst[1] = make_uint4(ow[4], ow[5], ow[6], ow[7]);
+                store_out16(q, ow);
               } else {
-                float4* dst = reinterpret_cast<float4*>(p.part_o + (slot * kHeads + h) * kDv + 256 * c + 16 * q);
+                // the workspace is 256-byte aligned: two 32-byte stores
+                float* dst = p.part_o + (slot * kHeads + h) * kDv + 256 * c + 16 * q;
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                  dst[j] = make_float4(__uint_as_float(r[4 * j]) * inv, __uint_as_float(r[4 * j + 1]) * inv,
-                                       __uint_as_float(r[4 * j + 2]) * inv, __uint_as_float(r[4 * j + 3]) * inv);
+                for (int j = 0; j < 2; ++j) {
+                  uint32_t w[8];
+#pragma unroll
+                  for (int k = 0; k < 8; ++k) w[k] = __float_as_uint(__uint_as_float(r[8 * j + k]) * inv);
+                  st_global_v8(dst + 8 * j, w);
+                }
               }
             }
             if (!dead && c == 0) {
@@ -1034,6 +1064,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
           }
           tc_fence_before();
           mbar_arrive(&bars[L::kBarOFree]);
+          if (tid == 0) WIDE_TRACE(tl, kEvEpiEnd);
         }
         if (++kt == p.nt) {
           kt = 0;
@@ -1052,6 +1083,9 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
   }
   // no CTA leaves while its peer may still write into its shared memory
   cluster_sync_all();
+#ifdef SMLA_TRACE
+  if (tid == 0) WIDE_TRACE(0, kEvExit);
+#endif
 }
 
 // Q of the FP8 path: each (token, head) row of 576 bf16 values is scaled by
@@ -1224,6 +1258,7 @@ cudaError_t launch_wide(const AttnArgs& a, const AttnPlan& plan, cudaStream_t st
   p.R = a.R;
   p.MB = a.MB;
   p.out = static_cast<__nv_bfloat16*>(a.out);
+  p.out_v8 = (reinterpret_cast<uintptr_t>(a.out) & 31u) == 0 ? 1 : 0;
   p.lse = a.lse;
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
   p.status = reinterpret_cast<int*>(ws);

@@ -1,13 +1,15 @@
-"""Per-tile timeline of the 16-head FP8 decode kernel, for performance work.
+"""Per-tile timelines of the FP8 decode kernels, for performance work.
 
 Builds a separate traced copy of the library (all sources compiled with
 SMLA_TRACE, in ``_build_trace/``), runs the memory-bound decode workload
 (64 requests x 1 token, H = 16, top-k 2048) a few times, then once with the
 trace buffer attached, and prints per-tile timings taken from %globaltimer at
 the kernel roles' hand-off points (median over CTAs, microseconds from the
-CTA's first index translation):
+CTA's first index translation); with --wide, the same for the 128-head
+CTA-pair kernel on its tensor-bound workload (clock64 cycles within a CTA):
 
     python -m sparse_mla_attention_fp8_gb300.trace
+    python -m sparse_mla_attention_fp8_gb300.trace --wide   # the 128-head FP8 decode
 
 The normal library (``libsmla.so``) carries none of this: the hooks compile
 to nothing without SMLA_TRACE.
@@ -160,5 +162,109 @@ def main(lib_path: str | None = None):
         print(f"decode call in CUDA graphs of {n}: {e0.elapsed_time(e1) / (40 * n) * 1e3:.1f} us per call")
 
 
+WIDE_EVENTS = ["s_full", "s_loaded", "x_free", "sent", "x_full", "p_ready", "p_full", "qk", "pv", "issue", "qk_seen",
+               "k_empty", "converted", "raw_full", "x_top", "x_k_full", "enter", "epi_start", "epi_end", "exit"]
+WIDE_TILES = 64
+
+
+def main_wide(lib_path: str | None = None):
+    """Per-tile timeline of the 128-head FP8 decode (128 requests x 1 token,
+    H = 128, top-k 2048, context 65536) from the CTA-pair kernel's clock64()
+    marks: cycles within each CTA (SM clocks are not comparable across SMs)."""
+    import torch
+
+    root = os.path.dirname(_PKG)
+    if root not in sys.path:
+        sys.path.insert(0, root)
+    import smla_inputs as inp
+
+    L = ctypes.CDLL(lib_path or build_traced())
+    P, i32, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    L.sparse_mla_decode_fp8.argtypes = [P, P, P, P, P, f32, i32, P, P, i32, i32, i32, i32, i32, i32, P, sz, P]
+    L.mla_cache_store_fp8.argtypes = [P, P, P, i32, i32, P]
+    L.sparse_mla_decode_workspace_bytes.argtypes = [i32, i32, i32, i32]
+    L.sparse_mla_decode_workspace_bytes.restype = sz
+    L.sparse_mla_attention_plan.argtypes = [i32, i32, i32, i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32)]
+    L.smla_trace_set_wide.argtypes = [P]
+    ptr = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+
+    dev = torch.device("cuda", 0)
+    case = inp.rotating_decode(seed=2, R=128, ctx_lo=65536, ctx_hi=65536, K=2048, H=128, outliers=True)
+    T, H, K, NB = case.q.shape[0], case.H, case.K, case.num_blocks
+    cache = torch.zeros((NB, 64, 656), dtype=torch.uint8, device=dev)
+    lat = inp.device_latent(len(case.ctx_slots), case.latent_seed, case.outlier_channels, dev)
+    slots = torch.from_numpy(case.ctx_slots).to(dev)
+    assert L.mla_cache_store_fp8(ptr(lat), ptr(slots), ptr(cache), lat.shape[0], NB, None) == 0
+    del lat
+    q = torch.from_numpy(case.q.view(np.int16)).to(dev)
+    idx = [torch.from_numpy(s).to(dev) for s in case.index_sets]
+    bt = torch.from_numpy(case.block_table).to(dev)
+    req = torch.from_numpy(case.req_id_per_token).to(dev)
+    ws_bytes = L.sparse_mla_decode_workspace_bytes(T, H, K, 0)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+    out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+    launches, ctas = ctypes.c_int(0), ctypes.c_int(0)
+    L.sparse_mla_attention_plan(1, T, H, K, 0, ctypes.byref(launches), ctypes.byref(ctas))
+    G = ctas.value
+    buf = torch.zeros((G, WIDE_TILES, len(WIDE_EVENTS)), dtype=torch.int64, device=dev)
+
+    def call(i):
+        rc = L.sparse_mla_decode_fp8(ptr(q), ptr(cache), ptr(idx[i % len(idx)]), ptr(bt), ptr(req),
+                                     f32(case.sm_scale), 0, ptr(out), ptr(lse), T, H, K, bt.shape[0], bt.shape[1],
+                                     NB, ptr(ws), ws_bytes, None)
+        assert rc == 0
+
+    for i in range(4):
+        call(i)
+    torch.cuda.synchronize()
+    assert L.smla_trace_set_wide(ptr(buf)) == 0
+    call(4)
+    torch.cuda.synchronize()
+    assert L.smla_trace_set_wide(None) == 0
+    ev = buf.cpu().numpy().astype(np.float64)
+    ev[ev == 0] = np.nan
+    E = {n: ev[:, :, i] for i, n in enumerate(WIDE_EVENTS)}
+    kc = lambda x: f"{np.nanmedian(x) / 1e3:7.2f}"  # noqa: E731
+    print(f"CTAs {G} ({G // 2} pairs), {launches.value} launches per call; clock64 cycles within each CTA (K = 1000)")
+    print("event position in its tile relative to the tile's QK^T issue (median K cycles):")
+    for n in WIDE_EVENTS[:16]:
+        d = E[n] - E["qk"]
+        if np.isfinite(d).any():
+            print(f"  {n:10s} {kc(d)}")
+    pv = E["pv"]
+    n_t = np.sum(np.isfinite(pv), axis=1)
+    seg_first = np.isfinite(E["epi_start"])  # a segment ends at this tile
+    d = np.diff(pv, axis=1)
+    cross = seg_first[:, :-1]  # the step from a segment's last tile to the next segment's first
+    print(f"P.V cadence inside a segment: {kc(d[~cross])} K cycles; across a segment boundary: {kc(d[cross])}")
+    print(f"segment epilogue (start -> end): {kc(E['epi_end'] - E['epi_start'])} K cycles; "
+          f"segments per CTA: {np.nanmedian(np.sum(seg_first, axis=1)):.1f}, tiles per CTA {np.median(n_t):.0f}")
+    # epilogue by segment kind: a CTA's first segment starts mid-token (the
+    # token's second part) except in the first pair, its last ends mid-token
+    # (first part, merged there) except in the last pair, the others are whole
+    kinds = {"second part (publishes)": [], "whole token": [], "first part (merges)": []}
+    for i in range(G):
+        ends = np.where(np.isfinite(E["epi_start"][i]))[0]
+        for j, t in enumerate(ends):
+            dd = E["epi_end"][i, t] - E["epi_start"][i, t]
+            if j == 0 and i >= 2:
+                kinds["second part (publishes)"].append(dd)
+            elif j == len(ends) - 1 and i < G - 2:
+                kinds["first part (merges)"].append(dd)
+            else:
+                kinds["whole token"].append(dd)
+    print("segment epilogue by kind (median K cycles): " +
+          ", ".join(f"{k} {np.median(v) / 1e3:.2f}" for k, v in kinds.items() if v))
+    enter, ex = E["enter"][:, 0], E["exit"][:, 0]
+    first_pv = pv[:, 0]
+    last_pv = np.array([row[np.isfinite(row)][-1] if np.isfinite(row).any() else np.nan for row in pv])
+    print(f"entry -> first P.V {kc(first_pv - enter)}; last P.V -> exit {kc(ex - last_pv)}; "
+          f"entry -> exit {kc(ex - enter)} K cycles")
+
+
 if __name__ == "__main__":
-    main()
+    if "--wide" in sys.argv:
+        main_wide()
+    else:
+        main()
