@@ -44,16 +44,16 @@ UNIT = "query-tokens/s"
 # figure no longer applies and the roofline reports null.
 TRAFFIC_SOURCES = ("smla_decode.cu", "smla_combine.cuh", "smla_common.cuh", "sm103_ptx.cuh")
 TRAFFIC_BY_SOURCE = {
-    "bb863e2a8d4971a2": 100_922_112 + 2_977_280,  # 128-row tiles, cluster merge: no combine launch
+    "ea3d7b5dc0646f12": 100_911_872 + 2_947_584,  # 128-row tiles, symmetric cluster merge: no combine launch
 }
 # The same for the 128-head CTA-pair kernel, per workload: the bf16 prefill's
-# attention kernel plus its combine; the FP8 decode's attention kernel alone
-# (its capture left out the Q preparation and the combine).
+# attention kernel plus its combine; the FP8 decode's attention kernel, which
+# merges its split tokens itself (the Q preparation, 18.9 MB, is left out).
 WIDE_TRAFFIC_SOURCES = ("smla_wide.cu", "smla_combine.cuh", "smla_common.cuh", "sm103_ptx.cuh")
 WIDE_TRAFFIC_BY_SOURCE = {
-    ("71d5b8755a8edd55", "prefill_h128_k2048"): (671_053_056 + 524_675_840 + 38_473_472 + 210_944,
+    ("493cf41b1e606a5a", "prefill_h128_k2048"): (674_349_568 + 531_697_664 + 38_474_496 + 186_880,
                                                  "attention kernel + combine"),
-    ("71d5b8755a8edd55", "decode_h128_k2048"): (231_825_408 + 23_199_232, "attention kernel only"),
+    ("493cf41b1e606a5a", "decode_h128_k2048"): (250_123_264 + 20_676_352, "attention kernel (merges its split tokens)"),
 }
 
 
