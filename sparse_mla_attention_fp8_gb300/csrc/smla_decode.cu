@@ -66,7 +66,7 @@ constexpr uint32_t kFullMask = 0xffffffffu;
 // through smla_trace_set_fp8.  Compiled out otherwise.
 #ifdef SMLA_TRACE
 __device__ unsigned long long* g_smla_trace_fp8 = nullptr;
-constexpr int kTraceTiles = 16, kTraceEvents = 22;
+constexpr int kTraceTiles = 16, kTraceEvents = 23;
 #define SMLA_TRACE_SET(tl, ev)                                                                                  \
   do {                                                                                                          \
     if (trace_buf && (tl) < kTraceTiles)                                                                        \
@@ -82,10 +82,11 @@ constexpr int kTraceTiles = 16, kTraceEvents = 22;
 // segment's first tile), epilogue past the last P.V, cluster merge: before
 // the wait for the other CTA, after it; the CTA's first instruction and its
 // exit (tile 0's slots); cluster merge steps: sums and LSEs done, readiness
-// signalled, the others' readiness seen, values sent, output written
+// signalled, the others' readiness seen, values sent, output written; set-up
+// done (barriers initialised, tensor memory allocated, cluster synchronised)
 enum { kEvIdx = 0, kEvBufFree, kEvIssued, kEvLanded, kEvOpFull, kEvQk, kEvSoftStart, kEvSoftBar, kEvPWritten, kEvPv,
        kEvEpi, kEvQReady, kEvEpiStart, kEvMergeWait, kEvMergeGo, kEvEnter, kEvExit, kEvEpiLse, kEvEpiSignal,
-       kEvEpiReady, kEvEpiSent, kEvEpiWritten };
+       kEvEpiReady, kEvEpiSent, kEvEpiWritten, kEvSetup };
 
 constexpr int HG = 16;                 // heads per CTA work unit
 constexpr int kRows = 128;             // top-k rows per tile
@@ -366,6 +367,18 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(cons
   const int64_t xbeg = tile_begin(blockIdx.x, p.total, p.G);
   const int64_t xend = tile_begin(blockIdx.x + 1, p.total, p.G);
   const int n_local = (int)(xend - xbeg);
+  // the index warp's loads for the first tile go out before the set-up below,
+  // so their memory latency overlaps it
+  int32_t idx0[4] = {-1, -1, -1, -1}, req0 = 0;
+  if (warp == kIndexWarp && n_local > 0) {
+    const TileInfo t0 = tile_info(p, xbeg, xbeg, xend);
+    req0 = __ldg(p.req_id + t0.t);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int k = t0.kt * kRows + lane + 32 * i;
+      idx0[i] = k < p.K ? __ldg(p.indices + (int64_t)t0.t * p.K + k) : -1;
+    }
+  }
 
   if (tid == 0) {
     for (int i = 0; i < kOpBufs; ++i) {
@@ -407,6 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(cons
     __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  if (tid == 0) SMLA_TRACE_SET(0, kEvSetup);
   // Launched as a programmatic dependent (of the cache store, typically): the
   // index translation and the Q split read only this call's inputs and write
   // only shared memory, so they start at once; every other role reads the
@@ -419,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(cons
     // ------------------------------------------------------------ index translation
     // The next tile's indices are loaded before this tile's block-table reads,
     // so each tile costs about one memory round trip.
-    int32_t cur[4], nxt[4], req_cur = 0, req_nxt = 0;
+    int32_t cur[4] = {idx0[0], idx0[1], idx0[2], idx0[3]}, nxt[4], req_cur = req0, req_nxt = 0;
     auto load_idx = [&](int tl, int32_t (&v)[4], int32_t& rq) {
       const TileInfo ti = tile_info(p, xbeg + tl, xbeg, xend);
       rq = __ldg(p.req_id + ti.t);
@@ -429,7 +443,6 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(cons
         v[i] = k < p.K ? __ldg(p.indices + (int64_t)ti.t * p.K + k) : -1;
       }
     };
-    if (n_local > 0) load_idx(0, cur, req_cur);
     for (int tl = 0; tl < n_local; ++tl) {
       if (tl + 1 < n_local) load_idx(tl + 1, nxt, req_nxt);
       const int b4 = tl & 3;

@@ -27,7 +27,7 @@ from . import NVCC_FLAGS, SOURCES, _CSRC, _PKG, _nvcc
 
 EVENTS = ["idx", "buf_free", "issued", "landed", "op_full", "qk", "soft_start", "soft_bar", "p_written", "pv",
           "epilogue", "q_ready", "epi_start", "merge_wait", "merge_go", "enter", "exit", "epi_lse", "epi_signal",
-          "epi_ready", "epi_sent", "epi_written"]
+          "epi_ready", "epi_sent", "epi_written", "setup"]
 # per-tile links: (name, from event, to event, tile offset of the end event)
 LINKS = [("copy issue (loader 0)", "buf_free", "issued", 0), ("copy landing (loader 0)", "issued", "landed", 0),
          ("other loaders after loader 0", "landed", "op_full", 0), ("QK^T issue", "op_full", "qk", 0),
@@ -145,6 +145,11 @@ def main(lib_path: str | None = None):
     print(f"CTA entry: first {np.nanmin(enter):.2f} last {np.nanmax(enter):.2f} us; exit: first {np.nanmin(ex):.2f} "
           f"median {np.nanmedian(ex):.2f} last {np.nanmax(ex):.2f} us; first entry to last exit "
           f"{np.nanmax(ex) - np.nanmin(enter):.2f} us")
+    setup = rel[:, 0, EVENTS.index("setup")]
+    print(f"start-up (median over CTAs, us from the CTA's entry): set-up done {np.nanmedian(setup - enter):.2f}, "
+          f"tile 0 translated {np.nanmedian(rel[:, 0, 0] - enter):.2f}, its copies issued "
+          f"{np.nanmedian(rel[:, 0, EVENTS.index('issued')] - enter):.2f}, landed "
+          f"{np.nanmedian(rel[:, 0, EVENTS.index('landed')] - enter):.2f}, first P.V {np.nanmedian(pv[:, 0] - enter):.2f}")
     # the same call timed alone and in CUDA graphs of 1 and 8 calls (no trace buffer)
     for n in (1, 8):
         g = torch.cuda.CUDAGraph()
