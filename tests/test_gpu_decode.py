@@ -239,3 +239,14 @@ def test_h128_split_tokens_merged_in_the_attention_kernel():
     case.indices[9, :] = -1      # a token without any
     check_decode(case)
     check_decode(case)  # the merge flags start from zero on the next call too
+
+
+def test_h128_in_kernel_merge_with_ranges_one_token_long():
+    # 77 tokens of 19 tiles (the last one ragged, 48 rows) over 76 CTA pairs: most ranges are exactly one
+    # token long, so a pair's first segment is a token's second part and its last the next token's first
+    # part, with no whole token in between.
+    import sparse_mla_attention_fp8_gb300 as smla
+    case = inp.memory_bound_decode(seed=42, R=77, ctx_lo=1300, ctx_hi=3000, K=1200, H=128)
+    launches, _ = smla.attention_plan(True, 77, 128, 1200, 0)
+    assert launches in (2, 3)
+    check_decode(case)
