@@ -40,6 +40,10 @@ __global__ void __launch_bounds__(256) quantize_store_kernel(const uint4* __rest
   // a decode launched behind this grid as its programmatic dependent may start
   // its prologue now; it waits for this grid before it reads the cache
   grid_launch_dependents();
+  // launched itself as a programmatic dependent of the preceding kernel (a
+  // decode still reading the cache, say): nothing is read or written before
+  // that grid has completed
+  grid_dependency_wait();
   const int token = (int)((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (token >= T) return;
@@ -198,8 +202,20 @@ cudaError_t launch_quantize_store(const void* kv_new, const int64_t* slot_mappin
   if (T <= 0) return cudaSuccess;
   const int threads = 256;
   const int64_t blocks = ((int64_t)T * 32 + threads - 1) / threads;
-  quantize_store_kernel<<<(unsigned)blocks, threads, 0, stream>>>(static_cast<const uint4*>(kv_new), slot_mapping,
-                                                                  cache, T, NB);
+  // a programmatic dependent of the preceding kernel on the stream: its launch
+  // overlaps that kernel's tail, and the kernel waits for it before any access
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)blocks, 1, 1);
+  cfg.blockDim = dim3(threads, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, quantize_store_kernel, static_cast<const uint4*>(kv_new), slot_mapping,
+                                     cache, T, NB);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
