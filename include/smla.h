@@ -195,7 +195,10 @@ int sparse_mla_attention_plan(int fp8, int T, int H, int K, int num_splits, int*
  *   kv_cache     uint8 [NB, 64, 656], 16-byte aligned
  * Per group of 128 NoPE values: scale = amax / 448 in IEEE float32, code = the float32 quotient
  * value / scale rounded to nearest-even e4m3 with saturation (a group with scale 0 stores zeros);
- * the 4 scales and the RoPE values are stored verbatim.  Two tokens with the same slot race. */
+ * the 4 scales and the RoPE values are stored verbatim.  Two tokens with the same slot race.
+ * Launch order: the kernel is a programmatic dependent of the preceding kernel on `stream` (its
+ * launch may overlap that kernel's tail); it reads and writes nothing before that kernel has
+ * completed, so stream order holds as for an ordinary launch. */
 int mla_cache_store_fp8(const void* kv_new, const int64_t* slot_mapping, uint8_t* kv_cache, int T, int NB,
                         void* stream);
 
