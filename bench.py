@@ -425,7 +425,7 @@ def run_ours(args):
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": step_ms_max, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "vs_baseline": None, "dtype": "e4m3", "data": "synthetic",
             "config": {
                 "workload": f"{case.name}: memory-bound FP8 sparse decode, {T} requests x 1 token, H={H}, "
                             f"top-k {K}, context U[8192,32768], block 64, 656-byte FP8 cache ({NB} blocks, "
