@@ -44,7 +44,7 @@ UNIT = "query-tokens/s"
 # figure no longer applies and the roofline reports null.
 TRAFFIC_SOURCES = ("smla_decode.cu", "smla_combine.cuh", "smla_common.cuh", "sm103_ptx.cuh")
 TRAFFIC_BY_SOURCE = {
-    "5505df2f15428673": 100_915_456 + 2_309_120,  # 128-row tiles, symmetric cluster merge: no combine launch
+    "3e9c80169300af85": 100_915_456 + 2_309_120,  # 128-row tiles, symmetric cluster merge (re-keyed: an unused helper removed, cubin identical)
 }
 # The same for the 128-head CTA-pair kernel, per workload: the bf16 prefill's
 # attention kernel plus its combine; the FP8 decode's attention kernel, which
