@@ -250,3 +250,16 @@ def test_h128_in_kernel_merge_with_ranges_one_token_long():
     launches, _ = smla.attention_plan(True, 77, 128, 1200, 0)
     assert launches in (2, 3)
     check_decode(case)
+
+
+@pytest.mark.parametrize("H", [16, 32])
+@pytest.mark.parametrize("K", [512, 1000])
+@pytest.mark.parametrize("num_splits", [3, 4])
+def test_cluster_merge_of_three_and_four_parts(num_splits, K, H):
+    # every unit cut into 3 or 4 aligned parts run as one cluster: each CTA writes the value chunks q with
+    # q % S == rank and receives the others' values of them (S = 3: ranks own 2, 1, 1 chunks)
+    import sparse_mla_attention_fp8_gb300 as smla
+    case = inp.memory_bound_decode(seed=43, R=5, ctx_lo=1100, ctx_hi=3000, K=K, H=H)
+    launches, ctas = smla.attention_plan(True, 5, H, K, num_splits)
+    assert launches == 1 and ctas == 5 * (H // 16) * num_splits  # no combine launch: merged in the cluster
+    check_decode(case, num_splits=num_splits)
