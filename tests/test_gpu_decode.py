@@ -263,3 +263,35 @@ def test_cluster_merge_of_three_and_four_parts(num_splits, K, H):
     launches, ctas = smla.attention_plan(True, 5, H, K, num_splits)
     assert launches == 1 and ctas == 5 * (H // 16) * num_splits  # no combine launch: merged in the cluster
     check_decode(case, num_splits=num_splits)
+
+
+def test_store_launched_after_a_decode_waits_for_it():
+    # decode, then a cache store that overwrites 64 rows the decode reads (the store is launched as a
+    # programmatic dependent of the decode), then a second decode: the first sees the old rows only,
+    # the second the new ones
+    import torch
+    import sparse_mla_attention_fp8_gb300 as smla
+    case = inp.memory_bound_decode(seed=44, R=6, ctx_lo=500, ctx_hi=1500, K=256, H=16)
+    cache_old = oracle_cache(case)
+    slots = oracle.translate(case.indices, case.block_table, case.req_id_per_token, case.num_blocks)
+    tgt = np.unique(slots[slots >= 0])[:64].astype(np.int64)
+    rng = np.random.default_rng(45)
+    new_rows = inp.bf16_bits((rng.standard_normal((len(tgt), 576)) * 2.0).astype(np.float32))
+    cache_new = cache_old.copy()
+    oracle.quantize_store(new_rows, tgt, cache_new)
+    T = case.q.shape[0]
+    d_cache = dev(cache_old)
+    q, idx, bt, req = bf16_dev(case.q), dev(case.indices), dev(case.block_table), dev(case.req_id_per_token)
+    outs = [torch.empty((T, 16, 512), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    lses = [torch.empty((T, 16), dtype=torch.float32, device="cuda") for _ in range(2)]
+    torch.cuda.synchronize()
+    smla.sparse_mla_decode_fp8(q, d_cache, idx, bt, req, case.sm_scale, 0, outs[0], lses[0])
+    smla.mla_cache_store_fp8(bf16_dev(new_rows), dev(tgt), d_cache)
+    smla.sparse_mla_decode_fp8(q, d_cache, idx, bt, req, case.sm_scale, 0, outs[1], lses[1])
+    torch.cuda.synchronize()
+    for k, cache in enumerate((cache_old, cache_new)):
+        ref_out, ref_lse = oracle.sparse_mla_decode(case.q, cache, case.indices, case.block_table,
+                                                    case.req_id_per_token, case.sm_scale)
+        assert_out_close(outs[k].float().cpu().numpy(), ref_out, f"decode {k}")
+        assert_lse_close(lses[k].cpu().numpy(), ref_lse, f"decode {k}")
+    assert np.array_equal(d_cache.cpu().numpy(), cache_new)
