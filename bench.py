@@ -713,6 +713,30 @@ def tensor_workload(args, quiet=False):
                      "avg_launch_us": ms * 1e3},
         "cpu_baseline": cpu, "e2e": None, "gpu_launches": launches * args.steps, "clocks": clk,
     }
+    if args.workload == "decode_h128_k2048":
+        # the FP8-query variant of the same call (its own CTA-pair kernel at 128 heads: e4m3 MMAs)
+        def launch_q8(i):
+            smla.sparse_mla_decode_fp8_qfp8(q, cache, idx_sets[i % len(idx_sets)], bt, req, case.sm_scale, 0, out,
+                                            lse, ws, stream=stream)
+        with torch.cuda.stream(stream):
+            for i in range(max(args.warmup, 3)):
+                launch_q8(i)
+        stream.synchronize()
+        graphs_q8 = []
+        for i in range(n_graphs):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                launch_q8(i)
+            graphs_q8.append(g)
+        time_graphs(graphs_q8, max(args.warmup, 3), stream)
+        ms_q8 = time_graphs(graphs_q8, args.steps, stream)
+        if smla.read_device_status(ws, stream) != 0:
+            raise SystemExit("device status reports a kernel wait timeout")
+        tf_q8 = flops / (ms_q8 * 1e-3) / 1e12
+        line["fp8_query_variant"] = {
+            "call": "sparse_mla_decode_fp8_qfp8", "ms_per_step": ms_q8, "value": T / (ms_q8 * 1e-3), "unit": UNIT,
+            "tflops": tf_q8, "dtype": "e4m3", "frac_of_fp8_peak": tf_q8 / tensor_peak_tflops(peaks, True),
+            "frac_of_bf16_peak": tf_q8 / peak, "gpu_launches": launches * args.steps}
     if algo_bytes is not None:
         gbs = algo_bytes / (ms * 1e-3) / 1e9
         line["metric"] = f"{args.workload} query-tokens/s + GB/s vs HBM roofline"

@@ -72,8 +72,26 @@ int sparse_mla_decode_fp8(const void* q, const uint8_t* kv_cache, const int32_t*
                           int num_splits, void* out, float* lse, int T, int H, int K, int R, int MB, int NB,
                           void* workspace, size_t workspace_bytes, void* stream);
 
-/* Workspace bytes sparse_mla_decode_fp8 needs on the current device. */
+/* Workspace bytes sparse_mla_decode_fp8 (and sparse_mla_decode_fp8_qfp8) needs on the current device. */
 size_t sparse_mla_decode_workspace_bytes(int T, int H, int K, int num_splits);
+
+/* sparse_mla_decode_fp8 with the query quantized to FP8 and both products on
+ * the FP8 tensor path at every head count: the query-precision variant of
+ * [vLLM PR #59342] (its tests quantize the query to fp8 for every quantized
+ * cache).  Same arguments, layouts, error codes, workspace and launch order
+ * as sparse_mla_decode_fp8.  Each (token, head, 128-column group) of q is
+ * scaled by a power of two and split into two e4m3 terms, |q - (hi + lo)| <=
+ * 2^-8 |q| + 2^-17 of the group's largest; the cache codes enter QK^T and P.V
+ * as stored (tcgen05 kind::f8f6f4), the row scales folded into the logits and
+ * into P, which is itself split into two e4m3 terms.  For H < 128 this is
+ * what sparse_mla_decode_fp8 computes already, and the call is the same.  For
+ * H = 128 it runs a CTA-pair kernel of its own, slower on GB300 than
+ * sparse_mla_decode_fp8's (which converts the codes to f16 on chip) and less
+ * exact in P (about 8 significant bits against f16's 11). */
+int sparse_mla_decode_fp8_qfp8(const void* q, const uint8_t* kv_cache, const int32_t* indices,
+                               const int32_t* block_table, const int32_t* req_id_per_token, float sm_scale,
+                               int num_splits, void* out, float* lse, int T, int H, int K, int R, int MB, int NB,
+                               void* workspace, size_t workspace_bytes, void* stream);
 
 /* sparse_mla_decode_fp8 without any allocation: the same computation and
  * arguments, minus the workspace, whose role a fixed scratch array compiled

@@ -28,7 +28,7 @@ _BUILD = os.path.join(_PKG, "_build")
 LIB_PATH = os.path.join(_PKG, "libsmla.so")
 HEADER = os.path.join(_ROOT, "include", "smla.h")
 
-SOURCES = ["smla_decode.cu", "smla_attn.cu", "smla_wide.cu", "smla_store.cu", "smla_absorb.cu", "smla_api.cu"]
+SOURCES = ["smla_decode.cu", "smla_attn.cu", "smla_wide.cu", "smla_wide8.cu", "smla_store.cu", "smla_absorb.cu", "smla_api.cu"]
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-std=c++17", "-lineinfo",
               "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall"]
 
@@ -95,6 +95,8 @@ def lib():
             P, i32, sz, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_float
             L.sparse_mla_decode_fp8.argtypes = [P, P, P, P, P, f32, i32, P, P, i32, i32, i32, i32, i32, i32, P, sz, P]
             L.sparse_mla_decode_fp8.restype = i32
+            L.sparse_mla_decode_fp8_qfp8.argtypes = L.sparse_mla_decode_fp8.argtypes
+            L.sparse_mla_decode_fp8_qfp8.restype = i32
             L.sparse_mla_decode_fp8_noalloc.argtypes = [P, P, P, P, P, f32, i32, P, P, i32, i32, i32, i32, i32, i32, P]
             L.sparse_mla_decode_fp8_noalloc.restype = i32
             L.sparse_mla_decode_workspace_bytes.argtypes = [i32, i32, i32, i32]
@@ -198,6 +200,21 @@ def sparse_mla_decode_fp8(q, kv_cache, indices, block_table, req_id_per_token, s
     """FP8 sparse decode.  q bf16 [T,H,576]; kv_cache uint8 [NB,64,656];
     indices int32 [T,K] (logical, <0 = none); block_table int32 [R,MB];
     req_id_per_token int32 [T].  Returns (out bf16 [T,H,512], lse fp32 [T,H])."""
+    return _decode("sparse_mla_decode_fp8", q, kv_cache, indices, block_table, req_id_per_token, sm_scale,
+                   num_splits, out, lse, workspace, stream)
+
+
+def sparse_mla_decode_fp8_qfp8(q, kv_cache, indices, block_table, req_id_per_token, sm_scale: float,
+                               num_splits: int = 0, out=None, lse=None, workspace=None, stream=None):
+    """sparse_mla_decode_fp8 with the query quantized to FP8 (two e4m3 terms)
+    and both products on the FP8 tensor path; at H = 128 a kernel of its own
+    (slower than sparse_mla_decode_fp8's on GB300).  Same arguments and results."""
+    return _decode("sparse_mla_decode_fp8_qfp8", q, kv_cache, indices, block_table, req_id_per_token, sm_scale,
+                   num_splits, out, lse, workspace, stream)
+
+
+def _decode(name, q, kv_cache, indices, block_table, req_id_per_token, sm_scale, num_splits, out, lse, workspace,
+            stream):
     import torch
     dev = _dev(q, kv_cache, indices, block_table, req_id_per_token, out, lse, workspace)
     T, H, D = q.shape
@@ -217,10 +234,10 @@ def sparse_mla_decode_fp8(q, kv_cache, indices, block_table, req_id_per_token, s
     _expect(out, torch.bfloat16, (T, H, 512), "out")
     _expect(lse, torch.float32, (T, H), "lse")
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    rc = lib().sparse_mla_decode_fp8(_ptr(q), _ptr(kv_cache), _ptr(indices), _ptr(block_table),
-                                     _ptr(req_id_per_token), float(sm_scale), int(num_splits), _ptr(out), _ptr(lse),
-                                     T, H, K, R, MB, NB, _ptr(workspace), ws_bytes, _stream_ptr(stream, dev))
-    _check(rc, "sparse_mla_decode_fp8")
+    rc = getattr(lib(), name)(_ptr(q), _ptr(kv_cache), _ptr(indices), _ptr(block_table), _ptr(req_id_per_token),
+                              float(sm_scale), int(num_splits), _ptr(out), _ptr(lse), T, H, K, R, MB, NB,
+                              _ptr(workspace), ws_bytes, _stream_ptr(stream, dev))
+    _check(rc, name)
     return out, lse
 
 

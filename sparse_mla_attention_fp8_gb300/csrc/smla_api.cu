@@ -95,12 +95,18 @@ int check_heads(int H) {
   return SMLA_OK;
 }
 
+// qfp8: the FP8-query variant of the decode (its own kernel at 128 heads).
+smla::AttnPlan plan_for(bool fp8, bool qfp8, int T, int H, int K, int num_splits, int sms) {
+  if (fp8 && qfp8 && smla::wide_supported(H)) return smla::plan_decode_wide8(T, K, num_splits, sms);
+  return smla::plan_attention(fp8, T, H, K, num_splits, sms);
+}
+
 int run_attention(bool fp8, smla::AttnArgs& a, int num_splits, void* workspace, size_t workspace_bytes,
-                  void* stream) {
+                  void* stream, bool qfp8 = false) {
   int sms = 0;
   int rc = num_sms(&sms);
   if (rc != SMLA_OK) return rc;
-  const smla::AttnPlan plan = smla::plan_attention(fp8, a.T, a.H, a.K, num_splits, sms);
+  const smla::AttnPlan plan = plan_for(fp8, qfp8, a.T, a.H, a.K, num_splits, sms);
   if (workspace) {
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
       return fail(SMLA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
@@ -111,7 +117,9 @@ int run_attention(bool fp8, smla::AttnArgs& a, int num_splits, void* workspace, 
     if (rc != SMLA_OK) return rc;
   }
   a.workspace = workspace;
-  cudaError_t e = smla::launch_attention(fp8, a, plan, static_cast<cudaStream_t>(stream));
+  cudaError_t e = fp8 && qfp8 && plan.HG == 128
+                      ? smla::launch_decode_wide8(a, plan, static_cast<cudaStream_t>(stream))
+                      : smla::launch_attention(fp8, a, plan, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, fp8 ? "sparse_mla_decode_fp8 launch" : "sparse_mla_prefill_bf16 launch");
   return SMLA_OK;
 }
@@ -120,7 +128,10 @@ size_t workspace_bytes_for(bool fp8, int T, int H, int K, int num_splits) {
   if (T <= 0 || check_heads(H) != SMLA_OK || K < 0) return 0;
   int sms = 0;
   if (num_sms(&sms) != SMLA_OK) return 0;
-  return smla::plan_attention(fp8, T, H, K, num_splits, sms).ws_bytes;
+  const size_t ws = smla::plan_attention(fp8, T, H, K, num_splits, sms).ws_bytes;
+  // the decode's size covers its FP8-query variant too
+  const size_t ws8 = fp8 ? plan_for(true, true, T, H, K, num_splits, sms).ws_bytes : 0;
+  return ws > ws8 ? ws : ws8;
 }
 
 // ---- fixed scratch for sparse_mla_decode_fp8_noalloc: part of the module
@@ -147,14 +158,10 @@ int noalloc_scratch(void** out) {
 // Bytes of the translated index rows of sparse_mla_prefill_fp8 (256-byte aligned).
 size_t fp8_prefill_index_bytes(int T, int K) { return (((size_t)T * (size_t)K * 4 + 255) / 256) * 256; }
 
-}  // namespace
-
-extern "C" {
-
-int sparse_mla_decode_fp8(const void* q, const uint8_t* kv_cache, const int32_t* indices,
-                          const int32_t* block_table, const int32_t* req_id_per_token, float sm_scale,
-                          int num_splits, void* out, float* lse, int T, int H, int K, int R, int MB, int NB,
-                          void* workspace, size_t workspace_bytes, void* stream) {
+int decode_entry(bool qfp8, const void* q, const uint8_t* kv_cache, const int32_t* indices,
+                 const int32_t* block_table, const int32_t* req_id_per_token, float sm_scale, int num_splits,
+                 void* out, float* lse, int T, int H, int K, int R, int MB, int NB, void* workspace,
+                 size_t workspace_bytes, void* stream) {
   if (T < 0 || K < 0 || R <= 0 || MB <= 0 || NB <= 0 || num_splits < 0)
     return fail(SMLA_ERR_INVALID_ARG, "bad sizes T=%d K=%d R=%d MB=%d NB=%d num_splits=%d", T, K, R, MB, NB,
                 num_splits);
@@ -182,7 +189,27 @@ int sparse_mla_decode_fp8(const void* q, const uint8_t* kv_cache, const int32_t*
   a.R = R;
   a.MB = MB;
   a.NB = NB;
-  return run_attention(true, a, num_splits, workspace, workspace_bytes, stream);
+  return run_attention(true, a, num_splits, workspace, workspace_bytes, stream, qfp8);
+}
+
+}  // namespace
+
+extern "C" {
+
+int sparse_mla_decode_fp8(const void* q, const uint8_t* kv_cache, const int32_t* indices,
+                          const int32_t* block_table, const int32_t* req_id_per_token, float sm_scale,
+                          int num_splits, void* out, float* lse, int T, int H, int K, int R, int MB, int NB,
+                          void* workspace, size_t workspace_bytes, void* stream) {
+  return decode_entry(false, q, kv_cache, indices, block_table, req_id_per_token, sm_scale, num_splits, out, lse,
+                      T, H, K, R, MB, NB, workspace, workspace_bytes, stream);
+}
+
+int sparse_mla_decode_fp8_qfp8(const void* q, const uint8_t* kv_cache, const int32_t* indices,
+                               const int32_t* block_table, const int32_t* req_id_per_token, float sm_scale,
+                               int num_splits, void* out, float* lse, int T, int H, int K, int R, int MB, int NB,
+                               void* workspace, size_t workspace_bytes, void* stream) {
+  return decode_entry(true, q, kv_cache, indices, block_table, req_id_per_token, sm_scale, num_splits, out, lse,
+                      T, H, K, R, MB, NB, workspace, workspace_bytes, stream);
 }
 
 int sparse_mla_decode_fp8_noalloc(const void* q, const uint8_t* kv_cache, const int32_t* indices,

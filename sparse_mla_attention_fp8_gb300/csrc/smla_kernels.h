@@ -75,6 +75,12 @@ AttnPlan plan_decode_wide(int T, int K, int num_splits, int num_sms);
 cudaError_t launch_prefill_wide(const AttnArgs& a, const AttnPlan& plan, cudaStream_t stream);
 cudaError_t launch_decode_wide(const AttnArgs& a, const AttnPlan& plan, cudaStream_t stream);
 cudaError_t launch_decode_fp8(const AttnArgs& a, const AttnPlan& plan, cudaStream_t stream);
+
+// The 128-head FP8 decode with the query quantized to e4m3 (two terms) and
+// both products on the FP8 tensor path, the row scales folded into P
+// (smla_wide8.cu).
+AttnPlan plan_decode_wide8(int T, int K, int num_splits, int num_sms);
+cudaError_t launch_decode_wide8(const AttnArgs& a, const AttnPlan& plan, cudaStream_t stream);
 cudaError_t launch_prefill_bf16(const AttnArgs& a, const AttnPlan& plan, cudaStream_t stream);
 
 // Offsets inside the workspace.

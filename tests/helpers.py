@@ -54,9 +54,12 @@ def oracle_cache(case: inp.DecodeCase, with_new: bool = True) -> np.ndarray:
     return cache
 
 
-def run_gpu_decode(case: inp.DecodeCase, cache_np: np.ndarray, num_splits: int = 0, workspace=None):
+def run_gpu_decode(case: inp.DecodeCase, cache_np: np.ndarray, num_splits: int = 0, workspace=None,
+                   qfp8: bool = False):
+    """The decode through the C-ABI (qfp8: its FP8-query variant)."""
     import sparse_mla_attention_fp8_gb300 as smla
-    out, lse = smla.sparse_mla_decode_fp8(bf16_dev(case.q), dev(cache_np), dev(case.indices),
+    fn = smla.sparse_mla_decode_fp8_qfp8 if qfp8 else smla.sparse_mla_decode_fp8
+    out, lse = fn(bf16_dev(case.q), dev(cache_np), dev(case.indices),
                                           dev(case.block_table), dev(case.req_id_per_token), case.sm_scale,
                                           num_splits=num_splits, workspace=workspace)
     torch = torch_mod()
@@ -65,10 +68,10 @@ def run_gpu_decode(case: inp.DecodeCase, cache_np: np.ndarray, num_splits: int =
     return out.float().cpu().numpy(), lse.cpu().numpy()
 
 
-def check_decode(case: inp.DecodeCase, num_splits: int = 0, tokens=None, cache_np=None):
+def check_decode(case: inp.DecodeCase, num_splits: int = 0, tokens=None, cache_np=None, qfp8: bool = False):
     if cache_np is None:
         cache_np = oracle_cache(case)
-    out, lse = run_gpu_decode(case, cache_np, num_splits)
+    out, lse = run_gpu_decode(case, cache_np, num_splits, qfp8=qfp8)
     ref_out, ref_lse = oracle.sparse_mla_decode(case.q, cache_np, case.indices, case.block_table,
                                                 case.req_id_per_token, case.sm_scale, tokens=tokens)
     sel = slice(None) if tokens is None else np.asarray(tokens)
