@@ -10,6 +10,7 @@ CTA-pair kernel on its tensor-bound workload (clock64 cycles within a CTA):
 
     python -m sparse_mla_attention_fp8_gb300.trace
     python -m sparse_mla_attention_fp8_gb300.trace --wide   # the 128-head FP8 decode
+    python -m sparse_mla_attention_fp8_gb300.trace --wide8  # its FP8-query variant
 
 The normal library (``libsmla.so``) carries none of this: the hooks compile
 to nothing without SMLA_TRACE.
@@ -268,8 +269,86 @@ def main_wide(lib_path: str | None = None):
           f"entry -> exit {kc(ex - enter)} K cycles")
 
 
+WIDE8_EVENTS = ["idx", "kfull", "qk", "s_read", "sent", "received", "l_ready", "l_read", "pv_prev_done", "p_full",
+                "pv", "load_issue", "k_empty", "epi_start", "epi_end", "enter", "exit", "q_full"]
+
+
+def main_wide8(lib_path: str | None = None):
+    """Per-tile timeline of the FP8-query 128-head decode (sparse_mla_decode_fp8_qfp8)
+    on the tensor-bound workload: clock64 cycles within each CTA."""
+    import torch
+
+    root = os.path.dirname(_PKG)
+    if root not in sys.path:
+        sys.path.insert(0, root)
+    import smla_inputs as inp
+
+    L = ctypes.CDLL(lib_path or build_traced())
+    P, i32, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    L.sparse_mla_decode_fp8_qfp8.argtypes = [P, P, P, P, P, f32, i32, P, P, i32, i32, i32, i32, i32, i32, P, sz, P]
+    L.mla_cache_store_fp8.argtypes = [P, P, P, i32, i32, P]
+    L.sparse_mla_decode_workspace_bytes.argtypes = [i32, i32, i32, i32]
+    L.sparse_mla_decode_workspace_bytes.restype = sz
+    L.smla_trace_set_wide8.argtypes = [P]
+    ptr = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+
+    dev = torch.device("cuda", 0)
+    case = inp.rotating_decode(seed=2, R=128, ctx_lo=65536, ctx_hi=65536, K=2048, H=128, outliers=True)
+    T, H, K, NB = case.q.shape[0], case.H, case.K, case.num_blocks
+    cache = torch.zeros((NB, 64, 656), dtype=torch.uint8, device=dev)
+    lat = inp.device_latent(len(case.ctx_slots), case.latent_seed, case.outlier_channels, dev)
+    slots = torch.from_numpy(case.ctx_slots).to(dev)
+    assert L.mla_cache_store_fp8(ptr(lat), ptr(slots), ptr(cache), lat.shape[0], NB, None) == 0
+    del lat
+    q = torch.from_numpy(case.q.view(np.int16)).to(dev)
+    idx = [torch.from_numpy(s).to(dev) for s in case.index_sets]
+    bt = torch.from_numpy(case.block_table).to(dev)
+    req = torch.from_numpy(case.req_id_per_token).to(dev)
+    ws_bytes = L.sparse_mla_decode_workspace_bytes(T, H, K, 0)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+    out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+    n_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    buf = torch.zeros((n_sms, WIDE_TILES, len(WIDE8_EVENTS)), dtype=torch.int64, device=dev)
+
+    def call(i):
+        rc = L.sparse_mla_decode_fp8_qfp8(ptr(q), ptr(cache), ptr(idx[i % len(idx)]), ptr(bt), ptr(req),
+                                          f32(case.sm_scale), 0, ptr(out), ptr(lse), T, H, K, bt.shape[0],
+                                          bt.shape[1], NB, ptr(ws), ws_bytes, None)
+        assert rc == 0
+
+    for i in range(4):
+        call(i)
+    torch.cuda.synchronize()
+    assert L.smla_trace_set_wide8(ptr(buf)) == 0
+    call(4)
+    torch.cuda.synchronize()
+    assert L.smla_trace_set_wide8(None) == 0
+    ev = buf.cpu().numpy().astype(np.float64)
+    ev[ev == 0] = np.nan
+    ev = ev[np.isfinite(ev[:, 0, WIDE8_EVENTS.index("enter")])]  # CTAs of the launch
+    E = {n: ev[:, :, i] for i, n in enumerate(WIDE8_EVENTS)}
+    kc = lambda x: f"{np.nanmedian(x) / 1e3:7.2f}"  # noqa: E731
+    print(f"CTAs {ev.shape[0]}; clock64 cycles within each CTA (K = 1000), medians over CTAs and tiles")
+    print("event position in its tile relative to the tile's QK^T issue:")
+    for n in ["load_issue", "kfull", "q_full", "qk", "s_read", "sent", "received", "l_ready", "l_read",
+              "pv_prev_done", "p_full", "pv"]:
+        print(f"  {n:13s} {kc(E[n] - E['qk'])}")
+    print(f"cadence (QK^T issue to the next): {kc(np.diff(E['qk'], axis=1))}; "
+          f"P.V: {kc(np.diff(E['pv'], axis=1))}")
+    print(f"exchange warps, one tile (l_ready to the next): {kc(np.diff(E['l_ready'], axis=1))}; "
+          f"softmax, L read to P' written: {kc(E['p_full'] - E['l_read'])}")
+    print(f"row gather, issue to full: {kc(E['kfull'] - E['load_issue'])}; "
+          f"tile buffer free (P.V of tile t done) to reload (tile t + 4): {kc(E['k_empty'][:, 4:] - E['pv'][:, :-4])}")
+    print(f"segment epilogue: {kc(E['epi_end'] - E['epi_start'])}")
+    enter, ex = E["enter"][:, 0], E["exit"][:, 0]
+    print(f"entry -> first QK^T {kc(E['qk'][:, 0] - enter)}; entry -> exit {kc(ex - enter)}")
+
+
 if __name__ == "__main__":
-    if "--wide" in sys.argv:
+    if "--wide8" in sys.argv:
+        main_wide8()
+    elif "--wide" in sys.argv:
         main_wide()
     else:
         main()
