@@ -14,8 +14,9 @@ Every function cites the passage of the pages it follows (for the C
 functions, in the C source):
 vLLM ``flashmla_sparse.py`` (module docstring on the "FP8 with scale" layout,
 ``triton_convert_req_index_to_global_index`` and its docstring formula,
-``FlashMLASparseImpl.forward``) and the OCP 8-bit floating point
-specification for E4M3.
+``FlashMLASparseImpl.forward``), vLLM PR #59342 (the 352-byte
+``nvfp4_ds_mla`` row), the OCP 8-bit floating point specification for E4M3
+and the OCP Microscaling specification for FP4 E2M1.
 """
 from __future__ import annotations
 
@@ -33,6 +34,7 @@ _lock = threading.Lock()
 _lib = None
 
 ROW_BYTES = 656
+NVFP4_ROW_BYTES = 352
 D_QK = 576
 D_V = 512
 
@@ -64,6 +66,17 @@ def _load():
             lib.oracle_e4m3_from_float.restype = ctypes.c_uint8
             lib.oracle_dequant_row.argtypes = [P, P]
             lib.oracle_dequant_row.restype = None
+            lib.oracle_e2m1_to_double.argtypes = [ctypes.c_uint8]
+            lib.oracle_e2m1_to_double.restype = f64
+            lib.oracle_e2m1_from_float.argtypes = [ctypes.c_float]
+            lib.oracle_e2m1_from_float.restype = ctypes.c_uint8
+            lib.oracle_nvfp4_dequant_row.argtypes = [P, P]
+            lib.oracle_nvfp4_dequant_row.restype = None
+            lib.oracle_nvfp4_quantize_store.argtypes = [P, P, P, i32, i64]
+            lib.oracle_nvfp4_quantize_store.restype = None
+            lib.oracle_sparse_mla_decode_nvfp4.argtypes = [P, P, P, P, P, f64, i32, i32, i32, i32, i32, i64, P, i32,
+                                                           P, P, i32, P, P]
+            lib.oracle_sparse_mla_decode_nvfp4.restype = None
             lib.oracle_translate.argtypes = [P, P, P, i32, i32, i32, i32, i64, P]
             lib.oracle_translate.restype = None
             lib.oracle_quantize_store.argtypes = [P, P, P, i32, i64]
@@ -114,6 +127,27 @@ def dequant_row(row: np.ndarray) -> np.ndarray:
     return out
 
 
+def e2m1_to_double(code: int) -> float:
+    """OCP MX FP4 E2M1 code (4 bits) -> value."""
+    return _load().oracle_e2m1_to_double(int(code) & 0xF)
+
+
+def e2m1_from_float(y: float) -> int:
+    """Nearest E2M1 code (ties to even, saturating to 6)."""
+    return int(_load().oracle_e2m1_from_float(float(y)))
+
+
+def nvfp4_dequant_row(row: np.ndarray) -> np.ndarray:
+    """One 352-byte NVFP4 cache row -> float64[576] (the layout of reading
+    R13 in smla_oracle.c: E2M1 NoPE codes with an E4M3 scale per 16 values,
+    E4M3 RoPE)."""
+    row = _c(row, np.uint8).reshape(-1)
+    assert row.size == NVFP4_ROW_BYTES
+    out = np.empty(D_QK, np.float64)
+    _load().oracle_nvfp4_dequant_row(_p(row), _p(out))
+    return out
+
+
 # ---------------------------------------------------------------- steps
 
 def translate(indices, block_table, req_id_per_token, num_blocks: int) -> np.ndarray:
@@ -140,14 +174,38 @@ def quantize_store(kv_new_bits, slot_mapping, cache: np.ndarray) -> None:
     _load().oracle_quantize_store(_p(kv), _p(sm), _p(cache), T, NB)
 
 
+def nvfp4_quantize_store(kv_new_bits, slot_mapping, cache: np.ndarray) -> None:
+    """Quantize bf16 rows (uint16 bits [T, 576]) into the NVFP4 ``cache``
+    (uint8 [NB, 64, 352], modified in place) at ``slot_mapping`` (int64 [T])."""
+    kv = _c(kv_new_bits, np.uint16)
+    sm = _c(slot_mapping, np.int64)
+    assert cache.dtype == np.uint8 and cache.flags.c_contiguous and cache.shape[-1] == NVFP4_ROW_BYTES
+    NB = cache.shape[0]
+    T = kv.shape[0]
+    assert kv.shape == (T, D_QK) and sm.shape == (T,)
+    _load().oracle_nvfp4_quantize_store(_p(kv), _p(sm), _p(cache), T, NB)
+
+
 def sparse_mla_decode(q_bits, cache, indices, block_table, req_id_per_token, sm_scale: float,
                       tokens=None, nthreads: int | None = None):
     """FP8 sparse decode; returns (out float64 [n, H, 512], lse float64 [n, H])
     for the listed tokens (all tokens when ``tokens`` is None)."""
+    return _decode(_load().oracle_sparse_mla_decode, ROW_BYTES, q_bits, cache, indices, block_table,
+                   req_id_per_token, sm_scale, tokens, nthreads)
+
+
+def sparse_mla_decode_nvfp4(q_bits, cache, indices, block_table, req_id_per_token, sm_scale: float,
+                            tokens=None, nthreads: int | None = None):
+    """The same decode over the NVFP4 cache (uint8 [NB, 64, 352])."""
+    return _decode(_load().oracle_sparse_mla_decode_nvfp4, NVFP4_ROW_BYTES, q_bits, cache, indices, block_table,
+                   req_id_per_token, sm_scale, tokens, nthreads)
+
+
+def _decode(fn, row_bytes, q_bits, cache, indices, block_table, req_id_per_token, sm_scale, tokens, nthreads):
     q = _c(q_bits, np.uint16)
     T, H, D = q.shape
     assert D == D_QK
-    assert cache.dtype == np.uint8 and cache.flags.c_contiguous
+    assert cache.dtype == np.uint8 and cache.flags.c_contiguous and cache.shape[-1] == row_bytes
     NB = cache.shape[0]
     idx = _c(indices, np.int32)
     K = idx.shape[1]
@@ -161,8 +219,8 @@ def sparse_mla_decode(q_bits, cache, indices, block_table, req_id_per_token, sm_
     ws_s = np.empty((nth, max(K, 1)), np.float64)
     out = np.empty((n, H, D_V), np.float64)
     lse = np.empty((n, H), np.float64)
-    _load().oracle_sparse_mla_decode(_p(q), _p(cache), _p(idx), _p(bt), _p(req), float(sm_scale), T, H, K, R, MB,
-                                     NB, _p(tok), n, _p(ws_rows), _p(ws_s), nth, _p(out), _p(lse))
+    fn(_p(q), _p(cache), _p(idx), _p(bt), _p(req), float(sm_scale), T, H, K, R, MB, NB, _p(tok), n, _p(ws_rows),
+       _p(ws_s), nth, _p(out), _p(lse))
     return out, lse
 
 

@@ -20,6 +20,12 @@
  *         cache through slot_mapping (concat_and_cache_mla).
  *  [OCP] OCP 8-bit floating point specification, E4M3: 1 sign, 4 exponent
  *        (bias 7), 3 mantissa bits; subnormals; no infinities; S.1111.111 NaN.
+ *  [OCP-MX] OCP Microscaling Formats (MX) specification, FP4 E2M1 element:
+ *        1 sign, 2 exponent (bias 1), 1 mantissa bit; magnitudes
+ *        0, 0.5, 1, 1.5, 2, 3, 4, 6; no infinities or NaN.
+ *  [P3] vLLM PR #59342, "Purpose": the nvfp4_ds_mla cache holds 352 bytes
+ *        per token against the FP8 one's 576; the native decode reads the
+ *        rows as stored and sees the exact dequantized values.
  *
  * Readings where the pages are silent:
  *  R1 translate also rejects a physical block id outside [0, NB) and a request
@@ -34,6 +40,15 @@
  *  R9 separate-mode FP8 prefill: a row is up-converted to bf16 from the float32
  *     product code * scale (ties to even), an invalid slot gives a zero row,
  *     and a prefill request id outside [0, P) gives -1.
+ *  R13 the NVFP4 row (the pages give its size, 352 bytes, not its layout):
+ *     bytes 0..255 the 512 NoPE values as E2M1 codes, value 2i in the low
+ *     nibble of byte i and 2i + 1 in the high nibble; bytes 256..287 one E4M3
+ *     scale per block of 16 values (byte 256 + b for values 16b .. 16b + 15);
+ *     bytes 288..351 the 64 RoPE values as E4M3.  No per-tensor scale: a row
+ *     dequantizes alone.  Quantizer: block scale = e4m3(amax / 6) (float32
+ *     division, nearest-even, saturating); code = e2m1(x / s) with s the
+ *     scale's value (float32 division, nearest-even, saturating to 6); a
+ *     block whose scale is 0 stores code 0; RoPE = e4m3(value).
  *
  * Every floating-point step of attention is in double.  The quantizer decides
  * integer codes, so it runs in float32, the precision the CUDA kernel uses.
@@ -46,6 +61,8 @@
 #endif
 
 #define ROW_BYTES 656
+#define NVFP4_ROW_BYTES 352
+#define NVFP4_BLOCK 16
 #define D_QK 576
 #define D_V 512
 #define D_NOPE 512
@@ -99,6 +116,42 @@ uint8_t oracle_e4m3_from_float(float y) {
   return sign | (uint8_t)((biased << 3) | (m8 - 8));
 }
 
+/* [OCP-MX] E2M1 decode: value = (-1)^s * 2^(e-1) * (1 + m/2) for e > 0,
+ * (-1)^s * m/2 for e == 0 (code bits: s e1 e0 m). */
+double oracle_e2m1_to_double(uint8_t code) {
+  int s = (code >> 3) & 1;
+  int e = (code >> 1) & 3;
+  int m = code & 1;
+  double v = e == 0 ? 0.5 * (double)m : ldexp(1.0 + 0.5 * (double)m, e - 1);
+  return s ? -v : v;
+}
+
+/* [OCP-MX] encode a float to E2M1, round to nearest with ties to even and
+ * saturation to 6 (reading R13).  Each binade of the format is an evenly
+ * spaced grid: [0, 2) in steps of 1/2 (codes 0..4, the subnormal 0.5 and the
+ * binade [1, 2)), [2, 4) in steps of 1 (codes 4..6), [4, 6] in steps of 2
+ * (codes 6, 7); every grid starts at an even code, so ties to an even grid
+ * index are ties to an even code. */
+uint8_t oracle_e2m1_from_float(float y) {
+  if (isnan(y)) return 0;
+  uint8_t sign = signbit(y) ? 0x8 : 0x0;
+  double a = fabs((double)y);
+  if (a >= 6.0) return sign | 0x7;
+  double base = 0.0, step = 0.5;
+  int code0 = 0;
+  if (a >= 4.0) {
+    base = 4.0;
+    step = 2.0;
+    code0 = 6;
+  } else if (a >= 2.0) {
+    base = 2.0;
+    step = 1.0;
+    code0 = 4;
+  }
+  int k = (int)nearbyint((a - base) / step); /* default rounding mode: ties to even */
+  return sign | (uint8_t)(code0 + k);
+}
+
 double oracle_bf16_to_double(uint16_t bits) {
   uint32_t u = (uint32_t)bits << 16;
   float f;
@@ -127,6 +180,17 @@ void oracle_dequant_row(const uint8_t* row, double* out) {
     memcpy(&b, row + D_NOPE + 16 + 2 * r, 2);
     out[D_NOPE + r] = oracle_bf16_to_double(b);
   }
+}
+
+/* Reading R13: one 352-byte NVFP4 row as stored: K[c] = e2m1(nibble c) *
+ * e4m3(byte 256 + c / 16) for c < 512, K[512 + r] = e4m3(byte 288 + r). */
+void oracle_nvfp4_dequant_row(const uint8_t* row, double* out) {
+  for (int c = 0; c < D_NOPE; ++c) {
+    uint8_t code = (uint8_t)((row[c / 2] >> (4 * (c & 1))) & 0xF);
+    out[c] = oracle_e2m1_to_double(code) * oracle_e4m3_to_double(row[D_NOPE / 2 + c / NVFP4_BLOCK]);
+  }
+  for (int r = 0; r < D_QK - D_NOPE; ++r)
+    out[D_NOPE + r] = oracle_e4m3_to_double(row[D_NOPE / 2 + D_NOPE / NVFP4_BLOCK + r]);
 }
 
 /* ---------------------------------------------------------------- translate */
@@ -183,6 +247,36 @@ void oracle_quantize_store(const uint16_t* kv_new, const int64_t* slot_mapping, 
   }
 }
 
+/* [P3 "Purpose": nvfp4_ds_mla, 352 bytes per token] + reading R13: write each
+ * new token's latent into its NVFP4 cache row at slot_mapping[t] (the skip
+ * rule R5 as for the FP8 cache). */
+void oracle_nvfp4_quantize_store(const uint16_t* kv_new, const int64_t* slot_mapping, uint8_t* cache, int T,
+                                 int64_t NB) {
+  for (int t = 0; t < T; ++t) {
+    int64_t slot = slot_mapping[t];
+    if (slot < 0 || slot >= NB * BLOCK) continue;
+    const uint16_t* x = kv_new + (int64_t)t * D_QK;
+    uint8_t* row = cache + slot * NVFP4_ROW_BYTES;
+    memset(row, 0, D_NOPE / 2);
+    for (int b = 0; b < D_NOPE / NVFP4_BLOCK; ++b) {
+      float amax = 0.0f;
+      for (int c = b * NVFP4_BLOCK; c < (b + 1) * NVFP4_BLOCK; ++c) {
+        float v = fabsf(bf16_to_float(x[c]));
+        if (v > amax) amax = v;
+      }
+      uint8_t sb = oracle_e4m3_from_float(amax / 6.0f);
+      float s = (float)oracle_e4m3_to_double(sb);
+      row[D_NOPE / 2 + b] = sb;
+      for (int c = b * NVFP4_BLOCK; c < (b + 1) * NVFP4_BLOCK; ++c) {
+        uint8_t code = s == 0.0f ? 0 : oracle_e2m1_from_float(bf16_to_float(x[c]) / s);
+        row[c / 2] |= (uint8_t)(code << (4 * (c & 1)));
+      }
+    }
+    for (int r = 0; r < D_QK - D_NOPE; ++r)
+      row[D_NOPE / 2 + D_NOPE / NVFP4_BLOCK + r] = oracle_e4m3_from_float(bf16_to_float(x[D_NOPE + r]));
+  }
+}
+
 /* ---------------------------------------------------------------- attention */
 
 /* Attention of one query head over n dequantized rows (n x 576), [P2]
@@ -218,11 +312,37 @@ static void attend_head(const double* qh, const double* rows, int n, double sm_s
  * q: bf16 bits [T, H, 576]; cache: [NB, 64, 656] bytes; out: [n, H, 512];
  * lse: [n, H].  Workspace is allocated by the caller: rows [K * 576] and
  * s [K] doubles per thread (nthreads copies). */
+static void decode_rows(const uint16_t* q, const uint8_t* cache, int row_bytes,
+                        void (*dequant)(const uint8_t*, double*), const int32_t* indices,
+                        const int32_t* block_table, const int32_t* req_id, double sm_scale, int H, int K, int R,
+                        int MB, int64_t NB, const int32_t* tokens, int n_tokens, double* ws_rows, double* ws_s,
+                        int nthreads, double* out, double* lse);
+
 void oracle_sparse_mla_decode(const uint16_t* q, const uint8_t* cache, const int32_t* indices,
                               const int32_t* block_table, const int32_t* req_id, double sm_scale, int T, int H, int K,
                               int R, int MB, int64_t NB, const int32_t* tokens, int n_tokens, double* ws_rows,
                               double* ws_s, int nthreads, double* out, double* lse) {
   (void)T;
+  decode_rows(q, cache, ROW_BYTES, oracle_dequant_row, indices, block_table, req_id, sm_scale, H, K, R, MB, NB,
+              tokens, n_tokens, ws_rows, ws_s, nthreads, out, lse);
+}
+
+/* The same decode over the NVFP4 cache [NB, 64, 352] (reading R13): rows
+ * dequantized as stored, then the same attention. */
+void oracle_sparse_mla_decode_nvfp4(const uint16_t* q, const uint8_t* cache, const int32_t* indices,
+                                    const int32_t* block_table, const int32_t* req_id, double sm_scale, int T, int H,
+                                    int K, int R, int MB, int64_t NB, const int32_t* tokens, int n_tokens,
+                                    double* ws_rows, double* ws_s, int nthreads, double* out, double* lse) {
+  (void)T;
+  decode_rows(q, cache, NVFP4_ROW_BYTES, oracle_nvfp4_dequant_row, indices, block_table, req_id, sm_scale, H, K, R,
+              MB, NB, tokens, n_tokens, ws_rows, ws_s, nthreads, out, lse);
+}
+
+static void decode_rows(const uint16_t* q, const uint8_t* cache, int row_bytes,
+                        void (*dequant)(const uint8_t*, double*), const int32_t* indices,
+                        const int32_t* block_table, const int32_t* req_id, double sm_scale, int H, int K, int R,
+                        int MB, int64_t NB, const int32_t* tokens, int n_tokens, double* ws_rows, double* ws_s,
+                        int nthreads, double* out, double* lse) {
 #pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
   for (int i = 0; i < n_tokens; ++i) {
     int tid = 0;
@@ -237,7 +357,7 @@ void oracle_sparse_mla_decode(const uint16_t* q, const uint8_t* cache, const int
     for (int k = 0; k < K; ++k) {
       int32_t slot = oracle_translate_one(indices[(int64_t)t * K + k], req_id[t], block_table, R, MB, NB);
       if (slot < 0) continue;
-      oracle_dequant_row(cache + (int64_t)slot * ROW_BYTES, rows + (int64_t)n * D_QK);
+      dequant(cache + (int64_t)slot * row_bytes, rows + (int64_t)n * D_QK);
       ++n;
     }
     for (int h = 0; h < H; ++h) {

@@ -260,10 +260,11 @@ def prefill(seed: int = 3, R: int = 4, cached: int = 3072, new: int = 1024, K: i
     return PrefillCase(name=f"prefill_h{H}_k{K}_t{T}", H=H, K=K, sm_scale=D_QK ** -0.5, q=q, kv=kv, indices=indices)
 
 
-def make_cache(case: DecodeCase, quantize_store) -> np.ndarray:
-    """Allocate a zeroed [NB, 64, 656] cache and fill the pre-existing rows
-    with the given quantize-and-store implementation (rows, slots, cache)."""
-    cache = np.zeros((case.num_blocks, BLOCK, 656), np.uint8)
+def make_cache(case: DecodeCase, quantize_store, row_bytes: int = 656) -> np.ndarray:
+    """Allocate a zeroed [NB, 64, row_bytes] cache (656: FP8 rows, 352: NVFP4
+    rows) and fill the pre-existing rows with the given quantize-and-store
+    implementation (rows, slots, cache)."""
+    cache = np.zeros((case.num_blocks, BLOCK, row_bytes), np.uint8)
     if len(case.cache_slots):
         quantize_store(case.cache_rows, case.cache_slots, cache)
     return cache
