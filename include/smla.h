@@ -124,6 +124,39 @@ int sparse_mla_decode_fp8_noalloc(const void* q, const uint8_t* kv_cache, const 
                                   int num_splits, void* out, float* lse, int T, int H, int K, int R, int MB,
                                   int NB, void* stream);
 
+/* The NVFP4 cache (the nvfp4_ds_mla dtype of [vLLM PR #59342], "Purpose":
+ * 352 bytes per token).  The pages give the size, not the layout; this
+ * library's row is
+ *   bytes   0..255  the 512 NoPE values as OCP MX FP4 E2M1 codes, value 2i in the
+ *                   low nibble of byte i and 2i + 1 in the high nibble;
+ *   bytes 256..287  one E4M3 scale per block of 16 NoPE values (byte 256 + b for
+ *                   values 16b .. 16b + 15);
+ *   bytes 288..351  the 64 RoPE values as E4M3.
+ * A row dequantizes alone, exactly in bf16: NoPE c = e2m1(code c) * e4m3(scale
+ * c / 16), RoPE r = e4m3(byte 288 + r).  The cache is [NB, 64, 352] uint8,
+ * 16-byte aligned, paged through the same block tables as the FP8 cache. */
+
+/* Quantize-and-store into the NVFP4 cache: per block of 16, s = e4m3(amax / 6)
+ * and code = e2m1(x / s) (float32 divisions, nearest-even, saturating to 448
+ * and 6; a block whose scale is 0 stores code 0); RoPE = e4m3(x).  Arguments
+ * as for mla_cache_store_fp8 (a slot < 0 or >= NB * 64 skips the token). */
+int mla_cache_store_nvfp4(const void* kv_new, const int64_t* slot_mapping, uint8_t* kv_cache, int T, int NB,
+                          void* stream);
+
+/* Sparse MLA decode over the NVFP4 cache: the arguments, masking rules and
+ * results of sparse_mla_decode_fp8, kv_cache being [NB, 64, 352].  Each token's
+ * top-k rows are read as stored and dequantized exactly into bf16 rows of the
+ * workspace (T * K rows of 1152 bytes), over which the bf16 sparse attention
+ * runs; T * K must fit in int32.  No kernel of this call starts before the
+ * preceding work on `stream` has completed. */
+int sparse_mla_decode_nvfp4(const void* q, const uint8_t* kv_cache, const int32_t* indices,
+                            const int32_t* block_table, const int32_t* req_id_per_token, float sm_scale,
+                            int num_splits, void* out, float* lse, int T, int H, int K, int R, int MB, int NB,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace bytes sparse_mla_decode_nvfp4 needs on the current device. */
+size_t sparse_mla_decode_nvfp4_workspace_bytes(int T, int H, int K, int num_splits);
+
 /* Sparse MLA prefill over a dense bf16 latent buffer (flash_mla_sparse_prefill
  * as called by FlashMLASparseImpl._bf16_flash_mla_kernel in
  * [flashmla_sparse.py]; heads need no padding here).

@@ -28,7 +28,7 @@ _BUILD = os.path.join(_PKG, "_build")
 LIB_PATH = os.path.join(_PKG, "libsmla.so")
 HEADER = os.path.join(_ROOT, "include", "smla.h")
 
-SOURCES = ["smla_decode.cu", "smla_attn.cu", "smla_wide.cu", "smla_wide8.cu", "smla_store.cu", "smla_absorb.cu", "smla_api.cu"]
+SOURCES = ["smla_decode.cu", "smla_attn.cu", "smla_wide.cu", "smla_wide8.cu", "smla_store.cu", "smla_nvfp4.cu", "smla_absorb.cu", "smla_api.cu"]
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-std=c++17", "-lineinfo",
               "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall"]
 
@@ -97,6 +97,12 @@ def lib():
             L.sparse_mla_decode_fp8.restype = i32
             L.sparse_mla_decode_fp8_qfp8.argtypes = L.sparse_mla_decode_fp8.argtypes
             L.sparse_mla_decode_fp8_qfp8.restype = i32
+            L.sparse_mla_decode_nvfp4.argtypes = L.sparse_mla_decode_fp8.argtypes
+            L.sparse_mla_decode_nvfp4.restype = i32
+            L.sparse_mla_decode_nvfp4_workspace_bytes.argtypes = [i32, i32, i32, i32]
+            L.sparse_mla_decode_nvfp4_workspace_bytes.restype = sz
+            L.mla_cache_store_nvfp4.argtypes = [P, P, P, i32, i32, P]
+            L.mla_cache_store_nvfp4.restype = i32
             L.sparse_mla_decode_fp8_noalloc.argtypes = [P, P, P, P, P, f32, i32, P, P, i32, i32, i32, i32, i32, i32, P]
             L.sparse_mla_decode_fp8_noalloc.restype = i32
             L.sparse_mla_decode_workspace_bytes.argtypes = [i32, i32, i32, i32]
@@ -182,6 +188,10 @@ def decode_workspace_bytes(T: int, H: int, K: int, num_splits: int = 0) -> int:
     return int(lib().sparse_mla_decode_workspace_bytes(T, H, K, num_splits))
 
 
+def decode_nvfp4_workspace_bytes(T: int, H: int, K: int, num_splits: int = 0) -> int:
+    return int(lib().sparse_mla_decode_nvfp4_workspace_bytes(T, H, K, num_splits))
+
+
 def prefill_workspace_bytes(T: int, H: int, K: int, num_splits: int = 0) -> int:
     return int(lib().sparse_mla_prefill_workspace_bytes(T, H, K, num_splits))
 
@@ -213,8 +223,16 @@ def sparse_mla_decode_fp8_qfp8(q, kv_cache, indices, block_table, req_id_per_tok
                    num_splits, out, lse, workspace, stream)
 
 
+def sparse_mla_decode_nvfp4(q, kv_cache, indices, block_table, req_id_per_token, sm_scale: float,
+                            num_splits: int = 0, out=None, lse=None, workspace=None, stream=None):
+    """Sparse decode over the NVFP4 cache (kv_cache uint8 [NB,64,352]); the
+    other arguments and the results as for sparse_mla_decode_fp8."""
+    return _decode("sparse_mla_decode_nvfp4", q, kv_cache, indices, block_table, req_id_per_token, sm_scale,
+                   num_splits, out, lse, workspace, stream, row_bytes=352)
+
+
 def _decode(name, q, kv_cache, indices, block_table, req_id_per_token, sm_scale, num_splits, out, lse, workspace,
-            stream):
+            stream, row_bytes=656):
     import torch
     dev = _dev(q, kv_cache, indices, block_table, req_id_per_token, out, lse, workspace)
     T, H, D = q.shape
@@ -222,7 +240,7 @@ def _decode(name, q, kv_cache, indices, block_table, req_id_per_token, sm_scale,
     K = indices.shape[1]
     R, MB = block_table.shape
     _expect(q, torch.bfloat16, (T, H, 576), "q")
-    _expect(kv_cache, torch.uint8, (NB, 64, 656), "kv_cache")
+    _expect(kv_cache, torch.uint8, (NB, 64, row_bytes), "kv_cache")
     _expect(indices, torch.int32, (T, K), "indices")
     _expect(req_id_per_token, torch.int32, (T,), "req_id_per_token")
     if block_table.dtype != torch.int32:
@@ -446,6 +464,21 @@ def mla_cache_store_fp8(kv_new, slot_mapping, kv_cache, stream=None):
     _expect(kv_cache, torch.uint8, (NB, 64, 656), "kv_cache")
     rc = lib().mla_cache_store_fp8(_ptr(kv_new), _ptr(slot_mapping), _ptr(kv_cache), T, NB, _stream_ptr(stream, dev))
     _check(rc, "mla_cache_store_fp8")
+    return kv_cache
+
+
+def mla_cache_store_nvfp4(kv_new, slot_mapping, kv_cache, stream=None):
+    """Quantize bf16 [T,576] rows into the NVFP4 kv_cache uint8 [NB,64,352] at
+    slot_mapping int64 [T] (<0 skips).  Modifies kv_cache in place."""
+    import torch
+    dev = _dev(kv_new, slot_mapping, kv_cache)
+    T = kv_new.shape[0]
+    NB = kv_cache.shape[0]
+    _expect(kv_new, torch.bfloat16, (T, 576), "kv_new")
+    _expect(slot_mapping, torch.int64, (T,), "slot_mapping")
+    _expect(kv_cache, torch.uint8, (NB, 64, 352), "kv_cache")
+    rc = lib().mla_cache_store_nvfp4(_ptr(kv_new), _ptr(slot_mapping), _ptr(kv_cache), T, NB, _stream_ptr(stream, dev))
+    _check(rc, "mla_cache_store_nvfp4")
     return kv_cache
 
 

@@ -466,6 +466,79 @@ int mla_cache_store_fp8(const void* kv_new, const int64_t* slot_mapping, uint8_t
   return SMLA_OK;
 }
 
+int mla_cache_store_nvfp4(const void* kv_new, const int64_t* slot_mapping, uint8_t* kv_cache, int T, int NB,
+                          void* stream) {
+  if (T < 0 || NB <= 0) return fail(SMLA_ERR_INVALID_ARG, "bad sizes T=%d NB=%d", T, NB);
+  if (T == 0) return SMLA_OK;
+  if (!kv_new || !slot_mapping || !kv_cache) return fail(SMLA_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned16(kv_new) || !aligned16(kv_cache))
+    return fail(SMLA_ERR_INVALID_ARG, "kv_new and kv_cache must be 16-byte aligned");
+  cudaError_t e = smla::launch_nvfp4_store(kv_new, slot_mapping, kv_cache, T, NB, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "mla_cache_store_nvfp4 launch");
+  return SMLA_OK;
+}
+
+size_t sparse_mla_decode_nvfp4_workspace_bytes(int T, int H, int K, int num_splits) {
+  if (T <= 0 || K < 0 || (int64_t)T * K > INT32_MAX) return 0;
+  const size_t attn = workspace_bytes_for(false, T, H, K, num_splits);
+  if (attn == 0) return 0;
+  return ((attn + 255) / 256) * 256 + smla::nvfp4_stage_bytes(T, K);
+}
+
+int sparse_mla_decode_nvfp4(const void* q, const uint8_t* kv_cache, const int32_t* indices,
+                            const int32_t* block_table, const int32_t* req_id_per_token, float sm_scale,
+                            int num_splits, void* out, float* lse, int T, int H, int K, int R, int MB, int NB,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+  if (T < 0 || K < 0 || R <= 0 || MB <= 0 || NB <= 0 || num_splits < 0)
+    return fail(SMLA_ERR_INVALID_ARG, "bad sizes T=%d K=%d R=%d MB=%d NB=%d num_splits=%d", T, K, R, MB, NB,
+                num_splits);
+  int rc = check_heads(H);
+  if (rc != SMLA_OK) return rc;
+  if (T == 0) return SMLA_OK;
+  if (!q || !kv_cache || (!indices && K > 0) || !block_table || !req_id_per_token || !out || !lse)
+    return fail(SMLA_ERR_INVALID_ARG, "null pointer argument");
+  if (!aligned16(q) || !aligned16(kv_cache) || !aligned16(out))
+    return fail(SMLA_ERR_INVALID_ARG, "q, kv_cache and out must be 16-byte aligned");
+  if ((int64_t)NB * 64 > INT32_MAX) return fail(SMLA_ERR_UNSUPPORTED, "NB*64 must fit in int32");
+  if ((int64_t)T * K > INT32_MAX) return fail(SMLA_ERR_UNSUPPORTED, "T*K must fit in int32");
+  int sms = 0;
+  rc = num_sms(&sms);
+  if (rc != SMLA_OK) return rc;
+  // the bf16 attention's own workspace (its status word leads), then the staged rows
+  const smla::AttnPlan plan = smla::plan_attention(false, T, H, K, num_splits, sms);
+  const size_t attn_bytes = ((plan.ws_bytes + 255) / 256) * 256;
+  const size_t need = attn_bytes + smla::nvfp4_stage_bytes(T, K);
+  if (workspace) {
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+      return fail(SMLA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    if (workspace_bytes < need) return fail(SMLA_ERR_WORKSPACE, "workspace has %zu bytes, %zu needed", workspace_bytes, need);
+  } else {
+    rc = cached_workspace(need, &workspace);
+    if (rc != SMLA_OK) return rc;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* stage = static_cast<uint8_t*>(workspace) + attn_bytes;
+  cudaError_t e = smla::launch_nvfp4_stage(kv_cache, NB, indices, block_table, req_id_per_token, T, K, R, MB, stage, s);
+  if (e != cudaSuccess) return cuda_fail(e, "sparse_mla_decode_nvfp4 staging launch");
+  const int64_t n = (int64_t)T * K;
+  smla::AttnArgs a{};
+  a.q = q;
+  a.cache = nullptr;
+  a.kv = stage + ((n * 4 + 255) / 256) * 256;
+  a.indices = reinterpret_cast<const int32_t*>(stage);
+  a.out = out;
+  a.lse = lse;
+  a.sm_scale = sm_scale;
+  a.T = T;
+  a.H = H;
+  a.K = K;
+  a.NB = n > 0 ? n : 1;  // rows of the staged buffer
+  a.workspace = workspace;
+  e = smla::launch_attention(false, a, plan, s);
+  if (e != cudaSuccess) return cuda_fail(e, "sparse_mla_decode_nvfp4 launch");
+  return SMLA_OK;
+}
+
 int sparse_mla_translate_indices(const int32_t* indices, const int32_t* block_table,
                                  const int32_t* req_id_per_token, int32_t* slots_out, int T, int K, int R,
                                  int MB, int NB, void* stream) {

@@ -83,6 +83,15 @@ AttnPlan plan_decode_wide8(int T, int K, int num_splits, int num_sms);
 cudaError_t launch_decode_wide8(const AttnArgs& a, const AttnPlan& plan, cudaStream_t stream);
 cudaError_t launch_prefill_bf16(const AttnArgs& a, const AttnPlan& plan, cudaStream_t stream);
 
+// The NVFP4 cache (smla_nvfp4.cu): quantize-and-store, and the decode's
+// staging of each token's top-k rows as exact bf16 rows ([T * K] row indices,
+// -1 = invalid, then [T * K, 576] bf16 rows; nvfp4_stage_bytes in all).
+cudaError_t launch_nvfp4_store(const void* kv_new, const int64_t* slot_mapping, uint8_t* cache, int T, int64_t NB,
+                               cudaStream_t stream);
+size_t nvfp4_stage_bytes(int T, int K);
+cudaError_t launch_nvfp4_stage(const uint8_t* cache, int64_t NB, const int32_t* indices, const int32_t* block_table,
+                               const int32_t* req_id, int T, int K, int R, int MB, void* stage, cudaStream_t stream);
+
 // Offsets inside the workspace.
 constexpr size_t kWsStatusBytes = 256;
 
