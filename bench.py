@@ -178,14 +178,15 @@ def max_over_ranks(x: float, world: int, device=None) -> float:
     return float(t.item())
 
 
-def decode_algorithmic_bytes(case: inp.RotatingDecode, index_set: np.ndarray) -> int:
+def decode_algorithmic_bytes(case: inp.RotatingDecode, index_set: np.ndarray, row_bytes: int = 656) -> int:
     """Bytes one decode launch must move at minimum: every valid gathered row
-    once per query token (656 B), q, out, lse, the index row, the request id
-    and the used part of the request's block-table row."""
+    once per query token (656 B, or 352 B for the NVFP4 cache), q, out, lse,
+    the index row, the request id and the used part of the request's
+    block-table row."""
     T, H = case.q.shape[0], case.H
     rows = int((index_set >= 0).sum())
     used_blocks = int(((case.ctx_lens + 63) // 64).sum())  # block-table entries read (one request per token)
-    return (rows * 656 + T * H * 576 * 2 + T * H * 512 * 2 + T * H * 4 + index_set.size * 4 + T * 4
+    return (rows * row_bytes + T * H * 576 * 2 + T * H * 512 * 2 + T * H * 4 + index_set.size * 4 + T * 4
             + used_blocks * 4)
 
 
@@ -195,9 +196,11 @@ def decode_flops(case, index_set) -> int:
 
 # ---------------------------------------------------------------- CPU oracle sample
 
-def host_sample_cache(case: inp.RotatingDecode, index_set: np.ndarray, tokens: np.ndarray, seed: int):
+def host_sample_cache(case: inp.RotatingDecode, index_set: np.ndarray, tokens: np.ndarray, seed: int,
+                      nvfp4: bool = False):
     """Host cache holding every row the sampled tokens reference, quantized by
-    the oracle from host-drawn latent rows of the same distribution."""
+    the oracle (FP8 rows, or NVFP4 rows) from host-drawn latent rows of the
+    same distribution."""
     import oracle
     slots = oracle.translate(index_set[tokens], case.block_table, case.req_id_per_token[tokens], case.num_blocks)
     need = np.unique(slots[slots >= 0]).astype(np.int64)
@@ -205,8 +208,8 @@ def host_sample_cache(case: inp.RotatingDecode, index_set: np.ndarray, tokens: n
     x = rng.standard_normal((len(need), 576), dtype=np.float32)
     if len(case.outlier_channels):
         x[:, case.outlier_channels] *= 8.0
-    cache = np.zeros((case.num_blocks, 64, 656), np.uint8)
-    oracle.quantize_store(inp.bf16_bits(x), need, cache)
+    cache = np.zeros((case.num_blocks, 64, 352 if nvfp4 else 656), np.uint8)
+    (oracle.nvfp4_quantize_store if nvfp4 else oracle.quantize_store)(inp.bf16_bits(x), need, cache)
     return cache
 
 
@@ -549,6 +552,42 @@ def tensor_workload(args, quiet=False):
         def oracle_run():
             oracle.sparse_mla_decode(case.q, hcache, case.index_sets[0], case.block_table, case.req_id_per_token,
                                      case.sm_scale, tokens=tok, nthreads=nth)
+    elif args.workload == "decode_nvfp4_h16_k2048":
+        # the memory-bound decode's workload over the NVFP4 cache (352-byte rows, read as stored)
+        case = inp.rotating_decode(seed=1)
+        T, H, K, NB = case.q.shape[0], case.H, case.K, case.num_blocks
+        with torch.cuda.stream(stream):
+            cache = torch.zeros((NB, 64, 352), dtype=torch.uint8, device=device)
+            lat = inp.device_latent(len(case.ctx_slots), case.latent_seed, case.outlier_channels, device)
+            smla.mla_cache_store_nvfp4(lat, torch.from_numpy(case.ctx_slots).to(device), cache, stream=stream)
+            q = bf16(case.q)
+            idx_sets = [torch.from_numpy(x).to(device) for x in case.index_sets]
+            bt = torch.from_numpy(case.block_table).to(device)
+            req = torch.from_numpy(case.req_id_per_token).to(device)
+            ws = torch.zeros(smla.decode_nvfp4_workspace_bytes(T, H, K, 0), dtype=torch.uint8, device=device)
+            out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=device)
+            lse = torch.empty((T, H), dtype=torch.float32, device=device)
+        stream.synchronize()
+        del lat
+
+        def launch(i):
+            smla.sparse_mla_decode_nvfp4(q, cache, idx_sets[i % len(idx_sets)], bt, req, case.sm_scale, 0, out, lse,
+                                         ws, stream=stream)
+        n_graphs = len(idx_sets)
+        flops = statistics.mean(decode_flops(case, x) for x in case.index_sets)
+        algo_bytes = statistics.mean(decode_algorithmic_bytes(case, x, 352) for x in case.index_sets)
+        fp8 = False
+        mma_dtype = "bf16"
+        launches = smla.attention_plan(False, T, H, K, 0)[0]
+        desc = (f"{case.name}: NVFP4 sparse decode, {T} requests x 1 token, H={H}, top-k {K}, context "
+                f"U[8192,32768], 352-byte NVFP4 cache ({NB} blocks, {NB * 64 * 352 / 1e9:.2f} GB), "
+                f"{n_graphs} rotating index sets")
+        tok = np.arange(min(nth, 16), dtype=np.int32)
+        hcache = host_sample_cache(case, case.index_sets[0], tok, seed=778, nvfp4=True)
+
+        def oracle_run():
+            oracle.sparse_mla_decode_nvfp4(case.q, hcache, case.index_sets[0], case.block_table,
+                                           case.req_id_per_token, case.sm_scale, tokens=tok, nthreads=nth)
     elif args.workload == "mla_absorb_h128":
         # the weight absorption around the attention at the prefill workload's shape: 4096 tokens, H = 128,
         # q_nope 128 -> 512 (with q_pe appended) and 512 -> V = 128, synthetic weights
@@ -740,12 +779,18 @@ def tensor_workload(args, quiet=False):
     if algo_bytes is not None:
         gbs = algo_bytes / (ms * 1e-3) / 1e9
         line["metric"] = f"{args.workload} query-tokens/s + GB/s vs HBM roofline"
-        line["config"]["step"] = "the query-side and value-side GEMM launches"
-        line["config"]["l2"] = "inputs (1.5 GB per step) larger than L2"
+        if args.workload == "decode_nvfp4_h16_k2048":
+            line["dtype"] = "e2m1"
+            line["config"]["step"] = "one sparse decode launch over the NVFP4 cache (rows dequantized in the kernel)"
+            line["config"]["l2"] = "8 rotating top-k index sets (8 x 46 MB gathered) > 129 MB L2"
+            kernel = "sparse_mla_attn_kernel<16, NVFP4 rows>"
+        else:
+            line["config"]["step"] = "the query-side and value-side GEMM launches"
+            line["config"]["l2"] = "inputs (1.5 GB per step) larger than L2"
+            kernel = "head_gemm_kernel (two launches per step)"
         line["roofline"] = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                             "frac": gbs / peaks["hbm_gbs"], "traffic": None, "peak_source": peaks["source"],
-                            "kernel": "head_gemm_kernel (two launches per step)", "bytes_per_step": algo_bytes,
-                            "avg_step_us": ms * 1e3}
+                            "kernel": kernel, "bytes_per_step": algo_bytes, "avg_step_us": ms * 1e3}
     return line
 
 
@@ -921,7 +966,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-extra", action="store_true",
                     help="leave the tensor-bound configurations out of the default line")
-    ap.add_argument("--workload", choices=["decode_h16_k2048", "decode_h128_k2048", "prefill_h128_k2048",
+    ap.add_argument("--workload", choices=["decode_h16_k2048", "decode_h128_k2048", "decode_nvfp4_h16_k2048", "prefill_h128_k2048",
                                            "prefill_fp8_h128_k2048", "mla_absorb_h128"],
                     default="decode_h16_k2048",
                     help="decode_h16_k2048 (default) is the headline; the other two are the tensor-bound "

@@ -144,11 +144,13 @@ int mla_cache_store_nvfp4(const void* kv_new, const int64_t* slot_mapping, uint8
                           void* stream);
 
 /* Sparse MLA decode over the NVFP4 cache: the arguments, masking rules and
- * results of sparse_mla_decode_fp8, kv_cache being [NB, 64, 352].  Each token's
- * top-k rows are read as stored and dequantized exactly into bf16 rows of the
- * workspace (T * K rows of 1152 bytes), over which the bf16 sparse attention
- * runs; T * K must fit in int32.  No kernel of this call starts before the
- * preceding work on `stream` has completed. */
+ * results of sparse_mla_decode_fp8, kv_cache being [NB, 64, 352]; T * K must
+ * fit in int32.  The rows are read as stored and dequantized exactly into
+ * bf16: for H < 128 inside the attention kernel (the workspace holds only its
+ * status word and split partials); for H = 128 into bf16 rows of the
+ * workspace (T * K rows of 1152 bytes), over which the 128-head bf16 kernel
+ * runs.  No kernel of this call starts before the preceding work on `stream`
+ * has completed. */
 int sparse_mla_decode_nvfp4(const void* q, const uint8_t* kv_cache, const int32_t* indices,
                             const int32_t* block_table, const int32_t* req_id_per_token, float sm_scale,
                             int num_splits, void* out, float* lse, int T, int H, int K, int R, int MB, int NB,

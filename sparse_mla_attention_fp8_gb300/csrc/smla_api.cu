@@ -482,6 +482,7 @@ size_t sparse_mla_decode_nvfp4_workspace_bytes(int T, int H, int K, int num_spli
   if (T <= 0 || K < 0 || (int64_t)T * K > INT32_MAX) return 0;
   const size_t attn = workspace_bytes_for(false, T, H, K, num_splits);
   if (attn == 0) return 0;
+  if (smla::nvfp4_native_supported(H)) return attn;
   return ((attn + 255) / 256) * 256 + smla::nvfp4_stage_bytes(T, K);
 }
 
@@ -504,10 +505,12 @@ int sparse_mla_decode_nvfp4(const void* q, const uint8_t* kv_cache, const int32_
   int sms = 0;
   rc = num_sms(&sms);
   if (rc != SMLA_OK) return rc;
-  // the bf16 attention's own workspace (its status word leads), then the staged rows
+  // the bf16 attention's own workspace (its status word leads), then, at 128
+  // heads, the staged rows
   const smla::AttnPlan plan = smla::plan_attention(false, T, H, K, num_splits, sms);
+  const bool native = smla::nvfp4_native_supported(H);
   const size_t attn_bytes = ((plan.ws_bytes + 255) / 256) * 256;
-  const size_t need = attn_bytes + smla::nvfp4_stage_bytes(T, K);
+  const size_t need = native ? plan.ws_bytes : attn_bytes + smla::nvfp4_stage_bytes(T, K);
   if (workspace) {
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
       return fail(SMLA_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
@@ -517,6 +520,28 @@ int sparse_mla_decode_nvfp4(const void* q, const uint8_t* kv_cache, const int32_
     if (rc != SMLA_OK) return rc;
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (native) {
+    // the rows are read as stored and dequantized inside the attention kernel
+    smla::AttnArgs a{};
+    a.q = q;
+    a.cache = kv_cache;
+    a.indices = indices;
+    a.block_table = block_table;
+    a.req_id = req_id_per_token;
+    a.out = out;
+    a.lse = lse;
+    a.sm_scale = sm_scale;
+    a.T = T;
+    a.H = H;
+    a.K = K;
+    a.R = R;
+    a.MB = MB;
+    a.NB = NB;
+    a.workspace = workspace;
+    cudaError_t e = smla::launch_decode_nvfp4(a, plan, s);
+    if (e != cudaSuccess) return cuda_fail(e, "sparse_mla_decode_nvfp4 launch");
+    return SMLA_OK;
+  }
   uint8_t* stage = static_cast<uint8_t*>(workspace) + attn_bytes;
   cudaError_t e = smla::launch_nvfp4_stage(kv_cache, NB, indices, block_table, req_id_per_token, T, K, R, MB, stage, s);
   if (e != cudaSuccess) return cuda_fail(e, "sparse_mla_decode_nvfp4 staging launch");

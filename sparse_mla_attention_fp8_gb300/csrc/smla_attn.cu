@@ -1,5 +1,7 @@
 // BF16 sparse MLA prefill on sm_103a for head counts other than 128 (heads in
-// groups of 16 or 32), over a dense [N, 576] bf16 latent buffer.
+// groups of 16 or 32), over a dense [N, 576] bf16 latent buffer; the same
+// kernel decodes over the NVFP4 paged cache (kNv: rows dequantized exactly
+// into the bf16 operand tiles by the converter warps).
 //
 // What is computed (vLLM flashmla_sparse.py, FlashMLASparseImpl.forward on
 // the prefill path, flash_mla_sparse_prefill): every query token t attends
@@ -92,6 +94,11 @@ struct Params {
   const __nv_bfloat16* q;
   const __nv_bfloat16* kv;
   const int32_t* indices;
+  // NVFP4 rows (kNv): the [NB, 64, 352] cache and its paging; N = NB
+  const uint8_t* cache;
+  const int32_t* block_table;
+  const int32_t* req_id;
+  int R, MB;
   __nv_bfloat16* out;
   float* lse;
   float* part_o;
@@ -178,7 +185,53 @@ __device__ __forceinline__ float warp_reduce16(float (&v)[16], int lane) {
   return v[0];
 }
 
-template <int HG>
+// Two E2M1 codes (one byte, low nibble first) -> an f16 pair (exact).
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
+  uint32_t h2;
+  asm("{\n .reg .b8 c, z;\n mov.b16 {c, z}, %1;\n cvt.rn.f16x2.e2m1x2 %0, c;\n}"
+      : "=r"(h2)
+      : "h"((uint16_t)(byte & 0xFFu)));
+  return h2;
+}
+// An f16 pair -> a bf16 pair (exact for the values used here: at most 6
+// significant bits, normal in both formats or zero).
+__device__ __forceinline__ uint32_t f16x2_to_bf16x2(uint32_t h2) {
+  return pack_bf16x2(__half2float(__ushort_as_half((uint16_t)(h2 & 0xFFFFu))),
+                     __half2float(__ushort_as_half((uint16_t)(h2 >> 16))));
+}
+// Eight NVFP4 NoPE values (four code bytes) times their block scale (an E4M3
+// byte) -> one 16-byte chunk of bf16 values, exactly: code * scale has at most
+// 6 significant bits and lies in [2^-10, 2688] or is 0, so the f16 product and
+// its bf16 copy are exact.
+__device__ __forceinline__ uint4 nvfp4_chunk(uint32_t codes, uint32_t scale_byte) {
+  uint32_t sc2;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(sc2) : "h"((uint16_t)(scale_byte * 0x0101u)));
+  uint32_t o[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    uint32_t v;
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(v) : "r"(e2m1x2_to_f16x2(codes >> (8 * k))), "r"(sc2));
+    o[k] = f16x2_to_bf16x2(v);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+// Eight E4M3 RoPE values (two words) -> one 16-byte chunk of bf16 values (exact).
+__device__ __forceinline__ uint4 e4m3x8_chunk(uint32_t w0, uint32_t w1) {
+  const uint32_t w[2] = {w0, w1};
+  uint32_t o[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)(w[k >> 1] >> (16 * (k & 1)))));
+    o[k] = f16x2_to_bf16x2(h2);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// kNv: the rows are NVFP4 cache rows (352 bytes, paged through the block
+// table) instead of bf16 latent rows; they are dequantized exactly into the
+// same bf16 operand tiles.
+template <int HG, bool kNv>
 __global__ void __launch_bounds__(Cfg<HG>::kThreads, 1) sparse_mla_attn_kernel(const __grid_constant__ Params p) {
   using C = Cfg<HG>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -243,7 +296,10 @@ __global__ void __launch_bounds__(Cfg<HG>::kThreads, 1) sparse_mla_attn_kernel(c
         int32_t s = -1;
         if (k < p.K) {
           const int32_t idx = __ldg(p.indices + (int64_t)ti.t * p.K + k);
-          s = (idx >= 0 && (int64_t)idx < p.N) ? idx : -1;
+          if constexpr (kNv)
+            s = translate_slot(idx, __ldg(p.req_id + ti.t), p.block_table, p.R, p.MB, p.N);
+          else
+            s = (idx >= 0 && (int64_t)idx < p.N) ? idx : -1;
         }
         slots[r] = s;
       }
@@ -289,10 +345,25 @@ __global__ void __launch_bounds__(Cfg<HG>::kThreads, 1) sparse_mla_attn_kernel(c
       }
       rb.slot = slot;
       if (slot >= 0) {
-        const uint8_t* row = reinterpret_cast<const uint8_t*>(p.kv + (int64_t)slot * kDqk);
-        rb.a = ld_stream(row + 16 * lane);
-        rb.b = ld_stream(row + 16 * (lane + 32));
-        if (lane < 8) rb.c = ld_stream(row + 16 * (lane + 64));
+        if constexpr (kNv) {
+          // lane l: the codes of output chunks l and l + 32 (bytes 4 l and 128 + 4 l),
+          // their block scales (bytes 256 + l / 2 and 272 + l / 2) and, for l < 8,
+          // RoPE bytes 288 + 8 l .. + 7
+          const uint8_t* row = p.cache + (int64_t)slot * 352;
+          rb.a.x = __ldg(reinterpret_cast<const uint32_t*>(row) + lane);
+          rb.a.y = __ldg(reinterpret_cast<const uint32_t*>(row + 128) + lane);
+          rb.a.z = (uint32_t)__ldg(row + 256 + (lane >> 1)) | ((uint32_t)__ldg(row + 272 + (lane >> 1)) << 8);
+          if (lane < 8) {
+            const uint2 rr = __ldg(reinterpret_cast<const uint2*>(row + 288) + lane);
+            rb.b.x = rr.x;
+            rb.b.y = rr.y;
+          }
+        } else {
+          const uint8_t* row = reinterpret_cast<const uint8_t*>(p.kv + (int64_t)slot * kDqk);
+          rb.a = ld_stream(row + 16 * lane);
+          rb.b = ld_stream(row + 16 * (lane + 32));
+          if (lane < 8) rb.c = ld_stream(row + 16 * (lane + 64));
+        }
       }
     };
 
@@ -305,9 +376,15 @@ __global__ void __launch_bounds__(Cfg<HG>::kThreads, 1) sparse_mla_attn_kernel(c
       const uint32_t tile = smem_u32(smem + C::kOffKv + b * C::kKvTile);
       const bool v = rb.slot >= 0;
       const uint4 z = make_uint4(0, 0, 0, 0);
-      sts128(tile + sw128_chunk(C::kRows, r, lane), v ? rb.a : z);
-      sts128(tile + sw128_chunk(C::kRows, r, lane + 32), v ? rb.b : z);
-      if (lane < 8) sts128(tile + sw128_chunk(C::kRows, r, lane + 64), v ? rb.c : z);
+      if constexpr (kNv) {
+        sts128(tile + sw128_chunk(C::kRows, r, lane), v ? nvfp4_chunk(rb.a.x, rb.a.z & 0xFFu) : z);
+        sts128(tile + sw128_chunk(C::kRows, r, lane + 32), v ? nvfp4_chunk(rb.a.y, (rb.a.z >> 8) & 0xFFu) : z);
+        if (lane < 8) sts128(tile + sw128_chunk(C::kRows, r, lane + 64), v ? e4m3x8_chunk(rb.b.x, rb.b.y) : z);
+      } else {
+        sts128(tile + sw128_chunk(C::kRows, r, lane), v ? rb.a : z);
+        sts128(tile + sw128_chunk(C::kRows, r, lane + 32), v ? rb.b : z);
+        if (lane < 8) sts128(tile + sw128_chunk(C::kRows, r, lane + 64), v ? rb.c : z);
+      }
       if (lane == 0) valid[b * C::kRows + r] = v ? 1 : 0;
       if (k == RW - 1) {
         fence_proxy_async_smem();
@@ -597,22 +674,22 @@ __global__ void __launch_bounds__(Cfg<HG>::kThreads, 1) sparse_mla_attn_kernel(c
   }
 }
 
-// Per device and head-group size: the kernel's dynamic shared memory limit
-// has been raised (once, thread-safely).
-std::once_flag g_attr_once[2][64];
-cudaError_t g_attr_err[2][64];
+// Per device, head-group size and row format: the kernel's dynamic shared
+// memory limit has been raised (once, thread-safely).
+std::once_flag g_attr_once[4][64];
+cudaError_t g_attr_err[4][64];
 
-template <int HG>
+template <int HG, bool kNv>
 cudaError_t launch_impl(const AttnArgs& a, const AttnPlan& plan, cudaStream_t stream) {
   using C = Cfg<HG>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  const int hi = HG == 16 ? 0 : 1;
+  const int hi = (HG == 16 ? 0 : 1) + (kNv ? 2 : 0);
   std::call_once(g_attr_once[hi][dev], [hi, dev] {
-    g_attr_err[hi][dev] = cudaFuncSetAttribute(sparse_mla_attn_kernel<HG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               C::kSmemAlloc);
+    g_attr_err[hi][dev] = cudaFuncSetAttribute(sparse_mla_attn_kernel<HG, kNv>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemAlloc);
   });
   if (g_attr_err[hi][dev] != cudaSuccess) return g_attr_err[hi][dev];
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
@@ -621,6 +698,11 @@ cudaError_t launch_impl(const AttnArgs& a, const AttnPlan& plan, cudaStream_t st
   p.q = static_cast<const __nv_bfloat16*>(a.q);
   p.kv = static_cast<const __nv_bfloat16*>(a.kv);
   p.indices = a.indices;
+  p.cache = a.cache;
+  p.block_table = a.block_table;
+  p.req_id = a.req_id;
+  p.R = a.R;
+  p.MB = a.MB;
   p.out = static_cast<__nv_bfloat16*>(a.out);
   p.lse = a.lse;
   p.status = reinterpret_cast<int*>(ws);
@@ -635,7 +717,7 @@ cudaError_t launch_impl(const AttnArgs& a, const AttnPlan& plan, cudaStream_t st
   p.nt = plan.nt;
   p.total = plan.total;
   p.G = plan.G;
-  sparse_mla_attn_kernel<HG><<<plan.G, C::kThreads, C::kSmemAlloc, stream>>>(p);
+  sparse_mla_attn_kernel<HG, kNv><<<plan.G, C::kThreads, C::kSmemAlloc, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess || !plan.need_combine) return e;
   e = launch_combine<HG>(p.part_o, p.part_lse, p.out, p.lse, p.H, p.n_hg, p.nt, p.total, p.G, plan.units, stream);
@@ -666,7 +748,14 @@ AttnPlan plan_prefill_bf16(int T, int H, int K, int num_splits, int num_sms) {
 
 cudaError_t launch_prefill_bf16(const AttnArgs& a, const AttnPlan& plan, cudaStream_t stream) {
   if (plan.HG == 128) return launch_prefill_wide(a, plan, stream);
-  return plan.HG == 16 ? launch_impl<16>(a, plan, stream) : launch_impl<32>(a, plan, stream);
+  return plan.HG == 16 ? launch_impl<16, false>(a, plan, stream) : launch_impl<32, false>(a, plan, stream);
+}
+
+bool nvfp4_native_supported(int H) { return !wide_supported(H); }
+
+cudaError_t launch_decode_nvfp4(const AttnArgs& a, const AttnPlan& plan, cudaStream_t stream) {
+  if (plan.HG != 16 && plan.HG != 32) return cudaErrorInvalidValue;
+  return plan.HG == 16 ? launch_impl<16, true>(a, plan, stream) : launch_impl<32, true>(a, plan, stream);
 }
 
 AttnPlan plan_attention(bool fp8, int T, int H, int K, int num_splits, int num_sms) {

@@ -6,17 +6,19 @@
 //   bytes 256..287  one E4M3 scale per block of 16 NoPE values;
 //   bytes 288..351  the 64 RoPE values as E4M3.
 // A row dequantizes alone: value c = e2m1(code c) * e4m3(scale c / 16), RoPE
-// r = e4m3(byte 288 + r).  Every such value has at most 5 significant bits
-// and lies in [2^-10, 2688] or is 0, so it is exact in bf16.
+// r = e4m3(byte 288 + r).  Every such value has at most 6 significant bits (2
+// of the code times 4 of the scale) and lies in [2^-10, 2688] or is 0, so it
+// is exact in f16 and in bf16.
 //
 // Quantize-and-store: per block, s = e4m3(amax / 6) and code = e2m1(x / s),
 // float32 divisions, nearest-even with saturation on both grids (a block whose
 // scale is 0 stores code 0); RoPE = e4m3(x).
 //
-// Decode reads the rows it attends to as stored and dequantizes them exactly:
-// a staging kernel writes each token's top-k rows as bf16 rows of a workspace
-// (translated through the block table as for the FP8 cache), and the bf16
-// sparse attention kernels run over them.
+// Decode reads the rows it attends to as stored and dequantizes them exactly.
+// Below 128 heads the attention kernel's converter warps do it (smla_attn.cu).
+// At 128 heads a staging kernel (here) writes each token's top-k rows as bf16
+// rows of a workspace, translated through the block table as for the FP8
+// cache, and the 128-head bf16 kernel runs over them.
 #include <cstdint>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
