@@ -418,7 +418,8 @@ def run_ours(args):
         del cache
         torch.cuda.empty_cache()
         for name, k in (("decode_h128_k2048", max(20, args.steps // 20)), ("prefill_h128_k2048", max(5, args.steps // 200)),
-                        ("prefill_fp8_h128_k2048", max(5, args.steps // 200)), ("mla_absorb_h128", max(20, args.steps // 20))):
+                        ("prefill_fp8_h128_k2048", max(5, args.steps // 200)), ("mla_absorb_h128", max(20, args.steps // 20)),
+                        ("decode_nvfp4_h16_k2048", max(20, args.steps // 20))):
             sub = argparse.Namespace(**vars(args))
             sub.workload, sub.steps = name, k
             sub.no_cpu_baseline = True
@@ -969,8 +970,8 @@ def main():
     ap.add_argument("--workload", choices=["decode_h16_k2048", "decode_h128_k2048", "decode_nvfp4_h16_k2048", "prefill_h128_k2048",
                                            "prefill_fp8_h128_k2048", "mla_absorb_h128"],
                     default="decode_h16_k2048",
-                    help="decode_h16_k2048 (default) is the headline; the other two are the tensor-bound "
-                         "configurations, reported on their own line")
+                    help="decode_h16_k2048 (default) is the headline; each other workload is reported on its own "
+                         "line (and inside the default line, unless --no-extra)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -185,6 +185,23 @@ __device__ __forceinline__ float warp_reduce16(float (&v)[16], int lane) {
   return v[0];
 }
 
+// Optional per-tile timeline for performance work: with SMLA_TRACE defined,
+// roles record clock64() at their hand-off points into g_smla_trace_attn (set
+// by the host through smla_trace_set_attn).  Compiled out otherwise.
+#ifdef SMLA_TRACE
+__device__ long long* g_smla_trace_attn = nullptr;
+constexpr int kTraceTiles = 64, kTraceEvents = 14;
+#define ATTN_TRACE(tl, ev)                                                                                   \
+  do {                                                                                                       \
+    if (g_smla_trace_attn && (tl) < kTraceTiles)                                                           \
+      g_smla_trace_attn[((size_t)blockIdx.x * kTraceTiles + (tl)) * kTraceEvents + (ev)] = clock64();      \
+  } while (0)
+#else
+#define ATTN_TRACE(tl, ev) ((void)0)
+#endif
+enum { kAEvIdx = 0, kAEvConvIssue, kAEvConvFull, kAEvQk, kAEvSoftStart, kAEvSoftBar, kAEvPFull, kAEvPv, kAEvEpiEnd,
+       kAEvEnter, kAEvExit, kAEvPvWait, kAEvConvStart, kAEvConvHalf };
+
 // Two E2M1 codes (one byte, low nibble first) -> an f16 pair (exact).
 __device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
   uint32_t h2;
@@ -251,6 +268,7 @@ __global__ void __launch_bounds__(Cfg<HG>::kThreads, 1) sparse_mla_attn_kernel(c
   const int64_t xbeg = tile_begin(blockIdx.x, p.total, p.G);
   const int64_t xend = tile_begin(blockIdx.x + 1, p.total, p.G);
   const int n_local = (int)(xend - xbeg);
+  if (tid == 0) ATTN_TRACE(0, kAEvEnter);
 
   if (tid == 0) {
     for (int i = 0; i < 2; ++i) {
@@ -304,6 +322,7 @@ __global__ void __launch_bounds__(Cfg<HG>::kThreads, 1) sparse_mla_attn_kernel(c
         slots[r] = s;
       }
       mbar_arrive(&bars[C::kBarIdxFull + b4]);
+      if (lane == 0) ATTN_TRACE(tl, kAEvIdx);
       if (ti.seg_start) {
         const int qb = seg % C::kQBufs;
         if (seg >= C::kQBufs && !SMLA_WAIT(C::kBarQEmpty + qb, ((seg / C::kQBufs) - 1) & 1)) break;
@@ -338,6 +357,7 @@ __global__ void __launch_bounds__(Cfg<HG>::kThreads, 1) sparse_mla_attn_kernel(c
       const int b4 = tl & 3;
       if (k == 0) ok = ok && SMLA_WAIT(C::kBarIdxFull + b4, (tl >> 2) & 1);
       if (!ok) return;
+      if (k == 0 && cw == 0 && lane == 0) ATTN_TRACE(tl, kAEvConvIssue);
       const int32_t slot = slots_ring[b4 * C::kRows + r];
       if (k == RW - 1) {
         __syncwarp();
@@ -373,6 +393,8 @@ __global__ void __launch_bounds__(Cfg<HG>::kThreads, 1) sparse_mla_attn_kernel(c
       const int b = tl & 1;
       if (k == 0 && tl >= 2) ok = ok && SMLA_WAIT(C::kBarKvEmpty + b, ((tl >> 1) + 1) & 1);
       if (!ok) return;
+      if (k == 0 && cw == 0 && lane == 0) ATTN_TRACE(tl, kAEvConvStart);
+      if (k == 3 && cw == 0 && lane == 0) ATTN_TRACE(tl, kAEvConvHalf);
       const uint32_t tile = smem_u32(smem + C::kOffKv + b * C::kKvTile);
       const bool v = rb.slot >= 0;
       const uint4 z = make_uint4(0, 0, 0, 0);
@@ -390,6 +412,7 @@ __global__ void __launch_bounds__(Cfg<HG>::kThreads, 1) sparse_mla_attn_kernel(c
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[C::kBarKvFull + b]);
+        if (cw == 0 && lane == 0) ATTN_TRACE(tl, kAEvConvFull);
       }
     };
 
@@ -446,6 +469,7 @@ __global__ void __launch_bounds__(Cfg<HG>::kThreads, 1) sparse_mla_attn_kernel(c
               mma_ss(sbuf, da, db, idesc_qk, s == 0 ? 0u : 1u);
             }
             mma_commit(&bars[C::kBarSFull + b]);
+            ATTN_TRACE(tl, kAEvQk);
             if (ti.seg_end) mma_commit(&bars[C::kBarQEmpty + qb]);
             ++next_qk;
             progressed = true;
@@ -474,6 +498,7 @@ __global__ void __launch_bounds__(Cfg<HG>::kThreads, 1) sparse_mla_attn_kernel(c
             }
             mma_commit(&bars[C::kBarKvEmpty + b]);
             mma_commit(&bars[C::kBarPvDone + b]);
+            ATTN_TRACE(tl, kAEvPv);
             ++next_pv;
             progressed = true;
           }
@@ -519,6 +544,7 @@ __global__ void __launch_bounds__(Cfg<HG>::kThreads, 1) sparse_mla_attn_kernel(c
       }
       if (!dead) dead = !SMLA_WAIT(C::kBarSFull + b, (tl >> 1) & 1);
       if (!dead) dead = !SMLA_WAIT(C::kBarKvFull + b, (tl >> 1) & 1);  // orders the row-valid flags
+      if (tid == 0) ATTN_TRACE(tl, kAEvSoftStart);
       tc_fence_after();
       const bool row_ok = !dead && lane < 16 && valid[b * C::kRows + r] != 0;
       const uint32_t s_addr = tmem + lane_base + C::kSCol + b * HG;
@@ -547,6 +573,7 @@ __global__ void __launch_bounds__(Cfg<HG>::kThreads, 1) sparse_mla_attn_kernel(c
         if ((lane & 1) == 0) redm[w * HG + hb * 16 + (lane >> 1)] = mx;
       }
       named_bar_sync(1, 128);
+      if (tid == 0) ATTN_TRACE(tl, kAEvSoftBar);
       bool any_rescale = false;
       float alpha[HG];
 #pragma unroll
@@ -583,6 +610,7 @@ __global__ void __launch_bounds__(Cfg<HG>::kThreads, 1) sparse_mla_attn_kernel(c
       }
       // pass 2: probabilities, running sums, P^T rows
       if (tl >= 2 && !dead) dead = !SMLA_WAIT(C::kBarPvDone + b, ((tl >> 1) + 1) & 1);  // P buffers free
+      if (tid == 0) ATTN_TRACE(tl, kAEvPvWait);
 #pragma unroll
       for (int hb = 0; hb < NB16; ++hb) {
         float pr[16];
@@ -605,6 +633,7 @@ __global__ void __launch_bounds__(Cfg<HG>::kThreads, 1) sparse_mla_attn_kernel(c
       tc_fence_before();
       __syncwarp();
       if (lane == 0 && !dead) mbar_arrive(&bars[C::kBarPFull + b]);
+      if (tid == 0) ATTN_TRACE(tl, kAEvPFull);
       ++n_seg_tiles;
 
       if (ti.seg_end) {
@@ -661,6 +690,7 @@ __global__ void __launch_bounds__(Cfg<HG>::kThreads, 1) sparse_mla_attn_kernel(c
         tc_fence_before();
         __syncwarp();
         if (lane == 0 && !dead) mbar_arrive(&bars[C::kBarOFree]);
+        if (tid == 0) ATTN_TRACE(tl, kAEvEpiEnd);
       }
     }
   }
@@ -672,6 +702,7 @@ __global__ void __launch_bounds__(Cfg<HG>::kThreads, 1) sparse_mla_attn_kernel(c
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
+  if (tid == 0) ATTN_TRACE(0, kAEvExit);
 }
 
 // Per device, head-group size and row format: the kernel's dynamic shared
@@ -726,6 +757,12 @@ cudaError_t launch_impl(const AttnArgs& a, const AttnPlan& plan, cudaStream_t st
 }
 
 }  // namespace
+
+#ifdef SMLA_TRACE
+extern "C" int smla_trace_set_attn(long long* buf) {
+  return (int)cudaMemcpyToSymbol(g_smla_trace_attn, &buf, sizeof(buf));
+}
+#endif
 
 AttnPlan plan_prefill_bf16(int T, int H, int K, int num_splits, int num_sms) {
   if (wide_supported(H)) return plan_prefill_wide(T, K, num_splits, num_sms);

@@ -11,6 +11,7 @@ CTA-pair kernel on its tensor-bound workload (clock64 cycles within a CTA):
     python -m sparse_mla_attention_fp8_gb300.trace
     python -m sparse_mla_attention_fp8_gb300.trace --wide   # the 128-head FP8 decode
     python -m sparse_mla_attention_fp8_gb300.trace --wide8  # its FP8-query variant
+    python -m sparse_mla_attention_fp8_gb300.trace --nvfp4  # the NVFP4 decode (16-head groups)
 
 The normal library (``libsmla.so``) carries none of this: the hooks compile
 to nothing without SMLA_TRACE.
@@ -345,8 +346,85 @@ def main_wide8(lib_path: str | None = None):
     print(f"entry -> first QK^T {kc(E['qk'][:, 0] - enter)}; entry -> exit {kc(ex - enter)}")
 
 
+ATTN_EVENTS = ["idx", "conv_issue", "conv_full", "qk", "soft_start", "soft_bar", "p_full", "pv", "epi_end", "enter",
+               "exit", "pv_wait", "conv_start", "conv_row3"]
+
+
+def main_nvfp4(lib_path: str | None = None):
+    """Per-tile timeline of the NVFP4 decode (the 16-head-group kernel of
+    smla_attn.cu with NVFP4 rows) on the memory-bound decode's workload (64
+    requests x 1 token, H = 16, top-k 2048): clock64 cycles within each CTA."""
+    import torch
+
+    root = os.path.dirname(_PKG)
+    if root not in sys.path:
+        sys.path.insert(0, root)
+    import smla_inputs as inp
+
+    L = ctypes.CDLL(lib_path or build_traced())
+    P, i32, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    L.sparse_mla_decode_nvfp4.argtypes = [P, P, P, P, P, f32, i32, P, P, i32, i32, i32, i32, i32, i32, P, sz, P]
+    L.mla_cache_store_nvfp4.argtypes = [P, P, P, i32, i32, P]
+    L.sparse_mla_decode_nvfp4_workspace_bytes.argtypes = [i32, i32, i32, i32]
+    L.sparse_mla_decode_nvfp4_workspace_bytes.restype = sz
+    L.smla_trace_set_attn.argtypes = [P]
+    ptr = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    dev = torch.device("cuda", 0)
+    case = inp.rotating_decode(seed=1)
+    T, H, K, NB = case.q.shape[0], case.H, case.K, case.num_blocks
+    cache = torch.zeros((NB, 64, 352), dtype=torch.uint8, device=dev)
+    lat = inp.device_latent(len(case.ctx_slots), case.latent_seed, case.outlier_channels, dev)
+    slots = torch.from_numpy(case.ctx_slots).to(dev)
+    assert L.mla_cache_store_nvfp4(ptr(lat), ptr(slots), ptr(cache), lat.shape[0], NB, None) == 0
+    del lat
+    q = torch.from_numpy(case.q.view(np.int16)).to(dev)
+    idx = [torch.from_numpy(s).to(dev) for s in case.index_sets]
+    bt = torch.from_numpy(case.block_table).to(dev)
+    req = torch.from_numpy(case.req_id_per_token).to(dev)
+    ws_bytes = L.sparse_mla_decode_nvfp4_workspace_bytes(T, H, K, 0)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+    out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+    n_sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    buf = torch.zeros((n_sms, WIDE_TILES, len(ATTN_EVENTS)), dtype=torch.int64, device=dev)
+
+    def call(i):
+        rc = L.sparse_mla_decode_nvfp4(ptr(q), ptr(cache), ptr(idx[i % len(idx)]), ptr(bt), ptr(req),
+                                       f32(case.sm_scale), 0, ptr(out), ptr(lse), T, H, K, bt.shape[0], bt.shape[1],
+                                       NB, ptr(ws), ws_bytes, None)
+        assert rc == 0
+
+    for i in range(4):
+        call(i)
+    torch.cuda.synchronize()
+    assert L.smla_trace_set_attn(ptr(buf)) == 0
+    call(4)
+    torch.cuda.synchronize()
+    assert L.smla_trace_set_attn(None) == 0
+    ev = buf.cpu().numpy().astype(np.float64)
+    ev[ev == 0] = np.nan
+    ev = ev[np.isfinite(ev[:, 0, ATTN_EVENTS.index("enter")])]
+    E = {n: ev[:, :, i] for i, n in enumerate(ATTN_EVENTS)}
+    kc = lambda x: f"{np.nanmedian(x) / 1e3:7.2f}"  # noqa: E731
+    print(f"CTAs {ev.shape[0]}; clock64 cycles within each CTA (K = 1000), medians over CTAs and tiles")
+    print("event position in its tile relative to the tile's QK^T issue:")
+    for n in ["idx", "conv_issue", "conv_start", "conv_row3", "conv_full", "qk", "soft_start", "soft_bar", "pv_wait",
+              "p_full", "pv"]:
+        print(f"  {n:11s} {kc(E[n] - E['qk'])}")
+    print(f"cadence (QK^T to QK^T): {kc(np.diff(E['qk'], axis=1))}; P.V: {kc(np.diff(E['pv'], axis=1))}; "
+          f"converter full: {kc(np.diff(E['conv_full'], axis=1))}; softmax P written: {kc(np.diff(E['p_full'], axis=1))}")
+    print(f"converter warp 0: buffer free (tile t) after P.V(t - 2) issue {kc(E['conv_start'][:, 2:] - E['pv'][:, :-2])}; "
+          f"rows 0..2 {kc(E['conv_row3'] - E['conv_start'])}; rows 3.. to full {kc(E['conv_full'] - E['conv_row3'])}")
+    print(f"converter, first issue to full: {kc(E['conv_full'] - E['conv_issue'])}; "
+          f"tile t + 2 full after P.V of tile t: {kc(E['conv_full'][:, 2:] - E['pv'][:, :-2])}")
+    enter, ex = E["enter"][:, 0], E["exit"][:, 0]
+    print(f"entry -> first QK^T {kc(E['qk'][:, 0] - enter)}; entry -> exit {kc(ex - enter)}")
+
+
 if __name__ == "__main__":
-    if "--wide8" in sys.argv:
+    if "--nvfp4" in sys.argv:
+        main_nvfp4()
+    elif "--wide8" in sys.argv:
         main_wide8()
     elif "--wide" in sys.argv:
         main_wide()
