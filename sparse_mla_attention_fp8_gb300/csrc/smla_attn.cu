@@ -84,6 +84,13 @@ struct Cfg {
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort flag
   static constexpr int kSmemBytes = kOffMisc + 16;
   static constexpr int kSmemAlloc = kSmemBytes + 1024;
+  // NVFP4 rows: each converter warp stages kNvDepth rows of 352 bytes by
+  // cp.async (then their slots), after the rest of the layout
+  static constexpr int kNvDepth = 8;
+  static constexpr int kOffStage = (kSmemBytes + 127) / 128 * 128;
+  static constexpr int kOffStageSlots = kOffStage + kConvWarps * kNvDepth * 352;
+  static constexpr int kSmemAllocNv = kOffStageSlots + kConvWarps * kNvDepth * 4 + 1024;
+  static_assert(kSmemAllocNv <= 232448, "shared memory budget (NVFP4 rows)");
   static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0, "operand tiles must be 1024-byte aligned");
   static_assert(kOffBar % 8 == 0, "mbarrier alignment");
   static_assert(kSmemAlloc <= 232448, "shared memory budget");
@@ -202,34 +209,42 @@ constexpr int kTraceTiles = 64, kTraceEvents = 14;
 enum { kAEvIdx = 0, kAEvConvIssue, kAEvConvFull, kAEvQk, kAEvSoftStart, kAEvSoftBar, kAEvPFull, kAEvPv, kAEvEpiEnd,
        kAEvEnter, kAEvExit, kAEvPvWait, kAEvConvStart, kAEvConvHalf };
 
-// Two E2M1 codes (one byte, low nibble first) -> an f16 pair (exact).
-__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
-  uint32_t h2;
-  asm("{\n .reg .b8 c, z;\n mov.b16 {c, z}, %1;\n cvt.rn.f16x2.e2m1x2 %0, c;\n}"
-      : "=r"(h2)
-      : "h"((uint16_t)(byte & 0xFFu)));
-  return h2;
-}
 // An f16 pair -> a bf16 pair (exact for the values used here: at most 6
 // significant bits, normal in both formats or zero).
 __device__ __forceinline__ uint32_t f16x2_to_bf16x2(uint32_t h2) {
   return pack_bf16x2(__half2float(__ushort_as_half((uint16_t)(h2 & 0xFFFFu))),
                      __half2float(__ushort_as_half((uint16_t)(h2 >> 16))));
 }
+// Four E2M1 codes (16 bits, value i in nibble i) -> two bf16 pairs, exactly.
+// The bf16 bits of the eight magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6 are looked
+// up with byte permutes (high bytes 00 3F 3F 3F 40 40 40 40, low bytes
+// 00 00 80 C0 00 40 80 C0), and each code's sign bit is moved to bit 15 of its
+// half.
+__device__ __forceinline__ void e2m1x4_to_bf16x2(uint32_t c16, uint32_t& w01, uint32_t& w23) {
+  const uint32_t sel = c16 & 0x7777u;
+  const uint32_t hi = __byte_perm(0x3F3F3F00u, 0x40404040u, sel);
+  const uint32_t lo = __byte_perm(0xC0800000u, 0xC0804000u, sel);
+  w01 = __byte_perm(lo, hi, 0x5140) | ((c16 << 12) & 0x8000u) | ((c16 << 24) & 0x80000000u);
+  w23 = __byte_perm(lo, hi, 0x7362) | ((c16 << 4) & 0x8000u) | ((c16 << 16) & 0x80000000u);
+}
+__device__ __forceinline__ uint32_t mul_bf16x2_rn(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
 // Eight NVFP4 NoPE values (four code bytes) times their block scale (an E4M3
 // byte) -> one 16-byte chunk of bf16 values, exactly: code * scale has at most
-// 6 significant bits and lies in [2^-10, 2688] or is 0, so the f16 product and
-// its bf16 copy are exact.
+// 6 significant bits and lies in [2^-10, 2688] or is 0, so the bf16 product is
+// exact.
 __device__ __forceinline__ uint4 nvfp4_chunk(uint32_t codes, uint32_t scale_byte) {
   uint32_t sc2;
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(sc2) : "h"((uint16_t)(scale_byte * 0x0101u)));
+  const uint32_t s2 = f16x2_to_bf16x2(sc2);  // the scale in both halves, exact
   uint32_t o[4];
+  e2m1x4_to_bf16x2(codes & 0xFFFFu, o[0], o[1]);
+  e2m1x4_to_bf16x2(codes >> 16, o[2], o[3]);
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    uint32_t v;
-    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(v) : "r"(e2m1x2_to_f16x2(codes >> (8 * k))), "r"(sc2));
-    o[k] = f16x2_to_bf16x2(v);
-  }
+  for (int k = 0; k < 4; ++k) o[k] = mul_bf16x2_rn(o[k], s2);
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 // Eight E4M3 RoPE values (two words) -> one 16-byte chunk of bf16 values (exact).
@@ -339,6 +354,85 @@ __global__ void __launch_bounds__(Cfg<HG>::kThreads, 1) sparse_mla_attn_kernel(c
         ++seg;
       }
     }
+  } else if (kNv && warp >= C::kConvWarp0) {
+    // ------------------------------------------------------------ NVFP4 converters
+    // Converter warp cw handles rows cw, cw + 10, ... of every tile.  Each row
+    // is copied as stored (22 chunks of 16 bytes) by cp.async into the warp's
+    // ring of kNvDepth rows, kNvDepth rows ahead of its conversion; lane l then
+    // dequantizes output chunks l and l + 32 (and RoPE chunk l for l < 8) into
+    // the bf16 operand tile.
+    const int cw = warp - C::kConvWarp0;
+    const int RW = (C::kRows - cw + C::kConvWarps - 1) / C::kConvWarps;
+    const int n_items = n_local * RW;
+    uint8_t* ring = smem + C::kOffStage + cw * C::kNvDepth * 352;
+    int32_t* ring_slot = reinterpret_cast<int32_t*>(smem + C::kOffStageSlots) + cw * C::kNvDepth;
+    bool ok = true;
+    // one commit group per call, so that the wait below counts rows
+    auto issue = [&](int m) {
+      if (m < n_items && ok) {
+        const int tl = m / RW, k = m - tl * RW;
+        const int r = cw + k * C::kConvWarps;
+        const int b4 = tl & 3;
+        if (k == 0) ok = ok && SMLA_WAIT(C::kBarIdxFull + b4, (tl >> 2) & 1);
+        if (ok) {
+          if (k == 0 && cw == 0 && lane == 0) ATTN_TRACE(tl, kAEvConvIssue);
+          const int32_t slot = slots_ring[b4 * C::kRows + r];
+          if (k == RW - 1) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[C::kBarIdxEmpty + b4]);
+          }
+          const int ri = m % C::kNvDepth;
+          if (lane == 0) ring_slot[ri] = slot;
+          if (slot >= 0 && lane < 22)
+            cp_async16(smem_u32(ring + ri * 352 + 16 * lane), p.cache + (int64_t)slot * 352 + 16 * lane);
+        }
+      }
+      asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    for (int j = 0; j < C::kNvDepth; ++j) issue(j);
+    int tl = 0, k = 0;  // tile and row of item m
+    for (int m = 0; m < n_items && ok; ++m) {
+      asm volatile("cp.async.wait_group %0;" ::"n"(C::kNvDepth - 1) : "memory");
+      __syncwarp();  // row m has landed for every lane of the warp
+      const int r = cw + k * C::kConvWarps;
+      const int b = tl & 1;
+      if (k == 0 && tl >= 2) ok = ok && SMLA_WAIT(C::kBarKvEmpty + b, ((tl >> 1) + 1) & 1);
+      if (!ok) break;
+      if (k == 0 && cw == 0 && lane == 0) ATTN_TRACE(tl, kAEvConvStart);
+      if (k == 3 && cw == 0 && lane == 0) ATTN_TRACE(tl, kAEvConvHalf);
+      const int ri = m % C::kNvDepth;
+      const uint8_t* row = ring + ri * 352;
+      const bool v = ring_slot[ri] >= 0;
+      const uint32_t tile = smem_u32(smem + C::kOffKv + b * C::kKvTile);
+      const uint4 z = make_uint4(0, 0, 0, 0);
+      uint4 c0 = z, c1 = z, c2 = z;
+      if (v) {
+        c0 = nvfp4_chunk(*reinterpret_cast<const uint32_t*>(row + 4 * lane), row[256 + (lane >> 1)]);
+        c1 = nvfp4_chunk(*reinterpret_cast<const uint32_t*>(row + 128 + 4 * lane), row[272 + (lane >> 1)]);
+        if (lane < 8) {
+          const uint2 rr = *reinterpret_cast<const uint2*>(row + 288 + 8 * lane);
+          c2 = e4m3x8_chunk(rr.x, rr.y);
+        }
+      }
+      sts128(tile + sw128_chunk(C::kRows, r, lane), c0);
+      sts128(tile + sw128_chunk(C::kRows, r, lane + 32), c1);
+      if (lane < 8) sts128(tile + sw128_chunk(C::kRows, r, lane + 64), c2);
+      if (lane == 0) valid[b * C::kRows + r] = v ? 1 : 0;
+      if (k == RW - 1) {
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[C::kBarKvFull + b]);
+        if (cw == 0 && lane == 0) ATTN_TRACE(tl, kAEvConvFull);
+      }
+      __syncwarp();  // every lane has read ring slot ri before it is refilled
+      issue(m + C::kNvDepth);
+      if (++k == RW) {
+        k = 0;
+        ++tl;
+      }
+    }
+    // no copy may still be landing in shared memory when the CTA exits
+    cp_async_wait_all();
   } else if (warp >= C::kConvWarp0) {
     // ------------------------------------------------------------ converters
     const int cw = warp - C::kConvWarp0;
@@ -365,25 +459,10 @@ __global__ void __launch_bounds__(Cfg<HG>::kThreads, 1) sparse_mla_attn_kernel(c
       }
       rb.slot = slot;
       if (slot >= 0) {
-        if constexpr (kNv) {
-          // lane l: the codes of output chunks l and l + 32 (bytes 4 l and 128 + 4 l),
-          // their block scales (bytes 256 + l / 2 and 272 + l / 2) and, for l < 8,
-          // RoPE bytes 288 + 8 l .. + 7
-          const uint8_t* row = p.cache + (int64_t)slot * 352;
-          rb.a.x = __ldg(reinterpret_cast<const uint32_t*>(row) + lane);
-          rb.a.y = __ldg(reinterpret_cast<const uint32_t*>(row + 128) + lane);
-          rb.a.z = (uint32_t)__ldg(row + 256 + (lane >> 1)) | ((uint32_t)__ldg(row + 272 + (lane >> 1)) << 8);
-          if (lane < 8) {
-            const uint2 rr = __ldg(reinterpret_cast<const uint2*>(row + 288) + lane);
-            rb.b.x = rr.x;
-            rb.b.y = rr.y;
-          }
-        } else {
-          const uint8_t* row = reinterpret_cast<const uint8_t*>(p.kv + (int64_t)slot * kDqk);
-          rb.a = ld_stream(row + 16 * lane);
-          rb.b = ld_stream(row + 16 * (lane + 32));
-          if (lane < 8) rb.c = ld_stream(row + 16 * (lane + 64));
-        }
+        const uint8_t* row = reinterpret_cast<const uint8_t*>(p.kv + (int64_t)slot * kDqk);
+        rb.a = ld_stream(row + 16 * lane);
+        rb.b = ld_stream(row + 16 * (lane + 32));
+        if (lane < 8) rb.c = ld_stream(row + 16 * (lane + 64));
       }
     };
 
@@ -398,15 +477,9 @@ __global__ void __launch_bounds__(Cfg<HG>::kThreads, 1) sparse_mla_attn_kernel(c
       const uint32_t tile = smem_u32(smem + C::kOffKv + b * C::kKvTile);
       const bool v = rb.slot >= 0;
       const uint4 z = make_uint4(0, 0, 0, 0);
-      if constexpr (kNv) {
-        sts128(tile + sw128_chunk(C::kRows, r, lane), v ? nvfp4_chunk(rb.a.x, rb.a.z & 0xFFu) : z);
-        sts128(tile + sw128_chunk(C::kRows, r, lane + 32), v ? nvfp4_chunk(rb.a.y, (rb.a.z >> 8) & 0xFFu) : z);
-        if (lane < 8) sts128(tile + sw128_chunk(C::kRows, r, lane + 64), v ? e4m3x8_chunk(rb.b.x, rb.b.y) : z);
-      } else {
-        sts128(tile + sw128_chunk(C::kRows, r, lane), v ? rb.a : z);
-        sts128(tile + sw128_chunk(C::kRows, r, lane + 32), v ? rb.b : z);
-        if (lane < 8) sts128(tile + sw128_chunk(C::kRows, r, lane + 64), v ? rb.c : z);
-      }
+      sts128(tile + sw128_chunk(C::kRows, r, lane), v ? rb.a : z);
+      sts128(tile + sw128_chunk(C::kRows, r, lane + 32), v ? rb.b : z);
+      if (lane < 8) sts128(tile + sw128_chunk(C::kRows, r, lane + 64), v ? rb.c : z);
       if (lane == 0) valid[b * C::kRows + r] = v ? 1 : 0;
       if (k == RW - 1) {
         fence_proxy_async_smem();
@@ -720,7 +793,8 @@ cudaError_t launch_impl(const AttnArgs& a, const AttnPlan& plan, cudaStream_t st
   const int hi = (HG == 16 ? 0 : 1) + (kNv ? 2 : 0);
   std::call_once(g_attr_once[hi][dev], [hi, dev] {
     g_attr_err[hi][dev] = cudaFuncSetAttribute(sparse_mla_attn_kernel<HG, kNv>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemAlloc);
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               kNv ? C::kSmemAllocNv : C::kSmemAlloc);
   });
   if (g_attr_err[hi][dev] != cudaSuccess) return g_attr_err[hi][dev];
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
@@ -748,7 +822,7 @@ cudaError_t launch_impl(const AttnArgs& a, const AttnPlan& plan, cudaStream_t st
   p.nt = plan.nt;
   p.total = plan.total;
   p.G = plan.G;
-  sparse_mla_attn_kernel<HG, kNv><<<plan.G, C::kThreads, C::kSmemAlloc, stream>>>(p);
+  sparse_mla_attn_kernel<HG, kNv><<<plan.G, C::kThreads, kNv ? C::kSmemAllocNv : C::kSmemAlloc, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess || !plan.need_combine) return e;
   e = launch_combine<HG>(p.part_o, p.part_lse, p.out, p.lse, p.H, p.n_hg, p.nt, p.total, p.G, plan.units, stream);
