@@ -197,7 +197,7 @@ __device__ __forceinline__ float warp_reduce16(float (&v)[16], int lane) {
 // by the host through smla_trace_set_attn).  Compiled out otherwise.
 #ifdef SMLA_TRACE
 __device__ long long* g_smla_trace_attn = nullptr;
-constexpr int kTraceTiles = 64, kTraceEvents = 14;
+constexpr int kTraceTiles = 64, kTraceEvents = 15;
 #define ATTN_TRACE(tl, ev)                                                                                   \
   do {                                                                                                       \
     if (g_smla_trace_attn && (tl) < kTraceTiles)                                                           \
@@ -207,7 +207,7 @@ constexpr int kTraceTiles = 64, kTraceEvents = 14;
 #define ATTN_TRACE(tl, ev) ((void)0)
 #endif
 enum { kAEvIdx = 0, kAEvConvIssue, kAEvConvFull, kAEvQk, kAEvSoftStart, kAEvSoftBar, kAEvPFull, kAEvPv, kAEvEpiEnd,
-       kAEvEnter, kAEvExit, kAEvPvWait, kAEvConvStart, kAEvConvHalf };
+       kAEvEnter, kAEvExit, kAEvPvWait, kAEvConvStart, kAEvConvHalf, kAEvConvLanded };
 
 // An f16 pair -> a bf16 pair (exact for the values used here: at most 6
 // significant bits, normal in both formats or zero).
@@ -394,6 +394,7 @@ __global__ void __launch_bounds__(Cfg<HG>::kThreads, 1) sparse_mla_attn_kernel(c
     for (int m = 0; m < n_items && ok; ++m) {
       asm volatile("cp.async.wait_group %0;" ::"n"(C::kNvDepth - 1) : "memory");
       __syncwarp();  // row m has landed for every lane of the warp
+      if (k == 0 && cw == 0 && lane == 0) ATTN_TRACE(tl, kAEvConvLanded);
       const int r = cw + k * C::kConvWarps;
       const int b = tl & 1;
       if (k == 0 && tl >= 2) ok = ok && SMLA_WAIT(C::kBarKvEmpty + b, ((tl >> 1) + 1) & 1);

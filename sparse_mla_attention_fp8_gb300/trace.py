@@ -347,7 +347,7 @@ def main_wide8(lib_path: str | None = None):
 
 
 ATTN_EVENTS = ["idx", "conv_issue", "conv_full", "qk", "soft_start", "soft_bar", "p_full", "pv", "epi_end", "enter",
-               "exit", "pv_wait", "conv_start", "conv_row3"]
+               "exit", "pv_wait", "conv_start", "conv_row3", "conv_landed"]
 
 
 def main_nvfp4(lib_path: str | None = None):
@@ -408,8 +408,8 @@ def main_nvfp4(lib_path: str | None = None):
     kc = lambda x: f"{np.nanmedian(x) / 1e3:7.2f}"  # noqa: E731
     print(f"CTAs {ev.shape[0]}; clock64 cycles within each CTA (K = 1000), medians over CTAs and tiles")
     print("event position in its tile relative to the tile's QK^T issue:")
-    for n in ["idx", "conv_issue", "conv_start", "conv_row3", "conv_full", "qk", "soft_start", "soft_bar", "pv_wait",
-              "p_full", "pv"]:
+    for n in ["idx", "conv_issue", "conv_landed", "conv_start", "conv_row3", "conv_full", "qk", "soft_start",
+              "soft_bar", "pv_wait", "p_full", "pv"]:
         print(f"  {n:11s} {kc(E[n] - E['qk'])}")
     print(f"cadence (QK^T to QK^T): {kc(np.diff(E['qk'], axis=1))}; P.V: {kc(np.diff(E['pv'], axis=1))}; "
           f"converter full: {kc(np.diff(E['conv_full'], axis=1))}; softmax P written: {kc(np.diff(E['p_full'], axis=1))}")
