@@ -57,6 +57,14 @@ WIDE_TRAFFIC_BY_SOURCE = {
 }
 
 
+# The same for the NVFP4 decode (the 16-head-group kernel with NVFP4 rows,
+# plus the combine of tokens split between CTAs).
+NVFP4_TRAFFIC_SOURCES = ("smla_attn.cu", "smla_combine.cuh", "smla_common.cuh", "sm103_ptx.cuh")
+NVFP4_TRAFFIC_BY_SOURCE = {
+    "19da7f95bb3d2600": (59_149_056 + 25_088 + 7_372_800, "attention kernel + combine"),
+}
+
+
 def _source_key(files):
     import hashlib
     h = hashlib.sha256()
@@ -780,18 +788,21 @@ def tensor_workload(args, quiet=False):
     if algo_bytes is not None:
         gbs = algo_bytes / (ms * 1e-3) / 1e9
         line["metric"] = f"{args.workload} query-tokens/s + GB/s vs HBM roofline"
+        traffic, traffic_kernels = None, None
         if args.workload == "decode_nvfp4_h16_k2048":
             line["dtype"] = "e2m1"
             line["config"]["step"] = "one sparse decode launch over the NVFP4 cache (rows dequantized in the kernel)"
             line["config"]["l2"] = "8 rotating top-k index sets (8 x 46 MB gathered) > 129 MB L2"
-            kernel = "sparse_mla_attn_kernel<16, NVFP4 rows>"
+            kernel = "sparse_mla_attn_kernel<16, NVFP4 rows> (plus the combine)"
+            traffic, traffic_kernels = NVFP4_TRAFFIC_BY_SOURCE.get(_source_key(NVFP4_TRAFFIC_SOURCES), (None, None))
         else:
             line["config"]["step"] = "the query-side and value-side GEMM launches"
             line["config"]["l2"] = "inputs (1.5 GB per step) larger than L2"
             kernel = "head_gemm_kernel (two launches per step)"
         line["roofline"] = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                            "frac": gbs / peaks["hbm_gbs"], "traffic": None, "peak_source": peaks["source"],
-                            "kernel": kernel, "bytes_per_step": algo_bytes, "avg_step_us": ms * 1e3}
+                            "frac": gbs / peaks["hbm_gbs"], "traffic": traffic, "traffic_kernels": traffic_kernels,
+                            "peak_source": peaks["source"], "kernel": kernel, "bytes_per_step": algo_bytes,
+                            "avg_step_us": ms * 1e3}
     return line
 
 
