@@ -61,7 +61,7 @@ WIDE_TRAFFIC_BY_SOURCE = {
 # plus the combine of tokens split between CTAs).
 NVFP4_TRAFFIC_SOURCES = ("smla_attn.cu", "smla_combine.cuh", "smla_common.cuh", "sm103_ptx.cuh")
 NVFP4_TRAFFIC_BY_SOURCE = {
-    "19da7f95bb3d2600": (59_149_056 + 25_088 + 7_372_800, "attention kernel + combine"),
+    "6a45d9458053455a": (59_168_768 + 48_384 + 7_372_288, "attention kernel + combine"),
 }
 
 

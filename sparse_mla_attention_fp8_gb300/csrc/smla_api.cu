@@ -480,9 +480,11 @@ int mla_cache_store_nvfp4(const void* kv_new, const int64_t* slot_mapping, uint8
 
 size_t sparse_mla_decode_nvfp4_workspace_bytes(int T, int H, int K, int num_splits) {
   if (T <= 0 || K < 0 || (int64_t)T * K > INT32_MAX) return 0;
-  const size_t attn = workspace_bytes_for(false, T, H, K, num_splits);
-  if (attn == 0) return 0;
-  if (smla::nvfp4_native_supported(H)) return attn;
+  if (check_heads(H) != SMLA_OK) return 0;
+  int sms = 0;
+  if (num_sms(&sms) != SMLA_OK) return 0;
+  if (smla::nvfp4_native_supported(H)) return smla::plan_decode_nvfp4(T, H, K, num_splits, sms).ws_bytes;
+  const size_t attn = smla::plan_attention(false, T, H, K, num_splits, sms).ws_bytes;
   return ((attn + 255) / 256) * 256 + smla::nvfp4_stage_bytes(T, K);
 }
 
@@ -507,8 +509,9 @@ int sparse_mla_decode_nvfp4(const void* q, const uint8_t* kv_cache, const int32_
   if (rc != SMLA_OK) return rc;
   // the bf16 attention's own workspace (its status word leads), then, at 128
   // heads, the staged rows
-  const smla::AttnPlan plan = smla::plan_attention(false, T, H, K, num_splits, sms);
   const bool native = smla::nvfp4_native_supported(H);
+  const smla::AttnPlan plan = native ? smla::plan_decode_nvfp4(T, H, K, num_splits, sms)
+                                     : smla::plan_attention(false, T, H, K, num_splits, sms);
   const size_t attn_bytes = ((plan.ws_bytes + 255) / 256) * 256;
   const size_t need = native ? plan.ws_bytes : attn_bytes + smla::nvfp4_stage_bytes(T, K);
   if (workspace) {

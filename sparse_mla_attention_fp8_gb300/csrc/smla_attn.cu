@@ -49,14 +49,16 @@ namespace {
 
 constexpr uint32_t kFull = 0xffffffffu;
 
-template <int HG>
+template <int HG, bool kNv>
 struct Cfg {
   static constexpr int kRows = 64;                       // top-k rows per tile
   static constexpr int kPanel = kRows * 128;             // one 64-column panel of the row tile
   static constexpr int kKvTile = 9 * kPanel;             // 576 columns
   static constexpr int kQPanel = HG * 128;
   static constexpr int kQBytes = 9 * kQPanel;
-  static constexpr int kQBufs = HG == 16 ? 2 : 1;       // Q blocks in flight (next unit prefetched)
+  // Q blocks in flight (next unit prefetched); NVFP4 rows give the room to
+  // their staging instead
+  static constexpr int kQBufs = (HG == 16 && !kNv) ? 2 : 1;
   static constexpr int kPBytes = kRows * HG * 2;
   static constexpr int kMmaWarp = 4;
   static constexpr int kIndexWarp = 5;
@@ -84,13 +86,14 @@ struct Cfg {
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort flag
   static constexpr int kSmemBytes = kOffMisc + 16;
   static constexpr int kSmemAlloc = kSmemBytes + 1024;
-  // NVFP4 rows: each converter warp stages kNvDepth rows of 352 bytes by
-  // cp.async (then their slots), after the rest of the layout
-  static constexpr int kNvDepth = 8;
+  // NVFP4 rows: each converter warp stages its rows of two tiles (up to
+  // 2 x kNvRows rows of 352 bytes, then their slots) by cp.async, after the
+  // rest of the layout
+  static constexpr int kNvRows = (kRows + kConvWarps - 1) / kConvWarps;  // rows of a tile per converter warp, at most
   static constexpr int kOffStage = (kSmemBytes + 127) / 128 * 128;
-  static constexpr int kOffStageSlots = kOffStage + kConvWarps * kNvDepth * 352;
-  static constexpr int kSmemAllocNv = kOffStageSlots + kConvWarps * kNvDepth * 4 + 1024;
-  static_assert(kSmemAllocNv <= 232448, "shared memory budget (NVFP4 rows)");
+  static constexpr int kOffStageSlots = kOffStage + kConvWarps * 2 * kNvRows * 352;
+  static constexpr int kSmemAllocNv = kOffStageSlots + kConvWarps * 2 * kNvRows * 4 + 1024;
+  static_assert(!kNv || (HG == 16 && kSmemAllocNv <= 232448), "NVFP4 rows: 16-head groups, shared memory budget");
   static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0, "operand tiles must be 1024-byte aligned");
   static_assert(kOffBar % 8 == 0, "mbarrier alignment");
   static_assert(kSmemAlloc <= 232448, "shared memory budget");
@@ -264,8 +267,8 @@ __device__ __forceinline__ uint4 e4m3x8_chunk(uint32_t w0, uint32_t w1) {
 // table) instead of bf16 latent rows; they are dequantized exactly into the
 // same bf16 operand tiles.
 template <int HG, bool kNv>
-__global__ void __launch_bounds__(Cfg<HG>::kThreads, 1) sparse_mla_attn_kernel(const __grid_constant__ Params p) {
-  using C = Cfg<HG>;
+__global__ void __launch_bounds__(Cfg<HG, kNv>::kThreads, 1) sparse_mla_attn_kernel(const __grid_constant__ Params p) {
+  using C = Cfg<HG, kNv>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   grid_launch_dependents();  // the combine may be launched behind this grid right away
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -356,81 +359,73 @@ __global__ void __launch_bounds__(Cfg<HG>::kThreads, 1) sparse_mla_attn_kernel(c
     }
   } else if (kNv && warp >= C::kConvWarp0) {
     // ------------------------------------------------------------ NVFP4 converters
-    // Converter warp cw handles rows cw, cw + 10, ... of every tile.  Each row
-    // is copied as stored (22 chunks of 16 bytes) by cp.async into the warp's
-    // ring of kNvDepth rows, kNvDepth rows ahead of its conversion; lane l then
-    // dequantizes output chunks l and l + 32 (and RoPE chunk l for l < 8) into
-    // the bf16 operand tile.
+    // Converter warp cw handles rows cw, cw + 10, ... of every tile (RW rows).
+    // Two tiles ahead, it copies them as stored (22 chunks of 16 bytes each)
+    // by cp.async into its staging half for that tile (one commit group per
+    // tile); once a tile's rows have landed and its operand buffer is free,
+    // lane l dequantizes output chunks l and l + 32 (and RoPE chunk l for
+    // l < 8) of every row into the bf16 tile.
     const int cw = warp - C::kConvWarp0;
     const int RW = (C::kRows - cw + C::kConvWarps - 1) / C::kConvWarps;
-    const int n_items = n_local * RW;
-    uint8_t* ring = smem + C::kOffStage + cw * C::kNvDepth * 352;
-    int32_t* ring_slot = reinterpret_cast<int32_t*>(smem + C::kOffStageSlots) + cw * C::kNvDepth;
+    uint8_t* stage = smem + C::kOffStage + cw * 2 * C::kNvRows * 352;
+    int32_t* stage_slot = reinterpret_cast<int32_t*>(smem + C::kOffStageSlots) + cw * 2 * C::kNvRows;
     bool ok = true;
-    // one commit group per call, so that the wait below counts rows
-    auto issue = [&](int m) {
-      if (m < n_items && ok) {
-        const int tl = m / RW, k = m - tl * RW;
-        const int r = cw + k * C::kConvWarps;
-        const int b4 = tl & 3;
-        if (k == 0) ok = ok && SMLA_WAIT(C::kBarIdxFull + b4, (tl >> 2) & 1);
+    auto issue_tile = [&](int tl) {
+      if (tl < n_local && ok) {
+        const int b4 = tl & 3, half = tl & 1;
+        ok = SMLA_WAIT(C::kBarIdxFull + b4, (tl >> 2) & 1);
         if (ok) {
-          if (k == 0 && cw == 0 && lane == 0) ATTN_TRACE(tl, kAEvConvIssue);
-          const int32_t slot = slots_ring[b4 * C::kRows + r];
-          if (k == RW - 1) {
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[C::kBarIdxEmpty + b4]);
+          if (cw == 0 && lane == 0) ATTN_TRACE(tl, kAEvConvIssue);
+          for (int k = 0; k < RW; ++k) {
+            const int32_t slot = slots_ring[b4 * C::kRows + cw + k * C::kConvWarps];
+            if (lane == 0) stage_slot[half * C::kNvRows + k] = slot;
+            if (slot >= 0 && lane < 22)
+              cp_async16(smem_u32(stage + (half * C::kNvRows + k) * 352 + 16 * lane),
+                         p.cache + (int64_t)slot * 352 + 16 * lane);
           }
-          const int ri = m % C::kNvDepth;
-          if (lane == 0) ring_slot[ri] = slot;
-          if (slot >= 0 && lane < 22)
-            cp_async16(smem_u32(ring + ri * 352 + 16 * lane), p.cache + (int64_t)slot * 352 + 16 * lane);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars[C::kBarIdxEmpty + b4]);
         }
       }
       asm volatile("cp.async.commit_group;" ::: "memory");
     };
-    for (int j = 0; j < C::kNvDepth; ++j) issue(j);
-    int tl = 0, k = 0;  // tile and row of item m
-    for (int m = 0; m < n_items && ok; ++m) {
-      asm volatile("cp.async.wait_group %0;" ::"n"(C::kNvDepth - 1) : "memory");
-      __syncwarp();  // row m has landed for every lane of the warp
-      if (k == 0 && cw == 0 && lane == 0) ATTN_TRACE(tl, kAEvConvLanded);
-      const int r = cw + k * C::kConvWarps;
-      const int b = tl & 1;
-      if (k == 0 && tl >= 2) ok = ok && SMLA_WAIT(C::kBarKvEmpty + b, ((tl >> 1) + 1) & 1);
-      if (!ok) break;
-      if (k == 0 && cw == 0 && lane == 0) ATTN_TRACE(tl, kAEvConvStart);
-      if (k == 3 && cw == 0 && lane == 0) ATTN_TRACE(tl, kAEvConvHalf);
-      const int ri = m % C::kNvDepth;
-      const uint8_t* row = ring + ri * 352;
-      const bool v = ring_slot[ri] >= 0;
+    issue_tile(0);
+    issue_tile(1);
+    for (int tl = 0; tl < n_local && ok; ++tl) {
+      const int b = tl & 1, half = tl & 1;
+      asm volatile("cp.async.wait_group 1;" ::: "memory");
+      __syncwarp();  // the tile's rows have landed for every lane of the warp
+      if (cw == 0 && lane == 0) ATTN_TRACE(tl, kAEvConvLanded);
+      if (tl >= 2 && !(ok = SMLA_WAIT(C::kBarKvEmpty + b, ((tl >> 1) + 1) & 1))) break;
+      if (cw == 0 && lane == 0) ATTN_TRACE(tl, kAEvConvStart);
       const uint32_t tile = smem_u32(smem + C::kOffKv + b * C::kKvTile);
       const uint4 z = make_uint4(0, 0, 0, 0);
-      uint4 c0 = z, c1 = z, c2 = z;
-      if (v) {
-        c0 = nvfp4_chunk(*reinterpret_cast<const uint32_t*>(row + 4 * lane), row[256 + (lane >> 1)]);
-        c1 = nvfp4_chunk(*reinterpret_cast<const uint32_t*>(row + 128 + 4 * lane), row[272 + (lane >> 1)]);
-        if (lane < 8) {
-          const uint2 rr = *reinterpret_cast<const uint2*>(row + 288 + 8 * lane);
-          c2 = e4m3x8_chunk(rr.x, rr.y);
+#pragma unroll
+      for (int k = 0; k < C::kNvRows; ++k) {
+        if (k < RW) {
+          const int r = cw + k * C::kConvWarps;
+          const uint8_t* row = stage + (half * C::kNvRows + k) * 352;
+          const bool v = stage_slot[half * C::kNvRows + k] >= 0;
+          uint4 c0 = z, c1 = z, c2 = z;
+          if (v) {
+            c0 = nvfp4_chunk(*reinterpret_cast<const uint32_t*>(row + 4 * lane), row[256 + (lane >> 1)]);
+            c1 = nvfp4_chunk(*reinterpret_cast<const uint32_t*>(row + 128 + 4 * lane), row[272 + (lane >> 1)]);
+            if (lane < 8) {
+              const uint2 rr = *reinterpret_cast<const uint2*>(row + 288 + 8 * lane);
+              c2 = e4m3x8_chunk(rr.x, rr.y);
+            }
+          }
+          sts128(tile + sw128_chunk(C::kRows, r, lane), c0);
+          sts128(tile + sw128_chunk(C::kRows, r, lane + 32), c1);
+          if (lane < 8) sts128(tile + sw128_chunk(C::kRows, r, lane + 64), c2);
+          if (lane == 0) valid[b * C::kRows + r] = v ? 1 : 0;
         }
       }
-      sts128(tile + sw128_chunk(C::kRows, r, lane), c0);
-      sts128(tile + sw128_chunk(C::kRows, r, lane + 32), c1);
-      if (lane < 8) sts128(tile + sw128_chunk(C::kRows, r, lane + 64), c2);
-      if (lane == 0) valid[b * C::kRows + r] = v ? 1 : 0;
-      if (k == RW - 1) {
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[C::kBarKvFull + b]);
-        if (cw == 0 && lane == 0) ATTN_TRACE(tl, kAEvConvFull);
-      }
-      __syncwarp();  // every lane has read ring slot ri before it is refilled
-      issue(m + C::kNvDepth);
-      if (++k == RW) {
-        k = 0;
-        ++tl;
-      }
+      fence_proxy_async_smem();
+      __syncwarp();  // every lane has written its chunks and read the staging half
+      if (lane == 0) mbar_arrive(&bars[C::kBarKvFull + b]);
+      if (cw == 0 && lane == 0) ATTN_TRACE(tl, kAEvConvFull);
+      issue_tile(tl + 2);
     }
     // no copy may still be landing in shared memory when the CTA exits
     cp_async_wait_all();
@@ -506,9 +501,10 @@ __global__ void __launch_bounds__(Cfg<HG>::kThreads, 1) sparse_mla_attn_kernel(c
   } else if (warp == C::kMmaWarp) {
     // ------------------------------------------------------------ MMA issuer
     // One thread issues every tensor-core op.  It polls (never blocks on) the
-    // two inputs it can consume: the next converted tile for QK^T (which may
-    // run up to two tiles ahead of P.V, one per S buffer) and the next P
-    // operand for P.V, and issues whichever is ready first.
+    // two inputs it can consume: the next P operand for P.V, checked first
+    // because its completion frees an operand tile, and the next converted
+    // tile for QK^T (which may run up to two tiles ahead of P.V, one per S
+    // buffer).
     if (lane == 0 && n_local > 0) {
       int seg_q = 0, seg_o = 0;  // segments whose first QK^T / first P.V was issued
       constexpr uint32_t idesc_qk = make_idesc_bf16(64, HG, 0, 0);
@@ -521,34 +517,6 @@ __global__ void __launch_bounds__(Cfg<HG>::kThreads, 1) sparse_mla_attn_kernel(c
       uint64_t t_idle = 0;
       while (next_pv < n_local) {
         bool progressed = false;
-        // ---- QK^T of tile next_qk: needs its tile, its Q block and a free S buffer
-        if (next_qk < n_local && next_qk < next_pv + 2) {
-          const int tl = next_qk;
-          const TileInfo ti = tile_info(p, xbeg + tl, xbeg, xend);
-          const int b = tl & 1;
-          const int seg = ti.seg_start ? seg_q : seg_q - 1;
-          const int qb = seg % C::kQBufs;
-          const bool q_ok = !ti.seg_start || mbar_test_wait(&bars[C::kBarQFull + qb], (seg / C::kQBufs) & 1);
-          if (q_ok && mbar_test_wait(&bars[C::kBarKvFull + b], (tl >> 1) & 1)) {
-            if (ti.seg_start) ++seg_q;
-            tc_fence_after();
-            const uint32_t kv = kv_base + b * C::kKvTile;
-            const uint32_t qs = q_base + qb * C::kQBytes;
-            const uint32_t sbuf = tmem + C::kSCol + b * HG;
-#pragma unroll
-            for (int s = 0; s < 36; ++s) {
-              const uint32_t off = (s & 3) * 32;
-              const uint64_t da = make_sdesc(kv + (s >> 2) * C::kPanel + off, 16, 1024, kLayoutSw128);
-              const uint64_t db = make_sdesc(qs + (s >> 2) * C::kQPanel + off, 16, 1024, kLayoutSw128);
-              mma_ss(sbuf, da, db, idesc_qk, s == 0 ? 0u : 1u);
-            }
-            mma_commit(&bars[C::kBarSFull + b]);
-            ATTN_TRACE(tl, kAEvQk);
-            if (ti.seg_end) mma_commit(&bars[C::kBarQEmpty + qb]);
-            ++next_qk;
-            progressed = true;
-          }
-        }
         // ---- P.V of tile next_pv: needs its P operands (and, for a segment's
         // first tile, the previous segment's epilogue to have read O)
         if (next_pv < next_qk) {
@@ -574,6 +542,34 @@ __global__ void __launch_bounds__(Cfg<HG>::kThreads, 1) sparse_mla_attn_kernel(c
             mma_commit(&bars[C::kBarPvDone + b]);
             ATTN_TRACE(tl, kAEvPv);
             ++next_pv;
+            progressed = true;
+          }
+        }
+        // ---- QK^T of tile next_qk: needs its tile, its Q block and a free S buffer
+        if (next_qk < n_local && next_qk < next_pv + 2) {
+          const int tl = next_qk;
+          const TileInfo ti = tile_info(p, xbeg + tl, xbeg, xend);
+          const int b = tl & 1;
+          const int seg = ti.seg_start ? seg_q : seg_q - 1;
+          const int qb = seg % C::kQBufs;
+          const bool q_ok = !ti.seg_start || mbar_test_wait(&bars[C::kBarQFull + qb], (seg / C::kQBufs) & 1);
+          if (q_ok && mbar_test_wait(&bars[C::kBarKvFull + b], (tl >> 1) & 1)) {
+            if (ti.seg_start) ++seg_q;
+            tc_fence_after();
+            const uint32_t kv = kv_base + b * C::kKvTile;
+            const uint32_t qs = q_base + qb * C::kQBytes;
+            const uint32_t sbuf = tmem + C::kSCol + b * HG;
+#pragma unroll
+            for (int s = 0; s < 36; ++s) {
+              const uint32_t off = (s & 3) * 32;
+              const uint64_t da = make_sdesc(kv + (s >> 2) * C::kPanel + off, 16, 1024, kLayoutSw128);
+              const uint64_t db = make_sdesc(qs + (s >> 2) * C::kQPanel + off, 16, 1024, kLayoutSw128);
+              mma_ss(sbuf, da, db, idesc_qk, s == 0 ? 0u : 1u);
+            }
+            mma_commit(&bars[C::kBarSFull + b]);
+            ATTN_TRACE(tl, kAEvQk);
+            if (ti.seg_end) mma_commit(&bars[C::kBarQEmpty + qb]);
+            ++next_qk;
             progressed = true;
           }
         }
@@ -786,7 +782,7 @@ cudaError_t g_attr_err[4][64];
 
 template <int HG, bool kNv>
 cudaError_t launch_impl(const AttnArgs& a, const AttnPlan& plan, cudaStream_t stream) {
-  using C = Cfg<HG>;
+  using C = Cfg<HG, kNv>;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -865,9 +861,27 @@ cudaError_t launch_prefill_bf16(const AttnArgs& a, const AttnPlan& plan, cudaStr
 
 bool nvfp4_native_supported(int H) { return !wide_supported(H); }
 
+// The NVFP4 decode runs 16-head groups at every head count below 128 (its row
+// staging leaves no room for a 32-head group's Q and P buffers).
+AttnPlan plan_decode_nvfp4(int T, int H, int K, int num_splits, int num_sms) {
+  AttnPlan pl = plan_prefill_bf16(T, 16, K, num_splits, num_sms);
+  pl.n_hg = H / 16;
+  pl.units = (int64_t)T * pl.n_hg;
+  pl.total = pl.units * pl.nt;
+  int64_t G = num_splits > 0 ? pl.units * (int64_t)num_splits : (int64_t)num_sms;
+  if (G > pl.total) G = pl.total;
+  if (G < 1) G = 1;
+  pl.G = (int)G;
+  pl.need_combine = !(pl.total % pl.G == 0 && (pl.total / pl.G) % pl.nt == 0);
+  const int64_t n_slots = (int64_t)pl.G + pl.units - 1;
+  const size_t lse_bytes = (size_t)(((n_slots * pl.HG * 4) + 255) / 256) * 256;
+  pl.ws_bytes = kWsStatusBytes + lse_bytes + (size_t)n_slots * pl.HG * kDv * 4;
+  return pl;
+}
+
 cudaError_t launch_decode_nvfp4(const AttnArgs& a, const AttnPlan& plan, cudaStream_t stream) {
-  if (plan.HG != 16 && plan.HG != 32) return cudaErrorInvalidValue;
-  return plan.HG == 16 ? launch_impl<16, true>(a, plan, stream) : launch_impl<32, true>(a, plan, stream);
+  if (plan.HG != 16) return cudaErrorInvalidValue;
+  return launch_impl<16, true>(a, plan, stream);
 }
 
 AttnPlan plan_attention(bool fp8, int T, int H, int K, int num_splits, int num_sms) {

@@ -91,10 +91,10 @@ cudaError_t launch_nvfp4_store(const void* kv_new, const int64_t* slot_mapping, 
 size_t nvfp4_stage_bytes(int T, int K);
 cudaError_t launch_nvfp4_stage(const uint8_t* cache, int64_t NB, const int32_t* indices, const int32_t* block_table,
                                const int32_t* req_id, int T, int K, int R, int MB, void* stage, cudaStream_t stream);
-// The native NVFP4 decode (smla_attn.cu) for head counts the 16/32-head-group
-// kernel runs (all but 128): a plan of plan_prefill_bf16; a.cache is the
-// NVFP4 cache, a.NB its blocks.
+// The native NVFP4 decode (smla_attn.cu) below 128 heads, in 16-head groups:
+// a.cache is the NVFP4 cache, a.NB its blocks.
 bool nvfp4_native_supported(int H);
+AttnPlan plan_decode_nvfp4(int T, int H, int K, int num_splits, int num_sms);
 cudaError_t launch_decode_nvfp4(const AttnArgs& a, const AttnPlan& plan, cudaStream_t stream);
 
 // Offsets inside the workspace.

@@ -408,13 +408,13 @@ def main_nvfp4(lib_path: str | None = None):
     kc = lambda x: f"{np.nanmedian(x) / 1e3:7.2f}"  # noqa: E731
     print(f"CTAs {ev.shape[0]}; clock64 cycles within each CTA (K = 1000), medians over CTAs and tiles")
     print("event position in its tile relative to the tile's QK^T issue:")
-    for n in ["idx", "conv_issue", "conv_landed", "conv_start", "conv_row3", "conv_full", "qk", "soft_start",
-              "soft_bar", "pv_wait", "p_full", "pv"]:
+    for n in ["idx", "conv_issue", "conv_landed", "conv_start", "conv_full", "qk", "soft_start", "soft_bar",
+              "pv_wait", "p_full", "pv"]:
         print(f"  {n:11s} {kc(E[n] - E['qk'])}")
     print(f"cadence (QK^T to QK^T): {kc(np.diff(E['qk'], axis=1))}; P.V: {kc(np.diff(E['pv'], axis=1))}; "
           f"converter full: {kc(np.diff(E['conv_full'], axis=1))}; softmax P written: {kc(np.diff(E['p_full'], axis=1))}")
-    print(f"converter warp 0: buffer free (tile t) after P.V(t - 2) issue {kc(E['conv_start'][:, 2:] - E['pv'][:, :-2])}; "
-          f"rows 0..2 {kc(E['conv_row3'] - E['conv_start'])}; rows 3.. to full {kc(E['conv_full'] - E['conv_row3'])}")
+    print(f"converter warp 0: tile buffer free after P.V(t - 2) issue {kc(E['conv_start'][:, 2:] - E['pv'][:, :-2])}; "
+          f"conversion (buffer free to tile full) {kc(E['conv_full'] - E['conv_start'])}")
     print(f"converter, first issue to full: {kc(E['conv_full'] - E['conv_issue'])}; "
           f"tile t + 2 full after P.V of tile t: {kc(E['conv_full'][:, 2:] - E['pv'][:, :-2])}")
     enter, ex = E["enter"][:, 0], E["exit"][:, 0]

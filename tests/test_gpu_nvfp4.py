@@ -75,6 +75,14 @@ def test_decode_native_topk_widths(K, H):
     _check(case)
 
 
+@pytest.mark.parametrize("H", [32, 48])
+def test_decode_several_head_groups(H):
+    # below 128 heads the NVFP4 decode runs 16-head groups: H / 16 units per token
+    case = inp.memory_bound_decode(seed=65, R=5, ctx_lo=900, ctx_hi=2000, K=700, H=H)
+    _check(case)
+    _check(case, num_splits=2)
+
+
 @pytest.mark.parametrize("num_splits", [0, 1, 3])
 def test_decode_ragged_topk_and_splits(num_splits):
     case = inp.memory_bound_decode(seed=62, R=9, ctx_lo=300, ctx_hi=2500, K=200, H=16)
