@@ -10,6 +10,7 @@ CTA-pair kernel on its tensor-bound workload (clock64 cycles within a CTA):
 
     python -m sparse_mla_attention_fp8_gb300.trace
     python -m sparse_mla_attention_fp8_gb300.trace --wide   # the 128-head FP8 decode
+    python -m sparse_mla_attention_fp8_gb300.trace --wide-prefill  # the 128-head bf16 prefill
     python -m sparse_mla_attention_fp8_gb300.trace --wide8  # its FP8-query variant
     python -m sparse_mla_attention_fp8_gb300.trace --nvfp4  # the NVFP4 decode (16-head groups)
 
@@ -229,6 +230,11 @@ def main_wide(lib_path: str | None = None):
     call(4)
     torch.cuda.synchronize()
     assert L.smla_trace_set_wide(None) == 0
+    _wide_report(buf, G, launches.value)
+
+def _wide_report(buf, G, n_launches):
+    """Timeline summary of a traced call of the CTA-pair kernel (main_wide, main_wide_prefill)."""
+    launches = ctypes.c_int(n_launches)
     ev = buf.cpu().numpy().astype(np.float64)
     ev[ev == 0] = np.nan
     E = {n: ev[:, :, i] for i, n in enumerate(WIDE_EVENTS)}
@@ -268,6 +274,56 @@ def main_wide(lib_path: str | None = None):
     last_pv = np.array([row[np.isfinite(row)][-1] if np.isfinite(row).any() else np.nan for row in pv])
     print(f"entry -> first P.V {kc(first_pv - enter)}; last P.V -> exit {kc(ex - last_pv)}; "
           f"entry -> exit {kc(ex - enter)} K cycles")
+
+
+
+def main_wide_prefill(lib_path: str | None = None):
+    """Per-tile timeline of the 128-head bf16 prefill (4 requests x 1024 new
+    tokens over 3072 cached, H = 128, top-k 2048, latent buffer [16384, 576])
+    from the CTA-pair kernel's clock64() marks."""
+    import torch
+
+    root = os.path.dirname(_PKG)
+    if root not in sys.path:
+        sys.path.insert(0, root)
+    import smla_inputs as inp
+
+    L = ctypes.CDLL(lib_path or build_traced())
+    P, i32, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    L.sparse_mla_prefill_bf16.argtypes = [P, P, P, f32, i32, P, P, i32, i32, i32, i32, P, sz, P]
+    L.sparse_mla_prefill_workspace_bytes.argtypes = [i32, i32, i32, i32]
+    L.sparse_mla_prefill_workspace_bytes.restype = sz
+    L.sparse_mla_attention_plan.argtypes = [i32, i32, i32, i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32)]
+    L.smla_trace_set_wide.argtypes = [P]
+    ptr = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    dev = torch.device("cuda", 0)
+    case = inp.prefill(3)
+    T, H, K = case.T, case.H, case.K
+    N = case.kv.shape[0]
+    q = torch.from_numpy(np.ascontiguousarray(case.q).view(np.int16)).to(dev)
+    kv = torch.from_numpy(np.ascontiguousarray(case.kv).view(np.int16)).to(dev)
+    idx = torch.from_numpy(case.indices).to(dev)
+    ws_bytes = L.sparse_mla_prefill_workspace_bytes(T, H, K, 0)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+    out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+    launches, ctas = ctypes.c_int(0), ctypes.c_int(0)
+    L.sparse_mla_attention_plan(0, T, H, K, 0, ctypes.byref(launches), ctypes.byref(ctas))
+    G = ctas.value
+    buf = torch.zeros((G, WIDE_TILES, len(WIDE_EVENTS)), dtype=torch.int64, device=dev)
+
+    def call():
+        assert L.sparse_mla_prefill_bf16(ptr(q), ptr(kv), ptr(idx), f32(case.sm_scale), 0, ptr(out), ptr(lse), T, H,
+                                         N, K, ptr(ws), ws_bytes, None) == 0
+
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    assert L.smla_trace_set_wide(ptr(buf)) == 0
+    call()
+    torch.cuda.synchronize()
+    assert L.smla_trace_set_wide(None) == 0
+    _wide_report(buf, G, launches.value)
 
 
 WIDE8_EVENTS = ["idx", "kfull", "qk", "s_read", "sent", "received", "l_ready", "l_read", "pv_prev_done", "p_full",
@@ -426,6 +482,8 @@ if __name__ == "__main__":
         main_nvfp4()
     elif "--wide8" in sys.argv:
         main_wide8()
+    elif "--wide-prefill" in sys.argv:
+        main_wide_prefill()
     elif "--wide" in sys.argv:
         main_wide()
     else:
