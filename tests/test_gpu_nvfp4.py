@@ -83,16 +83,19 @@ def test_decode_several_head_groups(H):
     _check(case, num_splits=2)
 
 
+@pytest.mark.parametrize("H", [16, 128])
 @pytest.mark.parametrize("num_splits", [0, 1, 3])
-def test_decode_ragged_topk_and_splits(num_splits):
-    case = inp.memory_bound_decode(seed=62, R=9, ctx_lo=300, ctx_hi=2500, K=200, H=16)
+def test_decode_ragged_topk_and_splits(num_splits, H):
+    # K = 200: three full tiles of 64 rows and a ragged tail of 8 (H = 128 stages the rows)
+    case = inp.memory_bound_decode(seed=62, R=9, ctx_lo=300, ctx_hi=2500, K=200, H=H)
     _check(case, num_splits=num_splits)
 
 
-def test_decode_invalid_rows_single_rows_and_zero_topk():
+@pytest.mark.parametrize("H", [16, 128])
+def test_decode_invalid_rows_single_rows_and_zero_topk(H):
     import torch
     import sparse_mla_attention_fp8_gb300 as smla
-    case = inp.memory_bound_decode(seed=63, R=5, ctx_lo=700, ctx_hi=900, K=180, H=16)
+    case = inp.memory_bound_decode(seed=63, R=5, ctx_lo=700, ctx_hi=900, K=180, H=H)
     case.indices[:, 100:140] = case.indices[:, 0:40]          # duplicates count once per occurrence
     case.indices[0, 5] = case.block_table.shape[1] * 64 + 3    # block id >= MB
     case.indices[1, :] = -1                                    # a token without any valid row
