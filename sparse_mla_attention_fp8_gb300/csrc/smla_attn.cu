@@ -725,9 +725,9 @@ __global__ void __launch_bounds__(Cfg<HG, kNv>::kThreads, 1) sparse_mla_attn_ker
 #pragma unroll
         for (int h = 0; h < HG; ++h) {
           const float lt = red_sum[h] + red_sum[HG + h] + red_sum[2 * HG + h] + red_sum[3 * HG + h];
-          inv[h] = lt > 0.f ? 1.f / lt : 0.f;
+          inv[h] = lt > 0.f ? __fdividef(1.f, lt) : 0.f;  // approximate (a few ulp)
           if (tid == h) {
-            const float lse2 = lt > 0.f ? (m_used[h] + log2f(lt)) : -INFINITY;
+            const float lse2 = lt > 0.f ? (m_used[h] + __log2f(lt)) : -INFINITY;
             const float lse_v = lse2 * 0.69314718055994530942f;
             if (full) {
               p.lse[(int64_t)ti.t * p.H + ti.hg * HG + h] = lse_v;

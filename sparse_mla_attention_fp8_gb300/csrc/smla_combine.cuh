@@ -9,12 +9,18 @@
 
 namespace smla {
 
+// a / b for a >= 0, b > 0, in 32 bits whenever both fit: on the GPU a 64-bit
+// division is a long out-of-line routine (run at every CTA's entry here).
+__host__ __device__ __forceinline__ int64_t udiv_fast(int64_t a, int64_t b) {
+  return (a <= 0xFFFFFFFFll && b <= 0xFFFFFFFFll) ? (int64_t)((uint32_t)a / (uint32_t)b) : a / b;
+}
+
 // CTA c of G processes the unit-major tile range [tile_begin(c), tile_begin(c+1)).
-__host__ __device__ __forceinline__ int64_t tile_begin(int64_t c, int64_t total, int G) { return (c * total) / G; }
+__host__ __device__ __forceinline__ int64_t tile_begin(int64_t c, int64_t total, int G) { return udiv_fast(c * total, G); }
 
 // The CTA whose tile range holds tile x.
 __host__ __device__ __forceinline__ int64_t tile_owner(int64_t x, int64_t total, int G) {
-  int64_t c = ((x + 1) * G - 1) / total;
+  int64_t c = udiv_fast((x + 1) * G - 1, total);
   if (c >= G) c = G - 1;
   while (c + 1 < G && tile_begin(c + 1, total, G) <= x) ++c;
   while (c > 0 && tile_begin(c, total, G) > x) --c;
@@ -58,8 +64,8 @@ __global__ void __launch_bounds__(combine_threads<HG>()) combine_kernel(const fl
   if (by_boundary) {
     const int64_t c = blockIdx.x / kSplit + 1;  // boundary between CTA ranges c - 1 and c
     const int64_t b = tile_begin(c, total, G);
-    if (b % nt == 0) return;                                   // no unit is cut here
-    u = b / nt;
+    u = udiv_fast(b, nt);
+    if (b == u * nt) return;                                   // no unit is cut here
     if (tile_begin(c - 1, total, G) > u * nt) return;          // an earlier boundary cuts this unit
   } else {
     u = blockIdx.x / kSplit;
@@ -69,7 +75,7 @@ __global__ void __launch_bounds__(combine_threads<HG>()) combine_kernel(const fl
   if (c_lo == c_hi) return;  // finished inside one CTA, already written
   const int tid = threadIdx.x;
   const int h = tid / kChunks, j = part * kChunks + tid % kChunks;  // head, float4 column chunk
-  const int t = (int)(u / n_hg), hg = (int)(u % n_hg);
+  const int t = (int)udiv_fast(u, n_hg), hg = (int)(u - (int64_t)t * n_hg);
   const float4* po = reinterpret_cast<const float4*>(part_o);
   float m = -INFINITY, ssum = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -86,7 +92,7 @@ __global__ void __launch_bounds__(combine_threads<HG>()) combine_kernel(const fl
 #pragma unroll
     for (int e = 0; e < kCombineChunk; ++e) mn = fmaxf(mn, l[e]);
     if (mn == -INFINITY) continue;  // no valid row in any part so far
-    const float a = expf(m - mn);  // 0 when m was -inf
+    const float a = __expf(m - mn);  // 0 when m was -inf
     ssum *= a;
     acc.x *= a;
     acc.y *= a;
@@ -95,7 +101,7 @@ __global__ void __launch_bounds__(combine_threads<HG>()) combine_kernel(const fl
 #pragma unroll
     for (int e = 0; e < kCombineChunk; ++e) {
       if (e < np) {
-        const float wgt = expf(l[e] - mn);
+        const float wgt = __expf(l[e] - mn);
         ssum += wgt;
         acc.x += wgt * v[e].x;
         acc.y += wgt * v[e].y;
@@ -105,11 +111,12 @@ __global__ void __launch_bounds__(combine_threads<HG>()) combine_kernel(const fl
     }
     m = mn;
   }
-  const float inv = ssum > 0.f ? 1.f / ssum : 0.f;
+  // approximate reciprocal and log (a few ulp; ssum >= 1 here)
+  const float inv = ssum > 0.f ? __fdividef(1.f, ssum) : 0.f;
   __nv_bfloat162* d = reinterpret_cast<__nv_bfloat162*>(out + ((int64_t)t * H + hg * HG + h) * kDv + 4 * j);
   d[0] = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
   d[1] = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
-  if (part == 0 && j == 0) lse[(int64_t)t * H + hg * HG + h] = ssum > 0.f ? m + logf(ssum) : -INFINITY;
+  if (part == 0 && j == 0) lse[(int64_t)t * H + hg * HG + h] = ssum > 0.f ? m + __logf(ssum) : -INFINITY;
 }
 
 // Launches combine_kernel behind the attention kernel just issued on `stream`

@@ -187,9 +187,14 @@ struct TileInfo {
   bool seg_start, seg_end;
 };
 
+// Top-k tile index of tile x within its unit (x mod nt).
+__device__ __forceinline__ int tile_kt(const Params& p, int64_t x) {
+  return (int)(x - udiv_fast(x, p.nt) * p.nt);
+}
+
 __device__ __forceinline__ TileInfo tile_info(const Params& p, int64_t x, int64_t xbeg, int64_t xend) {
   TileInfo ti;
-  ti.u = (int)(x / p.nt);
+  ti.u = (int)udiv_fast(x, p.nt);
   ti.kt = (int)(x - (int64_t)ti.u * p.nt);
   ti.t = ti.u / p.n_hg;
   ti.hg = ti.u - ti.t * p.n_hg;
@@ -542,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(cons
       // bits 4..17 of the address, and no offset here carries out of it).
       const uint64_t dK0 = make_sdesc(smem_u32(smem + kOffOp), 16, 1024, kLayoutSw128);
       const uint64_t dQ = make_sdesc(smem_u32(smem + kOffQ), 16, 1024, kLayoutSw128);
-      int seg = 0, kt = (int)(xbeg % p.nt), issued = 0;
+      int seg = 0, kt = tile_kt(p, xbeg), issued = 0;
       for (int tl = 0; tl < n_local; ++tl) {
         const int sbuf = tl & 1, ob = tl % kOpBufs;
         const bool seg_start = tl == 0 || kt == 0;
@@ -592,7 +597,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(cons
       constexpr uint32_t id_pv = idesc_e4m3(128, 32, 1, 1);
       const uint64_t dV0 = make_sdesc(smem_u32(smem + kOffOp), kPanel, 1024, kLayoutSw128);
       const uint64_t dP0 = make_sdesc(smem_u32(smem + kOffP), 256, 128, kLayoutNone);
-      int seg_o = 0, kt = (int)(xbeg % p.nt), issued = 0;
+      int seg_o = 0, kt = tile_kt(p, xbeg), issued = 0;
       for (int tl = 0; tl < n_local; ++tl) {
         const int ob = tl % kOpBufs, pb = tl % kPBufs;
         const bool seg_start = tl == 0 || kt == 0;
@@ -913,25 +918,35 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(cons
           }
 #pragma unroll
           for (int h = 0; h < 8; ++h) {
-            inv[h] = lt[h] > 0.f ? __frcp_rn(lt[h]) : 0.f;
-            lse_own[h] = lt[h] > 0.f ? (m[h] + log2f(lt[h])) * 0.69314718055994530942f : -INFINITY;
+            // approximate reciprocal and log2 (a few ulp; lt >= 2^-0.75 here): the
+            // correctly rounded library forms cost about a microsecond of cold code
+            inv[h] = lt[h] > 0.f ? __fdividef(1.f, lt[h]) : 0.f;
+            lse_own[h] = lt[h] > 0.f ? (m[h] + __log2f(lt[h])) * 0.69314718055994530942f : -INFINITY;
           }
         }
         // The epilogue runs once per CTA, so its code is fetched cold: it is
         // kept compact (rolled loops over chunks and parts, no divisions).
-        // load_out: this thread's normalized output values of chunk q, head
-        // 8 hh + h, value column 128 q + 32 qd + lane.
-        auto load_out = [&](int q, float (&val)[8]) {
-          uint32_t ohi[8], olo[8];
-          tmem_ld8(tmem + lane_base + kOCol + 32 * q + 8 * hh, ohi);
-          tmem_ld8(tmem + lane_base + kOCol + 32 * q + 16 + 8 * hh, olo);
+        // load_out2: this thread's normalized output values of chunks q and
+        // q + 1 (one tensor-memory round trip), head 8 hh + h, value column
+        // 128 q' + 32 qd + lane.
+        auto load_out2 = [&](int q, float (&va)[8], float (&vb)[8]) {
+          uint32_t ah[8], al[8], bh[8], bl[8];
+          const uint32_t o = tmem + lane_base + kOCol + 32 * q + 8 * hh;
+          tmem_ld8(o, ah);
+          tmem_ld8(o + 16, al);
+          tmem_ld8(o + 32, bh);
+          tmem_ld8(o + 48, bl);
           tmem_ld_wait();
-          reg_fence8(ohi);
-          reg_fence8(olo);
-          const float rq = q == 0 ? Rq[0] : q == 1 ? Rq[1] : q == 2 ? Rq[2] : Rq[3];
-          const float rsc = rq * kPScaleInv;
+          reg_fence8(ah);
+          reg_fence8(al);
+          reg_fence8(bh);
+          reg_fence8(bl);
+          const float ra = (q == 0 ? Rq[0] : Rq[2]) * kPScaleInv, rb = (q == 0 ? Rq[1] : Rq[3]) * kPScaleInv;
 #pragma unroll
-          for (int h = 0; h < 8; ++h) val[h] = (__uint_as_float(ohi[h]) + __uint_as_float(olo[h])) * rsc * inv[h];
+          for (int h = 0; h < 8; ++h) {
+            va[h] = (__uint_as_float(ah[h]) + __uint_as_float(al[h])) * ra * inv[h];
+            vb[h] = (__uint_as_float(bh[h]) + __uint_as_float(bl[h])) * rb * inv[h];
+          }
         };
         const int c0 = 32 * qd + lane;
         if (tid == 0) SMLA_TRACE_SET(tl, kEvEpiLse);
@@ -969,23 +984,28 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(cons
           for (int h = 0; h < 8; ++h) own0[h] = own1[h] = 0.f;
           if (!dead) {
 #pragma unroll 1
-            for (int q = 0; q < 4; ++q) {
-              float val[8];
-              load_out(q, val);
-              const int o = q < S ? q : q - S, j = q < S ? 0 : 1;  // the chunk's CTA and its index there
-              if (o == rank) {
+            for (int q2 = 0; q2 < 4; q2 += 2) {
+              float vals[2][8];
+              load_out2(q2, vals[0], vals[1]);
 #pragma unroll
-                for (int h = 0; h < 8; ++h) {
-                  own0[h] = j == 0 ? val[h] : own0[h];
-                  own1[h] = j == 0 ? own1[h] : val[h];
+              for (int e = 0; e < 2; ++e) {
+                const int q = q2 + e;
+                const float(&val)[8] = vals[e];
+                const int o = q < S ? q : q - S, j = q < S ? 0 : 1;  // the chunk's CTA and its index there
+                if (o == rank) {
+#pragma unroll
+                  for (int h = 0; h < 8; ++h) {
+                    own0[h] = j == 0 ? val[h] : own0[h];
+                    own1[h] = j == 0 ? own1[h] : val[h];
+                  }
+                } else {
+                  const int n_o = o < 4 - S ? 2 : 1, ps = rank < o ? rank : rank - 1;
+                  const uint32_t dst =
+                      mapa_shared(recv + (uint32_t)(((ps * n_o + j) * kRows + c0) * (HG * 4) + 32 * hh), (uint32_t)o);
+                  const uint32_t bar = mapa_shared(recv_bar, (uint32_t)o);
+                  st_async_v4(dst, val[0], val[1], val[2], val[3], bar);
+                  st_async_v4(dst + 16, val[4], val[5], val[6], val[7], bar);
                 }
-              } else {
-                const int n_o = o < 4 - S ? 2 : 1, ps = rank < o ? rank : rank - 1;
-                const uint32_t dst =
-                    mapa_shared(recv + (uint32_t)(((ps * n_o + j) * kRows + c0) * (HG * 4) + 32 * hh), (uint32_t)o);
-                const uint32_t bar = mapa_shared(recv_bar, (uint32_t)o);
-                st_async_v4(dst, val[0], val[1], val[2], val[3], bar);
-                st_async_v4(dst + 16, val[4], val[5], val[6], val[7], bar);
               }
             }
             if (qd == 0 && lane == 0) {
@@ -1034,9 +1054,9 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(cons
             for (int h = 0; h < 8; ++h) {
               w0[h] = mx[h] == -INFINITY ? 0.f : __expf(lse_own[h] - mx[h]);
               const float wsum = iw[h] + w0[h];
-              iw[h] = wsum > 0.f ? 1.f / wsum : 0.f;
+              iw[h] = wsum > 0.f ? __fdividef(1.f, wsum) : 0.f;  // wsum in [1, S]
               w0[h] *= iw[h];
-              if (rank == 0 && qd == 0 && lane == h) p.lse[row0 + h] = wsum > 0.f ? mx[h] + logf(wsum) : -INFINITY;
+              if (rank == 0 && qd == 0 && lane == h) p.lse[row0 + h] = wsum > 0.f ? mx[h] + __logf(wsum) : -INFINITY;
             }
 #pragma unroll 1
             for (int j = 0; j < n_own; ++j) {
@@ -1072,15 +1092,19 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(cons
           }
           if (!dead) {
 #pragma unroll 1
-            for (int q = 0; q < 4; ++q) {
-              float val[8];
-              load_out(q, val);
+            for (int q2 = 0; q2 < 4; q2 += 2) {
+              float vals[2][8];
+              load_out2(q2, vals[0], vals[1]);
 #pragma unroll
-              for (int h = 0; h < 8; ++h) {
-                if (full)
-                  p.out[(row0 + h) * kDv + 128 * q + c0] = __float2bfloat16_rn(val[h]);
-                else
-                  p.part_o[(slot * HG + 8 * hh + h) * kDv + 128 * q + c0] = val[h];
+              for (int e = 0; e < 2; ++e) {
+                const int q = q2 + e;
+#pragma unroll
+                for (int h = 0; h < 8; ++h) {
+                  if (full)
+                    p.out[(row0 + h) * kDv + 128 * q + c0] = __float2bfloat16_rn(vals[e][h]);
+                  else
+                    p.part_o[(slot * HG + 8 * hh + h) * kDv + 128 * q + c0] = vals[e][h];
+                }
               }
             }
           }

@@ -791,9 +791,11 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
           if (tid == 0) W8_TRACE(tl, kEvEpiStart);
           const bool full_unit = n_seg_tiles == p.nt;  // the whole token ran in this pair
           // out = O_g R_g / (kPLift l)
-          const float inv0 = l_sum > 0.f ? rp0 * (1.f / kPLift) / l_sum : 0.f;
-          const float inv1 = l_sum > 0.f ? rp1 * (1.f / kPLift) / l_sum : 0.f;
-          const float lse_v = l_sum > 0.f ? (m_used + log2f(l_sum)) * 0.69314718055994531f : -INFINITY;
+          // approximate reciprocal and logarithms (a few ulp)
+          const float rl = l_sum > 0.f ? __fdividef(1.f, l_sum) : 0.f;
+          const float inv0 = rp0 * (1.f / kPLift) * rl;
+          const float inv1 = rp1 * (1.f / kPLift) * rl;
+          const float lse_v = l_sum > 0.f ? (m_used + __log2f(l_sum)) * 0.69314718055994531f : -INFINITY;
           const int64_t slot = (int64_t)pair + u;
           // A fused part's normalized output in the slot's block for CTA c,
           // lane-major so that a warp's accesses are contiguous: columns
@@ -863,7 +865,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
               const float l0 = part == 0 ? lse_v : lse_o, l1 = part == 0 ? lse_o : lse_v;
               const float M = fmaxf(l0, l1);
               const float w0 = M == -INFINITY ? 0.f : __expf(l0 - M), w1 = M == -INFINITY ? 0.f : __expf(l1 - M);
-              const float ws = w0 + w1, iw = ws > 0.f ? 1.f / ws : 0.f;
+              const float ws = w0 + w1, iw = ws > 0.f ? __fdividef(1.f, ws) : 0.f;
               const float4* oth = fused_block(slot_oth);
               // two 16-column chunks per step, the partner's eight loads issued first
 #pragma unroll 1
@@ -896,7 +898,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(96)
                   store_out16(q + e, ow);
                 }
               }
-              if (c == 0) p.lse[(int64_t)u * kHeads + h] = ws > 0.f ? M + logf(ws) : -INFINITY;
+              if (c == 0) p.lse[(int64_t)u * kHeads + h] = ws > 0.f ? M + __logf(ws) : -INFINITY;
             }
           } else {
             for (int q = 0; q < 256 / 16; ++q) {
