@@ -142,6 +142,7 @@ static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0 && kOpBuf % 1024 == 0, "ope
 static_assert(kOffBar % 8 == 0, "barriers 8-byte aligned");
 static_assert(kOffPre % 16 == 0 && kOffRedMax % 16 == 0 && kOffRedSc % 16 == 0 && kOffRedSum % 16 == 0, "float4");
 static_assert(kSmemAlloc <= 232448, "shared memory budget");
+static_assert(kOpBufs == 2, "operand tile tl uses S buffer tl % 2 as well");
 
 // ---- tensor memory columns
 constexpr int kSCols = 4 * 32 + HG;   // per S buffer: 4 groups x (hi, lo) x 16 heads + RoPE
@@ -456,11 +457,13 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(cons
   } else if (warp >= kLoadWarp0 && warp < kLoadWarp0 + kLoaders) {
     // ------------------------------------------------------------ loaders
     // Loader lw copies rows 32 lw .. 32 lw + 31 of every tile with 16-byte
-    // cp.async: per row one instruction for the 512 codes (lane k: bytes
-    // 16 k .. 16 k + 15, into code panel k / 8, 16-byte column k % 8 with the
-    // 128-byte swizzle), then nine for the 32 rows' scales and RoPE values
+    // cp.async: nine instructions for the 32 rows' scales and RoPE values
     // (chunk 0 of a row's 144 bytes from byte 512 is its scales, chunks 1..8
-    // its RoPE values).  Invalid rows are zero-filled.  Its arrival on the
+    // its RoPE values), as soon as the softmax has read the buffer's previous
+    // tile; then, once that tile's P.V has completed, per row one instruction
+    // for the 512 codes (lane k: bytes 16 k .. 16 k + 15, into code panel
+    // k / 8, 16-byte column k % 8 with the 128-byte swizzle).  Invalid rows
+    // are zero-filled.  Its arrival on the
     // tile's full barrier follows its own copies' completion and a proxy
     // fence (the tensor cores read the tile through the async proxy), and its
     // writes of the rows' valid flags.
@@ -479,16 +482,13 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(cons
       const int32_t slot = slots_ring[b4 * kRows + rw + lane];
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[kBarIdxEmpty + b4]);  // this loader's slots read
-      if (use >= 1 && !SMLA_WAIT(kBarOpEmpty + ob, (use + 1) & 1)) break;
-      if (lane == 0 && lw == 0) SMLA_TRACE_SET(tl, kEvBufFree);
+      // The tile two before in this buffer has been through QK^T and the
+      // softmax has read its rows' flags and scales (its S buffer is free
+      // again): the RoPE panel, the scales and the flags can take this tile's
+      // while the codes are still being read by its P.V.
+      if (use >= 1 && !SMLA_WAIT(kBarSFree + (tl & 1), ((tl - 2) >> 1) & 1)) break;
       valid[ob * kRows + rw + lane] = slot >= 0 ? 1 : 0;
       const uint32_t op = smem_u32(smem + kOffOp + ob * kOpBuf);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int32_t s = __shfl_sync(kFullMask, slot, i);
-        const uint8_t* src = cache_lane + (size_t)(uint32_t)max(s, 0) * kRowBytes;
-        cp_async_16(op + code_off[i & 7] + (uint32_t)((i >> 3) * 1024), src, s >= 0 ? 16u : 0u);
-      }
 #pragma unroll
       for (int it = 0; it < 9; ++it) {
         const int idx = 32 * it + lane;
@@ -498,6 +498,15 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(cons
         const uint8_t* src = p.cache + (int64_t)(s >= 0 ? s : 0) * kRowBytes + kScaleOff + 16 * k;
         const uint32_t dst = k == 0 ? op + kOpScale + 16 * r : op + kOpRope + sw128(r, k - 1);
         cp_async_16(dst, src, s >= 0 ? 16u : 0u);
+      }
+      // the code panels are free once that tile's P.V has completed
+      if (use >= 1 && !SMLA_WAIT(kBarOpEmpty + ob, (use + 1) & 1)) break;
+      if (lane == 0 && lw == 0) SMLA_TRACE_SET(tl, kEvBufFree);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int32_t s = __shfl_sync(kFullMask, slot, i);
+        const uint8_t* src = cache_lane + (size_t)(uint32_t)max(s, 0) * kRowBytes;
+        cp_async_16(op + code_off[i & 7] + (uint32_t)((i >> 3) * 1024), src, s >= 0 ? 16u : 0u);
       }
       if (lane == 0 && lw == 0) SMLA_TRACE_SET(tl, kEvIssued);
       asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
