@@ -11,14 +11,15 @@
 //
 // Design: the tensor cores read the cache codes as stored, with no
 // dequantization pass, 128 top-k rows per tile (M = 128 in every MMA).
-//  * Transport: the loader warps copy each row with 16-byte cp.async (LSU
-//    path, L2 only): one instruction moves one row's 512 codes (lane k: the
-//    k-th 16 bytes, into code panel k / 8 with the 128-byte swizzle), and
-//    nine more move the scales and RoPE values of 32 rows.  The tensor cores
-//    read the tile after each loader has waited for its own copies and made
-//    them visible to the async proxy.  Invalid rows are zero-filled.  Two
-//    operand tiles (4 code panels of 128 rows x 128 bytes, a RoPE panel and
-//    the 128 rows' scales: 82 KB each).
+//  * Transport: the loader warps copy the rows with 16-byte cp.async (LSU
+//    path, L2 only): one instruction moves 128 codes of 4 rows into a code
+//    panel with the 128-byte swizzle, nine move the scales and RoPE values of
+//    32 rows.  A buffer's RoPE panel and scales are refilled once the softmax
+//    has read its previous tile's, and each code panel once the P.V of that
+//    tile has read it.  The tensor cores read the tile after each loader has
+//    waited for its own copies and made them visible to the async proxy.
+//    Invalid rows are zero-filled.  Two operand tiles (4 code panels of 128
+//    rows x 128 bytes, a RoPE panel and the 128 rows' scales: 82 KB each).
 //  * Q is split once per (token, 16-head group) into two e4m3 terms,
 //    q * 2^s_hg = hi + lo (s_hg a power of two per head and 128-column scale
 //    group g putting the group's max |q| near 448), exact for all but
@@ -120,7 +121,8 @@ constexpr int kOffRedSc = kOffRedMax + 2 * 2 * 4 * 8 * 4;           // uint32 [2
 constexpr int kOffRedSum = kOffRedSc + 2 * 2 * 4 * 4 * 4;           // float [2 halves][4 quarters][8 heads]
 constexpr int kOffBar = kOffRedSum + 2 * 4 * 8 * 4;
 enum {
-  kBarOpFull = 0, kBarOpEmpty = kBarOpFull + kOpBufs, kBarSFull = kBarOpEmpty + kOpBufs, kBarSFree = kBarSFull + 2,
+  // kBarOpEmpty + 4 ob + q: code panel q of operand tile ob has been read by its P.V
+  kBarOpFull = 0, kBarOpEmpty = kBarOpFull + kOpBufs, kBarSFull = kBarOpEmpty + 4 * kOpBufs, kBarSFree = kBarSFull + 2,
   kBarPFull = kBarSFree + 2, kBarPvDone = kBarPFull + kPBufs, kBarIdxFull = kBarPvDone + kPBufs,
   kBarIdxEmpty = kBarIdxFull + 4, kBarQFull = kBarIdxEmpty + 4, kBarQEmpty = kBarQFull + kQBufs,
   kBarOFree = kBarQEmpty + kQBufs, kBarDrain = kBarOFree + 1, kBarDrainPv = kBarDrain + 1,
@@ -381,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(cons
   if (tid == 0) {
     for (int i = 0; i < kOpBufs; ++i) {
       mbar_init(&bars[kBarOpFull + i], kLoaders);  // one arrival per loader once its copies are visible
-      mbar_init(&bars[kBarOpEmpty + i], 1);
+      for (int q = 0; q < 4; ++q) mbar_init(&bars[kBarOpEmpty + 4 * i + q], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars[kBarSFull + i], 1);
@@ -460,22 +462,26 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(cons
     // cp.async: nine instructions for the 32 rows' scales and RoPE values
     // (chunk 0 of a row's 144 bytes from byte 512 is its scales, chunks 1..8
     // its RoPE values), as soon as the softmax has read the buffer's previous
-    // tile; then, once that tile's P.V has completed, per row one instruction
-    // for the 512 codes (lane k: bytes 16 k .. 16 k + 15, into code panel
-    // k / 8, 16-byte column k % 8 with the 128-byte swizzle).  Invalid rows
-    // are zero-filled.  Its arrival on the
+    // tile; then, per code panel q as soon as that tile's P.V has read it,
+    // eight instructions for the rows' codes 128 q .. 128 q + 127 (128-byte
+    // swizzle).  Invalid rows are zero-filled.  Its arrival on the
     // tile's full barrier follows its own copies' completion and a proxy
     // fence (the tensor cores read the tile through the async proxy), and its
     // writes of the rows' valid flags.
     const int lw = warp - kLoadWarp0;
     const int rw = 32 * lw;  // first tile row of this loader
-    // this lane's code chunk lands in panel lane / 8, at 16-byte column
-    // (lane % 8) ^ (row % 8) of its row: one offset per row % 8
-    uint32_t code_off[8];
+    // Codes: instruction i of panel q moves rows 4 i .. 4 i + 3 (of this
+    // loader's 32) x 128 codes; lane l copies 16-byte column l % 8 of row
+    // 4 i + l / 8, to column (l % 8) ^ (row % 8) of the panel's row.  The
+    // row's place in its 8-row group is 4 (i % 2) + l / 8: one offset per
+    // parity of i.
+    uint32_t code_off[2];
 #pragma unroll
-    for (int j = 0; j < 8; ++j)
-      code_off[j] = (uint32_t)((lane >> 3) * kPanel + (rw >> 3) * 1024 + j * 128 + (((lane & 7) ^ j) << 4));
-    const uint8_t* cache_lane = p.cache + 16 * lane;
+    for (int e = 0; e < 2; ++e) {
+      const int rr = 4 * e + (lane >> 3);
+      code_off[e] = (uint32_t)((rw >> 3) * 1024 + rr * 128 + (((lane & 7) ^ rr) << 4));
+    }
+    const uint8_t* cache_lane = p.cache + 16 * (lane & 7);
     for (int tl = 0; tl < n_local; ++tl) {
       const int b4 = tl & 3, ob = tl % kOpBufs, use = tl / kOpBufs;
       if (!SMLA_WAIT(kBarIdxFull + b4, (tl >> 2) & 1)) break;
@@ -499,15 +505,22 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(cons
         const uint32_t dst = k == 0 ? op + kOpScale + 16 * r : op + kOpRope + sw128(r, k - 1);
         cp_async_16(dst, src, s >= 0 ? 16u : 0u);
       }
-      // the code panels are free once that tile's P.V has completed
-      if (use >= 1 && !SMLA_WAIT(kBarOpEmpty + ob, (use + 1) & 1)) break;
-      if (lane == 0 && lw == 0) SMLA_TRACE_SET(tl, kEvBufFree);
+      // code panel q is free once that tile's P.V has read it (its chunk q)
+      bool gone = false;
+#pragma unroll 1
+      for (int q = 0; q < 4 && !gone; ++q) {
+        if (use >= 1 && !SMLA_WAIT(kBarOpEmpty + 4 * ob + q, (use + 1) & 1)) gone = true;
+        if (lane == 0 && lw == 0 && q == 0) SMLA_TRACE_SET(tl, kEvBufFree);
+        if (gone) break;
+        const uint32_t panel = op + q * kPanel;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int32_t s = __shfl_sync(kFullMask, slot, i);
-        const uint8_t* src = cache_lane + (size_t)(uint32_t)max(s, 0) * kRowBytes;
-        cp_async_16(op + code_off[i & 7] + (uint32_t)((i >> 3) * 1024), src, s >= 0 ? 16u : 0u);
+        for (int i = 0; i < 8; ++i) {
+          const int32_t s = __shfl_sync(kFullMask, slot, 4 * i + (lane >> 3));
+          const uint8_t* src = cache_lane + (size_t)(uint32_t)max(s, 0) * kRowBytes + 128 * q;
+          cp_async_16(panel + code_off[i & 1] + (uint32_t)((i >> 1) * 1024), src, s >= 0 ? 16u : 0u);
+        }
       }
+      if (gone) break;
       if (lane == 0 && lw == 0) SMLA_TRACE_SET(tl, kEvIssued);
       asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
       if (lane == 0 && lw == 0) SMLA_TRACE_SET(tl, kEvLanded);
@@ -599,9 +612,10 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(cons
   } else if (warp == kPvWarp) {
     // ------------------------------------------------------------ P.V issuer
     // One thread: O^T += E^T P' of each tile once its P' is written (and,
-    // first in a segment, the previous segment's epilogue has read O).  Its
-    // completion frees the operand tile (QK^T of the tile completed before its
-    // P' could be written) and the P' buffer.
+    // first in a segment, the previous segment's epilogue has read O).  The
+    // completion of its value chunk q frees code panel q of the operand tile
+    // (QK^T of the tile completed before its P' could be written); that of
+    // the whole tile frees the P' buffer.
     if (lane == 0 && n_local > 0) {
       constexpr uint32_t id_pv = idesc_e4m3(128, 32, 1, 1);
       const uint64_t dV0 = make_sdesc(smem_u32(smem + kOffOp), kPanel, 1024, kLayoutSw128);
@@ -622,8 +636,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(cons
             // A = codes^T (value column c x row j), MN-major; B = P'_q (row j x 32), MN-major
             mma_f8(tmem + kOCol + 32 * q, dv + ((q * kPanel + 4096 * k) >> 4), dp + ((q * kPGroup + 1024 * k) >> 4),
                    id_pv, (seg_start && k == 0) ? 0u : 1u);
+          mma_commit(&bars[kBarOpEmpty + 4 * ob + q]);  // code panel q read (QK^T of the tile completed earlier)
         }
-        mma_commit(&bars[kBarOpEmpty + ob]);
         mma_commit(&bars[kBarPvDone + pb]);
         SMLA_TRACE_SET(tl, kEvPv);
         ++issued;
