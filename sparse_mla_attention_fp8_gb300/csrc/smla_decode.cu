@@ -1048,7 +1048,40 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(cons
           if (!dead) dead = !SMLA_WAIT(kBarRecv, 0);
           dead = __any_sync(kFullMask, dead);
           if (tid == 0) SMLA_TRACE_SET(tl, kEvMergeGo);
-          if (!dead) {
+          if (!dead && S == 2) {
+            // Two parts (the usual cluster): straight-line code, both weights
+            // computed once per head and no divergent branch, since this code
+            // runs once per CTA and is fetched cold.  Each CTA owns chunks
+            // rank and rank + 2; the other part's values are in peer slot 0.
+            const uint32_t lse_base = recv + (uint32_t)(2 * kChunkBytes) + 32 * hh;
+            const float4 a = lds_f32x4(lse_base), b = lds_f32x4(lse_base + 16);
+            const float lp[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+            float w1[8], lse_mine = -INFINITY;
+#pragma unroll
+            for (int h = 0; h < 8; ++h) {
+              const float M = fmaxf(lse_own[h], lp[h]);
+              const float e0 = M == -INFINITY ? 0.f : __expf(lse_own[h] - M);
+              const float e1 = M == -INFINITY ? 0.f : __expf(lp[h] - M);
+              const float ws = e0 + e1;  // in [1, 2] unless both parts are empty
+              const float r = ws > 0.f ? __fdividef(1.f, ws) : 0.f;
+              own0[h] *= e0 * r;  // the own part's weighted values
+              own1[h] *= e0 * r;
+              w1[h] = e1 * r;
+              lse_mine = lane == h ? (ws > 0.f ? M + __logf(ws) : -INFINITY) : lse_mine;
+            }
+            if (rank == 0 && qd == 0 && lane < 8) p.lse[row0 + lane] = lse_mine;
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+              const uint32_t src = recv + (uint32_t)((j * kRows + c0) * (HG * 4) + 32 * hh);
+              const float4 x0 = lds_f32x4(src), x1 = lds_f32x4(src + 16);
+              const float x[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+              const int q = rank + 2 * j;
+#pragma unroll
+              for (int h = 0; h < 8; ++h)
+                p.out[(row0 + h) * kDv + 128 * q + c0] =
+                    __float2bfloat16_rn(fmaf(w1[h], x[h], j == 0 ? own0[h] : own1[h]));
+            }
+          } else if (!dead) {
             // merge weights per head: the maximum M, 1 / sum_r w_r and the own
             // part's weight are kept; a received part's weight is recomputed
             // from its LSE where it is used
