@@ -44,16 +44,18 @@ UNIT = "query-tokens/s"
 # figure no longer applies and the roofline reports null.
 TRAFFIC_SOURCES = ("smla_decode.cu", "smla_combine.cuh", "smla_common.cuh", "sm103_ptx.cuh")
 TRAFFIC_BY_SOURCE = {
-    "3e9c80169300af85": 100_915_456 + 2_309_120,  # 128-row tiles, symmetric cluster merge (re-keyed: an unused helper removed, cubin identical)
+    # 128-row tiles, symmetric cluster merge, per-panel refill, two-part merge path
+    # (writes vary 0.25 - 2.5 MB between launches with the L2's write-back; the middle one)
+    "d96b55bff8dc3a9e": 100_902_144 + 503_296,
 }
 # The same for the 128-head CTA-pair kernel, per workload: the bf16 prefill's
 # attention kernel plus its combine; the FP8 decode's attention kernel, which
 # merges its split tokens itself (the Q preparation, 18.9 MB, is left out).
 WIDE_TRAFFIC_SOURCES = ("smla_wide.cu", "smla_combine.cuh", "smla_common.cuh", "sm103_ptx.cuh")
 WIDE_TRAFFIC_BY_SOURCE = {
-    ("493cf41b1e606a5a", "prefill_h128_k2048"): (674_349_568 + 531_697_664 + 38_474_496 + 186_880,
+    ("f1d467be26141655", "prefill_h128_k2048"): (672_552_192 + 528_722_432 + 37_843_456 + 123_392,
                                                  "attention kernel + combine"),
-    ("493cf41b1e606a5a", "decode_h128_k2048"): (250_123_264 + 20_676_352, "attention kernel (merges its split tokens)"),
+    ("f1d467be26141655", "decode_h128_k2048"): (250_082_048 + 20_681_472, "attention kernel (merges its split tokens)"),
 }
 
 
@@ -61,7 +63,7 @@ WIDE_TRAFFIC_BY_SOURCE = {
 # plus the combine of tokens split between CTAs).
 NVFP4_TRAFFIC_SOURCES = ("smla_attn.cu", "smla_combine.cuh", "smla_common.cuh", "sm103_ptx.cuh")
 NVFP4_TRAFFIC_BY_SOURCE = {
-    "6a45d9458053455a": (59_168_768 + 48_384 + 7_372_288, "attention kernel + combine"),
+    "d63690ea74b7e5b2": (59_163_648 + 14_848 + 6_849_024, "attention kernel + combine"),
 }
 
 
