@@ -36,7 +36,7 @@ LINKS = [("copy issue (loader 0)", "buf_free", "issued", 0), ("copy landing (loa
          ("other loaders after loader 0", "landed", "op_full", 0), ("QK^T issue", "op_full", "qk", 0),
          ("S ready after issue", "qk", "soft_start", 0), ("softmax to tile-max barrier", "soft_start", "soft_bar", 0),
          ("softmax barrier to P' (warp 0)", "soft_bar", "p_written", 0), ("P' (warp 0) to P.V issued", "p_written", "pv", 0),
-         ("P.V issued to buffer free (tile + 2)", "pv", "buf_free", 2), ("Q ready to tile full", "q_ready", "op_full", 0),
+         ("P.V issued to code panel 0 free (tile + 2)", "pv", "buf_free", 2), ("Q ready to tile full", "q_ready", "op_full", 0),
          ("last P.V issued to epilogue start", "pv", "epi_start", 0),
          ("epilogue start to merge wait", "epi_start", "merge_wait", 0),
          ("merge wait (other CTA)", "merge_wait", "merge_go", 0), ("merge to epilogue end", "merge_go", "epilogue", 0)]
