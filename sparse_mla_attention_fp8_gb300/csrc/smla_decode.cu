@@ -1197,6 +1197,61 @@ extern "C" int smla_trace_set_fp8(unsigned long long* buf) {
 }
 #endif
 
+namespace {
+
+cudaError_t set_smem_attr() {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::call_once(g_attr_once[dev], [dev] {
+    g_attr_err[dev] =
+        cudaFuncSetAttribute(sparse_mla_decode_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+  });
+  return g_attr_err[dev];
+}
+
+// Clusters of s CTAs of the decode kernel that the GPU holds at once (one CTA
+// per SM; a cluster lives on one GPC, so fewer than SMs / s when the GPCs'
+// SM counts are not multiples of s), cached per device.  0 when unknown.
+int max_active_clusters(int s) {
+  static std::mutex mu;
+  static int cached[64][kMaxCluster + 1] = {};
+  int dev = 0;
+  if (s < 2 || s > kMaxCluster || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cached[dev][s] != 0) return cached[dev][s] > 0 ? cached[dev][s] : 0;
+  int n = 0;
+  if (set_smem_attr() == cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)s, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmemAlloc;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)s;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, sparse_mla_decode_fp8_kernel, &cfg) != cudaSuccess) {
+      (void)cudaGetLastError();
+      n = 0;
+    }
+  }
+  cached[dev][s] = n > 0 ? n : -1;
+  return n;
+}
+
+// Units cut into s parts run as clusters when all of them are resident at
+// once (if the query failed, assume they are).
+bool clusters_fit(int64_t units, int s) {
+  const int n = max_active_clusters(s);
+  return n <= 0 || units <= n;
+}
+
+}  // namespace
+
 AttnPlan plan_decode_fp8(int T, int H, int K, int num_splits, int num_sms) {
   if (wide_supported(H)) return plan_decode_wide(T, K, num_splits, num_sms);
   AttnPlan pl;
@@ -1209,15 +1264,27 @@ AttnPlan plan_decode_fp8(int T, int H, int K, int num_splits, int num_sms) {
   if (num_splits > 0) {
     G = pl.units * (int64_t)num_splits;
   } else {
-    // Automatic: equal contiguous ranges over all SMs, or, when that costs no
-    // more, every unit cut into s equal parts (one segment per CTA: one Q
-    // preparation and one epilogue each).  Cost in tiles, counting a segment
-    // boundary inside a CTA's range as one tile.
-    G = num_sms;
+    // Automatic.  Candidates: equal contiguous ranges over all SMs, or every
+    // unit cut into s parts (one segment per CTA: one Q preparation and one
+    // epilogue each).  Parts of a unit are merged on chip by a cluster when
+    // 2 <= s <= kMaxCluster and all the clusters are resident at once, else
+    // by the combine kernel.  Cost in tiles: the largest range or part, one
+    // tile per segment boundary inside a range, kCombineTiles when the
+    // combine runs (measured: about two tiles); on a tie the on-chip merge.
+    constexpr int64_t kCombineTiles = 2;
     const int64_t tpc = (pl.total + num_sms - 1) / num_sms;
-    const int64_t cost_range = tpc + (tpc + pl.nt - 1) / pl.nt;
-    const int64_t s = pl.units > 0 ? std::min<int64_t>(num_sms / pl.units, pl.nt) : 0;
-    if (s >= 1 && (pl.nt + s - 1) / s <= cost_range) G = pl.units * s;
+    const bool range_cut = !(pl.total % num_sms == 0 && (pl.total / num_sms) % pl.nt == 0);
+    int64_t best = 2 * (tpc + (tpc + pl.nt - 1) / pl.nt + (range_cut ? kCombineTiles : 0)) + (range_cut ? 1 : 0);
+    G = num_sms;
+    const int64_t s_max = pl.units > 0 ? std::min<int64_t>(num_sms / pl.units, pl.nt) : 0;
+    for (int64_t s = s_max; s >= 1; --s) {
+      const bool on_chip = s == 1 || (s <= kMaxCluster && clusters_fit(pl.units, (int)s));
+      const int64_t cost = 2 * ((pl.nt + s - 1) / s + (on_chip ? 0 : kCombineTiles)) + (on_chip ? 0 : 1);
+      if (cost < best) {
+        best = cost;
+        G = pl.units * s;
+      }
+    }
   }
   if (G > pl.total) G = pl.total;
   if (G < 1) G = 1;
@@ -1227,7 +1294,7 @@ AttnPlan plan_decode_fp8(int T, int H, int K, int num_splits, int num_sms) {
   // CTAs per unit merges them in distributed shared memory
   if (pl.need_combine && pl.G % pl.units == 0) {
     const int64_t s = pl.G / pl.units;
-    if (s >= 2 && s <= kMaxCluster) {
+    if (s >= 2 && s <= kMaxCluster && clusters_fit(pl.units, (int)s)) {
       pl.cluster = (int)s;
       pl.need_combine = false;
     }
@@ -1244,15 +1311,8 @@ AttnPlan plan_decode_fp8(int T, int H, int K, int num_splits, int num_sms) {
 
 cudaError_t launch_decode_fp8(const AttnArgs& a, const AttnPlan& plan, cudaStream_t stream) {
   if (plan.HG == 128) return launch_decode_wide(a, plan, stream);
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  cudaError_t e = set_smem_attr();
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  std::call_once(g_attr_once[dev], [dev] {
-    g_attr_err[dev] =
-        cudaFuncSetAttribute(sparse_mla_decode_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
-  });
-  if (g_attr_err[dev] != cudaSuccess) return g_attr_err[dev];
   uint8_t* ws = static_cast<uint8_t*>(a.workspace);
   const int64_t n_slots = (int64_t)plan.G + plan.units - 1;
   Params p;

@@ -6,7 +6,7 @@ import pytest
 import oracle
 import smla_inputs as inp
 from helpers import (assert_lse_close, assert_out_close, bf16_dev, check_decode, dev, oracle_cache,
-                     run_gpu_decode)
+                     run_gpu_decode, sample_tokens)
 
 pytestmark = pytest.mark.gpu
 
@@ -295,3 +295,15 @@ def test_store_launched_after_a_decode_waits_for_it():
         assert_out_close(outs[k].float().cpu().numpy(), ref_out, f"decode {k}")
         assert_lse_close(lses[k].cpu().numpy(), ref_lse, f"decode {k}")
     assert np.array_equal(d_cache.cpu().numpy(), cache_new)
+
+
+@pytest.mark.parametrize("R", [24, 40, 48, 56])
+def test_automatic_split_between_token_counts(R):
+    # the automatic split for token counts around the SM count's divisors: clusters of 2, 3 or 4 parts where
+    # all of them are resident at once, else contiguous ranges with the combine (the choice depends on the
+    # GPU's clusters); sampled tokens against the oracle, the first and last included
+    import sparse_mla_attention_fp8_gb300 as smla
+    case = inp.memory_bound_decode(seed=45 + R, R=R, ctx_lo=4096, ctx_hi=9000, K=2048, H=16)
+    launches, ctas = smla.attention_plan(True, R, 16, 2048, 0)
+    assert launches in (1, 2) and R <= ctas <= 4 * R
+    check_decode(case, tokens=sample_tokens(case.T, 6, seed=R))
