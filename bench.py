@@ -47,6 +47,8 @@ TRAFFIC_BY_SOURCE = {
     # 128-row tiles, symmetric cluster merge, per-panel refill, two-part merge path
     # (writes vary 0.25 - 2.5 MB between launches with the L2's write-back; the middle one)
     "d96b55bff8dc3a9e": 100_902_144 + 503_296,
+    # re-keyed: only the host-side planner changed (cluster residency), the kernel and this plan are the same
+    "1401db86d71b50f3": 100_902_144 + 503_296,
 }
 # The same for the 128-head CTA-pair kernel, per workload: the bf16 prefill's
 # attention kernel plus its combine; the FP8 decode's attention kernel, which
