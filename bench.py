@@ -530,7 +530,8 @@ def tensor_workload(args, quiet=False):
 
     algo_bytes = None  # set for an HBM-bound workload: its roofline is then bytes over measured copy bandwidth
     if args.workload == "decode_h128_k2048":
-        case = inp.rotating_decode(seed=2, R=128, ctx_lo=65536, ctx_hi=65536, K=2048, H=128, outliers=True)
+        ctx = args.context or 65536
+        case = inp.rotating_decode(seed=2, R=128, ctx_lo=ctx, ctx_hi=ctx, K=2048, H=128, outliers=True)
         T, H, K, NB = case.q.shape[0], case.H, case.K, case.num_blocks
         with torch.cuda.stream(stream):
             cache = torch.zeros((NB, 64, 656), dtype=torch.uint8, device=device)
@@ -556,7 +557,7 @@ def tensor_workload(args, quiet=False):
         mma_dtype = "f16" if H == 128 else "fp8"
         launches = smla.attention_plan(True, T, H, K, 0)[0]
         desc = (f"{case.name}: tensor-bound FP8 sparse decode, {T} requests x 1 token, H={H}, top-k {K}, "
-                f"context 65536, 656-byte FP8 cache ({NB} blocks, {NB * 64 * 656 / 1e9:.1f} GB), "
+                f"context {ctx}, 656-byte FP8 cache ({NB} blocks, {NB * 64 * 656 / 1e9:.1f} GB), "
                 f"{n_graphs} rotating index sets")
         # oracle sample: a few tokens on a host cache holding the rows they reference
         tok = np.arange(min(nth, 8), dtype=np.int32)
@@ -987,6 +988,9 @@ def main():
                     default="decode_h16_k2048",
                     help="decode_h16_k2048 (default) is the headline; each other workload is reported on its own "
                          "line (and inside the default line, unless --no-extra)")
+    ap.add_argument("--context", type=int, default=0,
+                    help="decode_h128_k2048 only: per-request context (default 65536, a 5.5 GB cache); a smaller "
+                         "one gives the same kernel launch on less device memory, for profiler captures")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
