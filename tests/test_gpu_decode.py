@@ -25,7 +25,8 @@ def test_tiny_decode_h16_k64():
 @pytest.mark.parametrize("H", [16, 128])
 @pytest.mark.parametrize("num_splits", [0, 1, 2, 3, 5])
 def test_ragged_topk_several_tiles(num_splits, H):
-    # K = 200: three full tiles of 64 rows and a ragged tail of 8 (H = 128 runs the CTA-pair kernel)
+    # K = 200: one full 128-row tile and a ragged tail of 72 (H = 16), or three 64-row tiles and a tail of 8
+    # (H = 128, the CTA-pair kernel)
     case = inp.memory_bound_decode(seed=5, R=9, ctx_lo=300, ctx_hi=2500, K=200, H=H)
     check_decode(case, num_splits=num_splits)
 
@@ -306,4 +307,13 @@ def test_automatic_split_between_token_counts(R):
     case = inp.memory_bound_decode(seed=45 + R, R=R, ctx_lo=4096, ctx_hi=9000, K=2048, H=16)
     launches, ctas = smla.attention_plan(True, R, 16, 2048, 0)
     assert launches in (1, 2) and R <= ctas <= 4 * R
+    check_decode(case, tokens=sample_tokens(case.T, 6, seed=R))
+
+
+@pytest.mark.parametrize("R,H,K", [(160, 16, 1024), (24, 48, 2048)])
+def test_long_ranges_across_units(R, H, K):
+    # more tiles than one ring pass per CTA, ranges that cross unit boundaries (160 tokens x 8 tiles over the
+    # SMs), and several 16-head groups per token: the operand buffers' per-panel barriers go through many
+    # phases and segments change inside a CTA; sampled tokens against the oracle
+    case = inp.memory_bound_decode(seed=46, R=R, ctx_lo=3000, ctx_hi=9000, K=K, H=H)
     check_decode(case, tokens=sample_tokens(case.T, 6, seed=R))
