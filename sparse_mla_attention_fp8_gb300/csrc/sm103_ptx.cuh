@@ -244,6 +244,17 @@ __device__ __forceinline__ void tma_store_2d(const void* map, uint32_t src, int 
                "r"(x), "r"(y)
                : "memory");
 }
+// Bulk copy from this CTA's shared memory to another CTA's of the cluster
+// (cluster addresses for the destination and its mbarrier), whose bytes
+// complete that mbarrier's transaction count.  16-byte aligned addresses, a
+// size that is a multiple of 16.
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, uint32_t src_cta, uint32_t bytes,
+                                                  uint32_t mbar_cluster) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   dst_cluster),
+               "r"(src_cta), "r"(bytes), "r"(mbar_cluster)
+               : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until every committed bulk store of this thread has finished reading shared memory.
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }

@@ -139,6 +139,10 @@ constexpr int kSmemAlloc = kSmemBytes + 1024;
 // LSEs in its operand tiles (free by then)
 constexpr int kMaxCluster = 4;
 constexpr int kChunkBytes = kRows * HG * 4;  // 8 KB: one value chunk of one part, [column][head]
+// two-part clusters: the values and LSEs a CTA sends, staged after its own receive buffer
+constexpr int kSendOff = 3 * kChunkBytes;
+static_assert(kSendOff >= 2 * kChunkBytes + HG * 4 && kSendOff + 2 * kChunkBytes + HG * 4 <= kOpBufs * kOpBuf,
+              "two-part send staging");
 static_assert((kMaxCluster - 1) * (2 * kChunkBytes + HG * 4) <= kOpBufs * kOpBuf, "cluster receive buffer");
 static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0 && kOpBuf % 1024 == 0, "operand alignment");
 static_assert(kOffBar % 8 == 0, "barriers 8-byte aligned");
@@ -998,13 +1002,64 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(cons
               if (r != rank) mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&bars[kBarReady]), (uint32_t)r));
           }
           if (tid == 0) SMLA_TRACE_SET(tl, kEvEpiSignal);
+          float own0[8], own1[8];  // this thread's values of chunks rank and rank + S
+#pragma unroll
+          for (int h = 0; h < 8; ++h) own0[h] = own1[h] = 0.f;
+          if (S == 2) {
+            // Two parts: this CTA's values of the other's chunks (rank ^ 1 and
+            // rank ^ 1 + 2) and its LSEs go to a staging area laid out as the
+            // other CTA's receive buffer, then one bulk copy moves them once
+            // the other CTA is ready.  The staging area follows the receive
+            // buffer in the free operand tiles.
+            const uint32_t stage = recv + (uint32_t)kSendOff;
+            if (!dead) {
+#pragma unroll 1
+              for (int q2 = 0; q2 < 4; q2 += 2) {
+                float vals[2][8];
+                load_out2(q2, vals[0], vals[1]);
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                  const int q = q2 + e, j = q >> 1;
+                  const float(&val)[8] = vals[e];
+                  if ((q & 1) == rank) {
+#pragma unroll
+                    for (int h = 0; h < 8; ++h) {
+                      own0[h] = j == 0 ? val[h] : own0[h];
+                      own1[h] = j == 0 ? own1[h] : val[h];
+                    }
+                  } else {
+                    const uint32_t dst = stage + (uint32_t)((j * kRows + c0) * (HG * 4) + 32 * hh);
+                    st_shared_v4(dst, __float_as_uint(val[0]), __float_as_uint(val[1]), __float_as_uint(val[2]),
+                                 __float_as_uint(val[3]));
+                    st_shared_v4(dst + 16, __float_as_uint(val[4]), __float_as_uint(val[5]), __float_as_uint(val[6]),
+                                 __float_as_uint(val[7]));
+                  }
+                }
+              }
+              if (qd == 0 && lane == 0) {
+                const uint32_t dst = stage + (uint32_t)(2 * kChunkBytes + 32 * hh);
+                st_shared_v4(dst, __float_as_uint(lse_own[0]), __float_as_uint(lse_own[1]), __float_as_uint(lse_own[2]),
+                             __float_as_uint(lse_own[3]));
+                st_shared_v4(dst + 16, __float_as_uint(lse_own[4]), __float_as_uint(lse_own[5]),
+                             __float_as_uint(lse_own[6]), __float_as_uint(lse_own[7]));
+              }
+            }
+            fence_proxy_async_smem();  // the bulk copy reads the staging area through the async proxy
+            named_bar_sync(3, 32 * kSoftWarps);
+            if (tid == 0) SMLA_TRACE_SET(tl, kEvMergeWait);
+            if (tid == 0 && !dead) {
+              if (SMLA_WAIT(kBarReady, 0)) {
+                if (tid == 0) SMLA_TRACE_SET(tl, kEvEpiReady);
+                const uint32_t other = (uint32_t)(rank ^ 1);
+                bulk_copy_to_peer(mapa_shared(recv, other), stage, (uint32_t)(2 * kChunkBytes + HG * 4),
+                                  mapa_shared(recv_bar, other));
+              }
+            }
+          } else {
           if (tid == 0) SMLA_TRACE_SET(tl, kEvMergeWait);
           if (!dead) dead = !SMLA_WAIT(kBarReady, 0);
           dead = __any_sync(kFullMask, dead);
           if (tid == 0) SMLA_TRACE_SET(tl, kEvEpiReady);
-          float own0[8], own1[8];  // this thread's values of chunks rank and rank + S
-#pragma unroll
-          for (int h = 0; h < 8; ++h) own0[h] = own1[h] = 0.f;
           if (!dead) {
 #pragma unroll 1
             for (int q2 = 0; q2 < 4; q2 += 2) {
@@ -1043,6 +1098,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(cons
                 st_async_v4(dst + 16, lse_own[4], lse_own[5], lse_own[6], lse_own[7], bar);
               }
             }
+          }
           }
           if (tid == 0) SMLA_TRACE_SET(tl, kEvEpiSent);
           if (!dead) dead = !SMLA_WAIT(kBarRecv, 0);
