@@ -1112,20 +1112,24 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(cons
             const uint32_t lse_base = recv + (uint32_t)(2 * kChunkBytes) + 32 * hh;
             const float4 a = lds_f32x4(lse_base), b = lds_f32x4(lse_base + 16);
             const float lp[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-            float w1[8], lse_mine = -INFINITY;
+            // per head: the larger LSE M, e = exp(-|lse_own - lse_peer|) (0 when a
+            // part is empty), weights 1 / (1 + e) and e / (1 + e): one exponential
+            // and one reciprocal; lse = M + log(1 + e) for the head this lane writes
+            float w1[8], m_mine = -INFINITY, s_mine = 1.f;
 #pragma unroll
             for (int h = 0; h < 8; ++h) {
               const float M = fmaxf(lse_own[h], lp[h]);
-              const float e0 = M == -INFINITY ? 0.f : __expf(lse_own[h] - M);
-              const float e1 = M == -INFINITY ? 0.f : __expf(lp[h] - M);
-              const float ws = e0 + e1;  // in [1, 2] unless both parts are empty
-              const float r = ws > 0.f ? __fdividef(1.f, ws) : 0.f;
-              own0[h] *= e0 * r;  // the own part's weighted values
-              own1[h] *= e0 * r;
-              w1[h] = e1 * r;
-              lse_mine = lane == h ? (ws > 0.f ? M + __logf(ws) : -INFINITY) : lse_mine;
+              const bool own_big = lse_own[h] >= lp[h];
+              const float e = M == -INFINITY ? 0.f : __expf(-fabsf(lse_own[h] - lp[h]));
+              const float r = M == -INFINITY ? 0.f : __fdividef(1.f, 1.f + e);
+              own0[h] *= own_big ? r : e * r;  // the own part's weighted values
+              own1[h] *= own_big ? r : e * r;
+              w1[h] = own_big ? e * r : r;
+              m_mine = lane == h ? M : m_mine;
+              s_mine = lane == h ? 1.f + e : s_mine;
             }
-            if (rank == 0 && qd == 0 && lane < 8) p.lse[row0 + lane] = lse_mine;
+            if (rank == 0 && qd == 0 && lane < 8)
+              p.lse[row0 + lane] = m_mine == -INFINITY ? -INFINITY : m_mine + __logf(s_mine);
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
               const uint32_t src = recv + (uint32_t)((j * kRows + c0) * (HG * 4) + 32 * hh);
