@@ -139,9 +139,11 @@ constexpr int kSmemAlloc = kSmemBytes + 1024;
 // LSEs in its operand tiles (free by then)
 constexpr int kMaxCluster = 4;
 constexpr int kChunkBytes = kRows * HG * 4;  // 8 KB: one value chunk of one part, [column][head]
-// two-part clusters: the values and LSEs a CTA sends, staged after its own receive buffer
+// two-part clusters: a CTA sends its raw values of the other's two chunks and
+// its heads' running maxima and sums (fp32), staged after its own receive buffer
+constexpr int kTwoPartBytes = 2 * kChunkBytes + 2 * HG * 4;
 constexpr int kSendOff = 3 * kChunkBytes;
-static_assert(kSendOff >= 2 * kChunkBytes + HG * 4 && kSendOff + 2 * kChunkBytes + HG * 4 <= kOpBufs * kOpBuf,
+static_assert(kSendOff >= kTwoPartBytes && kSendOff + kTwoPartBytes <= kOpBufs * kOpBuf && kTwoPartBytes % 16 == 0,
               "two-part send staging");
 static_assert((kMaxCluster - 1) * (2 * kChunkBytes + HG * 4) <= kOpBufs * kOpBuf, "cluster receive buffer");
 static_assert(kOffQ % 1024 == 0 && kOffP % 1024 == 0 && kOpBuf % 1024 == 0, "operand alignment");
@@ -925,36 +927,37 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(cons
         const bool full = (seg_first_kt == 0) && (ti.kt == p.nt - 1);
         const int64_t slot = (int64_t)blockIdx.x + ti.u;
         const int64_t row0 = (int64_t)ti.t * p.H + ti.hg * HG + 8 * hh;  // first head of this half
-        float inv[8], lse_own[8];
-        {
-          float lt[8];
+        // the heads' sums over the segment's rows; a two-part cluster merges raw
+        // sums and values (below), the other paths normalize here
+        float inv[8], lse_own[8], lt[8];
 #pragma unroll
-          for (int h = 0; h < 8; ++h) lt[h] = 0.f;
+        for (int h = 0; h < 8; ++h) lt[h] = 0.f;
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            const float4 a0 = *reinterpret_cast<const float4*>(rs + v * 8);
-            const float4 a1 = *reinterpret_cast<const float4*>(rs + v * 8 + 4);
-            lt[0] += a0.x;
-            lt[1] += a0.y;
-            lt[2] += a0.z;
-            lt[3] += a0.w;
-            lt[4] += a1.x;
-            lt[5] += a1.y;
-            lt[6] += a1.z;
-            lt[7] += a1.w;
-          }
+        for (int v = 0; v < 4; ++v) {
+          const float4 a0 = *reinterpret_cast<const float4*>(rs + v * 8);
+          const float4 a1 = *reinterpret_cast<const float4*>(rs + v * 8 + 4);
+          lt[0] += a0.x;
+          lt[1] += a0.y;
+          lt[2] += a0.z;
+          lt[3] += a0.w;
+          lt[4] += a1.x;
+          lt[5] += a1.y;
+          lt[6] += a1.z;
+          lt[7] += a1.w;
+        }
+        const bool two_parts = p.cluster == 2;
 #pragma unroll
-          for (int h = 0; h < 8; ++h) {
-            // approximate reciprocal and log2 (a few ulp; lt >= 2^-0.75 here): the
-            // correctly rounded library forms cost about a microsecond of cold code
-            inv[h] = lt[h] > 0.f ? __fdividef(1.f, lt[h]) : 0.f;
-            lse_own[h] = lt[h] > 0.f ? (m[h] + __log2f(lt[h])) * 0.69314718055994530942f : -INFINITY;
-          }
+        for (int h = 0; h < 8; ++h) {
+          // approximate reciprocal and log2 (a few ulp; lt >= 2^-0.75 here): the
+          // correctly rounded library forms cost about a microsecond of cold code
+          inv[h] = two_parts ? 1.f : (lt[h] > 0.f ? __fdividef(1.f, lt[h]) : 0.f);
+          lse_own[h] = two_parts || !(lt[h] > 0.f) ? -INFINITY : (m[h] + __log2f(lt[h])) * 0.69314718055994530942f;
         }
         // The epilogue runs once per CTA, so its code is fetched cold: it is
         // kept compact (rolled loops over chunks and parts, no divisions).
-        // load_out2: this thread's normalized output values of chunks q and
-        // q + 1 (one tensor-memory round trip), head 8 hh + h, value column
+        // load_out2: this thread's output values of chunks q and (normalized,
+        // except in a two-part cluster)
+        // chunk q + 1 (one tensor-memory round trip), head 8 hh + h, value column
         // 128 q' + 32 qd + lane.
         auto load_out2 = [&](int q, float (&va)[8], float (&vb)[8]) {
           uint32_t ah[8], al[8], bh[8], bl[8];
@@ -996,7 +999,8 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(cons
           const uint32_t recv = smem_u32(smem + kOffOp);
           const uint32_t recv_bar = smem_u32(&bars[kBarRecv]);
           if (tid == 0 && !dead) {
-            mbar_arrive_expect_tx(&bars[kBarRecv], (uint32_t)((S - 1) * (n_own * kChunkBytes + HG * 4)));
+            mbar_arrive_expect_tx(&bars[kBarRecv], (uint32_t)(S == 2 ? kTwoPartBytes
+                                                                    : (S - 1) * (n_own * kChunkBytes + HG * 4)));
 #pragma unroll 1
             for (int r = 0; r < S; ++r)
               if (r != rank) mbar_arrive_cluster_relaxed(mapa_shared(smem_u32(&bars[kBarReady]), (uint32_t)r));
@@ -1006,11 +1010,12 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(cons
 #pragma unroll
           for (int h = 0; h < 8; ++h) own0[h] = own1[h] = 0.f;
           if (S == 2) {
-            // Two parts: this CTA's values of the other's chunks (rank ^ 1 and
-            // rank ^ 1 + 2) and its LSEs go to a staging area laid out as the
-            // other CTA's receive buffer, then one bulk copy moves them once
-            // the other CTA is ready.  The staging area follows the receive
-            // buffer in the free operand tiles.
+            // Two parts: this CTA's raw (unnormalized) values of the other's
+            // chunks (rank ^ 1 and rank ^ 1 + 2) and its heads' running maxima
+            // and sums go to a staging area laid out as the other CTA's receive
+            // buffer, then one bulk copy moves them once the other CTA is ready.
+            // The staging area follows the receive buffer in the free operand
+            // tiles.
             const uint32_t stage = recv + (uint32_t)kSendOff;
             if (!dead) {
 #pragma unroll 1
@@ -1037,11 +1042,15 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(cons
                 }
               }
               if (qd == 0 && lane == 0) {
-                const uint32_t dst = stage + (uint32_t)(2 * kChunkBytes + 32 * hh);
-                st_shared_v4(dst, __float_as_uint(lse_own[0]), __float_as_uint(lse_own[1]), __float_as_uint(lse_own[2]),
-                             __float_as_uint(lse_own[3]));
-                st_shared_v4(dst + 16, __float_as_uint(lse_own[4]), __float_as_uint(lse_own[5]),
-                             __float_as_uint(lse_own[6]), __float_as_uint(lse_own[7]));
+                const uint32_t dst = stage + (uint32_t)(2 * kChunkBytes + 64 * hh);
+                st_shared_v4(dst, __float_as_uint(m[0]), __float_as_uint(m[1]), __float_as_uint(m[2]),
+                             __float_as_uint(m[3]));
+                st_shared_v4(dst + 16, __float_as_uint(m[4]), __float_as_uint(m[5]), __float_as_uint(m[6]),
+                             __float_as_uint(m[7]));
+                st_shared_v4(dst + 32, __float_as_uint(lt[0]), __float_as_uint(lt[1]), __float_as_uint(lt[2]),
+                             __float_as_uint(lt[3]));
+                st_shared_v4(dst + 48, __float_as_uint(lt[4]), __float_as_uint(lt[5]), __float_as_uint(lt[6]),
+                             __float_as_uint(lt[7]));
               }
             }
             fence_proxy_async_smem();  // the bulk copy reads the staging area through the async proxy
@@ -1051,8 +1060,7 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(cons
               if (SMLA_WAIT(kBarReady, 0)) {
                 if (tid == 0) SMLA_TRACE_SET(tl, kEvEpiReady);
                 const uint32_t other = (uint32_t)(rank ^ 1);
-                bulk_copy_to_peer(mapa_shared(recv, other), stage, (uint32_t)(2 * kChunkBytes + HG * 4),
-                                  mapa_shared(recv_bar, other));
+                bulk_copy_to_peer(mapa_shared(recv, other), stage, (uint32_t)kTwoPartBytes, mapa_shared(recv_bar, other));
               }
             }
           } else {
@@ -1105,31 +1113,38 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(cons
           dead = __any_sync(kFullMask, dead);
           if (tid == 0) SMLA_TRACE_SET(tl, kEvMergeGo);
           if (!dead && S == 2) {
-            // Two parts (the usual cluster): straight-line code, both weights
-            // computed once per head and no divergent branch, since this code
-            // runs once per CTA and is fetched cold.  Each CTA owns chunks
-            // rank and rank + 2; the other part's values are in peer slot 0.
-            const uint32_t lse_base = recv + (uint32_t)(2 * kChunkBytes) + 32 * hh;
-            const float4 a = lds_f32x4(lse_base), b = lds_f32x4(lse_base + 16);
-            const float lp[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-            // per head: the larger LSE M, e = exp(-|lse_own - lse_peer|) (0 when a
-            // part is empty), weights 1 / (1 + e) and e / (1 + e): one exponential
-            // and one reciprocal; lse = M + log(1 + e) for the head this lane writes
+            // Two parts (the usual cluster): straight-line code, since it runs
+            // once per CTA and is fetched cold.  Each CTA owns chunks rank and
+            // rank + 2; the other part's raw values are in peer slot 0, its
+            // maxima and sums after them.  Per head, with d = m_own - m_peer
+            // (log2 units): the smaller part is scaled by e = 2^-|d|, the sum is
+            // L = l_own a_own + l_peer a_peer and out = (O_own a_own + O_peer
+            // a_peer) / L, lse = ln 2 (max(m_own, m_peer) + log2 L): one
+            // exponential and one reciprocal per head.
+            const uint32_t ml_base = recv + (uint32_t)(2 * kChunkBytes) + 64 * hh;
+            const float4 ma = lds_f32x4(ml_base), mb = lds_f32x4(ml_base + 16);
+            const float4 la = lds_f32x4(ml_base + 32), lb = lds_f32x4(ml_base + 48);
+            const float mp[8] = {ma.x, ma.y, ma.z, ma.w, mb.x, mb.y, mb.z, mb.w};
+            const float lp[8] = {la.x, la.y, la.z, la.w, lb.x, lb.y, lb.z, lb.w};
             float w1[8], m_mine = -INFINITY, s_mine = 1.f;
 #pragma unroll
             for (int h = 0; h < 8; ++h) {
-              const float M = fmaxf(lse_own[h], lp[h]);
-              const bool own_big = lse_own[h] >= lp[h];
-              const float e = M == -INFINITY ? 0.f : __expf(-fabsf(lse_own[h] - lp[h]));
-              const float r = M == -INFINITY ? 0.f : __fdividef(1.f, 1.f + e);
-              own0[h] *= own_big ? r : e * r;  // the own part's weighted values
-              own1[h] *= own_big ? r : e * r;
-              w1[h] = own_big ? e * r : r;
+              const float M = fmaxf(m[h], mp[h]);
+              const bool own_big = m[h] >= mp[h];
+              const float e = M == -INFINITY ? 0.f : ex2_approx(-fabsf(m[h] - mp[h]));
+              const float a_own = own_big ? 1.f : e, a_peer = own_big ? e : 1.f;
+              const float L = lt[h] * a_own + lp[h] * a_peer;
+              const float r = L > 0.f ? __fdividef(1.f, L) : 0.f;
+              const float ro = a_own * r;
+              own0[h] *= ro;  // the own part's weighted values
+              own1[h] *= ro;
+              w1[h] = a_peer * r;
               m_mine = lane == h ? M : m_mine;
-              s_mine = lane == h ? 1.f + e : s_mine;
+              s_mine = lane == h ? L : s_mine;
             }
             if (rank == 0 && qd == 0 && lane < 8)
-              p.lse[row0 + lane] = m_mine == -INFINITY ? -INFINITY : m_mine + __logf(s_mine);
+              p.lse[row0 + lane] =
+                  s_mine > 0.f ? (m_mine + __log2f(s_mine)) * 0.69314718055994530942f : -INFINITY;
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
               const uint32_t src = recv + (uint32_t)((j * kRows + c0) * (HG * 4) + 32 * hh);
