@@ -44,11 +44,9 @@ UNIT = "query-tokens/s"
 # figure no longer applies and the roofline reports null.
 TRAFFIC_SOURCES = ("smla_decode.cu", "smla_combine.cuh", "smla_common.cuh", "sm103_ptx.cuh")
 TRAFFIC_BY_SOURCE = {
-    # 128-row tiles, symmetric cluster merge, per-panel refill, two-part merge path
-    # (writes vary 0.25 - 2.5 MB between launches with the L2's write-back; the middle one)
-    "d96b55bff8dc3a9e": 100_902_144 + 503_296,
-    # re-keyed: only the host-side planner changed (cluster residency), the kernel and this plan are the same
-    "1401db86d71b50f3": 100_902_144 + 503_296,
+    # 128-row tiles refilled panel by panel, two-part clusters merged from raw sums by one bulk copy
+    # (writes vary 0.09 - 2.3 MB between launches with the L2's write-back; the middle one)
+    "936d956d040f5ef2": 100_892_416 + 253_952,
 }
 # The same for the 128-head CTA-pair kernel, per workload: the bf16 prefill's
 # attention kernel plus its combine; the FP8 decode's attention kernel, which
