@@ -56,6 +56,9 @@ WIDE_TRAFFIC_BY_SOURCE = {
     ("f1d467be26141655", "prefill_h128_k2048"): (672_552_192 + 528_722_432 + 37_843_456 + 123_392,
                                                  "attention kernel + combine"),
     ("f1d467be26141655", "decode_h128_k2048"): (250_082_048 + 20_681_472, "attention kernel (merges its split tokens)"),
+    # re-keyed: the shared header gained a helper that only the 16-head decode uses; these kernels are unchanged
+    ("ad3021e155c41e5f", "prefill_h128_k2048"): (672_552_192 + 528_722_432 + 37_843_456 + 123_392, "attention kernel + combine"),
+    ("ad3021e155c41e5f", "decode_h128_k2048"): (250_082_048 + 20_681_472, "attention kernel (merges its split tokens)"),
 }
 
 
@@ -64,6 +67,8 @@ WIDE_TRAFFIC_BY_SOURCE = {
 NVFP4_TRAFFIC_SOURCES = ("smla_attn.cu", "smla_combine.cuh", "smla_common.cuh", "sm103_ptx.cuh")
 NVFP4_TRAFFIC_BY_SOURCE = {
     "d63690ea74b7e5b2": (59_163_648 + 14_848 + 6_849_024, "attention kernel + combine"),
+    # re-keyed: the shared header gained a helper that only the 16-head decode uses; this kernel is unchanged
+    "44d0ca0de63d94b5": (59_163_648 + 14_848 + 6_849_024, "attention kernel + combine"),
 }
 
 
