@@ -47,6 +47,7 @@ TRAFFIC_BY_SOURCE = {
     # 128-row tiles refilled panel by panel, two-part clusters merged from raw sums by one bulk copy
     # (writes vary 0.09 - 2.3 MB between launches with the L2's write-back; the middle one)
     "936d956d040f5ef2": 100_892_416 + 253_952,
+    "5dc4295d6b49c62c": 100_892_416 + 253_952,  # re-keyed: a comment of the same kernel rewritten
 }
 # The same for the 128-head CTA-pair kernel, per workload: the bf16 prefill's
 # attention kernel plus its combine; the FP8 decode's attention kernel, which

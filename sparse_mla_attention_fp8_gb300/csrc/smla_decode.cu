@@ -984,15 +984,18 @@ __global__ void __launch_bounds__(kThreads, 1) sparse_mla_decode_fp8_kernel(cons
           // The unit's parts are the cluster's S CTAs (2 <= S <= 4, one
           // segment each).  CTA `rank` writes the value chunks q with
           // q % S == rank (rank and rank + S).  Every CTA, its last P.V done,
-          // tells the others that its operand tiles are free, sends its
-          // normalized values of each chunk it does not write (and its LSEs)
-          // to the chunk's CTA by 16-byte st.async counted on that CTA's
-          // receive barrier, and merges what it receives for its own chunks:
+          // tells the others that its operand tiles are free and sends its
+          // values of each chunk it does not write to the chunk's CTA, counted
+          // on that CTA's receive barrier; each CTA merges what it receives for
+          // its own chunks (CTA 0 writes the LSE).  Three or four parts send
+          // normalized values and LSEs by 16-byte st.async and merge as
           // M = max_r lse_r, w_r = exp(lse_r - M), out = sum_r w_r out_r /
-          // sum_r w_r, lse = M + log sum_r w_r (CTA 0).  Receive layout of a
-          // CTA owning n chunks: the part in peer slot ps (the other ranks in
-          // order) has chunk j at (ps * n + j) * kChunkBytes, column c and head
-          // h at (c * 16 + h) * 4; the LSEs follow all values, 64 bytes per slot.
+          // sum_r w_r, lse = M + log sum_r w_r; two parts send raw values and
+          // their heads' running maxima and sums by one bulk copy (below).
+          // Receive layout of a CTA owning n chunks: the part in peer slot ps
+          // (the other ranks in order) has chunk j at (ps * n + j) *
+          // kChunkBytes, column c and head h at (c * 16 + h) * 4; the LSEs (or
+          // the maxima and sums) follow all values, 64 (128) bytes per slot.
           const int rank = (int)cluster_ctarank();
           const int S = p.cluster;
           const int n_own = rank < 4 - S ? 2 : 1;
