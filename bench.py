@@ -73,6 +73,20 @@ NVFP4_TRAFFIC_BY_SOURCE = {
 }
 
 
+# The same for the separate-mode FP8 prefill (gather + up-convert, workspace
+# translation, the 128-head bf16 kernel, the combine: one step) and for the
+# two weight-absorption GEMM launches of one step.
+PREFILL_FP8_TRAFFIC_SOURCES = ("smla_store.cu", "smla_wide.cu", "smla_combine.cuh", "smla_common.cuh", "sm103_ptx.cuh")
+PREFILL_FP8_TRAFFIC_BY_SOURCE = {
+    "6884e8a0cd6030d4": (10_755_584 + 33_576_704 + 180_224 + 672_449_536 + 528_017_920 + 37_842_176 + 112_640,
+              "gather + up-convert, translation, attention kernel, combine"),
+}
+ABSORB_TRAFFIC_SOURCES = ("smla_absorb.cu", "sm103_ptx.cuh")
+ABSORB_TRAFFIC_BY_SOURCE = {
+    "34ee1d10223418ff": (218_148_608 + 543_458_048 + 553_696_000 + 111_604_480, "both head_gemm launches"),
+}
+
+
 def _source_key(files):
     import hashlib
     h = hashlib.sha256()
@@ -748,6 +762,9 @@ def tensor_workload(args, quiet=False):
     tflops = flops / (ms * 1e-3) / 1e12
     peak = tensor_peak_tflops(peaks, fp8)
     wide_traffic, wide_traffic_kernels = captured_wide_traffic(args.workload)
+    if args.workload == "prefill_fp8_h128_k2048":
+        wide_traffic, wide_traffic_kernels = PREFILL_FP8_TRAFFIC_BY_SOURCE.get(
+            _source_key(PREFILL_FP8_TRAFFIC_SOURCES), (None, None))
     cpu = None
     if not args.no_cpu_baseline:
         t0 = time.perf_counter()
@@ -808,6 +825,7 @@ def tensor_workload(args, quiet=False):
             line["config"]["step"] = "the query-side and value-side GEMM launches"
             line["config"]["l2"] = "inputs (1.5 GB per step) larger than L2"
             kernel = "head_gemm_kernel (two launches per step)"
+            traffic, traffic_kernels = ABSORB_TRAFFIC_BY_SOURCE.get(_source_key(ABSORB_TRAFFIC_SOURCES), (None, None))
         line["roofline"] = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                             "frac": gbs / peaks["hbm_gbs"], "traffic": traffic, "traffic_kernels": traffic_kernels,
                             "peak_source": peaks["source"], "kernel": kernel, "bytes_per_step": algo_bytes,
