@@ -250,8 +250,11 @@ int sparse_mla_attention_plan(int fp8, int T, int H, int K, int num_splits, int*
  * value / scale rounded to nearest-even e4m3 with saturation (a group with scale 0 stores zeros);
  * the 4 scales and the RoPE values are stored verbatim.  Two tokens with the same slot race.
  * Launch order: the kernel is a programmatic dependent of the preceding kernel on `stream` (its
- * launch may overlap that kernel's tail); it reads and writes nothing before that kernel has
- * completed, so stream order holds as for an ordinary launch. */
+ * launch may overlap that kernel's tail).  It writes kv_cache only after that kernel has
+ * completed, so a decode running before it still reads the old rows.  If that kernel signals its
+ * dependents early (this library's decode and attention kernels do; ordinary kernels do not),
+ * kv_new and slot_mapping may be read before it has finished: write those two with other kernels,
+ * not with a kernel of this library launched directly before the call. */
 int mla_cache_store_fp8(const void* kv_new, const int64_t* slot_mapping, uint8_t* kv_cache, int T, int NB,
                         void* stream);
 

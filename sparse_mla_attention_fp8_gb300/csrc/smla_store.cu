@@ -40,10 +40,10 @@ __global__ void __launch_bounds__(256) quantize_store_kernel(const uint4* __rest
   // a decode launched behind this grid as its programmatic dependent may start
   // its prologue now; it waits for this grid before it reads the cache
   grid_launch_dependents();
-  // launched itself as a programmatic dependent of the preceding kernel (a
-  // decode still reading the cache, say): nothing is read or written before
-  // that grid has completed
-  grid_dependency_wait();
+  // Launched itself as a programmatic dependent of the preceding kernel (a
+  // decode still reading the cache, say): the new rows and their slots, this
+  // call's own inputs, are read and quantized at once; the cache is written
+  // only after that grid has completed.
   const int token = (int)((blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (token >= T) return;
@@ -77,10 +77,12 @@ __global__ void __launch_bounds__(256) quantize_store_kernel(const uint4* __rest
       codes[i] = (uint32_t)lo | ((uint32_t)hi << 16);
     }
   }
+  const uint4 rope = lane < 8 ? __ldg(src + 64 + lane) : make_uint4(0u, 0u, 0u, 0u);
+  grid_dependency_wait();
   uint8_t* row = cache + slot * kRowBytes;
   *reinterpret_cast<uint4*>(row + 16 * lane) = make_uint4(codes[0], codes[1], codes[2], codes[3]);
   if ((lane & 7) == 0) *reinterpret_cast<float*>(row + kScaleOff + 4 * (lane >> 3)) = scale;
-  if (lane < 8) *reinterpret_cast<uint4*>(row + kRopeOff + 16 * lane) = __ldg(src + 64 + lane);
+  if (lane < 8) *reinterpret_cast<uint4*>(row + kRopeOff + 16 * lane) = rope;
 }
 
 __global__ void translate_kernel(const int32_t* __restrict__ indices, const int32_t* __restrict__ block_table,
